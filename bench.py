@@ -1,0 +1,418 @@
+"""Benchmark: gate-level time-based power analysis on GB300.
+
+One step = one pass of the whole hot path over the loaded workload: event-count
+partition -> fused dynamic + leakage power kernel -> final reduction (one
+``pa_run``). Default workload: the very large skewed configuration (5M gates,
+64 cells with 1-4 inputs and 8x8 LUTs, 100k cycles at 1 ns, 1B events with
+Zipf(1.1) gate activity), seeded synthetic inputs.
+
+Printed (rank 0, one JSON line):
+  value    events/s over all ranks, inputs resident in HBM, timed with CUDA
+           events on the library's stream, max over ranks
+  e2e      same metric through the public API with host buffers: per step the
+           events are copied from pinned host memory (pa_load_events, with
+           device-side validation), the pass runs, and the waveform and counts
+           come back to the host
+  roofline the fused kernel's algorithmic bytes per launch / its mean duration
+           (CUDA events recorded on its stream inside pa_run) against the
+           measured HBM copy bandwidth
+  cpu_baseline  the fp64 oracle timed on this host's cores on a bounded gate
+           sample of the same workload
+
+``--impl reference`` times the oracle alone (rank 0), on the same workload and
+metric.
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "events/sec (dyn+leak) at 1 GB300; achieved HBM GB/s as % of roofline"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", type=int, default=4)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle sample time")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------- distributed
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class Dist:
+    def __init__(self, backend):
+        self.world, self.rank, self.local = dist_env()
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as td
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            td.init_process_group(backend)
+            self.pg = td
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        dev = torch.device("cuda", self.local) if torch.cuda.is_available() else torch.device("cpu")
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) while timed work runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.rows = []
+        self.proc = None
+        self.sel = self._selector(device_index)
+        self.active = False
+        self._t = None
+
+    @staticmethod
+    def _selector(idx):
+        try:
+            import torch
+            u = str(torch.cuda.get_device_properties(idx).uuid)
+            if u and not u.startswith("GPU-"):
+                u = "GPU-" + u
+            return ["-i", u]
+        except Exception:
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+            first = vis.split(",")[idx] if vis else str(idx)
+            return ["-i", first]
+
+    def start(self):
+        cmd = ["nvidia-smi", *self.sel, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            if self.active:
+                self.rows.append(line.strip())
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in self.rows:
+            f = [x.strip() for x in r.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() in ("active", "1"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- workload
+
+def pinned_alloc():
+    import torch
+    keep = []
+
+    def alloc(shape, dtype):
+        n = int(np.prod(shape))
+        tt = torch.empty(n * np.dtype(dtype).itemsize, dtype=torch.uint8, pin_memory=True)
+        keep.append(tt)
+        return tt.numpy().view(dtype).reshape(shape)
+    return alloc, keep
+
+
+def algorithmic_bytes(w) -> int:
+    """Bytes the method must move once per pass: events (t + slew, 8 B each),
+    pin offsets (8 B per pin + 1), per-gate cell id, load and initial state
+    (4 + 4 + 1 B), per-cycle outputs (waveform f32 + two u32 counts) and the
+    tables."""
+    return int(8 * w.n_events + 8 * (w.n_pins + 1) + 9 * w.n_gates + 12 * w.n_cycles
+               + 4 * len(w.lut) + 4 * len(w.leak))
+
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gate_level_power_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    with open(os.path.join(ROOT, "include", "pa.h"), "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(config: int):
+    """DRAM bytes per fused launch from the committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "fused_power_kernel.md")
+    if not os.path.exists(p):
+        return None
+    txt = open(p).read()
+    m = re.search(r"traffic_bytes_per_launch_config%d:\s*([0-9.eE+]+)\s+source:\s*([0-9a-f]+)" % config, txt)
+    if not m or m.group(2) != kernel_source_digest():
+        return None
+    return float(m.group(1))
+
+
+def cpu_baseline(config, seed, target_s, n_events_total, n_gates_total):
+    """Time the oracle (fp64, as it stands) on a contiguous gate block of the
+    workload, grown until one run takes about target_s."""
+    import oracle
+    import synth
+    cores = os.cpu_count() or 1
+    g0 = n_gates_total // 3
+    n = max(64, min(n_gates_total, 2000))
+    el = 0.0
+    while True:
+        w = synth.generate_range(config, g0, min(n_gates_total, g0 + n), seed=seed)
+        t0 = time.perf_counter()
+        oracle.run(w, threads=cores)
+        el = time.perf_counter() - t0
+        if el >= 0.5 * target_s or n >= n_gates_total or g0 + n >= n_gates_total:
+            break
+        grow = target_s / max(el, 1e-3)
+        n = int(min(n_gates_total - g0, max(2 * n, n * min(grow, 50))))
+    ev = w.n_events
+    return {"value": ev / el, "unit": "events/s", "cores": cores, "kind": "oracle",
+            "sample": f"fp64 oracle, full waveform, gates [{g0}, {g0 + w.n_gates}) of {n_gates_total} "
+                      f"({ev} of {n_events_total} events), {el:.2f} s on {cores} threads"}
+
+
+# ----------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    import synth
+    cfg = synth.make_cfg(args.config, args.seed)
+    G, E = int(cfg.n_gates), int(cfg.n_events)
+    cores = os.cpu_count() or 1
+    # size the per-step sample so warmup + steps take a few minutes at most
+    probe = synth.generate_range(args.config, G // 3, G // 3 + 2000, seed=args.seed)
+    t0 = time.perf_counter()
+    oracle.run(probe, threads=cores)
+    per_gate = (time.perf_counter() - t0) / probe.n_gates
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    n = int(max(200, min(G // 3, budget / max(per_gate, 1e-9))))
+    w = synth.generate_range(args.config, G // 3, G // 3 + n, seed=args.seed)
+    for _ in range(args.warmup):
+        oracle.run(w, threads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.run(w, threads=cores)
+    el = time.perf_counter() - t0
+    v = w.n_events * args.steps / el
+    sample = (f"fp64 oracle, full waveform, gates [{G // 3}, {G // 3 + w.n_gates}) of {G} "
+              f"({w.n_events} of {E} events) per step, {cores} threads")
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "events/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(args.config, G, E, cfg),
+            "cpu_baseline": {"value": v, "unit": "events/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": "events/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(config, G, E, cfg):
+    import synth
+    return {"workload": f"config {config}: " + synth.CONFIG_NAMES.get(config, "custom"),
+            "gates": G, "events": E, "cycles": int(cfg.n_cycles), "t_clk_ns": float(cfg.t_clk_ns),
+            "seed": int(cfg.seed),
+            "l2": "inputs larger than L2 (events alone exceed 129 MB); no flush between steps"
+            if E * 8 > 256e6 else "inputs smaller than L2: L2 not flushed (context only)"}
+
+
+# ----------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import torch
+
+    import gate_level_power_gb300 as glp
+    import synth
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = Dist("nccl")
+    glp.load_library()
+    alloc, keep = pinned_alloc()
+    t0 = time.perf_counter()
+    w = synth.generate(args.config, seed=args.seed, alloc=alloc)
+    gen_s = time.perf_counter() - t0
+    cfg = synth.make_cfg(args.config, args.seed)
+    E, G, N = w.n_events, w.n_gates, w.n_cycles
+    stream = torch.cuda.Stream(device=local)
+    pa = glp.PowerAnalyzer(local, stream.cuda_stream)
+    pa.load_workload(w)
+    wave = np.empty(N, np.float32)
+    evc = np.empty(N, np.uint32)
+    glc = np.empty(N, np.uint32)
+    out = dict(waveform=wave, event_count=evc, glitch_count=glc)
+
+    def step(timing=False):
+        return pa.run(w.vdd, w.t_clk_ns, N, out=out, timing=timing)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    clk = ClockSampler(local)
+    clk.start()
+    time.sleep(0.3)
+    # ---- device-resident timed region
+    dist.barrier()
+    torch.cuda.synchronize()
+    clk.active = True
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    fused_ms = []
+    launches = 0
+    for _ in range(args.steps):
+        r = step(timing=True)
+        fused_ms.append(r["ms_fused"])
+        launches += r["kernel_launches"]
+    e1.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    el_ms = e0.elapsed_time(e1)
+    el_ms = dist.max(el_ms)
+    value = world * E * args.steps / (el_ms * 1e-3)
+    # ---- end to end through the public API, host buffers
+    h2d = 8 * (w.n_pins + 1) + 4 * E + 4 * E + E
+    d2h = 4 * N + 4 * N + 4 * N + 4 * 8
+    for _ in range(2):
+        pa.load_events(w.pin_off, w.t_ns, w.slew_ps, w.value)
+        step()
+    dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        pa.load_events(w.pin_off, w.t_ns, w.slew_ps, w.value)
+        step()
+    torch.cuda.synchronize()
+    e2e_s = dist.max(time.perf_counter() - t0)
+    clk.active = False
+    clk.stop()
+    e2e_value = world * E * args.e2e_steps / e2e_s
+    # ---- roofline of the fused kernel
+    fused_mean = statistics.mean(fused_ms)
+    B = algorithmic_bytes(w)
+    peak, peak_kind = hbm_peak()
+    achieved = B / (fused_mean * 1e-3) / 1e9
+    traffic = ncu_traffic(args.config)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.config, args.seed, args.cpu_seconds, E, G)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "events/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": el_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": workload_config(args.config, G, E, cfg),
+            "gate_cycles_per_s": world * G * N * args.steps / (el_ms * 1e-3),
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "kernel": "k_fused (fused dynamic + leakage power)",
+                         "algorithmic_bytes_per_launch": B, "mean_launch_ms": fused_mean,
+                         "peak_source": f"{peak_kind} HBM copy bandwidth"},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "events/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+                    "note": "per step: pa_load_events from pinned host memory (device-side validation) + "
+                            "pa_run + waveform/count copy to host; library and netlist loaded once"},
+            "clocks": clk.summary(),
+            "gpu_launches": launches,
+            "gen_seconds": gen_s,
+            "p_total_w": r["p_int"] + r["p_sw"] + r["p_gl"] + r["p_leak"],
+            "n_tiles": r["n_tiles"], "n_heavy": r["n_heavy"],
+        }
+        print(json.dumps(line), flush=True)
+    pa.close()
+    dist.close()
+    del keep
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,242 @@
+/*
+ * pa.h -- gate-level time-based power analysis on one GB300 (sm_103a).
+ *
+ * C ABI of libpa.so. The operation is the power-computation step of "GPU-
+ * Accelerated Gate-Level Time-Based Power Analysis via Event-Density-Aware
+ * Partitioning and Kernel Fusion":
+ *   - per-event dynamic power (Section 2.4.1, Fig. 2): the gate state before
+ *     the event's timestamp selects the state-dependent NLDM internal-power
+ *     table, which is bilinearly interpolated on input slew and output load;
+ *     switching energy of an output transition from load and supply (Eq. 1);
+ *     clock-cycle glitch detection (more than one event on a pin within a
+ *     cycle) with the glitch energy scaled by r_gl (Eq. 2); each contribution
+ *     p = E / t_max (Eq. 3) goes to the design-level internal, switching and
+ *     glitch totals and to the per-cycle power waveform;
+ *   - per-gate leakage (Section 2.4.2, Fig. 3): k-way merge of the per-pin
+ *     event streams, state-indexed leakage held over each inter-event interval
+ *     (Eq. 4), each interval split across cycle bins in proportion to overlap;
+ *   - fused into one pass as in the fused kernel of Fig. 7 (all pins with an
+ *     event at t_cur see the same state S; per-pin event counter per cycle).
+ *
+ * Readings where the extracted text of the paper lost its equations:
+ *   E_sw = 1/2 * C * V^2 per output transition (rise or fall);
+ *   r_gl = min(1, pulse_width / ((rSlew + fSlew) / 2)), pulse width = time since
+ *     the previous event on the same pin, slews of the pulse's two edges;
+ *   the first event of a pin in a cycle is regular, the 2nd and later in that
+ *     cycle are glitches and contribute only r_gl * (E_int + E_sw);
+ *   input-pin events carry E_int, output-pin events E_sw; the gate state is
+ *     the vector of input-pin values (bit j = input j);
+ *   cycle of an event c = floor(fl32(t / t_clk)), IEEE fp32 division;
+ *   leakage is integrated over [0, t_max) including the intervals before the
+ *     first and after the last event; t_max defaults to n_cycles * t_clk.
+ *
+ * Units: time ns, slew ps, load fF, vdd V, internal energy fJ, leakage nW;
+ * results in W.
+ *
+ * Threading: a pa_ctx is used by one host thread at a time. Every call is
+ * synchronous with respect to the host: when it returns, its device work on
+ * the context's stream has completed.
+ *
+ * Errors: every int-returning call returns PA_OK (0) or a negative PA_ERR_*.
+ * No C++ exception crosses the ABI. pa_last_error() describes the most recent
+ * failure (first offending pin/event for validation errors). Outputs are
+ * written only on PA_OK.
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PA_VERSION 1
+
+#define PA_OK 0
+#define PA_ERR_ARG (-1)      /* null pointer, bad size, bad axis, bad parameter      */
+#define PA_ERR_ORDER (-2)    /* library -> netlist -> events -> run order violated    */
+#define PA_ERR_UNSORTED (-3) /* a pin's event times are not strictly increasing       */
+#define PA_ERR_RANGE (-4)    /* t < 0, t not finite, slew <= 0, cell id out of range,
+                                event cycle >= n_cycles, t_max earlier than an event  */
+#define PA_ERR_TOGGLE (-5)   /* an event's value equals the pin's previous value      */
+#define PA_ERR_OOM (-6)      /* device or host allocation failed                     */
+#define PA_ERR_CUDA (-7)     /* a CUDA runtime call failed                           */
+#define PA_ERR_INTERNAL (-8) /* a device-side consistency check failed               */
+
+#define PA_MEM_HOST 0   /* pointers are host memory (pageable or pinned)   */
+#define PA_MEM_DEVICE 1 /* pointers are device memory on the ctx's device  */
+
+#define PA_MAX_INPUTS 4 /* k, inputs per cell: 1..4 (2^k gate states)       */
+#define PA_MAX_AXIS 8   /* LUT axis points per dimension: 2..8              */
+
+typedef struct pa_ctx pa_ctx;
+
+/*
+ * Cell library (Section 2.4.1 Fig. 2; Section 2.4.2 Fig. 3). Host memory,
+ * copied by pa_load_library; the caller keeps ownership.
+ *   n_inputs[c]          k in [1, 4]; cell c has 2^k states, state bit j = input j
+ *   n_slew[c], n_load[c] axis lengths in [2, 8]
+ *   slew_axis[c*8 + i]   ps, strictly increasing over i < n_slew[c]
+ *   load_axis[c*8 + j]   fF, strictly increasing over j < n_load[c]
+ *   lut[lut_off[c] + (S*n_slew[c] + i)*n_load[c] + j]   fJ, internal energy
+ *                        of an input transition in state S at (slew_i, load_j)
+ *   leak[leak_off[c] + S]  nW, leakage power in state S
+ * Interpolation: interval index = largest axis index <= x clamped to
+ * [0, n - 2]; linear extrapolation outside the axes.
+ */
+typedef struct pa_library {
+  uint32_t n_cells;
+  const uint8_t *n_inputs;
+  const uint8_t *n_slew;
+  const uint8_t *n_load;
+  const float *slew_axis;
+  const float *load_axis;
+  const uint32_t *lut_off;
+  const float *lut;
+  uint64_t lut_len;
+  const uint32_t *leak_off;
+  const float *leak;
+  uint64_t leak_len;
+} pa_library;
+
+/*
+ * Netlist. Host memory, copied by pa_load_netlist (requires a library).
+ * Gate g is an instance of cell_id[g] with k = n_inputs[cell_id[g]] inputs; it
+ * owns pins pin_base(g) .. pin_base(g) + k where pin_base(g) = sum over g' < g
+ * of (k(g') + 1): inputs 0..k-1 first, the output pin last.
+ *   load_ff[g]   total output load capacitance (load pins + interconnect), fF
+ *   init_in[g]   initial input values, bit j = input j
+ *   init_out[g]  initial output value, 0 or 1
+ */
+typedef struct pa_netlist {
+  uint32_t n_gates;
+  const uint32_t *cell_id;
+  const float *load_ff;
+  const uint8_t *init_in;
+  const uint8_t *init_out;
+} pa_netlist;
+
+/*
+ * Per-pin event streams in CSR form (requires a netlist).
+ *   pin_off[n_pins + 1]  events of pin p are [pin_off[p], pin_off[p+1]);
+ *                        pin_off[0] = 0, pin_off[n_pins] = n_events;
+ *                        n_pins must equal the netlist's pin count
+ *   t_ns[e]              event time, finite, >= 0, strictly increasing per pin
+ *   slew_ps[e]           transition time, finite, > 0
+ *   value[e]             new logic value (0/1), must differ from the pin's
+ *                        previous value; NULL means every event toggles
+ * mem = PA_MEM_HOST: host arrays, copied. PA_MEM_DEVICE: device arrays on the
+ * ctx's device; copied on the device, so the caller may free them after the
+ * call. Device arrays must be complete when the call is made: the ctx's
+ * stream does not wait on other streams. Either way the library keeps its own padded copy of pin_off, t_ns and
+ * slew_ps until the next pa_load_events or pa_destroy.
+ */
+typedef struct pa_events {
+  uint64_t n_pins;
+  uint64_t n_events;
+  const uint64_t *pin_off;
+  const float *t_ns;
+  const float *slew_ps;
+  const uint8_t *value;
+  int32_t mem;
+} pa_events;
+
+#define PA_RUN_TIMING 1u /* record per-kernel CUDA-event times in pa_result */
+
+/*
+ * Run parameters. pa_default_params() fills the defaults.
+ *   vdd            supply voltage, V
+ *   t_clk_ns       clock period, ns (> 0)
+ *   n_cycles       cycle bins (> 0); every event needs floor(fl32(t/t_clk)) < n_cycles
+ *   t_max_ns       analysis window end for Eq. 3 and leakage; 0 -> n_cycles * t_clk;
+ *                  otherwise it must be >= the latest event time
+ *   tile_events    work partition: target events per light tile (0 = default 2048)
+ *   heavy_events   gates with more events than this are streamed in event-count
+ *                  windows by one CTA (0 = default 2048); tile_events +
+ *                  heavy_events must not exceed 4096
+ *   flags          PA_RUN_* bits
+ * The partition knobs change only how work is cut, never the results beyond
+ * floating-point summation order.
+ */
+typedef struct pa_run_params {
+  double vdd;
+  float t_clk_ns;
+  uint32_t n_cycles;
+  double t_max_ns;
+  uint32_t tile_events;
+  uint32_t heavy_events;
+  uint32_t flags;
+} pa_run_params;
+
+/*
+ * Results. Scalars are outputs; array pointers are caller-owned inputs (NULL =
+ * not wanted), host or device memory per out_mem.
+ *   waveform_w[n_cycles]    per-cycle power, W (energy in the cycle / t_clk)
+ *   event_count[n_cycles]   events per cycle
+ *   glitch_count[n_cycles]  glitch events per cycle
+ *   state_pre[n_events]     per event: input state before its timestamp (debug)
+ *   lut_ij[n_events]        per input event: (i << 4) | j of the LUT interval;
+ *                           0xFF for output events (debug)
+ *   is_glitch[n_events]     per event: 1 if a glitch (debug)
+ * With PA_RUN_TIMING, ms_* hold CUDA-event times of the partition, fused and
+ * reduction kernels and of the whole device pass.
+ */
+typedef struct pa_result {
+  double p_int_w, p_sw_w, p_gl_w, p_leak_w;
+  double t_max_ns;
+  int32_t out_mem;
+  float *waveform_w;
+  uint32_t *event_count;
+  uint32_t *glitch_count;
+  uint8_t *state_pre;
+  uint8_t *lut_ij;
+  uint8_t *is_glitch;
+  float ms_partition, ms_fused, ms_reduce, ms_total;
+  uint32_t n_tiles, n_heavy;
+  uint32_t kernel_launches;
+} pa_result;
+
+/* Create a context on CUDA device `cuda_device`. `cuda_stream` is a
+ * cudaStream_t to run on (borrowed, must outlive the ctx) or NULL for a stream
+ * the ctx creates. Errors: PA_ERR_ARG, PA_ERR_CUDA, PA_ERR_OOM. */
+int pa_create(pa_ctx **out, int cuda_device, void *cuda_stream);
+
+/* Free every device and host buffer the ctx owns. NULL is a no-op. */
+void pa_destroy(pa_ctx *ctx);
+
+/* Load (replace) the cell library. Replacing it drops the netlist and events.
+ * Errors: PA_ERR_ARG (k, axis length, non-increasing axis, offsets out of
+ * range, non-finite values), PA_ERR_OOM, PA_ERR_CUDA. */
+int pa_load_library(pa_ctx *ctx, const pa_library *lib);
+
+/* Load (replace) the netlist; requires a library. Drops loaded events.
+ * Errors: PA_ERR_ORDER, PA_ERR_ARG, PA_ERR_RANGE (cell id >= n_cells, load
+ * not finite or < 0, init bits beyond k), PA_ERR_OOM, PA_ERR_CUDA. */
+int pa_load_netlist(pa_ctx *ctx, const pa_netlist *nl);
+
+/* Load (replace) the events; requires a netlist. Validates them on the device.
+ * Errors: PA_ERR_ORDER, PA_ERR_ARG (pin count, pin_off not monotone or not
+ * ending at n_events), PA_ERR_UNSORTED, PA_ERR_RANGE, PA_ERR_TOGGLE,
+ * PA_ERR_OOM, PA_ERR_CUDA. On error no events are loaded. */
+int pa_load_events(pa_ctx *ctx, const pa_events *ev);
+
+/* Run partition -> fused power kernel -> final reduction on the loaded data.
+ * May be called repeatedly with different parameters. Errors: PA_ERR_ORDER,
+ * PA_ERR_ARG, PA_ERR_RANGE (an event's cycle >= n_cycles, t_max too early),
+ * PA_ERR_OOM, PA_ERR_CUDA, PA_ERR_INTERNAL. */
+int pa_run(pa_ctx *ctx, const pa_run_params *params, pa_result *out);
+
+/* Defaults: vdd 0.9 V, t_clk 1 ns, n_cycles 1, t_max 0, partition knobs 0. */
+void pa_default_params(pa_run_params *params);
+
+/* Text of the most recent error on ctx; valid until the next call on ctx. */
+const char *pa_last_error(const pa_ctx *ctx);
+
+/* PA_VERSION of the library. */
+int pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PA_H */

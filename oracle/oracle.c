@@ -71,6 +71,8 @@ typedef struct {
   or_out *out;
   const uint64_t *pin_base; /* [gate_end - gate_begin + 1] */
   const int32_t *bin_of;    /* [n_cycles] sample index or -1; NULL in full mode */
+  const uint32_t *sorted;   /* sampled cycles, ascending and distinct (sample mode) */
+  uint32_t n_sorted;
   uint32_t n_bins;
   double T;                 /* (double) t_clk */
   double t_max;
@@ -103,17 +105,28 @@ static void leak_interval(const ctx_t *X, acc_t *A, double p_nw, double a, doubl
   const int64_t n_cyc = (int64_t)X->par->n_cycles;
   int64_t c0 = (int64_t)floor(a / T);
   if (c0 < 0) c0 = 0;
+  if (X->bin_of) {
+    /* only the sampled cycles: first sampled cycle >= c0, then walk */
+    uint32_t lo_i = 0, hi_i = X->n_sorted;
+    while (lo_i < hi_i) {
+      const uint32_t mid = (lo_i + hi_i) / 2;
+      if ((int64_t)X->sorted[mid] < c0) lo_i = mid + 1; else hi_i = mid;
+    }
+    for (uint32_t i = lo_i; i < X->n_sorted; ++i) {
+      const int64_t c = X->sorted[i];
+      const double lo = (double)c * T, hi = (double)(c + 1) * T;
+      if (lo >= b) break;
+      const double ov = (b < hi ? b : hi) - (a > lo ? a : lo);
+      if (ov > 0) A->wave[X->bin_of[c]] += p_nw * ov * 1e-3;
+    }
+    return;
+  }
   for (int64_t c = c0; c < n_cyc; ++c) {
     const double lo = (double)c * T, hi = (double)(c + 1) * T;
     if (lo >= b) break;
     const double ov = (b < hi ? b : hi) - (a > lo ? a : lo);
     if (ov <= 0) continue;
-    if (X->bin_of) {
-      const int32_t k = X->bin_of[c];
-      if (k >= 0) A->wave[k] += p_nw * ov * 1e-3;
-    } else {
-      A->wave[c] += p_nw * ov * 1e-3;
-    }
+    A->wave[c] += p_nw * ov * 1e-3;
   }
 }
 
@@ -285,17 +298,33 @@ int or_run(const or_lib *lib, const or_net *net, const or_ev *ev, const or_par *
   X.pin_base = pin_base;
 
   int32_t *bin_of = NULL;
+  uint32_t *sorted = NULL;
   X.n_bins = par->n_cycles;
   if (par->wave_mode == OR_WAVE_SAMPLE) {
     bin_of = (int32_t *)malloc((size_t)par->n_cycles * sizeof(int32_t));
-    if (!bin_of) {
+    sorted = (uint32_t *)malloc(((size_t)par->n_sample + 1) * sizeof(uint32_t));
+    if (!bin_of || !sorted) {
+      free(bin_of);
+      free(sorted);
       free(pin_base);
       return -2;
     }
     for (uint32_t c = 0; c < par->n_cycles; ++c) bin_of[c] = -1;
-    for (uint32_t i = 0; i < par->n_sample; ++i)
-      if (par->sample_cycles[i] < par->n_cycles) bin_of[par->sample_cycles[i]] = (int32_t)i;
+    for (uint32_t i = 0; i < par->n_sample; ++i) {
+      if (par->sample_cycles[i] >= par->n_cycles || bin_of[par->sample_cycles[i]] >= 0) {
+        free(bin_of);
+        free(sorted);
+        free(pin_base);
+        return -1; /* sampled cycles must be distinct and in range */
+      }
+      bin_of[par->sample_cycles[i]] = (int32_t)i;
+    }
+    uint32_t n = 0;
+    for (uint32_t c = 0; c < par->n_cycles; ++c)
+      if (bin_of[c] >= 0) sorted[n++] = c;
     X.bin_of = bin_of;
+    X.sorted = sorted;
+    X.n_sorted = n;
     X.n_bins = par->n_sample;
   }
 
@@ -359,6 +388,7 @@ int or_run(const or_lib *lib, const or_net *net, const or_ev *ev, const or_par *
   free(jobs);
   free(th);
   free(bin_of);
+  free(sorted);
   free(pin_base);
   return rc;
 }

@@ -110,6 +110,8 @@ def _load():
         L.synth_fill_netlist.argtypes = [vp] * 5
         L.synth_fill_events.argtypes = [vp] * 5 + [ctypes.POINTER(SynthStats)]
         L.synth_get_stats.argtypes = [vp, ctypes.POINTER(SynthStats)]
+        L.synth_range.argtypes = [vp, ctypes.c_int64, ctypes.c_int64, u64p, u64p, u64p, u64p]
+        L.synth_fill_range.argtypes = [vp, ctypes.c_int64, ctypes.c_int64, vp, vp, vp, vp]
         _lib = L
     return _lib
 
@@ -220,6 +222,45 @@ def generate(config: int, seed: int = 0, alloc=None, with_value: bool = True, **
                         load_axis=lax, lut_off=lut_off, lut=lut, leak_off=leak_off, leak=leak,
                         cell_id=cell, load_ff=load, init_in=ii, init_out=io, pin_off=pin_off,
                         t_ns=t, slew_ps=s, value=v, stats=stats)
+    finally:
+        L.synth_destroy(h)
+
+
+def generate_range(config: int, g0: int, g1: int, seed: int = 0, **overrides) -> Workload:
+    """Gates [g0, g1) of a workload as a workload of their own (pin offsets
+    rebased), identical to that slice of ``generate(config, seed)``. Lets a
+    CPU sample of a large workload be drawn without generating all of it."""
+    L = _load()
+    cfg = make_cfg(config, seed, **overrides)
+    h = L.synth_create(ctypes.byref(cfg))
+    try:
+        L.synth_get_cfg(h, ctypes.byref(cfg))
+        nc = ctypes.c_uint32()
+        lut_len, leak_len, G, P, E = (ctypes.c_uint64() for _ in range(5))
+        L.synth_sizes(h, ctypes.byref(nc), ctypes.byref(lut_len), ctypes.byref(leak_len),
+                      ctypes.byref(G), ctypes.byref(P), ctypes.byref(E))
+        nc, G = nc.value, G.value
+        g0, g1 = max(0, int(g0)), min(G, int(g1))
+        k = np.empty(nc, np.uint8); ns = np.empty(nc, np.uint8); nl = np.empty(nc, np.uint8)
+        sax = np.empty((nc, 8), np.float32); lax = np.empty((nc, 8), np.float32)
+        lut_off = np.empty(nc, np.uint32); leak_off = np.empty(nc, np.uint32)
+        lut = np.empty(lut_len.value, np.float32); leak = np.empty(leak_len.value, np.float32)
+        L.synth_fill_library(h, *(_ptr(a) for a in (k, ns, nl, sax, lax, lut_off, lut, leak_off, leak)))
+        cell = np.empty(G, np.uint32); load = np.empty(G, np.float32)
+        ii = np.empty(G, np.uint8); io = np.empty(G, np.uint8)
+        L.synth_fill_netlist(h, _ptr(cell), _ptr(load), _ptr(ii), _ptr(io))
+        plo, phi, elo, ehi = (ctypes.c_uint64() for _ in range(4))
+        L.synth_range(h, g0, g1, ctypes.byref(plo), ctypes.byref(phi), ctypes.byref(elo), ctypes.byref(ehi))
+        n_p, n_e = phi.value - plo.value, ehi.value - elo.value
+        pin_off = np.empty(n_p + 1, np.uint64)
+        t = np.empty(n_e, np.float32); s = np.empty(n_e, np.float32); v = np.empty(n_e, np.uint8)
+        L.synth_fill_range(h, g0, g1, _ptr(pin_off), _ptr(t), _ptr(s), _ptr(v))
+        return Workload(config=config, seed=seed, vdd=cfg.vdd, t_clk_ns=float(np.float32(cfg.t_clk_ns)),
+                        n_cycles=cfg.n_cycles, n_inputs=k, n_slew=ns, n_load=nl, slew_axis=sax,
+                        load_axis=lax, lut_off=lut_off, lut=lut, leak_off=leak_off, leak=leak,
+                        cell_id=cell[g0:g1].copy(), load_ff=load[g0:g1].copy(), init_in=ii[g0:g1].copy(),
+                        init_out=io[g0:g1].copy(), pin_off=pin_off, t_ns=t, slew_ps=s, value=v,
+                        stats={"gate_range": (g0, g1), "n_gates_total": G})
     finally:
         L.synth_destroy(h)
 

@@ -566,4 +566,28 @@ void synth_fill_events(void* h, uint64_t* pin_off, float* t, float* slew, uint8_
 
 void synth_get_stats(void* h, synth_stats* stats) { *stats = ((Synth*)h)->stats; }
 
+// Pin and event ranges of gates [g0, g1).
+void synth_range(void* h, int64_t g0, int64_t g1, uint64_t* pin_lo, uint64_t* pin_hi, uint64_t* ev_lo,
+                 uint64_t* ev_hi) {
+  Synth* S = (Synth*)h;
+  *pin_lo = S->pin_base[g0];
+  *pin_hi = S->pin_base[g1];
+  *ev_lo = S->pin_off[*pin_lo];
+  *ev_hi = S->pin_off[*pin_hi];
+}
+
+// Events of gates [g0, g1) only, rebased: pin_off[0] = 0. Bit-identical to
+// the same slice of synth_fill_events.
+void synth_fill_range(void* h, int64_t g0, int64_t g1, uint64_t* pin_off, float* t, float* slew,
+                      uint8_t* value) {
+  Synth* S = (Synth*)h;
+  const uint64_t p0 = S->pin_base[g0], p1 = S->pin_base[g1];
+  const uint64_t e0 = S->pin_off[p0];
+  for (uint64_t p = p0; p <= p1; ++p) pin_off[p - p0] = S->pin_off[p] - e0;
+  parallel_blocks(g1 - g0, 1024, hw_threads(S->cfg.threads), [&](int64_t lo, int64_t hi) {
+    uint64_t a = 0, m = 0;
+    fill_gates(*S, g0 + lo, g0 + hi, e0, t, slew, value, &a, &m);
+  });
+}
+
 }  // extern "C"

@@ -1,0 +1,81 @@
+"""Full-size parity on the large configurations (200M, 1B and 2B events), in
+the launch configuration the benchmark times.
+
+At these sizes the oracle cannot afford its full per-cycle leakage split over
+every gate, so it checks what it can compute one by one:
+  * all four power totals and the per-cycle event and glitch counts over every
+    gate (totals within 1e-5 relative, counts bit-exact);
+  * the waveform on sampled cycles, including the GPU's peak cycle (each
+    within 1e-4 of the peak bin), all gates contributing;
+  * per-event gate state, LUT interval and glitch flag bit-exact on sampled gate
+    blocks, which include the heaviest gates (streamed in windows).
+"""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+TOL_P = 1e-5
+TOL_W = 1e-4
+
+
+@pytest.fixture(scope="module")
+def glp():
+    import gate_level_power_gb300 as glp
+    glp.build()
+    return glp
+
+
+def sub_workload(w, pb, g0, g1):
+    """Gates [g0, g1) of w as a workload of their own (offsets rebased)."""
+    import copy
+    p0, p1 = int(pb[g0]), int(pb[g1])
+    e0, e1 = int(w.pin_off[p0]), int(w.pin_off[p1])
+    s = copy.copy(w)
+    s.cell_id, s.load_ff = w.cell_id[g0:g1], w.load_ff[g0:g1]
+    s.init_in, s.init_out = w.init_in[g0:g1], w.init_out[g0:g1]
+    s.pin_off = w.pin_off[p0:p1 + 1] - w.pin_off[p0]
+    s.t_ns, s.slew_ps = w.t_ns[e0:e1], w.slew_ps[e0:e1]
+    s.value = w.value[e0:e1]
+    return s, e0, e1
+
+
+@pytest.mark.parametrize("cfg", [3, 4, 5])
+def test_full_size_config(glp, cfg):
+    threads = os.cpu_count() or 8
+    w = synth.generate(cfg)
+    E, G, N = w.n_events, w.n_gates, w.n_cycles
+    with glp.PowerAnalyzer(0) as pa:
+        pa.load_workload(w)
+        r = pa.run(w.vdd, w.t_clk_ns, N, debug=True, timing=True)
+    assert r["n_heavy"] > 0 and r["n_tiles"] > 0
+    # totals, counts and sampled cycles over all gates
+    rng = np.random.default_rng(cfg)
+    peak_c = int(np.argmax(r["waveform"]))
+    cyc = np.unique(np.concatenate([[0, N - 1, peak_c], rng.choice(N, 61, replace=False)])).astype(np.uint32)
+    o = oracle.run(w, wave="sample", sample_cycles=cyc, threads=threads)
+    for key in ("p_int", "p_sw", "p_gl", "p_leak"):
+        assert abs(r[key] - o[key]) <= TOL_P * abs(o[key]), (key, r[key], o[key])
+    np.testing.assert_array_equal(r["event_count"].astype(np.uint64), o["evcount"])
+    np.testing.assert_array_equal(r["glitch_count"].astype(np.uint64), o["glcount"])
+    assert int(o["evcount"].sum()) == E
+    peak = float(np.abs(o["waveform"]).max())
+    err = np.abs(r["waveform"][cyc].astype(np.float64) - o["waveform"])
+    assert float(err.max()) <= TOL_W * peak, (float(err.max()), peak)
+    # per-event outputs on sampled gate blocks, heaviest gates included
+    pb = w.pin_base().astype(np.int64)
+    n_g = np.diff(w.pin_off.astype(np.int64)[pb])
+    heavy = np.argsort(n_g)[-12:]
+    blocks = [(int(g), int(g) + 1) for g in heavy]
+    for b in rng.choice(G - 3000, 6, replace=False):
+        blocks.append((int(b), int(b) + 3000))
+    for g0, g1 in blocks:
+        s, e0, e1 = sub_workload(w, pb, g0, g1)
+        so = oracle.run(s, wave="none", debug=True)
+        for key in ("state_pre", "lut_ij", "is_glitch"):
+            np.testing.assert_array_equal(r[key][e0:e1], so[key], err_msg=f"{key} gates [{g0}, {g1})")

@@ -250,3 +250,34 @@ def test_gate_order_invariance():
         assert r[key] == pytest.approx(r2[key], rel=1e-13)
     np.testing.assert_allclose(r["waveform"], r2["waveform"], rtol=1e-12)
     np.testing.assert_array_equal(r["evcount"], r2["evcount"])
+
+
+def test_sampled_cycles_match_full_waveform():
+    w = synth.generate(2)
+    full = oracle.run(w, threads=4)
+    cyc = np.array([0, 3, 17, 500, 998, 999, 250], np.uint32)
+    smp = oracle.run(w, threads=4, wave="sample", sample_cycles=cyc)
+    np.testing.assert_allclose(smp["waveform"], full["waveform"][cyc], rtol=1e-12)
+    none = oracle.run(w, threads=4, wave="none")
+    for key in ("p_int", "p_sw", "p_gl", "p_leak"):
+        assert none[key] == pytest.approx(full[key], rel=1e-13)
+    np.testing.assert_array_equal(none["evcount"], full["evcount"])
+
+
+def test_generator_range_matches_full_slice():
+    w = synth.generate(2)
+    g0, g1 = 1234, 5678
+    r = synth.generate_range(2, g0, g1)
+    pb = pin_base(w)
+    p0, p1 = int(pb[g0]), int(pb[g1])
+    e0, e1 = int(w.pin_off[p0]), int(w.pin_off[p1])
+    np.testing.assert_array_equal(r.pin_off, w.pin_off[p0:p1 + 1] - w.pin_off[p0])
+    np.testing.assert_array_equal(r.t_ns, w.t_ns[e0:e1])
+    np.testing.assert_array_equal(r.slew_ps, w.slew_ps[e0:e1])
+    np.testing.assert_array_equal(r.value, w.value[e0:e1])
+    np.testing.assert_array_equal(r.cell_id, w.cell_id[g0:g1])
+    # the oracle on the block equals the oracle restricted to those gates (same events, same units)
+    a = oracle.run(r, wave="none")
+    b = oracle.run(w, wave="none", gate_range=(g0, g1))
+    for key in ("e_int", "e_sw", "e_gl", "e_leak"):
+        assert a[key] == pytest.approx(b[key], rel=1e-13)
