@@ -68,7 +68,9 @@ class PaError(RuntimeError):
 
 
 EXPORTS = ("pa_create", "pa_destroy", "pa_load_library", "pa_load_netlist", "pa_load_events", "pa_run",
-           "pa_default_params", "pa_last_error", "pa_version")
+           "pa_run_noalloc", "pa_default_params", "pa_last_error", "pa_version")
+PA_NOALLOC_MAX_CYCLES = 65536
+PA_NOALLOC_MAX_GATES = 262144
 
 _lib = None
 
@@ -91,6 +93,7 @@ def load_library():
         L.pa_load_netlist.argtypes = [_vp, ctypes.POINTER(PaNetlist)]
         L.pa_load_events.argtypes = [_vp, ctypes.POINTER(PaEvents)]
         L.pa_run.argtypes = [_vp, ctypes.POINTER(PaRunParams), ctypes.POINTER(PaResult)]
+        L.pa_run_noalloc.argtypes = [_vp, ctypes.POINTER(PaRunParams), ctypes.POINTER(PaResult)]
         L.pa_default_params.argtypes = [ctypes.POINTER(PaRunParams)]
         L.pa_default_params.restype = None
         L.pa_last_error.argtypes = [_vp]
@@ -134,6 +137,13 @@ def pa_load_events(ctx: int, ev: PaEvents) -> None:
 
 def pa_run(ctx: int, params: PaRunParams, result: PaResult) -> None:
     _check(ctx, load_library().pa_run(ctx, ctypes.byref(params), ctypes.byref(result)))
+
+
+def pa_run_noalloc(ctx: int, params: PaRunParams, result: PaResult) -> None:
+    """pa_run without any device allocation (scratch in a fixed 5 MiB device
+    array; device output arrays only; limits PA_NOALLOC_MAX_CYCLES and
+    PA_NOALLOC_MAX_GATES). For callers that may not allocate at run time."""
+    _check(ctx, load_library().pa_run_noalloc(ctx, ctypes.byref(params), ctypes.byref(result)))
 
 
 def pa_default_params() -> PaRunParams:

@@ -8,6 +8,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -538,3 +539,183 @@ int pa_run(pa_ctx* c, const pa_run_params* prm, pa_result* out) {
 }
 
 }  // extern "C"
+
+// ----------------------------------------------------------------- pa_run_noalloc
+//
+// The per-run scratch of pa_run_noalloc: one file-scope device array, so the
+// entry point never allocates. Its name is only meaningful in device code; the
+// host takes its device address once per device with cudaGetSymbolAddress.
+// Layout (each part 256-byte aligned): cycle bins [W f32 | D f32 | ev u32 |
+// gl u32] x PA_NOALLOC_MAX_CYCLES, per-block partition counts, the four
+// partition counters, tiles and heavy-gate lists for PA_NOALLOC_MAX_GATES
+// gates, P0 and totals (8 doubles) and the four result powers.
+
+namespace {
+
+constexpr size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+constexpr size_t kNaBins = 0;
+constexpr size_t kNaPartBlk = align256(kNaBins + (size_t)PA_NOALLOC_MAX_CYCLES * 16);
+constexpr size_t kNaPartCounts =
+    align256(kNaPartBlk + ((size_t)PA_NOALLOC_MAX_GATES / 256 + 2) * 2 * sizeof(uint32_t));
+constexpr size_t kNaTiles = align256(kNaPartCounts + 4 * sizeof(uint32_t));
+constexpr size_t kNaHeavy = align256(kNaTiles + ((size_t)PA_NOALLOC_MAX_GATES + 1) * sizeof(Tile));
+constexpr size_t kNaP0Tot = align256(kNaHeavy + ((size_t)PA_NOALLOC_MAX_GATES + 1) * sizeof(uint32_t));
+constexpr size_t kNaPOut = align256(kNaP0Tot + 8 * sizeof(double));
+constexpr size_t kNaEnd = align256(kNaPOut + 4 * sizeof(double));
+static_assert(kNaEnd <= (size_t)PA_NOALLOC_SCRATCH_BYTES, "no-alloc scratch layout exceeds its array");
+
+}  // namespace
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[PA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kNaMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kNaMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device `dev` (looked up
+// once per device).
+int noalloc_scratch(pa_ctx* c, int dev, unsigned char** out) {
+  if (dev < 0 || dev >= kNaMaxDevices) return fail(c, PA_ERR_ARG, "pa_run_noalloc: device ordinal %d too large", dev);
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p) {
+      cudaGetLastError();
+      return fail(c, PA_ERR_CUDA, "pa_run_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+    }
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = (unsigned char*)g_noalloc_ptr[dev];
+  return PA_OK;
+}
+
+}  // namespace
+
+extern "C" int pa_run_noalloc(pa_ctx* c, const pa_run_params* prm, pa_result* out) {
+  if (!c) return PA_ERR_ARG;
+  if (!c->has_ev) return fail(c, PA_ERR_ORDER, "pa_run_noalloc: events not loaded");
+  if (!prm || !out) return fail(c, PA_ERR_ARG, "pa_run_noalloc: null params or result");
+  if (!(prm->t_clk_ns > 0.f) || !is_finite_f(prm->t_clk_ns))
+    return fail(c, PA_ERR_ARG, "pa_run_noalloc: t_clk_ns must be > 0");
+  if (prm->n_cycles == 0) return fail(c, PA_ERR_ARG, "pa_run_noalloc: n_cycles must be > 0");
+  if (prm->n_cycles > PA_NOALLOC_MAX_CYCLES)
+    return fail(c, PA_ERR_ARG, "pa_run_noalloc: n_cycles %u exceeds PA_NOALLOC_MAX_CYCLES (%u)", prm->n_cycles,
+                PA_NOALLOC_MAX_CYCLES);
+  if (c->n_gates > PA_NOALLOC_MAX_GATES)
+    return fail(c, PA_ERR_ARG, "pa_run_noalloc: %u gates exceed PA_NOALLOC_MAX_GATES (%u)", c->n_gates,
+                PA_NOALLOC_MAX_GATES);
+  if (!std::isfinite(prm->vdd)) return fail(c, PA_ERR_ARG, "pa_run_noalloc: vdd not finite");
+  const bool any_array = out->waveform_w || out->event_count || out->glitch_count || out->state_pre ||
+                         out->lut_ij || out->is_glitch;
+  if (any_array && out->out_mem != PA_MEM_DEVICE)
+    return fail(c, PA_ERR_ARG, "pa_run_noalloc: output arrays must be device memory (out_mem = PA_MEM_DEVICE)");
+  const uint32_t tile = prm->tile_events ? prm->tile_events : kDefaultTile;
+  const uint32_t heavy = prm->heavy_events ? prm->heavy_events : kDefaultHeavy;
+  if ((uint64_t)tile + heavy > (uint64_t)kTileCap)
+    return fail(c, PA_ERR_ARG, "pa_run_noalloc: tile_events + heavy_events = %u exceeds %d", tile + heavy, kTileCap);
+  const float T = prm->t_clk_ns;
+  const double Td = (double)T;
+  const double t_max = prm->t_max_ns > 0 ? prm->t_max_ns : (double)prm->n_cycles * Td;
+  if (!std::isfinite(t_max)) return fail(c, PA_ERR_ARG, "pa_run_noalloc: t_max not finite");
+  if (c->n_events) {
+    const float cyc = std::floor(c->t_last / T);
+    if (!(cyc < (float)prm->n_cycles))
+      return fail(c, PA_ERR_RANGE, "pa_run_noalloc: latest event t = %.9g ns lies in cycle %.0f >= n_cycles %u",
+                  (double)c->t_last, (double)cyc, prm->n_cycles);
+    if ((double)c->t_last > t_max)
+      return fail(c, PA_ERR_RANGE, "pa_run_noalloc: t_max %.9g ns is earlier than the latest event %.9g ns",
+                  t_max, (double)c->t_last);
+  }
+  CUDA_TRY(c, cudaSetDevice(c->device));
+  unsigned char* base = nullptr;
+  PA_TRY(noalloc_scratch(c, c->device, &base));
+  const uint32_t N = prm->n_cycles;
+  const uint32_t G = c->n_gates;
+  const uint32_t nblk = partition_blocks(G);
+  const bool debug = out->state_pre || out->lut_ij || out->is_glitch;
+  const bool timing = (prm->flags & PA_RUN_TIMING) != 0;
+  const bool pow2 = is_pow2(T);
+  RunArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.cells = (const CellDesc*)c->cells.p;
+  a.n_cells = c->n_cells;
+  a.lut = (const float*)c->lut.p;
+  a.leak = (const float*)c->leak.p;
+  a.gates = (const GateRec*)c->gates.p;
+  a.n_gates = G;
+  a.pin_off = (const uint64_t*)c->pin_off.p;
+  a.gate_off = (const uint64_t*)c->gate_off.p;
+  a.t = (const float*)c->t.p;
+  a.s = (const float*)c->s.p;
+  a.t_clk = T;
+  a.inv_t_clk = pow2 ? 1.0f / T : 0.f;
+  a.t_max_f = (float)t_max;
+  a.half_vdd2 = (float)(0.5 * prm->vdd * prm->vdd);
+  a.n_cycles = N;
+  a.tile_target = tile;
+  a.heavy_thresh = heavy;
+  a.part_blk = (uint32_t*)(base + kNaPartBlk);
+  a.part_counts = (uint32_t*)(base + kNaPartCounts);
+  a.tiles = (Tile*)(base + kNaTiles);
+  a.heavy = (uint32_t*)(base + kNaHeavy);
+  a.p0 = (double*)(base + kNaP0Tot);
+  a.totals = (double*)(base + kNaP0Tot) + 4;
+  a.bin_w = (float*)(base + kNaBins);
+  a.bin_d = (float*)(base + kNaBins + (size_t)N * 4);
+  a.bin_ev = (uint32_t*)(base + kNaBins + (size_t)N * 8);
+  a.bin_gl = (uint32_t*)(base + kNaBins + (size_t)N * 12);
+  a.err = (unsigned long long*)c->err_word.p;
+  if (debug) {
+    a.dbg_state = out->state_pre;
+    a.dbg_lut = out->lut_ij;
+    a.dbg_glitch = out->is_glitch;
+  }
+  double* p_dev = (double*)(base + kNaPOut);
+  cudaStream_t st = c->stream;
+  uint32_t launches = 0;
+  if (timing) CUDA_TRY(c, cudaEventRecord(c->ev[0], st));
+  CUDA_TRY(c, cudaMemsetAsync(base + kNaBins, 0, (size_t)N * 16, st));
+  CUDA_TRY(c, cudaMemsetAsync(base + kNaP0Tot, 0, 8 * sizeof(double), st));
+  CUDA_TRY(c, cudaMemsetAsync(base + kNaPartCounts, 0, 4 * sizeof(uint32_t), st));
+  CUDA_TRY(c, cudaMemsetAsync(c->err_word.p, 0xff, sizeof(unsigned long long), st));
+  CUDA_TRY(c, launch_partition(a, nblk, st));
+  launches += nblk ? 3 : 0;
+  if (timing) CUDA_TRY(c, cudaEventRecord(c->ev[1], st));
+  const int grid = c->sm_count * fused_blocks_per_sm(pow2, debug);
+  CUDA_TRY(c, launch_fused(a, grid, pow2, debug, st));
+  launches += 1;
+  if (timing) CUDA_TRY(c, cudaEventRecord(c->ev[2], st));
+  CUDA_TRY(c, launch_final_reduce(a, Td, t_max, out->waveform_w, p_dev, st));
+  launches += 1;
+  if (timing) CUDA_TRY(c, cudaEventRecord(c->ev[3], st));
+  double p[4];
+  unsigned long long key = kNoErr;
+  uint32_t counts[4] = {0, 0, 0, 0};
+  CUDA_TRY(c, cudaMemcpyAsync(p, p_dev, sizeof(p), cudaMemcpyDeviceToHost, st));
+  CUDA_TRY(c, cudaMemcpyAsync(&key, c->err_word.p, sizeof(key), cudaMemcpyDeviceToHost, st));
+  CUDA_TRY(c, cudaMemcpyAsync(counts, a.part_counts, sizeof(counts), cudaMemcpyDeviceToHost, st));
+  if (out->event_count)
+    CUDA_TRY(c, cudaMemcpyAsync(out->event_count, a.bin_ev, (size_t)N * 4, cudaMemcpyDeviceToDevice, st));
+  if (out->glitch_count)
+    CUDA_TRY(c, cudaMemcpyAsync(out->glitch_count, a.bin_gl, (size_t)N * 4, cudaMemcpyDeviceToDevice, st));
+  CUDA_TRY(c, cudaStreamSynchronize(st));
+  if (key != kNoErr) return map_dev_err(c, key, "pa_run_noalloc");
+  out->p_int_w = p[0];
+  out->p_sw_w = p[1];
+  out->p_gl_w = p[2];
+  out->p_leak_w = p[3];
+  out->t_max_ns = t_max;
+  out->n_tiles = counts[0];
+  out->n_heavy = counts[1];
+  out->kernel_launches = launches;
+  if (timing) {
+    cudaEventElapsedTime(&out->ms_partition, c->ev[0], c->ev[1]);
+    cudaEventElapsedTime(&out->ms_fused, c->ev[1], c->ev[2]);
+    cudaEventElapsedTime(&out->ms_reduce, c->ev[2], c->ev[3]);
+    cudaEventElapsedTime(&out->ms_total, c->ev[0], c->ev[3]);
+  }
+  return PA_OK;
+}

@@ -227,6 +227,37 @@ int pa_load_events(pa_ctx *ctx, const pa_events *ev);
  * PA_ERR_OOM, PA_ERR_CUDA, PA_ERR_INTERNAL. */
 int pa_run(pa_ctx *ctx, const pa_run_params *params, pa_result *out);
 
+/*
+ * pa_run_noalloc -- pa_run for callers that must not allocate device memory
+ * at run time. (The paper has no counterpart: this is an integration entry
+ * point of this library.)
+ *
+ * Who needs it: code that owns the GPU's memory budget outright (a framework
+ * whose caching allocator has already reserved the device), loops that may
+ * not stall the device (cudaMalloc/cudaFree synchronise it), and processes
+ * that forbid allocation after start-up. pa_run may grow its scratch buffers
+ * on the first call or when n_cycles or the gate count grows; this entry point
+ * never does: its per-run scratch (cycle bins, work lists, totals) lives in
+ * one file-scope device array of PA_NOALLOC_SCRATCH_BYTES (5 MiB) that
+ * every GPU loading libpa.so holds until the process exits.
+ *
+ * Same arguments, computation and results as pa_run on the data loaded into
+ * ctx (loading itself still allocates; do it beforehand), with these limits:
+ *   n_cycles <= PA_NOALLOC_MAX_CYCLES, netlist gates <= PA_NOALLOC_MAX_GATES,
+ *   out->out_mem == PA_MEM_DEVICE for every non-NULL array in out.
+ * Beyond them it returns PA_ERR_ARG and says which limit was hit.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture. All calls share the one array and it keeps the last call's
+ * contents (each call clears what it needs zeroed): calls whose device work
+ * overlaps -- from several threads, contexts or streams at once -- race and
+ * must be serialised by the caller.
+ */
+#define PA_NOALLOC_MAX_CYCLES 65536u
+#define PA_NOALLOC_MAX_GATES 262144u
+#define PA_NOALLOC_SCRATCH_BYTES (5u << 20)
+int pa_run_noalloc(pa_ctx *ctx, const pa_run_params *params, pa_result *out);
+
 /* Defaults: vdd 0.9 V, t_clk 1 ns, n_cycles 1, t_max 0, partition knobs 0. */
 void pa_default_params(pa_run_params *params);
 
