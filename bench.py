@@ -57,6 +57,7 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle sample time")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--unbanded", action="store_true", help="skip pa_build_bands (unbanded kernel)")
     return ap.parse_args()
 
 
@@ -319,6 +320,8 @@ def run_ours(args):
     stream = torch.cuda.Stream(device=local)
     pa = glp.PowerAnalyzer(local, stream.cuda_stream)
     pa.load_workload(w)
+    if not args.unbanded:
+        pa.build_bands(w.t_clk_ns)
     wave = np.empty(N, np.float32)
     evc = np.empty(N, np.uint32)
     glc = np.empty(N, np.uint32)
@@ -354,20 +357,25 @@ def run_ours(args):
     # ---- end to end through the public API, host buffers
     h2d = 8 * (w.n_pins + 1) + 4 * E + 4 * E + E
     d2h = 4 * N + 4 * N + 4 * N + 4 * 8
-    for _ in range(2):
-        pa.load_events(w.pin_off, w.t_ns, w.slew_ps, w.value)
-        step()
-    dist.barrier()
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(args.e2e_steps):
-        pa.load_events(w.pin_off, w.t_ns, w.slew_ps, w.value)
-        step()
-    torch.cuda.synchronize()
-    e2e_s = dist.max(time.perf_counter() - t0)
+    e2e_value = None
+    if args.e2e_steps > 0:
+        def e2e_step():
+            pa.load_events(w.pin_off, w.t_ns, w.slew_ps, w.value)
+            if not args.unbanded:
+                pa.build_bands(w.t_clk_ns)
+            step()
+        for _ in range(2):
+            e2e_step()
+        dist.barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        torch.cuda.synchronize()
+        e2e_s = dist.max(time.perf_counter() - t0)
+        e2e_value = world * E * args.e2e_steps / e2e_s
     clk.active = False
     clk.stop()
-    e2e_value = world * E * args.e2e_steps / e2e_s
     # ---- roofline of the fused kernel
     fused_mean = statistics.mean(fused_ms)
     B = algorithmic_bytes(w)
@@ -386,19 +394,22 @@ def run_ours(args):
             "gate_cycles_per_s": world * G * N * args.steps / (el_ms * 1e-3),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
-                         "kernel": "k_fused (fused dynamic + leakage power)",
+                         "kernel": ("k_banded" if r["path"] == glp.PA_PATH_BANDED else "k_fused")
+                         + " (fused dynamic + leakage power)",
                          "algorithmic_bytes_per_launch": B, "mean_launch_ms": fused_mean,
                          "peak_source": f"{peak_kind} HBM copy bandwidth"},
             "cpu_baseline": cpu,
-            "e2e": {"value": e2e_value, "unit": "events/s", "h2d_bytes_per_step": h2d,
+            "e2e": None if e2e_value is None else {"value": e2e_value, "unit": "events/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
                     "note": "per step: pa_load_events from pinned host memory (device-side validation) + "
-                            "pa_run + waveform/count copy to host; library and netlist loaded once"},
+                            "pa_build_bands + pa_run + waveform/count copy to host; library and netlist "
+                            "loaded once"},
             "clocks": clk.summary(),
             "gpu_launches": launches,
             "gen_seconds": gen_s,
             "p_total_w": r["p_int"] + r["p_sw"] + r["p_gl"] + r["p_leak"],
             "n_tiles": r["n_tiles"], "n_heavy": r["n_heavy"],
+            "path": "banded" if r["path"] == glp.PA_PATH_BANDED else "unbanded",
         }
         print(json.dumps(line), flush=True)
     pa.close()

@@ -58,7 +58,8 @@ class PaResult(ctypes.Structure):
                 ("waveform_w", _vp), ("event_count", _vp), ("glitch_count", _vp), ("state_pre", _vp),
                 ("lut_ij", _vp), ("is_glitch", _vp), ("ms_partition", ctypes.c_float),
                 ("ms_fused", ctypes.c_float), ("ms_reduce", ctypes.c_float), ("ms_total", ctypes.c_float),
-                ("n_tiles", ctypes.c_uint32), ("n_heavy", ctypes.c_uint32), ("kernel_launches", ctypes.c_uint32)]
+                ("n_tiles", ctypes.c_uint32), ("n_heavy", ctypes.c_uint32), ("kernel_launches", ctypes.c_uint32),
+                ("path", ctypes.c_uint32)]
 
 
 class PaError(RuntimeError):
@@ -68,7 +69,8 @@ class PaError(RuntimeError):
 
 
 EXPORTS = ("pa_create", "pa_destroy", "pa_load_library", "pa_load_netlist", "pa_load_events", "pa_run",
-           "pa_run_noalloc", "pa_default_params", "pa_last_error", "pa_version")
+           "pa_run_noalloc", "pa_build_bands", "pa_default_params", "pa_last_error", "pa_version")
+PA_PATH_UNBANDED, PA_PATH_BANDED = 0, 1
 PA_NOALLOC_MAX_CYCLES = 65536
 PA_NOALLOC_MAX_GATES = 262144
 
@@ -94,6 +96,7 @@ def load_library():
         L.pa_load_events.argtypes = [_vp, ctypes.POINTER(PaEvents)]
         L.pa_run.argtypes = [_vp, ctypes.POINTER(PaRunParams), ctypes.POINTER(PaResult)]
         L.pa_run_noalloc.argtypes = [_vp, ctypes.POINTER(PaRunParams), ctypes.POINTER(PaResult)]
+        L.pa_build_bands.argtypes = [_vp, ctypes.c_float, ctypes.c_uint32]
         L.pa_default_params.argtypes = [ctypes.POINTER(PaRunParams)]
         L.pa_default_params.restype = None
         L.pa_last_error.argtypes = [_vp]
@@ -144,6 +147,10 @@ def pa_run_noalloc(ctx: int, params: PaRunParams, result: PaResult) -> None:
     array; device output arrays only; limits PA_NOALLOC_MAX_CYCLES and
     PA_NOALLOC_MAX_GATES). For callers that may not allocate at run time."""
     _check(ctx, load_library().pa_run_noalloc(ctx, ctypes.byref(params), ctypes.byref(result)))
+
+
+def pa_build_bands(ctx: int, t_clk_ns: float, band_cycles: int = 0) -> None:
+    _check(ctx, load_library().pa_build_bands(ctx, float(t_clk_ns), int(band_cycles)))
 
 
 def pa_default_params() -> PaRunParams:
@@ -234,6 +241,10 @@ class PowerAnalyzer:
         pa_load_events(self.ctx, ev)
         self.n_events = n_ev
 
+    def build_bands(self, t_clk_ns, band_cycles: int = 0):
+        """Regroup the loaded events by clock bands for runs at this clock."""
+        pa_build_bands(self.ctx, t_clk_ns, band_cycles)
+
     def load_workload(self, w, with_value: bool = True):
         self.load_library(w.n_inputs, w.n_slew, w.n_load, w.slew_axis, w.load_axis, w.lut_off, w.lut,
                           w.leak_off, w.leak)
@@ -273,7 +284,7 @@ class PowerAnalyzer:
         r.is_glitch = arr("is_glitch", self.n_events, np.uint8, debug)
         pa_run(self.ctx, p, r)
         res.update(p_int=r.p_int_w, p_sw=r.p_sw_w, p_gl=r.p_gl_w, p_leak=r.p_leak_w, t_max=r.t_max_ns,
-                   n_tiles=r.n_tiles, n_heavy=r.n_heavy, kernel_launches=r.kernel_launches)
+                   n_tiles=r.n_tiles, n_heavy=r.n_heavy, kernel_launches=r.kernel_launches, path=r.path)
         if timing:
             res.update(ms_partition=r.ms_partition, ms_fused=r.ms_fused, ms_reduce=r.ms_reduce,
                        ms_total=r.ms_total)

@@ -56,7 +56,13 @@ struct pa_ctx {
   // scratch
   DevBuf value_tmp, err_word, tmax_bits;
   DevBuf bins, part_blk, part_counts, tiles, heavy, p0_tot, p_out;
-  DevBuf dbg[3], wave_tmp, cnt_tmp;
+  DevBuf dbg[3], wave_tmp, cnt_tmp, chunk_sums;
+
+  // banded layout (pa_build_bands) and its per-run scratch
+  BandLayout band;
+  DevBuf b_bt, b_bs, b_lrec, b_hrec, b_lblk, b_lgate, b_hgate;
+  DevBuf b_cnt, b_heavy, b_rank, b_totals, b_scan, b_usize, b_uoff;
+  DevBuf b_grun, b_items, b_item_n, b_item_ev, b_flags, b_pos;
   DevBuf scratch_small;
 };
 
@@ -116,6 +122,7 @@ bool is_finite_f(float x) { return std::isfinite(x); }
 void drop_events(pa_ctx* c) {
   c->has_ev = false;
   c->n_events = 0;
+  c->band.built = false;
 }
 
 void drop_netlist(pa_ctx* c) {
@@ -159,6 +166,275 @@ bool is_pow2(float x) {
   int e;
   const float m = std::frexp(x, &e);
   return x > 0.f && m == 0.5f;
+}
+
+// Validated parameters of one run.
+struct RunPlan {
+  float T = 0.f;
+  double Td = 0.0, t_max = 0.0;
+  uint32_t tile = 0, heavy = 0, N = 0, G = 0, nblk = 0;
+  bool pow2 = false, debug = false, timing = false;
+  double vdd = 0.0;
+};
+
+// Device buffers of one run (owned by the ctx or by the no-alloc scratch).
+struct PassBufs {
+  float4* bins = nullptr;
+  uint32_t* part_blk = nullptr;
+  uint32_t* part_counts = nullptr;
+  Tile* tiles = nullptr;
+  uint32_t* heavy = nullptr;
+  double* p0_tot = nullptr;
+  double* p_out = nullptr;
+  double* chunk_sums = nullptr;
+  float* wave = nullptr;
+  uint32_t* cnt_ev = nullptr;
+  uint32_t* cnt_gl = nullptr;
+  uint8_t* dbg[3] = {nullptr, nullptr, nullptr};
+};
+
+int check_run(pa_ctx* c, const pa_run_params* prm, const pa_result* out, const char* who, RunPlan* plan) {
+  if (!c) return PA_ERR_ARG;
+  if (!c->has_ev) return fail(c, PA_ERR_ORDER, "%s: events not loaded", who);
+  if (!prm || !out) return fail(c, PA_ERR_ARG, "%s: null params or result", who);
+  if (!(prm->t_clk_ns > 0.f) || !is_finite_f(prm->t_clk_ns)) return fail(c, PA_ERR_ARG, "%s: t_clk_ns must be > 0", who);
+  if (prm->n_cycles == 0) return fail(c, PA_ERR_ARG, "%s: n_cycles must be > 0", who);
+  if (!std::isfinite(prm->vdd)) return fail(c, PA_ERR_ARG, "%s: vdd not finite", who);
+  if (out->out_mem != PA_MEM_HOST && out->out_mem != PA_MEM_DEVICE) return fail(c, PA_ERR_ARG, "%s: bad out_mem", who);
+  plan->tile = prm->tile_events ? prm->tile_events : kDefaultTile;
+  plan->heavy = prm->heavy_events ? prm->heavy_events : kDefaultHeavy;
+  if ((uint64_t)plan->tile + plan->heavy > (uint64_t)kTileCap)
+    return fail(c, PA_ERR_ARG, "%s: tile_events + heavy_events = %u exceeds %d", who, plan->tile + plan->heavy, kTileCap);
+  plan->T = prm->t_clk_ns;
+  plan->Td = (double)plan->T;
+  plan->t_max = prm->t_max_ns > 0 ? prm->t_max_ns : (double)prm->n_cycles * plan->Td;
+  if (!std::isfinite(plan->t_max)) return fail(c, PA_ERR_ARG, "%s: t_max not finite", who);
+  if (c->n_events) {
+    const float cyc = std::floor(c->t_last / plan->T);  // fp32 division, as the kernels take it
+    if (!(cyc < (float)prm->n_cycles))
+      return fail(c, PA_ERR_RANGE, "%s: latest event t = %.9g ns lies in cycle %.0f >= n_cycles %u", who,
+                  (double)c->t_last, (double)cyc, prm->n_cycles);
+    if ((double)c->t_last > plan->t_max)
+      return fail(c, PA_ERR_RANGE, "%s: t_max %.9g ns is earlier than the latest event %.9g ns", who, plan->t_max,
+                  (double)c->t_last);
+  }
+  plan->N = prm->n_cycles;
+  plan->G = c->n_gates;
+  plan->nblk = partition_blocks(plan->G);
+  plan->debug = out->state_pre || out->lut_ij || out->is_glitch;
+  plan->timing = (prm->flags & PA_RUN_TIMING) != 0;
+  plan->pow2 = is_pow2(plan->T);
+  plan->vdd = prm->vdd;
+  return PA_OK;
+}
+
+// Launch partition -> fused kernel -> final reduction; counts are taken in
+// f32 inside the one-per-event vector reduction and the pass is repeated with
+// integer counts if a cycle reached 2^24 events. Copies outputs on success.
+int run_pass(pa_ctx* c, const RunPlan& plan, const PassBufs& B, pa_result* out, const char* who) {
+  const uint32_t N = plan.N;
+  RunArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.cells = (const CellDesc*)c->cells.p;
+  a.n_cells = c->n_cells;
+  a.lut = (const float*)c->lut.p;
+  a.leak = (const float*)c->leak.p;
+  a.gates = (const GateRec*)c->gates.p;
+  a.n_gates = plan.G;
+  a.pin_off = (const uint64_t*)c->pin_off.p;
+  a.gate_off = (const uint64_t*)c->gate_off.p;
+  a.t = (const float*)c->t.p;
+  a.s = (const float*)c->s.p;
+  a.t_clk = plan.T;
+  a.inv_t_clk = plan.pow2 ? 1.0f / plan.T : 0.f;
+  a.t_max_f = (float)plan.t_max;
+  a.half_vdd2 = (float)(0.5 * plan.vdd * plan.vdd);
+  a.n_cycles = N;
+  a.tile_target = plan.tile;
+  a.heavy_thresh = plan.heavy;
+  a.part_blk = B.part_blk;
+  a.part_counts = B.part_counts;
+  a.tiles = B.tiles;
+  a.heavy = B.heavy;
+  a.p0 = B.p0_tot;
+  a.totals = B.p0_tot + 4;
+  a.bins = B.bins;
+  a.cnt_ev = B.cnt_ev;
+  a.cnt_gl = B.cnt_gl;
+  a.chunk_sums = B.chunk_sums;
+  a.err = (unsigned long long*)c->err_word.p;
+  a.dbg_state = B.dbg[0];
+  a.dbg_lut = B.dbg[1];
+  a.dbg_glitch = B.dbg[2];
+  cudaStream_t st = c->stream;
+  uint32_t launches = 0;
+  double p[4];
+  unsigned long long key = kNoErr;
+  uint32_t counts[4] = {0, 0, 0, 0};
+  for (int exact = 0; exact < 2; ++exact) {
+    if (plan.timing) CUDA_TRY(c, cudaEventRecord(c->ev[0], st));
+    CUDA_TRY(c, cudaMemsetAsync(B.bins, 0, (size_t)N * sizeof(float4), st));
+    if (exact) CUDA_TRY(c, cudaMemsetAsync(B.cnt_ev, 0, (size_t)N * sizeof(uint32_t), st));
+    if (exact) CUDA_TRY(c, cudaMemsetAsync(B.cnt_gl, 0, (size_t)N * sizeof(uint32_t), st));
+    CUDA_TRY(c, cudaMemsetAsync(B.p0_tot, 0, 8 * sizeof(double), st));
+    CUDA_TRY(c, cudaMemsetAsync(B.part_counts, 0, 4 * sizeof(uint32_t), st));
+    CUDA_TRY(c, cudaMemsetAsync(c->err_word.p, 0xff, sizeof(unsigned long long), st));
+    CUDA_TRY(c, launch_partition(a, plan.nblk, st));
+    launches += plan.nblk ? 3 : 0;
+    if (plan.timing) CUDA_TRY(c, cudaEventRecord(c->ev[1], st));
+    const int grid = c->sm_count * fused_blocks_per_sm(plan.pow2, plan.debug, exact != 0);
+    CUDA_TRY(c, launch_fused(a, grid, plan.pow2, plan.debug, exact != 0, st));
+    launches += 1;
+    if (plan.timing) CUDA_TRY(c, cudaEventRecord(c->ev[2], st));
+    CUDA_TRY(c, launch_final_reduce(a, plan.Td, plan.t_max, B.wave, B.p_out, exact != 0, st));
+    launches += 2;
+    if (plan.timing) CUDA_TRY(c, cudaEventRecord(c->ev[3], st));
+    CUDA_TRY(c, cudaMemcpyAsync(p, B.p_out, sizeof(p), cudaMemcpyDeviceToHost, st));
+    CUDA_TRY(c, cudaMemcpyAsync(&key, c->err_word.p, sizeof(key), cudaMemcpyDeviceToHost, st));
+    CUDA_TRY(c, cudaMemcpyAsync(counts, B.part_counts, sizeof(counts), cudaMemcpyDeviceToHost, st));
+    CUDA_TRY(c, cudaStreamSynchronize(st));
+    if (key == kNoErr) break;
+    if ((key & 0xff) != kErrCountOverflow || exact) return map_dev_err(c, key, who);
+  }
+  const cudaMemcpyKind dk = out->out_mem == PA_MEM_HOST ? cudaMemcpyDeviceToHost : cudaMemcpyDeviceToDevice;
+  if (out->waveform_w) CUDA_TRY(c, cudaMemcpyAsync(out->waveform_w, B.wave, (size_t)N * sizeof(float), dk, st));
+  if (out->event_count) CUDA_TRY(c, cudaMemcpyAsync(out->event_count, B.cnt_ev, (size_t)N * 4, dk, st));
+  if (out->glitch_count) CUDA_TRY(c, cudaMemcpyAsync(out->glitch_count, B.cnt_gl, (size_t)N * 4, dk, st));
+  if (plan.debug && c->n_events) {
+    uint8_t* dst[3] = {out->state_pre, out->lut_ij, out->is_glitch};
+    for (int i = 0; i < 3; ++i)
+      if (dst[i] && dst[i] != B.dbg[i]) CUDA_TRY(c, cudaMemcpyAsync(dst[i], B.dbg[i], c->n_events, dk, st));
+  }
+  CUDA_TRY(c, cudaStreamSynchronize(st));
+  out->p_int_w = p[0];
+  out->p_sw_w = p[1];
+  out->p_gl_w = p[2];
+  out->p_leak_w = p[3];
+  out->t_max_ns = plan.t_max;
+  out->n_tiles = counts[0];
+  out->n_heavy = counts[1];
+  out->kernel_launches = launches;
+  out->path = PA_PATH_UNBANDED;
+  if (plan.timing) {
+    cudaEventElapsedTime(&out->ms_partition, c->ev[0], c->ev[1]);
+    cudaEventElapsedTime(&out->ms_fused, c->ev[1], c->ev[2]);
+    cudaEventElapsedTime(&out->ms_reduce, c->ev[2], c->ev[3]);
+    cudaEventElapsedTime(&out->ms_total, c->ev[0], c->ev[3]);
+  }
+  return PA_OK;
+}
+
+
+bool same_bits(float a, float b) { return std::memcmp(&a, &b, sizeof(float)) == 0; }
+
+// The banded pass: per-run gate records (and P0), item list, banded fused
+// kernel, final reduction of the fp64 / u32 bins. Copies outputs on success.
+int run_banded(pa_ctx* c, const RunPlan& plan, pa_result* out) {
+  const uint32_t N = plan.N, G = plan.G;
+  const BandLayout& L = c->band;
+  const uint32_t max_items = band_max_items(L);
+  PA_TRY(dreserve(c, c->bins, (size_t)N * 16));
+  PA_TRY(dreserve(c, c->cnt_tmp, (size_t)N * 2 * sizeof(uint32_t)));
+  PA_TRY(dreserve(c, c->chunk_sums, (size_t)reduce_chunks(N) * sizeof(double)));
+  PA_TRY(dreserve(c, c->p0_tot, 8 * sizeof(double)));
+  PA_TRY(dreserve(c, c->p_out, 4 * sizeof(double)));
+  PA_TRY(dreserve(c, c->wave_tmp, (size_t)N * sizeof(float)));
+  PA_TRY(dreserve(c, c->b_grun, ((size_t)L.n_light + L.n_heavy + 1) * sizeof(GateRun)));
+  PA_TRY(dreserve(c, c->b_items, (size_t)max_items * sizeof(BandItem)));
+  PA_TRY(dreserve(c, c->b_item_n, (size_t)max_items * sizeof(uint32_t)));
+  PA_TRY(dreserve(c, c->b_item_ev, ((size_t)max_items + 1) * sizeof(uint64_t)));
+  PA_TRY(dreserve(c, c->b_flags, (size_t)max_items * sizeof(uint32_t)));
+  PA_TRY(dreserve(c, c->b_pos, ((size_t)max_items + 1) * sizeof(uint64_t)));
+  PA_TRY(dreserve(c, c->b_scan, ((size_t)band_scan_blocks(std::max<uint64_t>(max_items, G)) + 1) * sizeof(uint64_t)));
+  if (plan.debug)
+    for (int i = 0; i < 3; ++i) PA_TRY(dreserve(c, c->dbg[i], c->n_events));
+  BandRunArgs A;
+  std::memset(&A, 0, sizeof(A));
+  RunArgs& a = A.r;
+  a.cells = (const CellDesc*)c->cells.p;
+  a.n_cells = c->n_cells;
+  a.lut = (const float*)c->lut.p;
+  a.leak = (const float*)c->leak.p;
+  a.gates = (const GateRec*)c->gates.p;
+  a.n_gates = G;
+  a.pin_off = (const uint64_t*)c->pin_off.p;
+  a.gate_off = (const uint64_t*)c->gate_off.p;
+  a.t = (const float*)c->t.p;
+  a.s = (const float*)c->s.p;
+  a.t_clk = plan.T;
+  a.inv_t_clk = plan.pow2 ? 1.0f / plan.T : 0.f;
+  a.t_max_f = (float)plan.t_max;
+  a.half_vdd2 = (float)(0.5 * plan.vdd * plan.vdd);
+  a.n_cycles = N;
+  a.p0 = (double*)c->p0_tot.p;
+  a.totals = (double*)c->p0_tot.p + 4;
+  a.bins = (float4*)c->bins.p;
+  a.cnt_ev = (uint32_t*)c->cnt_tmp.p;
+  a.cnt_gl = (uint32_t*)c->cnt_tmp.p + N;
+  a.chunk_sums = (double*)c->chunk_sums.p;
+  a.err = (unsigned long long*)c->err_word.p;
+  if (plan.debug) {
+    a.dbg_state = (uint8_t*)c->dbg[0].p;
+    a.dbg_lut = (uint8_t*)c->dbg[1].p;
+    a.dbg_glitch = (uint8_t*)c->dbg[2].p;
+  }
+  A.L = L;
+  A.grun_l = (GateRun*)c->b_grun.p;
+  A.grun_h = (GateRun*)c->b_grun.p + L.n_light;
+  A.items = (BandItem*)c->b_items.p;
+  A.item_ev = (uint64_t*)c->b_item_ev.p;
+  A.max_items = max_items;
+  cudaStream_t st = c->stream;
+  if (plan.timing) CUDA_TRY(c, cudaEventRecord(c->ev[0], st));
+  CUDA_TRY(c, cudaMemsetAsync(c->bins.p, 0, (size_t)N * 16, st));
+  CUDA_TRY(c, cudaMemsetAsync(c->cnt_tmp.p, 0, (size_t)N * 2 * sizeof(uint32_t), st));
+  CUDA_TRY(c, cudaMemsetAsync(c->p0_tot.p, 0, 8 * sizeof(double), st));
+  CUDA_TRY(c, cudaMemsetAsync(c->err_word.p, 0xff, sizeof(unsigned long long), st));
+  CUDA_TRY(c, band_gate_run(A, st));
+  uint32_t items[2] = {0, 0};
+  CUDA_TRY(c, band_partition(A, (uint32_t*)c->b_flags.p, (uint64_t*)c->b_pos.p, (uint64_t*)c->b_scan.p,
+                             (uint32_t*)c->b_item_n.p, items, st));
+  const uint32_t n_items = items[0] + items[1];
+  uint32_t launches = 1 + (L.n_lblk ? 5 : 0) + (L.n_heavy ? 5 : 0) + 3;
+  if (plan.timing) CUDA_TRY(c, cudaEventRecord(c->ev[1], st));
+  CUDA_TRY(c, band_fused(A, n_items, c->sm_count, plan.debug, st));
+  launches += n_items ? 1 : 0;
+  if (plan.timing) CUDA_TRY(c, cudaEventRecord(c->ev[2], st));
+  CUDA_TRY(c, launch_final_reduce(a, plan.Td, plan.t_max, (float*)c->wave_tmp.p, (double*)c->p_out.p, true, st));
+  launches += 2;
+  if (plan.timing) CUDA_TRY(c, cudaEventRecord(c->ev[3], st));
+  double p[4];
+  unsigned long long key = kNoErr;
+  CUDA_TRY(c, cudaMemcpyAsync(p, c->p_out.p, sizeof(p), cudaMemcpyDeviceToHost, st));
+  CUDA_TRY(c, cudaMemcpyAsync(&key, c->err_word.p, sizeof(key), cudaMemcpyDeviceToHost, st));
+  CUDA_TRY(c, cudaStreamSynchronize(st));
+  if (key != kNoErr) return map_dev_err(c, key, "pa_run");
+  const cudaMemcpyKind dk = out->out_mem == PA_MEM_HOST ? cudaMemcpyDeviceToHost : cudaMemcpyDeviceToDevice;
+  if (out->waveform_w) CUDA_TRY(c, cudaMemcpyAsync(out->waveform_w, c->wave_tmp.p, (size_t)N * sizeof(float), dk, st));
+  if (out->event_count) CUDA_TRY(c, cudaMemcpyAsync(out->event_count, a.cnt_ev, (size_t)N * 4, dk, st));
+  if (out->glitch_count) CUDA_TRY(c, cudaMemcpyAsync(out->glitch_count, a.cnt_gl, (size_t)N * 4, dk, st));
+  if (plan.debug && c->n_events) {
+    uint8_t* dst[3] = {out->state_pre, out->lut_ij, out->is_glitch};
+    for (int i = 0; i < 3; ++i)
+      if (dst[i]) CUDA_TRY(c, cudaMemcpyAsync(dst[i], c->dbg[i].p, c->n_events, dk, st));
+  }
+  CUDA_TRY(c, cudaStreamSynchronize(st));
+  out->p_int_w = p[0];
+  out->p_sw_w = p[1];
+  out->p_gl_w = p[2];
+  out->p_leak_w = p[3];
+  out->t_max_ns = plan.t_max;
+  out->n_tiles = items[0];
+  out->n_heavy = items[1];
+  out->kernel_launches = launches;
+  out->path = PA_PATH_BANDED;
+  if (plan.timing) {
+    cudaEventElapsedTime(&out->ms_partition, c->ev[0], c->ev[1]);
+    cudaEventElapsedTime(&out->ms_fused, c->ev[1], c->ev[2]);
+    cudaEventElapsedTime(&out->ms_reduce, c->ev[2], c->ev[3]);
+    cudaEventElapsedTime(&out->ms_total, c->ev[0], c->ev[3]);
+  }
+  return PA_OK;
 }
 
 }  // namespace
@@ -224,7 +500,11 @@ void pa_destroy(pa_ctx* c) {
   DevBuf* all[] = {&c->cells, &c->lut, &c->leak, &c->gates, &c->pin_off, &c->gate_off, &c->t, &c->s,
                    &c->value_tmp, &c->err_word, &c->tmax_bits, &c->bins, &c->part_blk,
                    &c->part_counts, &c->tiles, &c->heavy, &c->p0_tot, &c->p_out, &c->dbg[0],
-                   &c->dbg[1], &c->dbg[2], &c->wave_tmp, &c->cnt_tmp, &c->scratch_small};
+                   &c->dbg[1], &c->dbg[2], &c->wave_tmp, &c->cnt_tmp, &c->scratch_small,
+                   &c->chunk_sums, &c->b_bt, &c->b_bs, &c->b_lrec, &c->b_hrec, &c->b_lblk,
+                   &c->b_lgate, &c->b_hgate, &c->b_cnt, &c->b_heavy, &c->b_rank, &c->b_totals,
+                   &c->b_scan, &c->b_usize, &c->b_uoff, &c->b_grun, &c->b_items, &c->b_item_n,
+                   &c->b_item_ev, &c->b_flags, &c->b_pos};
   for (DevBuf* b : all) dfree(*b);
   for (auto& e : c->ev)
     if (e) cudaEventDestroy(e);
@@ -397,145 +677,38 @@ int pa_load_events(pa_ctx* c, const pa_events* ev) {
 }
 
 int pa_run(pa_ctx* c, const pa_run_params* prm, pa_result* out) {
-  if (!c) return PA_ERR_ARG;
-  if (!c->has_ev) return fail(c, PA_ERR_ORDER, "pa_run: events not loaded");
-  if (!prm || !out) return fail(c, PA_ERR_ARG, "pa_run: null params or result");
-  if (!(prm->t_clk_ns > 0.f) || !is_finite_f(prm->t_clk_ns)) return fail(c, PA_ERR_ARG, "pa_run: t_clk_ns must be > 0");
-  if (prm->n_cycles == 0) return fail(c, PA_ERR_ARG, "pa_run: n_cycles must be > 0");
-  if (!std::isfinite(prm->vdd)) return fail(c, PA_ERR_ARG, "pa_run: vdd not finite");
-  if (out->out_mem != PA_MEM_HOST && out->out_mem != PA_MEM_DEVICE) return fail(c, PA_ERR_ARG, "pa_run: bad out_mem");
-  const uint32_t tile = prm->tile_events ? prm->tile_events : kDefaultTile;
-  const uint32_t heavy = prm->heavy_events ? prm->heavy_events : kDefaultHeavy;
-  if ((uint64_t)tile + heavy > (uint64_t)kTileCap)
-    return fail(c, PA_ERR_ARG, "pa_run: tile_events + heavy_events = %u exceeds %d", tile + heavy, kTileCap);
-  const float T = prm->t_clk_ns;
-  const double Td = (double)T;
-  const double t_max = prm->t_max_ns > 0 ? prm->t_max_ns : (double)prm->n_cycles * Td;
-  if (!std::isfinite(t_max)) return fail(c, PA_ERR_ARG, "pa_run: t_max not finite");
-  if (c->n_events) {
-    const float cyc = std::floor(c->t_last / T);  // fp32 division, as the kernels take it
-    if (!(cyc < (float)prm->n_cycles))
-      return fail(c, PA_ERR_RANGE, "pa_run: latest event t = %.9g ns lies in cycle %.0f >= n_cycles %u",
-                  (double)c->t_last, (double)cyc, prm->n_cycles);
-    if ((double)c->t_last > t_max)
-      return fail(c, PA_ERR_RANGE, "pa_run: t_max %.9g ns is earlier than the latest event %.9g ns", t_max,
-                  (double)c->t_last);
-  }
-  cudaSetDevice(c->device);
-  const uint32_t N = prm->n_cycles;
-  const uint32_t G = c->n_gates;
-  const uint32_t nblk = partition_blocks(G);
-  const bool debug = out->state_pre || out->lut_ij || out->is_glitch;
-  const bool timing = (prm->flags & PA_RUN_TIMING) != 0;
-  const bool pow2 = is_pow2(T);
-
-  // scratch: bins [W f32 | D f32 | ev u32 | gl u32] x N
-  PA_TRY(dreserve(c, c->bins, (size_t)N * 16));
-  PA_TRY(dreserve(c, c->part_blk, (size_t)(nblk + 1) * 2 * sizeof(uint32_t)));
+  RunPlan plan;
+  PA_TRY(check_run(c, prm, out, "pa_run", &plan));
+  CUDA_TRY(c, cudaSetDevice(c->device));
+  if (c->band.built && same_bits(c->band.t_clk, plan.T)) return run_banded(c, plan, out);
+  const uint32_t N = plan.N, G = plan.G;
+  PassBufs B;
+  PA_TRY(dreserve(c, c->bins, (size_t)N * sizeof(float4)));
+  PA_TRY(dreserve(c, c->part_blk, (size_t)(plan.nblk + 1) * 2 * sizeof(uint32_t)));
   PA_TRY(dreserve(c, c->part_counts, 4 * sizeof(uint32_t)));
   PA_TRY(dreserve(c, c->tiles, ((size_t)G + 1) * sizeof(Tile)));
   PA_TRY(dreserve(c, c->heavy, ((size_t)G + 1) * sizeof(uint32_t)));
   PA_TRY(dreserve(c, c->p0_tot, 8 * sizeof(double)));
   PA_TRY(dreserve(c, c->p_out, 4 * sizeof(double)));
-  if (debug) {
+  PA_TRY(dreserve(c, c->chunk_sums, (size_t)reduce_chunks(N) * sizeof(double)));
+  PA_TRY(dreserve(c, c->wave_tmp, (size_t)N * sizeof(float)));
+  PA_TRY(dreserve(c, c->cnt_tmp, (size_t)N * 2 * sizeof(uint32_t)));
+  if (plan.debug) {
     for (int i = 0; i < 3; ++i) PA_TRY(dreserve(c, c->dbg[i], c->n_events));
   }
-  float* wave_dev = nullptr;
-  if (out->waveform_w) {
-    if (out->out_mem == PA_MEM_DEVICE) {
-      wave_dev = out->waveform_w;
-    } else {
-      PA_TRY(dreserve(c, c->wave_tmp, (size_t)N * sizeof(float)));
-      wave_dev = (float*)c->wave_tmp.p;
-    }
-  }
-  uint8_t* bins = (uint8_t*)c->bins.p;
-  RunArgs a;
-  std::memset(&a, 0, sizeof(a));
-  a.cells = (const CellDesc*)c->cells.p;
-  a.n_cells = c->n_cells;
-  a.lut = (const float*)c->lut.p;
-  a.leak = (const float*)c->leak.p;
-  a.gates = (const GateRec*)c->gates.p;
-  a.n_gates = G;
-  a.pin_off = (const uint64_t*)c->pin_off.p;
-  a.gate_off = (const uint64_t*)c->gate_off.p;
-  a.t = (const float*)c->t.p;
-  a.s = (const float*)c->s.p;
-  a.t_clk = T;
-  a.inv_t_clk = pow2 ? 1.0f / T : 0.f;
-  a.t_max_f = (float)t_max;
-  a.half_vdd2 = (float)(0.5 * prm->vdd * prm->vdd);
-  a.n_cycles = N;
-  a.tile_target = tile;
-  a.heavy_thresh = heavy;
-  a.part_blk = (uint32_t*)c->part_blk.p;
-  a.part_counts = (uint32_t*)c->part_counts.p;
-  a.tiles = (Tile*)c->tiles.p;
-  a.heavy = (uint32_t*)c->heavy.p;
-  a.p0 = (double*)c->p0_tot.p;
-  a.totals = (double*)c->p0_tot.p + 4;
-  a.bin_w = (float*)bins;
-  a.bin_d = (float*)(bins + (size_t)N * 4);
-  a.bin_ev = (uint32_t*)(bins + (size_t)N * 8);
-  a.bin_gl = (uint32_t*)(bins + (size_t)N * 12);
-  a.err = (unsigned long long*)c->err_word.p;
-  if (debug) {
-    a.dbg_state = (uint8_t*)c->dbg[0].p;
-    a.dbg_lut = (uint8_t*)c->dbg[1].p;
-    a.dbg_glitch = (uint8_t*)c->dbg[2].p;
-  }
-  cudaStream_t st = c->stream;
-  uint32_t launches = 0;
-  if (timing) CUDA_TRY(c, cudaEventRecord(c->ev[0], st));
-  CUDA_TRY(c, cudaMemsetAsync(c->bins.p, 0, (size_t)N * 16, st));
-  CUDA_TRY(c, cudaMemsetAsync(c->p0_tot.p, 0, 8 * sizeof(double), st));
-  CUDA_TRY(c, cudaMemsetAsync(c->part_counts.p, 0, 4 * sizeof(uint32_t), st));
-  CUDA_TRY(c, cudaMemsetAsync(c->err_word.p, 0xff, sizeof(unsigned long long), st));
-  CUDA_TRY(c, launch_partition(a, nblk, st));
-  launches += nblk ? 3 : 0;
-  if (timing) CUDA_TRY(c, cudaEventRecord(c->ev[1], st));
-  const int grid = c->sm_count * fused_blocks_per_sm(pow2, debug);
-  CUDA_TRY(c, launch_fused(a, grid, pow2, debug, st));
-  launches += 1;
-  if (timing) CUDA_TRY(c, cudaEventRecord(c->ev[2], st));
-  CUDA_TRY(c, launch_final_reduce(a, Td, t_max, wave_dev, (double*)c->p_out.p, st));
-  launches += 1;
-  if (timing) CUDA_TRY(c, cudaEventRecord(c->ev[3], st));
-  // outputs
-  double p[4];
-  unsigned long long key = kNoErr;
-  uint32_t counts[4] = {0, 0, 0, 0};
-  CUDA_TRY(c, cudaMemcpyAsync(p, c->p_out.p, sizeof(p), cudaMemcpyDeviceToHost, st));
-  CUDA_TRY(c, cudaMemcpyAsync(&key, c->err_word.p, sizeof(key), cudaMemcpyDeviceToHost, st));
-  CUDA_TRY(c, cudaMemcpyAsync(counts, c->part_counts.p, sizeof(counts), cudaMemcpyDeviceToHost, st));
-  const cudaMemcpyKind dk = out->out_mem == PA_MEM_HOST ? cudaMemcpyDeviceToHost : cudaMemcpyDeviceToDevice;
-  if (out->waveform_w && out->out_mem == PA_MEM_HOST)
-    CUDA_TRY(c, cudaMemcpyAsync(out->waveform_w, wave_dev, (size_t)N * sizeof(float), dk, st));
-  if (out->event_count) CUDA_TRY(c, cudaMemcpyAsync(out->event_count, a.bin_ev, (size_t)N * 4, dk, st));
-  if (out->glitch_count) CUDA_TRY(c, cudaMemcpyAsync(out->glitch_count, a.bin_gl, (size_t)N * 4, dk, st));
-  if (debug && c->n_events) {
-    if (out->state_pre) CUDA_TRY(c, cudaMemcpyAsync(out->state_pre, c->dbg[0].p, c->n_events, dk, st));
-    if (out->lut_ij) CUDA_TRY(c, cudaMemcpyAsync(out->lut_ij, c->dbg[1].p, c->n_events, dk, st));
-    if (out->is_glitch) CUDA_TRY(c, cudaMemcpyAsync(out->is_glitch, c->dbg[2].p, c->n_events, dk, st));
-  }
-  CUDA_TRY(c, cudaStreamSynchronize(st));
-  if (key != kNoErr) return map_dev_err(c, key, "pa_run");
-  out->p_int_w = p[0];
-  out->p_sw_w = p[1];
-  out->p_gl_w = p[2];
-  out->p_leak_w = p[3];
-  out->t_max_ns = t_max;
-  out->n_tiles = counts[0];
-  out->n_heavy = counts[1];
-  out->kernel_launches = launches;
-  if (timing) {
-    cudaEventElapsedTime(&out->ms_partition, c->ev[0], c->ev[1]);
-    cudaEventElapsedTime(&out->ms_fused, c->ev[1], c->ev[2]);
-    cudaEventElapsedTime(&out->ms_reduce, c->ev[2], c->ev[3]);
-    cudaEventElapsedTime(&out->ms_total, c->ev[0], c->ev[3]);
-  }
-  return PA_OK;
+  B.bins = (float4*)c->bins.p;
+  B.part_blk = (uint32_t*)c->part_blk.p;
+  B.part_counts = (uint32_t*)c->part_counts.p;
+  B.tiles = (Tile*)c->tiles.p;
+  B.heavy = (uint32_t*)c->heavy.p;
+  B.p0_tot = (double*)c->p0_tot.p;
+  B.p_out = (double*)c->p_out.p;
+  B.chunk_sums = (double*)c->chunk_sums.p;
+  B.wave = (float*)c->wave_tmp.p;
+  B.cnt_ev = (uint32_t*)c->cnt_tmp.p;
+  B.cnt_gl = (uint32_t*)c->cnt_tmp.p + N;
+  for (int i = 0; i < 3; ++i) B.dbg[i] = plan.debug ? (uint8_t*)c->dbg[i].p : nullptr;
+  return run_pass(c, plan, B, out, "pa_run");
 }
 
 }  // extern "C"
@@ -545,23 +718,27 @@ int pa_run(pa_ctx* c, const pa_run_params* prm, pa_result* out) {
 // The per-run scratch of pa_run_noalloc: one file-scope device array, so the
 // entry point never allocates. Its name is only meaningful in device code; the
 // host takes its device address once per device with cudaGetSymbolAddress.
-// Layout (each part 256-byte aligned): cycle bins [W f32 | D f32 | ev u32 |
-// gl u32] x PA_NOALLOC_MAX_CYCLES, per-block partition counts, the four
-// partition counters, tiles and heavy-gate lists for PA_NOALLOC_MAX_GATES
-// gates, P0 and totals (8 doubles) and the four result powers.
+// Layout (each part 256-byte aligned): cycle bins {W, D, ev, gl} (float4) x
+// PA_NOALLOC_MAX_CYCLES, per-block partition counts, the four partition
+// counters, tiles and heavy-gate lists for PA_NOALLOC_MAX_GATES gates, P0 and
+// totals (8 doubles), the four result powers, the final reduction's chunk
+// sums, and staging for the waveform and the two count arrays.
 
 namespace {
 
 constexpr size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+constexpr size_t kNaMaxC = PA_NOALLOC_MAX_CYCLES, kNaMaxG = PA_NOALLOC_MAX_GATES;
 constexpr size_t kNaBins = 0;
-constexpr size_t kNaPartBlk = align256(kNaBins + (size_t)PA_NOALLOC_MAX_CYCLES * 16);
-constexpr size_t kNaPartCounts =
-    align256(kNaPartBlk + ((size_t)PA_NOALLOC_MAX_GATES / 256 + 2) * 2 * sizeof(uint32_t));
+constexpr size_t kNaPartBlk = align256(kNaBins + kNaMaxC * sizeof(float4));
+constexpr size_t kNaPartCounts = align256(kNaPartBlk + (kNaMaxG / 256 + 2) * 2 * sizeof(uint32_t));
 constexpr size_t kNaTiles = align256(kNaPartCounts + 4 * sizeof(uint32_t));
-constexpr size_t kNaHeavy = align256(kNaTiles + ((size_t)PA_NOALLOC_MAX_GATES + 1) * sizeof(Tile));
-constexpr size_t kNaP0Tot = align256(kNaHeavy + ((size_t)PA_NOALLOC_MAX_GATES + 1) * sizeof(uint32_t));
+constexpr size_t kNaHeavy = align256(kNaTiles + (kNaMaxG + 1) * sizeof(Tile));
+constexpr size_t kNaP0Tot = align256(kNaHeavy + (kNaMaxG + 1) * sizeof(uint32_t));
 constexpr size_t kNaPOut = align256(kNaP0Tot + 8 * sizeof(double));
-constexpr size_t kNaEnd = align256(kNaPOut + 4 * sizeof(double));
+constexpr size_t kNaChunks = align256(kNaPOut + 4 * sizeof(double));
+constexpr size_t kNaWave = align256(kNaChunks + (kNaMaxC / kReduceChunk + 1) * sizeof(double));
+constexpr size_t kNaCounts = align256(kNaWave + kNaMaxC * sizeof(float));
+constexpr size_t kNaEnd = align256(kNaCounts + 2 * kNaMaxC * sizeof(uint32_t));
 static_assert(kNaEnd <= (size_t)PA_NOALLOC_SCRATCH_BYTES, "no-alloc scratch layout exceeds its array");
 
 }  // namespace
@@ -595,127 +772,117 @@ int noalloc_scratch(pa_ctx* c, int dev, unsigned char** out) {
 }  // namespace
 
 extern "C" int pa_run_noalloc(pa_ctx* c, const pa_run_params* prm, pa_result* out) {
-  if (!c) return PA_ERR_ARG;
-  if (!c->has_ev) return fail(c, PA_ERR_ORDER, "pa_run_noalloc: events not loaded");
-  if (!prm || !out) return fail(c, PA_ERR_ARG, "pa_run_noalloc: null params or result");
-  if (!(prm->t_clk_ns > 0.f) || !is_finite_f(prm->t_clk_ns))
-    return fail(c, PA_ERR_ARG, "pa_run_noalloc: t_clk_ns must be > 0");
-  if (prm->n_cycles == 0) return fail(c, PA_ERR_ARG, "pa_run_noalloc: n_cycles must be > 0");
+  RunPlan plan;
+  PA_TRY(check_run(c, prm, out, "pa_run_noalloc", &plan));
   if (prm->n_cycles > PA_NOALLOC_MAX_CYCLES)
     return fail(c, PA_ERR_ARG, "pa_run_noalloc: n_cycles %u exceeds PA_NOALLOC_MAX_CYCLES (%u)", prm->n_cycles,
                 PA_NOALLOC_MAX_CYCLES);
   if (c->n_gates > PA_NOALLOC_MAX_GATES)
     return fail(c, PA_ERR_ARG, "pa_run_noalloc: %u gates exceed PA_NOALLOC_MAX_GATES (%u)", c->n_gates,
                 PA_NOALLOC_MAX_GATES);
-  if (!std::isfinite(prm->vdd)) return fail(c, PA_ERR_ARG, "pa_run_noalloc: vdd not finite");
   const bool any_array = out->waveform_w || out->event_count || out->glitch_count || out->state_pre ||
                          out->lut_ij || out->is_glitch;
   if (any_array && out->out_mem != PA_MEM_DEVICE)
     return fail(c, PA_ERR_ARG, "pa_run_noalloc: output arrays must be device memory (out_mem = PA_MEM_DEVICE)");
-  const uint32_t tile = prm->tile_events ? prm->tile_events : kDefaultTile;
-  const uint32_t heavy = prm->heavy_events ? prm->heavy_events : kDefaultHeavy;
-  if ((uint64_t)tile + heavy > (uint64_t)kTileCap)
-    return fail(c, PA_ERR_ARG, "pa_run_noalloc: tile_events + heavy_events = %u exceeds %d", tile + heavy, kTileCap);
-  const float T = prm->t_clk_ns;
-  const double Td = (double)T;
-  const double t_max = prm->t_max_ns > 0 ? prm->t_max_ns : (double)prm->n_cycles * Td;
-  if (!std::isfinite(t_max)) return fail(c, PA_ERR_ARG, "pa_run_noalloc: t_max not finite");
-  if (c->n_events) {
-    const float cyc = std::floor(c->t_last / T);
-    if (!(cyc < (float)prm->n_cycles))
-      return fail(c, PA_ERR_RANGE, "pa_run_noalloc: latest event t = %.9g ns lies in cycle %.0f >= n_cycles %u",
-                  (double)c->t_last, (double)cyc, prm->n_cycles);
-    if ((double)c->t_last > t_max)
-      return fail(c, PA_ERR_RANGE, "pa_run_noalloc: t_max %.9g ns is earlier than the latest event %.9g ns",
-                  t_max, (double)c->t_last);
-  }
   CUDA_TRY(c, cudaSetDevice(c->device));
   unsigned char* base = nullptr;
   PA_TRY(noalloc_scratch(c, c->device, &base));
-  const uint32_t N = prm->n_cycles;
+  PassBufs B;
+  B.bins = (float4*)(base + kNaBins);
+  B.part_blk = (uint32_t*)(base + kNaPartBlk);
+  B.part_counts = (uint32_t*)(base + kNaPartCounts);
+  B.tiles = (Tile*)(base + kNaTiles);
+  B.heavy = (uint32_t*)(base + kNaHeavy);
+  B.p0_tot = (double*)(base + kNaP0Tot);
+  B.p_out = (double*)(base + kNaPOut);
+  B.chunk_sums = (double*)(base + kNaChunks);
+  B.wave = (float*)(base + kNaWave);
+  B.cnt_ev = (uint32_t*)(base + kNaCounts);
+  B.cnt_gl = (uint32_t*)(base + kNaCounts) + plan.N;
+  // per-event debug outputs go straight to the caller's device arrays
+  B.dbg[0] = out->state_pre;
+  B.dbg[1] = out->lut_ij;
+  B.dbg[2] = out->is_glitch;
+  return run_pass(c, plan, B, out, "pa_run_noalloc");
+}
+
+// ----------------------------------------------------------------- pa_build_bands
+
+extern "C" int pa_build_bands(pa_ctx* c, float t_clk, uint32_t band_cycles) {
+  if (!c) return PA_ERR_ARG;
+  if (!c->has_ev) return fail(c, PA_ERR_ORDER, "pa_build_bands: events not loaded");
+  if (!(t_clk > 0.f) || !is_finite_f(t_clk)) return fail(c, PA_ERR_ARG, "pa_build_bands: t_clk_ns must be > 0");
+  const uint32_t cb = band_cycles ? band_cycles : kBandDefaultCycles;
+  if (cb > kBandMaxCycles)
+    return fail(c, PA_ERR_ARG, "pa_build_bands: band_cycles %u exceeds %u", cb, kBandMaxCycles);
+  CUDA_TRY(c, cudaSetDevice(c->device));
+  c->band.built = false;
+  const uint64_t E = c->n_events, P = c->n_pins;
   const uint32_t G = c->n_gates;
-  const uint32_t nblk = partition_blocks(G);
-  const bool debug = out->state_pre || out->lut_ij || out->is_glitch;
-  const bool timing = (prm->flags & PA_RUN_TIMING) != 0;
-  const bool pow2 = is_pow2(T);
-  RunArgs a;
+  const float c_last = E ? std::floor(c->t_last / t_clk) : 0.f;  // fp32 division, as the kernels take it
+  if (!(c_last < 4294967040.f)) return fail(c, PA_ERR_ARG, "pa_build_bands: events span too many cycles");
+  const uint32_t nb = (uint32_t)c_last / cb + 1;
+  if (nb > (uint32_t)kBandMaxBands)
+    return fail(c, PA_ERR_ARG, "pa_build_bands: events span %u bands of %u cycles; at most %d (use larger bands)",
+                nb, cb, kBandMaxBands);
+  const uint64_t nu = (uint64_t)nb * G;
+  const size_t ev_bytes = ((E + 64) & ~(size_t)15) * sizeof(float);
+  PA_TRY(dreserve(c, c->b_bt, ev_bytes));
+  PA_TRY(dreserve(c, c->b_bs, ev_bytes));
+  PA_TRY(dreserve(c, c->b_lgate, ((size_t)G + 1) * sizeof(uint32_t)));
+  PA_TRY(dreserve(c, c->b_hgate, ((size_t)G + 1) * sizeof(uint32_t)));
+  PA_TRY(dreserve(c, c->b_cnt, (P * nb + 1) * sizeof(uint32_t)));
+  PA_TRY(dreserve(c, c->b_heavy, (size_t)G + 1));
+  PA_TRY(dreserve(c, c->b_rank, ((size_t)G + 1) * sizeof(uint32_t)));
+  PA_TRY(dreserve(c, c->b_totals, 4 * sizeof(uint32_t)));
+  PA_TRY(dreserve(c, c->b_scan, ((size_t)band_scan_blocks(std::max<uint64_t>(nu, G)) + 1) * sizeof(uint64_t)));
+  PA_TRY(dreserve(c, c->b_usize, (nu + 1) * sizeof(uint32_t)));
+  PA_TRY(dreserve(c, c->b_uoff, (nu + 1) * sizeof(uint64_t)));
+  BandBuildArgs a;
   std::memset(&a, 0, sizeof(a));
-  a.cells = (const CellDesc*)c->cells.p;
-  a.n_cells = c->n_cells;
-  a.lut = (const float*)c->lut.p;
-  a.leak = (const float*)c->leak.p;
   a.gates = (const GateRec*)c->gates.p;
   a.n_gates = G;
+  a.n_pins = P;
+  a.n_events = E;
   a.pin_off = (const uint64_t*)c->pin_off.p;
-  a.gate_off = (const uint64_t*)c->gate_off.p;
   a.t = (const float*)c->t.p;
   a.s = (const float*)c->s.p;
-  a.t_clk = T;
-  a.inv_t_clk = pow2 ? 1.0f / T : 0.f;
-  a.t_max_f = (float)t_max;
-  a.half_vdd2 = (float)(0.5 * prm->vdd * prm->vdd);
-  a.n_cycles = N;
-  a.tile_target = tile;
-  a.heavy_thresh = heavy;
-  a.part_blk = (uint32_t*)(base + kNaPartBlk);
-  a.part_counts = (uint32_t*)(base + kNaPartCounts);
-  a.tiles = (Tile*)(base + kNaTiles);
-  a.heavy = (uint32_t*)(base + kNaHeavy);
-  a.p0 = (double*)(base + kNaP0Tot);
-  a.totals = (double*)(base + kNaP0Tot) + 4;
-  a.bin_w = (float*)(base + kNaBins);
-  a.bin_d = (float*)(base + kNaBins + (size_t)N * 4);
-  a.bin_ev = (uint32_t*)(base + kNaBins + (size_t)N * 8);
-  a.bin_gl = (uint32_t*)(base + kNaBins + (size_t)N * 12);
+  a.t_clk = t_clk;
+  a.pow2 = is_pow2(t_clk);
+  a.inv_t_clk = a.pow2 ? 1.0f / t_clk : 0.f;
+  a.band_cycles = cb;
+  a.n_bands = nb;
+  a.cnt = (uint32_t*)c->b_cnt.p;
+  a.heavy = (uint8_t*)c->b_heavy.p;
+  a.rank = (uint32_t*)c->b_rank.p;
+  a.totals = (uint32_t*)c->b_totals.p;
+  a.unit_size = (uint32_t*)c->b_usize.p;
+  a.unit_off = (uint64_t*)c->b_uoff.p;
+  a.scan_blk = (uint64_t*)c->b_scan.p;
   a.err = (unsigned long long*)c->err_word.p;
-  if (debug) {
-    a.dbg_state = out->state_pre;
-    a.dbg_lut = out->lut_ij;
-    a.dbg_glitch = out->is_glitch;
-  }
-  double* p_dev = (double*)(base + kNaPOut);
-  cudaStream_t st = c->stream;
-  uint32_t launches = 0;
-  if (timing) CUDA_TRY(c, cudaEventRecord(c->ev[0], st));
-  CUDA_TRY(c, cudaMemsetAsync(base + kNaBins, 0, (size_t)N * 16, st));
-  CUDA_TRY(c, cudaMemsetAsync(base + kNaP0Tot, 0, 8 * sizeof(double), st));
-  CUDA_TRY(c, cudaMemsetAsync(base + kNaPartCounts, 0, 4 * sizeof(uint32_t), st));
-  CUDA_TRY(c, cudaMemsetAsync(c->err_word.p, 0xff, sizeof(unsigned long long), st));
-  CUDA_TRY(c, launch_partition(a, nblk, st));
-  launches += nblk ? 3 : 0;
-  if (timing) CUDA_TRY(c, cudaEventRecord(c->ev[1], st));
-  const int grid = c->sm_count * fused_blocks_per_sm(pow2, debug);
-  CUDA_TRY(c, launch_fused(a, grid, pow2, debug, st));
-  launches += 1;
-  if (timing) CUDA_TRY(c, cudaEventRecord(c->ev[2], st));
-  CUDA_TRY(c, launch_final_reduce(a, Td, t_max, out->waveform_w, p_dev, st));
-  launches += 1;
-  if (timing) CUDA_TRY(c, cudaEventRecord(c->ev[3], st));
-  double p[4];
-  unsigned long long key = kNoErr;
-  uint32_t counts[4] = {0, 0, 0, 0};
-  CUDA_TRY(c, cudaMemcpyAsync(p, p_dev, sizeof(p), cudaMemcpyDeviceToHost, st));
-  CUDA_TRY(c, cudaMemcpyAsync(&key, c->err_word.p, sizeof(key), cudaMemcpyDeviceToHost, st));
-  CUDA_TRY(c, cudaMemcpyAsync(counts, a.part_counts, sizeof(counts), cudaMemcpyDeviceToHost, st));
-  if (out->event_count)
-    CUDA_TRY(c, cudaMemcpyAsync(out->event_count, a.bin_ev, (size_t)N * 4, cudaMemcpyDeviceToDevice, st));
-  if (out->glitch_count)
-    CUDA_TRY(c, cudaMemcpyAsync(out->glitch_count, a.bin_gl, (size_t)N * 4, cudaMemcpyDeviceToDevice, st));
-  CUDA_TRY(c, cudaStreamSynchronize(st));
-  if (key != kNoErr) return map_dev_err(c, key, "pa_run_noalloc");
-  out->p_int_w = p[0];
-  out->p_sw_w = p[1];
-  out->p_gl_w = p[2];
-  out->p_leak_w = p[3];
-  out->t_max_ns = t_max;
-  out->n_tiles = counts[0];
-  out->n_heavy = counts[1];
-  out->kernel_launches = launches;
-  if (timing) {
-    cudaEventElapsedTime(&out->ms_partition, c->ev[0], c->ev[1]);
-    cudaEventElapsedTime(&out->ms_fused, c->ev[1], c->ev[2]);
-    cudaEventElapsedTime(&out->ms_reduce, c->ev[2], c->ev[3]);
-    cudaEventElapsedTime(&out->ms_total, c->ev[0], c->ev[3]);
-  }
+  a.L.bt = (float*)c->b_bt.p;
+  a.L.bs = (float*)c->b_bs.p;
+  a.L.lgate = (uint32_t*)c->b_lgate.p;
+  a.L.hgate = (uint32_t*)c->b_hgate.p;
+  a.L.t_clk = t_clk;
+  a.L.band_cycles = cb;
+  a.L.n_bands = nb;
+  CUDA_TRY(c, band_build_phase1(a, c->stream));
+  uint32_t tot[2] = {0, 0};
+  CUDA_TRY(c, cudaMemcpyAsync(tot, a.totals, sizeof(tot), cudaMemcpyDeviceToHost, c->stream));
+  CUDA_TRY(c, cudaStreamSynchronize(c->stream));
+  a.L.n_light = tot[0];
+  a.L.n_heavy = tot[1];
+  a.L.n_lblk = (tot[0] + kLightBlock - 1) / kLightBlock;
+  PA_TRY(dreserve(c, c->b_lrec, ((size_t)nb * a.L.n_light + 1) * sizeof(uint32_t)));
+  PA_TRY(dreserve(c, c->b_hrec, ((size_t)nb * a.L.n_heavy + 1) * sizeof(HeavyRec)));
+  PA_TRY(dreserve(c, c->b_lblk, ((size_t)nb * (a.L.n_lblk + 1) + 1) * sizeof(uint64_t)));
+  a.L.lrec = (uint32_t*)c->b_lrec.p;
+  a.L.hrec = (HeavyRec*)c->b_hrec.p;
+  a.L.lblk = (uint64_t*)c->b_lblk.p;
+  CUDA_TRY(c, band_build_phase2(a, c->stream));
+  CUDA_TRY(c, cudaStreamSynchronize(c->stream));
+  a.L.built = true;
+  c->band = a.L;
   return PA_OK;
 }

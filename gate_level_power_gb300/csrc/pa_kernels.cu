@@ -10,7 +10,7 @@
 //    every gate with more than `heavy_thresh` events is streamed by one CTA in
 //    time windows of at most kTileCap events, sized in proportion to each pin's
 //    remaining events (the role of the paper's event-density-aware per-gate
-//    cycle partitioning, Section 4.2, without a fixed cycles-per-thread).
+//    cycle partitioning, Figs. 5, 19 and 20, without a fixed cycles-per-thread).
 //  * One thread per event inside a staged tile. The gate state before the
 //    event's timestamp (the "preceding gate state" of Section 2.4.1 and the
 //    per-timestamp state S of Fig. 7) is rebuilt from parities: an input pin's
@@ -335,7 +335,7 @@ struct Acc {
   float e_int, e_sw, e_gl, e_lk;
 };
 
-template <bool kPow2, bool kDebug>
+template <bool kPow2, bool kDebug, bool kExact>
 __device__ __forceinline__ void do_event(const RunArgs& a, const float* __restrict__ ts,
                                          const float* __restrict__ ss, const Slot& S, int p, int e,
                                          const CellDesc* cells, bool have_prev0, float prev_t0,
@@ -398,12 +398,22 @@ __device__ __forceinline__ void do_event(const RunArgs& a, const float* __restri
   if (p < k) {
     const float rem = fmaf(-(float)c, a.t_clk, t);  // t - c T
     e_w = fmaf(dp, a.t_clk - rem, e_w);
-    atomicAdd(a.bin_d + c, dp);
     acc.e_lk = fmaf(dp, a.t_max_f - t, acc.e_lk);
   }
-  atomicAdd(a.bin_w + c, e_w);
-  atomicAdd(a.bin_ev + c, 1u);
-  if (glitch) atomicAdd(a.bin_gl + c, 1u);
+  if (kExact) {
+    // dense cycles: fp64 energy and step sums, integer counts
+    double* bin = reinterpret_cast<double*>(a.bins + c);
+    atomicAdd(bin, (double)e_w);
+    if (p < k) atomicAdd(bin + 1, (double)dp);
+    atomicAdd(a.cnt_ev + c, 1u);
+    if (glitch) atomicAdd(a.cnt_gl + c, 1u);
+  } else {
+    float* bin = reinterpret_cast<float*>(a.bins + c);
+    // one 16-byte reduction per event: energy, leakage step, event and glitch counts
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(bin), "f"(e_w), "f"(dp), "f"(1.0f),
+                 "f"(glitch ? 1.0f : 0.0f)
+                 : "memory");
+  }
   if (kDebug) {
     a.dbg_state[gidx] = (uint8_t)s_pre;
     a.dbg_lut[gidx] = p < k ? (uint8_t)((li << 4) | S.j) : (uint8_t)0xFF;
@@ -442,7 +452,7 @@ __device__ __forceinline__ void flush_acc(Acc& acc, double* s_tot) {
   acc = Acc{0.f, 0.f, 0.f, 0.f};
 }
 
-template <bool kPow2, bool kDebug>
+template <bool kPow2, bool kDebug, bool kExact>
 __global__ void __launch_bounds__(kThreads) k_fused(const RunArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   float* ts = reinterpret_cast<float*>(smem);
@@ -513,13 +523,16 @@ __global__ void __launch_bounds__(kThreads) k_fused(const RunArgs a) {
               }
               S.st[p] = (uint16_t)pos;
               pos += (uint32_t)ap;
-              hs.bound[p] = hs.cur[p] + ap < hs.end[p] ? a.t[hs.cur[p] + ap] : FLT_MAX;
             }
             S.st[k + 1] = (uint16_t)pos;
           }
         }
         __syncthreads();
         if (hs.done) break;
+        if (tid <= k) {  // first event past each pin's chunk bounds the window
+          const uint64_t nx = hs.cur[tid] + (uint64_t)(S.st[tid + 1] - S.st[tid]);
+          hs.bound[tid] = nx < hs.end[tid] ? a.t[nx] : FLT_MAX;
+        }
         const int n = S.st[k + 1];
         for (int i = tid; i < n; i += kThreads) {
           int p = 0;
@@ -541,7 +554,7 @@ __global__ void __launch_bounds__(kThreads) k_fused(const RunArgs a) {
         __syncthreads();
         for (int i = tid; i < n; i += kThreads) {
           const int p = tag[i];
-          do_event<kPow2, kDebug>(a, ts, ss, S, p, i, cells, hs.has_prev[p] != 0, hs.prev_t[p],
+          do_event<kPow2, kDebug, kExact>(a, ts, ss, S, p, i, cells, hs.has_prev[p] != 0, hs.prev_t[p],
                                   hs.prev_s[p], hs.cur[p] + (uint64_t)(i - (int)S.st[p]), acc);
         }
         flush_acc(acc, s_tot);
@@ -602,7 +615,7 @@ __global__ void __launch_bounds__(kThreads) k_fused(const RunArgs a) {
       __syncthreads();
       for (int e = tid; e < n; e += kThreads) {
         const uint32_t tg = tag[e];
-        do_event<kPow2, kDebug>(a, ts, ss, slots[tg >> 3], (int)(tg & 7u), e, cells, false, 0.f, 0.f,
+        do_event<kPow2, kDebug, kExact>(a, ts, ss, slots[tg >> 3], (int)(tg & 7u), e, cells, false, 0.f, 0.f,
                                 ea + (uint64_t)e, acc);
       }
       flush_acc(acc, s_tot);
@@ -613,50 +626,121 @@ __global__ void __launch_bounds__(kThreads) k_fused(const RunArgs a) {
   if (tid < 4) atomicAdd(a.totals + tid, s_tot[tid]);
 }
 
-template <bool P, bool D>
+template <bool P, bool D, bool X>
 static void set_fused_attrs() {
   static bool done = false;
   if (!done) {
-    cudaFuncSetAttribute(k_fused<P, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemTotal);
+    cudaFuncSetAttribute(k_fused<P, D, X>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemTotal);
     done = true;
   }
 }
 
-int fused_blocks_per_sm(bool pow2, bool debug) {
+template <bool P, bool D, bool X>
+static int occupancy_of() {
+  set_fused_attrs<P, D, X>();
   int n = 0;
-  if (pow2 && debug) { set_fused_attrs<true, true>(); cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_fused<true, true>, kThreads, kSmemTotal); }
-  else if (pow2) { set_fused_attrs<true, false>(); cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_fused<true, false>, kThreads, kSmemTotal); }
-  else if (debug) { set_fused_attrs<false, true>(); cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_fused<false, true>, kThreads, kSmemTotal); }
-  else { set_fused_attrs<false, false>(); cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_fused<false, false>, kThreads, kSmemTotal); }
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_fused<P, D, X>, kThreads, kSmemTotal);
+  return n;
+}
+
+template <bool P, bool D, bool X>
+static void launch_of(const RunArgs& a, int grid, cudaStream_t st) {
+  set_fused_attrs<P, D, X>();
+  k_fused<P, D, X><<<grid, kThreads, kSmemTotal, st>>>(a);
+}
+
+int fused_blocks_per_sm(bool pow2, bool debug, bool exact) {
+  const int sel = (pow2 ? 4 : 0) | (debug ? 2 : 0) | (exact ? 1 : 0);
+  int n = 0;
+  switch (sel) {
+    case 0: n = occupancy_of<false, false, false>(); break;
+    case 1: n = occupancy_of<false, false, true>(); break;
+    case 2: n = occupancy_of<false, true, false>(); break;
+    case 3: n = occupancy_of<false, true, true>(); break;
+    case 4: n = occupancy_of<true, false, false>(); break;
+    case 5: n = occupancy_of<true, false, true>(); break;
+    case 6: n = occupancy_of<true, true, false>(); break;
+    default: n = occupancy_of<true, true, true>(); break;
+  }
   return n > 0 ? n : 1;
 }
 
-cudaError_t launch_fused(const RunArgs& a, int grid, bool pow2, bool debug, cudaStream_t st) {
-  if (pow2 && debug) { set_fused_attrs<true, true>(); k_fused<true, true><<<grid, kThreads, kSmemTotal, st>>>(a); }
-  else if (pow2) { set_fused_attrs<true, false>(); k_fused<true, false><<<grid, kThreads, kSmemTotal, st>>>(a); }
-  else if (debug) { set_fused_attrs<false, true>(); k_fused<false, true><<<grid, kThreads, kSmemTotal, st>>>(a); }
-  else { set_fused_attrs<false, false>(); k_fused<false, false><<<grid, kThreads, kSmemTotal, st>>>(a); }
+cudaError_t launch_fused(const RunArgs& a, int grid, bool pow2, bool debug, bool exact, cudaStream_t st) {
+  const int sel = (pow2 ? 4 : 0) | (debug ? 2 : 0) | (exact ? 1 : 0);
+  switch (sel) {
+    case 0: launch_of<false, false, false>(a, grid, st); break;
+    case 1: launch_of<false, false, true>(a, grid, st); break;
+    case 2: launch_of<false, true, false>(a, grid, st); break;
+    case 3: launch_of<false, true, true>(a, grid, st); break;
+    case 4: launch_of<true, false, false>(a, grid, st); break;
+    case 5: launch_of<true, false, true>(a, grid, st); break;
+    case 6: launch_of<true, true, false>(a, grid, st); break;
+    default: launch_of<true, true, true>(a, grid, st); break;
+  }
   return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ final reduction
 //
-// One CTA. Prefix-sums the per-cycle leakage steps in fp64 and adds the
-// leakage power held over each cycle, (P0 + steps of earlier cycles) * the
-// cycle's length inside [0, t_max), to the cycle's energy bin; converts bins to
-// W (Eq. 3 per cycle: energy / t_clk). Totals: P_x = E_x / t_max (Eq. 3), with
-// E_leak = P0 t_max + sum over input events of dP (t_max - t).
+// Prefix-sums the per-cycle leakage steps in fp64 and adds the leakage power
+// held over each cycle, (P0 + steps of earlier cycles) * the cycle's length
+// inside [0, t_max), to the cycle's energy bin; converts bins to W (energy /
+// t_clk). Totals: P_x = E_x / t_max (Eq. 3), with E_leak = P0 t_max + sum over
+// input events of dP (t_max - t). Two kernels over chunks of kReduceChunk
+// cycles: step sums per chunk, then a block scan per chunk on top of the sum of
+// the chunks before it.
 
-__global__ void __launch_bounds__(1024) k_final_reduce(const RunArgs a, double T, double t_max,
-                                                       float* wave, double* p_out) {
-  __shared__ double wsum[32];
+constexpr int kRedThreads = 256;
+constexpr int kRedPer = (int)kReduceChunk / kRedThreads;  // cycles per thread
+
+// Energy W and step D of cycle c: f32 {W, D, ev, gl} bins, or fp64 {W, D}
+// bins (same 16 bytes) when counts are taken exactly.
+template <bool kExact>
+__device__ __forceinline__ double2 bin_wd(const RunArgs& a, uint32_t c) {
+  if (kExact) return reinterpret_cast<const double2*>(a.bins)[c];
+  const float4 v = a.bins[c];
+  return make_double2((double)v.x, (double)v.y);
+}
+
+template <bool kExact>
+__global__ void __launch_bounds__(kRedThreads) k_reduce_chunks(const RunArgs a) {
+  const uint32_t c0 = blockIdx.x * kReduceChunk;
+  double s = 0.0;
+  for (uint32_t i = threadIdx.x; i < kReduceChunk; i += kRedThreads) {
+    const uint32_t c = c0 + i;
+    if (c < a.n_cycles) s += bin_wd<kExact>(a, c).y;
+  }
+  __shared__ double ws[kRedThreads / 32];
+  s = warp_sum_f64(s);
+  if ((threadIdx.x & 31) == 0) ws[threadIdx.x >> 5] = s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double t = 0.0;
+    for (int i = 0; i < kRedThreads / 32; ++i) t += ws[i];
+    a.chunk_sums[blockIdx.x] = t;
+  }
+}
+
+template <bool kExact>
+__global__ void __launch_bounds__(kRedThreads) k_reduce_apply(const RunArgs a, double T, double t_max, float* wave,
+                                                            double* p_out) {
+  __shared__ double wsum[kRedThreads / 32];
+  __shared__ double s_base;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  const uint32_t N = a.n_cycles;
-  const uint32_t chunk = (N + 1023) / 1024;
-  const uint32_t c0 = min(N, tid * chunk), c1 = min(N, c0 + chunk);
+  if (tid == 0) {
+    double b = *a.p0;
+    for (uint32_t j = 0; j < blockIdx.x; ++j) b += a.chunk_sums[j];
+    s_base = b;
+  }
+  const uint32_t c0 = blockIdx.x * kReduceChunk + (uint32_t)tid * kRedPer;
+  double2 v[kRedPer];
   double local = 0.0;
-  for (uint32_t c = c0; c < c1; ++c) local += (double)a.bin_d[c];
-  // block exclusive scan (fp64)
+#pragma unroll
+  for (int i = 0; i < kRedPer; ++i) {
+    const uint32_t c = c0 + i;
+    v[i] = c < a.n_cycles ? bin_wd<kExact>(a, c) : make_double2(0.0, 0.0);
+    local += v[i].y;
+  }
   double incl = local;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -665,29 +749,31 @@ __global__ void __launch_bounds__(1024) k_final_reduce(const RunArgs a, double T
   }
   if (lane == 31) wsum[w] = incl;
   __syncthreads();
-  if (w == 0) {
-    double x = wsum[lane];
+  double pre = s_base + incl - local;
+  for (int i = 0; i < w; ++i) pre += wsum[i];
+  bool overflow = false;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const double n = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += n;
-    }
-    wsum[lane] = x;
-  }
-  __syncthreads();
-  const double p0 = *a.p0;
-  double pre = p0 + (w ? wsum[w - 1] : 0.0) + incl - local;
-  for (uint32_t c = c0; c < c1; ++c) {
+  for (int i = 0; i < kRedPer; ++i) {
+    const uint32_t c = c0 + i;
+    if (c >= a.n_cycles) break;
     const double lo = (double)c * T, hi = lo + T;
     const double len = t_max >= hi ? T : (t_max > lo ? t_max - lo : 0.0);
-    const double d = (double)a.bin_d[c];
-    double e = (double)a.bin_w[c] + pre * len;
+    const double d = v[i].y;
+    double e = v[i].x + pre * len;
     if (t_max > lo && t_max < hi) e -= d * (hi - t_max);
     if (wave) wave[c] = (float)(e / T * 1e-6);
+    if (!kExact) {
+      // f32 counts are exact integers while below 2^24
+      const float4 f = a.bins[c];
+      if (f.z >= 16777216.0f) overflow = true;
+      if (a.cnt_ev) a.cnt_ev[c] = (uint32_t)f.z;
+      if (a.cnt_gl) a.cnt_gl[c] = (uint32_t)f.w;
+    }
     pre += d;
   }
-  if (tid == 0) {
-    const double e_leak = p0 * t_max + a.totals[3];
+  if (overflow) dev_err(a.err, 0, kErrCountOverflow);
+  if (blockIdx.x == 0 && tid == 0) {
+    const double e_leak = *a.p0 * t_max + a.totals[3];
     p_out[0] = a.totals[0] / t_max * 1e-6;
     p_out[1] = a.totals[1] / t_max * 1e-6;
     p_out[2] = a.totals[2] / t_max * 1e-6;
@@ -696,8 +782,12 @@ __global__ void __launch_bounds__(1024) k_final_reduce(const RunArgs a, double T
 }
 
 cudaError_t launch_final_reduce(const RunArgs& a, double t_clk, double t_max, float* wave_out,
-                                double* p_out, cudaStream_t st) {
-  k_final_reduce<<<1, 1024, 0, st>>>(a, t_clk, t_max, wave_out, p_out);
+                                double* p_out, bool exact, cudaStream_t st) {
+  const uint32_t nc = reduce_chunks(a.n_cycles);
+  if (exact) k_reduce_chunks<true><<<nc, kRedThreads, 0, st>>>(a);
+  else k_reduce_chunks<false><<<nc, kRedThreads, 0, st>>>(a);
+  if (exact) k_reduce_apply<true><<<nc, kRedThreads, 0, st>>>(a, t_clk, t_max, wave_out, p_out);
+  else k_reduce_apply<false><<<nc, kRedThreads, 0, st>>>(a, t_clk, t_max, wave_out, p_out);
   return cudaGetLastError();
 }
 

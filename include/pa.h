@@ -180,7 +180,8 @@ typedef struct pa_run_params {
  *                           0xFF for output events (debug)
  *   is_glitch[n_events]     per event: 1 if a glitch (debug)
  * With PA_RUN_TIMING, ms_* hold CUDA-event times of the partition, fused and
- * reduction kernels and of the whole device pass.
+ * reduction kernels and of the whole device pass. n_tiles / n_heavy count the
+ * work items (light tiles / heavy items); path says which kernel ran.
  */
 typedef struct pa_result {
   double p_int_w, p_sw_w, p_gl_w, p_leak_w;
@@ -195,7 +196,11 @@ typedef struct pa_result {
   float ms_partition, ms_fused, ms_reduce, ms_total;
   uint32_t n_tiles, n_heavy;
   uint32_t kernel_launches;
+  uint32_t path;  /* out: PA_PATH_UNBANDED or PA_PATH_BANDED */
 } pa_result;
+
+#define PA_PATH_UNBANDED 0u
+#define PA_PATH_BANDED 1u
 
 /* Create a context on CUDA device `cuda_device`. `cuda_stream` is a
  * cudaStream_t to run on (borrowed, must outlive the ctx) or NULL for a stream
@@ -220,6 +225,24 @@ int pa_load_netlist(pa_ctx *ctx, const pa_netlist *nl);
  * ending at n_events), PA_ERR_UNSORTED, PA_ERR_RANGE, PA_ERR_TOGGLE,
  * PA_ERR_OOM, PA_ERR_CUDA. On error no events are loaded. */
 int pa_load_events(pa_ctx *ctx, const pa_events *ev);
+
+/*
+ * pa_build_bands -- regroup the loaded events by clock bands (load-time layout).
+ * Call after pa_load_events, with the clock period the runs will use. Events
+ * are copied into bands of band_cycles consecutive clock cycles (cycle =
+ * floor(fl32(t / t_clk_ns))); inside a band they keep the per-pin CSR order.
+ * Every pa_run whose t_clk_ns equals this t_clk_ns bit for bit then uses the
+ * banded kernel, which keeps each band's cycle bins in shared memory instead of
+ * adding every event to global memory; other clocks use the unbanded kernel.
+ * Results agree with the unbanded path to floating-point summation order.
+ *   band_cycles  cycles per band; 0 = default 6144; at most 6144
+ * The events may span at most 64 bands. Memory: a second copy of the times and
+ * slews (8 bytes per event) and about 4 bytes per (band, gate).
+ * Errors: PA_ERR_ORDER (no events loaded), PA_ERR_ARG (t_clk_ns not > 0,
+ * band_cycles too large, events spanning more than 64 bands), PA_ERR_OOM,
+ * PA_ERR_CUDA. Loading a new library, netlist or events drops the bands.
+ */
+int pa_build_bands(pa_ctx *ctx, float t_clk_ns, uint32_t band_cycles);
 
 /* Run partition -> fused power kernel -> final reduction on the loaded data.
  * May be called repeatedly with different parameters. Errors: PA_ERR_ORDER,
@@ -251,7 +274,9 @@ int pa_run(pa_ctx *ctx, const pa_run_params *params, pa_result *out);
  * capture. All calls share the one array and it keeps the last call's
  * contents (each call clears what it needs zeroed): calls whose device work
  * overlaps -- from several threads, contexts or streams at once -- race and
- * must be serialised by the caller.
+ * must be serialised by the caller. Per-event debug arrays are written in
+ * place and may hold partial data after an error; the other outputs are
+ * written only on PA_OK.
  */
 #define PA_NOALLOC_MAX_CYCLES 65536u
 #define PA_NOALLOC_MAX_GATES 262144u

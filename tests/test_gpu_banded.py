@@ -1,0 +1,126 @@
+"""GPU parity of the banded path (pa_build_bands + pa_run at the banding
+clock) against the fp64 oracle, with the same bar as the unbanded path:
+states, LUT intervals, glitch flags and per-cycle counts bit-exact; totals
+within 1e-5; waveform bins within 1e-4 of the peak bin."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests.test_gpu_parity import assert_parity, golden
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def glp():
+    import gate_level_power_gb300 as glp
+    glp.build()
+    glp.load_library()
+    return glp
+
+
+def banded_run(glp, w, band_cycles=0, t_max=0.0, debug=True, with_value=True):
+    with glp.PowerAnalyzer(0) as pa:
+        pa.load_workload(w, with_value=with_value)
+        pa.build_bands(w.t_clk_ns, band_cycles)
+        r = pa.run(w.vdd, w.t_clk_ns, w.n_cycles, t_max_ns=t_max, debug=debug)
+    assert r["path"] == glp.PA_PATH_BANDED
+    return r
+
+
+@pytest.mark.parametrize("name", ["w1_inverter_glitch.json", "w2_nand2_tie.json"])
+def test_golden_banded(glp, name):
+    w, d = golden(name)
+    for bc in (0, 1, 3):
+        r = banded_run(glp, w, band_cycles=bc)
+        ex = d["expected"]
+        for key in ("p_int", "p_sw", "p_gl", "p_leak"):
+            assert r[key] == pytest.approx(ex[key], rel=1e-5, abs=1e-30), (bc, key)
+        np.testing.assert_array_equal(r["event_count"], ex["evcount"])
+        for key in ("state_pre", "lut_ij", "is_glitch"):
+            np.testing.assert_array_equal(r[key], ex[key], err_msg=f"{key} bands of {bc}")
+
+
+@pytest.mark.parametrize("cfg,bc", [(1, 0), (1, 7), (2, 0), (2, 100), (2, 16)])
+def test_standard_configs_banded(glp, cfg, bc):
+    w = synth.generate(cfg)
+    r = banded_run(glp, w, band_cycles=bc)
+    o = oracle.run(w, debug=True, threads=8)
+    assert_parity(r, o)
+
+
+@pytest.mark.parametrize("seed,quantum,k_mode,t_clk,bc", [
+    (41, 0.25, 1, 1.0, 5), (42, 0.125, 2, 0.8, 8), (43, 0.0, 0, 0.8, 3), (44, 1.0, 2, 1.0, 4),
+    (45, 0.05, 1, 0.3, 64),
+])
+def test_random_tie_heavy_banded(glp, seed, quantum, k_mode, t_clk, bc):
+    w = synth.custom(seed=seed, n_gates=60, n_cells=12, k_mode=k_mode, n_slew=5, n_load=4, n_cycles=90,
+                     t_clk_ns=t_clk, n_events=6000, pair_frac=0.2, quantum_ns=quantum, threads=2)
+    r = banded_run(glp, w, band_cycles=bc)
+    o = oracle.run(w, debug=True)
+    assert_parity(r, o)
+
+
+@pytest.mark.parametrize("bc", [0, 40, 7])
+def test_heavy_units_and_streaming_banded(glp, bc):
+    # few gates with many events: heavy units, some streamed within a band
+    w = synth.custom(seed=21, n_gates=12, n_cells=8, k_mode=1, n_slew=6, n_load=6, n_cycles=400,
+                     t_clk_ns=1.0, n_events=120000, pair_frac=0.1, quantum_ns=0.01, threads=4)
+    r = banded_run(glp, w, band_cycles=bc)
+    o = oracle.run(w, debug=True, threads=4)
+    assert_parity(r, o)
+    assert r["n_heavy"] > 0
+
+
+def test_mixed_light_heavy_skewed_banded(glp):
+    w = synth.custom(seed=22, n_gates=20000, n_cells=32, k_mode=1, n_cycles=2000, t_clk_ns=1.0,
+                     n_events=3000000, activity=1, zipf_s=1.2, pair_frac=0.1, threads=8)
+    r = banded_run(glp, w, band_cycles=256)
+    o = oracle.run(w, debug=True, threads=8)
+    assert_parity(r, o)
+    assert r["n_heavy"] > 0 and r["n_tiles"] > 0
+
+
+@pytest.mark.parametrize("factor", [2.0, "last"])
+def test_t_max_override_banded(glp, factor):
+    w = synth.custom(seed=5, n_gates=60, n_cells=8, n_events=2000, n_cycles=30, t_clk_ns=1.0, pair_frac=0.1)
+    t_max = float(w.t_ns.max()) if factor == "last" else factor * w.n_cycles * w.t_clk_ns
+    r = banded_run(glp, w, band_cycles=4, t_max=t_max)
+    o = oracle.run(w, debug=True, t_max=t_max)
+    assert_parity(r, o)
+
+
+def test_zero_events_banded(glp):
+    w = synth.custom(seed=3, n_gates=500, n_cells=8, n_events=0, n_cycles=20)
+    r = banded_run(glp, w)
+    o = oracle.run(w, debug=True)
+    assert_parity(r, o)
+
+
+def test_other_clock_falls_back_to_unbanded(glp):
+    w = synth.generate(1)
+    o = oracle.run(w, t_clk=0.5, n_cycles=200)
+    with glp.PowerAnalyzer(0) as pa:
+        pa.load_workload(w)
+        pa.build_bands(w.t_clk_ns)
+        r = pa.run(w.vdd, 0.5, 200)
+        assert r["path"] == glp.PA_PATH_UNBANDED
+        for key in ("p_int", "p_sw", "p_gl", "p_leak"):
+            assert r[key] == pytest.approx(o[key], rel=1e-5)
+        # reloading events drops the bands
+        pa.load_events(w.pin_off, w.t_ns, w.slew_ps, w.value)
+        assert pa.run(w.vdd, w.t_clk_ns, w.n_cycles)["path"] == glp.PA_PATH_UNBANDED
+
+
+def test_build_bands_errors(glp):
+    w = synth.generate(1)
+    with glp.PowerAnalyzer(0) as pa:
+        with pytest.raises(glp.PaError) as ei:
+            pa.build_bands(1.0)
+        assert ei.value.code == glp.PA_ERR_ORDER
+        pa.load_workload(w)
+        for args in ((0.0, 0), (1.0, 7000), (1.0, 1)):  # 100 cycles in bands of 1 > 64 bands
+            with pytest.raises(glp.PaError) as ei:
+                pa.build_bands(*args)
+            assert ei.value.code == glp.PA_ERR_ARG

@@ -180,4 +180,15 @@ def test_timing_and_work_counts_reported(glp):
     w = synth.generate(2)
     r = gpu_run(glp, w, debug=False, timing=True)
     assert r["ms_fused"] > 0 and r["ms_total"] >= r["ms_fused"]
-    assert r["n_tiles"] > 0 and r["kernel_launches"] == 5
+    assert r["n_tiles"] > 0 and r["kernel_launches"] == 6
+
+
+def test_more_than_2_pow_24_events_in_one_cycle_counts_exactly(glp):
+    # per-cycle counts travel as f32 in the one-per-event vector reduction; a
+    # cycle with 2^24 or more events makes the pass repeat with integer counts
+    w = synth.custom(seed=31, n_gates=300000, n_cells=8, n_cycles=2, t_clk_ns=1.0, n_events=17_000_000,
+                     burst_frac=1.0, burst_width=1, burst_cover=0.5, threads=8)
+    r = gpu_run(glp, w, debug=False)
+    o = oracle.run(w, threads=8)
+    assert int(o["evcount"].max()) >= 1 << 24
+    assert_parity(r, o, debug=False)
