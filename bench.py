@@ -57,7 +57,12 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle sample time")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--unbanded", action="store_true", help="skip pa_build_bands (unbanded kernel)")
+    ap.add_argument("--banded", action="store_true",
+                    help="build cycle bands (pa_build_bands) and time the banded kernel")
+    ap.add_argument("--band-cycles", type=int, default=0, help="cycles per band (0 = library default)")
+    ap.add_argument("--synth", nargs="*", default=[], metavar="KNOB=VALUE",
+                    help="generator overrides for a scaled-down profiling case, e.g. n_gates=1000000 "
+                         "n_events=200000000 (the line then names the workload as modified)")
     return ap.parse_args()
 
 
@@ -291,6 +296,14 @@ def run_reference(args):
     return 0
 
 
+def synth_overrides(items):
+    out = {}
+    for it in items:
+        k, v = it.split("=", 1)
+        out[k] = float(v) if any(ch in v for ch in ".e") and not v.isdigit() else int(v)
+    return out
+
+
 def workload_config(config, G, E, cfg):
     import synth
     return {"workload": f"config {config}: " + synth.CONFIG_NAMES.get(config, "custom"),
@@ -313,15 +326,16 @@ def run_ours(args):
     glp.load_library()
     alloc, keep = pinned_alloc()
     t0 = time.perf_counter()
-    w = synth.generate(args.config, seed=args.seed, alloc=alloc)
+    over = synth_overrides(args.synth)
+    w = synth.generate(args.config, seed=args.seed, alloc=alloc, **over)
     gen_s = time.perf_counter() - t0
-    cfg = synth.make_cfg(args.config, args.seed)
+    cfg = synth.make_cfg(args.config, args.seed, **over)
     E, G, N = w.n_events, w.n_gates, w.n_cycles
     stream = torch.cuda.Stream(device=local)
     pa = glp.PowerAnalyzer(local, stream.cuda_stream)
     pa.load_workload(w)
-    if not args.unbanded:
-        pa.build_bands(w.t_clk_ns)
+    if args.banded:
+        pa.build_bands(w.t_clk_ns, args.band_cycles)
     wave = np.empty(N, np.float32)
     evc = np.empty(N, np.uint32)
     glc = np.empty(N, np.uint32)
@@ -361,8 +375,8 @@ def run_ours(args):
     if args.e2e_steps > 0:
         def e2e_step():
             pa.load_events(w.pin_off, w.t_ns, w.slew_ps, w.value)
-            if not args.unbanded:
-                pa.build_bands(w.t_clk_ns)
+            if args.banded:
+                pa.build_bands(w.t_clk_ns, args.band_cycles)
             step()
         for _ in range(2):
             e2e_step()
@@ -390,7 +404,8 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": "events/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": el_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": workload_config(args.config, G, E, cfg),
+            "config": dict(workload_config(args.config, G, E, cfg),
+                           **({"modified": " ".join(args.synth)} if args.synth else {})),
             "gate_cycles_per_s": world * G * N * args.steps / (el_ms * 1e-3),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
@@ -402,8 +417,8 @@ def run_ours(args):
             "e2e": None if e2e_value is None else {"value": e2e_value, "unit": "events/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
                     "note": "per step: pa_load_events from pinned host memory (device-side validation) + "
-                            "pa_build_bands + pa_run + waveform/count copy to host; library and netlist "
-                            "loaded once"},
+                            + ("pa_build_bands + " if args.banded else "")
+                            + "pa_run + waveform/count copy to host; library and netlist loaded once"},
             "clocks": clk.summary(),
             "gpu_launches": launches,
             "gen_seconds": gen_s,

@@ -874,7 +874,8 @@ extern "C" int pa_build_bands(pa_ctx* c, float t_clk, uint32_t band_cycles) {
   a.L.n_light = tot[0];
   a.L.n_heavy = tot[1];
   a.L.n_lblk = (tot[0] + kLightBlock - 1) / kLightBlock;
-  PA_TRY(dreserve(c, c->b_lrec, ((size_t)nb * a.L.n_light + 1) * sizeof(uint32_t)));
+  // + 8: staged copies round record ranges up to 16 bytes
+  PA_TRY(dreserve(c, c->b_lrec, ((size_t)nb * a.L.n_light + 8) * sizeof(uint32_t)));
   PA_TRY(dreserve(c, c->b_hrec, ((size_t)nb * a.L.n_heavy + 1) * sizeof(HeavyRec)));
   PA_TRY(dreserve(c, c->b_lblk, ((size_t)nb * (a.L.n_lblk + 1) + 1) * sizeof(uint64_t)));
   a.L.lrec = (uint32_t*)c->b_lrec.p;

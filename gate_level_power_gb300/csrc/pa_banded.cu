@@ -445,6 +445,9 @@ __global__ void __launch_bounds__(256) k_bp_emit(const BandLayout L, uint32_t ki
     ev = h1.base + hunit_n(h1) - h0.base;
     it.kind = (e == j + 1 && ev > (uint64_t)kBTileCap) ? 2u : 1u;
   }
+  it.e0 = kind == 0 ? lblk_at(L, b, j) : L.hrec[(uint64_t)b * L.n_heavy + j].base;
+  it.n = (uint32_t)ev;
+  it.pad = 0;
   const uint32_t k = item_base + (uint32_t)pos[i];
   items[k] = it;
   item_n[k] = (uint32_t)ev;
@@ -522,11 +525,18 @@ cudaError_t band_gate_run(BandRunArgs& A, cudaStream_t st) {
 }
 
 // ------------------------------------------------------------------ banded fused kernel
+//
+// One CTA per SM takes a contiguous, event-balanced run of band-major items.
+// Thread 0 prefetches item i+1 with TMA bulk copies (events, unit records,
+// per-run gate records) into the spare one of two shared-memory stages while
+// the CTA works on item i; an mbarrier per stage signals completion. Events
+// add into the band's cycle bins in shared memory; a band change flushes them.
 
 namespace {
 
 constexpr int kBThreads = 512;
 constexpr int kBWarps = kBThreads / 32;
+static_assert(kBGateCap == kBThreads, "one unit per thread in tile setup");
 
 struct __align__(16) BSlot {
   uint16_t st[5];   // staged start of each pin's segment
@@ -550,13 +560,61 @@ struct BAcc {
   float e_int, e_sw, e_gl, e_lk;
 };
 
+struct StageMeta {
+  BandItem it;
+  uint32_t ev_off, rec_off;
+};
+
+constexpr int kStEv = kBTileCap + 8;  // staged floats per array (16-byte rounding slack)
+constexpr size_t kStTs = (size_t)kStEv * 4;
+constexpr size_t kStRec = (size_t)kBGateCap * sizeof(HeavyRec) + 16;
+constexpr size_t kStGrun = (size_t)kBGateCap * sizeof(GateRun);
+constexpr size_t kStage = 2 * kStTs + kStRec + kStGrun;
+static_assert(kStage % 16 == 0, "stage alignment");
+
 constexpr size_t kBHist = (size_t)kBandMaxCycles * 16;
-constexpr size_t kBTs = (size_t)kBTileCap * 4;
-constexpr size_t kBTag = (size_t)kBTileCap * 2;
 constexpr size_t kBSlots = (size_t)kBGateCap * sizeof(BSlot);
+constexpr size_t kBTag = (size_t)kBTileCap * 2;
 constexpr size_t kBGates = (size_t)kBGateCap * 4;
 constexpr size_t kBCells = (size_t)kSmemCells * sizeof(CellDesc);
-constexpr size_t kBSmem = kBHist + 2 * kBTs + kBTag + kBSlots + kBGates + kBCells;
+constexpr size_t kBSmem = kBHist + 2 * kStage + kBSlots + kBTag + kBGates + kBCells;
+static_assert(kBSmem <= 227 * 1024, "shared memory budget");
+
+constexpr uint32_t kWaitLimit = 1u << 24;  // mbarrier polls before giving up
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_arrive(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bulk copy global -> shared, completing on the mbarrier (16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
 
 __device__ __forceinline__ int lb_f(const float* a, int n, float x) {
   int lo = 0;
@@ -577,8 +635,6 @@ struct BCtx {
   float* D;
   uint32_t* EV;
   uint32_t* GL;
-  float* ts;
-  float* ss;
   uint16_t* tag;
   BSlot* slots;
   uint32_t* sgate;  // gate id per slot (debug outputs)
@@ -589,30 +645,33 @@ struct BCtx {
 // One event of a staged segment (gate state, LUT, switching, glitch, leakage)
 // into the shared-memory band histogram.
 template <bool kPow2, bool kDebug>
-__device__ __forceinline__ void bevent(const BandRunArgs& A, const BCtx& X, int si, int p, int e,
-                                       bool hp0, float pt0, float ps0, BAcc& acc) {
+__device__ __forceinline__ void bevent(const BandRunArgs& A, const BCtx& X, const float* __restrict__ ts,
+                                       const float* __restrict__ ss, int si, int p, int e, bool hp0, float pt0,
+                                       float ps0, BAcc& acc) {
   const RunArgs& a = A.r;
-  const BSlot S = X.slots[si];
-  const int idx = e - (int)S.st[p];
+  const BSlot& S = X.slots[si];
+  const int a0 = S.st[p];
+  const int idx = e - a0;
   if (idx >= (int)S.len[p]) return;
-  const float t = X.ts[e], s = X.ss[e];
+  const float t = ts[e], s = ss[e];
   const uint32_t c = cyc<kPow2>(t, a.t_clk, a.inv_t_clk);
   bool has_prev = hp0;
   float tp = pt0, sp = ps0;
   if (idx > 0) {
     has_prev = true;
-    tp = X.ts[e - 1];
-    sp = X.ss[e - 1];
+    tp = ts[e - 1];
+    sp = ss[e - 1];
   }
   const bool glitch = has_prev && cyc<kPow2>(tp, a.t_clk, a.inv_t_clk) == c;
-  const int k = S.kj & 15;
+  const uint32_t kj = S.kj;
+  const int k = (int)(kj & 15u);
   float e_int = 0.f, e_sw = 0.f, dp = 0.f;
   uint32_t s_pre = S.state;
   int li = 0;
   if (p == k) {
     e_sw = S.esw;
     if (kDebug) {
-      for (int q = 0; q < k; ++q) s_pre ^= ((uint32_t)lb_f(X.ts + S.st[q], S.len[q], t) & 1u) << q;
+      for (int q = 0; q < k; ++q) s_pre ^= ((uint32_t)lb_f(ts + S.st[q], S.len[q], t) & 1u) << q;
     }
   } else {
     const CellDesc& cd = X.cells[S.cell];
@@ -621,18 +680,28 @@ __device__ __forceinline__ void bevent(const BandRunArgs& A, const BCtx& X, int 
     for (int q = 0; q < k; ++q) {
       if (q == p) continue;
       const int qa = S.st[q], qn = S.len[q];
-      const int r = lb_f(X.ts + qa, qn, t);
+      const int r = lb_f(ts + qa, qn, t);
       const uint32_t par = (uint32_t)r & 1u;
       s_pre ^= par << q;
-      const bool eq = q < p && r < qn && X.ts[qa + r] == t;
+      const bool eq = q < p && r < qn && ts[qa + r] == t;
       s_b ^= (par ^ (uint32_t)eq) << q;
     }
-    const int ns = cd.ns, nl = cd.nl, j = S.kj >> 4;
-    for (int m = 1; m <= ns - 2; ++m) li += (s >= cd.sax[m]) ? 1 : 0;
+    // slew interval: largest i <= ns - 2 with axis[i] <= s (axes have <= 8 points)
+    const int ns = cd.ns, nl = cd.nl;
+    {
+      const int hi = ns - 2;
+      int w = 4;
+      while (w > 0) {
+        const int cand = li + w;
+        if (cand <= hi && s >= cd.sax[cand]) li = cand;
+        w >>= 1;
+      }
+    }
     const float u = (s - cd.sax[li]) * cd.isax[li];
-    const float* L = a.lut + cd.lut_off + ((int)s_pre * ns + li) * nl + j;
+    const float* L = a.lut + cd.lut_off + ((int)s_pre * ns + li) * nl + (int)(kj >> 4);
     const float l00 = __ldg(L), l01 = __ldg(L + 1), l10 = __ldg(L + nl), l11 = __ldg(L + nl + 1);
-    const float r0 = fmaf(S.v, l01 - l00, l00), r1 = fmaf(S.v, l11 - l10, l10);
+    const float v = S.v;
+    const float r0 = fmaf(v, l01 - l00, l00), r1 = fmaf(v, l11 - l10, l10);
     e_int = fmaf(u, r1 - r0, r0);
     const float* lk = a.leak + cd.leak_off;
     dp = __ldg(lk + (s_b ^ (1u << p))) - __ldg(lk + s_b);
@@ -678,7 +747,7 @@ __device__ __forceinline__ void bevent(const BandRunArgs& A, const BCtx& X, int 
       }
     }
     a.dbg_state[l] = (uint8_t)s_pre;
-    a.dbg_lut[l] = p < k ? (uint8_t)((li << 4) | (S.kj >> 4)) : (uint8_t)0xFF;
+    a.dbg_lut[l] = p < k ? (uint8_t)((li << 4) | (int)(kj >> 4)) : (uint8_t)0xFF;
     a.dbg_glitch[l] = (uint8_t)glitch;
   }
 }
@@ -726,25 +795,78 @@ __device__ __forceinline__ void bslot_from(BSlot& S, const GateRun& gr, uint32_t
   S.esw = gr.esw;
 }
 
+// Thread 0: stage item `i` into stage buffer `stage` (TMA bulk copies).
+__device__ void bprefetch(const BandRunArgs& A, uint32_t i, uint8_t* stage, StageMeta& meta, uint64_t* bar) {
+  const BandItem it = A.items[i];
+  meta.it = it;
+  meta.ev_off = 0;
+  meta.rec_off = 0;
+  if (it.kind == 2) {  // streamed: nothing staged
+    mbar_expect_arrive(bar, 0);
+    return;
+  }
+  float* ts = reinterpret_cast<float*>(stage);
+  float* ss = reinterpret_cast<float*>(stage + kStTs);
+  uint8_t* rec = stage + 2 * kStTs;
+  uint8_t* grun = rec + kStRec;
+  const bool light = it.kind == 0;
+  const uint32_t u0 = light ? it.first * kLightBlock : it.first;
+  const uint32_t u1 = light ? min(it.last * (uint32_t)kLightBlock, A.L.n_light) : it.last;
+  const uint32_t nu = u1 - u0;
+  if (it.n > (uint32_t)kBTileCap || nu > (uint32_t)kBGateCap || u1 < u0) {  // never stage past a buffer
+    meta.it.kind = 3;
+    mbar_expect_arrive(bar, 0);
+    return;
+  }
+  const uint64_t ea = it.e0 & ~3ull;
+  const uint32_t ev_off = (uint32_t)(it.e0 - ea);
+  const uint32_t ev_bytes = it.n ? ((ev_off + it.n + 3u) & ~3u) * 4u : 0u;
+  uint32_t rec_bytes = 0, rec_off = 0;
+  const void* rec_src = nullptr;
+  if (light) {
+    const uint64_t rb = (uint64_t)it.band * A.L.n_light + u0;
+    const uint64_t ra = rb & ~3ull;
+    rec_off = (uint32_t)(rb - ra);
+    rec_bytes = nu ? ((rec_off + nu + 3u) & ~3u) * 4u : 0u;
+    rec_src = A.L.lrec + ra;
+  } else {
+    rec_bytes = nu * (uint32_t)sizeof(HeavyRec);
+    rec_src = A.L.hrec + (uint64_t)it.band * A.L.n_heavy + u0;
+  }
+  const uint32_t g_bytes = nu * (uint32_t)sizeof(GateRun);
+  const void* g_src = (light ? A.grun_l : A.grun_h) + u0;
+  meta.ev_off = ev_off;
+  meta.rec_off = rec_off;
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  mbar_expect_arrive(bar, 2 * ev_bytes + rec_bytes + g_bytes);
+  if (ev_bytes) {
+    bulk_g2s(ts, A.L.bt + ea, ev_bytes, bar);
+    bulk_g2s(ss, A.L.bs + ea, ev_bytes, bar);
+  }
+  if (rec_bytes) bulk_g2s(rec, rec_src, rec_bytes, bar);
+  if (g_bytes) bulk_g2s(grun, g_src, g_bytes, bar);
+}
+
 }  // namespace
 
 namespace {
 
 template <bool kPow2, bool kDebug>
 __global__ void __launch_bounds__(kBThreads, 1) k_banded(const BandRunArgs A, uint32_t n_items) {
-  extern __shared__ __align__(16) uint8_t smem[];
+  extern __shared__ __align__(128) uint8_t smem[];
   BCtx X;
   const uint32_t cb = A.L.band_cycles;
   X.W = reinterpret_cast<float*>(smem);
   X.D = X.W + kBandMaxCycles;
   X.EV = reinterpret_cast<uint32_t*>(X.D + kBandMaxCycles);
   X.GL = X.EV + kBandMaxCycles;
-  X.ts = reinterpret_cast<float*>(smem + kBHist);
-  X.ss = X.ts + kBTileCap;
-  X.tag = reinterpret_cast<uint16_t*>(X.ss + kBTileCap);
-  X.slots = reinterpret_cast<BSlot*>(smem + kBHist + 2 * kBTs + kBTag);
-  X.sgate = reinterpret_cast<uint32_t*>(smem + kBHist + 2 * kBTs + kBTag + kBSlots);
-  CellDesc* cells_s = reinterpret_cast<CellDesc*>(smem + kBHist + 2 * kBTs + kBTag + kBSlots + kBGates);
+  uint8_t* stages = smem + kBHist;
+  X.slots = reinterpret_cast<BSlot*>(stages + 2 * kStage);
+  X.tag = reinterpret_cast<uint16_t*>(stages + 2 * kStage + kBSlots);
+  X.sgate = reinterpret_cast<uint32_t*>(stages + 2 * kStage + kBSlots + kBTag);
+  CellDesc* cells_s = reinterpret_cast<CellDesc*>(stages + 2 * kStage + kBSlots + kBTag + kBGates);
+  __shared__ __align__(8) uint64_t s_bar[2];
+  __shared__ StageMeta s_meta[2];
   __shared__ BStream hs;
   __shared__ double s_tot[4];
   __shared__ uint32_t s_range[2];
@@ -783,60 +905,83 @@ __global__ void __launch_bounds__(kBThreads, 1) k_banded(const BandRunArgs A, ui
     }
     s_range[tid] = (blockIdx.x + tid == gridDim.x) ? n_items : lo;
   }
+  if (tid == 0) {
+    mbar_init(&s_bar[0], 1);
+    mbar_init(&s_bar[1], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
   __syncthreads();
   const uint32_t i0 = s_range[0], i1 = s_range[1];
+  if (tid == 0 && i0 < i1) bprefetch(A, i0, stages, s_meta[0], &s_bar[0]);
   uint32_t band = 0xFFFFFFFFu;
   BAcc acc{0.f, 0.f, 0.f, 0.f};
   int since_flush = 0;
 
   for (uint32_t item = i0; item < i1; ++item) {
-    const BandItem it = A.items[item];
-    if (it.band != band) {
-      if (band != 0xFFFFFFFFu) {
-        __syncthreads();
-        bflush_band(A, X, band);
+    const uint32_t q = item - i0, st = q & 1u;
+    if (tid == 0 && item + 1 < i1)  // the other stage was released by the barrier ending item - 1
+      bprefetch(A, item + 1, stages + (st ^ 1u) * kStage, s_meta[st ^ 1u], &s_bar[st ^ 1u]);
+    bool ok = false;
+    for (uint32_t it = 0; it < kWaitLimit && !ok; ++it) ok = mbar_try_wait(&s_bar[st], (q >> 1) & 1u);
+    if (__syncthreads_or(!ok)) {  // a staged copy never landed: report and stop this CTA
+      if (tid == 0) {
+        berr(a.err, item, kErrTileOverflow);
+        if (item + 1 < i1) {  // let our own prefetch of the next item land (bounded) before leaving
+          bool done = false;
+          for (uint32_t it = 0; it < kWaitLimit && !done; ++it)
+            done = mbar_try_wait(&s_bar[st ^ 1u], ((q + 1) >> 1) & 1u);
+        }
       }
+      return;
+    }
+    const StageMeta M = s_meta[st];
+    const BandItem it = M.it;
+    uint8_t* stage = stages + st * kStage;
+    const float* ts = reinterpret_cast<const float*>(stage) + M.ev_off;
+    const float* ss = reinterpret_cast<const float*>(stage + kStTs) + M.ev_off;
+    if (it.band != band) {
+      if (band != 0xFFFFFFFFu) bflush_band(A, X, band);
       band = it.band;
       X.c0 = band * cb;
       __syncthreads();
     }
+    if (it.kind == 3) {  // refused by the prefetch bounds check
+      if (tid == 0) berr(a.err, item, kErrTileOverflow);
+      __syncthreads();
+      continue;
+    }
     if (it.kind == 0 || it.kind == 1) {
       // ---------------- a tile of whole units (light gates or small heavy units)
       const bool light = it.kind == 0;
-      uint32_t u0, u1;
-      uint64_t e0;
-      if (light) {
-        u0 = it.first * kLightBlock;
-        u1 = min(it.last * (uint32_t)kLightBlock, A.L.n_light);
-        e0 = A.L.lblk[(uint64_t)band * (A.L.n_lblk + 1) + it.first];
-      } else {
-        u0 = it.first;
-        u1 = it.last;
-        e0 = A.L.hrec[(uint64_t)band * A.L.n_heavy + u0].base;
-      }
+      const uint32_t u0 = light ? it.first * kLightBlock : it.first;
+      const uint32_t u1 = light ? min(it.last * (uint32_t)kLightBlock, A.L.n_light) : it.last;
       const uint32_t ng = u1 - u0;
-      // unit counts and states; unit starts by a block scan (2 units per thread)
-      uint32_t cnt2[2][5], st2[2], tot2[2];
-      for (int h = 0; h < 2; ++h) {
-        const uint32_t gi = (uint32_t)tid * 2 + h;
-        tot2[h] = 0;
-        st2[h] = 0;
-        for (int p = 0; p < 5; ++p) cnt2[h][p] = 0;
-        if (gi < ng) {
-          if (light) {
-            const uint32_t rec = A.L.lrec[(uint64_t)band * A.L.n_light + u0 + gi];
-            for (int p = 0; p < 5; ++p) cnt2[h][p] = (rec >> (5 * p)) & 31u;
-            st2[h] = rec >> 25;
-          } else {
-            const HeavyRec hr = A.L.hrec[(uint64_t)band * A.L.n_heavy + u0 + gi];
-            for (int p = 0; p < 5; ++p) cnt2[h][p] = hr.cnt[p];
-            st2[h] = hr.state;
-          }
-          for (int p = 0; p < 5; ++p) tot2[h] += cnt2[h][p];
-        }
+      const uint32_t n = it.n;
+      if (n > (uint32_t)kBTileCap || ng > (uint32_t)kBGateCap) {
+        if (tid == 0) berr(a.err, item, kErrTileOverflow);
+        __syncthreads();
+        continue;
       }
-      const uint32_t mine = tot2[0] + tot2[1];
-      uint32_t inc = mine;
+      const uint8_t* rec = stage + 2 * kStTs;
+      const GateRun* grun = reinterpret_cast<const GateRun*>(rec + kStRec);
+      uint32_t c5 = 0, state = 0, tot = 0;
+      uint32_t hc[5] = {0, 0, 0, 0, 0};  // events of each pin of this thread's unit
+      if ((uint32_t)tid < ng) {
+        if (light) {
+          c5 = reinterpret_cast<const uint32_t*>(rec)[M.rec_off + tid];
+          state = c5 >> 25;
+#pragma unroll
+          for (int p = 0; p < 5; ++p) hc[p] = (c5 >> (5 * p)) & 31u;
+        } else {
+          const HeavyRec& hr = reinterpret_cast<const HeavyRec*>(rec)[tid];
+#pragma unroll
+          for (int p = 0; p < 5; ++p) hc[p] = hr.cnt[p];
+          state = hr.state;
+        }
+#pragma unroll
+        for (int p = 0; p < 5; ++p) tot += hc[p];
+      }
+      uint32_t inc = tot;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const uint32_t nn = __shfl_up_sync(0xffffffffu, inc, o);
@@ -844,36 +989,21 @@ __global__ void __launch_bounds__(kBThreads, 1) k_banded(const BandRunArgs A, ui
       }
       if (lane == 31) s_wsum[warp] = inc;
       __syncthreads();
-      uint32_t off = inc - mine, n = 0;
-      for (int w = 0; w < kBWarps; ++w) {
-        if (w < warp) off += s_wsum[w];
-        n += s_wsum[w];
-      }
-      if (n > (uint32_t)kBTileCap || ng > (uint32_t)kBGateCap) {
-        if (tid == 0) berr(a.err, item, kErrTileOverflow);
-        __syncthreads();
-        continue;
-      }
-      for (int h = 0; h < 2; ++h) {
-        const uint32_t gi = (uint32_t)tid * 2 + h;
-        if (gi < ng) {
-          const GateRun gr = light ? A.grun_l[u0 + gi] : A.grun_h[u0 + gi];
-          BSlot S;
-          bslot_from(S, gr, st2[h]);
-          uint32_t pos = off;
-          for (int p = 0; p < 5; ++p) {
-            S.st[p] = (uint16_t)pos;
-            S.len[p] = (uint16_t)cnt2[h][p];
-            pos += cnt2[h][p];
-          }
-          X.slots[gi] = S;
-          X.sgate[gi] = gr.gate;
+      uint32_t off = inc - tot;
+      for (int w = 0; w < warp; ++w) off += s_wsum[w];
+      if ((uint32_t)tid < ng) {
+        const GateRun gr = grun[tid];
+        BSlot S;
+        bslot_from(S, gr, state);
+        uint32_t pos = off;
+#pragma unroll
+        for (int p = 0; p < 5; ++p) {
+          S.st[p] = (uint16_t)pos;
+          S.len[p] = (uint16_t)hc[p];
+          pos += hc[p];
         }
-        off += tot2[h];
-      }
-      for (uint32_t i = tid; i < n; i += kBThreads) {
-        X.ts[i] = A.L.bt[e0 + i];
-        X.ss[i] = A.L.bs[e0 + i];
+        X.slots[tid] = S;
+        X.sgate[tid] = gr.gate;
       }
       __syncthreads();
       for (uint32_t gi = warp; gi < ng; gi += kBWarps) {
@@ -882,18 +1012,20 @@ __global__ void __launch_bounds__(kBThreads, 1) k_banded(const BandRunArgs A, ui
         const int b0 = S.st[0], b1 = S.st[k] + S.len[k];
         for (int e = b0 + lane; e < b1; e += 32) {
           int p = 0;
-          for (int q = 1; q <= k; ++q) p += (e >= (int)S.st[q]) ? 1 : 0;
+          for (int qq = 1; qq <= k; ++qq) p += (e >= (int)S.st[qq]) ? 1 : 0;
           X.tag[e] = (uint16_t)((gi << 3) | (uint32_t)p);
         }
       }
       __syncthreads();
       for (uint32_t e = tid; e < n; e += kBThreads) {
         const uint32_t tg = X.tag[e];
-        bevent<kPow2, kDebug>(A, X, (int)(tg >> 3), (int)(tg & 7u), (int)e, false, 0.f, 0.f, acc);
+        bevent<kPow2, kDebug>(A, X, ts, ss, (int)(tg >> 3), (int)(tg & 7u), (int)e, false, 0.f, 0.f, acc);
       }
       __syncthreads();
     } else {
       // ---------------- one big heavy unit: stream it in event-count windows
+      float* wts = reinterpret_cast<float*>(stage);
+      float* wss = reinterpret_cast<float*>(stage + kStTs);
       const HeavyRec hr = A.L.hrec[(uint64_t)band * A.L.n_heavy + it.first];
       const GateRun gr = A.grun_h[it.first];
       const int k = (int)((gr.packed >> 16) & 15u);
@@ -949,27 +1081,27 @@ __global__ void __launch_bounds__(kBThreads, 1) k_banded(const BandRunArgs A, ui
           const uint64_t nx = hs.cur[tid] + S.len[tid];
           hs.bound[tid] = nx < hs.end[tid] ? A.L.bt[nx] : FLT_MAX;
         }
-        const int n = S.st[k] + S.len[k];
-        for (int i = tid; i < n; i += kBThreads) {
+        const int nw = S.st[k] + S.len[k];
+        for (int i = tid; i < nw; i += kBThreads) {
           int p = 0;
-          for (int q = 1; q <= k; ++q) p += (i >= (int)S.st[q]) ? 1 : 0;
+          for (int qq = 1; qq <= k; ++qq) p += (i >= (int)S.st[qq]) ? 1 : 0;
           const uint64_t ge = hs.cur[p] + (uint64_t)(i - (int)S.st[p]);
-          X.ts[i] = A.L.bt[ge];
-          X.ss[i] = A.L.bs[ge];
+          wts[i] = A.L.bt[ge];
+          wss[i] = A.L.bs[ge];
           X.tag[i] = (uint16_t)p;
         }
         __syncthreads();
         if (tid <= k) {
           float tau = FLT_MAX;
-          for (int q = 0; q <= k; ++q) tau = fminf(tau, hs.bound[q]);
+          for (int qq = 0; qq <= k; ++qq) tau = fminf(tau, hs.bound[qq]);
           // events at or after the horizon wait for the next window; a
           // timestamp group is never split
-          if (tau != FLT_MAX) S.len[tid] = (uint16_t)lb_f(X.ts + S.st[tid], S.len[tid], tau);
+          if (tau != FLT_MAX) S.len[tid] = (uint16_t)lb_f(wts + S.st[tid], S.len[tid], tau);
         }
         __syncthreads();
-        for (int i = tid; i < n; i += kBThreads) {
+        for (int i = tid; i < nw; i += kBThreads) {
           const int p = X.tag[i];
-          bevent<kPow2, kDebug>(A, X, 0, p, i, hs.has_prev[p] != 0, hs.prev_t[p], hs.prev_s[p], acc);
+          bevent<kPow2, kDebug>(A, X, wts, wss, 0, p, i, hs.has_prev[p] != 0, hs.prev_t[p], hs.prev_s[p], acc);
         }
         __syncthreads();
         if (tid == 0) {
@@ -977,8 +1109,8 @@ __global__ void __launch_bounds__(kBThreads, 1) k_banded(const BandRunArgs A, ui
           for (int p = 0; p <= k; ++p) {
             const uint32_t m = S.len[p];
             if (m > 0) {
-              hs.prev_t[p] = X.ts[S.st[p] + m - 1];
-              hs.prev_s[p] = X.ss[S.st[p] + m - 1];
+              hs.prev_t[p] = wts[S.st[p] + m - 1];
+              hs.prev_s[p] = wss[S.st[p] + m - 1];
               hs.has_prev[p] = 1;
               hs.cur[p] += m;
               hs.pre ^= (uint8_t)((m & 1u) << p);

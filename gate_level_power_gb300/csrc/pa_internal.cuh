@@ -127,10 +127,10 @@ struct RunArgs {
 constexpr int kLightPinMax = 31;       // per-pin events per band of a light gate
 constexpr int kLightBlock = 8;         // light gates per partition block
 constexpr int kBandMaxBands = 64;
-constexpr uint32_t kBandDefaultCycles = 6144;
-constexpr uint32_t kBandMaxCycles = 6144;  // shared-memory histogram capacity (cycles)
+constexpr uint32_t kBandDefaultCycles = 4096;
+constexpr uint32_t kBandMaxCycles = 4096;  // shared-memory histogram capacity (cycles)
 constexpr int kBTileCap = 4096;        // events per banded tile
-constexpr int kBGateCap = 1024;        // gates per banded tile (multiple of kLightBlock)
+constexpr int kBGateCap = 512;         // gates per banded tile (multiple of kLightBlock)
 constexpr uint32_t kBTileTarget = 2560;  // bucket size; + one light block (<= 8 * 155) stays <= kBTileCap
 constexpr uint32_t kBUnitSmall = kBTileCap - kBTileTarget;  // heavy units up to this share tiles
 
@@ -149,11 +149,14 @@ struct __align__(16) GateRun {
   uint32_t gate;
 };
 
-struct BandItem {
+struct __align__(16) BandItem {
   uint32_t band;
   uint32_t kind;   // 0 light tile, 1 heavy tile, 2 streamed heavy unit
   uint32_t first;  // light block / heavy rank
   uint32_t last;   // exclusive
+  uint64_t e0;     // first event in the banded arrays
+  uint32_t n;      // events
+  uint32_t pad;
 };
 
 struct BandLayout {

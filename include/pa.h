@@ -235,7 +235,7 @@ int pa_load_events(pa_ctx *ctx, const pa_events *ev);
  * banded kernel, which keeps each band's cycle bins in shared memory instead of
  * adding every event to global memory; other clocks use the unbanded kernel.
  * Results agree with the unbanded path to floating-point summation order.
- *   band_cycles  cycles per band; 0 = default 6144; at most 6144
+ *   band_cycles  cycles per band; 0 = default 4096; at most 4096
  * The events may span at most 64 bands. Memory: a second copy of the times and
  * slews (8 bytes per event) and about 4 bytes per (band, gate).
  * Errors: PA_ERR_ORDER (no events loaded), PA_ERR_ARG (t_clk_ns not > 0,

