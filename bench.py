@@ -334,8 +334,11 @@ def run_ours(args):
     stream = torch.cuda.Stream(device=local)
     pa = glp.PowerAnalyzer(local, stream.cuda_stream)
     pa.load_workload(w)
+    build_ms = None
     if args.banded:
+        t0 = time.perf_counter()
         pa.build_bands(w.t_clk_ns, args.band_cycles)
+        build_ms = (time.perf_counter() - t0) * 1e3
     wave = np.empty(N, np.float32)
     evc = np.empty(N, np.uint32)
     glc = np.empty(N, np.uint32)
@@ -425,6 +428,7 @@ def run_ours(args):
             "p_total_w": r["p_int"] + r["p_sw"] + r["p_gl"] + r["p_leak"],
             "n_tiles": r["n_tiles"], "n_heavy": r["n_heavy"],
             "path": "banded" if r["path"] == glp.PA_PATH_BANDED else "unbanded",
+            **({"build_bands_ms": build_ms} if build_ms is not None else {}),
         }
         print(json.dumps(line), flush=True)
     pa.close()

@@ -58,11 +58,12 @@ struct pa_ctx {
   DevBuf bins, part_blk, part_counts, tiles, heavy, p0_tot, p_out;
   DevBuf dbg[3], wave_tmp, cnt_tmp, chunk_sums;
 
-  // banded layout (pa_build_bands) and its per-run scratch
+  // banded layout (pa_build_bands): persistent parts, build temporaries, run scratch
   BandLayout band;
-  DevBuf b_bt, b_bs, b_lrec, b_hrec, b_lblk, b_lgate, b_hgate;
-  DevBuf b_cnt, b_heavy, b_rank, b_totals, b_scan, b_usize, b_uoff;
-  DevBuf b_grun, b_items, b_item_n, b_item_ev, b_flags, b_pos;
+  uint32_t band_windowed = 0;  // gates cut into windows narrower than a band
+  DevBuf b_bt, b_bs, b_urec, b_ugate, b_items, b_big;
+  DevBuf b_bigf, b_cnt, b_evc, b_ubase, b_ebase, b_uband, b_uoff, b_flags, b_ipos, b_scan, b_counters;
+  DevBuf b_part;
   DevBuf scratch_small;
 };
 
@@ -228,10 +229,13 @@ int check_run(pa_ctx* c, const pa_run_params* prm, const pa_result* out, const c
   return PA_OK;
 }
 
-// Launch partition -> fused kernel -> final reduction; counts are taken in
-// f32 inside the one-per-event vector reduction and the pass is repeated with
-// integer counts if a cycle reached 2^24 events. Copies outputs on success.
-int run_pass(pa_ctx* c, const RunPlan& plan, const PassBufs& B, pa_result* out, const char* who) {
+// One run: unbanded (partition -> fused kernel -> final reduction) or, with a
+// banded layout, P0 -> banded kernel (+ the unbanded kernel streaming the big
+// gates) -> final reduction. Counts are taken in f32 and the pass is repeated
+// with integer counts and fp64 bins if a cycle reached 2^24 events. Copies
+// outputs on success.
+int run_pass(pa_ctx* c, const RunPlan& plan, const PassBufs& B, pa_result* out, const char* who,
+             const BandLayout* band) {
   const uint32_t N = plan.N;
   RunArgs a;
   std::memset(&a, 0, sizeof(a));
@@ -255,7 +259,7 @@ int run_pass(pa_ctx* c, const RunPlan& plan, const PassBufs& B, pa_result* out, 
   a.part_blk = B.part_blk;
   a.part_counts = B.part_counts;
   a.tiles = B.tiles;
-  a.heavy = B.heavy;
+  a.heavy = band ? band->big : B.heavy;
   a.p0 = B.p0_tot;
   a.totals = B.p0_tot + 4;
   a.bins = B.bins;
@@ -266,25 +270,45 @@ int run_pass(pa_ctx* c, const RunPlan& plan, const PassBufs& B, pa_result* out, 
   a.dbg_state = B.dbg[0];
   a.dbg_lut = B.dbg[1];
   a.dbg_glitch = B.dbg[2];
+  BandRunArgs A;
+  if (band) {
+    A.r = a;
+    A.L = *band;
+  }
   cudaStream_t st = c->stream;
   uint32_t launches = 0;
   double p[4];
   unsigned long long key = kNoErr;
   uint32_t counts[4] = {0, 0, 0, 0};
   for (int exact = 0; exact < 2; ++exact) {
+    launches = 0;
     if (plan.timing) CUDA_TRY(c, cudaEventRecord(c->ev[0], st));
     CUDA_TRY(c, cudaMemsetAsync(B.bins, 0, (size_t)N * sizeof(float4), st));
     if (exact) CUDA_TRY(c, cudaMemsetAsync(B.cnt_ev, 0, (size_t)N * sizeof(uint32_t), st));
     if (exact) CUDA_TRY(c, cudaMemsetAsync(B.cnt_gl, 0, (size_t)N * sizeof(uint32_t), st));
     CUDA_TRY(c, cudaMemsetAsync(B.p0_tot, 0, 8 * sizeof(double), st));
-    CUDA_TRY(c, cudaMemsetAsync(B.part_counts, 0, 4 * sizeof(uint32_t), st));
     CUDA_TRY(c, cudaMemsetAsync(c->err_word.p, 0xff, sizeof(unsigned long long), st));
-    CUDA_TRY(c, launch_partition(a, plan.nblk, st));
-    launches += plan.nblk ? 3 : 0;
+    if (band) {
+      // the unbanded kernel's work list: no tiles, the big gates as heavy gates
+      const uint32_t part[4] = {0, band->n_big, 0, 0};
+      CUDA_TRY(c, cudaMemcpyAsync(B.part_counts, part, sizeof(part), cudaMemcpyHostToDevice, st));
+      CUDA_TRY(c, band_p0(a, st));
+      launches += plan.G ? 1 : 0;
+    } else {
+      CUDA_TRY(c, cudaMemsetAsync(B.part_counts, 0, 4 * sizeof(uint32_t), st));
+      CUDA_TRY(c, launch_partition(a, plan.nblk, st));
+      launches += plan.nblk ? 3 : 0;
+    }
     if (plan.timing) CUDA_TRY(c, cudaEventRecord(c->ev[1], st));
-    const int grid = c->sm_count * fused_blocks_per_sm(plan.pow2, plan.debug, exact != 0);
-    CUDA_TRY(c, launch_fused(a, grid, plan.pow2, plan.debug, exact != 0, st));
-    launches += 1;
+    if (band) {
+      CUDA_TRY(c, band_fused(A, c->sm_count, plan.debug, exact != 0, st));
+      launches += band->n_items ? 1 : 0;
+    }
+    if (!band || band->n_big) {
+      const int grid = c->sm_count * fused_blocks_per_sm(plan.pow2, plan.debug, exact != 0);
+      CUDA_TRY(c, launch_fused(a, grid, plan.pow2, plan.debug, exact != 0, st));
+      launches += 1;
+    }
     if (plan.timing) CUDA_TRY(c, cudaEventRecord(c->ev[2], st));
     CUDA_TRY(c, launch_final_reduce(a, plan.Td, plan.t_max, B.wave, B.p_out, exact != 0, st));
     launches += 2;
@@ -311,10 +335,15 @@ int run_pass(pa_ctx* c, const RunPlan& plan, const PassBufs& B, pa_result* out, 
   out->p_gl_w = p[2];
   out->p_leak_w = p[3];
   out->t_max_ns = plan.t_max;
-  out->n_tiles = counts[0];
-  out->n_heavy = counts[1];
+  if (band) {
+    out->n_tiles = band->n_items;
+    out->n_heavy = c->band_windowed + band->n_big;
+  } else {
+    out->n_tiles = counts[0];
+    out->n_heavy = counts[1];
+  }
   out->kernel_launches = launches;
-  out->path = PA_PATH_UNBANDED;
+  out->path = band ? PA_PATH_BANDED : PA_PATH_UNBANDED;
   if (plan.timing) {
     cudaEventElapsedTime(&out->ms_partition, c->ev[0], c->ev[1]);
     cudaEventElapsedTime(&out->ms_fused, c->ev[1], c->ev[2]);
@@ -323,119 +352,8 @@ int run_pass(pa_ctx* c, const RunPlan& plan, const PassBufs& B, pa_result* out, 
   }
   return PA_OK;
 }
-
 
 bool same_bits(float a, float b) { return std::memcmp(&a, &b, sizeof(float)) == 0; }
-
-// The banded pass: per-run gate records (and P0), item list, banded fused
-// kernel, final reduction of the fp64 / u32 bins. Copies outputs on success.
-int run_banded(pa_ctx* c, const RunPlan& plan, pa_result* out) {
-  const uint32_t N = plan.N, G = plan.G;
-  const BandLayout& L = c->band;
-  const uint32_t max_items = band_max_items(L);
-  PA_TRY(dreserve(c, c->bins, (size_t)N * 16));
-  PA_TRY(dreserve(c, c->cnt_tmp, (size_t)N * 2 * sizeof(uint32_t)));
-  PA_TRY(dreserve(c, c->chunk_sums, (size_t)reduce_chunks(N) * sizeof(double)));
-  PA_TRY(dreserve(c, c->p0_tot, 8 * sizeof(double)));
-  PA_TRY(dreserve(c, c->p_out, 4 * sizeof(double)));
-  PA_TRY(dreserve(c, c->wave_tmp, (size_t)N * sizeof(float)));
-  PA_TRY(dreserve(c, c->b_grun, ((size_t)L.n_light + L.n_heavy + 1) * sizeof(GateRun)));
-  PA_TRY(dreserve(c, c->b_items, (size_t)max_items * sizeof(BandItem)));
-  PA_TRY(dreserve(c, c->b_item_n, (size_t)max_items * sizeof(uint32_t)));
-  PA_TRY(dreserve(c, c->b_item_ev, ((size_t)max_items + 1) * sizeof(uint64_t)));
-  PA_TRY(dreserve(c, c->b_flags, (size_t)max_items * sizeof(uint32_t)));
-  PA_TRY(dreserve(c, c->b_pos, ((size_t)max_items + 1) * sizeof(uint64_t)));
-  PA_TRY(dreserve(c, c->b_scan, ((size_t)band_scan_blocks(std::max<uint64_t>(max_items, G)) + 1) * sizeof(uint64_t)));
-  if (plan.debug)
-    for (int i = 0; i < 3; ++i) PA_TRY(dreserve(c, c->dbg[i], c->n_events));
-  BandRunArgs A;
-  std::memset(&A, 0, sizeof(A));
-  RunArgs& a = A.r;
-  a.cells = (const CellDesc*)c->cells.p;
-  a.n_cells = c->n_cells;
-  a.lut = (const float*)c->lut.p;
-  a.leak = (const float*)c->leak.p;
-  a.gates = (const GateRec*)c->gates.p;
-  a.n_gates = G;
-  a.pin_off = (const uint64_t*)c->pin_off.p;
-  a.gate_off = (const uint64_t*)c->gate_off.p;
-  a.t = (const float*)c->t.p;
-  a.s = (const float*)c->s.p;
-  a.t_clk = plan.T;
-  a.inv_t_clk = plan.pow2 ? 1.0f / plan.T : 0.f;
-  a.t_max_f = (float)plan.t_max;
-  a.half_vdd2 = (float)(0.5 * plan.vdd * plan.vdd);
-  a.n_cycles = N;
-  a.p0 = (double*)c->p0_tot.p;
-  a.totals = (double*)c->p0_tot.p + 4;
-  a.bins = (float4*)c->bins.p;
-  a.cnt_ev = (uint32_t*)c->cnt_tmp.p;
-  a.cnt_gl = (uint32_t*)c->cnt_tmp.p + N;
-  a.chunk_sums = (double*)c->chunk_sums.p;
-  a.err = (unsigned long long*)c->err_word.p;
-  if (plan.debug) {
-    a.dbg_state = (uint8_t*)c->dbg[0].p;
-    a.dbg_lut = (uint8_t*)c->dbg[1].p;
-    a.dbg_glitch = (uint8_t*)c->dbg[2].p;
-  }
-  A.L = L;
-  A.grun_l = (GateRun*)c->b_grun.p;
-  A.grun_h = (GateRun*)c->b_grun.p + L.n_light;
-  A.items = (BandItem*)c->b_items.p;
-  A.item_ev = (uint64_t*)c->b_item_ev.p;
-  A.max_items = max_items;
-  cudaStream_t st = c->stream;
-  if (plan.timing) CUDA_TRY(c, cudaEventRecord(c->ev[0], st));
-  CUDA_TRY(c, cudaMemsetAsync(c->bins.p, 0, (size_t)N * 16, st));
-  CUDA_TRY(c, cudaMemsetAsync(c->cnt_tmp.p, 0, (size_t)N * 2 * sizeof(uint32_t), st));
-  CUDA_TRY(c, cudaMemsetAsync(c->p0_tot.p, 0, 8 * sizeof(double), st));
-  CUDA_TRY(c, cudaMemsetAsync(c->err_word.p, 0xff, sizeof(unsigned long long), st));
-  CUDA_TRY(c, band_gate_run(A, st));
-  uint32_t items[2] = {0, 0};
-  CUDA_TRY(c, band_partition(A, (uint32_t*)c->b_flags.p, (uint64_t*)c->b_pos.p, (uint64_t*)c->b_scan.p,
-                             (uint32_t*)c->b_item_n.p, items, st));
-  const uint32_t n_items = items[0] + items[1];
-  uint32_t launches = 1 + (L.n_lblk ? 5 : 0) + (L.n_heavy ? 5 : 0) + 3;
-  if (plan.timing) CUDA_TRY(c, cudaEventRecord(c->ev[1], st));
-  CUDA_TRY(c, band_fused(A, n_items, c->sm_count, plan.debug, st));
-  launches += n_items ? 1 : 0;
-  if (plan.timing) CUDA_TRY(c, cudaEventRecord(c->ev[2], st));
-  CUDA_TRY(c, launch_final_reduce(a, plan.Td, plan.t_max, (float*)c->wave_tmp.p, (double*)c->p_out.p, true, st));
-  launches += 2;
-  if (plan.timing) CUDA_TRY(c, cudaEventRecord(c->ev[3], st));
-  double p[4];
-  unsigned long long key = kNoErr;
-  CUDA_TRY(c, cudaMemcpyAsync(p, c->p_out.p, sizeof(p), cudaMemcpyDeviceToHost, st));
-  CUDA_TRY(c, cudaMemcpyAsync(&key, c->err_word.p, sizeof(key), cudaMemcpyDeviceToHost, st));
-  CUDA_TRY(c, cudaStreamSynchronize(st));
-  if (key != kNoErr) return map_dev_err(c, key, "pa_run");
-  const cudaMemcpyKind dk = out->out_mem == PA_MEM_HOST ? cudaMemcpyDeviceToHost : cudaMemcpyDeviceToDevice;
-  if (out->waveform_w) CUDA_TRY(c, cudaMemcpyAsync(out->waveform_w, c->wave_tmp.p, (size_t)N * sizeof(float), dk, st));
-  if (out->event_count) CUDA_TRY(c, cudaMemcpyAsync(out->event_count, a.cnt_ev, (size_t)N * 4, dk, st));
-  if (out->glitch_count) CUDA_TRY(c, cudaMemcpyAsync(out->glitch_count, a.cnt_gl, (size_t)N * 4, dk, st));
-  if (plan.debug && c->n_events) {
-    uint8_t* dst[3] = {out->state_pre, out->lut_ij, out->is_glitch};
-    for (int i = 0; i < 3; ++i)
-      if (dst[i]) CUDA_TRY(c, cudaMemcpyAsync(dst[i], c->dbg[i].p, c->n_events, dk, st));
-  }
-  CUDA_TRY(c, cudaStreamSynchronize(st));
-  out->p_int_w = p[0];
-  out->p_sw_w = p[1];
-  out->p_gl_w = p[2];
-  out->p_leak_w = p[3];
-  out->t_max_ns = plan.t_max;
-  out->n_tiles = items[0];
-  out->n_heavy = items[1];
-  out->kernel_launches = launches;
-  out->path = PA_PATH_BANDED;
-  if (plan.timing) {
-    cudaEventElapsedTime(&out->ms_partition, c->ev[0], c->ev[1]);
-    cudaEventElapsedTime(&out->ms_fused, c->ev[1], c->ev[2]);
-    cudaEventElapsedTime(&out->ms_reduce, c->ev[2], c->ev[3]);
-    cudaEventElapsedTime(&out->ms_total, c->ev[0], c->ev[3]);
-  }
-  return PA_OK;
-}
 
 }  // namespace
 
@@ -501,10 +419,10 @@ void pa_destroy(pa_ctx* c) {
                    &c->value_tmp, &c->err_word, &c->tmax_bits, &c->bins, &c->part_blk,
                    &c->part_counts, &c->tiles, &c->heavy, &c->p0_tot, &c->p_out, &c->dbg[0],
                    &c->dbg[1], &c->dbg[2], &c->wave_tmp, &c->cnt_tmp, &c->scratch_small,
-                   &c->chunk_sums, &c->b_bt, &c->b_bs, &c->b_lrec, &c->b_hrec, &c->b_lblk,
-                   &c->b_lgate, &c->b_hgate, &c->b_cnt, &c->b_heavy, &c->b_rank, &c->b_totals,
-                   &c->b_scan, &c->b_usize, &c->b_uoff, &c->b_grun, &c->b_items, &c->b_item_n,
-                   &c->b_item_ev, &c->b_flags, &c->b_pos};
+                   &c->chunk_sums, &c->b_bt, &c->b_bs, &c->b_urec, &c->b_ugate, &c->b_items,
+                   &c->b_big, &c->b_bigf, &c->b_cnt, &c->b_evc, &c->b_ubase, &c->b_ebase,
+                   &c->b_uband, &c->b_uoff, &c->b_flags, &c->b_ipos, &c->b_scan, &c->b_counters,
+                   &c->b_part};
   for (DevBuf* b : all) dfree(*b);
   for (auto& e : c->ev)
     if (e) cudaEventDestroy(e);
@@ -680,7 +598,7 @@ int pa_run(pa_ctx* c, const pa_run_params* prm, pa_result* out) {
   RunPlan plan;
   PA_TRY(check_run(c, prm, out, "pa_run", &plan));
   CUDA_TRY(c, cudaSetDevice(c->device));
-  if (c->band.built && same_bits(c->band.t_clk, plan.T)) return run_banded(c, plan, out);
+  const bool banded = c->band.built && same_bits(c->band.t_clk, plan.T);
   const uint32_t N = plan.N, G = plan.G;
   PassBufs B;
   PA_TRY(dreserve(c, c->bins, (size_t)N * sizeof(float4)));
@@ -708,7 +626,7 @@ int pa_run(pa_ctx* c, const pa_run_params* prm, pa_result* out) {
   B.cnt_ev = (uint32_t*)c->cnt_tmp.p;
   B.cnt_gl = (uint32_t*)c->cnt_tmp.p + N;
   for (int i = 0; i < 3; ++i) B.dbg[i] = plan.debug ? (uint8_t*)c->dbg[i].p : nullptr;
-  return run_pass(c, plan, B, out, "pa_run");
+  return run_pass(c, plan, B, out, "pa_run", banded ? &c->band : nullptr);
 }
 
 }  // extern "C"
@@ -803,46 +721,49 @@ extern "C" int pa_run_noalloc(pa_ctx* c, const pa_run_params* prm, pa_result* ou
   B.dbg[0] = out->state_pre;
   B.dbg[1] = out->lut_ij;
   B.dbg[2] = out->is_glitch;
-  return run_pass(c, plan, B, out, "pa_run_noalloc");
+  return run_pass(c, plan, B, out, "pa_run_noalloc", nullptr);
 }
 
 // ----------------------------------------------------------------- pa_build_bands
 
-extern "C" int pa_build_bands(pa_ctx* c, float t_clk, uint32_t band_cycles) {
-  if (!c) return PA_ERR_ARG;
-  if (!c->has_ev) return fail(c, PA_ERR_ORDER, "pa_build_bands: events not loaded");
-  if (!(t_clk > 0.f) || !is_finite_f(t_clk)) return fail(c, PA_ERR_ARG, "pa_build_bands: t_clk_ns must be > 0");
-  const uint32_t cb = band_cycles ? band_cycles : kBandDefaultCycles;
-  if (cb > kBandMaxCycles)
-    return fail(c, PA_ERR_ARG, "pa_build_bands: band_cycles %u exceeds %u", cb, kBandMaxCycles);
-  CUDA_TRY(c, cudaSetDevice(c->device));
-  c->band.built = false;
-  const uint64_t E = c->n_events, P = c->n_pins;
+namespace {
+
+// Read one device word back (after the stream's earlier work).
+template <typename T>
+int read_back(pa_ctx* c, const void* src, T* dst) {
+  CUDA_TRY(c, cudaMemcpyAsync(dst, src, sizeof(T), cudaMemcpyDeviceToHost, c->stream));
+  CUDA_TRY(c, cudaStreamSynchronize(c->stream));
+  return PA_OK;
+}
+
+int check_build_err(pa_ctx* c) {
+  unsigned long long key = kNoErr;
+  PA_TRY(read_back(c, c->err_word.p, &key));
+  if (key != kNoErr) return map_dev_err(c, key, "pa_build_bands");
+  return PA_OK;
+}
+
+void free_build_temps(pa_ctx* c) {
+  DevBuf* tmp[] = {&c->b_bigf, &c->b_cnt, &c->b_evc, &c->b_ubase, &c->b_ebase, &c->b_uband,
+                   &c->b_uoff, &c->b_flags, &c->b_ipos, &c->b_scan, &c->b_counters};
+  for (DevBuf* b : tmp) dfree(*b);
+}
+
+int build_bands(pa_ctx* c, float t_clk, uint32_t cb) {
+  const uint64_t E = c->n_events;
   const uint32_t G = c->n_gates;
   const float c_last = E ? std::floor(c->t_last / t_clk) : 0.f;  // fp32 division, as the kernels take it
   if (!(c_last < 4294967040.f)) return fail(c, PA_ERR_ARG, "pa_build_bands: events span too many cycles");
   const uint32_t nb = (uint32_t)c_last / cb + 1;
-  if (nb > (uint32_t)kBandMaxBands)
-    return fail(c, PA_ERR_ARG, "pa_build_bands: events span %u bands of %u cycles; at most %d (use larger bands)",
-                nb, cb, kBandMaxBands);
-  const uint64_t nu = (uint64_t)nb * G;
-  const size_t ev_bytes = ((E + 64) & ~(size_t)15) * sizeof(float);
-  PA_TRY(dreserve(c, c->b_bt, ev_bytes));
-  PA_TRY(dreserve(c, c->b_bs, ev_bytes));
-  PA_TRY(dreserve(c, c->b_lgate, ((size_t)G + 1) * sizeof(uint32_t)));
-  PA_TRY(dreserve(c, c->b_hgate, ((size_t)G + 1) * sizeof(uint32_t)));
-  PA_TRY(dreserve(c, c->b_cnt, (P * nb + 1) * sizeof(uint32_t)));
-  PA_TRY(dreserve(c, c->b_heavy, (size_t)G + 1));
-  PA_TRY(dreserve(c, c->b_rank, ((size_t)G + 1) * sizeof(uint32_t)));
-  PA_TRY(dreserve(c, c->b_totals, 4 * sizeof(uint32_t)));
-  PA_TRY(dreserve(c, c->b_scan, ((size_t)band_scan_blocks(std::max<uint64_t>(nu, G)) + 1) * sizeof(uint64_t)));
-  PA_TRY(dreserve(c, c->b_usize, (nu + 1) * sizeof(uint32_t)));
-  PA_TRY(dreserve(c, c->b_uoff, (nu + 1) * sizeof(uint64_t)));
+  if (nb > kBandMaxBands)
+    return fail(c, PA_ERR_ARG, "pa_build_bands: events span %u bands of %u cycles; at most %u", nb, cb, kBandMaxBands);
+  uint32_t mb = 0;
+  while ((1u << mb) < cb) ++mb;
+  const uint64_t nbg = (uint64_t)nb * G;
   BandBuildArgs a;
   std::memset(&a, 0, sizeof(a));
   a.gates = (const GateRec*)c->gates.p;
   a.n_gates = G;
-  a.n_pins = P;
   a.n_events = E;
   a.pin_off = (const uint64_t*)c->pin_off.p;
   a.t = (const float*)c->t.p;
@@ -850,40 +771,95 @@ extern "C" int pa_build_bands(pa_ctx* c, float t_clk, uint32_t band_cycles) {
   a.t_clk = t_clk;
   a.pow2 = is_pow2(t_clk);
   a.inv_t_clk = a.pow2 ? 1.0f / t_clk : 0.f;
-  a.band_cycles = cb;
+  a.mb = mb;
   a.n_bands = nb;
-  a.cnt = (uint32_t*)c->b_cnt.p;
-  a.heavy = (uint8_t*)c->b_heavy.p;
-  a.rank = (uint32_t*)c->b_rank.p;
-  a.totals = (uint32_t*)c->b_totals.p;
-  a.unit_size = (uint32_t*)c->b_usize.p;
-  a.unit_off = (uint64_t*)c->b_uoff.p;
-  a.scan_blk = (uint64_t*)c->b_scan.p;
   a.err = (unsigned long long*)c->err_word.p;
-  a.L.bt = (float*)c->b_bt.p;
-  a.L.bs = (float*)c->b_bs.p;
-  a.L.lgate = (uint32_t*)c->b_lgate.p;
-  a.L.hgate = (uint32_t*)c->b_hgate.p;
-  a.L.t_clk = t_clk;
-  a.L.band_cycles = cb;
-  a.L.n_bands = nb;
-  CUDA_TRY(c, band_build_phase1(a, c->stream));
-  uint32_t tot[2] = {0, 0};
-  CUDA_TRY(c, cudaMemcpyAsync(tot, a.totals, sizeof(tot), cudaMemcpyDeviceToHost, c->stream));
+  BandLayout& L = a.L;
+  L.t_clk = t_clk;
+  L.band_cycles = cb;
+  L.mb = mb;
+  L.n_bands = nb;
+  // count: units and events per (band, gate), big gates
+  PA_TRY(dreserve(c, c->b_big, ((size_t)G + 1) * sizeof(uint32_t)));
+  PA_TRY(dreserve(c, c->b_counters, 4 * sizeof(uint32_t)));
+  PA_TRY(dreserve(c, c->b_bigf, (size_t)G + 1));
+  PA_TRY(dreserve(c, c->b_cnt, (nbg + 1) * sizeof(uint32_t)));
+  PA_TRY(dreserve(c, c->b_evc, (nbg + 1) * sizeof(uint32_t)));
+  PA_TRY(dreserve(c, c->b_ubase, (nbg + 1) * sizeof(uint64_t)));
+  PA_TRY(dreserve(c, c->b_ebase, (nbg + 1) * sizeof(uint64_t)));
+  PA_TRY(dreserve(c, c->b_scan, ((size_t)band_scan_blocks(nbg) + 1) * sizeof(uint64_t)));
+  L.big = (uint32_t*)c->b_big.p;
+  a.counters = (uint32_t*)c->b_counters.p;
+  a.bigf = (uint8_t*)c->b_bigf.p;
+  a.cnt_gb = (uint32_t*)c->b_cnt.p;
+  a.evc_gb = (uint32_t*)c->b_evc.p;
+  a.ubase = (uint64_t*)c->b_ubase.p;
+  a.ebase = (uint64_t*)c->b_ebase.p;
+  a.scan_blk = (uint64_t*)c->b_scan.p;
+  CUDA_TRY(c, cudaMemsetAsync(c->err_word.p, 0xff, sizeof(unsigned long long), c->stream));
+  CUDA_TRY(c, band_build_count(a, c->stream));
+  uint64_t n_units = 0, n_ev = 0;
+  uint32_t counters[4] = {0, 0, 0, 0};
+  CUDA_TRY(c, cudaMemcpyAsync(&n_units, a.ubase + nbg, sizeof(n_units), cudaMemcpyDeviceToHost, c->stream));
+  CUDA_TRY(c, cudaMemcpyAsync(&n_ev, a.ebase + nbg, sizeof(n_ev), cudaMemcpyDeviceToHost, c->stream));
+  CUDA_TRY(c, cudaMemcpyAsync(counters, a.counters, sizeof(counters), cudaMemcpyDeviceToHost, c->stream));
   CUDA_TRY(c, cudaStreamSynchronize(c->stream));
-  a.L.n_light = tot[0];
-  a.L.n_heavy = tot[1];
-  a.L.n_lblk = (tot[0] + kLightBlock - 1) / kLightBlock;
-  // + 8: staged copies round record ranges up to 16 bytes
-  PA_TRY(dreserve(c, c->b_lrec, ((size_t)nb * a.L.n_light + 8) * sizeof(uint32_t)));
-  PA_TRY(dreserve(c, c->b_hrec, ((size_t)nb * a.L.n_heavy + 1) * sizeof(HeavyRec)));
-  PA_TRY(dreserve(c, c->b_lblk, ((size_t)nb * (a.L.n_lblk + 1) + 1) * sizeof(uint64_t)));
-  a.L.lrec = (uint32_t*)c->b_lrec.p;
-  a.L.hrec = (HeavyRec*)c->b_hrec.p;
-  a.L.lblk = (uint64_t*)c->b_lblk.p;
-  CUDA_TRY(c, band_build_phase2(a, c->stream));
-  CUDA_TRY(c, cudaStreamSynchronize(c->stream));
-  a.L.built = true;
-  c->band = a.L;
+  PA_TRY(check_build_err(c));
+  if (n_units >= 0xFFFFFFF0ull) return fail(c, PA_ERR_ARG, "pa_build_bands: too many units (%llu)", (unsigned long long)n_units);
+  L.n_units = (uint32_t)n_units;
+  L.n_ev = n_ev;
+  L.n_big = counters[0];
+  // write: records, event copy, item heads
+  const size_t nu = (size_t)n_units;
+  const size_t ev_bytes = ((n_ev + 64) & ~(size_t)15) * sizeof(float);
+  PA_TRY(dreserve(c, c->b_urec, (nu + 2) * sizeof(uint2)));
+  PA_TRY(dreserve(c, c->b_ugate, (nu + 1) * sizeof(uint32_t)));
+  PA_TRY(dreserve(c, c->b_uband, (nu + 1) * sizeof(uint32_t)));
+  PA_TRY(dreserve(c, c->b_uoff, (nu + 1) * sizeof(uint64_t)));
+  PA_TRY(dreserve(c, c->b_flags, (nu + 1) * sizeof(uint32_t)));
+  PA_TRY(dreserve(c, c->b_ipos, (nu + 1) * sizeof(uint64_t)));
+  PA_TRY(dreserve(c, c->b_bt, ev_bytes));
+  PA_TRY(dreserve(c, c->b_bs, ev_bytes));
+  PA_TRY(dreserve(c, c->b_scan, ((size_t)band_scan_blocks(std::max<uint64_t>(nbg, nu)) + 1) * sizeof(uint64_t)));
+  L.urec = (uint2*)c->b_urec.p;
+  L.ugate = (uint32_t*)c->b_ugate.p;
+  L.bt = (float*)c->b_bt.p;
+  L.bs = (float*)c->b_bs.p;
+  a.uband = (uint32_t*)c->b_uband.p;
+  a.uoff = (uint64_t*)c->b_uoff.p;
+  a.flags = (uint32_t*)c->b_flags.p;
+  a.ipos = (uint64_t*)c->b_ipos.p;
+  a.scan_blk = (uint64_t*)c->b_scan.p;
+  CUDA_TRY(c, band_build_write(a, c->stream));
+  uint64_t n_items = 0;
+  PA_TRY(read_back(c, a.ipos + nu, &n_items));
+  PA_TRY(check_build_err(c));
+  L.n_items = (uint32_t)n_items;
+  // items
+  PA_TRY(dreserve(c, c->b_items, ((size_t)n_items + 1) * sizeof(BandItem)));
+  L.items = (BandItem*)c->b_items.p;
+  CUDA_TRY(c, band_build_items(a, c->stream));
+  PA_TRY(check_build_err(c));
+  L.built = true;
+  c->band = L;
+  c->band_windowed = counters[1];
   return PA_OK;
+}
+
+}  // namespace
+
+extern "C" int pa_build_bands(pa_ctx* c, float t_clk, uint32_t band_cycles) {
+  if (!c) return PA_ERR_ARG;
+  if (!c->has_ev) return fail(c, PA_ERR_ORDER, "pa_build_bands: events not loaded");
+  if (!(t_clk > 0.f) || !is_finite_f(t_clk)) return fail(c, PA_ERR_ARG, "pa_build_bands: t_clk_ns must be > 0");
+  const uint32_t cb = band_cycles ? band_cycles : kBandDefaultCycles;
+  if (cb > kBandMaxCycles || (cb & (cb - 1)) != 0)
+    return fail(c, PA_ERR_ARG, "pa_build_bands: band_cycles %u is not a power of two <= %u", cb, kBandMaxCycles);
+  if (c->n_cells > (uint32_t)kSmemCells)
+    return fail(c, PA_ERR_ARG, "pa_build_bands: %u cells; the banded kernel holds at most %d", c->n_cells, kSmemCells);
+  CUDA_TRY(c, cudaSetDevice(c->device));
+  c->band.built = false;
+  const int rc = build_bands(c, t_clk, cb);
+  free_build_temps(c);
+  return rc;
 }

@@ -3,14 +3,18 @@
 // The power step of "GPU-Accelerated Gate-Level Time-Based Power Analysis via
 // Event-Density-Aware Partitioning and Kernel Fusion" (Sections 2.4.1-2.4.2,
 // Eqs. 1-4, Figs. 2, 3 and 7) adds every event's energy to the waveform bin of
-// its clock cycle (Fig. 7's atomicAdd into w). Done with one global atomic per
-// event, a billion events are bound by the L2 atomic units. Here the events are
-// first regrouped into bands of consecutive cycles (a load-time layout for one
-// clock period): work items never leave their band, so each CTA keeps the
-// band's cycle bins in shared memory and flushes them to global memory once per
-// band it touches. Within a band the per-pin CSR order is kept, so the gate
-// state and glitch rules are the ones of the unbanded kernel; the state at the
-// band start travels in the per-(band, gate) record.
+// its clock cycle (Fig. 7's atomicAdd into w). With one global atomic per event
+// a billion events are bound by the L2 atomic units. Here the events are first
+// regrouped (a load-time layout for one clock period) into units: one gate's
+// events inside one aligned window of 2^m cycles, the window chosen per gate so
+// that no pin has more than 15 events in it (the role of the paper's
+// event-density-aware cycle partitioning, Figs. 5, 19 and 20: dense gates get
+// narrow windows, sparse gates one window per band). Units are stored band by
+// band, so a CTA keeps the band's cycle bins in shared memory and adds them to
+// global memory once per band with a TMA bulk reduction. Inside a unit the
+// per-pin CSR order is kept, each pin segment holds at most 15 events, and the
+// gate state before an event is the unit's start state flipped by the parities
+// of the earlier events on each pin (short searches in the staged segments).
 #include <cfloat>
 #include <cstdint>
 
@@ -30,15 +34,6 @@ template <bool kPow2>
 __device__ __forceinline__ uint32_t cyc(float t, float T, float inv_T) {
   if (kPow2) return (uint32_t)(t * inv_T);
   return (uint32_t)__fdiv_rn(t, T);
-}
-
-__device__ __forceinline__ uint32_t wscan_incl_u32(uint32_t v, int lane) {
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t n = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += n;
-  }
-  return v;
 }
 
 __device__ __forceinline__ uint64_t wscan_incl_u64(uint64_t v, int lane) {
@@ -124,6 +119,8 @@ __global__ void __launch_bounds__(256) k_scan_apply(const uint32_t* __restrict__
   if (blockIdx.x == gridDim.x - 1 && threadIdx.x == 0) out[n] = blk[gridDim.x];
 }
 
+}  // namespace
+
 cudaError_t scan_u32_to_u64(const uint32_t* in, uint64_t n, uint64_t* blk, uint64_t* out, cudaStream_t st) {
   const uint32_t nb = (uint32_t)((n + kScanBlock - 1) / kScanBlock);
   if (nb == 0) return cudaMemsetAsync(out, 0, sizeof(uint64_t), st);
@@ -133,624 +130,308 @@ cudaError_t scan_u32_to_u64(const uint32_t* in, uint64_t n, uint64_t* blk, uint6
   return cudaGetLastError();
 }
 
-}  // namespace
-
 uint32_t band_scan_blocks(uint64_t n) { return (uint32_t)((n + kScanBlock - 1) / kScanBlock) + 1; }
 
 // ------------------------------------------------------------------ layout build (load time)
-
-namespace {
-
-// Events per (pin, band): one warp per gate; the band of consecutive events of
-// a pin is non-decreasing, so a warp adds each band's share with one atomic.
-template <bool kPow2>
-__global__ void __launch_bounds__(256) k_bb_count(const BandBuildArgs a) {
-  const int lane = threadIdx.x & 31;
-  const uint64_t warp = (blockIdx.x * (uint64_t)blockDim.x + threadIdx.x) >> 5;
-  const uint64_t n_warps = ((uint64_t)gridDim.x * blockDim.x) >> 5;
-  const uint32_t nb = a.n_bands;
-  for (uint64_t g = warp; g < a.n_gates; g += n_warps) {
-    const GateRec r = a.gates[g];
-    const int k = (int)((r.init >> 16) & 0xff);
-    for (int p = 0; p <= k; ++p) {
-      const uint64_t pin = (uint64_t)r.pin_base + p;
-      const uint64_t lo = a.pin_off[pin], hi = a.pin_off[pin + 1];
-      for (uint64_t e0 = lo; e0 < hi; e0 += 32) {
-        const uint64_t e = e0 + lane;
-        const bool act = e < hi;
-        const uint32_t b = act ? cyc<kPow2>(a.t[e], a.t_clk, a.inv_t_clk) / a.band_cycles : 0xFFFFFFFFu;
-        const unsigned grp = __match_any_sync(0xffffffffu, b);
-        if (act && lane == __ffs(grp) - 1) atomicAdd(a.cnt + pin * nb + b, (uint32_t)__popc(grp));
-      }
-    }
-  }
-}
-
-// Heavy if some pin has more than kLightPinMax events in some band.
-__global__ void __launch_bounds__(256) k_bb_classify(const BandBuildArgs a) {
-  const uint32_t g = blockIdx.x * 256u + threadIdx.x;
-  if (g >= a.n_gates) return;
-  const GateRec r = a.gates[g];
-  const int k = (int)((r.init >> 16) & 0xff);
-  const uint32_t nb = a.n_bands;
-  bool heavy = false;
-  for (int p = 0; p <= k && !heavy; ++p) {
-    const uint32_t* c = a.cnt + ((uint64_t)r.pin_base + p) * nb;
-    for (uint32_t b = 0; b < nb; ++b) heavy |= c[b] > (uint32_t)kLightPinMax;
-  }
-  a.heavy[g] = heavy ? 1 : 0;
-}
-
-// Light / heavy ranks: scan of (light ? 1 : 2^32) over gates.
-__global__ void __launch_bounds__(256) k_bb_flag_sum(const BandBuildArgs a, uint64_t* blk) {
-  const uint64_t i0 = (uint64_t)blockIdx.x * kScanBlock + (uint64_t)threadIdx.x * kScanPer;
-  uint64_t s = 0;
-#pragma unroll
-  for (int i = 0; i < kScanPer; ++i)
-    if (i0 + i < a.n_gates) s += a.heavy[i0 + i] ? (1ull << 32) : 1ull;
-  uint64_t tot;
-  bscan_excl_u64(s, tot);
-  if (threadIdx.x == 0) blk[blockIdx.x] = tot;
-}
-
-__global__ void __launch_bounds__(256) k_bb_flag_apply(const BandBuildArgs a, const uint64_t* blk) {
-  const uint64_t i0 = (uint64_t)blockIdx.x * kScanBlock + (uint64_t)threadIdx.x * kScanPer;
-  uint64_t v[kScanPer];
-  uint64_t s = 0;
-#pragma unroll
-  for (int i = 0; i < kScanPer; ++i) {
-    v[i] = i0 + i < a.n_gates ? (a.heavy[i0 + i] ? (1ull << 32) : 1ull) : 0ull;
-    s += v[i];
-  }
-  uint64_t tot;
-  uint64_t off = blk[blockIdx.x] + bscan_excl_u64(s, tot);
-#pragma unroll
-  for (int i = 0; i < kScanPer; ++i) {
-    const uint64_t g = i0 + i;
-    if (g < a.n_gates) {
-      const uint32_t lr = (uint32_t)off, hr = (uint32_t)(off >> 32);
-      if (a.heavy[g]) {
-        a.rank[g] = hr;
-        a.L.hgate[hr] = (uint32_t)g;
-      } else {
-        a.rank[g] = lr;
-        a.L.lgate[lr] = (uint32_t)g;
-      }
-    }
-    off += v[i];
-  }
-  if (blockIdx.x == gridDim.x - 1 && threadIdx.x == 0) {
-    const uint64_t t = blk[gridDim.x];
-    a.totals[0] = (uint32_t)t;
-    a.totals[1] = (uint32_t)(t >> 32);
-  }
-}
-
-// Unit of (band b, gate g): position b * G + (light ? lr : n_light + hr).
-__device__ __forceinline__ uint64_t unit_pos(const BandBuildArgs& a, uint32_t g) {
-  return a.heavy[g] ? (uint64_t)a.L.n_light + a.rank[g] : (uint64_t)a.rank[g];
-}
-
-__global__ void __launch_bounds__(256) k_bb_unitsize(const BandBuildArgs a) {
-  const uint32_t g = blockIdx.x * 256u + threadIdx.x;
-  if (g >= a.n_gates) return;
-  const GateRec r = a.gates[g];
-  const int k = (int)((r.init >> 16) & 0xff);
-  const uint32_t nb = a.n_bands;
-  const uint64_t pos = unit_pos(a, g);
-  const uint32_t* c = a.cnt + (uint64_t)r.pin_base * nb;
-  for (uint32_t b = 0; b < nb; ++b) {
-    uint32_t sz = 0;
-    for (int p = 0; p <= k; ++p) sz += c[(uint64_t)p * nb + b];
-    a.unit_size[(uint64_t)b * a.n_gates + pos] = sz;
-  }
-}
-
-// Scatter: one warp per gate; lane b (and b + 32) holds band b's running
-// offset, count and count-before for the current pin.
-template <bool kPow2>
-__global__ void __launch_bounds__(256) k_bb_scatter(const BandBuildArgs a) {
-  const int lane = threadIdx.x & 31;
-  const uint64_t warp = (blockIdx.x * (uint64_t)blockDim.x + threadIdx.x) >> 5;
-  const uint64_t n_warps = ((uint64_t)gridDim.x * blockDim.x) >> 5;
-  const uint32_t nb = a.n_bands, G = a.n_gates;
-  const uint32_t b0 = (uint32_t)lane, b1 = (uint32_t)lane + 32;
-  for (uint64_t g = warp; g < G; g += n_warps) {
-    const GateRec r = a.gates[g];
-    const int k = (int)((r.init >> 16) & 0xff);
-    const bool heavy = a.heavy[g] != 0;
-    const uint64_t pos = unit_pos(a, (uint32_t)g);
-    uint64_t off0 = b0 < nb ? a.unit_off[(uint64_t)b0 * G + pos] : 0;
-    uint64_t off1 = b1 < nb ? a.unit_off[(uint64_t)b1 * G + pos] : 0;
-    const uint64_t base0 = off0, base1 = off1;
-    const uint32_t init = r.init & 0xffu;
-    uint32_t st0 = init, st1 = init, rec0 = 0, rec1 = 0;
-    for (int p = 0; p <= k; ++p) {
-      const uint64_t pin = (uint64_t)r.pin_base + p;
-      const uint32_t c0 = b0 < nb ? a.cnt[pin * nb + b0] : 0u;
-      const uint32_t c1 = b1 < nb ? a.cnt[pin * nb + b1] : 0u;
-      const uint32_t inc0 = wscan_incl_u32(c0, lane);
-      const uint32_t tot0 = __shfl_sync(0xffffffffu, inc0, 31);
-      const uint32_t inc1 = wscan_incl_u32(c1, lane) + tot0;
-      const uint32_t cum0 = inc0 - c0, cum1 = inc1 - c1;  // events of the pin in earlier bands
-      if (p < k) {
-        st0 ^= (cum0 & 1u) << p;
-        st1 ^= (cum1 & 1u) << p;
-      }
-      rec0 |= (c0 & 31u) << (5 * p);
-      rec1 |= (c1 & 31u) << (5 * p);
-      if (heavy) {
-        if (b0 < nb) a.L.hrec[(uint64_t)b0 * a.L.n_heavy + a.rank[g]].cnt[p] = c0;
-        if (b1 < nb) a.L.hrec[(uint64_t)b1 * a.L.n_heavy + a.rank[g]].cnt[p] = c1;
-      }
-      const uint64_t lo = a.pin_off[pin], hi = a.pin_off[pin + 1];
-      for (uint64_t e0 = lo; e0 < hi; e0 += 32) {
-        const uint64_t e = e0 + lane;
-        const bool act = e < hi;
-        const float t = act ? a.t[e] : 0.f;
-        const uint32_t b = act ? cyc<kPow2>(t, a.t_clk, a.inv_t_clk) / a.band_cycles : 0u;
-        const int src = (int)(b & 31u);
-        const uint32_t cum_a = __shfl_sync(0xffffffffu, cum0, src);
-        const uint32_t cum_b = __shfl_sync(0xffffffffu, cum1, src);
-        const uint64_t off_a = __shfl_sync(0xffffffffu, off0, src);
-        const uint64_t off_b = __shfl_sync(0xffffffffu, off1, src);
-        if (act) {
-          const bool hi_band = b >= 32;
-          const uint64_t rank = (e - lo) - (hi_band ? cum_b : cum_a);
-          const uint64_t dest = (hi_band ? off_b : off_a) + rank;
-          a.L.bt[dest] = t;
-          a.L.bs[dest] = a.s[e];
-        }
-      }
-      off0 += c0;
-      off1 += c1;
-    }
-    if (!heavy) {
-      if (b0 < nb) a.L.lrec[(uint64_t)b0 * a.L.n_light + a.rank[g]] = rec0 | (st0 << 25);
-      if (b1 < nb) a.L.lrec[(uint64_t)b1 * a.L.n_light + a.rank[g]] = rec1 | (st1 << 25);
-    } else {
-      if (b0 < nb) {
-        HeavyRec& h = a.L.hrec[(uint64_t)b0 * a.L.n_heavy + a.rank[g]];
-        h.base = base0;
-        h.state = st0;
-        for (int p = k + 1; p < 5; ++p) h.cnt[p] = 0;
-      }
-      if (b1 < nb) {
-        HeavyRec& h = a.L.hrec[(uint64_t)b1 * a.L.n_heavy + a.rank[g]];
-        h.base = base1;
-        h.state = st1;
-        for (int p = k + 1; p < 5; ++p) h.cnt[p] = 0;
-      }
-    }
-  }
-}
-
-__global__ void __launch_bounds__(256) k_bb_lblk(const BandBuildArgs a) {
-  const uint32_t nlb = a.L.n_lblk;
-  const uint64_t i = blockIdx.x * (uint64_t)256 + threadIdx.x;
-  if (i >= (uint64_t)a.n_bands * (nlb + 1)) return;
-  const uint32_t b = (uint32_t)(i / (nlb + 1)), j = (uint32_t)(i % (nlb + 1));
-  const uint32_t lr = min(j * (uint32_t)kLightBlock, a.L.n_light);
-  a.L.lblk[i] = a.unit_off[(uint64_t)b * a.n_gates + lr];
-}
-
-int warp_grid(uint64_t n_gates) {
-  return (int)std::min<uint64_t>((n_gates * 32 + 255) / 256 + 1, 152ull * 64);
-}
-
-}  // namespace
-
-cudaError_t band_build_phase1(BandBuildArgs& a, cudaStream_t st) {
-  const uint64_t ncnt = a.n_pins * (uint64_t)a.n_bands;
-  cudaError_t e = cudaMemsetAsync(a.cnt, 0, ncnt * sizeof(uint32_t), st);
-  if (e != cudaSuccess) return e;
-  if (a.pow2) k_bb_count<true><<<warp_grid(a.n_gates), 256, 0, st>>>(a);
-  else k_bb_count<false><<<warp_grid(a.n_gates), 256, 0, st>>>(a);
-  const uint32_t gb = (a.n_gates + 255) / 256;
-  if (gb) k_bb_classify<<<gb, 256, 0, st>>>(a);
-  const uint32_t nb = (uint32_t)((a.n_gates + kScanBlock - 1) / kScanBlock);
-  if (nb) {
-    k_bb_flag_sum<<<nb, 256, 0, st>>>(a, a.scan_blk);
-    k_scan_blocks<<<1, 1024, 0, st>>>(a.scan_blk, nb);
-    k_bb_flag_apply<<<nb, 256, 0, st>>>(a, a.scan_blk);
-  } else {
-    e = cudaMemsetAsync(a.totals, 0, 2 * sizeof(uint32_t), st);
-    if (e != cudaSuccess) return e;
-  }
-  return cudaGetLastError();
-}
-
-cudaError_t band_build_phase2(BandBuildArgs& a, cudaStream_t st) {
-  const uint32_t gb = (a.n_gates + 255) / 256;
-  const uint64_t nu = (uint64_t)a.n_bands * a.n_gates;
-  if (gb) k_bb_unitsize<<<gb, 256, 0, st>>>(a);
-  cudaError_t e = scan_u32_to_u64(a.unit_size, nu, a.scan_blk, a.unit_off, st);
-  if (e != cudaSuccess) return e;
-  if (a.pow2) k_bb_scatter<true><<<warp_grid(a.n_gates), 256, 0, st>>>(a);
-  else k_bb_scatter<false><<<warp_grid(a.n_gates), 256, 0, st>>>(a);
-  const uint64_t nl = (uint64_t)a.n_bands * (a.L.n_lblk + 1);
-  k_bb_lblk<<<(uint32_t)((nl + 255) / 256), 256, 0, st>>>(a);
-  return cudaGetLastError();
-}
-
-// ------------------------------------------------------------------ banded partition (per run)
 //
-// Work items in band-major order: light tiles (runs of light blocks of one band
-// whose first event offsets share a kBTileTarget bucket; at most kBGateCap
-// gates), then heavy items (runs of small heavy units sharing a bucket, or one
-// unit alone when it has more than kBUnitSmall events; units above kBTileCap
-// events are streamed). The CTAs of the fused kernel take contiguous runs of
-// this list holding equal shares of the events, so each touches few bands.
+// One thread per gate walks the gate's cycles in order (a merge of its pins'
+// cycle streams; a pin's events are time-sorted, so its cycles are
+// non-decreasing) and cuts windows greedily: the current window closes at a
+// band boundary, or before a cycle whose events would take one of the pins
+// past kUnitPinMax in the window. Counting pass: units and events per
+// (band, gate). Writing pass: the same walk writes each unit's record and
+// copies its events, pin by pin, to the unit's place in the banded arrays.
+// Items: a unit starts an item at a band start, where its event offset enters
+// a new kItemBucket bucket of the band, or every kItemUnits units.
 
 namespace {
 
-__device__ __forceinline__ uint64_t lblk_at(const BandLayout& L, uint32_t b, uint32_t j) {
-  return L.lblk[(uint64_t)b * (L.n_lblk + 1) + j];
+__device__ __forceinline__ uint32_t bcyc(const BandBuildArgs& a, float t) {
+  return a.pow2 ? (uint32_t)(t * a.inv_t_clk) : (uint32_t)__fdiv_rn(t, a.t_clk);
 }
 
-__device__ __forceinline__ uint32_t hunit_n(const HeavyRec& h) {
-  return h.cnt[0] + h.cnt[1] + h.cnt[2] + h.cnt[3] + h.cnt[4];
-}
+constexpr uint32_t kNoCycle = 0xFFFFFFFFu;
 
-__device__ bool light_head(const BandLayout& L, uint32_t b, uint32_t j) {
-  if (j == 0 || j % (uint32_t)(kBGateCap / kLightBlock) == 0) return true;
-  const uint64_t base = lblk_at(L, b, 0);
-  return (lblk_at(L, b, j) - base) / kBTileTarget != (lblk_at(L, b, j - 1) - base) / kBTileTarget;
-}
+// Per-gate walk state: pin cursors and the cycle of each pin's next event.
+struct GateWalk {
+  uint64_t pos[kMaxK + 1], end[kMaxK + 1];
+  uint32_t nc[kMaxK + 1];
+  int k;
+};
 
-__device__ bool heavy_big(const BandLayout& L, uint32_t b, uint32_t h) {
-  return hunit_n(L.hrec[(uint64_t)b * L.n_heavy + h]) > kBUnitSmall;
-}
-
-__device__ bool heavy_head(const BandLayout& L, uint32_t b, uint32_t h) {
-  if (h == 0 || h % (uint32_t)kBGateCap == 0) return true;
-  if (heavy_big(L, b, h) || heavy_big(L, b, h - 1)) return true;
-  const uint64_t base = L.hrec[(uint64_t)b * L.n_heavy].base;
-  return (L.hrec[(uint64_t)b * L.n_heavy + h].base - base) / kBTileTarget !=
-         (L.hrec[(uint64_t)b * L.n_heavy + h - 1].base - base) / kBTileTarget;
-}
-
-// flags[i] = 1 where a light (kind 0) or heavy (kind 1) item starts.
-__global__ void __launch_bounds__(256) k_bp_flags(const BandLayout L, uint32_t kind, uint32_t* flags) {
-  const uint64_t per = kind == 0 ? L.n_lblk : L.n_heavy;
-  const uint64_t i = blockIdx.x * (uint64_t)256 + threadIdx.x;
-  if (i >= (uint64_t)L.n_bands * per) return;
-  const uint32_t b = (uint32_t)(i / per), j = (uint32_t)(i % per);
-  flags[i] = kind == 0 ? (uint32_t)light_head(L, b, j) : (uint32_t)heavy_head(L, b, j);
-}
-
-// Items of one kind at item_base + (exclusive scan of the flags); events per item.
-__global__ void __launch_bounds__(256) k_bp_emit(const BandLayout L, uint32_t kind, const uint32_t* flags,
-                                                 const uint64_t* pos, uint32_t item_base, BandItem* items,
-                                                 uint32_t* item_n) {
-  const uint64_t per = kind == 0 ? L.n_lblk : L.n_heavy;
-  const uint64_t n = (uint64_t)L.n_bands * per;
-  const uint64_t i = blockIdx.x * (uint64_t)256 + threadIdx.x;
-  if (i >= n || !flags[i]) return;
-  const uint32_t b = (uint32_t)(i / per), j = (uint32_t)(i % per);
-  // the item ends before the next head of the same band
-  uint32_t e = j + 1;
-  while (e < per && !flags[(uint64_t)b * per + e]) ++e;
-  BandItem it;
-  it.band = b;
-  it.first = j;
-  it.last = e;
-  uint64_t ev;
-  if (kind == 0) {
-    it.kind = 0;
-    ev = lblk_at(L, b, e) - lblk_at(L, b, j);
-  } else {
-    const HeavyRec& h0 = L.hrec[(uint64_t)b * L.n_heavy + j];
-    const HeavyRec& h1 = L.hrec[(uint64_t)b * L.n_heavy + e - 1];
-    ev = h1.base + hunit_n(h1) - h0.base;
-    it.kind = (e == j + 1 && ev > (uint64_t)kBTileCap) ? 2u : 1u;
+__device__ __forceinline__ void walk_init(const BandBuildArgs& a, const GateRec& r, GateWalk& W) {
+  W.k = (int)((r.init >> 16) & 0xff);
+  for (int p = 0; p <= kMaxK; ++p) {
+    W.pos[p] = W.end[p] = 0;
+    W.nc[p] = kNoCycle;
+    if (p <= W.k) {
+      W.pos[p] = a.pin_off[(uint64_t)r.pin_base + p];
+      W.end[p] = a.pin_off[(uint64_t)r.pin_base + p + 1];
+      W.nc[p] = W.pos[p] < W.end[p] ? bcyc(a, a.t[W.pos[p]]) : kNoCycle;
+    }
   }
-  it.e0 = kind == 0 ? lblk_at(L, b, j) : L.hrec[(uint64_t)b * L.n_heavy + j].base;
-  it.n = (uint32_t)ev;
-  it.pad = 0;
-  const uint32_t k = item_base + (uint32_t)pos[i];
-  items[k] = it;
-  item_n[k] = (uint32_t)ev;
+}
+
+// Next cycle with events (kNoCycle when done) and its event count per pin;
+// advances the cursors past it.
+__device__ __forceinline__ uint32_t walk_cycle(const BandBuildArgs& a, GateWalk& W, uint32_t n_c[kMaxK + 1]) {
+  uint32_t c = kNoCycle;
+  for (int p = 0; p <= W.k; ++p) c = min(c, W.nc[p]);
+  for (int p = 0; p <= kMaxK; ++p) n_c[p] = 0;
+  if (c == kNoCycle) return c;
+  for (int p = 0; p <= W.k; ++p) {
+    while (W.nc[p] == c) {
+      ++n_c[p];
+      ++W.pos[p];
+      W.nc[p] = W.pos[p] < W.end[p] ? bcyc(a, a.t[W.pos[p]]) : kNoCycle;
+    }
+  }
+  return c;
+}
+
+// kWrite false: units / events per (band, gate) and big gates; true: records,
+// unit offsets and the event copy.
+template <bool kWrite>
+__global__ void __launch_bounds__(128) k_bw_greedy(const BandBuildArgs a) {
+  const uint64_t g = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x;
+  if (g >= a.n_gates) return;
+  const uint64_t G = a.n_gates;
+  if (kWrite && a.bigf[g]) return;
+  const GateRec r = a.gates[g];
+  GateWalk W;
+  walk_init(a, r, W);
+  const int k = W.k;
+  uint32_t n_c[kMaxK + 1];
+  uint32_t cw[kMaxK + 1];        // events per pin in the open window
+  uint64_t wstart[kMaxK + 1];    // CSR position of each pin at the window start
+  for (int p = 0; p <= kMaxK; ++p) {
+    cw[p] = 0;
+    wstart[p] = W.pos[p];
+  }
+  uint32_t state = r.init & ((1u << k) - 1u);  // input state at the window start
+  uint32_t band = kNoCycle, units = 0, events = 0, wsize = 0;
+  uint64_t u = 0, dst = 0;                      // next unit / banded event of this (band, gate)
+  bool big = false, split = false;
+  for (;;) {
+    const uint32_t c = walk_cycle(a, W, n_c);
+    bool over = false;
+    for (int p = 0; p <= k; ++p) {
+      if (n_c[p] > (uint32_t)kUnitPinMax) big = true;
+      over |= cw[p] + n_c[p] > (uint32_t)kUnitPinMax;
+    }
+    if (big) break;
+    const uint32_t b = c == kNoCycle ? kNoCycle : c >> a.mb;
+    if (wsize > 0 && (c == kNoCycle || b != band || over)) {
+      // close the open window as one unit
+      if (kWrite) {
+        uint32_t x = 0;
+        for (int p = 0; p <= k; ++p) x |= cw[p] << (4 * p);
+        x |= state << 20;
+        x |= (r.cell & 0xffu) << 24;
+        if (u < (uint64_t)a.L.n_units && dst + wsize <= a.L.n_ev) {
+          a.L.urec[u] = make_uint2(x, __float_as_uint(r.load));
+          a.L.ugate[u] = (uint32_t)g;
+          a.uband[u] = band;
+          a.uoff[u] = dst;
+          uint64_t d = dst;
+          for (int p = 0; p <= k; ++p) {
+            for (uint32_t i = 0; i < cw[p]; ++i) {
+              a.L.bt[d + i] = a.t[wstart[p] + i];
+              a.L.bs[d + i] = a.s[wstart[p] + i];
+            }
+            d += cw[p];
+          }
+        } else {
+          atomicMin(a.err, (unsigned long long)((g << 8) | kErrTileOverflow));
+        }
+        ++u;
+        dst += wsize;
+      }
+      for (int p = 0; p <= k; ++p) {
+        if (p < k) state ^= (cw[p] & 1u) << p;
+        wstart[p] += cw[p];
+        cw[p] = 0;
+      }
+      if (!(c == kNoCycle || b != band)) split = true;
+      ++units;
+      events += wsize;
+      wsize = 0;
+    }
+    if (c == kNoCycle) break;
+    if (b != band) {
+      if (!kWrite && band != kNoCycle) {
+        a.cnt_gb[(uint64_t)band * G + g] = units;
+        a.evc_gb[(uint64_t)band * G + g] = events;
+      }
+      band = b;
+      units = 0;
+      events = 0;
+      if (kWrite) {
+        u = a.ubase[(uint64_t)b * G + g];
+        dst = a.ebase[(uint64_t)b * G + g];
+      }
+    }
+    for (int p = 0; p <= k; ++p) cw[p] += n_c[p];
+    for (int p = 0; p <= k; ++p) wsize += n_c[p];
+  }
+  if (!kWrite) {
+    if (big) {
+      // no unit of a big gate: clear what the walk wrote before it saw the cycle
+      for (uint32_t bb = 0; bb < a.n_bands; ++bb) {
+        a.cnt_gb[(uint64_t)bb * G + g] = 0;
+        a.evc_gb[(uint64_t)bb * G + g] = 0;
+      }
+      a.L.big[atomicAdd(a.counters, 1u)] = (uint32_t)g;
+      a.bigf[g] = 1;
+    } else {
+      a.bigf[g] = 0;
+      if (band != kNoCycle) {
+        a.cnt_gb[(uint64_t)band * G + g] = units;
+        a.evc_gb[(uint64_t)band * G + g] = events;
+      }
+      if (split) atomicAdd(a.counters + 1, 1u);
+    }
+  }
+}
+
+// Item heads over the units.
+__global__ void __launch_bounds__(256) k_bw_item_flags(const BandBuildArgs a, uint32_t n_units) {
+  const uint32_t u = blockIdx.x * 256u + threadIdx.x;
+  if (u >= n_units) return;
+  const uint32_t b = a.uband[u];
+  const uint32_t bu0 = (uint32_t)a.ubase[(uint64_t)b * a.n_gates];
+  const uint64_t be = a.uoff[bu0];
+  bool head = u == bu0;
+  if (!head) {
+    head = (a.uoff[u] - be) / kItemBucket != (a.uoff[u - 1] - be) / kItemBucket ||
+           (u - bu0) / (uint32_t)kItemUnits != (u - 1 - bu0) / (uint32_t)kItemUnits;
+  }
+  a.flags[u] = head ? 1u : 0u;
+}
+
+__global__ void __launch_bounds__(256) k_bw_item_emit(const BandBuildArgs a, uint32_t n_units, uint32_t n_items) {
+  const uint32_t u = blockIdx.x * 256u + threadIdx.x;
+  if (u < n_units && a.flags[u]) {
+    BandItem it;
+    it.e0 = a.uoff[u];
+    it.u0 = u;
+    it.band = a.uband[u];
+    a.L.items[a.ipos[u]] = it;
+  }
+  if (u == 0) {
+    BandItem s;
+    s.e0 = a.L.n_ev;
+    s.u0 = n_units;
+    s.band = a.n_bands;
+    a.L.items[n_items] = s;
+  }
 }
 
 }  // namespace
 
-uint32_t band_max_items(const BandLayout& L) {
-  return L.n_bands * (L.n_lblk + L.n_heavy) + 1;
+cudaError_t band_build_count(BandBuildArgs& a, cudaStream_t st) {
+  const uint64_t n = (uint64_t)a.n_bands * a.n_gates;
+  cudaError_t e = cudaMemsetAsync(a.counters, 0, 4 * sizeof(uint32_t), st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(a.cnt_gb, 0, (n + 1) * sizeof(uint32_t), st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(a.evc_gb, 0, (n + 1) * sizeof(uint32_t), st);
+  if (e != cudaSuccess) return e;
+  if (a.n_gates) k_bw_greedy<false><<<(a.n_gates + 127) / 128, 128, 0, st>>>(a);
+  e = scan_u32_to_u64(a.cnt_gb, n, a.scan_blk, a.ubase, st);
+  if (e == cudaSuccess) e = scan_u32_to_u64(a.evc_gb, n, a.scan_blk, a.ebase, st);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
 }
 
-// Build the item list; host_items[0..1] = light and heavy item counts.
-cudaError_t band_partition(BandRunArgs& A, uint32_t* flags, uint64_t* pos, uint64_t* scan_blk,
-                           uint32_t* item_n, uint32_t* host_items, cudaStream_t st) {
-  const BandLayout& L = A.L;
-  uint32_t base = 0;
-  for (uint32_t kind = 0; kind < 2; ++kind) {
-    const uint64_t n = (uint64_t)L.n_bands * (kind == 0 ? L.n_lblk : L.n_heavy);
-    host_items[kind] = 0;
-    if (n == 0) continue;
-    const uint32_t g = (uint32_t)((n + 255) / 256);
-    k_bp_flags<<<g, 256, 0, st>>>(L, kind, flags);
-    cudaError_t e = scan_u32_to_u64(flags, n, scan_blk, pos, st);
-    if (e != cudaSuccess) return e;
-    uint64_t cnt = 0;
-    e = cudaMemcpyAsync(&cnt, pos + n, sizeof(cnt), cudaMemcpyDeviceToHost, st);
-    if (e != cudaSuccess) return e;
-    k_bp_emit<<<g, 256, 0, st>>>(L, kind, flags, pos, base, A.items, item_n);
-    e = cudaStreamSynchronize(st);
-    if (e != cudaSuccess) return e;
-    host_items[kind] = (uint32_t)cnt;
-    base += (uint32_t)cnt;
-  }
-  // event prefix of the items
-  return scan_u32_to_u64(item_n, base, scan_blk, A.item_ev, st);
+cudaError_t band_build_write(BandBuildArgs& a, cudaStream_t st) {
+  if (a.n_gates) k_bw_greedy<true><<<(a.n_gates + 127) / 128, 128, 0, st>>>(a);
+  const uint32_t nu = a.L.n_units;
+  cudaError_t e = cudaMemcpyAsync(a.uoff + nu, &a.L.n_ev, sizeof(uint64_t), cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return e;
+  if (nu) k_bw_item_flags<<<(nu + 255) / 256, 256, 0, st>>>(a, nu);
+  e = scan_u32_to_u64(a.flags, nu, a.scan_blk, a.ipos, st);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
 }
 
-// ------------------------------------------------------------------ per-run gate records
+cudaError_t band_build_items(BandBuildArgs& a, cudaStream_t st) {
+  const uint32_t nu = a.L.n_units;
+  k_bw_item_emit<<<nu ? (nu + 255) / 256 : 1, 256, 0, st>>>(a, nu, a.L.n_items);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ P0 of a run
 
 namespace {
 
-__global__ void __launch_bounds__(256) k_bg_gaterun(const BandRunArgs A) {
-  const uint64_t i = blockIdx.x * (uint64_t)256 + threadIdx.x;
-  const uint64_t nl = A.L.n_light, nh = A.L.n_heavy;
+__global__ void __launch_bounds__(256) k_band_p0(const RunArgs a) {
+  const uint32_t g = blockIdx.x * 256u + threadIdx.x;
   double p0 = 0.0;
-  if (i < nl + nh) {
-    const bool light = i < nl;
-    const uint32_t g = light ? A.L.lgate[i] : A.L.hgate[i - nl];
-    const GateRec r = A.r.gates[g];
-    const CellDesc& cd = A.r.cells[r.cell];
-    const float C = r.load;
-    int j = 0;
-    for (int m = 1; m <= cd.nl - 2; ++m) j += (C >= cd.lax[m]) ? 1 : 0;
-    GateRun gr;
-    gr.packed = (r.cell & 0xffffu) | ((uint32_t)cd.k << 16) | ((uint32_t)j << 20);
-    gr.v = (C - cd.lax[j]) * cd.ilax[j];
-    gr.esw = A.r.half_vdd2 * C;
-    gr.gate = g;
-    if (light) A.grun_l[i] = gr;
-    else A.grun_h[i - nl] = gr;
-    // P0: leakage of every gate's initial input state
-    p0 = (double)A.r.leak[cd.leak_off + (r.init & ((1u << cd.k) - 1u))];
+  if (g < a.n_gates) {
+    const GateRec r = a.gates[g];
+    const CellDesc& cd = a.cells[r.cell];
+    p0 = (double)a.leak[cd.leak_off + (r.init & ((1u << cd.k) - 1u))];
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) p0 += __shfl_xor_sync(0xffffffffu, p0, o);
-  if ((threadIdx.x & 31) == 0 && p0 != 0.0) atomicAdd(A.r.p0, p0);
+  __shared__ double ws[8];
+  if ((threadIdx.x & 31) == 0) ws[threadIdx.x >> 5] = p0;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double s = 0.0;
+    for (int i = 0; i < 8; ++i) s += ws[i];
+    if (s != 0.0) atomicAdd(a.p0, s);
+  }
 }
 
 }  // namespace
 
-cudaError_t band_gate_run(BandRunArgs& A, cudaStream_t st) {
-  const uint64_t n = (uint64_t)A.L.n_light + A.L.n_heavy;
-  if (n) k_bg_gaterun<<<(uint32_t)((n + 255) / 256), 256, 0, st>>>(A);
+cudaError_t band_p0(const RunArgs& r, cudaStream_t st) {
+  if (r.n_gates) k_band_p0<<<(r.n_gates + 255) / 256, 256, 0, st>>>(r);
   return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ banded fused kernel
 //
-// One CTA per SM takes a contiguous, event-balanced run of band-major items.
-// Thread 0 prefetches item i+1 with TMA bulk copies (events, unit records,
-// per-run gate records) into the spare one of two shared-memory stages while
-// the CTA works on item i; an mbarrier per stage signals completion. Events
-// add into the band's cycle bins in shared memory; a band change flushes them.
+// One CTA of 32 warps per SM takes a contiguous, event-balanced run of items
+// and works through it band by band. Inside a band the warps take items from a
+// shared counter and work independently: a warp copies its item's events and
+// unit records into its own shared-memory buffer (coalesced streaming loads),
+// decodes one unit record per lane into a 16-byte slot and marks each unit's
+// first event in a bit mask, then processes one event per lane: unit from the
+// mask (count of unit starts at or before it), pin from the slot's pin
+// offsets, gate state, LUT, glitch and leakage, and the sums go into the
+// band's cycle bins in shared memory. When the band's items are done the CTA
+// adds the bins to global memory with one TMA bulk reduction.
 
 namespace {
 
-constexpr int kBThreads = 512;
-constexpr int kBWarps = kBThreads / 32;
-static_assert(kBGateCap == kBThreads, "one unit per thread in tile setup");
-
-struct __align__(16) BSlot {
-  uint16_t st[5];   // staged start of each pin's segment
-  uint16_t len[5];  // events of each pin to process
-  uint8_t kj;       // k (bits 0..3), load-axis interval j (bits 4..7)
-  uint8_t state;    // input state before the segments (band start, or stream window start)
-  uint16_t cell;
-  float v, esw;
-};
-static_assert(sizeof(BSlot) == 32, "slot size");
-
-struct BStream {
-  uint64_t cur[5], end[5];
-  float prev_t[5], prev_s[5], bound[5];
-  uint8_t has_prev[5];
-  uint8_t pre;  // parity of the events already processed, per pin
-  int done;
-};
-
-struct BAcc {
-  float e_int, e_sw, e_gl, e_lk;
-};
-
-struct StageMeta {
-  BandItem it;
-  uint32_t ev_off, rec_off;
-};
-
-constexpr int kStEv = kBTileCap + 8;  // staged floats per array (16-byte rounding slack)
-constexpr size_t kStTs = (size_t)kStEv * 4;
-constexpr size_t kStRec = (size_t)kBGateCap * sizeof(HeavyRec) + 16;
-constexpr size_t kStGrun = (size_t)kBGateCap * sizeof(GateRun);
-constexpr size_t kStage = 2 * kStTs + kStRec + kStGrun;
-static_assert(kStage % 16 == 0, "stage alignment");
-
-constexpr size_t kBHist = (size_t)kBandMaxCycles * 16;
-constexpr size_t kBSlots = (size_t)kBGateCap * sizeof(BSlot);
-constexpr size_t kBTag = (size_t)kBTileCap * 2;
-constexpr size_t kBGates = (size_t)kBGateCap * 4;
-constexpr size_t kBCells = (size_t)kSmemCells * sizeof(CellDesc);
-constexpr size_t kBSmem = kBHist + 2 * kStage + kBSlots + kBTag + kBGates + kBCells;
-static_assert(kBSmem <= 227 * 1024, "shared memory budget");
-
-constexpr uint32_t kWaitLimit = 1u << 24;  // mbarrier polls before giving up
+constexpr int kBT = 1024;
+constexpr int kBW = kBT / 32;
+constexpr int kMaskWords = kItemEvents / 32;
+constexpr size_t kWarpBytes = (size_t)kItemEvents * 8 + (size_t)kItemUnits * 16 + 2 * kMaskWords * 4;
+constexpr size_t kHist = (size_t)kBandMaxCycles * 16;
+constexpr size_t kCellsB = (size_t)kSmemCells * sizeof(CellDesc);
+constexpr size_t kSmemB = kHist + kCellsB + kBW * kWarpBytes;
+static_assert(kWarpBytes % 16 == 0 && kHist % 16 == 0 && kCellsB % 16 == 0, "alignment");
+static_assert(kSmemB <= 227 * 1024, "shared memory budget");
+constexpr int kTotEvery = 16;  // items between flushes of a warp's per-lane totals
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
 
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_arrive(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+// Bulk f32 add of shared memory into global memory (16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void bulk_red_add_f32(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(dst),
+               "r"(smem_u32(src)), "r"(bytes)
                : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bulk copy global -> shared, completing on the mbarrier (16-byte aligned, size % 16 == 0).
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ int lb_f(const float* a, int n, float x) {
-  int lo = 0;
-  while (n > 0) {
-    const int half = n >> 1;
-    if (a[lo + half] < x) {
-      lo += half + 1;
-      n -= half + 1;
-    } else {
-      n = half;
-    }
-  }
-  return lo;
-}
-
-struct BCtx {
-  float* W;
-  float* D;
-  uint32_t* EV;
-  uint32_t* GL;
-  uint16_t* tag;
-  BSlot* slots;
-  uint32_t* sgate;  // gate id per slot (debug outputs)
-  const CellDesc* cells;
-  uint32_t c0;      // first cycle of the current band
+struct BAcc {
+  float e_int, e_sw, e_gl, e_lk;
 };
-
-// One event of a staged segment (gate state, LUT, switching, glitch, leakage)
-// into the shared-memory band histogram.
-template <bool kPow2, bool kDebug>
-__device__ __forceinline__ void bevent(const BandRunArgs& A, const BCtx& X, const float* __restrict__ ts,
-                                       const float* __restrict__ ss, int si, int p, int e, bool hp0, float pt0,
-                                       float ps0, BAcc& acc) {
-  const RunArgs& a = A.r;
-  const BSlot& S = X.slots[si];
-  const int a0 = S.st[p];
-  const int idx = e - a0;
-  if (idx >= (int)S.len[p]) return;
-  const float t = ts[e], s = ss[e];
-  const uint32_t c = cyc<kPow2>(t, a.t_clk, a.inv_t_clk);
-  bool has_prev = hp0;
-  float tp = pt0, sp = ps0;
-  if (idx > 0) {
-    has_prev = true;
-    tp = ts[e - 1];
-    sp = ss[e - 1];
-  }
-  const bool glitch = has_prev && cyc<kPow2>(tp, a.t_clk, a.inv_t_clk) == c;
-  const uint32_t kj = S.kj;
-  const int k = (int)(kj & 15u);
-  float e_int = 0.f, e_sw = 0.f, dp = 0.f;
-  uint32_t s_pre = S.state;
-  int li = 0;
-  if (p == k) {
-    e_sw = S.esw;
-    if (kDebug) {
-      for (int q = 0; q < k; ++q) s_pre ^= ((uint32_t)lb_f(ts + S.st[q], S.len[q], t) & 1u) << q;
-    }
-  } else {
-    const CellDesc& cd = X.cells[S.cell];
-    s_pre ^= ((uint32_t)idx & 1u) << p;
-    uint32_t s_b = s_pre;
-    for (int q = 0; q < k; ++q) {
-      if (q == p) continue;
-      const int qa = S.st[q], qn = S.len[q];
-      const int r = lb_f(ts + qa, qn, t);
-      const uint32_t par = (uint32_t)r & 1u;
-      s_pre ^= par << q;
-      const bool eq = q < p && r < qn && ts[qa + r] == t;
-      s_b ^= (par ^ (uint32_t)eq) << q;
-    }
-    // slew interval: largest i <= ns - 2 with axis[i] <= s (axes have <= 8 points)
-    const int ns = cd.ns, nl = cd.nl;
-    {
-      const int hi = ns - 2;
-      int w = 4;
-      while (w > 0) {
-        const int cand = li + w;
-        if (cand <= hi && s >= cd.sax[cand]) li = cand;
-        w >>= 1;
-      }
-    }
-    const float u = (s - cd.sax[li]) * cd.isax[li];
-    const float* L = a.lut + cd.lut_off + ((int)s_pre * ns + li) * nl + (int)(kj >> 4);
-    const float l00 = __ldg(L), l01 = __ldg(L + 1), l10 = __ldg(L + nl), l11 = __ldg(L + nl + 1);
-    const float v = S.v;
-    const float r0 = fmaf(v, l01 - l00, l00), r1 = fmaf(v, l11 - l10, l10);
-    e_int = fmaf(u, r1 - r0, r0);
-    const float* lk = a.leak + cd.leak_off;
-    dp = __ldg(lk + (s_b ^ (1u << p))) - __ldg(lk + s_b);
-  }
-  const float e_dyn = e_int + e_sw;
-  float e_w;
-  if (glitch) {
-    const float r = fminf(1.f, 2000.f * (t - tp) / (s + sp));
-    e_w = r * e_dyn;
-    acc.e_gl += e_w;
-  } else {
-    acc.e_int += e_int;
-    acc.e_sw += e_sw;
-    e_w = e_dyn;
-  }
-  const uint32_t lc = c - X.c0;
-  if (lc >= A.L.band_cycles) {  // an event outside its band: layout inconsistency
-    berr(a.err, e, kErrTileOverflow);
-    return;
-  }
-  if (p < k) {
-    const float rem = fmaf(-(float)c, a.t_clk, t);  // t - c T
-    e_w = fmaf(dp, a.t_clk - rem, e_w);
-    acc.e_lk = fmaf(dp, a.t_max_f - t, acc.e_lk);
-    atomicAdd(X.D + lc, dp);
-  }
-  atomicAdd(X.W + lc, e_w);
-  atomicAdd(X.EV + lc, 1u);
-  if (glitch) atomicAdd(X.GL + lc, 1u);
-  if (kDebug) {
-    // original (CSR) index of this event: its rank among the pin's events
-    const GateRec r = a.gates[X.sgate[si]];
-    const uint64_t pin = (uint64_t)r.pin_base + p;
-    const uint64_t lo = a.pin_off[pin], hi = a.pin_off[pin + 1];
-    uint64_t l = lo, n = hi - lo;
-    while (n > 0) {
-      const uint64_t half = n >> 1;
-      if (a.t[l + half] < t) {
-        l += half + 1;
-        n -= half + 1;
-      } else {
-        n = half;
-      }
-    }
-    a.dbg_state[l] = (uint8_t)s_pre;
-    a.dbg_lut[l] = p < k ? (uint8_t)((li << 4) | (int)(kj >> 4)) : (uint8_t)0xFF;
-    a.dbg_glitch[l] = (uint8_t)glitch;
-  }
-}
 
 __device__ __forceinline__ void bflush_acc(BAcc& acc, double* s_tot) {
   float v[4] = {acc.e_int, acc.e_sw, acc.e_gl, acc.e_lk};
@@ -766,137 +447,306 @@ __device__ __forceinline__ void bflush_acc(BAcc& acc, double* s_tot) {
   acc = BAcc{0.f, 0.f, 0.f, 0.f};
 }
 
-// Add the band's shared-memory bins to the global fp64 / u32 bins and clear them.
-__device__ void bflush_band(const BandRunArgs& A, const BCtx& X, uint32_t band) {
+// Add the band's shared-memory bins to the global bins and clear them. Fast
+// mode: {W, D, ev, gl} as f32 by one bulk reduction (counts converted in
+// place). Exact mode adds per event to global memory; nothing to flush.
+template <bool kExact>
+__device__ void bflush_band(const BandRunArgs& A, float4* hist, uint32_t band) {
   const uint32_t cb = A.L.band_cycles, N = A.r.n_cycles;
-  double* bins = reinterpret_cast<double*>(A.r.bins);
-  for (uint32_t lc = threadIdx.x; lc < cb; lc += kBThreads) {
-    const uint32_t c = band * cb + lc;
-    const float w = X.W[lc], d = X.D[lc];
-    const uint32_t ev = X.EV[lc], gl = X.GL[lc];
-    if (c < N) {
-      if (w != 0.f) atomicAdd(bins + 2 * (uint64_t)c, (double)w);
-      if (d != 0.f) atomicAdd(bins + 2 * (uint64_t)c + 1, (double)d);
-      if (ev) atomicAdd(A.r.cnt_ev + c, ev);
-      if (gl) atomicAdd(A.r.cnt_gl + c, gl);
+  const uint32_t c0 = band * cb;
+  const uint32_t nb = c0 < N ? min(cb, N - c0) : 0u;
+  if (!kExact) {
+    for (uint32_t i = threadIdx.x; i < nb; i += kBT) {
+      float4 h = hist[i];
+      h.z = (float)__float_as_uint(h.z);
+      h.w = (float)__float_as_uint(h.w);
+      hist[i] = h;
     }
-    X.W[lc] = 0.f;
-    X.D[lc] = 0.f;
-    X.EV[lc] = 0u;
-    X.GL[lc] = 0u;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+    if (threadIdx.x == 0 && nb) bulk_red_add_f32(A.r.bins + c0, hist, nb * 16u);
+    __syncthreads();
   }
+  for (uint32_t i = threadIdx.x; i < cb; i += kBT) hist[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-__device__ __forceinline__ void bslot_from(BSlot& S, const GateRun& gr, uint32_t state) {
-  S.kj = (uint8_t)(((gr.packed >> 16) & 15u) | (((gr.packed >> 20) & 15u) << 4));
-  S.state = (uint8_t)state;
-  S.cell = (uint16_t)(gr.packed & 0xffffu);
-  S.v = gr.v;
-  S.esw = gr.esw;
+// First item in [lo, hi) whose band differs from `band` (items are band-sorted).
+__device__ uint32_t band_end(const BandLayout& L, uint32_t lo, uint32_t hi, uint32_t band) {
+  uint32_t n = hi - lo;
+  while (n > 0) {
+    const uint32_t half = n >> 1;
+    if (L.items[lo + half].band <= band) {
+      lo += half + 1;
+      n -= half + 1;
+    } else {
+      n = half;
+    }
+  }
+  return lo;
 }
 
-// Thread 0: stage item `i` into stage buffer `stage` (TMA bulk copies).
-__device__ void bprefetch(const BandRunArgs& A, uint32_t i, uint8_t* stage, StageMeta& meta, uint64_t* bar) {
-  const BandItem it = A.items[i];
-  meta.it = it;
-  meta.ev_off = 0;
-  meta.rec_off = 0;
-  if (it.kind == 2) {  // streamed: nothing staged
-    mbar_expect_arrive(bar, 0);
+// One item on one warp.
+template <bool kPow2, bool kDebug, bool kExact>
+__device__ __forceinline__ void band_item(const BandRunArgs& A, const CellDesc* cells, float4* hist, uint8_t* wbuf,
+                                          uint32_t item, const BandItem& it, const BandItem& nx, uint32_t c0,
+                                          BAcc& acc) {
+  const RunArgs& a = A.r;
+  const int lane = threadIdx.x & 31;
+  float* ts = reinterpret_cast<float*>(wbuf);
+  float* ss = ts + kItemEvents;
+  uint4* slots = reinterpret_cast<uint4*>(ss + kItemEvents);
+  uint32_t* mask = reinterpret_cast<uint32_t*>(slots + kItemUnits);
+  uint32_t* wpre = mask + kMaskWords;
+  const uint64_t n64 = nx.e0 - it.e0;
+  const uint32_t nu = nx.u0 - it.u0;
+  if (nx.e0 < it.e0 || nx.u0 < it.u0 || n64 == 0 || n64 > (uint64_t)kItemEvents || nu == 0 ||
+      nu > (uint32_t)kItemUnits) {
+    if (lane == 0) berr(a.err, item, kErrTileOverflow);
     return;
   }
-  float* ts = reinterpret_cast<float*>(stage);
-  float* ss = reinterpret_cast<float*>(stage + kStTs);
-  uint8_t* rec = stage + 2 * kStTs;
-  uint8_t* grun = rec + kStRec;
-  const bool light = it.kind == 0;
-  const uint32_t u0 = light ? it.first * kLightBlock : it.first;
-  const uint32_t u1 = light ? min(it.last * (uint32_t)kLightBlock, A.L.n_light) : it.last;
-  const uint32_t nu = u1 - u0;
-  if (it.n > (uint32_t)kBTileCap || nu > (uint32_t)kBGateCap || u1 < u0) {  // never stage past a buffer
-    meta.it.kind = 3;
-    mbar_expect_arrive(bar, 0);
+  const int n = (int)n64;
+  // ---- stage events (streaming loads: read once)
+#pragma unroll
+  for (int r = 0; r < kItemEvents / 32; ++r) {
+    const int e = lane + 32 * r;
+    if (e < n) {
+      ts[e] = __ldcs(A.L.bt + it.e0 + e);
+      ss[e] = __ldcs(A.L.bs + it.e0 + e);
+    }
+  }
+  // ---- units: sizes, offsets (warp scan), slots, start mask
+  uint32_t carry = 0;
+#pragma unroll
+  for (int r = 0; r < kItemUnits / 32; ++r) {
+    const uint32_t uu = (uint32_t)lane + 32u * r;
+    uint32_t x = 0, size = 0;
+    float C = 0.f;
+    if (uu < nu) {
+      const uint2 rec = __ldcs(A.L.urec + it.u0 + uu);
+      x = rec.x;
+      C = __uint_as_float(rec.y);
+#pragma unroll
+      for (int p = 0; p < 5; ++p) size += (x >> (4 * p)) & 15u;
+    }
+    uint32_t inc = size;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += v;
+    }
+    const uint32_t off = carry + inc - size;
+    carry += __shfl_sync(0xffffffffu, inc, 31);
+    if (uu < nu) {
+      const uint32_t cell = x >> 24;
+      const CellDesc& cd = cells[cell];
+      const int k = cd.k;
+      int j = 0;
+      for (int m = 1; m <= cd.nl - 2; ++m) j += (C >= cd.lax[m]) ? 1 : 0;
+      const float v = (C - cd.lax[j]) * cd.ilax[j];
+      uint32_t cum = 0, s = 0;
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        s += (x >> (4 * p)) & 15u;
+        cum |= s << (8 * p);
+      }
+      const uint32_t sa = off | (((x >> 20) & 15u) << 12) | ((uint32_t)k << 16) | ((uint32_t)j << 19) | (cell << 22);
+      slots[uu] = make_uint4(sa, cum, __float_as_uint(v), __float_as_uint(a.half_vdd2 * C));
+      if (off < (uint32_t)kItemEvents) atomicOr(mask + (off >> 5), 1u << (off & 31u));
+      // words whose first position lies in (off, off + size] follow this unit
+      const uint32_t end = off + size;
+      for (uint32_t w = (off >> 5) + 1; w <= (end >> 5) && w < (uint32_t)kMaskWords; ++w) wpre[w] = uu + 1;
+    }
+  }
+  if (lane == 0) wpre[0] = 0;
+  __syncwarp();
+  if (carry != (uint32_t)n) {  // records disagree with the item's event count
+    if (lane == 0) berr(a.err, item, kErrTileOverflow);
+    __syncwarp();
+    if (lane < kMaskWords) mask[lane] = 0u;
+    __syncwarp();
     return;
   }
-  const uint64_t ea = it.e0 & ~3ull;
-  const uint32_t ev_off = (uint32_t)(it.e0 - ea);
-  const uint32_t ev_bytes = it.n ? ((ev_off + it.n + 3u) & ~3u) * 4u : 0u;
-  uint32_t rec_bytes = 0, rec_off = 0;
-  const void* rec_src = nullptr;
-  if (light) {
-    const uint64_t rb = (uint64_t)it.band * A.L.n_light + u0;
-    const uint64_t ra = rb & ~3ull;
-    rec_off = (uint32_t)(rb - ra);
-    rec_bytes = nu ? ((rec_off + nu + 3u) & ~3u) * 4u : 0u;
-    rec_src = A.L.lrec + ra;
-  } else {
-    rec_bytes = nu * (uint32_t)sizeof(HeavyRec);
-    rec_src = A.L.hrec + (uint64_t)it.band * A.L.n_heavy + u0;
-  }
-  const uint32_t g_bytes = nu * (uint32_t)sizeof(GateRun);
-  const void* g_src = (light ? A.grun_l : A.grun_h) + u0;
-  meta.ev_off = ev_off;
-  meta.rec_off = rec_off;
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  mbar_expect_arrive(bar, 2 * ev_bytes + rec_bytes + g_bytes);
-  if (ev_bytes) {
-    bulk_g2s(ts, A.L.bt + ea, ev_bytes, bar);
-    bulk_g2s(ss, A.L.bs + ea, ev_bytes, bar);
-  }
-  if (rec_bytes) bulk_g2s(rec, rec_src, rec_bytes, bar);
-  if (g_bytes) bulk_g2s(grun, g_src, g_bytes, bar);
-}
-
-}  // namespace
-
-namespace {
-
-template <bool kPow2, bool kDebug>
-__global__ void __launch_bounds__(kBThreads, 1) k_banded(const BandRunArgs A, uint32_t n_items) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  BCtx X;
+  const float T = a.t_clk, inv_T = a.inv_t_clk;
   const uint32_t cb = A.L.band_cycles;
-  X.W = reinterpret_cast<float*>(smem);
-  X.D = X.W + kBandMaxCycles;
-  X.EV = reinterpret_cast<uint32_t*>(X.D + kBandMaxCycles);
-  X.GL = X.EV + kBandMaxCycles;
-  uint8_t* stages = smem + kBHist;
-  X.slots = reinterpret_cast<BSlot*>(stages + 2 * kStage);
-  X.tag = reinterpret_cast<uint16_t*>(stages + 2 * kStage + kBSlots);
-  X.sgate = reinterpret_cast<uint32_t*>(stages + 2 * kStage + kBSlots + kBTag);
-  CellDesc* cells_s = reinterpret_cast<CellDesc*>(stages + 2 * kStage + kBSlots + kBTag + kBGates);
-  __shared__ __align__(8) uint64_t s_bar[2];
-  __shared__ StageMeta s_meta[2];
-  __shared__ BStream hs;
-  __shared__ double s_tot[4];
+  // ---- events
+  const uint32_t le_mask = 0xFFFFFFFFu >> (31 - lane);  // lanes <= this one (e % 32 == lane)
+  for (int e = lane; e < n; e += 32) {
+    const int w = e >> 5;
+    const int u = (int)wpre[w] + __popc(mask[w] & le_mask) - 1;
+    const uint4 S = slots[u];
+    const int ustart = (int)(S.x & 0xFFFu);
+    const int li = e - ustart;
+    // pin starts: byte q of (cum << 8) for q <= 3, byte 3 of cum for q = 4
+    const uint32_t cum = S.y, cumx = cum << 8;
+    const int p = (li >= (int)(cum & 0xFFu)) + (li >= (int)((cum >> 8) & 0xFFu)) +
+                  (li >= (int)((cum >> 16) & 0xFFu)) + (li >= (int)(cum >> 24));
+    const int idx = li - (int)__byte_perm(cumx, cum, p < 4 ? (uint32_t)p : 7u);
+    const float t = ts[e], s = ss[e];
+    const uint32_t c = cyc<kPow2>(t, T, inv_T);
+    float tp = 0.f, sp = 0.f;
+    bool glitch = false;
+    if (idx > 0) {
+      tp = ts[e - 1];
+      sp = ss[e - 1];
+      glitch = cyc<kPow2>(tp, T, inv_T) == c;
+    }
+    const int k = (int)((S.x >> 16) & 7u);
+    const int j = (int)((S.x >> 19) & 7u);
+    float e_int = 0.f, e_sw = 0.f, dp = 0.f;
+    uint32_t s_pre = (S.x >> 12) & 15u;
+    int lis = 0;
+    const float* ub = ts + ustart;
+    if (p == k) {
+      e_sw = __uint_as_float(S.w);
+      if (kDebug) {
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) {
+          if (qq < k) {
+            const int qa = (int)__byte_perm(cumx, cum, (uint32_t)qq);
+            const int qn = (int)__byte_perm(cumx, cum, qq < 3 ? (uint32_t)qq + 1 : 7u) - qa;
+            const float* b = ub + qa;
+            int r = 0;
+#pragma unroll
+            for (int h = 8; h > 0; h >>= 1)
+              if (r + h <= qn && b[r + h - 1] < t) r += h;
+            s_pre ^= ((uint32_t)r & 1u) << qq;
+          }
+        }
+      }
+    } else {
+      const CellDesc& cd = cells[S.x >> 22];
+      s_pre ^= ((uint32_t)idx & 1u) << p;
+      uint32_t s_b = s_pre;
+      // other input pins: events before t (parity) and, for lower pins, a tie at t
+#pragma unroll
+      for (int qq = 0; qq < 4; ++qq) {
+        if (qq < k && qq != p) {
+          const int qa = (int)__byte_perm(cumx, cum, (uint32_t)qq);
+          const int qn = (int)__byte_perm(cumx, cum, qq < 3 ? (uint32_t)qq + 1 : 7u) - qa;
+          const float* b = ub + qa;
+          int r = 0;
+#pragma unroll
+          for (int h = 8; h > 0; h >>= 1)
+            if (r + h <= qn && b[r + h - 1] < t) r += h;
+          const bool eq = qq < p && r < qn && b[r] == t;
+          const uint32_t par = (uint32_t)r & 1u;
+          s_pre ^= par << qq;
+          s_b ^= (par ^ (uint32_t)eq) << qq;
+        }
+      }
+      const int ns = cd.ns, nl = cd.nl;
+#pragma unroll
+      for (int h = 4; h > 0; h >>= 1) {
+        const int cand = lis + h;
+        if (cand <= ns - 2 && s >= cd.sax[cand]) lis = cand;
+      }
+      const float uu = (s - cd.sax[lis]) * cd.isax[lis];
+      const float* L = a.lut + cd.lut_off + ((int)s_pre * ns + lis) * nl + j;
+      const float l00 = __ldg(L), l01 = __ldg(L + 1), l10 = __ldg(L + nl), l11 = __ldg(L + nl + 1);
+      const float vv = __uint_as_float(S.z);
+      const float r0 = fmaf(vv, l01 - l00, l00), r1 = fmaf(vv, l11 - l10, l10);
+      e_int = fmaf(uu, r1 - r0, r0);
+      const float* lk = a.leak + cd.leak_off;
+      dp = __ldg(lk + (s_b ^ (1u << p))) - __ldg(lk + s_b);
+    }
+    const float e_dyn = e_int + e_sw;
+    float e_w;
+    if (glitch) {
+      const float r = fminf(1.f, __fdividef(2000.f * (t - tp), s + sp));
+      e_w = r * e_dyn;
+      acc.e_gl += e_w;
+    } else {
+      acc.e_int += e_int;
+      acc.e_sw += e_sw;
+      e_w = e_dyn;
+    }
+    const uint32_t lc = c - c0;
+    if (lc >= cb) {  // an event outside its band: layout inconsistency
+      berr(a.err, item, kErrTileOverflow);
+      continue;
+    }
+    if (p < k) {
+      const float rem = fmaf(-(float)c, T, t);  // t - c T
+      e_w = fmaf(dp, T - rem, e_w);
+      acc.e_lk = fmaf(dp, a.t_max_f - t, acc.e_lk);
+    }
+    if (kExact) {
+      double* bin = reinterpret_cast<double*>(a.bins + c);
+      atomicAdd(bin, (double)e_w);
+      if (p < k) atomicAdd(bin + 1, (double)dp);
+      atomicAdd(a.cnt_ev + c, 1u);
+      if (glitch) atomicAdd(a.cnt_gl + c, 1u);
+    } else {
+      float* h = reinterpret_cast<float*>(hist + lc);
+      atomicAdd(h, e_w);
+      if (p < k) atomicAdd(h + 1, dp);
+      atomicAdd(reinterpret_cast<uint32_t*>(h + 2), 1u);
+      if (glitch) atomicAdd(reinterpret_cast<uint32_t*>(h + 3), 1u);
+    }
+    if (kDebug) {
+      // CSR index of this event: its rank among its pin's events
+      const uint32_t g = A.L.ugate[it.u0 + (uint32_t)u];
+      const GateRec gr = a.gates[g];
+      const uint64_t pin = (uint64_t)gr.pin_base + p;
+      const uint64_t hi = a.pin_off[pin + 1];
+      uint64_t l = a.pin_off[pin], cnt = hi - l;
+      while (cnt > 0) {
+        const uint64_t half = cnt >> 1;
+        if (a.t[l + half] < t) {
+          l += half + 1;
+          cnt -= half + 1;
+        } else {
+          cnt = half;
+        }
+      }
+      if (l < hi && a.t[l] == t) {
+        a.dbg_state[l] = (uint8_t)s_pre;
+        a.dbg_lut[l] = p < k ? (uint8_t)((lis << 4) | j) : (uint8_t)0xFF;
+        a.dbg_glitch[l] = (uint8_t)glitch;
+      } else {
+        berr(a.err, item, kErrTileOverflow);
+      }
+    }
+  }
+  __syncwarp();
+  if (lane < kMaskWords) mask[lane] = 0u;  // ready for the warp's next item
+  __syncwarp();
+}
+
+template <bool kPow2, bool kDebug, bool kExact>
+__global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  float4* hist = reinterpret_cast<float4*>(smem);
+  CellDesc* cells_s = reinterpret_cast<CellDesc*>(smem + kHist);
+  uint8_t* wbufs = smem + kHist + kCellsB;
   __shared__ uint32_t s_range[2];
-  __shared__ uint32_t s_wsum[kBWarps];
+  __shared__ uint32_t s_seg_end, s_band;
+  __shared__ unsigned int s_next;
+  __shared__ double s_tot[4];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const RunArgs& a = A.r;
+  const uint32_t cb = A.L.band_cycles;
+  const uint32_t n_items = A.L.n_items;
+  uint8_t* wbuf = wbufs + (size_t)warp * kWarpBytes;
 
   if (tid < 4) s_tot[tid] = 0.0;
-  const bool cells_in_smem = a.n_cells <= (uint32_t)kSmemCells;
-  if (cells_in_smem) {
-    const int words = (int)(a.n_cells * sizeof(CellDesc) / 4);
+  for (uint32_t i = tid; i < cb; i += kBT) hist[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  {  // the layout is only built for libraries of at most kSmemCells cells
+    const int words = (int)(min(a.n_cells, (uint32_t)kSmemCells) * sizeof(CellDesc) / 4);
     const uint32_t* src = reinterpret_cast<const uint32_t*>(a.cells);
     uint32_t* dst = reinterpret_cast<uint32_t*>(cells_s);
-    for (int i = tid; i < words; i += kBThreads) dst[i] = src[i];
+    for (int i = tid; i < words; i += kBT) dst[i] = src[i];
   }
-  X.cells = cells_in_smem ? cells_s : a.cells;
-  for (uint32_t i = tid; i < cb; i += kBThreads) {
-    X.W[i] = 0.f;
-    X.D[i] = 0.f;
-    X.EV[i] = 0u;
-    X.GL[i] = 0u;
-  }
+  const CellDesc* cells = cells_s;
+  if (lane < kMaskWords) reinterpret_cast<uint32_t*>(wbuf + (size_t)kItemEvents * 8 + (size_t)kItemUnits * 16)[lane] = 0u;
   if (tid < 2) {
-    // items whose first event falls in this CTA's share of all events
-    const uint64_t total = A.item_ev[n_items];
+    // items whose first event falls in this CTA's share of all banded events
+    const uint64_t total = A.L.n_ev;
     const uint64_t want = total * (uint64_t)(blockIdx.x + tid) / gridDim.x;
     uint32_t lo = 0, n = n_items;
     while (n > 0) {
       const uint32_t half = n >> 1;
-      if (A.item_ev[lo + half] < want) {
+      if (A.L.items[lo + half].e0 < want) {
         lo += half + 1;
         n -= half + 1;
       } else {
@@ -905,260 +755,119 @@ __global__ void __launch_bounds__(kBThreads, 1) k_banded(const BandRunArgs A, ui
     }
     s_range[tid] = (blockIdx.x + tid == gridDim.x) ? n_items : lo;
   }
-  if (tid == 0) {
-    mbar_init(&s_bar[0], 1);
-    mbar_init(&s_bar[1], 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
   __syncthreads();
   const uint32_t i0 = s_range[0], i1 = s_range[1];
-  if (tid == 0 && i0 < i1) bprefetch(A, i0, stages, s_meta[0], &s_bar[0]);
-  uint32_t band = 0xFFFFFFFFu;
   BAcc acc{0.f, 0.f, 0.f, 0.f};
-  int since_flush = 0;
-
-  for (uint32_t item = i0; item < i1; ++item) {
-    const uint32_t q = item - i0, st = q & 1u;
-    if (tid == 0 && item + 1 < i1)  // the other stage was released by the barrier ending item - 1
-      bprefetch(A, item + 1, stages + (st ^ 1u) * kStage, s_meta[st ^ 1u], &s_bar[st ^ 1u]);
-    bool ok = false;
-    for (uint32_t it = 0; it < kWaitLimit && !ok; ++it) ok = mbar_try_wait(&s_bar[st], (q >> 1) & 1u);
-    if (__syncthreads_or(!ok)) {  // a staged copy never landed: report and stop this CTA
-      if (tid == 0) {
-        berr(a.err, item, kErrTileOverflow);
-        if (item + 1 < i1) {  // let our own prefetch of the next item land (bounded) before leaving
-          bool done = false;
-          for (uint32_t it = 0; it < kWaitLimit && !done; ++it)
-            done = mbar_try_wait(&s_bar[st ^ 1u], ((q + 1) >> 1) & 1u);
-        }
-      }
-      return;
+  int since = 0;
+  for (uint32_t cur = i0; cur < i1;) {
+    if (tid == 0) {
+      const uint32_t b = A.L.items[cur].band;
+      s_band = b;
+      s_seg_end = band_end(A.L, cur, i1, b);
+      s_next = 0;
     }
-    const StageMeta M = s_meta[st];
-    const BandItem it = M.it;
-    uint8_t* stage = stages + st * kStage;
-    const float* ts = reinterpret_cast<const float*>(stage) + M.ev_off;
-    const float* ss = reinterpret_cast<const float*>(stage + kStTs) + M.ev_off;
-    if (it.band != band) {
-      if (band != 0xFFFFFFFFu) bflush_band(A, X, band);
-      band = it.band;
-      X.c0 = band * cb;
-      __syncthreads();
+    __syncthreads();
+    const uint32_t band = s_band, seg_end = s_seg_end;
+    const uint32_t c0 = band * cb;
+    // warps take the band's items in turn; the next item's records are
+    // fetched while the current one is worked on
+    uint32_t my = 0;
+    if (lane == 0) my = cur + atomicAdd(&s_next, 1u);
+    my = __shfl_sync(0xffffffffu, my, 0);
+    BandItem it{}, nx{};
+    if (my < seg_end && lane == 0) {
+      it = A.L.items[my];
+      nx = A.L.items[my + 1];
     }
-    if (it.kind == 3) {  // refused by the prefetch bounds check
-      if (tid == 0) berr(a.err, item, kErrTileOverflow);
-      __syncthreads();
-      continue;
+    while (my < seg_end) {
+      uint32_t nxt = 0;
+      if (lane == 0) nxt = cur + atomicAdd(&s_next, 1u);
+      nxt = __shfl_sync(0xffffffffu, nxt, 0);
+      BandItem it2{}, nx2{};
+      if (nxt < seg_end && lane == 0) {
+        it2 = A.L.items[nxt];
+        nx2 = A.L.items[nxt + 1];
+      }
+      BandItem ia, ib;
+      ia.e0 = __shfl_sync(0xffffffffu, it.e0, 0);
+      ia.u0 = __shfl_sync(0xffffffffu, it.u0, 0);
+      ia.band = band;
+      ib.e0 = __shfl_sync(0xffffffffu, nx.e0, 0);
+      ib.u0 = __shfl_sync(0xffffffffu, nx.u0, 0);
+      ib.band = band;
+      band_item<kPow2, kDebug, kExact>(A, cells, hist, wbuf, my, ia, ib, c0, acc);
+      if (++since == kTotEvery) {
+        bflush_acc(acc, s_tot);
+        since = 0;
+      }
+      my = nxt;
+      it = it2;
+      nx = nx2;
     }
-    if (it.kind == 0 || it.kind == 1) {
-      // ---------------- a tile of whole units (light gates or small heavy units)
-      const bool light = it.kind == 0;
-      const uint32_t u0 = light ? it.first * kLightBlock : it.first;
-      const uint32_t u1 = light ? min(it.last * (uint32_t)kLightBlock, A.L.n_light) : it.last;
-      const uint32_t ng = u1 - u0;
-      const uint32_t n = it.n;
-      if (n > (uint32_t)kBTileCap || ng > (uint32_t)kBGateCap) {
-        if (tid == 0) berr(a.err, item, kErrTileOverflow);
-        __syncthreads();
-        continue;
-      }
-      const uint8_t* rec = stage + 2 * kStTs;
-      const GateRun* grun = reinterpret_cast<const GateRun*>(rec + kStRec);
-      uint32_t c5 = 0, state = 0, tot = 0;
-      uint32_t hc[5] = {0, 0, 0, 0, 0};  // events of each pin of this thread's unit
-      if ((uint32_t)tid < ng) {
-        if (light) {
-          c5 = reinterpret_cast<const uint32_t*>(rec)[M.rec_off + tid];
-          state = c5 >> 25;
-#pragma unroll
-          for (int p = 0; p < 5; ++p) hc[p] = (c5 >> (5 * p)) & 31u;
-        } else {
-          const HeavyRec& hr = reinterpret_cast<const HeavyRec*>(rec)[tid];
-#pragma unroll
-          for (int p = 0; p < 5; ++p) hc[p] = hr.cnt[p];
-          state = hr.state;
-        }
-#pragma unroll
-        for (int p = 0; p < 5; ++p) tot += hc[p];
-      }
-      uint32_t inc = tot;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t nn = __shfl_up_sync(0xffffffffu, inc, o);
-        if (lane >= o) inc += nn;
-      }
-      if (lane == 31) s_wsum[warp] = inc;
-      __syncthreads();
-      uint32_t off = inc - tot;
-      for (int w = 0; w < warp; ++w) off += s_wsum[w];
-      if ((uint32_t)tid < ng) {
-        const GateRun gr = grun[tid];
-        BSlot S;
-        bslot_from(S, gr, state);
-        uint32_t pos = off;
-#pragma unroll
-        for (int p = 0; p < 5; ++p) {
-          S.st[p] = (uint16_t)pos;
-          S.len[p] = (uint16_t)hc[p];
-          pos += hc[p];
-        }
-        X.slots[tid] = S;
-        X.sgate[tid] = gr.gate;
-      }
-      __syncthreads();
-      for (uint32_t gi = warp; gi < ng; gi += kBWarps) {
-        const BSlot& S = X.slots[gi];
-        const int k = S.kj & 15;
-        const int b0 = S.st[0], b1 = S.st[k] + S.len[k];
-        for (int e = b0 + lane; e < b1; e += 32) {
-          int p = 0;
-          for (int qq = 1; qq <= k; ++qq) p += (e >= (int)S.st[qq]) ? 1 : 0;
-          X.tag[e] = (uint16_t)((gi << 3) | (uint32_t)p);
-        }
-      }
-      __syncthreads();
-      for (uint32_t e = tid; e < n; e += kBThreads) {
-        const uint32_t tg = X.tag[e];
-        bevent<kPow2, kDebug>(A, X, ts, ss, (int)(tg >> 3), (int)(tg & 7u), (int)e, false, 0.f, 0.f, acc);
-      }
-      __syncthreads();
-    } else {
-      // ---------------- one big heavy unit: stream it in event-count windows
-      float* wts = reinterpret_cast<float*>(stage);
-      float* wss = reinterpret_cast<float*>(stage + kStTs);
-      const HeavyRec hr = A.L.hrec[(uint64_t)band * A.L.n_heavy + it.first];
-      const GateRun gr = A.grun_h[it.first];
-      const int k = (int)((gr.packed >> 16) & 15u);
-      if (tid == 0) {
-        bslot_from(X.slots[0], gr, hr.state);
-        X.sgate[0] = gr.gate;
-        uint64_t pos = hr.base;
-        for (int p = 0; p <= k; ++p) {
-          hs.cur[p] = pos;
-          hs.end[p] = pos + hr.cnt[p];
-          pos += hr.cnt[p];
-          hs.has_prev[p] = 0;
-          hs.prev_t[p] = 0.f;
-          hs.prev_s[p] = 0.f;
-        }
-        hs.pre = 0;
-        hs.done = 0;
-      }
-      __syncthreads();
-      for (;;) {
-        BSlot& S = X.slots[0];
-        if (tid == 0) {
-          uint64_t R = 0;
-          for (int p = 0; p <= k; ++p) R += hs.end[p] - hs.cur[p];
-          if (R == 0) {
-            hs.done = 1;
-          } else {
-            const uint64_t budget = (uint64_t)(kBTileCap - (k + 1));
-            uint32_t pos = 0;
-            for (int p = 0; p <= k; ++p) {
-              const uint64_t r = hs.end[p] - hs.cur[p];
-              uint64_t ap = 0;
-              if (r > 0) {
-                const uint64_t share = budget * r / R;
-                ap = share < 1 ? 1 : share;
-                if (ap > r) ap = r;
-              }
-              S.st[p] = (uint16_t)pos;
-              S.len[p] = (uint16_t)ap;
-              pos += (uint32_t)ap;
-            }
-            for (int p = k + 1; p < 5; ++p) {
-              S.st[p] = (uint16_t)pos;
-              S.len[p] = 0;
-            }
-            // the window's state: band-start state flipped per event already processed
-            S.state = (uint8_t)((hr.state ^ hs.pre) & ((1u << k) - 1u));  // input pins only
-          }
-        }
-        __syncthreads();
-        if (hs.done) break;
-        if (tid <= k) {
-          const uint64_t nx = hs.cur[tid] + S.len[tid];
-          hs.bound[tid] = nx < hs.end[tid] ? A.L.bt[nx] : FLT_MAX;
-        }
-        const int nw = S.st[k] + S.len[k];
-        for (int i = tid; i < nw; i += kBThreads) {
-          int p = 0;
-          for (int qq = 1; qq <= k; ++qq) p += (i >= (int)S.st[qq]) ? 1 : 0;
-          const uint64_t ge = hs.cur[p] + (uint64_t)(i - (int)S.st[p]);
-          wts[i] = A.L.bt[ge];
-          wss[i] = A.L.bs[ge];
-          X.tag[i] = (uint16_t)p;
-        }
-        __syncthreads();
-        if (tid <= k) {
-          float tau = FLT_MAX;
-          for (int qq = 0; qq <= k; ++qq) tau = fminf(tau, hs.bound[qq]);
-          // events at or after the horizon wait for the next window; a
-          // timestamp group is never split
-          if (tau != FLT_MAX) S.len[tid] = (uint16_t)lb_f(wts + S.st[tid], S.len[tid], tau);
-        }
-        __syncthreads();
-        for (int i = tid; i < nw; i += kBThreads) {
-          const int p = X.tag[i];
-          bevent<kPow2, kDebug>(A, X, wts, wss, 0, p, i, hs.has_prev[p] != 0, hs.prev_t[p], hs.prev_s[p], acc);
-        }
-        __syncthreads();
-        if (tid == 0) {
-          uint32_t moved = 0;
-          for (int p = 0; p <= k; ++p) {
-            const uint32_t m = S.len[p];
-            if (m > 0) {
-              hs.prev_t[p] = wts[S.st[p] + m - 1];
-              hs.prev_s[p] = wss[S.st[p] + m - 1];
-              hs.has_prev[p] = 1;
-              hs.cur[p] += m;
-              hs.pre ^= (uint8_t)((m & 1u) << p);
-              moved += m;
-            }
-          }
-          if (moved == 0) {  // cannot happen for valid input; never spin
-            berr(a.err, item, kErrTileOverflow);
-            hs.done = 1;
-          }
-        }
-        __syncthreads();
-        if (hs.done) break;
-      }
-      __syncthreads();
-    }
-    if (++since_flush >= 16) {
-      bflush_acc(acc, s_tot);
-      since_flush = 0;
-    }
+    __syncthreads();
+    bflush_band<kExact>(A, hist, band);
+    cur = seg_end;
+    __syncthreads();
   }
   bflush_acc(acc, s_tot);
-  __syncthreads();
-  if (band != 0xFFFFFFFFu) bflush_band(A, X, band);
   __syncthreads();
   if (tid < 4) atomicAdd(a.totals + tid, s_tot[tid]);
 }
 
-template <bool P, bool D>
-void launch_banded(const BandRunArgs& A, uint32_t n_items, int grid, cudaStream_t st) {
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(k_banded<P, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBSmem);
-    attr = true;
+template <bool P, bool D, bool X>
+void band_attr() {
+  static bool done = false;
+  if (!done) {
+    cudaFuncSetAttribute(k_band<P, D, X>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemB);
+    done = true;
   }
-  k_banded<P, D><<<grid, kBThreads, kBSmem, st>>>(A, n_items);
+}
+
+template <bool P, bool D, bool X>
+int band_occ() {
+  band_attr<P, D, X>();
+  int n = 0;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_band<P, D, X>, kBT, kSmemB);
+  return n > 0 ? n : 1;
+}
+
+template <bool P, bool D, bool X>
+void band_launch(const BandRunArgs& A, int grid, cudaStream_t st) {
+  band_attr<P, D, X>();
+  k_band<P, D, X><<<grid, kBT, kSmemB, st>>>(A);
 }
 
 }  // namespace
 
-cudaError_t band_fused(BandRunArgs& A, uint32_t n_items, int sm_count, bool debug, cudaStream_t st) {
-  if (n_items == 0) return cudaSuccess;
+int band_blocks_per_sm(bool pow2, bool debug, bool exact) {
+  const int sel = (pow2 ? 4 : 0) | (debug ? 2 : 0) | (exact ? 1 : 0);
+  switch (sel) {
+    case 0: return band_occ<false, false, false>();
+    case 1: return band_occ<false, false, true>();
+    case 2: return band_occ<false, true, false>();
+    case 3: return band_occ<false, true, true>();
+    case 4: return band_occ<true, false, false>();
+    case 5: return band_occ<true, false, true>();
+    case 6: return band_occ<true, true, false>();
+    default: return band_occ<true, true, true>();
+  }
+}
+
+cudaError_t band_fused(const BandRunArgs& A, int sm_count, bool debug, bool exact, cudaStream_t st) {
+  if (A.L.n_items == 0) return cudaSuccess;
   const bool pow2 = A.r.inv_t_clk != 0.f;
-  const int grid = sm_count;
-  if (pow2 && debug) launch_banded<true, true>(A, n_items, grid, st);
-  else if (pow2) launch_banded<true, false>(A, n_items, grid, st);
-  else if (debug) launch_banded<false, true>(A, n_items, grid, st);
-  else launch_banded<false, false>(A, n_items, grid, st);
+  const int grid = sm_count * band_blocks_per_sm(pow2, debug, exact);
+  const int sel = (pow2 ? 4 : 0) | (debug ? 2 : 0) | (exact ? 1 : 0);
+  switch (sel) {
+    case 0: band_launch<false, false, false>(A, grid, st); break;
+    case 1: band_launch<false, false, true>(A, grid, st); break;
+    case 2: band_launch<false, true, false>(A, grid, st); break;
+    case 3: band_launch<false, true, true>(A, grid, st); break;
+    case 4: band_launch<true, false, false>(A, grid, st); break;
+    case 5: band_launch<true, false, true>(A, grid, st); break;
+    case 6: band_launch<true, true, false>(A, grid, st); break;
+    default: band_launch<true, true, true>(A, grid, st); break;
+  }
   return cudaGetLastError();
 }
 

@@ -115,96 +115,82 @@ struct RunArgs {
 
 // ------------------------------------------------------------------ banded layout
 //
-// A copy of the events regrouped by clock bands of band_cycles cycles (for one
-// clock period fixed when the layout is built). Inside a band, events keep the
-// per-pin CSR order; the band holds first the light gates (every pin has at
-// most kLightPinMax events in every band), in gate order, then the heavy
-// gates. Per (band, light gate) one packed u32 record: 5-bit event count of
-// each pin (pins 0..4) and, in bits 25..28, the input state at the band start;
-// per (band, heavy gate) an explicit record. Bands start on cycle boundaries,
-// so the first event of a pin in a band is never a glitch of an earlier one.
+// A copy of the events regrouped by clock bands of band_cycles = 2^mb cycles,
+// for one clock period fixed when the layout is built. Every gate's timeline is
+// cut greedily, in cycle order, into windows of whole cycles: a window closes
+// at a band boundary or before a cycle that would give one of its pins more
+// than kUnitPinMax events. A unit is one non-empty (gate, window): its events
+// are stored contiguously, pin by pin, each pin in time order, and its 8-byte
+// record holds the per-pin counts, the input state at the window start, the
+// cell and the load. Units are ordered band by band, gate by gate; work items
+// are runs of whole units of one band. Windows start on cycle boundaries, so
+// the event before a unit's first event on a pin lies in an earlier cycle:
+// glitches never straddle units. Gates with more than kUnitPinMax events of one
+// pin in a single cycle ("big" gates) stay out of the layout and are streamed
+// by the unbanded kernel.
 
-constexpr int kLightPinMax = 31;       // per-pin events per band of a light gate
-constexpr int kLightBlock = 8;         // light gates per partition block
-constexpr int kBandMaxBands = 64;
+constexpr int kUnitPinMax = 15;                  // events per pin per unit (4-bit counts)
+constexpr int kUnitMaxEvents = 5 * kUnitPinMax;  // events per unit
 constexpr uint32_t kBandDefaultCycles = 4096;
-constexpr uint32_t kBandMaxCycles = 4096;  // shared-memory histogram capacity (cycles)
-constexpr int kBTileCap = 4096;        // events per banded tile
-constexpr int kBGateCap = 512;         // gates per banded tile (multiple of kLightBlock)
-constexpr uint32_t kBTileTarget = 2560;  // bucket size; + one light block (<= 8 * 155) stays <= kBTileCap
-constexpr uint32_t kBUnitSmall = kBTileCap - kBTileTarget;  // heavy units up to this share tiles
+constexpr uint32_t kBandMaxCycles = 4096;        // shared-memory histogram capacity (cycles)
+constexpr uint32_t kBandMaxBands = 1u << 20;
+constexpr int kItemEvents = 256;                 // events per item (cap): one warp's work item
+constexpr int kItemUnits = 128;                  // units per item (cap)
+// A new item starts where a unit's event offset enters a new bucket of this
+// many events (or a new band, or every kItemUnits units), so an item holds
+// fewer than kItemBucket + kUnitMaxEvents <= kItemEvents events.
+constexpr uint32_t kItemBucket = kItemEvents - kUnitMaxEvents;
 
-struct __align__(16) HeavyRec {
-  uint64_t base;           // offset of the unit's first event in the banded arrays
-  uint32_t cnt[5];         // events per pin in the band
-  uint32_t state;          // input state at the band start
-};
-
-// Per-run gate record (light and heavy orders): cell (bits 0..15), k (16..19),
-// load-axis interval j (20..23), initial... ; load-axis fraction; switching energy.
-struct __align__(16) GateRun {
-  uint32_t packed;
-  float v;
-  float esw;
-  uint32_t gate;
-};
-
-struct __align__(16) BandItem {
-  uint32_t band;
-  uint32_t kind;   // 0 light tile, 1 heavy tile, 2 streamed heavy unit
-  uint32_t first;  // light block / heavy rank
-  uint32_t last;   // exclusive
-  uint64_t e0;     // first event in the banded arrays
-  uint32_t n;      // events
-  uint32_t pad;
+// Unit record: x = counts of pins 0..4 (4 bits each, bits 0..19) | input state
+// at the window start (bits 20..23) | cell (bits 24..31); y = load (f32 bits).
+struct BandItem {
+  uint64_t e0;    // first event in the banded arrays
+  uint32_t u0;    // first unit
+  uint32_t band;  // band of all its units; items[n_items] is a sentinel
 };
 
 struct BandLayout {
   bool built = false;
   float t_clk = 0.f;
-  uint32_t band_cycles = 0, n_bands = 0;
-  uint32_t n_light = 0, n_heavy = 0, n_lblk = 0;
-  float* bt = nullptr;        // [E] banded times
-  float* bs = nullptr;        // [E] banded slews
-  uint32_t* lrec = nullptr;   // [n_bands * n_light]
-  HeavyRec* hrec = nullptr;   // [n_bands * n_heavy]
-  uint64_t* lblk = nullptr;   // [n_bands * (n_lblk + 1)] offset of each light block; last = light region end
-  uint32_t* lgate = nullptr;  // [n_light] gate id of each light rank
-  uint32_t* hgate = nullptr;  // [n_heavy]
+  uint32_t band_cycles = 0, mb = 0, n_bands = 0;
+  uint64_t n_ev = 0;          // events in the banded arrays
+  uint32_t n_units = 0, n_items = 0, n_big = 0;
+  float* bt = nullptr;        // [n_ev + pad] banded times
+  float* bs = nullptr;        // [n_ev + pad] banded slews
+  uint2* urec = nullptr;      // [n_units + pad] unit records
+  uint32_t* ugate = nullptr;  // [n_units] gate of each unit
+  BandItem* items = nullptr;  // [n_items + 1]
+  uint32_t* big = nullptr;    // [n_big] gates streamed by the unbanded kernel
 };
 
 struct BandBuildArgs {
   const GateRec* gates;
   uint32_t n_gates;
-  uint64_t n_pins, n_events;
+  uint64_t n_events;
   const uint64_t* pin_off;
   const float* t;
   const float* s;
   float t_clk, inv_t_clk;
   bool pow2;
-  uint32_t band_cycles, n_bands;
-  uint32_t* cnt;         // [n_pins * n_bands] events per (pin, band) -- temporary
-  uint8_t* heavy;        // [n_gates] -- temporary
-  uint32_t* rank;        // [n_gates] light or heavy rank -- temporary
-  uint32_t* blk;         // scan scratch -- temporary
-  uint32_t* totals;      // [4] n_light, n_heavy -- temporary
-  uint32_t* unit_size;   // [n_bands * n_gates] -- temporary
-  uint64_t* unit_off;    // [n_bands * n_gates + 1] -- temporary
+  uint32_t mb, n_bands;
+  uint8_t* bigf;         // [G] 1 for a big gate -- temporary
+  uint32_t* cnt_gb;      // [n_bands * G] units per (band, gate) -- temporary
+  uint32_t* evc_gb;      // [n_bands * G] events per (band, gate) -- temporary
+  uint64_t* ubase;       // [n_bands * G + 1] first unit of each (band, gate) -- temporary
+  uint64_t* ebase;       // [n_bands * G + 1] first banded event of each (band, gate) -- temporary
+  uint32_t* uband;       // [n_units] -- temporary
+  uint64_t* uoff;        // [n_units + 1] -- temporary
+  uint32_t* flags;       // [n_units] item heads -- temporary
+  uint64_t* ipos;        // [n_units + 1] -- temporary
   uint64_t* scan_blk;    // scan scratch -- temporary
+  uint32_t* counters;    // [4]: big gates, gates with windows narrower than a band -- temporary
   BandLayout L;
   unsigned long long* err;
 };
 
 struct BandRunArgs {
-  RunArgs r;             // cells, lut, leak, gates, params, totals, err, debug, bins (fp64 layout)
+  RunArgs r;             // cells, lut, leak, gates, params, bins, totals, err, debug
   BandLayout L;
-  GateRun* grun_l;       // [n_light]
-  GateRun* grun_h;       // [n_heavy]
-  BandItem* items;
-  uint64_t* item_ev;     // [n_items + 1] event prefix of the items
-  uint32_t* item_counts; // [4]: light items, heavy items
-  uint32_t* blk;         // scan scratch
-  uint32_t max_items;
 };
 
 // kernels (pa_kernels.cu)
@@ -219,20 +205,23 @@ size_t fused_smem_bytes();
 // Two kernels: per-chunk step sums, then the scan/apply pass. In fast mode it
 // writes u32 counts to cnt_ev / cnt_gl (if set) and flags kErrCountOverflow
 // when a cycle's f32 count may be inexact.
-// banded layout (pa_banded.cu)
-// phase 1: counts per (pin, band), light/heavy ranks, totals[0..1] = n_light,
-// n_heavy; phase 2 (after L.lrec/hrec/lblk are allocated): offsets, scatter.
-cudaError_t band_build_phase1(BandBuildArgs& a, cudaStream_t st);
-cudaError_t band_build_phase2(BandBuildArgs& a, cudaStream_t st);
+// banded layout (pa_banded.cu), built in steps with host reads in between:
+// count  windows per gate: units and events per (band, gate), their scans
+//        (ubase / ebase, totals at index n_bands * G), big gates (counters[0]);
+// write  unit records and the event scatter, item heads and their scan
+//        (ipos[n_units] = n_items), after the layout arrays are allocated;
+// items  the item list (after it is allocated).
+cudaError_t band_build_count(BandBuildArgs& a, cudaStream_t st);
+cudaError_t band_build_write(BandBuildArgs& a, cudaStream_t st);
+cudaError_t band_build_items(BandBuildArgs& a, cudaStream_t st);
 uint32_t band_scan_blocks(uint64_t n);
-uint32_t band_max_items(const BandLayout& L);
-// Item list of a run: flags / pos / scan_blk / item_n are scratch sized for
-// band_max_items(); host_items[0..1] = light and heavy item counts.
-cudaError_t band_partition(BandRunArgs& A, uint32_t* flags, uint64_t* pos, uint64_t* scan_blk, uint32_t* item_n,
-                           uint32_t* host_items, cudaStream_t st);
-// Per-run gate records, then the banded fused kernel over n_items items.
-cudaError_t band_gate_run(BandRunArgs& A, cudaStream_t st);
-cudaError_t band_fused(BandRunArgs& A, uint32_t n_items, int sm_count, bool debug, cudaStream_t st);
+// Exclusive scan of u32 into u64 (out[n] = total); blk holds band_scan_blocks(n) entries.
+cudaError_t scan_u32_to_u64(const uint32_t* in, uint64_t n, uint64_t* blk, uint64_t* out, cudaStream_t st);
+// P0 of a run: leakage of every gate's initial input state, added to *r.p0.
+cudaError_t band_p0(const RunArgs& r, cudaStream_t st);
+// The banded fused kernel over the layout's items.
+cudaError_t band_fused(const BandRunArgs& A, int sm_count, bool debug, bool exact, cudaStream_t st);
+int band_blocks_per_sm(bool pow2, bool debug, bool exact);
 
 cudaError_t launch_final_reduce(const RunArgs& a, double t_clk, double t_max, float* wave_out,
                                 double* p_out, bool exact, cudaStream_t st);
