@@ -57,8 +57,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle sample time")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--banded", action="store_true",
-                    help="build cycle bands (pa_build_bands) and time the banded kernel")
+    ap.add_argument("--unbanded", action="store_true",
+                    help="skip the cycle-banded layout (pa_build_bands) and time the unbanded kernel")
     ap.add_argument("--band-cycles", type=int, default=0, help="cycles per band (0 = library default)")
     ap.add_argument("--synth", nargs="*", default=[], metavar="KNOB=VALUE",
                     help="generator overrides for a scaled-down profiling case, e.g. n_gates=1000000 "
@@ -221,17 +221,22 @@ def kernel_source_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(config: int):
-    """DRAM bytes per fused launch from the committed ncu summary, if it was
-    taken on the current kernel source (else None)."""
-    p = os.path.join(ROOT, "profiles", "fused_power_kernel.md")
-    if not os.path.exists(p):
+def ncu_traffic(kernel: str, config: int):
+    """DRAM bytes per launch of `kernel` on `config` from a committed ncu
+    summary under profiles/, if it was taken on the current kernel source
+    (else None)."""
+    pat = re.compile(r"traffic_bytes_per_launch\s+%s\s+config%d:\s*([0-9.eE+]+)\s+source:\s*([0-9a-f]+)"
+                     % (re.escape(kernel), config))
+    d = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(d):
         return None
-    txt = open(p).read()
-    m = re.search(r"traffic_bytes_per_launch_config%d:\s*([0-9.eE+]+)\s+source:\s*([0-9a-f]+)" % config, txt)
-    if not m or m.group(2) != kernel_source_digest():
-        return None
-    return float(m.group(1))
+    for name in sorted(os.listdir(d)):
+        if not name.endswith(".md"):
+            continue
+        m = pat.search(open(os.path.join(d, name)).read())
+        if m and m.group(2) == kernel_source_digest():
+            return float(m.group(1))
+    return None
 
 
 def cpu_baseline(config, seed, target_s, n_events_total, n_gates_total):
@@ -335,7 +340,8 @@ def run_ours(args):
     pa = glp.PowerAnalyzer(local, stream.cuda_stream)
     pa.load_workload(w)
     build_ms = None
-    if args.banded:
+    banded = not args.unbanded
+    if banded:
         t0 = time.perf_counter()
         pa.build_bands(w.t_clk_ns, args.band_cycles)
         build_ms = (time.perf_counter() - t0) * 1e3
@@ -378,7 +384,7 @@ def run_ours(args):
     if args.e2e_steps > 0:
         def e2e_step():
             pa.load_events(w.pin_off, w.t_ns, w.slew_ps, w.value)
-            if args.banded:
+            if banded:
                 pa.build_bands(w.t_clk_ns, args.band_cycles)
             step()
         for _ in range(2):
@@ -398,7 +404,8 @@ def run_ours(args):
     B = algorithmic_bytes(w)
     peak, peak_kind = hbm_peak()
     achieved = B / (fused_mean * 1e-3) / 1e9
-    traffic = ncu_traffic(args.config)
+    kname = "k_band" if r["path"] == glp.PA_PATH_BANDED else "k_fused"
+    traffic = None if args.synth else ncu_traffic(kname, args.config)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args.config, args.seed, args.cpu_seconds, E, G)
@@ -412,15 +419,16 @@ def run_ours(args):
             "gate_cycles_per_s": world * G * N * args.steps / (el_ms * 1e-3),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
-                         "kernel": ("k_banded" if r["path"] == glp.PA_PATH_BANDED else "k_fused")
-                         + " (fused dynamic + leakage power)",
+                         "kernel": kname + " (fused dynamic + leakage power"
+                         + (", with the unbanded kernel streaming big gates)" if r["path"] == glp.PA_PATH_BANDED
+                            else ")"),
                          "algorithmic_bytes_per_launch": B, "mean_launch_ms": fused_mean,
                          "peak_source": f"{peak_kind} HBM copy bandwidth"},
             "cpu_baseline": cpu,
             "e2e": None if e2e_value is None else {"value": e2e_value, "unit": "events/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
                     "note": "per step: pa_load_events from pinned host memory (device-side validation) + "
-                            + ("pa_build_bands + " if args.banded else "")
+                            + ("pa_build_bands + " if banded else "")
                             + "pa_run + waveform/count copy to host; library and netlist loaded once"},
             "clocks": clk.summary(),
             "gpu_launches": launches,

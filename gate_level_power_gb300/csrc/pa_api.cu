@@ -39,7 +39,7 @@ struct pa_ctx {
   bool has_lib = false;
   uint32_t n_cells = 0;
   std::vector<CellDesc> h_cells;
-  DevBuf cells, lut, leak;
+  DevBuf cells, lut, leak, patch, dleak;
 
   // netlist
   bool has_net = false;
@@ -243,6 +243,8 @@ int run_pass(pa_ctx* c, const RunPlan& plan, const PassBufs& B, pa_result* out, 
   a.n_cells = c->n_cells;
   a.lut = (const float*)c->lut.p;
   a.leak = (const float*)c->leak.p;
+  a.patch = (const float4*)c->patch.p;
+  a.dleak = (const float*)c->dleak.p;
   a.gates = (const GateRec*)c->gates.p;
   a.n_gates = plan.G;
   a.pin_off = (const uint64_t*)c->pin_off.p;
@@ -415,7 +417,7 @@ void pa_destroy(pa_ctx* c) {
   if (!c) return;
   cudaSetDevice(c->device);
   if (c->stream) cudaStreamSynchronize(c->stream);
-  DevBuf* all[] = {&c->cells, &c->lut, &c->leak, &c->gates, &c->pin_off, &c->gate_off, &c->t, &c->s,
+  DevBuf* all[] = {&c->cells, &c->lut, &c->leak, &c->patch, &c->dleak, &c->gates, &c->pin_off, &c->gate_off, &c->t, &c->s,
                    &c->value_tmp, &c->err_word, &c->tmax_bits, &c->bins, &c->part_blk,
                    &c->part_counts, &c->tiles, &c->heavy, &c->p0_tot, &c->p_out, &c->dbg[0],
                    &c->dbg[1], &c->dbg[2], &c->wave_tmp, &c->cnt_tmp, &c->scratch_small,
@@ -480,6 +482,32 @@ int pa_load_library(pa_ctx* c, const pa_library* L) {
     if (!is_finite_f(L->leak[i])) return fail(c, PA_ERR_ARG, "leakage value %llu not finite", (unsigned long long)i);
     leak_uw[i] = (float)((double)L->leak[i] * 1e-3);  // nW -> uW (= fJ / ns)
   }
+  // derived tables: LUT corner patches and per-(state, pin) leakage steps
+  std::vector<float> patch;
+  std::vector<float> dleak((size_t)L->n_cells * kDleakStride, 0.f);
+  for (uint32_t ci = 0; ci < L->n_cells; ++ci) {
+    CellDesc& d = cells[ci];
+    d.patch_off = (uint32_t)(patch.size() / 4);
+    const int k = d.k, ns = d.ns, nl = d.nl;
+    for (int st = 0; st < (1 << k); ++st) {
+      const float* T = L->lut + d.lut_off + (size_t)st * ns * nl;
+      for (int i = 0; i + 1 < ns; ++i)
+        for (int j = 0; j + 1 < nl; ++j) {
+          patch.push_back(T[i * nl + j]);
+          patch.push_back(T[i * nl + j + 1]);
+          patch.push_back(T[(i + 1) * nl + j]);
+          patch.push_back(T[(i + 1) * nl + j + 1]);
+        }
+      for (int p = 0; p < k; ++p) {
+        const float a = leak_uw[d.leak_off + (st ^ (1 << p))], b = leak_uw[d.leak_off + st];
+        dleak[(size_t)ci * kDleakStride + st * 4 + p] = a - b;
+      }
+    }
+  }
+  PA_TRY(dreserve(c, c->patch, patch.size() * sizeof(float)));
+  PA_TRY(dreserve(c, c->dleak, dleak.size() * sizeof(float)));
+  CUDA_TRY(c, cudaMemcpyAsync(c->patch.p, patch.data(), patch.size() * sizeof(float), cudaMemcpyHostToDevice, c->stream));
+  CUDA_TRY(c, cudaMemcpyAsync(c->dleak.p, dleak.data(), dleak.size() * sizeof(float), cudaMemcpyHostToDevice, c->stream));
   PA_TRY(dreserve(c, c->cells, cells.size() * sizeof(CellDesc)));
   PA_TRY(dreserve(c, c->lut, L->lut_len * sizeof(float)));
   PA_TRY(dreserve(c, c->leak, L->leak_len * sizeof(float)));

@@ -392,32 +392,74 @@ cudaError_t band_p0(const RunArgs& r, cudaStream_t st) {
 
 // ------------------------------------------------------------------ banded fused kernel
 //
-// One CTA of 32 warps per SM takes a contiguous, event-balanced run of items
+// One CTA of 24 warps per SM takes a contiguous, event-balanced run of items
 // and works through it band by band. Inside a band the warps take items from a
-// shared counter and work independently: a warp copies its item's events and
-// unit records into its own shared-memory buffer (coalesced streaming loads),
-// decodes one unit record per lane into a 16-byte slot and marks each unit's
-// first event in a bit mask, then processes one event per lane: unit from the
-// mask (count of unit starts at or before it), pin from the slot's pin
-// offsets, gate state, LUT, glitch and leakage, and the sums go into the
-// band's cycle bins in shared memory. When the band's items are done the CTA
-// adds the bins to global memory with one TMA bulk reduction.
+// shared counter and work independently, each with two shared-memory stages:
+// while a warp works on one item, lane 0 has the next item's events and unit
+// records on their way into the other stage (TMA bulk copies completing on the
+// stage's mbarrier) and the item after that's record loaded. Per item, one lane
+// per unit decodes its record into a 16-byte slot and marks the unit's first
+// event in a bit mask; then one lane per event finds its unit from the mask
+// (count of unit starts at or before it), its pin from the slot's pin offsets,
+// and computes gate state, LUT energy (one corner-patch load), glitch and
+// leakage step; the sums go into the band's cycle bins in shared memory. When
+// the band's items are done the CTA adds the bins to global memory with one
+// TMA bulk reduction.
 
 namespace {
 
-constexpr int kBT = 1024;
-constexpr int kBW = kBT / 32;
+constexpr int kBW = 32;
+constexpr int kBT = kBW * 32;
 constexpr int kMaskWords = kItemEvents / 32;
-constexpr size_t kWarpBytes = (size_t)kItemEvents * 8 + (size_t)kItemUnits * 16 + 2 * kMaskWords * 4;
+constexpr int kStEv = kItemEvents + 8;                         // staged floats (16-byte rounding)
+constexpr size_t kStRecB = (size_t)(kItemUnits + 2) * 8;
+constexpr size_t kStageB = 2 * (size_t)kStEv * 4 + kStRecB;
+// stage, unit slots, input / output start masks and word prefixes, rank maps
+constexpr size_t kWarpB = kStageB + (size_t)kItemUnits * 16 + 4 * kMaskWords * 4 + 2 * (size_t)kItemUnits * 4;
 constexpr size_t kHist = (size_t)kBandMaxCycles * 16;
-constexpr size_t kCellsB = (size_t)kSmemCells * sizeof(CellDesc);
-constexpr size_t kSmemB = kHist + kCellsB + kBW * kWarpBytes;
-static_assert(kWarpBytes % 16 == 0 && kHist % 16 == 0 && kCellsB % 16 == 0, "alignment");
-static_assert(kSmemB <= 227 * 1024, "shared memory budget");
-constexpr int kTotEvery = 16;  // items between flushes of a warp's per-lane totals
+// Cell table in shared memory, structure of arrays: per cell one info word
+// (ns | nl << 8 | k << 16), the patch offset, and the four axis arrays at a
+// stride of 9 words, so lanes reading different cells hit different banks.
+constexpr int kAxStride = 9;
+constexpr size_t kCellsB = (size_t)kSmemCells * (2 + 4 * kAxStride) * 4;
+constexpr size_t kSmemB = kHist + kCellsB + kBW * kWarpB;
+static_assert(kStageB % 16 == 0 && kWarpB % 16 == 0 && kHist % 16 == 0 && kCellsB % 16 == 0, "alignment");
+static_assert(kSmemB + 1024 <= 227 * 1024, "shared memory budget");
+constexpr int kTotEvery = 16;              // items between flushes of a warp's per-lane totals
+constexpr uint32_t kWaitLimit = 1u << 24;  // mbarrier polls before giving up
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_arrive(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bulk copy global -> shared, completing on the mbarrier (16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
 }
 
 // Bulk f32 add of shared memory into global memory (16-byte aligned, size % 16 == 0).
@@ -447,9 +489,18 @@ __device__ __forceinline__ void bflush_acc(BAcc& acc, double* s_tot) {
   acc = BAcc{0.f, 0.f, 0.f, 0.f};
 }
 
+// The band's bins in shared memory: 16 bytes per cycle holding {W, D, ev, gl}
+// with the fields rotated by (cycle >> 3) & 3 words, so that one field of
+// 32 different cycles falls in 32 different banks (unrotated, every W would
+// sit in the same 8 banks). Word of field f of local cycle lc:
+__device__ __forceinline__ uint32_t hist_word(uint32_t lc, uint32_t f) {
+  return 4u * lc + ((f + (lc >> 3)) & 3u);
+}
+
 // Add the band's shared-memory bins to the global bins and clear them. Fast
-// mode: {W, D, ev, gl} as f32 by one bulk reduction (counts converted in
-// place). Exact mode adds per event to global memory; nothing to flush.
+// mode: rows are put back in {W, D, ev, gl} order as f32 (counts converted in
+// place), then one bulk reduction. Exact mode adds per event to global
+// memory; nothing to flush.
 template <bool kExact>
 __device__ void bflush_band(const BandRunArgs& A, float4* hist, uint32_t band) {
   const uint32_t cb = A.L.band_cycles, N = A.r.n_cycles;
@@ -457,10 +508,27 @@ __device__ void bflush_band(const BandRunArgs& A, float4* hist, uint32_t band) {
   const uint32_t nb = c0 < N ? min(cb, N - c0) : 0u;
   if (!kExact) {
     for (uint32_t i = threadIdx.x; i < nb; i += kBT) {
-      float4 h = hist[i];
-      h.z = (float)__float_as_uint(h.z);
-      h.w = (float)__float_as_uint(h.w);
-      hist[i] = h;
+      const uint32_t w = __float_as_uint(hist[i].x), x = __float_as_uint(hist[i].y),
+                     y = __float_as_uint(hist[i].z), z = __float_as_uint(hist[i].w);
+      const uint32_t rot = (i >> 3) & 3u;
+      // field f sits at word (f + rot) & 3: rotate the row left by rot words
+      uint32_t f0 = w, f1 = x, f2 = y, f3 = z;
+      if (rot & 1u) {
+        const uint32_t t0 = f0;
+        f0 = f1;
+        f1 = f2;
+        f2 = f3;
+        f3 = t0;
+      }
+      if (rot & 2u) {
+        uint32_t t0 = f0;
+        f0 = f2;
+        f2 = t0;
+        t0 = f1;
+        f1 = f3;
+        f3 = t0;
+      }
+      hist[i] = make_float4(__uint_as_float(f0), __uint_as_float(f1), (float)f2, (float)f3);
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
@@ -485,231 +553,329 @@ __device__ uint32_t band_end(const BandLayout& L, uint32_t lo, uint32_t hi, uint
   return lo;
 }
 
-// One item on one warp.
+// Staging geometry of an item: events [e0, e0 + n) and units [u0, u0 + nu),
+// rounded out to 16-byte copies. ok is false for an item that cannot be
+// staged (never for a consistent layout).
+struct ItemGeo {
+  uint64_t e0, ea;
+  uint32_t u0, ra, n, nu, ev_off, rec_off, ev_bytes, rec_bytes;
+  bool ok;
+};
+
+__device__ __forceinline__ ItemGeo item_geo(uint64_t e0, uint32_t u0, uint64_t e1, uint32_t u1) {
+  ItemGeo g;
+  g.e0 = e0;
+  g.u0 = u0;
+  g.ea = e0 & ~3ull;
+  g.ra = u0 & ~1u;
+  g.ev_off = (uint32_t)(e0 - g.ea);
+  g.rec_off = u0 - g.ra;
+  g.ok = e1 > e0 && u1 > u0 && e1 - e0 <= (uint64_t)kItemEvents && u1 - u0 <= (uint32_t)kItemUnits;
+  g.n = g.ok ? (uint32_t)(e1 - e0) : 0u;
+  g.nu = g.ok ? u1 - u0 : 0u;
+  g.ev_bytes = ((g.ev_off + g.n + 3u) & ~3u) * 4u;
+  g.rec_bytes = ((g.rec_off + g.nu + 1u) & ~1u) * 8u;
+  return g;
+}
+
+// Lane 0: start the copies of an item into a stage (an empty arrival for an
+// item that cannot be staged, so the wait still completes).
+__device__ __forceinline__ void stage_item(const BandLayout& L, const ItemGeo& g, uint8_t* stage, uint64_t* bar) {
+  if (!g.ok) {
+    mbar_expect_arrive(bar, 0);
+    return;
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  mbar_expect_arrive(bar, 2 * g.ev_bytes + g.rec_bytes);
+  bulk_g2s(stage, L.bt + g.ea, g.ev_bytes, bar);
+  bulk_g2s(stage + (size_t)kStEv * 4, L.bs + g.ea, g.ev_bytes, bar);
+  bulk_g2s(stage + 2 * (size_t)kStEv * 4, L.urec + g.ra, g.rec_bytes, bar);
+}
+
+// Events of a sorted pin segment b[0, qn) (qn <= 15) earlier than t: the
+// first three without branches, the rest by binary lifting.
+__device__ __forceinline__ int seg_rank(const float* b, int qn, float t) {
+  int r = ((int)(qn > 0) & (int)(b[0] < t)) + ((int)(qn > 1) & (int)(b[1] < t)) + ((int)(qn > 2) & (int)(b[2] < t));
+  if (r == 3 && qn > 3) {
+#pragma unroll
+    for (int h = 8; h > 0; h >>= 1)
+      if (r + h <= qn && b[r + h - 1] < t) r += h;
+  }
+  return r;
+}
+
+// Start of pin q (0..4) inside its unit from the slot's cumulative counts.
+__device__ __forceinline__ int pin_start(uint32_t cum, int q) {
+  return (int)__byte_perm(cum << 8, cum, q < 4 ? (uint32_t)q : 7u);
+}
+
+struct CellTab {
+  const uint32_t* info;   // [kSmemCells] ns | nl << 8 | k << 16
+  const uint32_t* patch;  // [kSmemCells] patch offset
+  const float* sax;       // [kSmemCells * kAxStride]
+  const float* isax;
+  const float* lax;
+  const float* ilax;
+};
+
+// Per-warp scratch of the banded kernel.
+struct WarpScratch {
+  const uint8_t* stage;
+  uint4* slots;        // [kItemUnits]
+  uint32_t* in_mask;   // [kMaskWords] first input event of each unit, input index space
+  uint32_t* in_pre;    // [kMaskWords] units starting before each word
+  uint32_t* out_mask;  // [kMaskWords] same for the output index space
+  uint32_t* out_pre;
+  uint32_t* in_map;    // [kItemUnits] unit | first input index << 8, by rank
+  uint32_t* out_map;
+};
+
+// Everything after the gate state and energies are known: glitch scaling,
+// totals, in-cycle leakage part and the bins (and the debug outputs).
 template <bool kPow2, bool kDebug, bool kExact>
-__device__ __forceinline__ void band_item(const BandRunArgs& A, const CellDesc* cells, float4* hist, uint8_t* wbuf,
-                                          uint32_t item, const BandItem& it, const BandItem& nx, uint32_t c0,
+__device__ __forceinline__ void event_tail(const BandRunArgs& A, float4* hist, const float* ts, const float* ss,
+                                           int e, int idx, int p, int k, float t, float s, float e_int,
+                                           float e_sw, float dp, uint32_t s_pre, int lis, int j, uint32_t gate,
+                                           uint32_t item, uint32_t c0, BAcc& acc) {
+  const RunArgs& a = A.r;
+  const float T = a.t_clk, inv_T = a.inv_t_clk;
+  const uint32_t c = cyc<kPow2>(t, T, inv_T);
+  float tp = 0.f, sp = 0.f;
+  bool glitch = false;
+  if (idx > 0) {  // the pin's previous event is the staged event before this one
+    tp = ts[e - 1];
+    sp = ss[e - 1];
+    glitch = cyc<kPow2>(tp, T, inv_T) == c;
+  }
+  const float e_dyn = e_int + e_sw;
+  float e_w;
+  if (glitch) {
+    const float r = fminf(1.f, __fdividef(2000.f * (t - tp), s + sp));
+    e_w = r * e_dyn;
+    acc.e_gl += e_w;
+  } else {
+    acc.e_int += e_int;
+    acc.e_sw += e_sw;
+    e_w = e_dyn;
+  }
+  const uint32_t lc = c - c0;
+  if (lc >= A.L.band_cycles) {  // an event outside its band: layout inconsistency
+    berr(a.err, item, kErrTileOverflow);
+    return;
+  }
+  if (p < k) {
+    const float rem = fmaf(-(float)c, T, t);  // t - c T
+    e_w = fmaf(dp, T - rem, e_w);
+    acc.e_lk = fmaf(dp, a.t_max_f - t, acc.e_lk);
+  }
+  if (kExact) {
+    double* bin = reinterpret_cast<double*>(a.bins + c);
+    atomicAdd(bin, (double)e_w);
+    if (p < k) atomicAdd(bin + 1, (double)dp);
+    atomicAdd(a.cnt_ev + c, 1u);
+    if (glitch) atomicAdd(a.cnt_gl + c, 1u);
+  } else {
+    float* h = reinterpret_cast<float*>(hist);
+    atomicAdd(h + hist_word(lc, 0), e_w);
+    if (p < k) atomicAdd(h + hist_word(lc, 1), dp);
+    atomicAdd(reinterpret_cast<uint32_t*>(h + hist_word(lc, 2)), 1u);
+    if (glitch) atomicAdd(reinterpret_cast<uint32_t*>(h + hist_word(lc, 3)), 1u);
+  }
+  if (kDebug) {
+    // CSR index of this event: its rank among its pin's events
+    const GateRec gr = a.gates[gate];
+    const uint64_t pin = (uint64_t)gr.pin_base + p;
+    const uint64_t hi = a.pin_off[pin + 1];
+    uint64_t l = a.pin_off[pin], cnt = hi - l;
+    while (cnt > 0) {
+      const uint64_t half = cnt >> 1;
+      if (a.t[l + half] < t) {
+        l += half + 1;
+        cnt -= half + 1;
+      } else {
+        cnt = half;
+      }
+    }
+    if (l < hi && a.t[l] == t) {
+      a.dbg_state[l] = (uint8_t)s_pre;
+      a.dbg_lut[l] = p < k ? (uint8_t)((lis << 4) | j) : (uint8_t)0xFF;
+      a.dbg_glitch[l] = (uint8_t)glitch;
+    } else {
+      berr(a.err, item, kErrTileOverflow);
+    }
+  }
+}
+
+// Rank of this lane's index i in an index space (start mask + word prefixes):
+// the number of unit starts at or before i, minus one.
+__device__ __forceinline__ int space_rank(const uint32_t* mask, const uint32_t* pre, int i, uint32_t le_mask) {
+  const int w = i >> 5;
+  return (int)pre[w] + __popc(mask[w] & le_mask) - 1;
+}
+
+// Marks a unit that starts at index o of a space and covers cnt indices.
+__device__ __forceinline__ void space_mark(uint32_t* mask, uint32_t* pre, uint32_t* map, uint32_t rank, uint32_t o,
+                                           uint32_t cnt, uint32_t unit) {
+  map[rank] = unit | (o << 8);
+  if (o < (uint32_t)kItemEvents) atomicOr(mask + (o >> 5), 1u << (o & 31u));
+  // words whose first index lies in (o, o + cnt] follow this unit
+  const uint32_t end = o + cnt;
+  for (uint32_t w = (o >> 5) + 1; w <= (end >> 5) && w < (uint32_t)kMaskWords; ++w) pre[w] = rank + 1;
+}
+
+// One staged item on one warp: unit slots, then the input events, then the
+// output events (each lane one event of one kind at a time).
+template <bool kPow2, bool kDebug, bool kExact>
+__device__ __forceinline__ void band_item(const BandRunArgs& A, const CellTab& CT, float4* hist,
+                                          const WarpScratch& X, uint32_t item, const ItemGeo& g, uint32_t c0,
                                           BAcc& acc) {
   const RunArgs& a = A.r;
   const int lane = threadIdx.x & 31;
-  float* ts = reinterpret_cast<float*>(wbuf);
-  float* ss = ts + kItemEvents;
-  uint4* slots = reinterpret_cast<uint4*>(ss + kItemEvents);
-  uint32_t* mask = reinterpret_cast<uint32_t*>(slots + kItemUnits);
-  uint32_t* wpre = mask + kMaskWords;
-  const uint64_t n64 = nx.e0 - it.e0;
-  const uint32_t nu = nx.u0 - it.u0;
-  if (nx.e0 < it.e0 || nx.u0 < it.u0 || n64 == 0 || n64 > (uint64_t)kItemEvents || nu == 0 ||
-      nu > (uint32_t)kItemUnits) {
+  if (!g.ok) {
     if (lane == 0) berr(a.err, item, kErrTileOverflow);
     return;
   }
-  const int n = (int)n64;
-  // ---- stage events (streaming loads: read once)
-#pragma unroll
-  for (int r = 0; r < kItemEvents / 32; ++r) {
-    const int e = lane + 32 * r;
-    if (e < n) {
-      ts[e] = __ldcs(A.L.bt + it.e0 + e);
-      ss[e] = __ldcs(A.L.bs + it.e0 + e);
-    }
-  }
-  // ---- units: sizes, offsets (warp scan), slots, start mask
+  const float* ts = reinterpret_cast<const float*>(X.stage) + g.ev_off;
+  const float* ss = reinterpret_cast<const float*>(X.stage + (size_t)kStEv * 4) + g.ev_off;
+  const uint2* rec = reinterpret_cast<const uint2*>(X.stage + 2 * (size_t)kStEv * 4) + g.rec_off;
+  const int n = (int)g.n, nu = (int)g.nu;
+  // ---- units. One packed scan gives, per unit, its offsets in the input and
+  // output index spaces and its ranks among units with inputs / outputs.
   uint32_t carry = 0;
-#pragma unroll
-  for (int r = 0; r < kItemUnits / 32; ++r) {
-    const uint32_t uu = (uint32_t)lane + 32u * r;
-    uint32_t x = 0, size = 0;
+  for (int r = 0; r < (nu + 31) / 32; ++r) {
+    const int uu = lane + 32 * r;
+    uint32_t x = 0, pk = 0, n_in = 0, n_out = 0;
     float C = 0.f;
+    int k = 0;
     if (uu < nu) {
-      const uint2 rec = __ldcs(A.L.urec + it.u0 + uu);
-      x = rec.x;
-      C = __uint_as_float(rec.y);
+      const uint2 rr = rec[uu];
+      x = rr.x;
+      C = __uint_as_float(rr.y);
+      k = (int)((CT.info[x >> 24] >> 16) & 0xFFu);
 #pragma unroll
-      for (int p = 0; p < 5; ++p) size += (x >> (4 * p)) & 15u;
+      for (int p = 0; p < 4; ++p) n_in += p < k ? (x >> (4 * p)) & 15u : 0u;
+      n_out = (x >> (4 * k)) & 15u;
+      pk = n_in | (n_out << 9) | ((uint32_t)(n_in > 0) << 18) | ((uint32_t)(n_out > 0) << 25);
     }
-    uint32_t inc = size;
+    uint32_t inc = pk;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const uint32_t v = __shfl_up_sync(0xffffffffu, inc, o);
       if (lane >= o) inc += v;
     }
-    const uint32_t off = carry + inc - size;
+    const uint32_t ex = carry + inc - pk;
     carry += __shfl_sync(0xffffffffu, inc, 31);
     if (uu < nu) {
+      const uint32_t oi = ex & 511u, oo = (ex >> 9) & 511u, ri = (ex >> 18) & 127u, ro = ex >> 25;
       const uint32_t cell = x >> 24;
-      const CellDesc& cd = cells[cell];
-      const int k = cd.k;
+      const int nl = (int)((CT.info[cell] >> 8) & 0xFFu);
+      const float* lax = CT.lax + cell * kAxStride;
       int j = 0;
-      for (int m = 1; m <= cd.nl - 2; ++m) j += (C >= cd.lax[m]) ? 1 : 0;
-      const float v = (C - cd.lax[j]) * cd.ilax[j];
+      for (int m = 1; m <= nl - 2; ++m) j += (C >= lax[m]) ? 1 : 0;
+      const float v = (C - lax[j]) * CT.ilax[cell * kAxStride + j];
       uint32_t cum = 0, s = 0;
 #pragma unroll
       for (int p = 0; p < 4; ++p) {
         s += (x >> (4 * p)) & 15u;
         cum |= s << (8 * p);
       }
+      const uint32_t off = oi + oo;  // staged position of the unit's first event
       const uint32_t sa = off | (((x >> 20) & 15u) << 12) | ((uint32_t)k << 16) | ((uint32_t)j << 19) | (cell << 22);
-      slots[uu] = make_uint4(sa, cum, __float_as_uint(v), __float_as_uint(a.half_vdd2 * C));
-      if (off < (uint32_t)kItemEvents) atomicOr(mask + (off >> 5), 1u << (off & 31u));
-      // words whose first position lies in (off, off + size] follow this unit
-      const uint32_t end = off + size;
-      for (uint32_t w = (off >> 5) + 1; w <= (end >> 5) && w < (uint32_t)kMaskWords; ++w) wpre[w] = uu + 1;
+      X.slots[uu] = make_uint4(sa, cum, __float_as_uint(v), __float_as_uint(a.half_vdd2 * C));
+      if (n_in) space_mark(X.in_mask, X.in_pre, X.in_map, ri, oi, n_in, (uint32_t)uu);
+      if (n_out) space_mark(X.out_mask, X.out_pre, X.out_map, ro, oo, n_out, (uint32_t)uu);
     }
   }
-  if (lane == 0) wpre[0] = 0;
+  if (lane == 0) {
+    X.in_pre[0] = 0;
+    X.out_pre[0] = 0;
+  }
   __syncwarp();
-  if (carry != (uint32_t)n) {  // records disagree with the item's event count
-    if (lane == 0) berr(a.err, item, kErrTileOverflow);
-    __syncwarp();
-    if (lane < kMaskWords) mask[lane] = 0u;
-    __syncwarp();
-    return;
-  }
-  const float T = a.t_clk, inv_T = a.inv_t_clk;
-  const uint32_t cb = A.L.band_cycles;
-  // ---- events
-  const uint32_t le_mask = 0xFFFFFFFFu >> (31 - lane);  // lanes <= this one (e % 32 == lane)
-  for (int e = lane; e < n; e += 32) {
-    const int w = e >> 5;
-    const int u = (int)wpre[w] + __popc(mask[w] & le_mask) - 1;
-    const uint4 S = slots[u];
-    const int ustart = (int)(S.x & 0xFFFu);
-    const int li = e - ustart;
-    // pin starts: byte q of (cum << 8) for q <= 3, byte 3 of cum for q = 4
-    const uint32_t cum = S.y, cumx = cum << 8;
-    const int p = (li >= (int)(cum & 0xFFu)) + (li >= (int)((cum >> 8) & 0xFFu)) +
-                  (li >= (int)((cum >> 16) & 0xFFu)) + (li >= (int)(cum >> 24));
-    const int idx = li - (int)__byte_perm(cumx, cum, p < 4 ? (uint32_t)p : 7u);
-    const float t = ts[e], s = ss[e];
-    const uint32_t c = cyc<kPow2>(t, T, inv_T);
-    float tp = 0.f, sp = 0.f;
-    bool glitch = false;
-    if (idx > 0) {
-      tp = ts[e - 1];
-      sp = ss[e - 1];
-      glitch = cyc<kPow2>(tp, T, inv_T) == c;
-    }
-    const int k = (int)((S.x >> 16) & 7u);
-    const int j = (int)((S.x >> 19) & 7u);
-    float e_int = 0.f, e_sw = 0.f, dp = 0.f;
-    uint32_t s_pre = (S.x >> 12) & 15u;
-    int lis = 0;
-    const float* ub = ts + ustart;
-    if (p == k) {
-      e_sw = __uint_as_float(S.w);
-      if (kDebug) {
-#pragma unroll
-        for (int qq = 0; qq < 4; ++qq) {
-          if (qq < k) {
-            const int qa = (int)__byte_perm(cumx, cum, (uint32_t)qq);
-            const int qn = (int)__byte_perm(cumx, cum, qq < 3 ? (uint32_t)qq + 1 : 7u) - qa;
-            const float* b = ub + qa;
-            int r = 0;
-#pragma unroll
-            for (int h = 8; h > 0; h >>= 1)
-              if (r + h <= qn && b[r + h - 1] < t) r += h;
-            s_pre ^= ((uint32_t)r & 1u) << qq;
-          }
-        }
-      }
-    } else {
-      const CellDesc& cd = cells[S.x >> 22];
-      s_pre ^= ((uint32_t)idx & 1u) << p;
+  const int n_in_all = (int)(carry & 511u), n_out_all = (int)((carry >> 9) & 511u);
+  const uint32_t le_mask = 0xFFFFFFFFu >> (31 - lane);  // lanes <= this one (index % 32 == lane)
+  if (n_in_all + n_out_all == n) {
+    // ---- input events: gate state, LUT, leakage step
+    for (int i = lane; i < n_in_all; i += 32) {
+      const uint32_t m = X.in_map[space_rank(X.in_mask, X.in_pre, i, le_mask)];
+      const int uu = (int)(m & 0xFFu);
+      const int li = i - (int)(m >> 8);  // inputs open the unit
+      const uint4 S = X.slots[uu];
+      const int ustart = (int)(S.x & 0xFFFu);
+      const int e = ustart + li;
+      const uint32_t cum = S.y;
+      const int p = (li >= (int)(cum & 0xFFu)) + (li >= (int)((cum >> 8) & 0xFFu)) +
+                    (li >= (int)((cum >> 16) & 0xFFu));
+      const int idx = li - pin_start(cum, p);
+      const int k = (int)((S.x >> 16) & 7u);
+      const int j = (int)((S.x >> 19) & 7u);
+      const float t = ts[e], s = ss[e];
+      const float* ub = ts + ustart;
+      uint32_t s_pre = ((S.x >> 12) & 15u) ^ (((uint32_t)idx & 1u) << p);
       uint32_t s_b = s_pre;
       // other input pins: events before t (parity) and, for lower pins, a tie at t
-#pragma unroll
-      for (int qq = 0; qq < 4; ++qq) {
-        if (qq < k && qq != p) {
-          const int qa = (int)__byte_perm(cumx, cum, (uint32_t)qq);
-          const int qn = (int)__byte_perm(cumx, cum, qq < 3 ? (uint32_t)qq + 1 : 7u) - qa;
-          const float* b = ub + qa;
-          int r = 0;
-#pragma unroll
-          for (int h = 8; h > 0; h >>= 1)
-            if (r + h <= qn && b[r + h - 1] < t) r += h;
-          const bool eq = qq < p && r < qn && b[r] == t;
-          const uint32_t par = (uint32_t)r & 1u;
-          s_pre ^= par << qq;
-          s_b ^= (par ^ (uint32_t)eq) << qq;
-        }
+      for (int jj = 0; jj < k - 1; ++jj) {
+        const int qq = jj + (jj >= p ? 1 : 0);
+        const int qa = pin_start(cum, qq);
+        const int qn = pin_start(cum, qq + 1) - qa;
+        const float* b = ub + qa;
+        const int r = seg_rank(b, qn, t);
+        const bool eq = qq < p && r < qn && b[r] == t;
+        const uint32_t par = (uint32_t)r & 1u;
+        s_pre ^= par << qq;
+        s_b ^= (par ^ (uint32_t)eq) << qq;
       }
-      const int ns = cd.ns, nl = cd.nl;
+      const uint32_t cell = S.x >> 22;
+      const uint32_t info = CT.info[cell];
+      const int ns = (int)(info & 0xFFu), nl = (int)((info >> 8) & 0xFFu);
+      const float* sax = CT.sax + cell * kAxStride;
+      int lis = 0;
 #pragma unroll
       for (int h = 4; h > 0; h >>= 1) {
         const int cand = lis + h;
-        if (cand <= ns - 2 && s >= cd.sax[cand]) lis = cand;
+        if (cand <= ns - 2 && s >= sax[cand]) lis = cand;
       }
-      const float uu = (s - cd.sax[lis]) * cd.isax[lis];
-      const float* L = a.lut + cd.lut_off + ((int)s_pre * ns + lis) * nl + j;
-      const float l00 = __ldg(L), l01 = __ldg(L + 1), l10 = __ldg(L + nl), l11 = __ldg(L + nl + 1);
+      const float uu2 = (s - sax[lis]) * CT.isax[cell * kAxStride + lis];
+      // corners {L[i][j], L[i][j+1], L[i+1][j], L[i+1][j+1]} of the state's table
+      const float4 P = __ldg(a.patch + CT.patch[cell] + ((int)s_pre * (ns - 1) + lis) * (nl - 1) + j);
       const float vv = __uint_as_float(S.z);
-      const float r0 = fmaf(vv, l01 - l00, l00), r1 = fmaf(vv, l11 - l10, l10);
-      e_int = fmaf(uu, r1 - r0, r0);
-      const float* lk = a.leak + cd.leak_off;
-      dp = __ldg(lk + (s_b ^ (1u << p))) - __ldg(lk + s_b);
+      const float r0 = fmaf(vv, P.y - P.x, P.x), r1 = fmaf(vv, P.w - P.z, P.z);
+      const float e_int = fmaf(uu2, r1 - r0, r0);
+      const float dp = __ldg(a.dleak + cell * kDleakStride + s_b * 4 + p);
+      const uint32_t gate = kDebug ? A.L.ugate[g.u0 + (uint32_t)uu] : 0u;
+      event_tail<kPow2, kDebug, kExact>(A, hist, ts, ss, e, idx, p, k, t, s, e_int, 0.f, dp, s_pre, lis, j, gate,
+                                        item, c0, acc);
     }
-    const float e_dyn = e_int + e_sw;
-    float e_w;
-    if (glitch) {
-      const float r = fminf(1.f, __fdividef(2000.f * (t - tp), s + sp));
-      e_w = r * e_dyn;
-      acc.e_gl += e_w;
-    } else {
-      acc.e_int += e_int;
-      acc.e_sw += e_sw;
-      e_w = e_dyn;
-    }
-    const uint32_t lc = c - c0;
-    if (lc >= cb) {  // an event outside its band: layout inconsistency
-      berr(a.err, item, kErrTileOverflow);
-      continue;
-    }
-    if (p < k) {
-      const float rem = fmaf(-(float)c, T, t);  // t - c T
-      e_w = fmaf(dp, T - rem, e_w);
-      acc.e_lk = fmaf(dp, a.t_max_f - t, acc.e_lk);
-    }
-    if (kExact) {
-      double* bin = reinterpret_cast<double*>(a.bins + c);
-      atomicAdd(bin, (double)e_w);
-      if (p < k) atomicAdd(bin + 1, (double)dp);
-      atomicAdd(a.cnt_ev + c, 1u);
-      if (glitch) atomicAdd(a.cnt_gl + c, 1u);
-    } else {
-      float* h = reinterpret_cast<float*>(hist + lc);
-      atomicAdd(h, e_w);
-      if (p < k) atomicAdd(h + 1, dp);
-      atomicAdd(reinterpret_cast<uint32_t*>(h + 2), 1u);
-      if (glitch) atomicAdd(reinterpret_cast<uint32_t*>(h + 3), 1u);
-    }
-    if (kDebug) {
-      // CSR index of this event: its rank among its pin's events
-      const uint32_t g = A.L.ugate[it.u0 + (uint32_t)u];
-      const GateRec gr = a.gates[g];
-      const uint64_t pin = (uint64_t)gr.pin_base + p;
-      const uint64_t hi = a.pin_off[pin + 1];
-      uint64_t l = a.pin_off[pin], cnt = hi - l;
-      while (cnt > 0) {
-        const uint64_t half = cnt >> 1;
-        if (a.t[l + half] < t) {
-          l += half + 1;
-          cnt -= half + 1;
-        } else {
-          cnt = half;
+    // ---- output events: switching energy
+    for (int o = lane; o < n_out_all; o += 32) {
+      const uint32_t m = X.out_map[space_rank(X.out_mask, X.out_pre, o, le_mask)];
+      const int uu = (int)(m & 0xFFu);
+      const int idx = o - (int)(m >> 8);
+      const uint4 S = X.slots[uu];
+      const int ustart = (int)(S.x & 0xFFFu);
+      const uint32_t cum = S.y;
+      const int k = (int)((S.x >> 16) & 7u);
+      const int e = ustart + pin_start(cum, k) + idx;
+      const float t = ts[e], s = ss[e];
+      uint32_t s_pre = (S.x >> 12) & 15u;
+      if (kDebug) {
+        const float* ub = ts + ustart;
+        for (int qq = 0; qq < k; ++qq) {
+          const int qa = pin_start(cum, qq);
+          s_pre ^= ((uint32_t)seg_rank(ub + qa, pin_start(cum, qq + 1) - qa, t) & 1u) << qq;
         }
       }
-      if (l < hi && a.t[l] == t) {
-        a.dbg_state[l] = (uint8_t)s_pre;
-        a.dbg_lut[l] = p < k ? (uint8_t)((lis << 4) | j) : (uint8_t)0xFF;
-        a.dbg_glitch[l] = (uint8_t)glitch;
-      } else {
-        berr(a.err, item, kErrTileOverflow);
-      }
+      const uint32_t gate = kDebug ? A.L.ugate[g.u0 + (uint32_t)uu] : 0u;
+      event_tail<kPow2, kDebug, kExact>(A, hist, ts, ss, e, idx, k, k, t, s, 0.f, __uint_as_float(S.w), 0.f, s_pre,
+                                        0, 0, gate, item, c0, acc);
     }
+  } else if (lane == 0) {  // records disagree with the item's event count
+    berr(a.err, item, kErrTileOverflow);
   }
   __syncwarp();
-  if (lane < kMaskWords) mask[lane] = 0u;  // ready for the warp's next item
+  if (lane < kMaskWords) {  // ready for the warp's next item
+    X.in_mask[lane] = 0u;
+    X.out_mask[lane] = 0u;
+  }
   __syncwarp();
 }
 
@@ -717,36 +883,72 @@ template <bool kPow2, bool kDebug, bool kExact>
 __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
   extern __shared__ __align__(128) uint8_t smem[];
   float4* hist = reinterpret_cast<float4*>(smem);
-  CellDesc* cells_s = reinterpret_cast<CellDesc*>(smem + kHist);
-  uint8_t* wbufs = smem + kHist + kCellsB;
+  uint32_t* cells_s = reinterpret_cast<uint32_t*>(smem + kHist);
+  __shared__ __align__(8) uint64_t s_bar[kBW];
   __shared__ uint32_t s_range[2];
   __shared__ uint32_t s_seg_end, s_band;
   __shared__ unsigned int s_next;
   __shared__ double s_tot[4];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const RunArgs& a = A.r;
-  const uint32_t cb = A.L.band_cycles;
-  const uint32_t n_items = A.L.n_items;
-  uint8_t* wbuf = wbufs + (size_t)warp * kWarpBytes;
+  const BandLayout& L = A.L;
+  const uint32_t cb = L.band_cycles;
+  const uint32_t n_items = L.n_items;
+  uint8_t* wbuf = smem + kHist + kCellsB + (size_t)warp * kWarpB;
+  WarpScratch X;
+  X.stage = wbuf;
+  X.slots = reinterpret_cast<uint4*>(wbuf + kStageB);
+  X.in_mask = reinterpret_cast<uint32_t*>(X.slots + kItemUnits);
+  X.in_pre = X.in_mask + kMaskWords;
+  X.out_mask = X.in_pre + kMaskWords;
+  X.out_pre = X.out_mask + kMaskWords;
+  X.in_map = X.out_pre + kMaskWords;
+  X.out_map = X.in_map + kItemUnits;
+  uint64_t* bar = &s_bar[warp];
 
   if (tid < 4) s_tot[tid] = 0.0;
   for (uint32_t i = tid; i < cb; i += kBT) hist[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  CellTab CT;
   {  // the layout is only built for libraries of at most kSmemCells cells
-    const int words = (int)(min(a.n_cells, (uint32_t)kSmemCells) * sizeof(CellDesc) / 4);
-    const uint32_t* src = reinterpret_cast<const uint32_t*>(a.cells);
-    uint32_t* dst = reinterpret_cast<uint32_t*>(cells_s);
-    for (int i = tid; i < words; i += kBT) dst[i] = src[i];
+    uint32_t* info = cells_s;
+    uint32_t* patch = info + kSmemCells;
+    float* ax = reinterpret_cast<float*>(patch + kSmemCells);  // sax, isax, lax, ilax
+    const uint32_t nc = min(a.n_cells, (uint32_t)kSmemCells);
+    for (uint32_t i = tid; i < nc * 8u; i += kBT) {
+      const uint32_t ci = i >> 3, m = i & 7u;
+      const CellDesc& cd = a.cells[ci];
+      if (m == 0) {
+        info[ci] = (uint32_t)cd.ns | ((uint32_t)cd.nl << 8) | ((uint32_t)cd.k << 16);
+        patch[ci] = cd.patch_off;
+      }
+      ax[0 * kSmemCells * kAxStride + ci * kAxStride + m] = cd.sax[m];
+      ax[1 * kSmemCells * kAxStride + ci * kAxStride + m] = cd.isax[m];
+      ax[2 * kSmemCells * kAxStride + ci * kAxStride + m] = cd.lax[m];
+      ax[3 * kSmemCells * kAxStride + ci * kAxStride + m] = cd.ilax[m];
+    }
+    CT.info = info;
+    CT.patch = patch;
+    CT.sax = ax;
+    CT.isax = ax + kSmemCells * kAxStride;
+    CT.lax = ax + 2 * kSmemCells * kAxStride;
+    CT.ilax = ax + 3 * kSmemCells * kAxStride;
   }
-  const CellDesc* cells = cells_s;
-  if (lane < kMaskWords) reinterpret_cast<uint32_t*>(wbuf + (size_t)kItemEvents * 8 + (size_t)kItemUnits * 16)[lane] = 0u;
+  if (lane < kMaskWords) {
+    X.in_mask[lane] = 0u;
+    X.out_mask[lane] = 0u;
+  }
+  if (lane == 0) {
+    mbar_init(bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
   if (tid < 2) {
     // items whose first event falls in this CTA's share of all banded events
-    const uint64_t total = A.L.n_ev;
+    const uint64_t total = L.n_ev;
     const uint64_t want = total * (uint64_t)(blockIdx.x + tid) / gridDim.x;
     uint32_t lo = 0, n = n_items;
     while (n > 0) {
       const uint32_t half = n >> 1;
-      if (A.L.items[lo + half].e0 < want) {
+      if (L.items[lo + half].e0 < want) {
         lo += half + 1;
         n -= half + 1;
       } else {
@@ -759,50 +961,70 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
   const uint32_t i0 = s_range[0], i1 = s_range[1];
   BAcc acc{0.f, 0.f, 0.f, 0.f};
   int since = 0;
+  uint32_t phase = 0;  // parity of the stage barrier's next completion
+  bool bad = false;    // a stage copy never landed: this warp stops working
   for (uint32_t cur = i0; cur < i1;) {
     if (tid == 0) {
-      const uint32_t b = A.L.items[cur].band;
+      const uint32_t b = L.items[cur].band;
       s_band = b;
-      s_seg_end = band_end(A.L, cur, i1, b);
+      s_seg_end = band_end(L, cur, i1, b);
       s_next = 0;
     }
     __syncthreads();
     const uint32_t band = s_band, seg_end = s_seg_end;
     const uint32_t c0 = band * cb;
-    // warps take the band's items in turn; the next item's records are
-    // fetched while the current one is worked on
-    uint32_t my = 0;
-    if (lane == 0) my = cur + atomicAdd(&s_next, 1u);
-    my = __shfl_sync(0xffffffffu, my, 0);
-    BandItem it{}, nx{};
-    if (my < seg_end && lane == 0) {
-      it = A.L.items[my];
-      nx = A.L.items[my + 1];
-    }
-    while (my < seg_end) {
-      uint32_t nxt = 0;
-      if (lane == 0) nxt = cur + atomicAdd(&s_next, 1u);
-      nxt = __shfl_sync(0xffffffffu, nxt, 0);
-      BandItem it2{}, nx2{};
-      if (nxt < seg_end && lane == 0) {
-        it2 = A.L.items[nxt];
-        nx2 = A.L.items[nxt + 1];
+    // lane 0 keeps the record of the warp's next item loaded ahead
+    uint32_t my = seg_end;
+    BandItem my_a{}, my_b{};
+    if (lane == 0 && !bad) {
+      my = cur + atomicAdd(&s_next, 1u);
+      if (my < seg_end) {
+        my_a = L.items[my];
+        my_b = L.items[my + 1];
       }
-      BandItem ia, ib;
-      ia.e0 = __shfl_sync(0xffffffffu, it.e0, 0);
-      ia.u0 = __shfl_sync(0xffffffffu, it.u0, 0);
-      ia.band = band;
-      ib.e0 = __shfl_sync(0xffffffffu, nx.e0, 0);
-      ib.u0 = __shfl_sync(0xffffffffu, nx.u0, 0);
-      ib.band = band;
-      band_item<kPow2, kDebug, kExact>(A, cells, hist, wbuf, my, ia, ib, c0, acc);
+    }
+    my = __shfl_sync(0xffffffffu, my, 0);
+    while (my < seg_end) {
+      uint32_t nx = seg_end;
+      BandItem nx_a{}, nx_b{};
+      ItemGeo gl{};
+      if (lane == 0) {
+        gl = item_geo(my_a.e0, my_a.u0, my_b.e0, my_b.u0);
+        stage_item(L, gl, wbuf, bar);
+        nx = cur + atomicAdd(&s_next, 1u);
+        if (nx < seg_end) {
+          nx_a = L.items[nx];
+          nx_b = L.items[nx + 1];
+        }
+      }
+      ItemGeo gcur;
+      gcur.e0 = __shfl_sync(0xffffffffu, gl.e0, 0);
+      gcur.ea = __shfl_sync(0xffffffffu, gl.ea, 0);
+      gcur.u0 = __shfl_sync(0xffffffffu, gl.u0, 0);
+      gcur.ra = __shfl_sync(0xffffffffu, gl.ra, 0);
+      gcur.n = __shfl_sync(0xffffffffu, gl.n, 0);
+      gcur.nu = __shfl_sync(0xffffffffu, gl.nu, 0);
+      gcur.ev_off = __shfl_sync(0xffffffffu, gl.ev_off, 0);
+      gcur.rec_off = __shfl_sync(0xffffffffu, gl.rec_off, 0);
+      gcur.ev_bytes = gcur.rec_bytes = 0;
+      gcur.ok = __shfl_sync(0xffffffffu, (int)gl.ok, 0) != 0;
+      bool ok = false;
+      for (uint32_t it = 0; it < kWaitLimit && !ok; ++it) ok = mbar_try_wait(bar, phase);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) {
+        if (lane == 0) berr(a.err, my, kErrTileOverflow);
+        bad = true;
+        break;
+      }
+      phase ^= 1u;
+      band_item<kPow2, kDebug, kExact>(A, CT, hist, X, my, gcur, c0, acc);
       if (++since == kTotEvery) {
         bflush_acc(acc, s_tot);
         since = 0;
       }
-      my = nxt;
-      it = it2;
-      nx = nx2;
+      my = __shfl_sync(0xffffffffu, nx, 0);
+      my_a = nx_a;
+      my_b = nx_b;
     }
     __syncthreads();
     bflush_band<kExact>(A, hist, band);
@@ -810,6 +1032,11 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
     __syncthreads();
   }
   bflush_acc(acc, s_tot);
+  if (bad && lane == 0) {
+    // let this warp's copy in flight land (bounded) before the CTA ends
+    bool done = false;
+    for (uint32_t it = 0; it < kWaitLimit && !done; ++it) done = mbar_try_wait(bar, phase);
+  }
   __syncthreads();
   if (tid < 4) atomicAdd(a.totals + tid, s_tot[tid]);
 }

@@ -23,10 +23,17 @@ struct __align__(16) CellDesc {
   uint8_t k, ns, nl, pad0;
   uint32_t lut_off;   // floats into the LUT array: [2^k][ns][nl]
   uint32_t leak_off;  // floats into the leakage array: [2^k], in uW (fJ/ns)
-  uint32_t pad1;
+  uint32_t patch_off; // float4s into the patch table: [2^k][ns - 1][nl - 1]
   float sax[8], lax[8];    // slew (ps) / load (fF) axes
   float isax[8], ilax[8];  // 1 / (ax[i+1] - ax[i])
 };
+
+// Derived tables built with the library (used by the banded kernel): for each
+// state and interpolation cell (i, j) of a LUT the four corners {L[i][j],
+// L[i][j+1], L[i+1][j], L[i+1][j+1]} as one float4, and for each cell, state s
+// and input pin p the leakage step leak[s ^ (1 << p)] - leak[s] (f32, uW) at
+// index cell * kDleakStride + s * 4 + p.
+constexpr int kDleakStride = 64;
 
 // Per-gate record (16 B): pin base, cell, load, initial values and k.
 struct __align__(16) GateRec {
@@ -76,6 +83,8 @@ struct RunArgs {
   uint32_t n_cells;
   const float* lut;
   const float* leak;       // uW
+  const float4* patch;     // LUT corner patches
+  const float* dleak;      // leakage steps per (cell, state, pin)
   const GateRec* gates;
   uint32_t n_gates;
   const uint64_t* pin_off;
@@ -135,7 +144,7 @@ constexpr uint32_t kBandDefaultCycles = 4096;
 constexpr uint32_t kBandMaxCycles = 4096;        // shared-memory histogram capacity (cycles)
 constexpr uint32_t kBandMaxBands = 1u << 20;
 constexpr int kItemEvents = 256;                 // events per item (cap): one warp's work item
-constexpr int kItemUnits = 128;                  // units per item (cap)
+constexpr int kItemUnits = 64;                   // units per item (cap)
 // A new item starts where a unit's event offset enters a new bucket of this
 // many events (or a new band, or every kItemUnits units), so an item holds
 // fewer than kItemBucket + kUnitMaxEvents <= kItemEvents events.

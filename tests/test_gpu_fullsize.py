@@ -1,5 +1,6 @@
 """Full-size parity on the large configurations (200M, 1B and 2B events), in
-the launch configuration the benchmark times.
+the launch configuration the benchmark times (the banded layout, and the
+unbanded kernel alongside).
 
 At these sizes the oracle cannot afford its full per-cycle leakage split over
 every gate, so it checks what it can compute one by one:
@@ -45,7 +46,7 @@ def sub_workload(w, pb, g0, g1):
     return s, e0, e1
 
 
-@pytest.mark.parametrize("cfg,banded", [(3, False), (3, True), (4, False), (5, False)])
+@pytest.mark.parametrize("cfg,banded", [(3, False), (3, True), (4, False), (4, True), (5, True)])
 def test_full_size_config(glp, cfg, banded):
     threads = os.cpu_count() or 8
     w = synth.generate(cfg)
