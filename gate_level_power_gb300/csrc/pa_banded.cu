@@ -152,70 +152,54 @@ __device__ __forceinline__ uint32_t bcyc(const BandBuildArgs& a, float t) {
 
 constexpr uint32_t kNoCycle = 0xFFFFFFFFu;
 
-// Per-gate walk state: pin cursors and the cycle of each pin's next event.
-struct GateWalk {
-  uint64_t pos[kMaxK + 1], end[kMaxK + 1];
-  uint32_t nc[kMaxK + 1];
-  int k;
-};
-
-__device__ __forceinline__ void walk_init(const BandBuildArgs& a, const GateRec& r, GateWalk& W) {
-  W.k = (int)((r.init >> 16) & 0xff);
-  for (int p = 0; p <= kMaxK; ++p) {
-    W.pos[p] = W.end[p] = 0;
-    W.nc[p] = kNoCycle;
-    if (p <= W.k) {
-      W.pos[p] = a.pin_off[(uint64_t)r.pin_base + p];
-      W.end[p] = a.pin_off[(uint64_t)r.pin_base + p + 1];
-      W.nc[p] = W.pos[p] < W.end[p] ? bcyc(a, a.t[W.pos[p]]) : kNoCycle;
-    }
-  }
-}
-
-// Next cycle with events (kNoCycle when done) and its event count per pin;
-// advances the cursors past it.
-__device__ __forceinline__ uint32_t walk_cycle(const BandBuildArgs& a, GateWalk& W, uint32_t n_c[kMaxK + 1]) {
-  uint32_t c = kNoCycle;
-  for (int p = 0; p <= W.k; ++p) c = min(c, W.nc[p]);
-  for (int p = 0; p <= kMaxK; ++p) n_c[p] = 0;
-  if (c == kNoCycle) return c;
-  for (int p = 0; p <= W.k; ++p) {
-    while (W.nc[p] == c) {
-      ++n_c[p];
-      ++W.pos[p];
-      W.nc[p] = W.pos[p] < W.end[p] ? bcyc(a, a.t[W.pos[p]]) : kNoCycle;
-    }
-  }
-  return c;
-}
-
 // kWrite false: units / events per (band, gate) and big gates; true: records,
-// unit offsets and the event copy.
+// unit offsets and the event copy. Every per-pin array is indexed only by
+// compile-time pin numbers (loops over the kMaxK + 1 pins fully unrolled), so
+// the walk state stays in registers.
 template <bool kWrite>
 __global__ void __launch_bounds__(128) k_bw_greedy(const BandBuildArgs a) {
+  constexpr int P = kMaxK + 1;
   const uint64_t g = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x;
   if (g >= a.n_gates) return;
   const uint64_t G = a.n_gates;
   if (kWrite && a.bigf[g]) return;
   const GateRec r = a.gates[g];
-  GateWalk W;
-  walk_init(a, r, W);
-  const int k = W.k;
-  uint32_t n_c[kMaxK + 1];
-  uint32_t cw[kMaxK + 1];        // events per pin in the open window
-  uint64_t wstart[kMaxK + 1];    // CSR position of each pin at the window start
-  for (int p = 0; p <= kMaxK; ++p) {
+  const int k = (int)((r.init >> 16) & 0xff);
+  uint64_t pos[P], end[P], wstart[P];
+  uint32_t nc[P], cw[P];
+#pragma unroll
+  for (int p = 0; p < P; ++p) {
+    pos[p] = end[p] = 0;
+    nc[p] = kNoCycle;
     cw[p] = 0;
-    wstart[p] = W.pos[p];
+    if (p <= k) {
+      pos[p] = a.pin_off[(uint64_t)r.pin_base + p];
+      end[p] = a.pin_off[(uint64_t)r.pin_base + p + 1];
+      nc[p] = pos[p] < end[p] ? bcyc(a, a.t[pos[p]]) : kNoCycle;
+    }
+    wstart[p] = pos[p];
   }
   uint32_t state = r.init & ((1u << k) - 1u);  // input state at the window start
   uint32_t band = kNoCycle, units = 0, events = 0, wsize = 0;
   uint64_t u = 0, dst = 0;                      // next unit / banded event of this (band, gate)
   bool big = false, split = false;
   for (;;) {
-    const uint32_t c = walk_cycle(a, W, n_c);
+    // the next cycle with events, and its events per pin
+    uint32_t c = kNoCycle;
+#pragma unroll
+    for (int p = 0; p < P; ++p) c = min(c, nc[p]);
+    uint32_t n_c[P];
     bool over = false;
-    for (int p = 0; p <= k; ++p) {
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+      n_c[p] = 0;
+      if (c != kNoCycle) {
+        while (nc[p] == c) {
+          ++n_c[p];
+          ++pos[p];
+          nc[p] = pos[p] < end[p] ? bcyc(a, a.t[pos[p]]) : kNoCycle;
+        }
+      }
       if (n_c[p] > (uint32_t)kUnitPinMax) big = true;
       over |= cw[p] + n_c[p] > (uint32_t)kUnitPinMax;
     }
@@ -225,7 +209,8 @@ __global__ void __launch_bounds__(128) k_bw_greedy(const BandBuildArgs a) {
       // close the open window as one unit
       if (kWrite) {
         uint32_t x = 0;
-        for (int p = 0; p <= k; ++p) x |= cw[p] << (4 * p);
+#pragma unroll
+        for (int p = 0; p < P; ++p) x |= cw[p] << (4 * p);
         x |= state << 20;
         x |= (r.cell & 0xffu) << 24;
         if (u < (uint64_t)a.L.n_units && dst + wsize <= a.L.n_ev) {
@@ -234,7 +219,8 @@ __global__ void __launch_bounds__(128) k_bw_greedy(const BandBuildArgs a) {
           a.uband[u] = band;
           a.uoff[u] = dst;
           uint64_t d = dst;
-          for (int p = 0; p <= k; ++p) {
+#pragma unroll
+          for (int p = 0; p < P; ++p) {
             for (uint32_t i = 0; i < cw[p]; ++i) {
               a.L.bt[d + i] = a.t[wstart[p] + i];
               a.L.bs[d + i] = a.s[wstart[p] + i];
@@ -247,7 +233,8 @@ __global__ void __launch_bounds__(128) k_bw_greedy(const BandBuildArgs a) {
         ++u;
         dst += wsize;
       }
-      for (int p = 0; p <= k; ++p) {
+#pragma unroll
+      for (int p = 0; p < P; ++p) {
         if (p < k) state ^= (cw[p] & 1u) << p;
         wstart[p] += cw[p];
         cw[p] = 0;
@@ -271,8 +258,11 @@ __global__ void __launch_bounds__(128) k_bw_greedy(const BandBuildArgs a) {
         dst = a.ebase[(uint64_t)b * G + g];
       }
     }
-    for (int p = 0; p <= k; ++p) cw[p] += n_c[p];
-    for (int p = 0; p <= k; ++p) wsize += n_c[p];
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+      cw[p] += n_c[p];
+      wsize += n_c[p];
+    }
   }
   if (!kWrite) {
     if (big) {
@@ -413,7 +403,7 @@ constexpr int kBT = kBW * 32;
 constexpr int kMaskWords = kItemEvents / 32;
 constexpr int kStEv = kItemEvents + 8;                         // staged floats (16-byte rounding)
 constexpr size_t kStRecB = (size_t)(kItemUnits + 2) * 8;
-constexpr size_t kStageB = 2 * (size_t)kStEv * 4 + kStRecB;
+constexpr size_t kStageB = (size_t)kStEv * 4 + kStRecB;  // times and unit records (slews stay in HBM)
 // stage, unit slots, input / output start masks and word prefixes, rank maps
 constexpr size_t kWarpB = kStageB + (size_t)kItemUnits * 16 + 4 * kMaskWords * 4 + 2 * (size_t)kItemUnits * 4;
 constexpr size_t kHist = (size_t)kBandMaxCycles * 16;
@@ -570,7 +560,7 @@ __device__ __forceinline__ ItemGeo item_geo(uint64_t e0, uint32_t u0, uint64_t e
   g.ra = u0 & ~1u;
   g.ev_off = (uint32_t)(e0 - g.ea);
   g.rec_off = u0 - g.ra;
-  g.ok = e1 > e0 && u1 > u0 && e1 - e0 <= (uint64_t)kItemEvents && u1 - u0 <= (uint32_t)kItemUnits;
+  g.ok = e1 > e0 && u1 > u0 && e1 - e0 < (uint64_t)kItemEvents && u1 - u0 <= (uint32_t)kItemUnits;
   g.n = g.ok ? (uint32_t)(e1 - e0) : 0u;
   g.nu = g.ok ? u1 - u0 : 0u;
   g.ev_bytes = ((g.ev_off + g.n + 3u) & ~3u) * 4u;
@@ -586,10 +576,9 @@ __device__ __forceinline__ void stage_item(const BandLayout& L, const ItemGeo& g
     return;
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  mbar_expect_arrive(bar, 2 * g.ev_bytes + g.rec_bytes);
+  mbar_expect_arrive(bar, g.ev_bytes + g.rec_bytes);
   bulk_g2s(stage, L.bt + g.ea, g.ev_bytes, bar);
-  bulk_g2s(stage + (size_t)kStEv * 4, L.bs + g.ea, g.ev_bytes, bar);
-  bulk_g2s(stage + 2 * (size_t)kStEv * 4, L.urec + g.ra, g.rec_bytes, bar);
+  bulk_g2s(stage + (size_t)kStEv * 4, L.urec + g.ra, g.rec_bytes, bar);
 }
 
 // Events of a sorted pin segment b[0, qn) (qn <= 15) earlier than t: the
@@ -633,7 +622,7 @@ struct WarpScratch {
 // Everything after the gate state and energies are known: glitch scaling,
 // totals, in-cycle leakage part and the bins (and the debug outputs).
 template <bool kPow2, bool kDebug, bool kExact>
-__device__ __forceinline__ void event_tail(const BandRunArgs& A, float4* hist, const float* ts, const float* ss,
+__device__ __forceinline__ void event_tail(const BandRunArgs& A, float4* hist, const float* ts, const float* gs,
                                            int e, int idx, int p, int k, float t, float s, float e_int,
                                            float e_sw, float dp, uint32_t s_pre, int lis, int j, uint32_t gate,
                                            uint32_t item, uint32_t c0, BAcc& acc) {
@@ -644,8 +633,8 @@ __device__ __forceinline__ void event_tail(const BandRunArgs& A, float4* hist, c
   bool glitch = false;
   if (idx > 0) {  // the pin's previous event is the staged event before this one
     tp = ts[e - 1];
-    sp = ss[e - 1];
     glitch = cyc<kPow2>(tp, T, inv_T) == c;
+    if (glitch) sp = __ldg(gs + e - 1);
   }
   const float e_dyn = e_int + e_sw;
   float e_w;
@@ -736,8 +725,8 @@ __device__ __forceinline__ void band_item(const BandRunArgs& A, const CellTab& C
     return;
   }
   const float* ts = reinterpret_cast<const float*>(X.stage) + g.ev_off;
-  const float* ss = reinterpret_cast<const float*>(X.stage + (size_t)kStEv * 4) + g.ev_off;
-  const uint2* rec = reinterpret_cast<const uint2*>(X.stage + 2 * (size_t)kStEv * 4) + g.rec_off;
+  const float* gs = A.L.bs + g.e0;  // slews: read once, from HBM
+  const uint2* rec = reinterpret_cast<const uint2*>(X.stage + (size_t)kStEv * 4) + g.rec_off;
   const int n = (int)g.n, nu = (int)g.nu;
   // ---- units. One packed scan gives, per unit, its offsets in the input and
   // output index spaces and its ranks among units with inputs / outputs.
@@ -794,79 +783,85 @@ __device__ __forceinline__ void band_item(const BandRunArgs& A, const CellTab& C
   const int n_in_all = (int)(carry & 511u), n_out_all = (int)((carry >> 9) & 511u);
   const uint32_t le_mask = 0xFFFFFFFFu >> (31 - lane);  // lanes <= this one (index % 32 == lane)
   if (n_in_all + n_out_all == n) {
-    // ---- input events: gate state, LUT, leakage step
-    for (int i = lane; i < n_in_all; i += 32) {
-      const uint32_t m = X.in_map[space_rank(X.in_mask, X.in_pre, i, le_mask)];
-      const int uu = (int)(m & 0xFFu);
-      const int li = i - (int)(m >> 8);  // inputs open the unit
-      const uint4 S = X.slots[uu];
-      const int ustart = (int)(S.x & 0xFFFu);
-      const int e = ustart + li;
-      const uint32_t cum = S.y;
-      const int p = (li >= (int)(cum & 0xFFu)) + (li >= (int)((cum >> 8) & 0xFFu)) +
-                    (li >= (int)((cum >> 16) & 0xFFu));
-      const int idx = li - pin_start(cum, p);
-      const int k = (int)((S.x >> 16) & 7u);
-      const int j = (int)((S.x >> 19) & 7u);
-      const float t = ts[e], s = ss[e];
-      const float* ub = ts + ustart;
-      uint32_t s_pre = ((S.x >> 12) & 15u) ^ (((uint32_t)idx & 1u) << p);
-      uint32_t s_b = s_pre;
-      // other input pins: events before t (parity) and, for lower pins, a tie at t
-      for (int jj = 0; jj < k - 1; ++jj) {
-        const int qq = jj + (jj >= p ? 1 : 0);
-        const int qa = pin_start(cum, qq);
-        const int qn = pin_start(cum, qq + 1) - qa;
-        const float* b = ub + qa;
-        const int r = seg_rank(b, qn, t);
-        const bool eq = qq < p && r < qn && b[r] == t;
-        const uint32_t par = (uint32_t)r & 1u;
-        s_pre ^= par << qq;
-        s_b ^= (par ^ (uint32_t)eq) << qq;
-      }
-      const uint32_t cell = S.x >> 22;
-      const uint32_t info = CT.info[cell];
-      const int ns = (int)(info & 0xFFu), nl = (int)((info >> 8) & 0xFFu);
-      const float* sax = CT.sax + cell * kAxStride;
-      int lis = 0;
-#pragma unroll
-      for (int h = 4; h > 0; h >>= 1) {
-        const int cand = lis + h;
-        if (cand <= ns - 2 && s >= sax[cand]) lis = cand;
-      }
-      const float uu2 = (s - sax[lis]) * CT.isax[cell * kAxStride + lis];
-      // corners {L[i][j], L[i][j+1], L[i+1][j], L[i+1][j+1]} of the state's table
-      const float4 P = __ldg(a.patch + CT.patch[cell] + ((int)s_pre * (ns - 1) + lis) * (nl - 1) + j);
-      const float vv = __uint_as_float(S.z);
-      const float r0 = fmaf(vv, P.y - P.x, P.x), r1 = fmaf(vv, P.w - P.z, P.z);
-      const float e_int = fmaf(uu2, r1 - r0, r0);
-      const float dp = __ldg(a.dleak + cell * kDleakStride + s_b * 4 + p);
-      const uint32_t gate = kDebug ? A.L.ugate[g.u0 + (uint32_t)uu] : 0u;
-      event_tail<kPow2, kDebug, kExact>(A, hist, ts, ss, e, idx, p, k, t, s, e_int, 0.f, dp, s_pre, lis, j, gate,
-                                        item, c0, acc);
-    }
-    // ---- output events: switching energy
-    for (int o = lane; o < n_out_all; o += 32) {
-      const uint32_t m = X.out_map[space_rank(X.out_mask, X.out_pre, o, le_mask)];
-      const int uu = (int)(m & 0xFFu);
-      const int idx = o - (int)(m >> 8);
-      const uint4 S = X.slots[uu];
-      const int ustart = (int)(S.x & 0xFFFu);
-      const uint32_t cum = S.y;
-      const int k = (int)((S.x >> 16) & 7u);
-      const int e = ustart + pin_start(cum, k) + idx;
-      const float t = ts[e], s = ss[e];
-      uint32_t s_pre = (S.x >> 12) & 15u;
-      if (kDebug) {
+    // ---- one pass over the input index space, then the output index space:
+    // only the round that crosses from one to the other mixes the two paths
+    for (int i = lane; i < n; i += 32) {
+      if (i < n_in_all) {
+        // input event: gate state, LUT, leakage step
+        const uint32_t m = X.in_map[space_rank(X.in_mask, X.in_pre, i, le_mask)];
+        const int uu = (int)(m & 0xFFu);
+        const int li = i - (int)(m >> 8);  // inputs open the unit
+        const uint4 S = X.slots[uu];
+        const int ustart = (int)(S.x & 0xFFFu);
+        const int e = ustart + li;
+        const uint32_t cum = S.y;
+        const int p = (li >= (int)(cum & 0xFFu)) + (li >= (int)((cum >> 8) & 0xFFu)) +
+                      (li >= (int)((cum >> 16) & 0xFFu));
+        const int idx = li - pin_start(cum, p);
+        const int k = (int)((S.x >> 16) & 7u);
+        const int j = (int)((S.x >> 19) & 7u);
+        const float t = ts[e], s = __ldg(gs + e);
         const float* ub = ts + ustart;
-        for (int qq = 0; qq < k; ++qq) {
+        uint32_t s_pre = ((S.x >> 12) & 15u) ^ (((uint32_t)idx & 1u) << p);
+        uint32_t s_b = s_pre;
+        // other input pins: events before t (parity) and, for lower pins, a tie at t
+        for (int jj = 0; jj < k - 1; ++jj) {
+          const int qq = jj + (jj >= p ? 1 : 0);
           const int qa = pin_start(cum, qq);
-          s_pre ^= ((uint32_t)seg_rank(ub + qa, pin_start(cum, qq + 1) - qa, t) & 1u) << qq;
+          const int qn = pin_start(cum, qq + 1) - qa;
+          const float* b = ub + qa;
+          const int r = seg_rank(b, qn, t);
+          const bool eq = qq < p && r < qn && b[r] == t;
+          const uint32_t par = (uint32_t)r & 1u;
+          s_pre ^= par << qq;
+          s_b ^= (par ^ (uint32_t)eq) << qq;
         }
+        const uint32_t cell = S.x >> 22;
+        const uint32_t info = CT.info[cell];
+        const int ns = (int)(info & 0xFFu), nl = (int)((info >> 8) & 0xFFu);
+        const float* sax = CT.sax + cell * kAxStride;
+        int lis = 0;
+#pragma unroll
+        for (int h = 4; h > 0; h >>= 1) {
+          const int cand = lis + h;
+          if (cand <= ns - 2 && s >= sax[cand]) lis = cand;
+        }
+        const float uu2 = (s - sax[lis]) * CT.isax[cell * kAxStride + lis];
+        // corners {L[i][j], L[i][j+1], L[i+1][j], L[i+1][j+1]} of the state's table
+        const float4 P = __ldg(a.patch + CT.patch[cell] + ((int)s_pre * (ns - 1) + lis) * (nl - 1) + j);
+        const float vv = __uint_as_float(S.z);
+        const float r0 = fmaf(vv, P.y - P.x, P.x), r1 = fmaf(vv, P.w - P.z, P.z);
+        const float e_int = fmaf(uu2, r1 - r0, r0);
+        const float dp = __ldg(a.dleak + cell * kDleakStride + s_b * 4 + p);
+        const uint32_t gate = kDebug ? A.L.ugate[g.u0 + (uint32_t)uu] : 0u;
+        event_tail<kPow2, kDebug, kExact>(A, hist, ts, gs, e, idx, p, k, t, s, e_int, 0.f, dp, s_pre, lis, j, gate,
+                                          item, c0, acc);
+      } else {
+        // output event: switching energy
+        const int o = i - n_in_all;
+        const uint32_t ole = 0xFFFFFFFFu >> (31 - (o & 31));
+        const uint32_t m = X.out_map[space_rank(X.out_mask, X.out_pre, o, ole)];
+        const int uu = (int)(m & 0xFFu);
+        const int idx = o - (int)(m >> 8);
+        const uint4 S = X.slots[uu];
+        const int ustart = (int)(S.x & 0xFFFu);
+        const uint32_t cum = S.y;
+        const int k = (int)((S.x >> 16) & 7u);
+        const int e = ustart + pin_start(cum, k) + idx;
+        const float t = ts[e];
+        uint32_t s_pre = (S.x >> 12) & 15u;
+        if (kDebug) {
+          const float* ub = ts + ustart;
+          for (int qq = 0; qq < k; ++qq) {
+            const int qa = pin_start(cum, qq);
+            s_pre ^= ((uint32_t)seg_rank(ub + qa, pin_start(cum, qq + 1) - qa, t) & 1u) << qq;
+          }
+        }
+        const uint32_t gate = kDebug ? A.L.ugate[g.u0 + (uint32_t)uu] : 0u;
+        const float s = idx > 0 ? __ldg(gs + e) : 0.f;  // only a glitch ratio uses it
+        event_tail<kPow2, kDebug, kExact>(A, hist, ts, gs, e, idx, k, k, t, s, 0.f, __uint_as_float(S.w), 0.f,
+                                          s_pre, 0, 0, gate, item, c0, acc);
       }
-      const uint32_t gate = kDebug ? A.L.ugate[g.u0 + (uint32_t)uu] : 0u;
-      event_tail<kPow2, kDebug, kExact>(A, hist, ts, ss, e, idx, k, k, t, s, 0.f, __uint_as_float(S.w), 0.f, s_pre,
-                                        0, 0, gate, item, c0, acc);
     }
   } else if (lane == 0) {  // records disagree with the item's event count
     berr(a.err, item, kErrTileOverflow);

@@ -143,12 +143,12 @@ constexpr int kUnitMaxEvents = 5 * kUnitPinMax;  // events per unit
 constexpr uint32_t kBandDefaultCycles = 4096;
 constexpr uint32_t kBandMaxCycles = 4096;        // shared-memory histogram capacity (cycles)
 constexpr uint32_t kBandMaxBands = 1u << 20;
-constexpr int kItemEvents = 256;                 // events per item (cap): one warp's work item
+constexpr int kItemEvents = 512;                 // events per item (cap): one warp's work item
 constexpr int kItemUnits = 64;                   // units per item (cap)
 // A new item starts where a unit's event offset enters a new bucket of this
 // many events (or a new band, or every kItemUnits units), so an item holds
-// fewer than kItemBucket + kUnitMaxEvents <= kItemEvents events.
-constexpr uint32_t kItemBucket = kItemEvents - kUnitMaxEvents;
+// fewer than kItemBucket + kUnitMaxEvents < kItemEvents events.
+constexpr uint32_t kItemBucket = kItemEvents - kUnitMaxEvents - 1;
 
 // Unit record: x = counts of pins 0..4 (4 bits each, bits 0..19) | input state
 // at the window start (bits 20..23) | cell (bits 24..31); y = load (f32 bits).
