@@ -62,7 +62,7 @@ struct pa_ctx {
   BandLayout band;
   uint32_t band_windowed = 0;  // gates cut into windows narrower than a band
   DevBuf b_bt, b_bs, b_urec, b_ugate, b_items, b_big;
-  DevBuf b_bigf, b_cnt, b_evc, b_ubase, b_ebase, b_uband, b_uoff, b_flags, b_ipos, b_scan, b_counters;
+  DevBuf b_bigf, b_grank, b_cnt, b_evc, b_ubase, b_ebase, b_uband, b_uoff, b_flags, b_ipos, b_scan, b_counters;
   DevBuf b_part;
   DevBuf scratch_small;
 };
@@ -276,6 +276,7 @@ int run_pass(pa_ctx* c, const RunPlan& plan, const PassBufs& B, pa_result* out, 
   if (band) {
     A.r = a;
     A.L = *band;
+    A.item_ctr = B.part_counts + 3;  // part_counts[2] is the unbanded kernel's item counter
   }
   cudaStream_t st = c->stream;
   uint32_t launches = 0;
@@ -422,7 +423,7 @@ void pa_destroy(pa_ctx* c) {
                    &c->part_counts, &c->tiles, &c->heavy, &c->p0_tot, &c->p_out, &c->dbg[0],
                    &c->dbg[1], &c->dbg[2], &c->wave_tmp, &c->cnt_tmp, &c->scratch_small,
                    &c->chunk_sums, &c->b_bt, &c->b_bs, &c->b_urec, &c->b_ugate, &c->b_items,
-                   &c->b_big, &c->b_bigf, &c->b_cnt, &c->b_evc, &c->b_ubase, &c->b_ebase,
+                   &c->b_big, &c->b_bigf, &c->b_grank, &c->b_cnt, &c->b_evc, &c->b_ubase, &c->b_ebase,
                    &c->b_uband, &c->b_uoff, &c->b_flags, &c->b_ipos, &c->b_scan, &c->b_counters,
                    &c->b_part};
   for (DevBuf* b : all) dfree(*b);
@@ -772,7 +773,7 @@ int check_build_err(pa_ctx* c) {
 }
 
 void free_build_temps(pa_ctx* c) {
-  DevBuf* tmp[] = {&c->b_bigf, &c->b_cnt, &c->b_evc, &c->b_ubase, &c->b_ebase, &c->b_uband,
+  DevBuf* tmp[] = {&c->b_bigf, &c->b_grank, &c->b_cnt, &c->b_evc, &c->b_ubase, &c->b_ebase, &c->b_uband,
                    &c->b_uoff, &c->b_flags, &c->b_ipos, &c->b_scan, &c->b_counters};
   for (DevBuf* b : tmp) dfree(*b);
 }
@@ -811,6 +812,9 @@ int build_bands(pa_ctx* c, float t_clk, uint32_t cb) {
   PA_TRY(dreserve(c, c->b_big, ((size_t)G + 1) * sizeof(uint32_t)));
   PA_TRY(dreserve(c, c->b_counters, 4 * sizeof(uint32_t)));
   PA_TRY(dreserve(c, c->b_bigf, (size_t)G + 1));
+  PA_TRY(dreserve(c, c->b_grank, ((size_t)G + 1) * sizeof(uint32_t)));
+  PA_TRY(dreserve(c, c->b_flags, ((size_t)G + 1) * sizeof(uint32_t)));
+  PA_TRY(dreserve(c, c->b_ipos, ((size_t)G + 2) * sizeof(uint64_t)));
   PA_TRY(dreserve(c, c->b_cnt, (nbg + 1) * sizeof(uint32_t)));
   PA_TRY(dreserve(c, c->b_evc, (nbg + 1) * sizeof(uint32_t)));
   PA_TRY(dreserve(c, c->b_ubase, (nbg + 1) * sizeof(uint64_t)));
@@ -819,6 +823,9 @@ int build_bands(pa_ctx* c, float t_clk, uint32_t cb) {
   L.big = (uint32_t*)c->b_big.p;
   a.counters = (uint32_t*)c->b_counters.p;
   a.bigf = (uint8_t*)c->b_bigf.p;
+  a.grank = (uint32_t*)c->b_grank.p;
+  a.flags = (uint32_t*)c->b_flags.p;
+  a.ipos = (uint64_t*)c->b_ipos.p;
   a.cnt_gb = (uint32_t*)c->b_cnt.p;
   a.evc_gb = (uint32_t*)c->b_evc.p;
   a.ubase = (uint64_t*)c->b_ubase.p;
@@ -844,8 +851,8 @@ int build_bands(pa_ctx* c, float t_clk, uint32_t cb) {
   PA_TRY(dreserve(c, c->b_ugate, (nu + 1) * sizeof(uint32_t)));
   PA_TRY(dreserve(c, c->b_uband, (nu + 1) * sizeof(uint32_t)));
   PA_TRY(dreserve(c, c->b_uoff, (nu + 1) * sizeof(uint64_t)));
-  PA_TRY(dreserve(c, c->b_flags, (nu + 1) * sizeof(uint32_t)));
-  PA_TRY(dreserve(c, c->b_ipos, (nu + 1) * sizeof(uint64_t)));
+  PA_TRY(dreserve(c, c->b_flags, (std::max<size_t>(nu, G) + 1) * sizeof(uint32_t)));
+  PA_TRY(dreserve(c, c->b_ipos, (std::max<size_t>(nu + 1, (size_t)G + 2) + 1) * sizeof(uint64_t)));
   PA_TRY(dreserve(c, c->b_bt, ev_bytes));
   PA_TRY(dreserve(c, c->b_bs, ev_bytes));
   PA_TRY(dreserve(c, c->b_scan, ((size_t)band_scan_blocks(std::max<uint64_t>(nbg, nu)) + 1) * sizeof(uint64_t)));

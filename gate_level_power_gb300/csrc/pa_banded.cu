@@ -163,6 +163,7 @@ __global__ void __launch_bounds__(128) k_bw_greedy(const BandBuildArgs a) {
   if (g >= a.n_gates) return;
   const uint64_t G = a.n_gates;
   if (kWrite && a.bigf[g]) return;
+  const uint64_t gr = a.grank[g];  // the gate's place in the layout's gate order
   const GateRec r = a.gates[g];
   const int k = (int)((r.init >> 16) & 0xff);
   uint64_t pos[P], end[P], wstart[P];
@@ -247,15 +248,15 @@ __global__ void __launch_bounds__(128) k_bw_greedy(const BandBuildArgs a) {
     if (c == kNoCycle) break;
     if (b != band) {
       if (!kWrite && band != kNoCycle) {
-        a.cnt_gb[(uint64_t)band * G + g] = units;
-        a.evc_gb[(uint64_t)band * G + g] = events;
+        a.cnt_gb[(uint64_t)band * G + gr] = units;
+        a.evc_gb[(uint64_t)band * G + gr] = events;
       }
       band = b;
       units = 0;
       events = 0;
       if (kWrite) {
-        u = a.ubase[(uint64_t)b * G + g];
-        dst = a.ebase[(uint64_t)b * G + g];
+        u = a.ubase[(uint64_t)b * G + gr];
+        dst = a.ebase[(uint64_t)b * G + gr];
       }
     }
 #pragma unroll
@@ -268,20 +269,50 @@ __global__ void __launch_bounds__(128) k_bw_greedy(const BandBuildArgs a) {
     if (big) {
       // no unit of a big gate: clear what the walk wrote before it saw the cycle
       for (uint32_t bb = 0; bb < a.n_bands; ++bb) {
-        a.cnt_gb[(uint64_t)bb * G + g] = 0;
-        a.evc_gb[(uint64_t)bb * G + g] = 0;
+        a.cnt_gb[(uint64_t)bb * G + gr] = 0;
+        a.evc_gb[(uint64_t)bb * G + gr] = 0;
       }
       a.L.big[atomicAdd(a.counters, 1u)] = (uint32_t)g;
       a.bigf[g] = 1;
     } else {
       a.bigf[g] = 0;
       if (band != kNoCycle) {
-        a.cnt_gb[(uint64_t)band * G + g] = units;
-        a.evc_gb[(uint64_t)band * G + g] = events;
+        a.cnt_gb[(uint64_t)band * G + gr] = units;
+        a.evc_gb[(uint64_t)band * G + gr] = events;
       }
       if (split) atomicAdd(a.counters + 1, 1u);
     }
   }
+}
+
+// Layout gate order: gates grouped by class (k, and whether the gate has more
+// than kDenseGate events), gate order kept inside a class. Units of a band
+// follow this order, so the lanes of a warp mostly see cells with the same
+// number of inputs and pin segments of similar length.
+constexpr uint64_t kDenseGate = 256;
+constexpr int kGateClasses = 2 * (kMaxK + 1);
+
+__device__ __forceinline__ uint32_t gate_class(const BandBuildArgs& a, uint32_t g) {
+  const GateRec r = a.gates[g];
+  const uint32_t k = (r.init >> 16) & 0xffu;
+  const uint64_t n = a.pin_off[(uint64_t)r.pin_base + k + 1] - a.pin_off[r.pin_base];
+  return 2u * k + (n > kDenseGate ? 1u : 0u);
+}
+
+__global__ void __launch_bounds__(256) k_bw_class_flags(const BandBuildArgs a, uint32_t cls) {
+  const uint32_t g = blockIdx.x * 256u + threadIdx.x;
+  if (g < a.n_gates) a.flags[g] = gate_class(a, g) == cls ? 1u : 0u;
+}
+
+// grank[g] = base + (exclusive scan of the class flags) for the gates of class cls.
+__global__ void __launch_bounds__(256) k_bw_class_rank(const BandBuildArgs a, uint32_t cls, const uint64_t* pos,
+                                                       const uint64_t* base) {
+  const uint32_t g = blockIdx.x * 256u + threadIdx.x;
+  if (g < a.n_gates && a.flags[g]) a.grank[g] = (uint32_t)(*base + pos[g]);
+}
+
+__global__ void k_bw_class_base(uint64_t* base, const uint64_t* pos, uint32_t n_gates) {
+  if (threadIdx.x == 0 && blockIdx.x == 0) *base += pos[n_gates];
 }
 
 // Item heads over the units.
@@ -321,7 +352,18 @@ __global__ void __launch_bounds__(256) k_bw_item_emit(const BandBuildArgs a, uin
 
 cudaError_t band_build_count(BandBuildArgs& a, cudaStream_t st) {
   const uint64_t n = (uint64_t)a.n_bands * a.n_gates;
-  cudaError_t e = cudaMemsetAsync(a.counters, 0, 4 * sizeof(uint32_t), st);
+  // gate order: one stable pass per class (flags, scan, ranks after the earlier classes)
+  cudaError_t e = cudaMemsetAsync(a.ipos + a.n_gates + 1, 0, sizeof(uint64_t), st);  // running class base
+  if (e != cudaSuccess) return e;
+  const uint32_t gb = (a.n_gates + 255) / 256;
+  for (uint32_t cls = 0; cls < (uint32_t)kGateClasses && a.n_gates; ++cls) {
+    k_bw_class_flags<<<gb, 256, 0, st>>>(a, cls);
+    e = scan_u32_to_u64(a.flags, a.n_gates, a.scan_blk, a.ipos, st);
+    if (e != cudaSuccess) return e;
+    k_bw_class_rank<<<gb, 256, 0, st>>>(a, cls, a.ipos, a.ipos + a.n_gates + 1);
+    k_bw_class_base<<<1, 32, 0, st>>>(a.ipos + a.n_gates + 1, a.ipos, a.n_gates);
+  }
+  e = cudaMemsetAsync(a.counters, 0, 4 * sizeof(uint32_t), st);
   if (e == cudaSuccess) e = cudaMemsetAsync(a.cnt_gb, 0, (n + 1) * sizeof(uint32_t), st);
   if (e == cudaSuccess) e = cudaMemsetAsync(a.evc_gb, 0, (n + 1) * sizeof(uint32_t), st);
   if (e != cudaSuccess) return e;
@@ -416,6 +458,7 @@ constexpr size_t kSmemB = kHist + kCellsB + kBW * kWarpB;
 static_assert(kStageB % 16 == 0 && kWarpB % 16 == 0 && kHist % 16 == 0 && kCellsB % 16 == 0, "alignment");
 static_assert(kSmemB + 1024 <= 227 * 1024, "shared memory budget");
 constexpr int kTotEvery = 16;              // items between flushes of a warp's per-lane totals
+constexpr int kChunkItems = 256;           // items a CTA takes from the global counter at a time
 constexpr uint32_t kWaitLimit = 1u << 24;  // mbarrier polls before giving up
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -880,8 +923,7 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
   float4* hist = reinterpret_cast<float4*>(smem);
   uint32_t* cells_s = reinterpret_cast<uint32_t*>(smem + kHist);
   __shared__ __align__(8) uint64_t s_bar[kBW];
-  __shared__ uint32_t s_range[2];
-  __shared__ uint32_t s_seg_end, s_band;
+  __shared__ uint32_t s_chunk, s_seg_end, s_band;
   __shared__ unsigned int s_next;
   __shared__ double s_tot[4];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -936,96 +978,105 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
     mbar_init(bar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (tid < 2) {
-    // items whose first event falls in this CTA's share of all banded events
-    const uint64_t total = L.n_ev;
-    const uint64_t want = total * (uint64_t)(blockIdx.x + tid) / gridDim.x;
-    uint32_t lo = 0, n = n_items;
-    while (n > 0) {
-      const uint32_t half = n >> 1;
-      if (L.items[lo + half].e0 < want) {
-        lo += half + 1;
-        n -= half + 1;
-      } else {
-        n = half;
-      }
-    }
-    s_range[tid] = (blockIdx.x + tid == gridDim.x) ? n_items : lo;
-  }
   __syncthreads();
-  const uint32_t i0 = s_range[0], i1 = s_range[1];
   BAcc acc{0.f, 0.f, 0.f, 0.f};
   int since = 0;
   uint32_t phase = 0;  // parity of the stage barrier's next completion
   bool bad = false;    // a stage copy never landed: this warp stops working
-  for (uint32_t cur = i0; cur < i1;) {
-    if (tid == 0) {
-      const uint32_t b = L.items[cur].band;
-      s_band = b;
-      s_seg_end = band_end(L, cur, i1, b);
-      s_next = 0;
-    }
-    __syncthreads();
-    const uint32_t band = s_band, seg_end = s_seg_end;
-    const uint32_t c0 = band * cb;
-    // lane 0 keeps the record of the warp's next item loaded ahead
-    uint32_t my = seg_end;
-    BandItem my_a{}, my_b{};
-    if (lane == 0 && !bad) {
-      my = cur + atomicAdd(&s_next, 1u);
-      if (my < seg_end) {
-        my_a = L.items[my];
-        my_b = L.items[my + 1];
+  // CTAs take chunks of kChunkItems items from a global counter (the next
+  // chunk's start fetched one chunk ahead by thread 0); the band bins stay in
+  // shared memory until a chunk brings a new band.
+  uint32_t pref = 0;
+  if (tid == 0) {
+    s_chunk = atomicAdd(A.item_ctr, (uint32_t)kChunkItems);
+    pref = atomicAdd(A.item_ctr, (uint32_t)kChunkItems);
+    s_band = 0xFFFFFFFFu;
+  }
+  __syncthreads();
+  for (;;) {
+    const uint32_t c_lo = s_chunk;
+    if (c_lo >= n_items) break;
+    const uint32_t c_hi = min(c_lo + (uint32_t)kChunkItems, n_items);
+    for (uint32_t cur = c_lo; cur < c_hi;) {
+      const uint32_t old_band = s_band;
+      __syncthreads();  // everyone has read s_band / s_chunk
+      if (tid == 0) {
+        const uint32_t b = L.items[cur].band;
+        s_band = b;
+        s_seg_end = band_end(L, cur, c_hi, b);
+        s_next = 0;
       }
-    }
-    my = __shfl_sync(0xffffffffu, my, 0);
-    while (my < seg_end) {
-      uint32_t nx = seg_end;
-      BandItem nx_a{}, nx_b{};
-      ItemGeo gl{};
-      if (lane == 0) {
-        gl = item_geo(my_a.e0, my_a.u0, my_b.e0, my_b.u0);
-        stage_item(L, gl, wbuf, bar);
-        nx = cur + atomicAdd(&s_next, 1u);
-        if (nx < seg_end) {
-          nx_a = L.items[nx];
-          nx_b = L.items[nx + 1];
+      __syncthreads();
+      const uint32_t band = s_band, seg_end = s_seg_end;
+      if (band != old_band && old_band != 0xFFFFFFFFu) {
+        bflush_band<kExact>(A, hist, old_band);
+        __syncthreads();
+      }
+      const uint32_t c0 = band * cb;
+      // lane 0 keeps the record of the warp's next item loaded ahead
+      uint32_t my = seg_end;
+      BandItem my_a{}, my_b{};
+      if (lane == 0 && !bad) {
+        my = cur + atomicAdd(&s_next, 1u);
+        if (my < seg_end) {
+          my_a = L.items[my];
+          my_b = L.items[my + 1];
         }
       }
-      ItemGeo gcur;
-      gcur.e0 = __shfl_sync(0xffffffffu, gl.e0, 0);
-      gcur.ea = __shfl_sync(0xffffffffu, gl.ea, 0);
-      gcur.u0 = __shfl_sync(0xffffffffu, gl.u0, 0);
-      gcur.ra = __shfl_sync(0xffffffffu, gl.ra, 0);
-      gcur.n = __shfl_sync(0xffffffffu, gl.n, 0);
-      gcur.nu = __shfl_sync(0xffffffffu, gl.nu, 0);
-      gcur.ev_off = __shfl_sync(0xffffffffu, gl.ev_off, 0);
-      gcur.rec_off = __shfl_sync(0xffffffffu, gl.rec_off, 0);
-      gcur.ev_bytes = gcur.rec_bytes = 0;
-      gcur.ok = __shfl_sync(0xffffffffu, (int)gl.ok, 0) != 0;
-      bool ok = false;
-      for (uint32_t it = 0; it < kWaitLimit && !ok; ++it) ok = mbar_try_wait(bar, phase);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) {
-        if (lane == 0) berr(a.err, my, kErrTileOverflow);
-        bad = true;
-        break;
+      my = __shfl_sync(0xffffffffu, my, 0);
+      while (my < seg_end) {
+        uint32_t nx = seg_end;
+        BandItem nx_a{}, nx_b{};
+        ItemGeo gl{};
+        if (lane == 0) {
+          gl = item_geo(my_a.e0, my_a.u0, my_b.e0, my_b.u0);
+          stage_item(L, gl, wbuf, bar);
+          nx = cur + atomicAdd(&s_next, 1u);
+          if (nx < seg_end) {
+            nx_a = L.items[nx];
+            nx_b = L.items[nx + 1];
+          }
+        }
+        ItemGeo gcur;
+        gcur.e0 = __shfl_sync(0xffffffffu, gl.e0, 0);
+        gcur.ea = __shfl_sync(0xffffffffu, gl.ea, 0);
+        gcur.u0 = __shfl_sync(0xffffffffu, gl.u0, 0);
+        gcur.ra = __shfl_sync(0xffffffffu, gl.ra, 0);
+        gcur.n = __shfl_sync(0xffffffffu, gl.n, 0);
+        gcur.nu = __shfl_sync(0xffffffffu, gl.nu, 0);
+        gcur.ev_off = __shfl_sync(0xffffffffu, gl.ev_off, 0);
+        gcur.rec_off = __shfl_sync(0xffffffffu, gl.rec_off, 0);
+        gcur.ev_bytes = gcur.rec_bytes = 0;
+        gcur.ok = __shfl_sync(0xffffffffu, (int)gl.ok, 0) != 0;
+        bool ok = false;
+        for (uint32_t it = 0; it < kWaitLimit && !ok; ++it) ok = mbar_try_wait(bar, phase);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) {
+          if (lane == 0) berr(a.err, my, kErrTileOverflow);
+          bad = true;
+          break;
+        }
+        phase ^= 1u;
+        band_item<kPow2, kDebug, kExact>(A, CT, hist, X, my, gcur, c0, acc);
+        if (++since == kTotEvery) {
+          bflush_acc(acc, s_tot);
+          since = 0;
+        }
+        my = __shfl_sync(0xffffffffu, nx, 0);
+        my_a = nx_a;
+        my_b = nx_b;
       }
-      phase ^= 1u;
-      band_item<kPow2, kDebug, kExact>(A, CT, hist, X, my, gcur, c0, acc);
-      if (++since == kTotEvery) {
-        bflush_acc(acc, s_tot);
-        since = 0;
-      }
-      my = __shfl_sync(0xffffffffu, nx, 0);
-      my_a = nx_a;
-      my_b = nx_b;
+      cur = seg_end;
+    }
+    __syncthreads();  // the chunk's items are done
+    if (tid == 0) {
+      s_chunk = pref;
+      pref = atomicAdd(A.item_ctr, (uint32_t)kChunkItems);
     }
     __syncthreads();
-    bflush_band<kExact>(A, hist, band);
-    cur = seg_end;
-    __syncthreads();
   }
+  __syncthreads();
+  if (s_band != 0xFFFFFFFFu) bflush_band<kExact>(A, hist, s_band);
   bflush_acc(acc, s_tot);
   if (bad && lane == 0) {
     // let this warp's copy in flight land (bounded) before the CTA ends

@@ -183,14 +183,15 @@ struct BandBuildArgs {
   bool pow2;
   uint32_t mb, n_bands;
   uint8_t* bigf;         // [G] 1 for a big gate -- temporary
+  uint32_t* grank;       // [G] place of each gate in the layout's gate order -- temporary
   uint32_t* cnt_gb;      // [n_bands * G] units per (band, gate) -- temporary
   uint32_t* evc_gb;      // [n_bands * G] events per (band, gate) -- temporary
   uint64_t* ubase;       // [n_bands * G + 1] first unit of each (band, gate) -- temporary
   uint64_t* ebase;       // [n_bands * G + 1] first banded event of each (band, gate) -- temporary
   uint32_t* uband;       // [n_units] -- temporary
   uint64_t* uoff;        // [n_units + 1] -- temporary
-  uint32_t* flags;       // [n_units] item heads -- temporary
-  uint64_t* ipos;        // [n_units + 1] -- temporary
+  uint32_t* flags;       // [max(G, n_units)] class flags, then item heads -- temporary
+  uint64_t* ipos;        // [max(G + 2, n_units + 1)] scans -- temporary
   uint64_t* scan_blk;    // scan scratch -- temporary
   uint32_t* counters;    // [4]: big gates, gates with windows narrower than a band -- temporary
   BandLayout L;
@@ -200,6 +201,7 @@ struct BandBuildArgs {
 struct BandRunArgs {
   RunArgs r;             // cells, lut, leak, gates, params, bins, totals, err, debug
   BandLayout L;
+  uint32_t* item_ctr;    // items handed out so far (zero before the launch)
 };
 
 // kernels (pa_kernels.cu)
