@@ -456,6 +456,7 @@ constexpr int kAxStride = 9;
 constexpr size_t kCellsB = (size_t)kSmemCells * (2 + 4 * kAxStride) * 4;
 constexpr size_t kSmemB = kHist + kCellsB + kBW * kWarpB;
 static_assert(kStageB % 16 == 0 && kWarpB % 16 == 0 && kHist % 16 == 0 && kCellsB % 16 == 0, "alignment");
+static_assert(kBW * kWarpB >= kHist, "a band's rows fit the warp buffers");
 static_assert(kSmemB + 1024 <= 227 * 1024, "shared memory budget");
 constexpr int kTotEvery = 16;              // items between flushes of a warp's per-lane totals
 constexpr int kChunkItems = 256;           // items a CTA takes from the global counter at a time
@@ -522,53 +523,33 @@ __device__ __forceinline__ void bflush_acc(BAcc& acc, double* s_tot) {
   acc = BAcc{0.f, 0.f, 0.f, 0.f};
 }
 
-// The band's bins in shared memory: 16 bytes per cycle holding {W, D, ev, gl}
-// with the fields rotated by (cycle >> 3) & 3 words, so that one field of
-// 32 different cycles falls in 32 different banks (unrotated, every W would
-// sit in the same 8 banks). Word of field f of local cycle lc:
-__device__ __forceinline__ uint32_t hist_word(uint32_t lc, uint32_t f) {
-  return 4u * lc + ((f + (lc >> 3)) & 3u);
-}
+// The band's bins in shared memory: four arrays of kBandMaxCycles words,
+// W and D (f32) then ev and gl (u32), so one field of 32 different cycles falls
+// in 32 different banks.
+constexpr uint32_t kHW = 0, kHD = kBandMaxCycles, kHE = 2 * kBandMaxCycles, kHG = 3 * kBandMaxCycles;
 
 // Add the band's shared-memory bins to the global bins and clear them. Fast
-// mode: rows are put back in {W, D, ev, gl} order as f32 (counts converted in
-// place), then one bulk reduction. Exact mode adds per event to global
-// memory; nothing to flush.
+// mode: the rows {W, D, ev, gl} (counts as f32) are written to `rows` (free
+// shared memory while no warp holds an item), then one bulk reduction. Exact
+// mode adds per event to global memory; nothing to flush.
 template <bool kExact>
-__device__ void bflush_band(const BandRunArgs& A, float4* hist, uint32_t band) {
+__device__ void bflush_band(const BandRunArgs& A, float* hist, float4* rows, uint32_t band) {
   const uint32_t cb = A.L.band_cycles, N = A.r.n_cycles;
   const uint32_t c0 = band * cb;
   const uint32_t nb = c0 < N ? min(cb, N - c0) : 0u;
+  const uint32_t* hu = reinterpret_cast<const uint32_t*>(hist);
   if (!kExact) {
-    for (uint32_t i = threadIdx.x; i < nb; i += kBT) {
-      const uint32_t w = __float_as_uint(hist[i].x), x = __float_as_uint(hist[i].y),
-                     y = __float_as_uint(hist[i].z), z = __float_as_uint(hist[i].w);
-      const uint32_t rot = (i >> 3) & 3u;
-      // field f sits at word (f + rot) & 3: rotate the row left by rot words
-      uint32_t f0 = w, f1 = x, f2 = y, f3 = z;
-      if (rot & 1u) {
-        const uint32_t t0 = f0;
-        f0 = f1;
-        f1 = f2;
-        f2 = f3;
-        f3 = t0;
-      }
-      if (rot & 2u) {
-        uint32_t t0 = f0;
-        f0 = f2;
-        f2 = t0;
-        t0 = f1;
-        f1 = f3;
-        f3 = t0;
-      }
-      hist[i] = make_float4(__uint_as_float(f0), __uint_as_float(f1), (float)f2, (float)f3);
-    }
+    for (uint32_t i = threadIdx.x; i < nb; i += kBT)
+      rows[i] = make_float4(hist[kHW + i], hist[kHD + i], (float)hu[kHE + i], (float)hu[kHG + i]);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
-    if (threadIdx.x == 0 && nb) bulk_red_add_f32(A.r.bins + c0, hist, nb * 16u);
+    if (threadIdx.x == 0 && nb) bulk_red_add_f32(A.r.bins + c0, rows, nb * 16u);
     __syncthreads();
   }
-  for (uint32_t i = threadIdx.x; i < cb; i += kBT) hist[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (uint32_t i = threadIdx.x; i < 4 * cb; i += kBT) {
+    const uint32_t f = i / cb, c = i - f * cb;
+    hist[f * kBandMaxCycles + c] = 0.f;
+  }
 }
 
 // First item in [lo, hi) whose band differs from `band` (items are band-sorted).
@@ -622,6 +603,8 @@ __device__ __forceinline__ void stage_item(const BandLayout& L, const ItemGeo& g
   mbar_expect_arrive(bar, g.ev_bytes + g.rec_bytes);
   bulk_g2s(stage, L.bt + g.ea, g.ev_bytes, bar);
   bulk_g2s(stage + (size_t)kStEv * 4, L.urec + g.ra, g.rec_bytes, bar);
+  // the slews stay in HBM; start bringing them into L2 now
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(L.bs + g.ea), "r"(g.ev_bytes) : "memory");
 }
 
 // Events of a sorted pin segment b[0, qn) (qn <= 15) earlier than t: the
@@ -665,7 +648,7 @@ struct WarpScratch {
 // Everything after the gate state and energies are known: glitch scaling,
 // totals, in-cycle leakage part and the bins (and the debug outputs).
 template <bool kPow2, bool kDebug, bool kExact>
-__device__ __forceinline__ void event_tail(const BandRunArgs& A, float4* hist, const float* ts, const float* gs,
+__device__ __forceinline__ void event_tail(const BandRunArgs& A, float* hist, const float* ts, const float* gs,
                                            int e, int idx, int p, int k, float t, float s, float e_int,
                                            float e_sw, float dp, uint32_t s_pre, int lis, int j, uint32_t gate,
                                            uint32_t item, uint32_t c0, BAcc& acc) {
@@ -707,11 +690,11 @@ __device__ __forceinline__ void event_tail(const BandRunArgs& A, float4* hist, c
     atomicAdd(a.cnt_ev + c, 1u);
     if (glitch) atomicAdd(a.cnt_gl + c, 1u);
   } else {
-    float* h = reinterpret_cast<float*>(hist);
-    atomicAdd(h + hist_word(lc, 0), e_w);
-    if (p < k) atomicAdd(h + hist_word(lc, 1), dp);
-    atomicAdd(reinterpret_cast<uint32_t*>(h + hist_word(lc, 2)), 1u);
-    if (glitch) atomicAdd(reinterpret_cast<uint32_t*>(h + hist_word(lc, 3)), 1u);
+    float* h = hist + lc;
+    atomicAdd(h + kHW, e_w);
+    if (p < k) atomicAdd(h + kHD, dp);
+    atomicAdd(reinterpret_cast<uint32_t*>(h + kHE), 1u);
+    if (glitch) atomicAdd(reinterpret_cast<uint32_t*>(h + kHG), 1u);
   }
   if (kDebug) {
     // CSR index of this event: its rank among its pin's events
@@ -758,7 +741,7 @@ __device__ __forceinline__ void space_mark(uint32_t* mask, uint32_t* pre, uint32
 // One staged item on one warp: unit slots, then the input events, then the
 // output events (each lane one event of one kind at a time).
 template <bool kPow2, bool kDebug, bool kExact>
-__device__ __forceinline__ void band_item(const BandRunArgs& A, const CellTab& CT, float4* hist,
+__device__ __forceinline__ void band_item(const BandRunArgs& A, const CellTab& CT, float* hist,
                                           const WarpScratch& X, uint32_t item, const ItemGeo& g, uint32_t c0,
                                           BAcc& acc) {
   const RunArgs& a = A.r;
@@ -768,8 +751,11 @@ __device__ __forceinline__ void band_item(const BandRunArgs& A, const CellTab& C
     return;
   }
   const float* ts = reinterpret_cast<const float*>(X.stage) + g.ev_off;
-  const float* gs = A.L.bs + g.e0;  // slews: read once, from HBM
+  const float* gs = A.L.bs + g.e0;  // slews: read once, from HBM (prefetched into L2 at staging)
   const uint2* rec = reinterpret_cast<const uint2*>(X.stage + (size_t)kStEv * 4) + g.rec_off;
+  // and into L1 while the unit slots are built: one 128-byte line per lane
+  if ((uint32_t)lane * 32u < g.ev_off + g.n)
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(A.L.bs + g.ea + 32u * (uint32_t)lane) : "memory");
   const int n = (int)g.n, nu = (int)g.nu;
   // ---- units. One packed scan gives, per unit, its offsets in the input and
   // output index spaces and its ranks among units with inputs / outputs.
@@ -920,7 +906,8 @@ __device__ __forceinline__ void band_item(const BandRunArgs& A, const CellTab& C
 template <bool kPow2, bool kDebug, bool kExact>
 __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
   extern __shared__ __align__(128) uint8_t smem[];
-  float4* hist = reinterpret_cast<float4*>(smem);
+  float* hist = reinterpret_cast<float*>(smem);
+  float4* rows = reinterpret_cast<float4*>(smem + kHist + kCellsB);  // the warp buffers, during a flush
   uint32_t* cells_s = reinterpret_cast<uint32_t*>(smem + kHist);
   __shared__ __align__(8) uint64_t s_bar[kBW];
   __shared__ uint32_t s_chunk, s_seg_end, s_band;
@@ -944,7 +931,7 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
   uint64_t* bar = &s_bar[warp];
 
   if (tid < 4) s_tot[tid] = 0.0;
-  for (uint32_t i = tid; i < cb; i += kBT) hist[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (uint32_t i = tid; i < 4 * kBandMaxCycles; i += kBT) hist[i] = 0.f;
   CellTab CT;
   {  // the layout is only built for libraries of at most kSmemCells cells
     uint32_t* info = cells_s;
@@ -1009,7 +996,11 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
       __syncthreads();
       const uint32_t band = s_band, seg_end = s_seg_end;
       if (band != old_band && old_band != 0xFFFFFFFFu) {
-        bflush_band<kExact>(A, hist, old_band);
+        bflush_band<kExact>(A, hist, rows, old_band);
+        if (lane < kMaskWords) {  // the flush used the warp buffers
+          X.in_mask[lane] = 0u;
+          X.out_mask[lane] = 0u;
+        }
         __syncthreads();
       }
       const uint32_t c0 = band * cb;
@@ -1052,7 +1043,14 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
         for (uint32_t it = 0; it < kWaitLimit && !ok; ++it) ok = mbar_try_wait(bar, phase);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) {
-          if (lane == 0) berr(a.err, my, kErrTileOverflow);
+          if (lane == 0) {
+            berr(a.err, my, kErrTileOverflow);
+            // keep waiting (bounded) for the copy in flight: the warp buffers
+            // are reused as flush rows once the band's items are done
+            bool done = false;
+            for (uint32_t it = 0; it < kWaitLimit && !done; ++it) done = mbar_try_wait(bar, phase);
+          }
+          __syncwarp();
           bad = true;
           break;
         }
@@ -1076,13 +1074,8 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
     __syncthreads();
   }
   __syncthreads();
-  if (s_band != 0xFFFFFFFFu) bflush_band<kExact>(A, hist, s_band);
+  if (s_band != 0xFFFFFFFFu) bflush_band<kExact>(A, hist, rows, s_band);
   bflush_acc(acc, s_tot);
-  if (bad && lane == 0) {
-    // let this warp's copy in flight land (bounded) before the CTA ends
-    bool done = false;
-    for (uint32_t it = 0; it < kWaitLimit && !done; ++it) done = mbar_try_wait(bar, phase);
-  }
   __syncthreads();
   if (tid < 4) atomicAdd(a.totals + tid, s_tot[tid]);
 }
