@@ -153,136 +153,152 @@ __device__ __forceinline__ uint32_t bcyc(const BandBuildArgs& a, float t) {
 constexpr uint32_t kNoCycle = 0xFFFFFFFFu;
 
 // kWrite false: units / events per (band, gate) and big gates; true: records,
-// unit offsets and the event copy. Every per-pin array is indexed only by
-// compile-time pin numbers (loops over the kMaxK + 1 pins fully unrolled), so
-// the walk state stays in registers.
+// unit offsets and the event copy. One warp per gate. Each pin keeps a chunk of
+// 32 consecutive events' cycles in the warp's lanes, refilled (one coalesced
+// load) before its lookahead of 16 events would leave the chunk. One window
+// per step: it starts at the earliest next cycle of the pins and ends at the
+// band end or at the cycle of some pin's 16th event from its cursor, whichever
+// is first; each pin's count in the window is one ballot. This gives the same
+// windows as walking the gate's cycles one by one.
 template <bool kWrite>
-__global__ void __launch_bounds__(128) k_bw_greedy(const BandBuildArgs a) {
+__global__ void __launch_bounds__(256) k_bw_walk(const BandBuildArgs a) {
   constexpr int P = kMaxK + 1;
-  const uint64_t g = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x;
-  if (g >= a.n_gates) return;
+  const int lane = threadIdx.x & 31;
+  const uint64_t warp = (blockIdx.x * (uint64_t)blockDim.x + threadIdx.x) >> 5;
+  const uint64_t n_warps = ((uint64_t)gridDim.x * blockDim.x) >> 5;
   const uint64_t G = a.n_gates;
-  if (kWrite && a.bigf[g]) return;
-  const uint64_t gr = a.grank[g];  // the gate's place in the layout's gate order
-  const GateRec r = a.gates[g];
-  const int k = (int)((r.init >> 16) & 0xff);
-  uint64_t pos[P], end[P], wstart[P];
-  uint32_t nc[P], cw[P];
-#pragma unroll
-  for (int p = 0; p < P; ++p) {
-    pos[p] = end[p] = 0;
-    nc[p] = kNoCycle;
-    cw[p] = 0;
-    if (p <= k) {
-      pos[p] = a.pin_off[(uint64_t)r.pin_base + p];
-      end[p] = a.pin_off[(uint64_t)r.pin_base + p + 1];
-      nc[p] = pos[p] < end[p] ? bcyc(a, a.t[pos[p]]) : kNoCycle;
-    }
-    wstart[p] = pos[p];
-  }
-  uint32_t state = r.init & ((1u << k) - 1u);  // input state at the window start
-  uint32_t band = kNoCycle, units = 0, events = 0, wsize = 0;
-  uint64_t u = 0, dst = 0;                      // next unit / banded event of this (band, gate)
-  bool big = false, split = false;
-  for (;;) {
-    // the next cycle with events, and its events per pin
-    uint32_t c = kNoCycle;
-#pragma unroll
-    for (int p = 0; p < P; ++p) c = min(c, nc[p]);
-    uint32_t n_c[P];
-    bool over = false;
+  for (uint64_t g = warp; g < G; g += n_warps) {
+    if (kWrite && a.bigf[g]) continue;
+    const uint64_t gr = a.grank[g];  // the gate's place in the layout's gate order
+    const GateRec r = a.gates[g];
+    const int k = (int)((r.init >> 16) & 0xff);
+    uint64_t lo[P];
+    uint32_t hi[P], j[P], cb[P], cy[P];  // pin length, cursor, chunk base (relative to lo), lane's chunk cycle
 #pragma unroll
     for (int p = 0; p < P; ++p) {
-      n_c[p] = 0;
-      if (c != kNoCycle) {
-        while (nc[p] == c) {
-          ++n_c[p];
-          ++pos[p];
-          nc[p] = pos[p] < end[p] ? bcyc(a, a.t[pos[p]]) : kNoCycle;
+      lo[p] = 0;
+      hi[p] = 0;
+      j[p] = 0;
+      cb[p] = 0;
+      if (p <= k) {
+        lo[p] = a.pin_off[(uint64_t)r.pin_base + p];
+        hi[p] = (uint32_t)(a.pin_off[(uint64_t)r.pin_base + p + 1] - lo[p]);
+      }
+      cy[p] = (uint32_t)lane < hi[p] ? bcyc(a, a.t[lo[p] + lane]) : kNoCycle;
+    }
+    uint32_t state = r.init & ((1u << k) - 1u);  // input state at the window start
+    uint32_t band = kNoCycle, units = 0, events = 0;
+    uint64_t u = 0, dst = 0;  // next unit / banded event of this (band, gate)
+    bool big = false, split = false;
+    for (;;) {
+      uint32_t c_start = kNoCycle;
+#pragma unroll
+      for (int p = 0; p < P; ++p) {
+        const uint32_t c = __shfl_sync(0xffffffffu, cy[p], (int)(j[p] - cb[p]) & 31);
+        if (j[p] < hi[p]) c_start = min(c_start, c);
+      }
+      if (c_start == kNoCycle) break;
+      const uint32_t b = c_start >> a.mb;
+      if (b != band) {
+        if (!kWrite && band != kNoCycle && lane == 0) {
+          a.cnt_gb[(uint64_t)band * G + gr] = units;
+          a.evc_gb[(uint64_t)band * G + gr] = events;
+        }
+        band = b;
+        units = 0;
+        events = 0;
+        if (kWrite) {
+          u = a.ubase[(uint64_t)b * G + gr];
+          dst = a.ebase[(uint64_t)b * G + gr];
         }
       }
-      if (n_c[p] > (uint32_t)kUnitPinMax) big = true;
-      over |= cw[p] + n_c[p] > (uint32_t)kUnitPinMax;
-    }
-    if (big) break;
-    const uint32_t b = c == kNoCycle ? kNoCycle : c >> a.mb;
-    if (wsize > 0 && (c == kNoCycle || b != band || over)) {
-      // close the open window as one unit
-      if (kWrite) {
-        uint32_t x = 0;
+      const uint64_t be = ((uint64_t)b + 1) << a.mb;
+      uint32_t c_end = be > 0xFFFFFFFFull ? 0xFFFFFFFFu : (uint32_t)be;
+      const uint32_t c_band_end = c_end;
 #pragma unroll
-        for (int p = 0; p < P; ++p) x |= cw[p] << (4 * p);
-        x |= state << 20;
-        x |= (r.cell & 0xffu) << 24;
-        if (u < (uint64_t)a.L.n_units && dst + wsize <= a.L.n_ev) {
-          a.L.urec[u] = make_uint2(x, __float_as_uint(r.load));
-          a.L.ugate[u] = (uint32_t)g;
-          a.uband[u] = band;
-          a.uoff[u] = dst;
+      for (int p = 0; p < P; ++p) {
+        const uint32_t c = __shfl_sync(0xffffffffu, cy[p], (int)(j[p] + kUnitPinMax - cb[p]) & 31);
+        if (j[p] + kUnitPinMax < hi[p]) c_end = min(c_end, c);
+      }
+      if (c_end <= c_start) {  // 16 events of one pin in one cycle
+        big = true;
+        break;
+      }
+      if (c_end < c_band_end) split = true;
+      uint32_t n[P], size = 0;
+#pragma unroll
+      for (int p = 0; p < P; ++p) {
+        const int l0 = (int)(j[p] - cb[p]);
+        const bool in = lane >= l0 && lane < l0 + 16 && cy[p] < c_end;
+        n[p] = (uint32_t)__popc(__ballot_sync(0xffffffffu, in));
+        size += n[p];
+      }
+      if (kWrite) {
+        if (u < (uint64_t)a.L.n_units && dst + size <= a.L.n_ev) {
+          if (lane == 0) {
+            uint32_t x = 0;
+#pragma unroll
+            for (int p = 0; p < P; ++p) x |= n[p] << (4 * p);
+            x |= state << 20;
+            x |= (r.cell & 0xffu) << 24;
+            a.L.urec[u] = make_uint2(x, __float_as_uint(r.load));
+            a.L.ugate[u] = (uint32_t)g;
+            a.uband[u] = band;
+            a.uoff[u] = dst;
+          }
           uint64_t d = dst;
 #pragma unroll
           for (int p = 0; p < P; ++p) {
-            for (uint32_t i = 0; i < cw[p]; ++i) {
-              a.L.bt[d + i] = a.t[wstart[p] + i];
-              a.L.bs[d + i] = a.s[wstart[p] + i];
+            if ((uint32_t)lane < n[p]) {
+              const uint64_t src = lo[p] + j[p] + lane;
+              a.L.bt[d + lane] = a.t[src];
+              a.L.bs[d + lane] = a.s[src];
             }
-            d += cw[p];
+            d += n[p];
           }
-        } else {
+        } else if (lane == 0) {
           atomicMin(a.err, (unsigned long long)((g << 8) | kErrTileOverflow));
         }
         ++u;
-        dst += wsize;
+        dst += size;
       }
 #pragma unroll
       for (int p = 0; p < P; ++p) {
-        if (p < k) state ^= (cw[p] & 1u) << p;
-        wstart[p] += cw[p];
-        cw[p] = 0;
+        if (p < k) state ^= (n[p] & 1u) << p;
+        j[p] += n[p];
+        if (j[p] - cb[p] > 16u && j[p] < hi[p]) {  // keep 16 events of lookahead inside the chunk
+          cb[p] = j[p];
+          cy[p] = j[p] + (uint32_t)lane < hi[p] ? bcyc(a, a.t[lo[p] + j[p] + lane]) : kNoCycle;
+        }
       }
-      if (!(c == kNoCycle || b != band)) split = true;
       ++units;
-      events += wsize;
-      wsize = 0;
+      events += size;
     }
-    if (c == kNoCycle) break;
-    if (b != band) {
-      if (!kWrite && band != kNoCycle) {
-        a.cnt_gb[(uint64_t)band * G + gr] = units;
-        a.evc_gb[(uint64_t)band * G + gr] = events;
+    if (!kWrite) {
+      if (big) {
+        // no unit of a big gate: clear what the walk wrote before it saw the cycle
+        for (uint32_t bb = lane; bb < a.n_bands; bb += 32) {
+          a.cnt_gb[(uint64_t)bb * G + gr] = 0;
+          a.evc_gb[(uint64_t)bb * G + gr] = 0;
+        }
+        if (lane == 0) {
+          a.L.big[atomicAdd(a.counters, 1u)] = (uint32_t)g;
+          a.bigf[g] = 1;
+        }
+      } else if (lane == 0) {
+        a.bigf[g] = 0;
+        if (band != kNoCycle) {
+          a.cnt_gb[(uint64_t)band * G + gr] = units;
+          a.evc_gb[(uint64_t)band * G + gr] = events;
+        }
+        if (split) atomicAdd(a.counters + 1, 1u);
       }
-      band = b;
-      units = 0;
-      events = 0;
-      if (kWrite) {
-        u = a.ubase[(uint64_t)b * G + gr];
-        dst = a.ebase[(uint64_t)b * G + gr];
-      }
-    }
-#pragma unroll
-    for (int p = 0; p < P; ++p) {
-      cw[p] += n_c[p];
-      wsize += n_c[p];
-    }
-  }
-  if (!kWrite) {
-    if (big) {
-      // no unit of a big gate: clear what the walk wrote before it saw the cycle
-      for (uint32_t bb = 0; bb < a.n_bands; ++bb) {
-        a.cnt_gb[(uint64_t)bb * G + gr] = 0;
-        a.evc_gb[(uint64_t)bb * G + gr] = 0;
-      }
-      a.L.big[atomicAdd(a.counters, 1u)] = (uint32_t)g;
-      a.bigf[g] = 1;
-    } else {
-      a.bigf[g] = 0;
-      if (band != kNoCycle) {
-        a.cnt_gb[(uint64_t)band * G + gr] = units;
-        a.evc_gb[(uint64_t)band * G + gr] = events;
-      }
-      if (split) atomicAdd(a.counters + 1, 1u);
     }
   }
+}
+
+int walk_grid(uint64_t n_gates) {
+  return (int)std::min<uint64_t>((n_gates * 32 + 255) / 256 + 1, 152ull * 64);
 }
 
 // Layout gate order: gates grouped by class (k, and whether the gate has more
@@ -367,7 +383,7 @@ cudaError_t band_build_count(BandBuildArgs& a, cudaStream_t st) {
   if (e == cudaSuccess) e = cudaMemsetAsync(a.cnt_gb, 0, (n + 1) * sizeof(uint32_t), st);
   if (e == cudaSuccess) e = cudaMemsetAsync(a.evc_gb, 0, (n + 1) * sizeof(uint32_t), st);
   if (e != cudaSuccess) return e;
-  if (a.n_gates) k_bw_greedy<false><<<(a.n_gates + 127) / 128, 128, 0, st>>>(a);
+  if (a.n_gates) k_bw_walk<false><<<walk_grid(a.n_gates), 256, 0, st>>>(a);
   e = scan_u32_to_u64(a.cnt_gb, n, a.scan_blk, a.ubase, st);
   if (e == cudaSuccess) e = scan_u32_to_u64(a.evc_gb, n, a.scan_blk, a.ebase, st);
   if (e != cudaSuccess) return e;
@@ -375,7 +391,7 @@ cudaError_t band_build_count(BandBuildArgs& a, cudaStream_t st) {
 }
 
 cudaError_t band_build_write(BandBuildArgs& a, cudaStream_t st) {
-  if (a.n_gates) k_bw_greedy<true><<<(a.n_gates + 127) / 128, 128, 0, st>>>(a);
+  if (a.n_gates) k_bw_walk<true><<<walk_grid(a.n_gates), 256, 0, st>>>(a);
   const uint32_t nu = a.L.n_units;
   cudaError_t e = cudaMemcpyAsync(a.uoff + nu, &a.L.n_ev, sizeof(uint64_t), cudaMemcpyHostToDevice, st);
   if (e != cudaSuccess) return e;
