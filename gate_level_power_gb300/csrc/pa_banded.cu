@@ -476,7 +476,7 @@ static_assert(kBW * kWarpB >= kHist, "a band's rows fit the warp buffers");
 static_assert(kSmemB + 1024 <= 227 * 1024, "shared memory budget");
 constexpr int kTotEvery = 16;              // items between flushes of a warp's per-lane totals
 constexpr int kChunkItems = 256;           // items a CTA takes from the global counter at a time
-constexpr uint32_t kWaitLimit = 1u << 24;  // mbarrier polls before giving up
+constexpr uint32_t kWaitLimit = 1u << 16;  // bounded mbarrier waits before giving up (seconds in all)
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -491,14 +491,16 @@ __device__ __forceinline__ void mbar_expect_arrive(uint64_t* bar, uint32_t bytes
                : "memory");
 }
 
+// One bounded wait on the barrier's phase: the thread may be suspended for up
+// to about 0.1 ms (the suspend-time hint) before it reports "not yet".
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(100000u)
       : "memory");
   return ok != 0;
 }
@@ -623,15 +625,15 @@ __device__ __forceinline__ void stage_item(const BandLayout& L, const ItemGeo& g
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(L.bs + g.ea), "r"(g.ev_bytes) : "memory");
 }
 
-// Events of a sorted pin segment b[0, qn) (qn <= 15) earlier than t: the
-// first three without branches, the rest by binary lifting.
+// Events of a sorted pin segment b[0, qn) (qn <= 15) earlier than t: up to
+// three by branch-free compares, longer segments by binary lifting.
 __device__ __forceinline__ int seg_rank(const float* b, int qn, float t) {
-  int r = ((int)(qn > 0) & (int)(b[0] < t)) + ((int)(qn > 1) & (int)(b[1] < t)) + ((int)(qn > 2) & (int)(b[2] < t));
-  if (r == 3 && qn > 3) {
+  if (qn <= 3)
+    return ((int)(qn > 0) & (int)(b[0] < t)) + ((int)(qn > 1) & (int)(b[1] < t)) + ((int)(qn > 2) & (int)(b[2] < t));
+  int r = 0;
 #pragma unroll
-    for (int h = 8; h > 0; h >>= 1)
-      if (r + h <= qn && b[r + h - 1] < t) r += h;
-  }
+  for (int h = 8; h > 0; h >>= 1)
+    if (r + h <= qn && b[r + h - 1] < t) r += h;
   return r;
 }
 
