@@ -475,7 +475,10 @@ static_assert(kStageB % 16 == 0 && kWarpB % 16 == 0 && kHist % 16 == 0 && kCells
 static_assert(kBW * kWarpB >= kHist, "a band's rows fit the warp buffers");
 static_assert(kSmemB + 1024 <= 227 * 1024, "shared memory budget");
 constexpr int kTotEvery = 16;              // items between flushes of a warp's per-lane totals
-constexpr int kChunkItems = 256;           // items a CTA takes from the global counter at a time
+// Items a CTA takes from the global counter at a time: about 16 chunks per
+// CTA, within [kChunkMin, kChunkMax] (big chunks mean fewer CTA-wide syncs,
+// small ones a shorter tail).
+constexpr uint32_t kChunkMin = 64, kChunkMax = 1024;
 constexpr uint32_t kWaitLimit = 1u << 16;  // bounded mbarrier waits before giving up (seconds in all)
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -988,20 +991,20 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
   int since = 0;
   uint32_t phase = 0;  // parity of the stage barrier's next completion
   bool bad = false;    // a stage copy never landed: this warp stops working
-  // CTAs take chunks of kChunkItems items from a global counter (the next
+  // CTAs take chunks of A.chunk items from a global counter (the next
   // chunk's start fetched one chunk ahead by thread 0); the band bins stay in
   // shared memory until a chunk brings a new band.
   uint32_t pref = 0;
   if (tid == 0) {
-    s_chunk = atomicAdd(A.item_ctr, (uint32_t)kChunkItems);
-    pref = atomicAdd(A.item_ctr, (uint32_t)kChunkItems);
+    s_chunk = atomicAdd(A.item_ctr, A.chunk);
+    pref = atomicAdd(A.item_ctr, A.chunk);
     s_band = 0xFFFFFFFFu;
   }
   __syncthreads();
   for (;;) {
     const uint32_t c_lo = s_chunk;
     if (c_lo >= n_items) break;
-    const uint32_t c_hi = min(c_lo + (uint32_t)kChunkItems, n_items);
+    const uint32_t c_hi = min(c_lo + A.chunk, n_items);
     for (uint32_t cur = c_lo; cur < c_hi;) {
       const uint32_t old_band = s_band;
       __syncthreads();  // everyone has read s_band / s_chunk
@@ -1087,7 +1090,7 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
     __syncthreads();  // the chunk's items are done
     if (tid == 0) {
       s_chunk = pref;
-      pref = atomicAdd(A.item_ctr, (uint32_t)kChunkItems);
+      pref = atomicAdd(A.item_ctr, A.chunk);
     }
     __syncthreads();
   }
@@ -1137,10 +1140,12 @@ int band_blocks_per_sm(bool pow2, bool debug, bool exact) {
   }
 }
 
-cudaError_t band_fused(const BandRunArgs& A, int sm_count, bool debug, bool exact, cudaStream_t st) {
-  if (A.L.n_items == 0) return cudaSuccess;
-  const bool pow2 = A.r.inv_t_clk != 0.f;
+cudaError_t band_fused(const BandRunArgs& A0, int sm_count, bool debug, bool exact, cudaStream_t st) {
+  if (A0.L.n_items == 0) return cudaSuccess;
+  const bool pow2 = A0.r.inv_t_clk != 0.f;
   const int grid = sm_count * band_blocks_per_sm(pow2, debug, exact);
+  BandRunArgs A = A0;
+  A.chunk = std::min(kChunkMax, std::max(kChunkMin, A.L.n_items / (16u * (uint32_t)grid)));
   const int sel = (pow2 ? 4 : 0) | (debug ? 2 : 0) | (exact ? 1 : 0);
   switch (sel) {
     case 0: band_launch<false, false, false>(A, grid, st); break;

@@ -202,6 +202,7 @@ struct BandRunArgs {
   RunArgs r;             // cells, lut, leak, gates, params, bins, totals, err, debug
   BandLayout L;
   uint32_t* item_ctr;    // items handed out so far (zero before the launch)
+  uint32_t chunk;        // items a CTA takes at a time (set by band_fused)
 };
 
 // kernels (pa_kernels.cu)
