@@ -61,8 +61,9 @@ struct pa_ctx {
   // banded layout (pa_build_bands): persistent parts, build temporaries, run scratch
   BandLayout band;
   uint32_t band_windowed = 0;  // gates cut into windows narrower than a band
-  DevBuf b_bt, b_bs, b_urec, b_ugate, b_items, b_big;
-  DevBuf b_bigf, b_grank, b_cnt, b_evc, b_ubase, b_ebase, b_uband, b_uoff, b_flags, b_ipos, b_scan, b_counters;
+  DevBuf b_bt, b_bs, b_btag, b_urec, b_ugate, b_items, b_big;
+  DevBuf b_bigf, b_grank, b_cnt, b_evc, b_ubase, b_ebase, b_uband, b_uoff, b_flags, b_ipos, b_scan, b_counters,
+      b_urec2;
   DevBuf b_part;
   DevBuf scratch_small;
 };
@@ -422,10 +423,10 @@ void pa_destroy(pa_ctx* c) {
                    &c->value_tmp, &c->err_word, &c->tmax_bits, &c->bins, &c->part_blk,
                    &c->part_counts, &c->tiles, &c->heavy, &c->p0_tot, &c->p_out, &c->dbg[0],
                    &c->dbg[1], &c->dbg[2], &c->wave_tmp, &c->cnt_tmp, &c->scratch_small,
-                   &c->chunk_sums, &c->b_bt, &c->b_bs, &c->b_urec, &c->b_ugate, &c->b_items,
+                   &c->chunk_sums, &c->b_bt, &c->b_bs, &c->b_btag, &c->b_urec, &c->b_ugate, &c->b_items,
                    &c->b_big, &c->b_bigf, &c->b_grank, &c->b_cnt, &c->b_evc, &c->b_ubase, &c->b_ebase,
                    &c->b_uband, &c->b_uoff, &c->b_flags, &c->b_ipos, &c->b_scan, &c->b_counters,
-                   &c->b_part};
+                   &c->b_urec2, &c->b_part};
   for (DevBuf* b : all) dfree(*b);
   for (auto& e : c->ev)
     if (e) cudaEventDestroy(e);
@@ -774,7 +775,7 @@ int check_build_err(pa_ctx* c) {
 
 void free_build_temps(pa_ctx* c) {
   DevBuf* tmp[] = {&c->b_bigf, &c->b_grank, &c->b_cnt, &c->b_evc, &c->b_ubase, &c->b_ebase, &c->b_uband,
-                   &c->b_uoff, &c->b_flags, &c->b_ipos, &c->b_scan, &c->b_counters};
+                   &c->b_uoff, &c->b_flags, &c->b_ipos, &c->b_scan, &c->b_counters, &c->b_urec2};
   for (DevBuf* b : tmp) dfree(*b);
 }
 
@@ -803,6 +804,7 @@ int build_bands(pa_ctx* c, float t_clk, uint32_t cb) {
   a.mb = mb;
   a.n_bands = nb;
   a.err = (unsigned long long*)c->err_word.p;
+  a.cells = (const CellDesc*)c->cells.p;
   BandLayout& L = a.L;
   L.t_clk = t_clk;
   L.band_cycles = cb;
@@ -847,7 +849,9 @@ int build_bands(pa_ctx* c, float t_clk, uint32_t cb) {
   // write: records, event copy, item heads
   const size_t nu = (size_t)n_units;
   const size_t ev_bytes = ((n_ev + 64) & ~(size_t)15) * sizeof(float);
-  PA_TRY(dreserve(c, c->b_urec, (nu + 2) * sizeof(uint2)));
+  PA_TRY(dreserve(c, c->b_urec2, (nu + 1) * sizeof(uint2)));
+  PA_TRY(dreserve(c, c->b_urec, (nu + 1) * sizeof(uint4)));
+  PA_TRY(dreserve(c, c->b_btag, (size_t)n_ev + 64));
   PA_TRY(dreserve(c, c->b_ugate, (nu + 1) * sizeof(uint32_t)));
   PA_TRY(dreserve(c, c->b_uband, (nu + 1) * sizeof(uint32_t)));
   PA_TRY(dreserve(c, c->b_uoff, (nu + 1) * sizeof(uint64_t)));
@@ -856,7 +860,9 @@ int build_bands(pa_ctx* c, float t_clk, uint32_t cb) {
   PA_TRY(dreserve(c, c->b_bt, ev_bytes));
   PA_TRY(dreserve(c, c->b_bs, ev_bytes));
   PA_TRY(dreserve(c, c->b_scan, ((size_t)band_scan_blocks(std::max<uint64_t>(nbg, nu)) + 1) * sizeof(uint64_t)));
-  L.urec = (uint2*)c->b_urec.p;
+  L.urec = (uint4*)c->b_urec.p;
+  L.btag = (uint8_t*)c->b_btag.p;
+  a.urec2 = (uint2*)c->b_urec2.p;
   L.ugate = (uint32_t*)c->b_ugate.p;
   L.bt = (float*)c->b_bt.p;
   L.bs = (float*)c->b_bs.p;

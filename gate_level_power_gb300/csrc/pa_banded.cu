@@ -241,7 +241,7 @@ __global__ void __launch_bounds__(256) k_bw_walk(const BandBuildArgs a) {
             for (int p = 0; p < P; ++p) x |= n[p] << (4 * p);
             x |= state << 20;
             x |= (r.cell & 0xffu) << 24;
-            a.L.urec[u] = make_uint2(x, __float_as_uint(r.load));
+            a.urec2[u] = make_uint2(x, __float_as_uint(r.load));
             a.L.ugate[u] = (uint32_t)g;
             a.uband[u] = band;
             a.uoff[u] = dst;
@@ -352,15 +352,132 @@ __global__ void __launch_bounds__(256) k_bw_item_emit(const BandBuildArgs a, uin
     BandItem it;
     it.e0 = a.uoff[u];
     it.u0 = u;
-    it.band = a.uband[u];
+    it.bw = a.uband[u];  // the finalize pass adds the input-event count
     a.L.items[a.ipos[u]] = it;
   }
   if (u == 0) {
     BandItem s;
     s.e0 = a.L.n_ev;
     s.u0 = n_units;
-    s.band = a.n_bands;
+    s.bw = a.n_bands;
     a.L.items[n_items] = s;
+  }
+}
+
+// Finalize pass, one warp per item: the item's events are moved into an
+// input region (every unit's input-pin events, unit by unit) followed by an
+// output region (every unit's output-pin events, unit by unit), each event
+// gets its tag, and each unit its 16-byte record. The load-axis interval and
+// fraction of the unit's gate are fixed here (the library and the netlist do
+// not change while the layout lives); everything that depends on the events'
+// arithmetic is left to the run.
+constexpr int kFinWarps = 8;
+
+__global__ void __launch_bounds__(kFinWarps * 32) k_bw_finalize(const BandBuildArgs a) {
+  __shared__ float tb[kFinWarps][kItemEvents];
+  __shared__ float sb[kFinWarps][kItemEvents];
+  __shared__ uint8_t gb[kFinWarps][kItemEvents];
+  __shared__ uint32_t ust[kFinWarps][kItemUnits];  // unit starts in the walk's order, item-relative
+  __shared__ uint32_t udst[kFinWarps][kItemUnits]; // input offset | output offset (in the region) << 9 | inputs << 18
+  __shared__ uint32_t upin[kFinWarps][kItemUnits]; // record word y
+  const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
+  const uint64_t warp = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const uint64_t n_warps = ((uint64_t)gridDim.x * blockDim.x) >> 5;
+  const BandLayout& L = a.L;
+  for (uint64_t it = warp; it < L.n_items; it += n_warps) {
+    const uint64_t e0 = L.items[it].e0, e1 = L.items[it + 1].e0;
+    const uint32_t u0 = L.items[it].u0, u1 = L.items[it + 1].u0;
+    if (e1 <= e0 || e1 - e0 >= (uint64_t)kItemEvents || u1 <= u0 || u1 - u0 > (uint32_t)kItemUnits) {
+      if (lane == 0) atomicMin(a.err, (unsigned long long)((it << 8) | kErrTileOverflow));
+      continue;
+    }
+    const int n = (int)(e1 - e0), nu = (int)(u1 - u0);
+    // units: sizes, the two regions' offsets, pin starts
+    uint32_t carry = 0;
+    for (int r = 0; r < 2; ++r) {
+      const int uu = lane + 32 * r;
+      uint32_t pk = 0, n_in = 0, x = 0, y = 0;
+      if (uu < nu) {
+        x = a.urec2[u0 + uu].x;
+        const uint32_t k = a.cells[x >> 24].k;
+        uint32_t s = 0;
+#pragma unroll
+        for (int p = 0; p < kMaxK; ++p) {
+          if ((uint32_t)p < k) s += (x >> (4 * p)) & 15u;
+          y |= s << (8 * p);
+        }
+        y |= (k - 1u) << 30;
+        n_in = s;
+        const uint32_t n_out = (x >> (4 * k)) & 15u;
+        pk = (n_in + n_out) | (n_in << 10) | (n_out << 20);
+      }
+      uint32_t inc = pk;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += v;
+      }
+      const uint32_t ex = carry + inc - pk;
+      carry += __shfl_sync(0xffffffffu, inc, 31);
+      if (uu < nu) {
+        ust[wl][uu] = ex & 1023u;
+        udst[wl][uu] = ((ex >> 10) & 1023u) | (((ex >> 20) & 1023u) << 9) | (n_in << 18);
+        upin[wl][uu] = y;
+      }
+    }
+    __syncwarp();
+    const uint32_t n_in_all = (carry >> 10) & 1023u;
+    if ((carry & 1023u) != (uint32_t)n || n_in_all + ((carry >> 20) & 1023u) != (uint32_t)n) {
+      if (lane == 0) atomicMin(a.err, (unsigned long long)((it << 8) | kErrTileOverflow));
+      continue;
+    }
+    for (int r = 0; r < 2; ++r) {
+      const int uu = lane + 32 * r;
+      if (uu < nu) {
+        const uint2 w = a.urec2[u0 + uu];
+        const uint32_t cell = w.x >> 24;
+        const CellDesc& cd = a.cells[cell];
+        const float C = __uint_as_float(w.y);
+        int j = 0;
+        for (int m = 1; m <= (int)cd.nl - 2; ++m) j += (C >= cd.lax[m]) ? 1 : 0;
+        const float v = (C - cd.lax[j]) * cd.ilax[j];
+        const uint32_t d = udst[wl][uu];
+        const uint32_t x = (d & 511u) | ((n_in_all + ((d >> 9) & 511u)) << 9) | (cell << 18) |
+                           (((w.x >> 20) & 15u) << 24) | ((uint32_t)j << 28);
+        L.urec[u0 + uu] = make_uint4(x, upin[wl][uu], __float_as_uint(v), w.y);
+      }
+    }
+    // events: each to its place in the two regions
+    for (int i = lane; i < n; i += 32) {
+      int u = 0;
+#pragma unroll
+      for (int h = kItemUnits / 2; h > 0; h >>= 1)
+        if (u + h < nu && ust[wl][u + h] <= (uint32_t)i) u += h;
+      const int li = i - (int)ust[wl][u];
+      const uint32_t d = udst[wl][u], y = upin[wl][u];
+      const int n_in = (int)(d >> 18);
+      int dst;
+      uint32_t tag = (uint32_t)u;
+      if (li < n_in) {
+        dst = (int)(d & 511u) + li;
+        const uint32_t p = (uint32_t)(li >= (int)(y & 63u)) + (uint32_t)(li >= (int)((y >> 8) & 63u)) +
+                           (uint32_t)(li >= (int)((y >> 16) & 63u));
+        tag |= p << 6;
+      } else {
+        dst = (int)n_in_all + (int)((d >> 9) & 511u) + (li - n_in);
+      }
+      tb[wl][dst] = L.bt[e0 + i];
+      sb[wl][dst] = L.bs[e0 + i];
+      gb[wl][dst] = (uint8_t)tag;
+    }
+    __syncwarp();
+    for (int i = lane; i < n; i += 32) {
+      L.bt[e0 + i] = tb[wl][i];
+      L.bs[e0 + i] = sb[wl][i];
+      L.btag[e0 + i] = gb[wl][i];
+    }
+    if (lane == 0) L.items[it].bw = (L.items[it].bw & kItemBandMask) | (n_in_all << kItemBandBits);
+    __syncwarp();
   }
 }
 
@@ -404,6 +521,10 @@ cudaError_t band_build_write(BandBuildArgs& a, cudaStream_t st) {
 cudaError_t band_build_items(BandBuildArgs& a, cudaStream_t st) {
   const uint32_t nu = a.L.n_units;
   k_bw_item_emit<<<nu ? (nu + 255) / 256 : 1, 256, 0, st>>>(a, nu, a.L.n_items);
+  if (a.L.n_items) {
+    const uint64_t blocks = ((uint64_t)a.L.n_items + kFinWarps - 1) / kFinWarps;
+    k_bw_finalize<<<(int)std::min<uint64_t>(blocks, 152ull * 16), kFinWarps * 32, 0, st>>>(a);
+  }
   return cudaGetLastError();
 }
 
@@ -440,38 +561,36 @@ cudaError_t band_p0(const RunArgs& r, cudaStream_t st) {
 
 // ------------------------------------------------------------------ banded fused kernel
 //
-// One CTA of 24 warps per SM takes a contiguous, event-balanced run of items
-// and works through it band by band. Inside a band the warps take items from a
-// shared counter and work independently, each with two shared-memory stages:
-// while a warp works on one item, lane 0 has the next item's events and unit
-// records on their way into the other stage (TMA bulk copies completing on the
-// stage's mbarrier) and the item after that's record loaded. Per item, one lane
-// per unit decodes its record into a 16-byte slot and marks the unit's first
-// event in a bit mask; then one lane per event finds its unit from the mask
-// (count of unit starts at or before it), its pin from the slot's pin offsets,
-// and computes gate state, LUT energy (one corner-patch load), glitch and
-// leakage step; the sums go into the band's cycle bins in shared memory. When
-// the band's items are done the CTA adds the bins to global memory with one
-// TMA bulk reduction.
+// One CTA of 32 warps per SM takes chunks of items from a global counter and
+// works through each chunk band by band. Inside a band the warps take items
+// from a shared counter and work independently: lane 0 starts the TMA bulk
+// copies of the item's times, event tags and unit records into the warp's
+// stage (completing on the warp's mbarrier), with the record of the warp's
+// next item loaded ahead. Then one lane per event: first the item's input
+// region (gate state from the unit's start state and the parities of the
+// other input pins' earlier events, LUT energy from one corner-patch load,
+// glitch and leakage step), then its output region (switching energy); the
+// sums go into the band's cycle bins in shared memory. When the band's items
+// are done the CTA adds the bins to global memory with one TMA bulk reduction.
 
 namespace {
 
 constexpr int kBW = 32;
 constexpr int kBT = kBW * 32;
-constexpr int kMaskWords = kItemEvents / 32;
-constexpr int kStEv = kItemEvents + 8;                         // staged floats (16-byte rounding)
-constexpr size_t kStRecB = (size_t)(kItemUnits + 2) * 8;
-constexpr size_t kStageB = (size_t)kStEv * 4 + kStRecB;  // times and unit records (slews stay in HBM)
-// stage, unit slots, input / output start masks and word prefixes, rank maps
-constexpr size_t kWarpB = kStageB + (size_t)kItemUnits * 16 + 4 * kMaskWords * 4 + 2 * (size_t)kItemUnits * 4;
+constexpr int kStEv = kItemEvents + 8;                     // staged times (16-byte rounding)
+constexpr size_t kStTagOff = (size_t)kStEv * 4;            // staged event tags
+constexpr size_t kStRecOff = kStTagOff + kItemEvents + 32; // staged unit records
+constexpr size_t kWarpB = kStRecOff + (size_t)kItemUnits * 16;
 constexpr size_t kHist = (size_t)kBandMaxCycles * 16;
 // Cell table in shared memory, structure of arrays: per cell one info word
-// (ns | nl << 8 | k << 16), the patch offset, and the four axis arrays at a
-// stride of 9 words, so lanes reading different cells hit different banks.
+// (ns | nl << 8 | k << 16), the patch offset, and the two slew-axis arrays at
+// a stride of 9 words, so lanes reading different cells hit different banks.
 constexpr int kAxStride = 9;
-constexpr size_t kCellsB = (size_t)kSmemCells * (2 + 4 * kAxStride) * 4;
+constexpr size_t kCellsB = (size_t)kSmemCells * (2 + 2 * kAxStride) * 4;
 constexpr size_t kSmemB = kHist + kCellsB + kBW * kWarpB;
-static_assert(kStageB % 16 == 0 && kWarpB % 16 == 0 && kHist % 16 == 0 && kCellsB % 16 == 0, "alignment");
+static_assert(kStTagOff % 16 == 0 && kStRecOff % 16 == 0 && kWarpB % 16 == 0 && kHist % 16 == 0 &&
+                  kCellsB % 16 == 0,
+              "alignment");
 static_assert(kBW * kWarpB >= kHist, "a band's rows fit the warp buffers");
 static_assert(kSmemB + 1024 <= 227 * 1024, "shared memory budget");
 constexpr int kTotEvery = 16;              // items between flushes of a warp's per-lane totals
@@ -573,12 +692,14 @@ __device__ void bflush_band(const BandRunArgs& A, float* hist, float4* rows, uin
   }
 }
 
+__device__ __forceinline__ uint32_t item_band(const BandItem& it) { return it.bw & kItemBandMask; }
+
 // First item in [lo, hi) whose band differs from `band` (items are band-sorted).
 __device__ uint32_t band_end(const BandLayout& L, uint32_t lo, uint32_t hi, uint32_t band) {
   uint32_t n = hi - lo;
   while (n > 0) {
     const uint32_t half = n >> 1;
-    if (L.items[lo + half].band <= band) {
+    if ((L.items[lo + half].bw & kItemBandMask) <= band) {
       lo += half + 1;
       n -= half + 1;
     } else {
@@ -588,28 +709,30 @@ __device__ uint32_t band_end(const BandLayout& L, uint32_t lo, uint32_t hi, uint
   return lo;
 }
 
-// Staging geometry of an item: events [e0, e0 + n) and units [u0, u0 + nu),
-// rounded out to 16-byte copies. ok is false for an item that cannot be
-// staged (never for a consistent layout).
+// Staging geometry of an item: events [e0, e0 + n) (the first n_in of them
+// input-pin events) and units [u0, u0 + nu), rounded out to 16-byte copies.
+// ok is false for an item that cannot be staged (never for a consistent
+// layout).
 struct ItemGeo {
   uint64_t e0, ea;
-  uint32_t u0, ra, n, nu, ev_off, rec_off, ev_bytes, rec_bytes;
+  uint32_t u0, n, nu, n_in, ev_off, tag_off, ev_bytes, tag_bytes;
   bool ok;
 };
 
-__device__ __forceinline__ ItemGeo item_geo(uint64_t e0, uint32_t u0, uint64_t e1, uint32_t u1) {
+__device__ __forceinline__ ItemGeo item_geo(const BandItem& a, const BandItem& b) {
   ItemGeo g;
-  g.e0 = e0;
-  g.u0 = u0;
-  g.ea = e0 & ~3ull;
-  g.ra = u0 & ~1u;
-  g.ev_off = (uint32_t)(e0 - g.ea);
-  g.rec_off = u0 - g.ra;
-  g.ok = e1 > e0 && u1 > u0 && e1 - e0 < (uint64_t)kItemEvents && u1 - u0 <= (uint32_t)kItemUnits;
-  g.n = g.ok ? (uint32_t)(e1 - e0) : 0u;
-  g.nu = g.ok ? u1 - u0 : 0u;
+  g.e0 = a.e0;
+  g.u0 = a.u0;
+  g.ea = a.e0 & ~3ull;
+  g.ev_off = (uint32_t)(a.e0 - g.ea);
+  g.tag_off = (uint32_t)(a.e0 & 15ull);
+  g.n_in = a.bw >> kItemBandBits;
+  g.ok = b.e0 > a.e0 && b.u0 > a.u0 && b.e0 - a.e0 < (uint64_t)kItemEvents && b.u0 - a.u0 <= (uint32_t)kItemUnits &&
+         (uint64_t)g.n_in <= b.e0 - a.e0;
+  g.n = g.ok ? (uint32_t)(b.e0 - a.e0) : 0u;
+  g.nu = g.ok ? b.u0 - a.u0 : 0u;
   g.ev_bytes = ((g.ev_off + g.n + 3u) & ~3u) * 4u;
-  g.rec_bytes = ((g.rec_off + g.nu + 1u) & ~1u) * 8u;
+  g.tag_bytes = (g.tag_off + g.n + 15u) & ~15u;
   return g;
 }
 
@@ -621,28 +744,29 @@ __device__ __forceinline__ void stage_item(const BandLayout& L, const ItemGeo& g
     return;
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  mbar_expect_arrive(bar, g.ev_bytes + g.rec_bytes);
+  mbar_expect_arrive(bar, g.ev_bytes + g.tag_bytes + g.nu * 16u);
   bulk_g2s(stage, L.bt + g.ea, g.ev_bytes, bar);
-  bulk_g2s(stage + (size_t)kStEv * 4, L.urec + g.ra, g.rec_bytes, bar);
+  bulk_g2s(stage + kStTagOff, L.btag + (g.e0 - g.tag_off), g.tag_bytes, bar);
+  bulk_g2s(stage + kStRecOff, L.urec + g.u0, g.nu * 16u, bar);
   // the slews stay in HBM; start bringing them into L2 now
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(L.bs + g.ea), "r"(g.ev_bytes) : "memory");
 }
 
-// Events of a sorted pin segment b[0, qn) (qn <= 15) earlier than t: up to
-// three by branch-free compares, longer segments by binary lifting.
+// Events of a sorted pin segment b[0, qn) (qn <= 7) earlier than t, by
+// three steps of binary lifting.
+static_assert(kUnitPinMax <= 7, "three lifting steps cover a pin segment");
 __device__ __forceinline__ int seg_rank(const float* b, int qn, float t) {
-  if (qn <= 3)
-    return ((int)(qn > 0) & (int)(b[0] < t)) + ((int)(qn > 1) & (int)(b[1] < t)) + ((int)(qn > 2) & (int)(b[2] < t));
   int r = 0;
 #pragma unroll
-  for (int h = 8; h > 0; h >>= 1)
+  for (int h = 4; h > 0; h >>= 1)
     if (r + h <= qn && b[r + h - 1] < t) r += h;
   return r;
 }
 
-// Start of pin q (0..4) inside its unit from the slot's cumulative counts.
-__device__ __forceinline__ int pin_start(uint32_t cum, int q) {
-  return (int)__byte_perm(cum << 8, cum, q < 4 ? (uint32_t)q : 7u);
+// Start of input pin q (0..4; 4 = end of the inputs) inside the unit's input
+// run, from record word y.
+__device__ __forceinline__ int pin_start(uint32_t y, int q) {
+  return (int)(__byte_perm(y << 8, y, q < 4 ? (uint32_t)q : 7u) & 63u);
 }
 
 struct CellTab {
@@ -650,35 +774,21 @@ struct CellTab {
   const uint32_t* patch;  // [kSmemCells] patch offset
   const float* sax;       // [kSmemCells * kAxStride]
   const float* isax;
-  const float* lax;
-  const float* ilax;
-};
-
-// Per-warp scratch of the banded kernel.
-struct WarpScratch {
-  const uint8_t* stage;
-  uint4* slots;        // [kItemUnits]
-  uint32_t* in_mask;   // [kMaskWords] first input event of each unit, input index space
-  uint32_t* in_pre;    // [kMaskWords] units starting before each word
-  uint32_t* out_mask;  // [kMaskWords] same for the output index space
-  uint32_t* out_pre;
-  uint32_t* in_map;    // [kItemUnits] unit | first input index << 8, by rank
-  uint32_t* out_map;
 };
 
 // Everything after the gate state and energies are known: glitch scaling,
-// totals, in-cycle leakage part and the bins (and the debug outputs).
+// totals, in-cycle leakage part and the bins (and the debug outputs). e is
+// the event's staged index; the pin's previous event, if idx > 0, is e - 1.
 template <bool kPow2, bool kDebug, bool kExact>
 __device__ __forceinline__ void event_tail(const BandRunArgs& A, float* hist, const float* ts, const float* gs,
-                                           int e, int idx, int p, int k, float t, float s, float e_int,
-                                           float e_sw, float dp, uint32_t s_pre, int lis, int j, uint32_t gate,
-                                           uint32_t item, uint32_t c0, BAcc& acc) {
+                                           int e, int idx, bool input, float t, float s, float e_int, float e_sw,
+                                           float dp, uint32_t item, uint32_t c0, BAcc& acc) {
   const RunArgs& a = A.r;
   const float T = a.t_clk, inv_T = a.inv_t_clk;
   const uint32_t c = cyc<kPow2>(t, T, inv_T);
   float tp = 0.f, sp = 0.f;
   bool glitch = false;
-  if (idx > 0) {  // the pin's previous event is the staged event before this one
+  if (idx > 0) {
     tp = ts[e - 1];
     glitch = cyc<kPow2>(tp, T, inv_T) == c;
     if (glitch) sp = __ldg(gs + e - 1);
@@ -699,7 +809,7 @@ __device__ __forceinline__ void event_tail(const BandRunArgs& A, float* hist, co
     berr(a.err, item, kErrTileOverflow);
     return;
   }
-  if (p < k) {
+  if (input) {
     const float rem = fmaf(-(float)c, T, t);  // t - c T
     e_w = fmaf(dp, T - rem, e_w);
     acc.e_lk = fmaf(dp, a.t_max_f - t, acc.e_lk);
@@ -707,63 +817,50 @@ __device__ __forceinline__ void event_tail(const BandRunArgs& A, float* hist, co
   if (kExact) {
     double* bin = reinterpret_cast<double*>(a.bins + c);
     atomicAdd(bin, (double)e_w);
-    if (p < k) atomicAdd(bin + 1, (double)dp);
+    if (input) atomicAdd(bin + 1, (double)dp);
     atomicAdd(a.cnt_ev + c, 1u);
     if (glitch) atomicAdd(a.cnt_gl + c, 1u);
   } else {
     float* h = hist + lc;
     atomicAdd(h + kHW, e_w);
-    if (p < k) atomicAdd(h + kHD, dp);
+    if (input) atomicAdd(h + kHD, dp);
     atomicAdd(reinterpret_cast<uint32_t*>(h + kHE), 1u);
     if (glitch) atomicAdd(reinterpret_cast<uint32_t*>(h + kHG), 1u);
   }
-  if (kDebug) {
-    // CSR index of this event: its rank among its pin's events
-    const GateRec gr = a.gates[gate];
-    const uint64_t pin = (uint64_t)gr.pin_base + p;
-    const uint64_t hi = a.pin_off[pin + 1];
-    uint64_t l = a.pin_off[pin], cnt = hi - l;
-    while (cnt > 0) {
-      const uint64_t half = cnt >> 1;
-      if (a.t[l + half] < t) {
-        l += half + 1;
-        cnt -= half + 1;
-      } else {
-        cnt = half;
-      }
-    }
-    if (l < hi && a.t[l] == t) {
-      a.dbg_state[l] = (uint8_t)s_pre;
-      a.dbg_lut[l] = p < k ? (uint8_t)((lis << 4) | j) : (uint8_t)0xFF;
-      a.dbg_glitch[l] = (uint8_t)glitch;
+}
+
+// Debug outputs of one event: its CSR index is found by its time among its
+// pin's events.
+__device__ void event_debug(const RunArgs& a, uint32_t gate, int p, float t, uint32_t s_pre, int lut_ij,
+                            bool glitch, uint32_t item) {
+  const GateRec gr = a.gates[gate];
+  const uint64_t pin = (uint64_t)gr.pin_base + p;
+  const uint64_t hi = a.pin_off[pin + 1];
+  uint64_t l = a.pin_off[pin], cnt = hi - l;
+  while (cnt > 0) {
+    const uint64_t half = cnt >> 1;
+    if (a.t[l + half] < t) {
+      l += half + 1;
+      cnt -= half + 1;
     } else {
-      berr(a.err, item, kErrTileOverflow);
+      cnt = half;
     }
+  }
+  if (l < hi && a.t[l] == t) {
+    a.dbg_state[l] = (uint8_t)s_pre;
+    a.dbg_lut[l] = (uint8_t)lut_ij;
+    a.dbg_glitch[l] = (uint8_t)glitch;
+  } else {
+    berr(a.err, item, kErrTileOverflow);
   }
 }
 
-// Rank of this lane's index i in an index space (start mask + word prefixes):
-// the number of unit starts at or before i, minus one.
-__device__ __forceinline__ int space_rank(const uint32_t* mask, const uint32_t* pre, int i, uint32_t le_mask) {
-  const int w = i >> 5;
-  return (int)pre[w] + __popc(mask[w] & le_mask) - 1;
-}
-
-// Marks a unit that starts at index o of a space and covers cnt indices.
-__device__ __forceinline__ void space_mark(uint32_t* mask, uint32_t* pre, uint32_t* map, uint32_t rank, uint32_t o,
-                                           uint32_t cnt, uint32_t unit) {
-  map[rank] = unit | (o << 8);
-  if (o < (uint32_t)kItemEvents) atomicOr(mask + (o >> 5), 1u << (o & 31u));
-  // words whose first index lies in (o, o + cnt] follow this unit
-  const uint32_t end = o + cnt;
-  for (uint32_t w = (o >> 5) + 1; w <= (end >> 5) && w < (uint32_t)kMaskWords; ++w) pre[w] = rank + 1;
-}
-
-// One staged item on one warp: unit slots, then the input events, then the
-// output events (each lane one event of one kind at a time).
+// One staged item on one warp: one lane per event, the input region first,
+// then the output region (only the round that crosses from one to the other
+// mixes the two paths).
 template <bool kPow2, bool kDebug, bool kExact>
 __device__ __forceinline__ void band_item(const BandRunArgs& A, const CellTab& CT, float* hist,
-                                          const WarpScratch& X, uint32_t item, const ItemGeo& g, uint32_t c0,
+                                          const uint8_t* stage, uint32_t item, const ItemGeo& g, uint32_t c0,
                                           BAcc& acc) {
   const RunArgs& a = A.r;
   const int lane = threadIdx.x & 31;
@@ -771,155 +868,85 @@ __device__ __forceinline__ void band_item(const BandRunArgs& A, const CellTab& C
     if (lane == 0) berr(a.err, item, kErrTileOverflow);
     return;
   }
-  const float* ts = reinterpret_cast<const float*>(X.stage) + g.ev_off;
+  const float* ts = reinterpret_cast<const float*>(stage) + g.ev_off;
+  const uint8_t* tg = stage + kStTagOff + g.tag_off;
+  const uint4* rec = reinterpret_cast<const uint4*>(stage + kStRecOff);
   const float* gs = A.L.bs + g.e0;  // slews: read once, from HBM (prefetched into L2 at staging)
-  const uint2* rec = reinterpret_cast<const uint2*>(X.stage + (size_t)kStEv * 4) + g.rec_off;
-  // and into L1 while the unit slots are built: one 128-byte line per lane
+  // and into L1: one 128-byte line per lane
   if ((uint32_t)lane * 32u < g.ev_off + g.n)
     asm volatile("prefetch.global.L1 [%0];" ::"l"(A.L.bs + g.ea + 32u * (uint32_t)lane) : "memory");
-  const int n = (int)g.n, nu = (int)g.nu;
-  // ---- units. One packed scan gives, per unit, its offsets in the input and
-  // output index spaces and its ranks among units with inputs / outputs.
-  uint32_t carry = 0;
-  for (int r = 0; r < (nu + 31) / 32; ++r) {
-    const int uu = lane + 32 * r;
-    uint32_t x = 0, pk = 0, n_in = 0, n_out = 0;
-    float C = 0.f;
-    int k = 0;
-    if (uu < nu) {
-      const uint2 rr = rec[uu];
-      x = rr.x;
-      C = __uint_as_float(rr.y);
-      k = (int)((CT.info[x >> 24] >> 16) & 0xFFu);
+  const int n = (int)g.n, n_in = (int)g.n_in;
+  const float T = a.t_clk, inv_T = a.inv_t_clk;
+  for (int i = lane; i < n; i += 32) {
+    const uint32_t tag = tg[i];
+    const uint4 R = rec[tag & 63u];
+    const float t = ts[i];
+    const uint32_t y = R.y;
+    const int k = (int)(y >> 30) + 1;
+    if (i < n_in) {
+      // input event: gate state, LUT, leakage step
+      const int p = (int)(tag >> 6);
+      const int in_off = (int)(R.x & 511u);
+      const int idx = i - in_off - pin_start(y, p);
+      const float s = __ldg(gs + i);
+      const float* ub = ts + in_off;
+      uint32_t s_pre = ((R.x >> 24) & 15u) ^ (((uint32_t)idx & 1u) << p);
+      uint32_t s_b = s_pre;
+      // other input pins: parity of their events before t and, for lower
+      // pins, a tie at t (leakage steps are taken in pin order at a tie)
 #pragma unroll
-      for (int p = 0; p < 4; ++p) n_in += p < k ? (x >> (4 * p)) & 15u : 0u;
-      n_out = (x >> (4 * k)) & 15u;
-      pk = n_in | (n_out << 9) | ((uint32_t)(n_in > 0) << 18) | ((uint32_t)(n_out > 0) << 25);
-    }
-    uint32_t inc = pk;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t v = __shfl_up_sync(0xffffffffu, inc, o);
-      if (lane >= o) inc += v;
-    }
-    const uint32_t ex = carry + inc - pk;
-    carry += __shfl_sync(0xffffffffu, inc, 31);
-    if (uu < nu) {
-      const uint32_t oi = ex & 511u, oo = (ex >> 9) & 511u, ri = (ex >> 18) & 127u, ro = ex >> 25;
-      const uint32_t cell = x >> 24;
-      const int nl = (int)((CT.info[cell] >> 8) & 0xFFu);
-      const float* lax = CT.lax + cell * kAxStride;
-      int j = 0;
-      for (int m = 1; m <= nl - 2; ++m) j += (C >= lax[m]) ? 1 : 0;
-      const float v = (C - lax[j]) * CT.ilax[cell * kAxStride + j];
-      uint32_t cum = 0, s = 0;
-#pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        s += (x >> (4 * p)) & 15u;
-        cum |= s << (8 * p);
-      }
-      const uint32_t off = oi + oo;  // staged position of the unit's first event
-      const uint32_t sa = off | (((x >> 20) & 15u) << 12) | ((uint32_t)k << 16) | ((uint32_t)j << 19) | (cell << 22);
-      X.slots[uu] = make_uint4(sa, cum, __float_as_uint(v), __float_as_uint(a.half_vdd2 * C));
-      if (n_in) space_mark(X.in_mask, X.in_pre, X.in_map, ri, oi, n_in, (uint32_t)uu);
-      if (n_out) space_mark(X.out_mask, X.out_pre, X.out_map, ro, oo, n_out, (uint32_t)uu);
-    }
-  }
-  if (lane == 0) {
-    X.in_pre[0] = 0;
-    X.out_pre[0] = 0;
-  }
-  __syncwarp();
-  const int n_in_all = (int)(carry & 511u), n_out_all = (int)((carry >> 9) & 511u);
-  const uint32_t le_mask = 0xFFFFFFFFu >> (31 - lane);  // lanes <= this one (index % 32 == lane)
-  if (n_in_all + n_out_all == n) {
-    // ---- one pass over the input index space, then the output index space:
-    // only the round that crosses from one to the other mixes the two paths
-    for (int i = lane; i < n; i += 32) {
-      if (i < n_in_all) {
-        // input event: gate state, LUT, leakage step
-        const uint32_t m = X.in_map[space_rank(X.in_mask, X.in_pre, i, le_mask)];
-        const int uu = (int)(m & 0xFFu);
-        const int li = i - (int)(m >> 8);  // inputs open the unit
-        const uint4 S = X.slots[uu];
-        const int ustart = (int)(S.x & 0xFFFu);
-        const int e = ustart + li;
-        const uint32_t cum = S.y;
-        const int p = (li >= (int)(cum & 0xFFu)) + (li >= (int)((cum >> 8) & 0xFFu)) +
-                      (li >= (int)((cum >> 16) & 0xFFu));
-        const int idx = li - pin_start(cum, p);
-        const int k = (int)((S.x >> 16) & 7u);
-        const int j = (int)((S.x >> 19) & 7u);
-        const float t = ts[e], s = __ldg(gs + e);
-        const float* ub = ts + ustart;
-        uint32_t s_pre = ((S.x >> 12) & 15u) ^ (((uint32_t)idx & 1u) << p);
-        uint32_t s_b = s_pre;
-        // other input pins: events before t (parity) and, for lower pins, a tie at t
-        for (int jj = 0; jj < k - 1; ++jj) {
-          const int qq = jj + (jj >= p ? 1 : 0);
-          const int qa = pin_start(cum, qq);
-          const int qn = pin_start(cum, qq + 1) - qa;
+      for (int q = 0; q < kMaxK; ++q) {
+        if (q < k && q != p) {
+          const int qa = pin_start(y, q);
+          const int qn = pin_start(y, q + 1) - qa;
           const float* b = ub + qa;
           const int r = seg_rank(b, qn, t);
-          const bool eq = qq < p && r < qn && b[r] == t;
+          const bool eq = q < p && r < qn && b[r] == t;
           const uint32_t par = (uint32_t)r & 1u;
-          s_pre ^= par << qq;
-          s_b ^= (par ^ (uint32_t)eq) << qq;
+          s_pre ^= par << q;
+          s_b ^= (par ^ (uint32_t)eq) << q;
         }
-        const uint32_t cell = S.x >> 22;
-        const uint32_t info = CT.info[cell];
-        const int ns = (int)(info & 0xFFu), nl = (int)((info >> 8) & 0xFFu);
-        const float* sax = CT.sax + cell * kAxStride;
-        int lis = 0;
+      }
+      const uint32_t cell = (R.x >> 18) & 63u;
+      const uint32_t info = CT.info[cell];
+      const int ns = (int)(info & 0xFFu), nl = (int)((info >> 8) & 0xFFu);
+      const float* sax = CT.sax + cell * kAxStride;
+      int lis = 0;
 #pragma unroll
-        for (int h = 4; h > 0; h >>= 1) {
-          const int cand = lis + h;
-          if (cand <= ns - 2 && s >= sax[cand]) lis = cand;
+      for (int h = 4; h > 0; h >>= 1) {
+        const int cand = lis + h;
+        if (cand <= ns - 2 && s >= sax[cand]) lis = cand;
+      }
+      const float uu2 = (s - sax[lis]) * CT.isax[cell * kAxStride + lis];
+      const int j = (int)((R.x >> 28) & 7u);
+      // corners {L[i][j], L[i][j+1], L[i+1][j], L[i+1][j+1]} of the state's table
+      const float4 P = __ldg(a.patch + CT.patch[cell] + ((int)s_pre * (ns - 1) + lis) * (nl - 1) + j);
+      const float vv = __uint_as_float(R.z);
+      const float r0 = fmaf(vv, P.y - P.x, P.x), r1 = fmaf(vv, P.w - P.z, P.z);
+      const float e_int = fmaf(uu2, r1 - r0, r0);
+      const float dp = __ldg(a.dleak + cell * kDleakStride + s_b * 4 + p);
+      event_tail<kPow2, kDebug, kExact>(A, hist, ts, gs, i, idx, true, t, s, e_int, 0.f, dp, item, c0, acc);
+      if (kDebug) {
+        const bool gl = idx > 0 && cyc<kPow2>(ts[i - 1], T, inv_T) == cyc<kPow2>(t, T, inv_T);
+        event_debug(a, A.L.ugate[g.u0 + (tag & 63u)], p, t, s_pre, (lis << 4) | j, gl, item);
+      }
+    } else {
+      // output event: switching energy
+      const int idx = i - (int)((R.x >> 9) & 511u);
+      const float s = idx > 0 ? __ldg(gs + i) : 0.f;  // only a glitch ratio uses it
+      const float e_sw = a.half_vdd2 * __uint_as_float(R.w);
+      event_tail<kPow2, kDebug, kExact>(A, hist, ts, gs, i, idx, false, t, s, 0.f, e_sw, 0.f, item, c0, acc);
+      if (kDebug) {
+        uint32_t s_pre = (R.x >> 24) & 15u;
+        const float* ub = ts + (int)(R.x & 511u);
+        for (int q = 0; q < k; ++q) {
+          const int qa = pin_start(y, q);
+          s_pre ^= ((uint32_t)seg_rank(ub + qa, pin_start(y, q + 1) - qa, t) & 1u) << q;
         }
-        const float uu2 = (s - sax[lis]) * CT.isax[cell * kAxStride + lis];
-        // corners {L[i][j], L[i][j+1], L[i+1][j], L[i+1][j+1]} of the state's table
-        const float4 P = __ldg(a.patch + CT.patch[cell] + ((int)s_pre * (ns - 1) + lis) * (nl - 1) + j);
-        const float vv = __uint_as_float(S.z);
-        const float r0 = fmaf(vv, P.y - P.x, P.x), r1 = fmaf(vv, P.w - P.z, P.z);
-        const float e_int = fmaf(uu2, r1 - r0, r0);
-        const float dp = __ldg(a.dleak + cell * kDleakStride + s_b * 4 + p);
-        const uint32_t gate = kDebug ? A.L.ugate[g.u0 + (uint32_t)uu] : 0u;
-        event_tail<kPow2, kDebug, kExact>(A, hist, ts, gs, e, idx, p, k, t, s, e_int, 0.f, dp, s_pre, lis, j, gate,
-                                          item, c0, acc);
-      } else {
-        // output event: switching energy
-        const int o = i - n_in_all;
-        const uint32_t ole = 0xFFFFFFFFu >> (31 - (o & 31));
-        const uint32_t m = X.out_map[space_rank(X.out_mask, X.out_pre, o, ole)];
-        const int uu = (int)(m & 0xFFu);
-        const int idx = o - (int)(m >> 8);
-        const uint4 S = X.slots[uu];
-        const int ustart = (int)(S.x & 0xFFFu);
-        const uint32_t cum = S.y;
-        const int k = (int)((S.x >> 16) & 7u);
-        const int e = ustart + pin_start(cum, k) + idx;
-        const float t = ts[e];
-        uint32_t s_pre = (S.x >> 12) & 15u;
-        if (kDebug) {
-          const float* ub = ts + ustart;
-          for (int qq = 0; qq < k; ++qq) {
-            const int qa = pin_start(cum, qq);
-            s_pre ^= ((uint32_t)seg_rank(ub + qa, pin_start(cum, qq + 1) - qa, t) & 1u) << qq;
-          }
-        }
-        const uint32_t gate = kDebug ? A.L.ugate[g.u0 + (uint32_t)uu] : 0u;
-        const float s = idx > 0 ? __ldg(gs + e) : 0.f;  // only a glitch ratio uses it
-        event_tail<kPow2, kDebug, kExact>(A, hist, ts, gs, e, idx, k, k, t, s, 0.f, __uint_as_float(S.w), 0.f,
-                                          s_pre, 0, 0, gate, item, c0, acc);
+        const bool gl = idx > 0 && cyc<kPow2>(ts[i - 1], T, inv_T) == cyc<kPow2>(t, T, inv_T);
+        event_debug(a, A.L.ugate[g.u0 + (tag & 63u)], k, t, s_pre, 0xFF, gl, item);
       }
     }
-  } else if (lane == 0) {  // records disagree with the item's event count
-    berr(a.err, item, kErrTileOverflow);
-  }
-  __syncwarp();
-  if (lane < kMaskWords) {  // ready for the warp's next item
-    X.in_mask[lane] = 0u;
-    X.out_mask[lane] = 0u;
   }
   __syncwarp();
 }
@@ -940,15 +967,6 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
   const uint32_t cb = L.band_cycles;
   const uint32_t n_items = L.n_items;
   uint8_t* wbuf = smem + kHist + kCellsB + (size_t)warp * kWarpB;
-  WarpScratch X;
-  X.stage = wbuf;
-  X.slots = reinterpret_cast<uint4*>(wbuf + kStageB);
-  X.in_mask = reinterpret_cast<uint32_t*>(X.slots + kItemUnits);
-  X.in_pre = X.in_mask + kMaskWords;
-  X.out_mask = X.in_pre + kMaskWords;
-  X.out_pre = X.out_mask + kMaskWords;
-  X.in_map = X.out_pre + kMaskWords;
-  X.out_map = X.in_map + kItemUnits;
   uint64_t* bar = &s_bar[warp];
 
   if (tid < 4) s_tot[tid] = 0.0;
@@ -957,7 +975,7 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
   {  // the layout is only built for libraries of at most kSmemCells cells
     uint32_t* info = cells_s;
     uint32_t* patch = info + kSmemCells;
-    float* ax = reinterpret_cast<float*>(patch + kSmemCells);  // sax, isax, lax, ilax
+    float* ax = reinterpret_cast<float*>(patch + kSmemCells);  // sax, isax
     const uint32_t nc = min(a.n_cells, (uint32_t)kSmemCells);
     for (uint32_t i = tid; i < nc * 8u; i += kBT) {
       const uint32_t ci = i >> 3, m = i & 7u;
@@ -968,19 +986,11 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
       }
       ax[0 * kSmemCells * kAxStride + ci * kAxStride + m] = cd.sax[m];
       ax[1 * kSmemCells * kAxStride + ci * kAxStride + m] = cd.isax[m];
-      ax[2 * kSmemCells * kAxStride + ci * kAxStride + m] = cd.lax[m];
-      ax[3 * kSmemCells * kAxStride + ci * kAxStride + m] = cd.ilax[m];
     }
     CT.info = info;
     CT.patch = patch;
     CT.sax = ax;
     CT.isax = ax + kSmemCells * kAxStride;
-    CT.lax = ax + 2 * kSmemCells * kAxStride;
-    CT.ilax = ax + 3 * kSmemCells * kAxStride;
-  }
-  if (lane < kMaskWords) {
-    X.in_mask[lane] = 0u;
-    X.out_mask[lane] = 0u;
   }
   if (lane == 0) {
     mbar_init(bar, 1);
@@ -1009,7 +1019,7 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
       const uint32_t old_band = s_band;
       __syncthreads();  // everyone has read s_band / s_chunk
       if (tid == 0) {
-        const uint32_t b = L.items[cur].band;
+        const uint32_t b = item_band(L.items[cur]);
         s_band = b;
         s_seg_end = band_end(L, cur, c_hi, b);
         s_next = 0;
@@ -1018,10 +1028,6 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
       const uint32_t band = s_band, seg_end = s_seg_end;
       if (band != old_band && old_band != 0xFFFFFFFFu) {
         bflush_band<kExact>(A, hist, rows, old_band);
-        if (lane < kMaskWords) {  // the flush used the warp buffers
-          X.in_mask[lane] = 0u;
-          X.out_mask[lane] = 0u;
-        }
         __syncthreads();
       }
       const uint32_t c0 = band * cb;
@@ -1041,7 +1047,7 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
         BandItem nx_a{}, nx_b{};
         ItemGeo gl{};
         if (lane == 0) {
-          gl = item_geo(my_a.e0, my_a.u0, my_b.e0, my_b.u0);
+          gl = item_geo(my_a, my_b);
           stage_item(L, gl, wbuf, bar);
           nx = cur + atomicAdd(&s_next, 1u);
           if (nx < seg_end) {
@@ -1053,12 +1059,12 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
         gcur.e0 = __shfl_sync(0xffffffffu, gl.e0, 0);
         gcur.ea = __shfl_sync(0xffffffffu, gl.ea, 0);
         gcur.u0 = __shfl_sync(0xffffffffu, gl.u0, 0);
-        gcur.ra = __shfl_sync(0xffffffffu, gl.ra, 0);
         gcur.n = __shfl_sync(0xffffffffu, gl.n, 0);
         gcur.nu = __shfl_sync(0xffffffffu, gl.nu, 0);
+        gcur.n_in = __shfl_sync(0xffffffffu, gl.n_in, 0);
         gcur.ev_off = __shfl_sync(0xffffffffu, gl.ev_off, 0);
-        gcur.rec_off = __shfl_sync(0xffffffffu, gl.rec_off, 0);
-        gcur.ev_bytes = gcur.rec_bytes = 0;
+        gcur.tag_off = __shfl_sync(0xffffffffu, gl.tag_off, 0);
+        gcur.ev_bytes = gcur.tag_bytes = 0;
         gcur.ok = __shfl_sync(0xffffffffu, (int)gl.ok, 0) != 0;
         bool ok = false;
         for (uint32_t it = 0; it < kWaitLimit && !ok; ++it) ok = mbar_try_wait(bar, phase);
@@ -1076,7 +1082,7 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
           break;
         }
         phase ^= 1u;
-        band_item<kPow2, kDebug, kExact>(A, CT, hist, X, my, gcur, c0, acc);
+        band_item<kPow2, kDebug, kExact>(A, CT, hist, wbuf, my, gcur, c0, acc);
         if (++since == kTotEvery) {
           bflush_acc(acc, s_tot);
           since = 0;

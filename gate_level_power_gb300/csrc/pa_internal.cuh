@@ -128,34 +128,50 @@ struct RunArgs {
 // for one clock period fixed when the layout is built. Every gate's timeline is
 // cut greedily, in cycle order, into windows of whole cycles: a window closes
 // at a band boundary or before a cycle that would give one of its pins more
-// than kUnitPinMax events. A unit is one non-empty (gate, window): its events
-// are stored contiguously, pin by pin, each pin in time order, and its 8-byte
-// record holds the per-pin counts, the input state at the window start, the
-// cell and the load. Units are ordered band by band, gate by gate; work items
-// are runs of whole units of one band. Windows start on cycle boundaries, so
-// the event before a unit's first event on a pin lies in an earlier cycle:
-// glitches never straddle units. Gates with more than kUnitPinMax events of one
-// pin in a single cycle ("big" gates) stay out of the layout and are streamed
-// by the unbanded kernel.
+// than kUnitPinMax events. A unit is one non-empty (gate, window). Units are
+// ordered band by band, gate by gate; work items are runs of whole units of
+// one band. Inside an item the events are stored in two regions: first the
+// input-pin events of all its units (unit by unit, each unit's pins in order,
+// each pin in time order), then the output-pin events (unit by unit, in time
+// order). Each event carries a one-byte tag (unit within the item, and the
+// input pin), each unit a 16-byte record (region offsets, pin starts, window
+// start state, cell, load-axis interval and fraction, load). Windows start on
+// cycle boundaries, so the event before a unit's first event on a pin lies in
+// an earlier cycle: glitches never straddle units. Gates with more than
+// kUnitPinMax events of one pin in a single cycle ("big" gates) stay out of
+// the layout and are streamed by the unbanded kernel.
 
-constexpr int kUnitPinMax = 15;                  // events per pin per unit (4-bit counts)
+constexpr int kUnitPinMax = 7;                   // events per pin per unit
 constexpr int kUnitMaxEvents = 5 * kUnitPinMax;  // events per unit
 constexpr uint32_t kBandDefaultCycles = 4096;
 constexpr uint32_t kBandMaxCycles = 4096;        // shared-memory histogram capacity (cycles)
 constexpr uint32_t kBandMaxBands = 1u << 20;
 constexpr int kItemEvents = 512;                 // events per item (cap): one warp's work item
-constexpr int kItemUnits = 64;                   // units per item (cap)
+constexpr int kItemUnits = 64;                   // units per item (cap): 6-bit unit tags
 // A new item starts where a unit's event offset enters a new bucket of this
 // many events (or a new band, or every kItemUnits units), so an item holds
 // fewer than kItemBucket + kUnitMaxEvents < kItemEvents events.
 constexpr uint32_t kItemBucket = kItemEvents - kUnitMaxEvents - 1;
 
-// Unit record: x = counts of pins 0..4 (4 bits each, bits 0..19) | input state
-// at the window start (bits 20..23) | cell (bits 24..31); y = load (f32 bits).
+// Item word `bw`: band (bits 0..20; items[n_items] is a sentinel with band =
+// n_bands) | input events of the item (bits 21..30).
+constexpr uint32_t kItemBandBits = 21;
+constexpr uint32_t kItemBandMask = (1u << kItemBandBits) - 1u;
+
+// Unit record (uint4), written by the finalize pass:
+//   x: input offset in the item (bits 0..8) | output offset in the item (9..17)
+//      | cell (18..23) | input state at the window start (24..27)
+//      | load-axis interval j (28..30)
+//   y: start of input pins 1, 2, 3 and the end of the inputs, one byte each
+//      (pins beyond k start at the end), | (k - 1) << 30
+//   z: load-axis fraction v (f32), w: load C (f32, fF)
+// Unit record of the walk (uint2, a build temporary): x = counts of pins 0..4
+// (4 bits each) | start state << 20 | cell << 24, y = load (f32 bits).
+// Event tag (u8): unit within the item (bits 0..5) | input pin (bits 6..7).
 struct BandItem {
   uint64_t e0;    // first event in the banded arrays
   uint32_t u0;    // first unit
-  uint32_t band;  // band of all its units; items[n_items] is a sentinel
+  uint32_t bw;    // band | input-event count << kItemBandBits
 };
 
 struct BandLayout {
@@ -166,7 +182,8 @@ struct BandLayout {
   uint32_t n_units = 0, n_items = 0, n_big = 0;
   float* bt = nullptr;        // [n_ev + pad] banded times
   float* bs = nullptr;        // [n_ev + pad] banded slews
-  uint2* urec = nullptr;      // [n_units + pad] unit records
+  uint8_t* btag = nullptr;    // [n_ev + pad] event tags
+  uint4* urec = nullptr;      // [n_units] unit records
   uint32_t* ugate = nullptr;  // [n_units] gate of each unit
   BandItem* items = nullptr;  // [n_items + 1]
   uint32_t* big = nullptr;    // [n_big] gates streamed by the unbanded kernel
@@ -194,6 +211,8 @@ struct BandBuildArgs {
   uint64_t* ipos;        // [max(G + 2, n_units + 1)] scans -- temporary
   uint64_t* scan_blk;    // scan scratch -- temporary
   uint32_t* counters;    // [4]: big gates, gates with windows narrower than a band -- temporary
+  uint2* urec2;          // [n_units] unit records of the walk -- temporary
+  const CellDesc* cells; // library (load axes for the unit records)
   BandLayout L;
   unsigned long long* err;
 };
@@ -222,7 +241,8 @@ size_t fused_smem_bytes();
 //        (ubase / ebase, totals at index n_bands * G), big gates (counters[0]);
 // write  unit records and the event scatter, item heads and their scan
 //        (ipos[n_units] = n_items), after the layout arrays are allocated;
-// items  the item list (after it is allocated).
+// items  the item list (after it is allocated), then the finalize pass:
+//        per item, the input / output regions, event tags and unit records.
 cudaError_t band_build_count(BandBuildArgs& a, cudaStream_t st);
 cudaError_t band_build_write(BandBuildArgs& a, cudaStream_t st);
 cudaError_t band_build_items(BandBuildArgs& a, cudaStream_t st);

@@ -232,22 +232,25 @@ int pa_load_events(pa_ctx *ctx, const pa_events *ev);
  * gate's timeline (cycle = floor(fl32(t / t_clk_ns))) is cut, in cycle order,
  * into windows of whole cycles inside bands of band_cycles cycles: a window
  * closes at a band boundary or before a cycle that would give one of the
- * gate's pins more than 15 events in it. The events of every (gate, window)
- * are copied into a contiguous unit, pin by pin in the per-pin CSR order,
- * units ordered band by band. Dense gates thus get narrow
+ * gate's pins more than 7 events in it. Every non-empty (gate, window) is a
+ * unit; units are ordered band by band and grouped into work items of at
+ * most 511 events, and inside an item the events are copied into an input
+ * region (the units' input-pin events, pin by pin in the per-pin CSR order)
+ * followed by an output region. Dense gates thus get narrow
  * cycle windows and sparse gates wide ones, as in the event-density-aware
  * per-gate cycle partitioning (Figs. 5, 19 and 20), fixed here at load time by
  * a per-pin event bound instead of a per-thread event target. Every pa_run whose t_clk_ns equals this
  * t_clk_ns bit for bit then uses the banded kernel, which keeps a band's cycle
  * bins in shared memory instead of adding every event to global memory; other
- * clocks use the unbanded kernel. Gates with more than 15 events of one pin in
+ * clocks use the unbanded kernel. Gates with more than 7 events of one pin in
  * a single cycle stay out of the layout and are streamed by the unbanded kernel
  * within the same run. Results agree with the unbanded path to floating-point
  * summation order.
  *   band_cycles  cycles per band: a power of two <= 4096; 0 = 4096
- * Memory: a second copy of the times and slews (8 bytes per event), 12 bytes
- * per unit and 16 bytes per work item; the build also takes temporary space of
- * about 24 bytes per (band, gate) and 24 bytes per unit.
+ * Memory: a second copy of the times and slews plus a one-byte tag (9 bytes
+ * per event), 20 bytes per unit and 16 bytes per work item; the build also
+ * takes temporary space of about 24 bytes per (band, gate) and 32 bytes per
+ * unit.
  * Errors: PA_ERR_ORDER (no events loaded), PA_ERR_ARG (t_clk_ns not > 0,
  * band_cycles not a power of two <= 4096, more than 64 cells, events spanning
  * more than 2^20 bands), PA_ERR_OOM, PA_ERR_CUDA. Loading a new library,

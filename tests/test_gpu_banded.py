@@ -127,7 +127,7 @@ def test_build_bands_errors(glp):
 
 
 def test_big_gates_banded(glp):
-    # more than 15 events of a pin in one cycle: those gates stay out of the
+    # more than 7 events of a pin in one cycle: those gates stay out of the
     # banded layout and are streamed by the unbanded kernel in the same run
     w = synth.custom(seed=23, n_gates=40, n_cells=8, k_mode=1, n_slew=6, n_load=6, n_cycles=24,
                      t_clk_ns=1.0, n_events=60000, pair_frac=0.1, quantum_ns=0.001, threads=4)
