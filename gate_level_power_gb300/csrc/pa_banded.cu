@@ -393,7 +393,7 @@ __global__ void __launch_bounds__(kFinWarps * 32) k_bw_finalize(const BandBuildA
     }
     const int n = (int)(e1 - e0), nu = (int)(u1 - u0);
     // units: sizes, the two regions' offsets, pin starts
-    uint32_t carry = 0;
+    uint32_t carry = 0, seg_max = 0;
     for (int r = 0; r < 2; ++r) {
       const int uu = lane + 32 * r;
       uint32_t pk = 0, n_in = 0, x = 0, y = 0;
@@ -403,7 +403,10 @@ __global__ void __launch_bounds__(kFinWarps * 32) k_bw_finalize(const BandBuildA
         uint32_t s = 0;
 #pragma unroll
         for (int p = 0; p < kMaxK; ++p) {
-          if ((uint32_t)p < k) s += (x >> (4 * p)) & 15u;
+          if ((uint32_t)p < k) {
+            s += (x >> (4 * p)) & 15u;
+            seg_max = max(seg_max, (x >> (4 * p)) & 15u);
+          }
           y |= s << (8 * p);
         }
         y |= (k - 1u) << 30;
@@ -476,7 +479,11 @@ __global__ void __launch_bounds__(kFinWarps * 32) k_bw_finalize(const BandBuildA
       L.bs[e0 + i] = sb[wl][i];
       L.btag[e0 + i] = gb[wl][i];
     }
-    if (lane == 0) L.items[it].bw = (L.items[it].bw & kItemBandMask) | (n_in_all << kItemBandBits);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) seg_max = max(seg_max, __shfl_xor_sync(0xffffffffu, seg_max, o));
+    const uint32_t steps = seg_max == 0 ? 0u : seg_max == 1 ? 1u : seg_max <= 3 ? 2u : 3u;
+    if (lane == 0)
+      L.items[it].bw = (L.items[it].bw & kItemBandMask) | (n_in_all << kItemBandBits) | (steps << kItemStepShift);
     __syncwarp();
   }
 }
@@ -582,22 +589,30 @@ constexpr size_t kStTagOff = (size_t)kStEv * 4;            // staged event tags
 constexpr size_t kStRecOff = kStTagOff + kItemEvents + 32; // staged unit records
 constexpr size_t kWarpB = kStRecOff + (size_t)kItemUnits * 16;
 constexpr size_t kHist = (size_t)kBandMaxCycles * 16;
-// Cell table in shared memory, structure of arrays: per cell one info word
-// (ns | nl << 8 | k << 16), the patch offset, and the two slew-axis arrays at
-// a stride of 9 words, so lanes reading different cells hit different banks.
+// Cell table in shared memory: per cell the slew axis as two float4 (points
+// 0..3 and 4..7, the halves swapped for cells with bit 2 set so that lanes
+// of different cells spread over the banks; points past ns - 2 read +inf),
+// then structure of arrays: one info word (ns | nl << 8 | k << 16), the patch
+// offset, and the slew axis and its reciprocal interval widths at a stride of
+// 9 words, so lanes reading different cells hit different banks.
 constexpr int kAxStride = 9;
-constexpr size_t kCellsB = (size_t)kSmemCells * (2 + 2 * kAxStride) * 4;
-constexpr size_t kSmemB = kHist + kCellsB + kBW * kWarpB;
+constexpr size_t kCellsB = (size_t)kSmemCells * 32 + (size_t)kSmemCells * (2 + 2 * kAxStride) * 4;
+// Item records of the CTA's current and next chunk (the next one's copy in
+// flight while the current one is worked on), one more for the end.
+constexpr uint32_t kChunkMaxItems = 1024;
+constexpr size_t kChunkRecB = (size_t)(kChunkMaxItems + 1) * sizeof(BandItem);
+constexpr size_t kSmemB = kHist + kCellsB + kBW * kWarpB + 2 * kChunkRecB;
 static_assert(kStTagOff % 16 == 0 && kStRecOff % 16 == 0 && kWarpB % 16 == 0 && kHist % 16 == 0 &&
-                  kCellsB % 16 == 0,
+                  kCellsB % 16 == 0 && kChunkRecB % 16 == 0,
               "alignment");
 static_assert(kBW * kWarpB >= kHist, "a band's rows fit the warp buffers");
 static_assert(kSmemB + 1024 <= 227 * 1024, "shared memory budget");
 constexpr int kTotEvery = 16;              // items between flushes of a warp's per-lane totals
 // Items a CTA takes from the global counter at a time: about 16 chunks per
 // CTA, within [kChunkMin, kChunkMax] (big chunks mean fewer CTA-wide syncs,
-// small ones a shorter tail).
-constexpr uint32_t kChunkMin = 64, kChunkMax = 1024;
+// small ones a shorter tail; item costs vary with the gate class, so chunks
+// that shrink over the run would leave the early, big ones unbalanced).
+constexpr uint32_t kChunkMin = 64, kChunkMax = kChunkMaxItems;
 constexpr uint32_t kWaitLimit = 1u << 16;  // bounded mbarrier waits before giving up (seconds in all)
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -694,12 +709,20 @@ __device__ void bflush_band(const BandRunArgs& A, float* hist, float4* rows, uin
 
 __device__ __forceinline__ uint32_t item_band(const BandItem& it) { return it.bw & kItemBandMask; }
 
-// First item in [lo, hi) whose band differs from `band` (items are band-sorted).
-__device__ uint32_t band_end(const BandLayout& L, uint32_t lo, uint32_t hi, uint32_t band) {
+// Thread 0 of a CTA: the next chunk [x, y) of items, y == x when none is left.
+__device__ __forceinline__ uint2 take_chunk(uint32_t* ctr, uint32_t n, uint32_t chunk) {
+  const uint32_t x = atomicAdd(ctr, chunk);
+  return x >= n ? make_uint2(n, n) : make_uint2(x, x + min(chunk, n - x));
+}
+
+// First item in [lo, hi) whose band differs from `band` (items are band-sorted;
+// it[] holds the records of the chunk from item lo on).
+__device__ uint32_t band_end(const BandItem* it, uint32_t lo, uint32_t hi, uint32_t band) {
+  const uint32_t base = lo;
   uint32_t n = hi - lo;
   while (n > 0) {
     const uint32_t half = n >> 1;
-    if ((L.items[lo + half].bw & kItemBandMask) <= band) {
+    if ((it[lo + half - base].bw & kItemBandMask) <= band) {
       lo += half + 1;
       n -= half + 1;
     } else {
@@ -715,7 +738,7 @@ __device__ uint32_t band_end(const BandLayout& L, uint32_t lo, uint32_t hi, uint
 // layout).
 struct ItemGeo {
   uint64_t e0, ea;
-  uint32_t u0, n, nu, n_in, ev_off, tag_off, ev_bytes, tag_bytes;
+  uint32_t u0, n, nu, n_in, steps, ev_off, tag_off, ev_bytes, tag_bytes;
   bool ok;
 };
 
@@ -726,7 +749,8 @@ __device__ __forceinline__ ItemGeo item_geo(const BandItem& a, const BandItem& b
   g.ea = a.e0 & ~3ull;
   g.ev_off = (uint32_t)(a.e0 - g.ea);
   g.tag_off = (uint32_t)(a.e0 & 15ull);
-  g.n_in = a.bw >> kItemBandBits;
+  g.n_in = (a.bw >> kItemBandBits) & 511u;
+  g.steps = a.bw >> kItemStepShift;
   g.ok = b.e0 > a.e0 && b.u0 > a.u0 && b.e0 - a.e0 < (uint64_t)kItemEvents && b.u0 - a.u0 <= (uint32_t)kItemUnits &&
          (uint64_t)g.n_in <= b.e0 - a.e0;
   g.n = g.ok ? (uint32_t)(b.e0 - a.e0) : 0u;
@@ -748,18 +772,28 @@ __device__ __forceinline__ void stage_item(const BandLayout& L, const ItemGeo& g
   bulk_g2s(stage, L.bt + g.ea, g.ev_bytes, bar);
   bulk_g2s(stage + kStTagOff, L.btag + (g.e0 - g.tag_off), g.tag_bytes, bar);
   bulk_g2s(stage + kStRecOff, L.urec + g.u0, g.nu * 16u, bar);
-  // the slews stay in HBM; start bringing them into L2 now
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(L.bs + g.ea), "r"(g.ev_bytes) : "memory");
 }
 
-// Events of a sorted pin segment b[0, qn) (qn <= 7) earlier than t, by
-// three steps of binary lifting.
+// Lane 0: bring an item that this warp will stage next into L2 (its times,
+// tags, unit records and slews), so that its stage copy does not wait on HBM.
+__device__ __forceinline__ void prefetch_item(const BandLayout& L, const ItemGeo& g) {
+  if (!g.ok) return;
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(L.bt + g.ea), "r"(g.ev_bytes) : "memory");
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(L.bs + g.ea), "r"(g.ev_bytes) : "memory");
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(L.btag + (g.e0 - g.tag_off)), "r"(g.tag_bytes)
+               : "memory");
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(L.urec + g.u0), "r"(g.nu * 16u) : "memory");
+}
+
+// Events of a sorted pin segment b[0, qn) earlier than t, by binary lifting
+// in `steps` steps (the same for the whole warp: enough for the item's
+// longest input-pin segment, qn < 2^steps).
 static_assert(kUnitPinMax <= 7, "three lifting steps cover a pin segment");
-__device__ __forceinline__ int seg_rank(const float* b, int qn, float t) {
+__device__ __forceinline__ int seg_rank(const float* b, int qn, float t, uint32_t steps) {
   int r = 0;
-#pragma unroll
-  for (int h = 4; h > 0; h >>= 1)
-    if (r + h <= qn && b[r + h - 1] < t) r += h;
+  if (steps >= 3 && 4 <= qn && b[3] < t) r = 4;
+  if (steps >= 2 && r + 2 <= qn && b[r + 1] < t) r += 2;
+  if (steps >= 1 && r + 1 <= qn && b[r] < t) r += 1;
   return r;
 }
 
@@ -770,60 +804,163 @@ __device__ __forceinline__ int pin_start(uint32_t y, int q) {
 }
 
 struct CellTab {
+  const float4* saxv;     // [kSmemCells * 2] swizzled slew axes, +inf past ns - 2
   const uint32_t* info;   // [kSmemCells] ns | nl << 8 | k << 16
   const uint32_t* patch;  // [kSmemCells] patch offset
   const float* sax;       // [kSmemCells * kAxStride]
   const float* isax;
 };
 
-// Everything after the gate state and energies are known: glitch scaling,
-// totals, in-cycle leakage part and the bins (and the debug outputs). e is
-// the event's staged index; the pin's previous event, if idx > 0, is e - 1.
-template <bool kPow2, bool kDebug, bool kExact>
-__device__ __forceinline__ void event_tail(const BandRunArgs& A, float* hist, const float* ts, const float* gs,
-                                           int e, int idx, bool input, float t, float s, float e_int, float e_sw,
-                                           float dp, uint32_t item, uint32_t c0, BAcc& acc) {
+// One event's result before any shared or global memory is written: its
+// cycle, the energy for the cycle's bin, the leakage step and its kind. The
+// per-event work is split in compute (loads and arithmetic only, so that the
+// compiler may interleave two events of a lane) and commit (the bins).
+struct EvOut {
+  uint32_t c;
+  float e_w, dp;
+  uint32_t flags;  // 1: input-pin event (carries a leakage step), 2: glitch
+};
+
+// Debug values of an event (only with kDebug).
+struct EvDbg {
+  uint32_t s_pre, lut_ij, unit;
+  int p;
+  float t;
+  bool glitch;
+};
+
+// Glitch test against the pin's previous event (staged index e - 1 if idx > 0;
+// for idx == 0 the event itself, unused) and scaling of the dynamic energy;
+// no branches, since on dense pins most warps hold a glitch somewhere.
+template <bool kPow2>
+__device__ __forceinline__ float glitch_scale(const RunArgs& a, const float* ts, const float* gs, int e, int idx,
+                                              float t, float s, uint32_t c, float e_dyn, bool& glitch) {
+  const int ep = e - (idx > 0 ? 1 : 0);
+  const float tp = ts[ep];
+  const float sp = __ldg(gs + ep);
+  glitch = idx > 0 && cyc<kPow2>(tp, a.t_clk, a.inv_t_clk) == c;
+  const float r = fminf(1.f, __fdividef(2000.f * (t - tp), s + sp));
+  return glitch ? r * e_dyn : e_dyn;
+}
+
+// Input-pin event at staged index i: gate state, LUT energy, leakage step,
+// glitch, totals. `valid` false: computed for a padding lane, not counted.
+template <bool kPow2, bool kDebug>
+__device__ __forceinline__ EvOut ev_input(const RunArgs& a, const CellTab& CT, const float* ts, const uint8_t* tg,
+                                          const uint4* rec, const float* gs, int i, uint32_t steps, bool valid,
+                                          BAcc& acc, EvDbg& dbg) {
+  const uint32_t tag = tg[i];
+  const uint4 R = rec[tag & 63u];
+  const float t = ts[i];
+  const float s = __ldg(gs + i);
+  const uint32_t y = R.y;
+  const int k = (int)(y >> 30) + 1;
+  const int p = (int)(tag >> 6);
+  const int in_off = (int)(R.x & 511u);
+  const int idx = i - in_off - pin_start(y, p);
+  const float* ub = ts + in_off;
+  uint32_t s_pre = ((R.x >> 24) & 15u) ^ (((uint32_t)idx & 1u) << p);
+  uint32_t s_b = s_pre;
+  // other input pins: parity of their events before t and, for lower pins, a
+  // tie at t (leakage steps are taken in pin order at a tie)
+#pragma unroll
+  for (int q = 0; q < kMaxK; ++q) {
+    if (q < k && q != p) {
+      const int qa = pin_start(y, q);
+      const int qn = pin_start(y, q + 1) - qa;
+      const float* b = ub + qa;
+      const int r = seg_rank(b, qn, t, steps);
+      const bool eq = q < p && r < qn && b[r] == t;
+      const uint32_t par = (uint32_t)r & 1u;
+      s_pre ^= par << q;
+      s_b ^= (par ^ (uint32_t)eq) << q;
+    }
+  }
+  const uint32_t cell = (R.x >> 18) & 63u;
+  const uint32_t info = CT.info[cell];
+  const int ns = (int)(info & 0xFFu), nl = (int)((info >> 8) & 0xFFu);
+  // slew interval: axis points 1 .. ns - 2 that are <= s (independent compares)
+  const uint32_t sw = (cell >> 2) & 1u;
+  const float4 A0 = CT.saxv[2 * cell + sw], A1 = CT.saxv[2 * cell + (sw ^ 1u)];
+  const int lis = (int)(s >= A0.y) + (int)(s >= A0.z) + (int)(s >= A0.w) + (int)(s >= A1.x) + (int)(s >= A1.y) +
+                  (int)(s >= A1.z);
+  const float uu2 = (s - CT.sax[cell * kAxStride + lis]) * CT.isax[cell * kAxStride + lis];
+  const int j = (int)((R.x >> 28) & 7u);
+  // corners {L[i][j], L[i][j+1], L[i+1][j], L[i+1][j+1]} of the state's table
+  const float4 P = __ldg(a.patch + CT.patch[cell] + ((int)s_pre * (ns - 1) + lis) * (nl - 1) + j);
+  const float vv = __uint_as_float(R.z);
+  const float r0 = fmaf(vv, P.y - P.x, P.x), r1 = fmaf(vv, P.w - P.z, P.z);
+  const float e_int = fmaf(uu2, r1 - r0, r0);
+  const float dp = __ldg(a.dleak + cell * kDleakStride + s_b * 4 + p);
+  const float T = a.t_clk;
+  const uint32_t c = cyc<kPow2>(t, T, a.inv_t_clk);
+  bool glitch;
+  float e_w = glitch_scale<kPow2>(a, ts, gs, i, idx, t, s, c, e_int, glitch);
+  if (valid) {
+    acc.e_gl += glitch ? e_w : 0.f;
+    acc.e_int += glitch ? 0.f : e_int;
+    acc.e_lk = fmaf(dp, a.t_max_f - t, acc.e_lk);
+  }
+  const float rem = fmaf(-(float)c, T, t);  // t - c T: the step's part inside its own cycle
+  e_w = fmaf(dp, T - rem, e_w);
+  if (kDebug) dbg = EvDbg{s_pre, (uint32_t)((lis << 4) | j), tag & 63u, p, t, glitch};
+  return EvOut{c, e_w, dp, 1u | (glitch ? 2u : 0u)};
+}
+
+// Output-pin event at staged index i: switching energy, glitch, totals.
+template <bool kPow2, bool kDebug>
+__device__ __forceinline__ EvOut ev_output(const RunArgs& a, const float* ts, const uint8_t* tg, const uint4* rec,
+                                           const float* gs, int i, uint32_t steps, bool valid, BAcc& acc,
+                                           EvDbg& dbg) {
+  const uint32_t tag = tg[i];
+  const uint4 R = rec[tag & 63u];
+  const float t = ts[i];
+  const float s = __ldg(gs + i);  // only a glitch ratio uses it
+  const int idx = i - (int)((R.x >> 9) & 511u);
+  const float e_sw = a.half_vdd2 * __uint_as_float(R.w);
+  const uint32_t c = cyc<kPow2>(t, a.t_clk, a.inv_t_clk);
+  bool glitch;
+  const float e_w = glitch_scale<kPow2>(a, ts, gs, i, idx, t, s, c, e_sw, glitch);
+  if (valid) {
+    acc.e_gl += glitch ? e_w : 0.f;
+    acc.e_sw += glitch ? 0.f : e_sw;
+  }
+  if (kDebug) {
+    const uint32_t y = R.y;
+    const int k = (int)(y >> 30) + 1;
+    uint32_t s_pre = (R.x >> 24) & 15u;
+    const float* ub = ts + (int)(R.x & 511u);
+    for (int q = 0; q < k; ++q) {
+      const int qa = pin_start(y, q);
+      s_pre ^= ((uint32_t)seg_rank(ub + qa, pin_start(y, q + 1) - qa, t, steps) & 1u) << q;
+    }
+    dbg = EvDbg{s_pre, 0xFFu, tag & 63u, k, t, glitch};
+  }
+  return EvOut{c, e_w, 0.f, glitch ? 2u : 0u};
+}
+
+// The bins of one event: the band's shared-memory bins, or (exact mode) the
+// global fp64 bins and integer counts.
+template <bool kExact>
+__device__ __forceinline__ void ev_commit(const BandRunArgs& A, float* hist, const EvOut& o, uint32_t item,
+                                          uint32_t c0) {
   const RunArgs& a = A.r;
-  const float T = a.t_clk, inv_T = a.inv_t_clk;
-  const uint32_t c = cyc<kPow2>(t, T, inv_T);
-  float tp = 0.f, sp = 0.f;
-  bool glitch = false;
-  if (idx > 0) {
-    tp = ts[e - 1];
-    glitch = cyc<kPow2>(tp, T, inv_T) == c;
-    if (glitch) sp = __ldg(gs + e - 1);
-  }
-  const float e_dyn = e_int + e_sw;
-  float e_w;
-  if (glitch) {
-    const float r = fminf(1.f, __fdividef(2000.f * (t - tp), s + sp));
-    e_w = r * e_dyn;
-    acc.e_gl += e_w;
-  } else {
-    acc.e_int += e_int;
-    acc.e_sw += e_sw;
-    e_w = e_dyn;
-  }
-  const uint32_t lc = c - c0;
+  const uint32_t lc = o.c - c0;
   if (lc >= A.L.band_cycles) {  // an event outside its band: layout inconsistency
     berr(a.err, item, kErrTileOverflow);
     return;
   }
-  if (input) {
-    const float rem = fmaf(-(float)c, T, t);  // t - c T
-    e_w = fmaf(dp, T - rem, e_w);
-    acc.e_lk = fmaf(dp, a.t_max_f - t, acc.e_lk);
-  }
+  const bool input = (o.flags & 1u) != 0u, glitch = (o.flags & 2u) != 0u;
   if (kExact) {
-    double* bin = reinterpret_cast<double*>(a.bins + c);
-    atomicAdd(bin, (double)e_w);
-    if (input) atomicAdd(bin + 1, (double)dp);
-    atomicAdd(a.cnt_ev + c, 1u);
-    if (glitch) atomicAdd(a.cnt_gl + c, 1u);
+    double* bin = reinterpret_cast<double*>(a.bins + o.c);
+    atomicAdd(bin, (double)o.e_w);
+    if (input) atomicAdd(bin + 1, (double)o.dp);
+    atomicAdd(a.cnt_ev + o.c, 1u);
+    if (glitch) atomicAdd(a.cnt_gl + o.c, 1u);
   } else {
     float* h = hist + lc;
-    atomicAdd(h + kHW, e_w);
-    if (input) atomicAdd(h + kHD, dp);
+    atomicAdd(h + kHW, o.e_w);
+    if (input) atomicAdd(h + kHD, o.dp);
     atomicAdd(reinterpret_cast<uint32_t*>(h + kHE), 1u);
     if (glitch) atomicAdd(reinterpret_cast<uint32_t*>(h + kHG), 1u);
   }
@@ -856,8 +993,8 @@ __device__ void event_debug(const RunArgs& a, uint32_t gate, int p, float t, uin
 }
 
 // One staged item on one warp: one lane per event, the input region first,
-// then the output region (only the round that crosses from one to the other
-// mixes the two paths).
+// then the output region. Where a region has events left for a second round,
+// each lane computes two events before committing either.
 template <bool kPow2, bool kDebug, bool kExact>
 __device__ __forceinline__ void band_item(const BandRunArgs& A, const CellTab& CT, float* hist,
                                           const uint8_t* stage, uint32_t item, const ItemGeo& g, uint32_t c0,
@@ -871,80 +1008,45 @@ __device__ __forceinline__ void band_item(const BandRunArgs& A, const CellTab& C
   const float* ts = reinterpret_cast<const float*>(stage) + g.ev_off;
   const uint8_t* tg = stage + kStTagOff + g.tag_off;
   const uint4* rec = reinterpret_cast<const uint4*>(stage + kStRecOff);
-  const float* gs = A.L.bs + g.e0;  // slews: read once, from HBM (prefetched into L2 at staging)
+  const float* gs = A.L.bs + g.e0;  // slews: read once, from HBM (prefetched into L2 ahead of the item)
   // and into L1: one 128-byte line per lane
   if ((uint32_t)lane * 32u < g.ev_off + g.n)
     asm volatile("prefetch.global.L1 [%0];" ::"l"(A.L.bs + g.ea + 32u * (uint32_t)lane) : "memory");
   const int n = (int)g.n, n_in = (int)g.n_in;
-  const float T = a.t_clk, inv_T = a.inv_t_clk;
-  for (int i = lane; i < n; i += 32) {
-    const uint32_t tag = tg[i];
-    const uint4 R = rec[tag & 63u];
-    const float t = ts[i];
-    const uint32_t y = R.y;
-    const int k = (int)(y >> 30) + 1;
-    if (i < n_in) {
-      // input event: gate state, LUT, leakage step
-      const int p = (int)(tag >> 6);
-      const int in_off = (int)(R.x & 511u);
-      const int idx = i - in_off - pin_start(y, p);
-      const float s = __ldg(gs + i);
-      const float* ub = ts + in_off;
-      uint32_t s_pre = ((R.x >> 24) & 15u) ^ (((uint32_t)idx & 1u) << p);
-      uint32_t s_b = s_pre;
-      // other input pins: parity of their events before t and, for lower
-      // pins, a tie at t (leakage steps are taken in pin order at a tie)
-#pragma unroll
-      for (int q = 0; q < kMaxK; ++q) {
-        if (q < k && q != p) {
-          const int qa = pin_start(y, q);
-          const int qn = pin_start(y, q + 1) - qa;
-          const float* b = ub + qa;
-          const int r = seg_rank(b, qn, t);
-          const bool eq = q < p && r < qn && b[r] == t;
-          const uint32_t par = (uint32_t)r & 1u;
-          s_pre ^= par << q;
-          s_b ^= (par ^ (uint32_t)eq) << q;
-        }
+  const uint32_t steps = g.steps;
+  EvDbg d0{}, d1{};
+  if (kDebug) {
+    for (int i = lane; i < n; i += 32) {
+      const EvOut o = i < n_in ? ev_input<kPow2, true>(a, CT, ts, tg, rec, gs, i, steps, true, acc, d0)
+                               : ev_output<kPow2, true>(a, ts, tg, rec, gs, i, steps, true, acc, d0);
+      ev_commit<kExact>(A, hist, o, item, c0);
+      event_debug(a, A.L.ugate[g.u0 + d0.unit], d0.p, d0.t, d0.s_pre, (int)d0.lut_ij, d0.glitch, item);
+    }
+  } else {
+    for (int base = 0; base < n_in; base += 64) {
+      const int i0 = base + lane;
+      if (base + 32 < n_in) {  // every lane has a first event; some a second
+        const int i1 = i0 + 32;
+        const EvOut o0 = ev_input<kPow2, false>(a, CT, ts, tg, rec, gs, i0, steps, true, acc, d0);
+        const EvOut o1 = ev_input<kPow2, false>(a, CT, ts, tg, rec, gs, min(i1, n_in - 1), steps, i1 < n_in,
+                                                acc, d1);
+        ev_commit<kExact>(A, hist, o0, item, c0);
+        if (i1 < n_in) ev_commit<kExact>(A, hist, o1, item, c0);
+      } else if (i0 < n_in) {
+        ev_commit<kExact>(A, hist, ev_input<kPow2, false>(a, CT, ts, tg, rec, gs, i0, steps, true, acc, d0), item,
+                          c0);
       }
-      const uint32_t cell = (R.x >> 18) & 63u;
-      const uint32_t info = CT.info[cell];
-      const int ns = (int)(info & 0xFFu), nl = (int)((info >> 8) & 0xFFu);
-      const float* sax = CT.sax + cell * kAxStride;
-      int lis = 0;
-#pragma unroll
-      for (int h = 4; h > 0; h >>= 1) {
-        const int cand = lis + h;
-        if (cand <= ns - 2 && s >= sax[cand]) lis = cand;
-      }
-      const float uu2 = (s - sax[lis]) * CT.isax[cell * kAxStride + lis];
-      const int j = (int)((R.x >> 28) & 7u);
-      // corners {L[i][j], L[i][j+1], L[i+1][j], L[i+1][j+1]} of the state's table
-      const float4 P = __ldg(a.patch + CT.patch[cell] + ((int)s_pre * (ns - 1) + lis) * (nl - 1) + j);
-      const float vv = __uint_as_float(R.z);
-      const float r0 = fmaf(vv, P.y - P.x, P.x), r1 = fmaf(vv, P.w - P.z, P.z);
-      const float e_int = fmaf(uu2, r1 - r0, r0);
-      const float dp = __ldg(a.dleak + cell * kDleakStride + s_b * 4 + p);
-      event_tail<kPow2, kDebug, kExact>(A, hist, ts, gs, i, idx, true, t, s, e_int, 0.f, dp, item, c0, acc);
-      if (kDebug) {
-        const bool gl = idx > 0 && cyc<kPow2>(ts[i - 1], T, inv_T) == cyc<kPow2>(t, T, inv_T);
-        event_debug(a, A.L.ugate[g.u0 + (tag & 63u)], p, t, s_pre, (lis << 4) | j, gl, item);
-      }
-    } else {
-      // output event: switching energy
-      const int idx = i - (int)((R.x >> 9) & 511u);
-      const float s = idx > 0 ? __ldg(gs + i) : 0.f;  // only a glitch ratio uses it
-      const float e_sw = a.half_vdd2 * __uint_as_float(R.w);
-      event_tail<kPow2, kDebug, kExact>(A, hist, ts, gs, i, idx, false, t, s, 0.f, e_sw, 0.f, item, c0, acc);
-      if (kDebug) {
-        uint32_t s_pre = (R.x >> 24) & 15u;
-        const float* ub = ts + (int)(R.x & 511u);
-        for (int q = 0; q < k; ++q) {
-          const int qa = pin_start(y, q);
-          s_pre ^= ((uint32_t)seg_rank(ub + qa, pin_start(y, q + 1) - qa, t) & 1u) << q;
-        }
-        const bool gl = idx > 0 && cyc<kPow2>(ts[i - 1], T, inv_T) == cyc<kPow2>(t, T, inv_T);
-        event_debug(a, A.L.ugate[g.u0 + (tag & 63u)], k, t, s_pre, 0xFF, gl, item);
+    }
+    for (int base = n_in; base < n; base += 64) {
+      const int i0 = base + lane;
+      if (base + 32 < n) {
+        const int i1 = i0 + 32;
+        const EvOut o0 = ev_output<kPow2, false>(a, ts, tg, rec, gs, i0, steps, true, acc, d0);
+        const EvOut o1 = ev_output<kPow2, false>(a, ts, tg, rec, gs, min(i1, n - 1), steps, i1 < n, acc, d1);
+        ev_commit<kExact>(A, hist, o0, item, c0);
+        if (i1 < n) ev_commit<kExact>(A, hist, o1, item, c0);
+      } else if (i0 < n) {
+        ev_commit<kExact>(A, hist, ev_output<kPow2, false>(a, ts, tg, rec, gs, i0, steps, true, acc, d0), item, c0);
       }
     }
   }
@@ -957,8 +1059,10 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
   float* hist = reinterpret_cast<float*>(smem);
   float4* rows = reinterpret_cast<float4*>(smem + kHist + kCellsB);  // the warp buffers, during a flush
   uint32_t* cells_s = reinterpret_cast<uint32_t*>(smem + kHist);
+  BandItem* s_items = reinterpret_cast<BandItem*>(smem + kHist + kCellsB + kBW * kWarpB);  // [2][kChunkMaxItems + 1]
   __shared__ __align__(8) uint64_t s_bar[kBW];
-  __shared__ uint32_t s_chunk, s_seg_end, s_band;
+  __shared__ __align__(8) uint64_t s_ibar[2];
+  __shared__ uint32_t s_chunk_lo, s_chunk_hi, s_seg_end, s_band, s_abort;
   __shared__ unsigned int s_next;
   __shared__ double s_tot[4];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -973,7 +1077,8 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
   for (uint32_t i = tid; i < 4 * kBandMaxCycles; i += kBT) hist[i] = 0.f;
   CellTab CT;
   {  // the layout is only built for libraries of at most kSmemCells cells
-    uint32_t* info = cells_s;
+    float* saxv = reinterpret_cast<float*>(cells_s);
+    uint32_t* info = cells_s + kSmemCells * 8;
     uint32_t* patch = info + kSmemCells;
     float* ax = reinterpret_cast<float*>(patch + kSmemCells);  // sax, isax
     const uint32_t nc = min(a.n_cells, (uint32_t)kSmemCells);
@@ -984,9 +1089,12 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
         info[ci] = (uint32_t)cd.ns | ((uint32_t)cd.nl << 8) | ((uint32_t)cd.k << 16);
         patch[ci] = cd.patch_off;
       }
+      const uint32_t half = (m >> 2) ^ ((ci >> 2) & 1u);
+      saxv[ci * 8 + half * 4 + (m & 3u)] = (int)m <= (int)cd.ns - 2 ? cd.sax[m] : __int_as_float(0x7f800000);
       ax[0 * kSmemCells * kAxStride + ci * kAxStride + m] = cd.sax[m];
       ax[1 * kSmemCells * kAxStride + ci * kAxStride + m] = cd.isax[m];
     }
+    CT.saxv = reinterpret_cast<const float4*>(saxv);
     CT.info = info;
     CT.patch = patch;
     CT.sax = ax;
@@ -994,6 +1102,10 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
   }
   if (lane == 0) {
     mbar_init(bar, 1);
+    if (tid == 0) {
+      mbar_init(&s_ibar[0], 1);
+      mbar_init(&s_ibar[1], 1);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
@@ -1001,27 +1113,52 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
   int since = 0;
   uint32_t phase = 0;  // parity of the stage barrier's next completion
   bool bad = false;    // a stage copy never landed: this warp stops working
-  // CTAs take chunks of A.chunk items from a global counter (the next
-  // chunk's start fetched one chunk ahead by thread 0); the band bins stay in
-  // shared memory until a chunk brings a new band.
-  uint32_t pref = 0;
+  // CTAs take chunks of A.chunk items from a global counter; thread 0 takes
+  // the next chunk one chunk ahead and copies its item records into the other
+  // half of s_items. The band bins stay in shared memory until a chunk brings
+  // a new band.
+  uint2 pref = make_uint2(0, 0);
+  uint32_t ibuf = 0, iphase = 0;  // records buffer of the current chunk, parity bits of both buffers
   if (tid == 0) {
-    s_chunk = atomicAdd(A.item_ctr, A.chunk);
-    pref = atomicAdd(A.item_ctr, A.chunk);
+    const uint2 c = take_chunk(A.item_ctr, n_items, A.chunk);
+    s_chunk_lo = c.x;
+    s_chunk_hi = c.y;
+    if (c.x < c.y) {
+      mbar_expect_arrive(&s_ibar[0], (c.y - c.x + 1) * 16u);
+      bulk_g2s(s_items, L.items + c.x, (c.y - c.x + 1) * 16u, &s_ibar[0]);
+    }
+    pref = take_chunk(A.item_ctr, n_items, A.chunk);
+    if (pref.x < pref.y) {
+      mbar_expect_arrive(&s_ibar[1], (pref.y - pref.x + 1) * 16u);
+      bulk_g2s(s_items + (kChunkMaxItems + 1), L.items + pref.x, (pref.y - pref.x + 1) * 16u, &s_ibar[1]);
+    }
     s_band = 0xFFFFFFFFu;
+    s_abort = 0;
   }
   __syncthreads();
   for (;;) {
-    const uint32_t c_lo = s_chunk;
-    if (c_lo >= n_items) break;
-    const uint32_t c_hi = min(c_lo + A.chunk, n_items);
+    const uint32_t c_lo = s_chunk_lo, c_hi = s_chunk_hi;
+    if (c_lo >= c_hi) break;
+    const BandItem* it = s_items + ibuf * (kChunkMaxItems + 1);  // records of items c_lo .. c_hi
+    if (tid == 0) {
+      bool ok = false;
+      for (uint32_t w = 0; w < kWaitLimit && !ok; ++w) ok = mbar_try_wait(&s_ibar[ibuf], (iphase >> ibuf) & 1u);
+      if (ok) {
+        iphase ^= 1u << ibuf;
+      } else {
+        berr(a.err, c_lo, kErrTileOverflow);
+        s_abort = 1;
+      }
+    }
+    __syncthreads();  // the chunk's records are in
+    if (s_abort) break;
     for (uint32_t cur = c_lo; cur < c_hi;) {
       const uint32_t old_band = s_band;
-      __syncthreads();  // everyone has read s_band / s_chunk
+      __syncthreads();  // everyone has read s_band
       if (tid == 0) {
-        const uint32_t b = item_band(L.items[cur]);
+        const uint32_t b = item_band(it[cur - c_lo]);
         s_band = b;
-        s_seg_end = band_end(L, cur, c_hi, b);
+        s_seg_end = band_end(it + (cur - c_lo), cur, c_hi, b);
         s_next = 0;
       }
       __syncthreads();
@@ -1031,29 +1168,18 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
         __syncthreads();
       }
       const uint32_t c0 = band * cb;
-      // lane 0 keeps the record of the warp's next item loaded ahead
       uint32_t my = seg_end;
-      BandItem my_a{}, my_b{};
-      if (lane == 0 && !bad) {
-        my = cur + atomicAdd(&s_next, 1u);
-        if (my < seg_end) {
-          my_a = L.items[my];
-          my_b = L.items[my + 1];
-        }
-      }
+      if (lane == 0 && !bad) my = cur + atomicAdd(&s_next, 1u);
       my = __shfl_sync(0xffffffffu, my, 0);
       while (my < seg_end) {
         uint32_t nx = seg_end;
-        BandItem nx_a{}, nx_b{};
         ItemGeo gl{};
         if (lane == 0) {
-          gl = item_geo(my_a, my_b);
+          gl = item_geo(it[my - c_lo], it[my + 1 - c_lo]);
           stage_item(L, gl, wbuf, bar);
+          // take the next item now and start bringing its data into L2
           nx = cur + atomicAdd(&s_next, 1u);
-          if (nx < seg_end) {
-            nx_a = L.items[nx];
-            nx_b = L.items[nx + 1];
-          }
+          if (nx < seg_end) prefetch_item(L, item_geo(it[nx - c_lo], it[nx + 1 - c_lo]));
         }
         ItemGeo gcur;
         gcur.e0 = __shfl_sync(0xffffffffu, gl.e0, 0);
@@ -1062,12 +1188,13 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
         gcur.n = __shfl_sync(0xffffffffu, gl.n, 0);
         gcur.nu = __shfl_sync(0xffffffffu, gl.nu, 0);
         gcur.n_in = __shfl_sync(0xffffffffu, gl.n_in, 0);
+        gcur.steps = __shfl_sync(0xffffffffu, gl.steps, 0);
         gcur.ev_off = __shfl_sync(0xffffffffu, gl.ev_off, 0);
         gcur.tag_off = __shfl_sync(0xffffffffu, gl.tag_off, 0);
         gcur.ev_bytes = gcur.tag_bytes = 0;
         gcur.ok = __shfl_sync(0xffffffffu, (int)gl.ok, 0) != 0;
         bool ok = false;
-        for (uint32_t it = 0; it < kWaitLimit && !ok; ++it) ok = mbar_try_wait(bar, phase);
+        for (uint32_t w = 0; w < kWaitLimit && !ok; ++w) ok = mbar_try_wait(bar, phase);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) {
           if (lane == 0) {
@@ -1075,7 +1202,7 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
             // keep waiting (bounded) for the copy in flight: the warp buffers
             // are reused as flush rows once the band's items are done
             bool done = false;
-            for (uint32_t it = 0; it < kWaitLimit && !done; ++it) done = mbar_try_wait(bar, phase);
+            for (uint32_t w = 0; w < kWaitLimit && !done; ++w) done = mbar_try_wait(bar, phase);
           }
           __syncwarp();
           bad = true;
@@ -1088,16 +1215,21 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
           since = 0;
         }
         my = __shfl_sync(0xffffffffu, nx, 0);
-        my_a = nx_a;
-        my_b = nx_b;
       }
       cur = seg_end;
     }
-    __syncthreads();  // the chunk's items are done
+    __syncthreads();  // the chunk's items are done and its records no longer read
     if (tid == 0) {
-      s_chunk = pref;
-      pref = atomicAdd(A.item_ctr, A.chunk);
+      s_chunk_lo = pref.x;
+      s_chunk_hi = pref.y;
+      pref = take_chunk(A.item_ctr, n_items, A.chunk);
+      if (pref.x < pref.y) {  // into the buffer just freed
+        mbar_expect_arrive(&s_ibar[ibuf], (pref.y - pref.x + 1) * 16u);
+        bulk_g2s(s_items + ibuf * (kChunkMaxItems + 1), L.items + pref.x, (pref.y - pref.x + 1) * 16u,
+                 &s_ibar[ibuf]);
+      }
     }
+    ibuf ^= 1u;
     __syncthreads();
   }
   __syncthreads();
@@ -1105,6 +1237,14 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
   bflush_acc(acc, s_tot);
   __syncthreads();
   if (tid < 4) atomicAdd(a.totals + tid, s_tot[tid]);
+  if (s_abort && tid == 0) {
+    // a records copy never landed: wait (bounded) for the copies that may
+    // still be in flight before the CTA's shared memory is released
+    for (int bsel = 0; bsel < 2; ++bsel) {
+      bool done = false;
+      for (uint32_t w = 0; w < kWaitLimit && !done; ++w) done = mbar_try_wait(&s_ibar[bsel], (iphase >> bsel) & 1u);
+    }
+  }
 }
 
 template <bool P, bool D, bool X>

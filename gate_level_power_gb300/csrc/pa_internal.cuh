@@ -154,9 +154,12 @@ constexpr int kItemUnits = 64;                   // units per item (cap): 6-bit 
 constexpr uint32_t kItemBucket = kItemEvents - kUnitMaxEvents - 1;
 
 // Item word `bw`: band (bits 0..20; items[n_items] is a sentinel with band =
-// n_bands) | input events of the item (bits 21..30).
+// n_bands) | input events of the item (bits 21..29) | binary-lifting steps
+// that cover the item's longest input-pin segment (bits 30..31: 0 for no
+// segment longer than 0, 1 for 1, 2 for up to 3, 3 for up to 7).
 constexpr uint32_t kItemBandBits = 21;
 constexpr uint32_t kItemBandMask = (1u << kItemBandBits) - 1u;
+constexpr uint32_t kItemStepShift = 30;
 
 // Unit record (uint4), written by the finalize pass:
 //   x: input offset in the item (bits 0..8) | output offset in the item (9..17)
