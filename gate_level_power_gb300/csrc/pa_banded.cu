@@ -592,7 +592,9 @@ constexpr size_t kHist = (size_t)kBandMaxCycles * 16;
 // Cell table in shared memory: per cell the slew axis as two float4 (points
 // 0..3 and 4..7, the halves swapped for cells with bit 2 set so that lanes
 // of different cells spread over the banks; points past ns - 2 read +inf),
-// then structure of arrays: one info word (ns | nl << 8 | k << 16), the patch
+// then structure of arrays: one info word (ns - 1 | (nl - 1) << 8 | patch
+// offset << 16; a library of at most 64 cells with axes of at most 8 points
+// has fewer than 2^16 corner patches), the patch
 // offset, and the slew axis and its reciprocal interval widths at a stride of
 // 9 words, so lanes reading different cells hit different banks.
 constexpr int kAxStride = 9;
@@ -805,7 +807,7 @@ __device__ __forceinline__ int pin_start(uint32_t y, int q) {
 
 struct CellTab {
   const float4* saxv;     // [kSmemCells * 2] swizzled slew axes, +inf past ns - 2
-  const uint32_t* info;   // [kSmemCells] ns | nl << 8 | k << 16
+  const uint32_t* info;   // [kSmemCells] ns - 1 | (nl - 1) << 8 | patch offset << 16
   const uint32_t* patch;  // [kSmemCells] patch offset
   const float* sax;       // [kSmemCells * kAxStride]
   const float* isax;
@@ -857,28 +859,30 @@ __device__ __forceinline__ EvOut ev_input(const RunArgs& a, const CellTab& CT, c
   const int k = (int)(y >> 30) + 1;
   const int p = (int)(tag >> 6);
   const int in_off = (int)(R.x & 511u);
-  const int idx = i - in_off - pin_start(y, p);
+  const int idx = i - in_off - (int)(__byte_perm(y << 8, 0u, (uint32_t)p) & 63u);  // p < 4
   const float* ub = ts + in_off;
   uint32_t s_pre = ((R.x >> 24) & 15u) ^ (((uint32_t)idx & 1u) << p);
   uint32_t s_b = s_pre;
   // other input pins: parity of their events before t and, for lower pins, a
   // tie at t (leakage steps are taken in pin order at a tie)
-#pragma unroll
-  for (int q = 0; q < kMaxK; ++q) {
-    if (q < k && q != p) {
-      const int qa = pin_start(y, q);
-      const int qn = pin_start(y, q + 1) - qa;
-      const float* b = ub + qa;
-      const int r = seg_rank(b, qn, t, steps);
-      const bool eq = q < p && r < qn && b[r] == t;
-      const uint32_t par = (uint32_t)r & 1u;
-      s_pre ^= par << q;
-      s_b ^= (par ^ (uint32_t)eq) << q;
-    }
+  // (exactly k - 1 iterations per lane: with k the same across most of a
+  // warp's units, no lane idles)
+  for (int jj = 0; jj < k - 1; ++jj) {
+    const int q = jj + (jj >= p ? 1 : 0);
+    // byte 0: start of pin q (from y << 8, whose byte 0 is 0), byte 1: start
+    // of pin q + 1 (byte q of y)
+    const uint32_t se = __byte_perm(y << 8, y, (uint32_t)q | ((uint32_t)(q + 4) << 4));
+    const int qa = (int)(se & 63u);
+    const int qn = (int)((se >> 8) & 63u) - qa;
+    const float* b = ub + qa;
+    const int r = seg_rank(b, qn, t, steps);
+    const bool eq = q < p && r < qn && b[r] == t;
+    const uint32_t par = (uint32_t)r & 1u;
+    s_pre ^= par << q;
+    s_b ^= (par ^ (uint32_t)eq) << q;
   }
   const uint32_t cell = (R.x >> 18) & 63u;
-  const uint32_t info = CT.info[cell];
-  const int ns = (int)(info & 0xFFu), nl = (int)((info >> 8) & 0xFFu);
+  const uint32_t info = CT.info[cell];  // ns - 1 | (nl - 1) << 8 | patch offset << 16
   // slew interval: axis points 1 .. ns - 2 that are <= s (independent compares)
   const uint32_t sw = (cell >> 2) & 1u;
   const float4 A0 = CT.saxv[2 * cell + sw], A1 = CT.saxv[2 * cell + (sw ^ 1u)];
@@ -887,7 +891,8 @@ __device__ __forceinline__ EvOut ev_input(const RunArgs& a, const CellTab& CT, c
   const float uu2 = (s - CT.sax[cell * kAxStride + lis]) * CT.isax[cell * kAxStride + lis];
   const int j = (int)((R.x >> 28) & 7u);
   // corners {L[i][j], L[i][j+1], L[i+1][j], L[i+1][j+1]} of the state's table
-  const float4 P = __ldg(a.patch + CT.patch[cell] + ((int)s_pre * (ns - 1) + lis) * (nl - 1) + j);
+  const float4 P =
+      __ldg(a.patch + (info >> 16) + ((int)s_pre * (int)(info & 0xFFu) + lis) * (int)((info >> 8) & 0xFFu) + j);
   const float vv = __uint_as_float(R.z);
   const float r0 = fmaf(vv, P.y - P.x, P.x), r1 = fmaf(vv, P.w - P.z, P.z);
   const float e_int = fmaf(uu2, r1 - r0, r0);
@@ -1086,7 +1091,7 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
       const uint32_t ci = i >> 3, m = i & 7u;
       const CellDesc& cd = a.cells[ci];
       if (m == 0) {
-        info[ci] = (uint32_t)cd.ns | ((uint32_t)cd.nl << 8) | ((uint32_t)cd.k << 16);
+        info[ci] = (uint32_t)(cd.ns - 1) | ((uint32_t)(cd.nl - 1) << 8) | (cd.patch_off << 16);
         patch[ci] = cd.patch_off;
       }
       const uint32_t half = (m >> 2) ^ ((ci >> 2) & 1u);
