@@ -380,6 +380,7 @@ __global__ void __launch_bounds__(kFinWarps * 32) k_bw_finalize(const BandBuildA
   __shared__ uint32_t ust[kFinWarps][kItemUnits];  // unit starts in the walk's order, item-relative
   __shared__ uint32_t udst[kFinWarps][kItemUnits]; // input offset | output offset (in the region) << 9 | inputs << 18
   __shared__ uint32_t upin[kFinWarps][kItemUnits]; // record word y
+  __shared__ uint32_t utie[kFinWarps][kItemUnits / 32];  // units with events at one time on two input pins
   const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
   const uint64_t warp = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const uint64_t n_warps = ((uint64_t)gridDim.x * blockDim.x) >> 5;
@@ -434,22 +435,6 @@ __global__ void __launch_bounds__(kFinWarps * 32) k_bw_finalize(const BandBuildA
       if (lane == 0) atomicMin(a.err, (unsigned long long)((it << 8) | kErrTileOverflow));
       continue;
     }
-    for (int r = 0; r < 2; ++r) {
-      const int uu = lane + 32 * r;
-      if (uu < nu) {
-        const uint2 w = a.urec2[u0 + uu];
-        const uint32_t cell = w.x >> 24;
-        const CellDesc& cd = a.cells[cell];
-        const float C = __uint_as_float(w.y);
-        int j = 0;
-        for (int m = 1; m <= (int)cd.nl - 2; ++m) j += (C >= cd.lax[m]) ? 1 : 0;
-        const float v = (C - cd.lax[j]) * cd.ilax[j];
-        const uint32_t d = udst[wl][uu];
-        const uint32_t x = (d & 511u) | ((n_in_all + ((d >> 9) & 511u)) << 9) | (cell << 18) |
-                           (((w.x >> 20) & 15u) << 24) | ((uint32_t)j << 28);
-        L.urec[u0 + uu] = make_uint4(x, upin[wl][uu], __float_as_uint(v), w.y);
-      }
-    }
     // events: each to its place in the two regions
     for (int i = lane; i < n; i += 32) {
       int u = 0;
@@ -473,7 +458,36 @@ __global__ void __launch_bounds__(kFinWarps * 32) k_bw_finalize(const BandBuildA
       sb[wl][dst] = L.bs[e0 + i];
       gb[wl][dst] = (uint8_t)tag;
     }
+    if (lane < kItemUnits / 32) utie[wl][lane] = 0u;
     __syncwarp();
+    // ties: an input event whose time another input pin of its unit also has
+    for (int i = lane; i < (int)n_in_all; i += 32) {
+      const uint32_t tag = gb[wl][i], u = tag & 63u;
+      const uint32_t d = udst[wl][u];
+      const int lo = (int)(d & 511u), hi = lo + (int)(d >> 18);
+      const float t = tb[wl][i];
+      bool tie = false;
+      for (int m = lo; m < hi; ++m) tie |= (gb[wl][m] >> 6) != (tag >> 6) && tb[wl][m] == t;
+      if (tie) atomicOr(&utie[wl][u >> 5], 1u << (u & 31u));
+    }
+    __syncwarp();
+    for (int r = 0; r < 2; ++r) {
+      const int uu = lane + 32 * r;
+      if (uu < nu) {
+        const uint2 w = a.urec2[u0 + uu];
+        const uint32_t cell = w.x >> 24;
+        const CellDesc& cd = a.cells[cell];
+        const float C = __uint_as_float(w.y);
+        int j = 0;
+        for (int m = 1; m <= (int)cd.nl - 2; ++m) j += (C >= cd.lax[m]) ? 1 : 0;
+        const float v = (C - cd.lax[j]) * cd.ilax[j];
+        const uint32_t d = udst[wl][uu];
+        const uint32_t x = (d & 511u) | ((n_in_all + ((d >> 9) & 511u)) << 9) | (cell << 18) |
+                           (((w.x >> 20) & 15u) << 24) | ((uint32_t)j << 28) |
+                           (((utie[wl][uu >> 5] >> (uu & 31)) & 1u) << 31);
+        L.urec[u0 + uu] = make_uint4(x, upin[wl][uu], __float_as_uint(v), w.y);
+      }
+    }
     for (int i = lane; i < n; i += 32) {
       L.bt[e0 + i] = tb[wl][i];
       L.bs[e0 + i] = sb[wl][i];
@@ -592,13 +606,11 @@ constexpr size_t kHist = (size_t)kBandMaxCycles * 16;
 // Cell table in shared memory: per cell the slew axis as two float4 (points
 // 0..3 and 4..7, the halves swapped for cells with bit 2 set so that lanes
 // of different cells spread over the banks; points past ns - 2 read +inf),
-// then structure of arrays: one info word (ns - 1 | (nl - 1) << 8 | patch
-// offset << 16; a library of at most 64 cells with axes of at most 8 points
-// has fewer than 2^16 corner patches), the patch
-// offset, and the slew axis and its reciprocal interval widths at a stride of
-// 9 words, so lanes reading different cells hit different banks.
-constexpr int kAxStride = 9;
-constexpr size_t kCellsB = (size_t)kSmemCells * 32 + (size_t)kSmemCells * (2 + 2 * kAxStride) * 4;
+// then one info word per cell (ns - 1 | (nl - 1) << 8 | patch offset << 16;
+// a library of at most 64 cells with axes of at most 8 points has fewer than
+// 2^16 corner patches), then per cell and slew interval i the pair
+// {axis point i, 1 / interval width} (one 8-byte load per event).
+constexpr size_t kCellsB = (size_t)kSmemCells * 32 + (size_t)kSmemCells * 4 + (size_t)kSmemCells * 8 * 8;
 // Item records of the CTA's current and next chunk (the next one's copy in
 // flight while the current one is worked on), one more for the end.
 constexpr uint32_t kChunkMaxItems = 1024;
@@ -808,9 +820,7 @@ __device__ __forceinline__ int pin_start(uint32_t y, int q) {
 struct CellTab {
   const float4* saxv;     // [kSmemCells * 2] swizzled slew axes, +inf past ns - 2
   const uint32_t* info;   // [kSmemCells] ns - 1 | (nl - 1) << 8 | patch offset << 16
-  const uint32_t* patch;  // [kSmemCells] patch offset
-  const float* sax;       // [kSmemCells * kAxStride]
-  const float* isax;
+  const float2* sxp;      // [kSmemCells * 8] {slew axis point i, 1 / (ax[i + 1] - ax[i])}
 };
 
 // One event's result before any shared or global memory is written: its
@@ -863,6 +873,7 @@ __device__ __forceinline__ EvOut ev_input(const RunArgs& a, const CellTab& CT, c
   const float* ub = ts + in_off;
   uint32_t s_pre = ((R.x >> 24) & 15u) ^ (((uint32_t)idx & 1u) << p);
   uint32_t s_b = s_pre;
+  const bool ties = (R.x >> 31) != 0u;  // the unit has events at one time on two input pins
   // other input pins: parity of their events before t and, for lower pins, a
   // tie at t (leakage steps are taken in pin order at a tie)
   // (exactly k - 1 iterations per lane: with k the same across most of a
@@ -876,7 +887,8 @@ __device__ __forceinline__ EvOut ev_input(const RunArgs& a, const CellTab& CT, c
     const int qn = (int)((se >> 8) & 63u) - qa;
     const float* b = ub + qa;
     const int r = seg_rank(b, qn, t, steps);
-    const bool eq = q < p && r < qn && b[r] == t;
+    bool eq = false;
+    if (ties) eq = q < p && r < qn && b[r] == t;
     const uint32_t par = (uint32_t)r & 1u;
     s_pre ^= par << q;
     s_b ^= (par ^ (uint32_t)eq) << q;
@@ -888,7 +900,8 @@ __device__ __forceinline__ EvOut ev_input(const RunArgs& a, const CellTab& CT, c
   const float4 A0 = CT.saxv[2 * cell + sw], A1 = CT.saxv[2 * cell + (sw ^ 1u)];
   const int lis = (int)(s >= A0.y) + (int)(s >= A0.z) + (int)(s >= A0.w) + (int)(s >= A1.x) + (int)(s >= A1.y) +
                   (int)(s >= A1.z);
-  const float uu2 = (s - CT.sax[cell * kAxStride + lis]) * CT.isax[cell * kAxStride + lis];
+  const float2 ax = CT.sxp[cell * 8 + lis];
+  const float uu2 = (s - ax.x) * ax.y;
   const int j = (int)((R.x >> 28) & 7u);
   // corners {L[i][j], L[i][j+1], L[i+1][j], L[i+1][j+1]} of the state's table
   const float4 P =
@@ -1084,26 +1097,19 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
   {  // the layout is only built for libraries of at most kSmemCells cells
     float* saxv = reinterpret_cast<float*>(cells_s);
     uint32_t* info = cells_s + kSmemCells * 8;
-    uint32_t* patch = info + kSmemCells;
-    float* ax = reinterpret_cast<float*>(patch + kSmemCells);  // sax, isax
+    float2* sxp = reinterpret_cast<float2*>(info + kSmemCells);
     const uint32_t nc = min(a.n_cells, (uint32_t)kSmemCells);
     for (uint32_t i = tid; i < nc * 8u; i += kBT) {
       const uint32_t ci = i >> 3, m = i & 7u;
       const CellDesc& cd = a.cells[ci];
-      if (m == 0) {
-        info[ci] = (uint32_t)(cd.ns - 1) | ((uint32_t)(cd.nl - 1) << 8) | (cd.patch_off << 16);
-        patch[ci] = cd.patch_off;
-      }
+      if (m == 0) info[ci] = (uint32_t)(cd.ns - 1) | ((uint32_t)(cd.nl - 1) << 8) | (cd.patch_off << 16);
       const uint32_t half = (m >> 2) ^ ((ci >> 2) & 1u);
       saxv[ci * 8 + half * 4 + (m & 3u)] = (int)m <= (int)cd.ns - 2 ? cd.sax[m] : __int_as_float(0x7f800000);
-      ax[0 * kSmemCells * kAxStride + ci * kAxStride + m] = cd.sax[m];
-      ax[1 * kSmemCells * kAxStride + ci * kAxStride + m] = cd.isax[m];
+      sxp[ci * 8 + m] = make_float2(cd.sax[m], cd.isax[m]);
     }
     CT.saxv = reinterpret_cast<const float4*>(saxv);
     CT.info = info;
-    CT.patch = patch;
-    CT.sax = ax;
-    CT.isax = ax + kSmemCells * kAxStride;
+    CT.sxp = sxp;
   }
   if (lane == 0) {
     mbar_init(bar, 1);
