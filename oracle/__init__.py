@@ -52,7 +52,7 @@ class OrOut(ctypes.Structure):
                 ("e_leak", ctypes.c_double), ("p_int", ctypes.c_double), ("p_sw", ctypes.c_double),
                 ("p_gl", ctypes.c_double), ("p_leak", ctypes.c_double), ("t_max", ctypes.c_double),
                 ("wave_energy", _vp), ("waveform", _vp), ("evcount", _vp), ("glcount", _vp),
-                ("state_pre", _vp), ("lut_ij", _vp), ("is_glitch", _vp)]
+                ("state_pre", _vp), ("lut_ij", _vp), ("is_glitch", _vp), ("gate_power", _vp)]
 
 
 def build(force: bool = False) -> str:
@@ -90,14 +90,15 @@ def _c(a, dtype):
 
 
 def run(w, *, vdd=None, t_clk=None, n_cycles=None, t_max=0.0, wave="full", sample_cycles=None,
-        gate_range=None, threads=1, debug=False, use_value=True):
+        gate_range=None, threads=1, debug=False, use_value=True, gate_power=False):
     """Run the oracle on workload-like object ``w`` (attributes as in ``synth.Workload``).
 
     Returns a dict: ``p_int, p_sw, p_gl, p_leak`` (W), ``e_*`` (fJ), ``t_max``
     (ns), and, as requested, ``waveform`` (W per cycle, or per sampled cycle),
     ``wave_energy`` (fJ), ``evcount``/``glcount`` (u64 per cycle), and per-event
     debug arrays ``state_pre``, ``lut_ij``, ``is_glitch`` (filled only for the
-    gates walked).
+    gates walked), and with ``gate_power`` the per-gate power ``gate_power``
+    (W, [gates walked, 4]: internal, switching, glitch, leakage).
     """
     L = _load()
     vdd = w.vdd if vdd is None else vdd
@@ -144,6 +145,9 @@ def run(w, *, vdd=None, t_clk=None, n_cycles=None, t_max=0.0, wave="full", sampl
         for name in ("state_pre", "lut_ij", "is_glitch"):
             res[name] = np.full(E, 0xEE, np.uint8)
             setattr(out, name, _p(res[name]))
+    if gate_power:
+        res["gate_power"] = np.zeros((g1 - g0, 4), np.float64)
+        out.gate_power = _p(res["gate_power"])
     rc = L.or_run(ctypes.byref(lib), ctypes.byref(net), ctypes.byref(ev), ctypes.byref(par), ctypes.byref(out))
     if rc != 0:
         raise RuntimeError(f"oracle failed (rc={rc})")

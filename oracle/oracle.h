@@ -61,6 +61,7 @@ typedef struct or_out {
   uint8_t *state_pre;               /* [E] input state before the event's timestamp */
   uint8_t *lut_ij;                  /* [E] (i << 4) | j for input events, 0xFF for output */
   uint8_t *is_glitch;               /* [E] */
+  double *gate_power;               /* [(gate_end - gate_begin) * 4] W per gate: int, sw, gl, leak; or NULL */
 } or_out;
 
 int or_run(const or_lib *lib, const or_net *net, const or_ev *ev, const or_par *par, or_out *out);

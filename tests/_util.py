@@ -81,8 +81,10 @@ def brute_force(w, vdd=None, t_clk=None, n_cycles=None, t_max=0.0):
     out = dict(e_int=0.0, e_sw=0.0, e_gl=0.0, e_leak=0.0,
                wave_energy=np.zeros(n_cyc), evcount=np.zeros(n_cyc, np.int64),
                glcount=np.zeros(n_cyc, np.int64), state_pre=np.zeros(E, np.int64),
-               lut_ij=np.zeros(E, np.int64), is_glitch=np.zeros(E, np.int64))
+               lut_ij=np.zeros(E, np.int64), is_glitch=np.zeros(E, np.int64),
+               gate_energy=np.zeros((len(w.cell_id), 4)))
     for g in range(len(w.cell_id)):
+        tot0 = [out["e_int"], out["e_sw"], out["e_gl"], out["e_leak"]]
         cell = int(w.cell_id[g]); k = int(w.n_inputs[cell])
         ns, nl = int(w.n_slew[cell]), int(w.n_load[cell])
         sax = [float(x) for x in w.slew_axis[cell][:ns]]; lax = [float(x) for x in w.load_axis[cell][:nl]]
@@ -149,6 +151,10 @@ def brute_force(w, vdd=None, t_clk=None, n_cycles=None, t_max=0.0):
             c = int(math.floor(0.5 * (a + b) / T))
             if c < n_cyc:
                 out["wave_energy"][c] += e
+        # this gate's share of each total
+        for m, name in enumerate(("e_int", "e_sw", "e_gl", "e_leak")):
+            out["gate_energy"][g, m] = out[name] - tot0[m]
+    out["gate_power"] = out["gate_energy"] / tm * 1e-6
     for name in ("int", "sw", "gl", "leak"):
         out["p_" + name] = out["e_" + name] / tm * 1e-6
     out["waveform"] = out["wave_energy"] / T * 1e-6

@@ -213,6 +213,38 @@ def test_oracle_matches_brute_force(seed, quantum, k_mode, t_clk):
         np.testing.assert_array_equal(r[key].astype(np.int64), b[key], err_msg=key)
 
 
+@pytest.mark.parametrize("seed,quantum,k_mode", [(1, 0.0, 1), (3, 0.125, 2), (6, 0.0, 0)])
+def test_per_gate_power_matches_brute_force(seed, quantum, k_mode):
+    # per-gate power: each gate's own energies over t_max, against the brute
+    # force's per-gate tally (a different formulation of the same quantities)
+    w = _tiny_random(seed, quantum, k_mode=k_mode)
+    r = oracle.run(w, gate_power=True)
+    b = brute_force(w)
+    scale = float(np.abs(b["gate_power"]).max())
+    np.testing.assert_allclose(r["gate_power"], b["gate_power"], rtol=1e-10, atol=1e-12 * scale)
+    assert (b["gate_power"][:, 0] > 0).sum() > 1 and (b["gate_power"][:, 2] > 0).any()
+
+
+@pytest.mark.parametrize("cfg", [1, 2])
+def test_per_gate_power_sums_to_totals(cfg):
+    w = synth.generate(cfg)
+    r = oracle.run(w, gate_power=True, threads=4)
+    for m, key in enumerate(("p_int", "p_sw", "p_gl", "p_leak")):
+        assert float(r["gate_power"][:, m].sum()) == pytest.approx(r[key], rel=1e-12), key
+    # a gate range walks only its gates, with the same per-gate values
+    G = len(w.cell_id)
+    part = oracle.run(w, gate_power=True, gate_range=(G // 3, G // 2))
+    np.testing.assert_array_equal(part["gate_power"], r["gate_power"][G // 3:G // 2])
+
+
+def test_per_gate_power_lone_gate_is_the_totals():
+    w, d = golden("w1_inverter_glitch.json")
+    r = oracle.run(w, gate_power=True)
+    assert r["gate_power"].shape == (1, 4)
+    for m, key in enumerate(("p_int", "p_sw", "p_gl", "p_leak")):
+        assert r["gate_power"][0, m] == pytest.approx(d["expected"][key], rel=1e-12), key
+
+
 def test_brute_force_ties_are_exercised():
     # the quantised workloads above must contain cross-pin ties, else the tie rule is unpinned
     w = _tiny_random(3, 0.125, k_mode=2)
