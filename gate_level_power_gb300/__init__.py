@@ -59,7 +59,7 @@ class PaResult(ctypes.Structure):
                 ("lut_ij", _vp), ("is_glitch", _vp), ("ms_partition", ctypes.c_float),
                 ("ms_fused", ctypes.c_float), ("ms_reduce", ctypes.c_float), ("ms_total", ctypes.c_float),
                 ("n_tiles", ctypes.c_uint32), ("n_heavy", ctypes.c_uint32), ("kernel_launches", ctypes.c_uint32),
-                ("path", ctypes.c_uint32)]
+                ("path", ctypes.c_uint32), ("gate_power_w", _vp)]
 
 
 class PaError(RuntimeError):
@@ -191,6 +191,7 @@ class PowerAnalyzer:
         self.ctx = pa_create(device, stream)
         self.n_cycles = None
         self.n_events = 0
+        self.n_gates = 0
 
     def close(self):
         if self.ctx:
@@ -221,6 +222,7 @@ class PowerAnalyzer:
         keep = [_host(cell_id, np.uint32), _host(load_ff, np.float32), _host(init_in, np.uint8),
                 _host(init_out, np.uint8)]
         pa_load_netlist(self.ctx, PaNetlist(len(keep[0]), *(k.ctypes.data for k in keep)))
+        self.n_gates = len(keep[0])
 
     def load_events(self, pin_off, t_ns, slew_ps, value=None):
         dev = hasattr(t_ns, "is_cuda") and t_ns.is_cuda
@@ -252,11 +254,13 @@ class PowerAnalyzer:
         self.load_events(w.pin_off, w.t_ns, w.slew_ps, w.value if with_value else None)
 
     def run(self, vdd, t_clk_ns, n_cycles, t_max_ns=0.0, tile_events=0, heavy_events=0, timing=False,
-            waveform=True, counts=True, debug=False, out=None):
+            waveform=True, counts=True, debug=False, gate_power=False, out=None):
         """Run the power computation. Returns a dict with ``p_int, p_sw, p_gl,
         p_leak`` (W), ``t_max`` and, as requested, ``waveform`` (f32 W per
         cycle), ``event_count``/``glitch_count`` (u32 per cycle), per-event
-        ``state_pre``/``lut_ij``/``is_glitch`` (u8), and ``ms_*`` timings.
+        ``state_pre``/``lut_ij``/``is_glitch`` (u8), per-gate ``gate_power``
+        (f64 W, [gates, 4]: internal, switching, glitch, leakage), and ``ms_*``
+        timings.
         ``out`` may hold preallocated arrays (numpy or CUDA tensors) under the
         same names; CUDA tensors select device output."""
         p = PaRunParams(float(vdd), float(t_clk_ns), int(n_cycles), float(t_max_ns), int(tile_events),
@@ -282,7 +286,10 @@ class PowerAnalyzer:
         r.state_pre = arr("state_pre", self.n_events, np.uint8, debug)
         r.lut_ij = arr("lut_ij", self.n_events, np.uint8, debug)
         r.is_glitch = arr("is_glitch", self.n_events, np.uint8, debug)
+        r.gate_power_w = arr("gate_power", self.n_gates * 4, np.float64, gate_power)
         pa_run(self.ctx, p, r)
+        if "gate_power" in res and not (hasattr(res["gate_power"], "is_cuda") and res["gate_power"].is_cuda):
+            res["gate_power"] = np.asarray(res["gate_power"]).reshape(-1, 4)
         res.update(p_int=r.p_int_w, p_sw=r.p_sw_w, p_gl=r.p_gl_w, p_leak=r.p_leak_w, t_max=r.t_max_ns,
                    n_tiles=r.n_tiles, n_heavy=r.n_heavy, kernel_launches=r.kernel_launches, path=r.path)
         if timing:

@@ -56,7 +56,7 @@ struct pa_ctx {
   // scratch
   DevBuf value_tmp, err_word, tmax_bits;
   DevBuf bins, part_blk, part_counts, tiles, heavy, p0_tot, p_out;
-  DevBuf dbg[3], wave_tmp, cnt_tmp, chunk_sums;
+  DevBuf dbg[3], wave_tmp, cnt_tmp, chunk_sums, gate_tmp;
 
   // banded layout (pa_build_bands): persistent parts, build temporaries, run scratch
   BandLayout band;
@@ -175,7 +175,7 @@ struct RunPlan {
   float T = 0.f;
   double Td = 0.0, t_max = 0.0;
   uint32_t tile = 0, heavy = 0, N = 0, G = 0, nblk = 0;
-  bool pow2 = false, debug = false, timing = false;
+  bool pow2 = false, debug = false, timing = false, gate = false;
   double vdd = 0.0;
 };
 
@@ -193,6 +193,7 @@ struct PassBufs {
   uint32_t* cnt_ev = nullptr;
   uint32_t* cnt_gl = nullptr;
   uint8_t* dbg[3] = {nullptr, nullptr, nullptr};
+  double* gate_e = nullptr;  // per-gate accumulators (fJ), converted to W in place
 };
 
 int check_run(pa_ctx* c, const pa_run_params* prm, const pa_result* out, const char* who, RunPlan* plan) {
@@ -223,7 +224,8 @@ int check_run(pa_ctx* c, const pa_run_params* prm, const pa_result* out, const c
   plan->N = prm->n_cycles;
   plan->G = c->n_gates;
   plan->nblk = partition_blocks(plan->G);
-  plan->debug = out->state_pre || out->lut_ij || out->is_glitch;
+  plan->gate = out->gate_power_w != nullptr;
+  plan->debug = out->state_pre || out->lut_ij || out->is_glitch || plan->gate;
   plan->timing = (prm->flags & PA_RUN_TIMING) != 0;
   plan->pow2 = is_pow2(plan->T);
   plan->vdd = prm->vdd;
@@ -273,6 +275,7 @@ int run_pass(pa_ctx* c, const RunPlan& plan, const PassBufs& B, pa_result* out, 
   a.dbg_state = B.dbg[0];
   a.dbg_lut = B.dbg[1];
   a.dbg_glitch = B.dbg[2];
+  a.gate_e = B.gate_e;
   BandRunArgs A;
   if (band) {
     A.r = a;
@@ -292,6 +295,7 @@ int run_pass(pa_ctx* c, const RunPlan& plan, const PassBufs& B, pa_result* out, 
     if (exact) CUDA_TRY(c, cudaMemsetAsync(B.cnt_gl, 0, (size_t)N * sizeof(uint32_t), st));
     CUDA_TRY(c, cudaMemsetAsync(B.p0_tot, 0, 8 * sizeof(double), st));
     CUDA_TRY(c, cudaMemsetAsync(c->err_word.p, 0xff, sizeof(unsigned long long), st));
+    if (B.gate_e) CUDA_TRY(c, cudaMemsetAsync(B.gate_e, 0, (size_t)plan.G * 4 * sizeof(double), st));
     if (band) {
       // the unbanded kernel's work list: no tiles, the big gates as heavy gates
       const uint32_t part[4] = {0, band->n_big, 0, 0};
@@ -316,6 +320,10 @@ int run_pass(pa_ctx* c, const RunPlan& plan, const PassBufs& B, pa_result* out, 
     if (plan.timing) CUDA_TRY(c, cudaEventRecord(c->ev[2], st));
     CUDA_TRY(c, launch_final_reduce(a, plan.Td, plan.t_max, B.wave, B.p_out, exact != 0, st));
     launches += 2;
+    if (B.gate_e && plan.G) {
+      CUDA_TRY(c, launch_gate_power(a, plan.t_max, st));
+      launches += 1;
+    }
     if (plan.timing) CUDA_TRY(c, cudaEventRecord(c->ev[3], st));
     CUDA_TRY(c, cudaMemcpyAsync(p, B.p_out, sizeof(p), cudaMemcpyDeviceToHost, st));
     CUDA_TRY(c, cudaMemcpyAsync(&key, c->err_word.p, sizeof(key), cudaMemcpyDeviceToHost, st));
@@ -328,6 +336,8 @@ int run_pass(pa_ctx* c, const RunPlan& plan, const PassBufs& B, pa_result* out, 
   if (out->waveform_w) CUDA_TRY(c, cudaMemcpyAsync(out->waveform_w, B.wave, (size_t)N * sizeof(float), dk, st));
   if (out->event_count) CUDA_TRY(c, cudaMemcpyAsync(out->event_count, B.cnt_ev, (size_t)N * 4, dk, st));
   if (out->glitch_count) CUDA_TRY(c, cudaMemcpyAsync(out->glitch_count, B.cnt_gl, (size_t)N * 4, dk, st));
+  if (out->gate_power_w && out->gate_power_w != B.gate_e && plan.G)
+    CUDA_TRY(c, cudaMemcpyAsync(out->gate_power_w, B.gate_e, (size_t)plan.G * 4 * sizeof(double), dk, st));
   if (plan.debug && c->n_events) {
     uint8_t* dst[3] = {out->state_pre, out->lut_ij, out->is_glitch};
     for (int i = 0; i < 3; ++i)
@@ -422,7 +432,7 @@ void pa_destroy(pa_ctx* c) {
   DevBuf* all[] = {&c->cells, &c->lut, &c->leak, &c->patch, &c->dleak, &c->gates, &c->pin_off, &c->gate_off, &c->t, &c->s,
                    &c->value_tmp, &c->err_word, &c->tmax_bits, &c->bins, &c->part_blk,
                    &c->part_counts, &c->tiles, &c->heavy, &c->p0_tot, &c->p_out, &c->dbg[0],
-                   &c->dbg[1], &c->dbg[2], &c->wave_tmp, &c->cnt_tmp, &c->scratch_small,
+                   &c->dbg[1], &c->dbg[2], &c->wave_tmp, &c->cnt_tmp, &c->gate_tmp, &c->scratch_small,
                    &c->chunk_sums, &c->b_bt, &c->b_bs, &c->b_btag, &c->b_urec, &c->b_ugate, &c->b_items,
                    &c->b_big, &c->b_bigf, &c->b_grank, &c->b_cnt, &c->b_evc, &c->b_ubase, &c->b_ebase,
                    &c->b_uband, &c->b_uoff, &c->b_flags, &c->b_ipos, &c->b_scan, &c->b_counters,
@@ -641,9 +651,11 @@ int pa_run(pa_ctx* c, const pa_run_params* prm, pa_result* out) {
   PA_TRY(dreserve(c, c->chunk_sums, (size_t)reduce_chunks(N) * sizeof(double)));
   PA_TRY(dreserve(c, c->wave_tmp, (size_t)N * sizeof(float)));
   PA_TRY(dreserve(c, c->cnt_tmp, (size_t)N * 2 * sizeof(uint32_t)));
-  if (plan.debug) {
+  const bool dbg_arrays = out->state_pre || out->lut_ij || out->is_glitch;
+  if (dbg_arrays) {
     for (int i = 0; i < 3; ++i) PA_TRY(dreserve(c, c->dbg[i], c->n_events));
   }
+  if (plan.gate && out->out_mem != PA_MEM_DEVICE) PA_TRY(dreserve(c, c->gate_tmp, ((size_t)G + 1) * 4 * sizeof(double)));
   B.bins = (float4*)c->bins.p;
   B.part_blk = (uint32_t*)c->part_blk.p;
   B.part_counts = (uint32_t*)c->part_counts.p;
@@ -655,7 +667,8 @@ int pa_run(pa_ctx* c, const pa_run_params* prm, pa_result* out) {
   B.wave = (float*)c->wave_tmp.p;
   B.cnt_ev = (uint32_t*)c->cnt_tmp.p;
   B.cnt_gl = (uint32_t*)c->cnt_tmp.p + N;
-  for (int i = 0; i < 3; ++i) B.dbg[i] = plan.debug ? (uint8_t*)c->dbg[i].p : nullptr;
+  for (int i = 0; i < 3; ++i) B.dbg[i] = dbg_arrays ? (uint8_t*)c->dbg[i].p : nullptr;
+  if (plan.gate) B.gate_e = out->out_mem == PA_MEM_DEVICE ? out->gate_power_w : (double*)c->gate_tmp.p;
   return run_pass(c, plan, B, out, "pa_run", banded ? &c->band : nullptr);
 }
 
@@ -729,7 +742,7 @@ extern "C" int pa_run_noalloc(pa_ctx* c, const pa_run_params* prm, pa_result* ou
     return fail(c, PA_ERR_ARG, "pa_run_noalloc: %u gates exceed PA_NOALLOC_MAX_GATES (%u)", c->n_gates,
                 PA_NOALLOC_MAX_GATES);
   const bool any_array = out->waveform_w || out->event_count || out->glitch_count || out->state_pre ||
-                         out->lut_ij || out->is_glitch;
+                         out->lut_ij || out->is_glitch || out->gate_power_w;
   if (any_array && out->out_mem != PA_MEM_DEVICE)
     return fail(c, PA_ERR_ARG, "pa_run_noalloc: output arrays must be device memory (out_mem = PA_MEM_DEVICE)");
   CUDA_TRY(c, cudaSetDevice(c->device));
@@ -751,6 +764,7 @@ extern "C" int pa_run_noalloc(pa_ctx* c, const pa_run_params* prm, pa_result* ou
   B.dbg[0] = out->state_pre;
   B.dbg[1] = out->lut_ij;
   B.dbg[2] = out->is_glitch;
+  B.gate_e = out->gate_power_w;  // accumulated in place
   return run_pass(c, plan, B, out, "pa_run_noalloc", nullptr);
 }
 

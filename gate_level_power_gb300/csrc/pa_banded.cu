@@ -833,12 +833,14 @@ struct EvOut {
   uint32_t flags;  // 1: input-pin event (carries a leakage step), 2: glitch
 };
 
-// Debug values of an event (only with kDebug).
+// Debug values of an event (only with kDebug): what the per-event outputs
+// need, and the event's share of its gate's energies.
 struct EvDbg {
   uint32_t s_pre, lut_ij, unit;
   int p;
   float t;
   bool glitch;
+  float g_int, g_sw, g_gl, g_lk;  // fJ
 };
 
 // Glitch test against the pin's previous event (staged index e - 1 if idx > 0;
@@ -919,9 +921,11 @@ __device__ __forceinline__ EvOut ev_input(const RunArgs& a, const CellTab& CT, c
     acc.e_int += glitch ? 0.f : e_int;
     acc.e_lk = fmaf(dp, a.t_max_f - t, acc.e_lk);
   }
+  if (kDebug)
+    dbg = EvDbg{s_pre, (uint32_t)((lis << 4) | j), tag & 63u, p, t, glitch, glitch ? 0.f : e_int, 0.f,
+                glitch ? e_w : 0.f, dp * (a.t_max_f - t)};
   const float rem = fmaf(-(float)c, T, t);  // t - c T: the step's part inside its own cycle
   e_w = fmaf(dp, T - rem, e_w);
-  if (kDebug) dbg = EvDbg{s_pre, (uint32_t)((lis << 4) | j), tag & 63u, p, t, glitch};
   return EvOut{c, e_w, dp, 1u | (glitch ? 2u : 0u)};
 }
 
@@ -952,7 +956,7 @@ __device__ __forceinline__ EvOut ev_output(const RunArgs& a, const float* ts, co
       const int qa = pin_start(y, q);
       s_pre ^= ((uint32_t)seg_rank(ub + qa, pin_start(y, q + 1) - qa, t, steps) & 1u) << q;
     }
-    dbg = EvDbg{s_pre, 0xFFu, tag & 63u, k, t, glitch};
+    dbg = EvDbg{s_pre, 0xFFu, tag & 63u, k, t, glitch, 0.f, glitch ? 0.f : e_sw, glitch ? e_w : 0.f, 0.f};
   }
   return EvOut{c, e_w, 0.f, glitch ? 2u : 0u};
 }
@@ -1002,9 +1006,9 @@ __device__ void event_debug(const RunArgs& a, uint32_t gate, int p, float t, uin
     }
   }
   if (l < hi && a.t[l] == t) {
-    a.dbg_state[l] = (uint8_t)s_pre;
-    a.dbg_lut[l] = (uint8_t)lut_ij;
-    a.dbg_glitch[l] = (uint8_t)glitch;
+    if (a.dbg_state) a.dbg_state[l] = (uint8_t)s_pre;
+    if (a.dbg_lut) a.dbg_lut[l] = (uint8_t)lut_ij;
+    if (a.dbg_glitch) a.dbg_glitch[l] = (uint8_t)glitch;
   } else {
     berr(a.err, item, kErrTileOverflow);
   }
@@ -1038,7 +1042,16 @@ __device__ __forceinline__ void band_item(const BandRunArgs& A, const CellTab& C
       const EvOut o = i < n_in ? ev_input<kPow2, true>(a, CT, ts, tg, rec, gs, i, steps, true, acc, d0)
                                : ev_output<kPow2, true>(a, ts, tg, rec, gs, i, steps, true, acc, d0);
       ev_commit<kExact>(A, hist, o, item, c0);
-      event_debug(a, A.L.ugate[g.u0 + d0.unit], d0.p, d0.t, d0.s_pre, (int)d0.lut_ij, d0.glitch, item);
+      const uint32_t gate = A.L.ugate[g.u0 + d0.unit];
+      if (a.gate_e) {  // this event's share of its gate's energies
+        double* ge = a.gate_e + (size_t)gate * 4;
+        if (d0.glitch) atomicAdd(ge + 2, (double)d0.g_gl);
+        else if (i < n_in) atomicAdd(ge + 0, (double)d0.g_int);
+        else atomicAdd(ge + 1, (double)d0.g_sw);
+        if (i < n_in) atomicAdd(ge + 3, (double)d0.g_lk);
+      }
+      if (a.dbg_state || a.dbg_lut || a.dbg_glitch)
+        event_debug(a, gate, d0.p, d0.t, d0.s_pre, (int)d0.lut_ij, d0.glitch, item);
     }
   } else {
     for (int base = 0; base < n_in; base += 64) {

@@ -116,10 +116,12 @@ struct RunArgs {
   double* chunk_sums;      // [ceil(n_cycles / kReduceChunk)] final-reduction partial sums
   double* totals;          // [4]: E_int, E_sw, E_gl (fJ), sum dP * (t_max - t) (fJ)
   unsigned long long* err;
-  // debug outputs (device, may be null)
+  // debug outputs (device, each may be null)
   uint8_t* dbg_state;
   uint8_t* dbg_lut;
   uint8_t* dbg_glitch;
+  // per-gate energies {E_int, E_sw, E_gl, sum dP (t_max - t)} (fJ, zeroed), or null
+  double* gate_e;
 };
 
 // ------------------------------------------------------------------ banded layout
@@ -260,6 +262,9 @@ int band_blocks_per_sm(bool pow2, bool debug, bool exact);
 
 cudaError_t launch_final_reduce(const RunArgs& a, double t_clk, double t_max, float* wave_out,
                                 double* p_out, bool exact, cudaStream_t st);
+// Per-gate power in place: a.gate_e (fJ) -> W, with each gate's initial-state
+// leakage held to t_max added to its leakage.
+cudaError_t launch_gate_power(const RunArgs& a, double t_max, cudaStream_t st);
 inline uint32_t reduce_chunks(uint32_t n_cycles) { return (n_cycles + kReduceChunk - 1) / kReduceChunk; }
 
 }  // namespace pa

@@ -277,7 +277,8 @@ struct __align__(16) Slot {
   uint8_t k, init, j, pre; // inputs, initial input bits, load-axis interval, parity of earlier events per pin
   uint32_t cell;
   float v, esw;            // load-axis fraction; switching energy C V^2 / 2 (fJ)
-  uint32_t pad[2];
+  uint32_t gate;           // gate index (per-gate outputs)
+  uint32_t pad;
 };
 static_assert(sizeof(Slot) == 48, "slot size");
 
@@ -395,6 +396,7 @@ __device__ __forceinline__ void do_event(const RunArgs& a, const float* __restri
     acc.e_sw += e_sw;
     e_w = e_dyn;
   }
+  const float e_dyn_w = e_w;  // the event's dynamic (or glitch) energy
   if (p < k) {
     const float rem = fmaf(-(float)c, a.t_clk, t);  // t - c T
     e_w = fmaf(dp, a.t_clk - rem, e_w);
@@ -415,9 +417,20 @@ __device__ __forceinline__ void do_event(const RunArgs& a, const float* __restri
                  : "memory");
   }
   if (kDebug) {
-    a.dbg_state[gidx] = (uint8_t)s_pre;
-    a.dbg_lut[gidx] = p < k ? (uint8_t)((li << 4) | S.j) : (uint8_t)0xFF;
-    a.dbg_glitch[gidx] = (uint8_t)glitch;
+    if (a.dbg_state) a.dbg_state[gidx] = (uint8_t)s_pre;
+    if (a.dbg_lut) a.dbg_lut[gidx] = p < k ? (uint8_t)((li << 4) | S.j) : (uint8_t)0xFF;
+    if (a.dbg_glitch) a.dbg_glitch[gidx] = (uint8_t)glitch;
+    if (a.gate_e) {  // this event's share of its gate's energies
+      double* ge = a.gate_e + (size_t)S.gate * 4;
+      if (glitch) {
+        atomicAdd(ge + 2, (double)e_dyn_w);
+      } else if (p < k) {
+        atomicAdd(ge + 0, (double)e_int);
+      } else {
+        atomicAdd(ge + 1, (double)e_sw);
+      }
+      if (p < k) atomicAdd(ge + 3, (double)(dp * (a.t_max_f - t)));
+    }
   }
 }
 
@@ -438,6 +451,7 @@ __device__ __forceinline__ void fill_slot(const RunArgs& a, const CellDesc* cell
   S.j = (uint8_t)j;
   S.v = (C - cd.lax[j]) * cd.ilax[j];
   S.esw = a.half_vdd2 * C;
+  S.gate = g;
 }
 
 __device__ __forceinline__ void flush_acc(Acc& acc, double* s_tot) {
@@ -788,6 +802,38 @@ cudaError_t launch_final_reduce(const RunArgs& a, double t_clk, double t_max, fl
   else k_reduce_chunks<false><<<nc, kRedThreads, 0, st>>>(a);
   if (exact) k_reduce_apply<true><<<nc, kRedThreads, 0, st>>>(a, t_clk, t_max, wave_out, p_out);
   else k_reduce_apply<false><<<nc, kRedThreads, 0, st>>>(a, t_clk, t_max, wave_out, p_out);
+  return cudaGetLastError();
+}
+
+}  // namespace pa
+
+// ------------------------------------------------------------------ per-gate power
+
+namespace pa {
+
+namespace {
+
+// Gate g's energies (fJ) -> power (W): E / t_max, and for leakage the initial
+// state's leakage held over the whole window plus the gate's power steps
+// carried to t_max, E_leak = leak(S0) t_max + sum dP (t_max - t).
+__global__ void __launch_bounds__(256) k_gate_power(const RunArgs a, double t_max) {
+  const uint64_t g = (uint64_t)blockIdx.x * 256u + threadIdx.x;
+  if (g >= a.n_gates) return;
+  const GateRec r = a.gates[g];
+  const CellDesc& cd = a.cells[r.cell];
+  const double p0 = (double)a.leak[cd.leak_off + (r.init & ((1u << cd.k) - 1u))];  // uW
+  double* ge = a.gate_e + g * 4;
+  const double f = 1e-6 / t_max;  // fJ / ns = uW -> W
+  ge[0] *= f;
+  ge[1] *= f;
+  ge[2] *= f;
+  ge[3] = (p0 * t_max + ge[3]) * f;
+}
+
+}  // namespace
+
+cudaError_t launch_gate_power(const RunArgs& a, double t_max, cudaStream_t st) {
+  if (a.n_gates && a.gate_e) k_gate_power<<<(a.n_gates + 255) / 256, 256, 0, st>>>(a, t_max);
   return cudaGetLastError();
 }
 

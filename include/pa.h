@@ -51,7 +51,7 @@
 extern "C" {
 #endif
 
-#define PA_VERSION 1
+#define PA_VERSION 2
 
 #define PA_OK 0
 #define PA_ERR_ARG (-1)      /* null pointer, bad size, bad axis, bad parameter      */
@@ -179,6 +179,16 @@ typedef struct pa_run_params {
  *   lut_ij[n_events]        per input event: (i << 4) | j of the LUT interval;
  *                           0xFF for output events (debug)
  *   is_glitch[n_events]     per event: 1 if a glitch (debug)
+ *   gate_power_w[n_gates * 4]  per gate g at [4g .. 4g + 3]: its internal,
+ *                           switching, glitch and leakage power, W (double); over
+ *                           all gates the four sum to p_int_w .. p_leak_w. This
+ *                           is the per-gate view the paper's accuracy study ranks
+ *                           gates by (Kendall's Tau of gate power, Fig. 10). With
+ *                           out_mem = PA_MEM_DEVICE the array itself accumulates
+ *                           the gate energies, so after an error it may hold
+ *                           partial values.
+ * The per-event debug arrays and gate_power_w take a slower per-event path
+ * (one event per lane, extra global writes); ask for them only when needed.
  * With PA_RUN_TIMING, ms_* hold CUDA-event times of the partition, fused and
  * reduction kernels and of the whole device pass. n_tiles / n_heavy count the
  * work items (light tiles / heavy items); path says which kernel ran.
@@ -197,6 +207,7 @@ typedef struct pa_result {
   uint32_t n_tiles, n_heavy;
   uint32_t kernel_launches;
   uint32_t path;  /* out: PA_PATH_UNBANDED or PA_PATH_BANDED */
+  double *gate_power_w;
 } pa_result;
 
 #define PA_PATH_UNBANDED 0u
@@ -288,9 +299,9 @@ int pa_run(pa_ctx *ctx, const pa_run_params *params, pa_result *out);
  * capture. All calls share the one array and it keeps the last call's
  * contents (each call clears what it needs zeroed): calls whose device work
  * overlaps -- from several threads, contexts or streams at once -- race and
- * must be serialised by the caller. Per-event debug arrays are written in
- * place and may hold partial data after an error; the other outputs are
- * written only on PA_OK.
+ * must be serialised by the caller. Per-event debug arrays and gate_power_w
+ * are written in place and may hold partial data after an error; the other
+ * outputs are written only on PA_OK.
  */
 #define PA_NOALLOC_MAX_CYCLES 65536u
 #define PA_NOALLOC_MAX_GATES 262144u

@@ -34,7 +34,7 @@ def test_library_exports_every_declared_symbol():
 def test_version_and_defaults_without_gpu():
     import gate_level_power_gb300 as glp
     glp.build()
-    assert glp.pa_version() == 1
+    assert glp.pa_version() == 2
     p = glp.pa_default_params()
     assert p.n_cycles == 1 and abs(p.vdd - 0.9) < 1e-12 and p.t_clk_ns == 1.0
 
