@@ -21,7 +21,7 @@ Printed (rank 0, one JSON line):
 
 ``--impl reference`` times the oracle alone (rank 0), on the same workload and
 metric.
-Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5]
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..6] [--synth KNOB=VALUE ...]
 """
 from __future__ import annotations
 
@@ -239,7 +239,7 @@ def ncu_traffic(kernel: str, config: int):
     return None
 
 
-def cpu_baseline(config, seed, target_s, n_events_total, n_gates_total):
+def cpu_baseline(config, seed, target_s, n_events_total, n_gates_total, **over):
     """Time the oracle (fp64, as it stands) on a contiguous gate block of the
     workload, grown until one run takes about target_s."""
     import oracle
@@ -249,7 +249,7 @@ def cpu_baseline(config, seed, target_s, n_events_total, n_gates_total):
     n = max(64, min(n_gates_total, 2000))
     el = 0.0
     while True:
-        w = synth.generate_range(config, g0, min(n_gates_total, g0 + n), seed=seed)
+        w = synth.generate_range(config, g0, min(n_gates_total, g0 + n), seed=seed, **over)
         t0 = time.perf_counter()
         oracle.run(w, threads=cores)
         el = time.perf_counter() - t0
@@ -271,17 +271,18 @@ def run_reference(args):
         return 0
     import oracle
     import synth
-    cfg = synth.make_cfg(args.config, args.seed)
-    G, E = int(cfg.n_gates), int(cfg.n_events)
+    over = synth_overrides(args.synth)
+    cfg = synth.make_cfg(args.config, args.seed, **over)
+    G, _, E = synth.sizes(args.config, args.seed, **over)
     cores = os.cpu_count() or 1
     # size the per-step sample so warmup + steps take a few minutes at most
-    probe = synth.generate_range(args.config, G // 3, G // 3 + 2000, seed=args.seed)
+    probe = synth.generate_range(args.config, G // 3, G // 3 + 2000, seed=args.seed, **over)
     t0 = time.perf_counter()
     oracle.run(probe, threads=cores)
     per_gate = (time.perf_counter() - t0) / probe.n_gates
     budget = 120.0 / max(1, args.steps + args.warmup)
     n = int(max(200, min(G // 3, budget / max(per_gate, 1e-9))))
-    w = synth.generate_range(args.config, G // 3, G // 3 + n, seed=args.seed)
+    w = synth.generate_range(args.config, G // 3, G // 3 + n, seed=args.seed, **over)
     for _ in range(args.warmup):
         oracle.run(w, threads=cores)
     t0 = time.perf_counter()
@@ -408,7 +409,7 @@ def run_ours(args):
     traffic = None if args.synth else ncu_traffic(kname, args.config)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(args.config, args.seed, args.cpu_seconds, E, G)
+        cpu = cpu_baseline(args.config, args.seed, args.cpu_seconds, E, G, **over)
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "events/s", "n_gpus": world, "steps": args.steps,

@@ -54,6 +54,7 @@ class SynthCfg(ctypes.Structure):
         ("quantum_ns", ctypes.c_double),
         ("vdd", ctypes.c_double),
         ("threads", ctypes.c_int32),
+        ("toggles", ctypes.c_int32),
     ]
 
 
@@ -77,6 +78,8 @@ CONFIG_NAMES = {
     3: "large skewed: 1M gates, 32 cells, 10k cycles @ 0.8 ns, 200M events, Zipf(1.2) top1%~50%, 15% glitch edges",
     4: "very large skewed: 5M gates, 64 cells k=1..4, 8x8 LUTs, 100k cycles @ 1 ns, 1B events, Zipf(1.1), lognormal slews",
     5: "bursty: 10M gates, 64 cells k=4, 8x8 LUTs, 50k cycles @ 1 ns, 2B events, 80% in 5% of cycles, Zipf(1.3)",
+    6: "waveform-bin stress: 1k gates, 32 cells k=1..4, 100k cycles @ 1 ns, every pin toggling 4 times per cycle "
+       "(knob toggles = 1, 2, 4, 8)",
 }
 
 
@@ -185,6 +188,21 @@ def make_cfg(config: int, seed: int = 0, **overrides) -> SynthCfg:
             raise KeyError(f"unknown synth knob {k!r}")
         setattr(c, k, v)
     return c
+
+
+def sizes(config: int, seed: int = 0, **overrides):
+    """(gates, pins, events) of a workload, without drawing its events."""
+    L = _load()
+    cfg = make_cfg(config, seed, **overrides)
+    h = L.synth_create(ctypes.byref(cfg))
+    try:
+        nc = ctypes.c_uint32()
+        lut_len, leak_len, G, P, E = (ctypes.c_uint64() for _ in range(5))
+        L.synth_sizes(h, ctypes.byref(nc), ctypes.byref(lut_len), ctypes.byref(leak_len),
+                      ctypes.byref(G), ctypes.byref(P), ctypes.byref(E))
+        return G.value, P.value, E.value
+    finally:
+        L.synth_destroy(h)
 
 
 def generate(config: int, seed: int = 0, alloc=None, with_value: bool = True, **overrides) -> Workload:

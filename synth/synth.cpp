@@ -104,6 +104,8 @@ typedef struct synth_cfg {
   double   quantum_ns;    // > 0: snap times to multiples of this (forces cross-pin ties)
   double   vdd;
   int32_t  threads;       // 0 = hardware concurrency
+  int32_t  toggles;       // > 0: every pin toggles exactly this many times in every cycle
+                          // (high-activity stress waveforms; n_events follows from the netlist)
 } synth_cfg;
 
 typedef struct synth_stats {
@@ -195,6 +197,9 @@ void set_defaults(synth_cfg* c, int config) {
       c->n_gates = 10000000; c->n_cells = 64; c->k_mode = 2; c->n_slew = 8; c->n_load = 8;
       c->n_cycles = 50000; c->n_events = 2000000000; c->activity = 1; c->zipf_s = 1.3;
       c->slew_dist = 1; c->load_dist = 1; c->burst_frac = 0.8;
+      break;
+    case 6:  // waveform-bin stress: 100k cycles, every pin toggling 1, 2, 4 or 8 times per cycle
+      c->n_gates = 1000; c->n_cells = 32; c->n_cycles = 100000; c->toggles = 4;
       break;
     default:  // custom: a small valid default
       c->n_gates = 16; c->n_cells = 4; c->n_cycles = 16; c->n_events = 200;
@@ -330,6 +335,13 @@ void build_netlist_and_counts(Synth& S) {
     }
     for (int64_t g = 0; g < G; ++g) w[g] = std::pow((double)rank[g] + 1.0 + c.zipf_q, -c.zipf_s);
   }
+  if (c.toggles > 0) {  // every pin: toggles events in each cycle
+    int64_t tot_ev = 0;
+    for (int64_t g = 0; g < G; ++g) tot_ev += (int64_t)(S.k[S.cell[g]] + 1) * c.toggles * (int64_t)c.n_cycles;
+    c.n_events = tot_ev;
+    S.cfg.n_events = tot_ev;
+    for (int64_t g = 0; g < G; ++g) w[g] = (double)(S.k[S.cell[g]] + 1);
+  }
   // Exact total: per-gate counts are differences of the rounded cumulative share.
   double tot = 0;
   for (int64_t g = 0; g < G; ++g) tot += w[g];
@@ -433,7 +445,13 @@ void fill_gates(Synth& S, int64_t g0, int64_t g1, uint64_t ev_base, float* t_out
         }
         return r.uniform() * window;
       };
-      for (uint64_t i = 0; i < n - 2 * pairs; ++i) buf.push_back({draw_t(), slew()});
+      if (c.toggles > 0) {  // stress waveform: toggles events in every cycle, jittered
+        pairs = 0;
+        for (int64_t cy = 0; cy < c.n_cycles; ++cy)
+          for (int j = 0; j < c.toggles; ++j)
+            buf.push_back({((double)cy + ((double)j + 0.1 + 0.8 * r.uniform()) / c.toggles) * T, slew()});
+      }
+      for (uint64_t i = 0; c.toggles <= 0 && i < n - 2 * pairs; ++i) buf.push_back({draw_t(), slew()});
       for (uint64_t i = 0; i < pairs; ++i) {
         double t0;
         if (!S.glitch_cycles.empty()) {

@@ -145,3 +145,15 @@ def test_more_than_2_pow_24_events_in_one_cycle_banded(glp):
     o = oracle.run(w, threads=8)
     assert int(o["evcount"].max()) >= 1 << 24
     assert_parity(r, o, debug=False)
+
+
+@pytest.mark.parametrize("m", [1, 2, 4, 8])
+def test_stress_waveform_banded(glp, m):
+    # every pin toggling m times per cycle: single-cycle windows for m >= 4,
+    # and at m = 8 (more than 7 events of a pin in a cycle) every gate is
+    # streamed by the unbanded kernel in the same run
+    w = synth.generate(6, n_gates=40, n_cycles=300, toggles=m)
+    r = banded_run(glp, w)
+    o = oracle.run(w, debug=True, threads=4)
+    assert_parity(r, o)
+    assert (r["n_tiles"] == 0) == (m == 8)

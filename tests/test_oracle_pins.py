@@ -245,6 +245,22 @@ def test_per_gate_power_lone_gate_is_the_totals():
         assert r["gate_power"][0, m] == pytest.approx(d["expected"][key], rel=1e-12), key
 
 
+@pytest.mark.parametrize("m", [1, 2, 4, 8])
+def test_stress_waveform_counts_closed_form(m):
+    # the waveform-bin stress workload: every pin toggles m times in every
+    # cycle, so each cycle holds m events per pin and, by the counter reading,
+    # m - 1 glitches per pin; bins still sum to the totals
+    w = synth.generate(6, n_gates=30, n_cycles=40, toggles=m)
+    P = w.n_pins
+    assert w.n_events == m * P * w.n_cycles
+    r = oracle.run(w)
+    assert (r["evcount"] == m * P).all()
+    assert (r["glcount"] == (m - 1) * P).all()
+    assert (r["p_gl"] > 0) == (m > 1)
+    e_tot = r["e_int"] + r["e_sw"] + r["e_gl"] + r["e_leak"]
+    assert float(r["wave_energy"].sum()) == pytest.approx(e_tot, rel=1e-12)
+
+
 def test_brute_force_ties_are_exercised():
     # the quantised workloads above must contain cross-pin ties, else the tie rule is unpinned
     w = _tiny_random(3, 0.125, k_mode=2)
