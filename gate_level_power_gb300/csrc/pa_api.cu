@@ -860,6 +860,9 @@ int build_bands(pa_ctx* c, float t_clk, uint32_t cb) {
   L.n_units = (uint32_t)n_units;
   L.n_ev = n_ev;
   L.n_big = counters[0];
+  // units hold at most 5 * kUnitPinMax events; the bucket leaves room for the largest one
+  if (counters[2] > (uint32_t)kUnitMaxEvents) return fail(c, PA_ERR_INTERNAL, "pa_build_bands: unit of %u events", counters[2]);
+  a.item_bucket = (uint32_t)kItemEvents - 1u - std::max<uint32_t>(counters[2], 1u);
   // write: records, event copy, item heads
   const size_t nu = (size_t)n_units;
   const size_t ev_bytes = ((n_ev + 64) & ~(size_t)15) * sizeof(float);

@@ -134,15 +134,18 @@ uint32_t band_scan_blocks(uint64_t n) { return (uint32_t)((n + kScanBlock - 1) /
 
 // ------------------------------------------------------------------ layout build (load time)
 //
-// One thread per gate walks the gate's cycles in order (a merge of its pins'
+// One warp per gate walks the gate's cycles in order (a merge of its pins'
 // cycle streams; a pin's events are time-sorted, so its cycles are
 // non-decreasing) and cuts windows greedily: the current window closes at a
 // band boundary, or before a cycle whose events would take one of the pins
-// past kUnitPinMax in the window. Counting pass: units and events per
+// past kUnitPinSoft in the window; a first cycle that alone takes a pin past
+// kUnitPinSoft is a window by itself (past kUnitPinMax: the gate is left to
+// the unbanded kernel). Counting pass: units and events per
 // (band, gate). Writing pass: the same walk writes each unit's record and
 // copies its events, pin by pin, to the unit's place in the banded arrays.
 // Items: a unit starts an item at a band start, where its event offset enters
-// a new kItemBucket bucket of the band, or every kItemUnits units.
+// a new bucket of the band (kItemEvents - 1 - the largest unit's events), or
+// every kItemUnits units.
 
 namespace {
 
@@ -187,7 +190,7 @@ __global__ void __launch_bounds__(256) k_bw_walk(const BandBuildArgs a) {
       cy[p] = (uint32_t)lane < hi[p] ? bcyc(a, a.t[lo[p] + lane]) : kNoCycle;
     }
     uint32_t state = r.init & ((1u << k) - 1u);  // input state at the window start
-    uint32_t band = kNoCycle, units = 0, events = 0;
+    uint32_t band = kNoCycle, units = 0, events = 0, max_unit = 0;
     uint64_t u = 0, dst = 0;  // next unit / banded event of this (band, gate)
     bool big = false, split = false;
     for (;;) {
@@ -213,16 +216,21 @@ __global__ void __launch_bounds__(256) k_bw_walk(const BandBuildArgs a) {
         }
       }
       const uint64_t be = ((uint64_t)b + 1) << a.mb;
-      uint32_t c_end = be > 0xFFFFFFFFull ? 0xFFFFFFFFu : (uint32_t)be;
-      const uint32_t c_band_end = c_end;
+      const uint32_t c_band_end = be > 0xFFFFFFFFull ? 0xFFFFFFFFu : (uint32_t)be;
+      uint32_t c_end = c_band_end, c_hard = c_band_end;
 #pragma unroll
       for (int p = 0; p < P; ++p) {
-        const uint32_t c = __shfl_sync(0xffffffffu, cy[p], (int)(j[p] + kUnitPinMax - cb[p]) & 31);
-        if (j[p] + kUnitPinMax < hi[p]) c_end = min(c_end, c);
+        const uint32_t cs = __shfl_sync(0xffffffffu, cy[p], (int)(j[p] + kUnitPinSoft - cb[p]) & 31);
+        if (j[p] + kUnitPinSoft < hi[p]) c_end = min(c_end, cs);
+        const uint32_t ch = __shfl_sync(0xffffffffu, cy[p], (int)(j[p] + kUnitPinMax - cb[p]) & 31);
+        if (j[p] + kUnitPinMax < hi[p]) c_hard = min(c_hard, ch);
       }
-      if (c_end <= c_start) {  // 16 events of one pin in one cycle
-        big = true;
-        break;
+      if (c_end <= c_start) {  // the first cycle alone gives a pin more than kUnitPinSoft events
+        if (c_hard <= c_start) {  // more than kUnitPinMax
+          big = true;
+          break;
+        }
+        c_end = c_start + 1;
       }
       if (c_end < c_band_end) split = true;
       uint32_t n[P], size = 0;
@@ -233,6 +241,7 @@ __global__ void __launch_bounds__(256) k_bw_walk(const BandBuildArgs a) {
         n[p] = (uint32_t)__popc(__ballot_sync(0xffffffffu, in));
         size += n[p];
       }
+      if (!kWrite) max_unit = max(max_unit, size);
       if (kWrite) {
         if (u < (uint64_t)a.L.n_units && dst + size <= a.L.n_ev) {
           if (lane == 0) {
@@ -292,6 +301,7 @@ __global__ void __launch_bounds__(256) k_bw_walk(const BandBuildArgs a) {
           a.evc_gb[(uint64_t)band * G + gr] = events;
         }
         if (split) atomicAdd(a.counters + 1, 1u);
+        if (max_unit) atomicMax(a.counters + 2, max_unit);
       }
     }
   }
@@ -340,7 +350,7 @@ __global__ void __launch_bounds__(256) k_bw_item_flags(const BandBuildArgs a, ui
   const uint64_t be = a.uoff[bu0];
   bool head = u == bu0;
   if (!head) {
-    head = (a.uoff[u] - be) / kItemBucket != (a.uoff[u - 1] - be) / kItemBucket ||
+    head = (a.uoff[u] - be) / a.item_bucket != (a.uoff[u - 1] - be) / a.item_bucket ||
            (u - bu0) / (uint32_t)kItemUnits != (u - 1 - bu0) / (uint32_t)kItemUnits;
   }
   a.flags[u] = head ? 1u : 0u;
@@ -495,7 +505,7 @@ __global__ void __launch_bounds__(kFinWarps * 32) k_bw_finalize(const BandBuildA
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) seg_max = max(seg_max, __shfl_xor_sync(0xffffffffu, seg_max, o));
-    const uint32_t steps = seg_max == 0 ? 0u : seg_max == 1 ? 1u : seg_max <= 3 ? 2u : 3u;
+    const uint32_t steps = seg_max == 0 ? 0u : seg_max == 1 ? 1u : seg_max <= 3 ? 2u : seg_max <= 7 ? 3u : 4u;
     if (lane == 0)
       L.items[it].bw = (L.items[it].bw & kItemBandMask) | (n_in_all << kItemBandBits) | (steps << kItemStepShift);
     __syncwarp();
@@ -763,7 +773,7 @@ __device__ __forceinline__ ItemGeo item_geo(const BandItem& a, const BandItem& b
   g.ea = a.e0 & ~3ull;
   g.ev_off = (uint32_t)(a.e0 - g.ea);
   g.tag_off = (uint32_t)(a.e0 & 15ull);
-  g.n_in = (a.bw >> kItemBandBits) & 511u;
+  g.n_in = (a.bw >> kItemBandBits) & 511u;  // bits 20..28
   g.steps = a.bw >> kItemStepShift;
   g.ok = b.e0 > a.e0 && b.u0 > a.u0 && b.e0 - a.e0 < (uint64_t)kItemEvents && b.u0 - a.u0 <= (uint32_t)kItemUnits &&
          (uint64_t)g.n_in <= b.e0 - a.e0;
@@ -802,10 +812,13 @@ __device__ __forceinline__ void prefetch_item(const BandLayout& L, const ItemGeo
 // Events of a sorted pin segment b[0, qn) earlier than t, by binary lifting
 // in `steps` steps (the same for the whole warp: enough for the item's
 // longest input-pin segment, qn < 2^steps).
-static_assert(kUnitPinMax <= 7, "three lifting steps cover a pin segment");
+// kLong: the item may hold segments of 8 to 15 events (a fourth step).
+static_assert(kUnitPinMax <= 15, "four lifting steps cover a pin segment");
+template <bool kLong>
 __device__ __forceinline__ int seg_rank(const float* b, int qn, float t, uint32_t steps) {
   int r = 0;
-  if (steps >= 3 && 4 <= qn && b[3] < t) r = 4;
+  if (kLong && 8 <= qn && b[7] < t) r = 8;
+  if (steps >= 3 && r + 4 <= qn && b[r + 3] < t) r += 4;
   if (steps >= 2 && r + 2 <= qn && b[r + 1] < t) r += 2;
   if (steps >= 1 && r + 1 <= qn && b[r] < t) r += 1;
   return r;
@@ -859,7 +872,7 @@ __device__ __forceinline__ float glitch_scale(const RunArgs& a, const float* ts,
 
 // Input-pin event at staged index i: gate state, LUT energy, leakage step,
 // glitch, totals. `valid` false: computed for a padding lane, not counted.
-template <bool kPow2, bool kDebug>
+template <bool kPow2, bool kDebug, bool kLong>
 __device__ __forceinline__ EvOut ev_input(const RunArgs& a, const CellTab& CT, const float* ts, const uint8_t* tg,
                                           const uint4* rec, const float* gs, int i, uint32_t steps, bool valid,
                                           BAcc& acc, EvDbg& dbg) {
@@ -888,7 +901,7 @@ __device__ __forceinline__ EvOut ev_input(const RunArgs& a, const CellTab& CT, c
     const int qa = (int)(se & 63u);
     const int qn = (int)((se >> 8) & 63u) - qa;
     const float* b = ub + qa;
-    const int r = seg_rank(b, qn, t, steps);
+    const int r = seg_rank<kLong>(b, qn, t, steps);
     bool eq = false;
     if (ties) eq = q < p && r < qn && b[r] == t;
     const uint32_t par = (uint32_t)r & 1u;
@@ -954,7 +967,7 @@ __device__ __forceinline__ EvOut ev_output(const RunArgs& a, const float* ts, co
     const float* ub = ts + (int)(R.x & 511u);
     for (int q = 0; q < k; ++q) {
       const int qa = pin_start(y, q);
-      s_pre ^= ((uint32_t)seg_rank(ub + qa, pin_start(y, q + 1) - qa, t, steps) & 1u) << q;
+      s_pre ^= ((uint32_t)seg_rank<true>(ub + qa, pin_start(y, q + 1) - qa, t, steps) & 1u) << q;
     }
     dbg = EvDbg{s_pre, 0xFFu, tag & 63u, k, t, glitch, 0.f, glitch ? 0.f : e_sw, glitch ? e_w : 0.f, 0.f};
   }
@@ -1017,7 +1030,7 @@ __device__ void event_debug(const RunArgs& a, uint32_t gate, int p, float t, uin
 // One staged item on one warp: one lane per event, the input region first,
 // then the output region. Where a region has events left for a second round,
 // each lane computes two events before committing either.
-template <bool kPow2, bool kDebug, bool kExact>
+template <bool kPow2, bool kDebug, bool kExact, bool kLong>
 __device__ __forceinline__ void band_item(const BandRunArgs& A, const CellTab& CT, float* hist,
                                           const uint8_t* stage, uint32_t item, const ItemGeo& g, uint32_t c0,
                                           BAcc& acc) {
@@ -1039,7 +1052,7 @@ __device__ __forceinline__ void band_item(const BandRunArgs& A, const CellTab& C
   EvDbg d0{}, d1{};
   if (kDebug) {
     for (int i = lane; i < n; i += 32) {
-      const EvOut o = i < n_in ? ev_input<kPow2, true>(a, CT, ts, tg, rec, gs, i, steps, true, acc, d0)
+      const EvOut o = i < n_in ? ev_input<kPow2, true, true>(a, CT, ts, tg, rec, gs, i, steps, true, acc, d0)
                                : ev_output<kPow2, true>(a, ts, tg, rec, gs, i, steps, true, acc, d0);
       ev_commit<kExact>(A, hist, o, item, c0);
       const uint32_t gate = A.L.ugate[g.u0 + d0.unit];
@@ -1058,13 +1071,13 @@ __device__ __forceinline__ void band_item(const BandRunArgs& A, const CellTab& C
       const int i0 = base + lane;
       if (base + 32 < n_in) {  // every lane has a first event; some a second
         const int i1 = i0 + 32;
-        const EvOut o0 = ev_input<kPow2, false>(a, CT, ts, tg, rec, gs, i0, steps, true, acc, d0);
-        const EvOut o1 = ev_input<kPow2, false>(a, CT, ts, tg, rec, gs, min(i1, n_in - 1), steps, i1 < n_in,
+        const EvOut o0 = ev_input<kPow2, false, kLong>(a, CT, ts, tg, rec, gs, i0, steps, true, acc, d0);
+        const EvOut o1 = ev_input<kPow2, false, kLong>(a, CT, ts, tg, rec, gs, min(i1, n_in - 1), steps, i1 < n_in,
                                                 acc, d1);
         ev_commit<kExact>(A, hist, o0, item, c0);
         if (i1 < n_in) ev_commit<kExact>(A, hist, o1, item, c0);
       } else if (i0 < n_in) {
-        ev_commit<kExact>(A, hist, ev_input<kPow2, false>(a, CT, ts, tg, rec, gs, i0, steps, true, acc, d0), item,
+        ev_commit<kExact>(A, hist, ev_input<kPow2, false, kLong>(a, CT, ts, tg, rec, gs, i0, steps, true, acc, d0), item,
                           c0);
       }
     }
@@ -1233,7 +1246,10 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
           break;
         }
         phase ^= 1u;
-        band_item<kPow2, kDebug, kExact>(A, CT, hist, wbuf, my, gcur, c0, acc);
+        if (gcur.steps > 3)  // an item with a pin segment of 8 to 15 events (warp-uniform)
+          band_item<kPow2, kDebug, kExact, true>(A, CT, hist, wbuf, my, gcur, c0, acc);
+        else
+          band_item<kPow2, kDebug, kExact, false>(A, CT, hist, wbuf, my, gcur, c0, acc);
         if (++since == kTotEvery) {
           bflush_acc(acc, s_tot);
           since = 0;

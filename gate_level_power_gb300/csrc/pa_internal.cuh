@@ -130,7 +130,9 @@ struct RunArgs {
 // for one clock period fixed when the layout is built. Every gate's timeline is
 // cut greedily, in cycle order, into windows of whole cycles: a window closes
 // at a band boundary or before a cycle that would give one of its pins more
-// than kUnitPinMax events. A unit is one non-empty (gate, window). Units are
+// than kUnitPinSoft events; a single cycle that alone gives a pin more than
+// kUnitPinSoft (but at most kUnitPinMax) events is a window of its own. A
+// unit is one non-empty (gate, window). Units are
 // ordered band by band, gate by gate; work items are runs of whole units of
 // one band. Inside an item the events are stored in two regions: first the
 // input-pin events of all its units (unit by unit, each unit's pins in order,
@@ -143,25 +145,25 @@ struct RunArgs {
 // kUnitPinMax events of one pin in a single cycle ("big" gates) stay out of
 // the layout and are streamed by the unbanded kernel.
 
-constexpr int kUnitPinMax = 7;                   // events per pin per unit
+constexpr int kUnitPinMax = 15;                  // events per pin per unit (a unit of one cycle)
+constexpr int kUnitPinSoft = 7;                  // events per pin per unit of several cycles
 constexpr int kUnitMaxEvents = 5 * kUnitPinMax;  // events per unit
 constexpr uint32_t kBandDefaultCycles = 4096;
 constexpr uint32_t kBandMaxCycles = 4096;        // shared-memory histogram capacity (cycles)
-constexpr uint32_t kBandMaxBands = 1u << 20;
+constexpr uint32_t kBandMaxBands = (1u << 20) - 1;  // the item word's band field also holds the sentinel
 constexpr int kItemEvents = 512;                 // events per item (cap): one warp's work item
 constexpr int kItemUnits = 64;                   // units per item (cap): 6-bit unit tags
-// A new item starts where a unit's event offset enters a new bucket of this
-// many events (or a new band, or every kItemUnits units), so an item holds
-// fewer than kItemBucket + kUnitMaxEvents < kItemEvents events.
-constexpr uint32_t kItemBucket = kItemEvents - kUnitMaxEvents - 1;
+// A new item starts where a unit's event offset enters a new bucket of
+// kItemEvents - 1 - (the layout's largest unit) events (or a new band, or
+// every kItemUnits units), so an item holds fewer than kItemEvents events.
 
-// Item word `bw`: band (bits 0..20; items[n_items] is a sentinel with band =
-// n_bands) | input events of the item (bits 21..29) | binary-lifting steps
-// that cover the item's longest input-pin segment (bits 30..31: 0 for no
-// segment longer than 0, 1 for 1, 2 for up to 3, 3 for up to 7).
-constexpr uint32_t kItemBandBits = 21;
+// Item word `bw`: band (bits 0..19; items[n_items] is a sentinel with band =
+// n_bands) | input events of the item (bits 20..28) | binary-lifting steps
+// that cover the item's longest input-pin segment (bits 29..31: the smallest
+// s with 2^s > that length, 0..4).
+constexpr uint32_t kItemBandBits = 20;
 constexpr uint32_t kItemBandMask = (1u << kItemBandBits) - 1u;
-constexpr uint32_t kItemStepShift = 30;
+constexpr uint32_t kItemStepShift = 29;
 
 // Unit record (uint4), written by the finalize pass:
 //   x: input offset in the item (bits 0..8) | output offset in the item (9..17)
@@ -215,7 +217,8 @@ struct BandBuildArgs {
   uint32_t* flags;       // [max(G, n_units)] class flags, then item heads -- temporary
   uint64_t* ipos;        // [max(G + 2, n_units + 1)] scans -- temporary
   uint64_t* scan_blk;    // scan scratch -- temporary
-  uint32_t* counters;    // [4]: big gates, gates with windows narrower than a band -- temporary
+  uint32_t* counters;    // [4]: big gates, gates with windows narrower than a band, largest unit -- temporary
+  uint32_t item_bucket;  // events per item bucket (set after the counting pass)
   uint2* urec2;          // [n_units] unit records of the walk -- temporary
   const CellDesc* cells; // library (load axes for the unit records)
   BandLayout L;

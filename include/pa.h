@@ -243,7 +243,8 @@ int pa_load_events(pa_ctx *ctx, const pa_events *ev);
  * gate's timeline (cycle = floor(fl32(t / t_clk_ns))) is cut, in cycle order,
  * into windows of whole cycles inside bands of band_cycles cycles: a window
  * closes at a band boundary or before a cycle that would give one of the
- * gate's pins more than 7 events in it. Every non-empty (gate, window) is a
+ * gate's pins more than 7 events in it; a single cycle that alone gives a pin
+ * 8 to 15 events is a window of its own. Every non-empty (gate, window) is a
  * unit; units are ordered band by band and grouped into work items of at
  * most 511 events, and inside an item the events are copied into an input
  * region (the units' input-pin events, pin by pin in the per-pin CSR order)
@@ -253,7 +254,7 @@ int pa_load_events(pa_ctx *ctx, const pa_events *ev);
  * a per-pin event bound instead of a per-thread event target. Every pa_run whose t_clk_ns equals this
  * t_clk_ns bit for bit then uses the banded kernel, which keeps a band's cycle
  * bins in shared memory instead of adding every event to global memory; other
- * clocks use the unbanded kernel. Gates with more than 7 events of one pin in
+ * clocks use the unbanded kernel. Gates with more than 15 events of one pin in
  * a single cycle stay out of the layout and are streamed by the unbanded kernel
  * within the same run. Results agree with the unbanded path to floating-point
  * summation order.

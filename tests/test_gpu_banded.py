@@ -127,7 +127,7 @@ def test_build_bands_errors(glp):
 
 
 def test_big_gates_banded(glp):
-    # more than 7 events of a pin in one cycle: those gates stay out of the
+    # more than 15 events of a pin in one cycle: those gates stay out of the
     # banded layout and are streamed by the unbanded kernel in the same run
     w = synth.custom(seed=23, n_gates=40, n_cells=8, k_mode=1, n_slew=6, n_load=6, n_cycles=24,
                      t_clk_ns=1.0, n_events=60000, pair_frac=0.1, quantum_ns=0.001, threads=4)
@@ -150,10 +150,10 @@ def test_more_than_2_pow_24_events_in_one_cycle_banded(glp):
 @pytest.mark.parametrize("m", [1, 2, 4, 8])
 def test_stress_waveform_banded(glp, m):
     # every pin toggling m times per cycle: single-cycle windows for m >= 4,
-    # and at m = 8 (more than 7 events of a pin in a cycle) every gate is
-    # streamed by the unbanded kernel in the same run
+    # and at m = 8 (more than 7 events of a pin in a cycle) single-cycle
+    # windows whose pin segments need a fourth search step
     w = synth.generate(6, n_gates=40, n_cycles=300, toggles=m)
     r = banded_run(glp, w)
     o = oracle.run(w, debug=True, threads=4)
     assert_parity(r, o)
-    assert (r["n_tiles"] == 0) == (m == 8)
+    assert r["n_tiles"] > 0 and r["n_heavy"] > 0

@@ -85,7 +85,7 @@ def test_gate_power_ties_and_pulses_with_debug_arrays(glp, banded):
 
 def test_gate_power_skewed_with_big_gates(glp):
     # heavy gates: narrow windows in the banded layout, and gates with more
-    # than 7 events of a pin in one cycle streamed by the unbanded kernel in
+    # than 15 events of a pin in one cycle streamed by the unbanded kernel in
     # the same run
     w = synth.custom(seed=23, n_gates=40, n_cells=8, k_mode=1, n_slew=6, n_load=6, n_cycles=24,
                      t_clk_ns=1.0, n_events=60000, pair_frac=0.1, quantum_ns=0.001, threads=4)
