@@ -44,7 +44,8 @@ class OrPar(ctypes.Structure):
     _fields_ = [("vdd", ctypes.c_double), ("t_clk", ctypes.c_float), ("n_cycles", ctypes.c_uint32),
                 ("t_max", ctypes.c_double), ("wave_mode", ctypes.c_int32), ("sample_cycles", _vp),
                 ("n_sample", ctypes.c_uint32), ("gate_begin", ctypes.c_uint64),
-                ("gate_end", ctypes.c_uint64), ("threads", ctypes.c_int32)]
+                ("gate_end", ctypes.c_uint64), ("threads", ctypes.c_int32), ("glitch_mode", ctypes.c_int32),
+                ("esw_mode", ctypes.c_int32)]
 
 
 class OrOut(ctypes.Structure):
@@ -90,7 +91,8 @@ def _c(a, dtype):
 
 
 def run(w, *, vdd=None, t_clk=None, n_cycles=None, t_max=0.0, wave="full", sample_cycles=None,
-        gate_range=None, threads=1, debug=False, use_value=True, gate_power=False):
+        gate_range=None, threads=1, debug=False, use_value=True, gate_power=False, glitch_mode=0,
+        esw_mode=0):
     """Run the oracle on workload-like object ``w`` (attributes as in ``synth.Workload``).
 
     Returns a dict: ``p_int, p_sw, p_gl, p_leak`` (W), ``e_*`` (fJ), ``t_max``
@@ -127,7 +129,7 @@ def run(w, *, vdd=None, t_clk=None, n_cycles=None, t_max=0.0, wave="full", sampl
         sc = np.ascontiguousarray(sample_cycles, dtype=np.uint32)
         keep.append(sc)
     par = OrPar(float(vdd), float(t_clk), int(n_cycles), float(t_max), mode, _p(sc),
-                0 if sc is None else len(sc), int(g0), int(g1), int(threads))
+                0 if sc is None else len(sc), int(g0), int(g1), int(threads), int(glitch_mode), int(esw_mode))
     out = OrOut()
     res = {}
     nb = n_cycles if mode == WAVE_FULL else (len(sc) if mode == WAVE_SAMPLE else 0)

@@ -36,6 +36,13 @@
  *   Glitch:  counter reading -- the first event of a pin in a cycle is regular,
  *            the second and later are glitches; a glitch contributes only
  *            r_gl * (E_int + E_sw), to the glitch total and to its cycle bin.
+ *            Alternative (glitch_mode 1, the other reading of the per-cycle
+ *            glitch definition): every event of a pin-cycle holding two or
+ *            more events is a glitch; the first one's pulse is the one it
+ *            opens (width and slew of the next event on the pin).
+ *   Eq. 1 alternative (esw_mode 1): C * V^2 on a rising output transition,
+ *            nothing on a falling one (the supply charges the load once per
+ *            rise; the same total over a rise/fall pair).
  *   Events:  input-pin events carry E_int only, output-pin events E_sw only;
  *            the gate state is the vector of input-pin values.
  *   Cycle:   c = floor(fl32(t / T)) with IEEE fp32 round-to-nearest division.
@@ -230,14 +237,26 @@ static void run_gate1(const ctx_t *X, acc_t *A, uint64_t g) {
       int li = 0, lj = 0;
       if (p < k) {
         e_int = bilerp(lut + (size_t)S * ns * nl, ns, nl, sax, lax, s, C, &li, &lj);
-      } else {
+      } else if (X->par->esw_mode == 0) {
         e_sw = 0.5 * (double)C * vdd * vdd;
+      } else {
+        /* new value of the output: given, else toggling from its initial value */
+        const unsigned v = E->value ? (unsigned)(E->value[e] & 1)
+                                    : ((unsigned)N->init_out[g] ^ (unsigned)((e - E->pin_off[pb + p] + 1) & 1));
+        e_sw = v ? (double)C * vdd * vdd : 0.0;
       }
       const double e_dyn = e_int + e_sw;
-      const int glitch = cnt[p] > 1;
+      /* the pin's next event, if it lies in the same cycle (glitch_mode 1) */
+      const int next_same = X->par->glitch_mode == 1 && e + 1 < end[p] &&
+                            (int64_t)floorf(E->t[e + 1] / Tf) == ce;
+      const int glitch = cnt[p] > 1 || (cnt[p] == 1 && next_same);
       if (glitch) {
-        const double pw_ps = (t - last_t[p]) * 1000.0;
-        const double avg_slew = ((double)s + (double)last_s[p]) * 0.5;
+        /* the pulse: the previous edge on the pin in this cycle, else the next */
+        const int prev = cnt[p] > 1;
+        const double t_o = prev ? last_t[p] : (double)E->t[e + 1];
+        const float s_o = prev ? last_s[p] : E->slew[e + 1];
+        const double pw_ps = (prev ? t - t_o : t_o - t) * 1000.0;
+        const double avg_slew = ((double)s + (double)s_o) * 0.5;
         double r = pw_ps / avg_slew;
         if (r > 1.0) r = 1.0;
         A->e_gl += r * e_dyn;

@@ -49,6 +49,10 @@ typedef struct or_par {
   uint32_t n_sample;
   uint64_t gate_begin, gate_end; /* gates to walk */
   int32_t threads;
+  int32_t glitch_mode;           /* 0: counter reading (2nd and later events of a pin in a
+                                    cycle); 1: every event of a pin-cycle with 2+ events */
+  int32_t esw_mode;              /* 0: C V^2 / 2 per output transition; 1: C V^2 on a rising
+                                    output transition, 0 on a falling one */
 } or_par;
 
 typedef struct or_out {

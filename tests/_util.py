@@ -61,14 +61,16 @@ def values_of(w):
     return v
 
 
-def brute_force(w, vdd=None, t_clk=None, n_cycles=None, t_max=0.0):
+def brute_force(w, vdd=None, t_clk=None, n_cycles=None, t_max=0.0, glitch_mode=0, esw_mode=0):
     """A second, structurally different fp64 formulation for tiny workloads.
 
     Instead of a k-way merge it evaluates the gate state as a function of time
     ("value of the last event at or before tau" per input pin), integrates
     leakage piecewise over the union of event times and cycle boundaries, and
     classifies each event by counting the earlier events of its pin in its
-    cycle. O(E^2); for a handful of gates only.
+    cycle. O(E^2); for a handful of gates only. glitch_mode 1: every event of
+    a pin-cycle with two or more events is a glitch (the first takes the pulse
+    to the next event); esw_mode 1: C V^2 per rising output edge only.
     """
     vdd = w.vdd if vdd is None else vdd
     Tf = np.float32(w.t_clk_ns if t_clk is None else t_clk)
@@ -113,9 +115,10 @@ def brute_force(w, vdd=None, t_clk=None, n_cycles=None, t_max=0.0):
             for n, (t, s, val, idx) in enumerate(pins[q]):
                 c = int(math.floor(np.float32(t) / Tf))
                 S = state(t, inclusive=False)
-                earlier_same_cycle = sum(1 for (t2, *_r) in pins[q][:n]
-                                         if int(math.floor(np.float32(t2) / Tf)) == c)
-                glitch = earlier_same_cycle >= 1
+                same_cycle = [m for m, (t2, *_r) in enumerate(pins[q])
+                              if int(math.floor(np.float32(t2) / Tf)) == c]
+                earlier_same_cycle = sum(1 for m in same_cycle if m < n)
+                glitch = earlier_same_cycle >= 1 or (glitch_mode == 1 and len(same_cycle) >= 2)
                 out["evcount"][c] += 1
                 if q < k:
                     i = max([m for m in range(ns - 1) if sax[m] <= s] + [0])
@@ -126,13 +129,19 @@ def brute_force(w, vdd=None, t_clk=None, n_cycles=None, t_max=0.0):
                     e_sw = 0.0
                     out["lut_ij"][idx] = (i << 4) | j
                 else:
-                    e_int, e_sw = 0.0, 0.5 * C * vdd * vdd
+                    e_int = 0.0
+                    e_sw = 0.5 * C * vdd * vdd if esw_mode == 0 else (C * vdd * vdd if val == 1 else 0.0)
                     out["lut_ij"][idx] = 0xFF
                 out["state_pre"][idx] = S
                 out["is_glitch"][idx] = int(glitch)
                 if glitch:
-                    tp, sp = pins[q][n - 1][0], pins[q][n - 1][1]
-                    r = min(1.0, (t - tp) * 1000.0 / ((s + sp) / 2.0))
+                    if earlier_same_cycle >= 1:
+                        tp, sp = pins[q][n - 1][0], pins[q][n - 1][1]
+                        pw = t - tp
+                    else:  # the first edge of the cycle: the pulse to the next event
+                        tp, sp = pins[q][n + 1][0], pins[q][n + 1][1]
+                        pw = tp - t
+                    r = min(1.0, pw * 1000.0 / ((s + sp) / 2.0))
                     out["e_gl"] += r * (e_int + e_sw)
                     out["wave_energy"][c] += r * (e_int + e_sw)
                     out["glcount"][c] += 1

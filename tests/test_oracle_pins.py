@@ -120,6 +120,44 @@ def test_glitch_ratio_exact_and_saturation():
     assert r["e_gl"] == 0.0 and r["e_sw"] == pytest.approx(2 * esw)
 
 
+@pytest.mark.parametrize("n,init_out", [(1, 0), (2, 0), (5, 0), (5, 1), (4, 1)])
+def test_rise_only_switching_closed_form(n, init_out):
+    # Eq. 1 alternative: C V^2 per rising output transition, none per falling;
+    # n toggles from init_out rise ceil(n/2) (from 0) or floor(n/2) (from 1) times
+    C, V = 7.0, 0.8
+    evs = [(c + 0.25, 20.0) for c in range(n)]
+    w = _one_gate(1, leak=[0.0, 0.0], lut_const=[0, 0], C=C, vdd=V, init_out=init_out, events=([], evs),
+                  n_cycles=8)
+    rises = (n + 1) // 2 if init_out == 0 else n // 2
+    for use_value in (True, False):
+        r = oracle.run(w, esw_mode=1, use_value=use_value)
+        assert r["p_sw"] == pytest.approx(rises * C * V * V / 8 * 1e-6, rel=1e-14, abs=1e-30)
+    # and the totals over a rise/fall pair equal the default reading's
+    w2 = _one_gate(1, leak=[0.0, 0.0], lut_const=[0, 0], C=C, vdd=V, events=([], [(0.25, 20.0), (1.25, 20.0)]),
+                   n_cycles=8)
+    assert oracle.run(w2, esw_mode=1)["p_sw"] == pytest.approx(oracle.run(w2)["p_sw"], rel=1e-14)
+
+
+@pytest.mark.parametrize("n", [2, 3, 6])
+def test_glitch_all_mode_marks_every_event_of_a_multi_event_cycle(n):
+    evs = [(2.0 + 0.1 * i, 50.0) for i in range(n)] + [(3.5, 50.0)]
+    w = _one_gate(1, leak=[0.0, 0.0], lut_const=[0, 0], C=4.0, events=([], evs), n_cycles=5)
+    r = oracle.run(w, debug=True, glitch_mode=1)
+    assert r["glcount"][2] == n and r["glcount"][3] == 0 and r["evcount"].sum() == n + 1
+    np.testing.assert_array_equal(r["is_glitch"], [1] * n + [0])
+
+
+def test_glitch_all_mode_ratio_of_the_first_edge():
+    # the first event of the cycle takes the pulse it opens: width to the next
+    # event, slews of both; pw = 31.25 ps, slews 40 / 85 -> r = 0.5 for both edges
+    C, V = 4.0, 1.0
+    esw = 0.5 * C * V * V
+    w = _one_gate(1, leak=[0.0, 0.0], lut_const=[0, 0], C=C, vdd=V,
+                  events=([], [(1.5, 40.0), (1.53125, 85.0)]), n_cycles=4)
+    r = oracle.run(w, glitch_mode=1)
+    assert r["e_gl"] == pytest.approx(2 * 0.5 * esw, rel=1e-14) and r["e_sw"] == 0.0
+
+
 def test_bilinear_reproduces_plane_inside_and_outside_axes():
     # a bilinear surface a + b s + c l + d s l is reproduced exactly by bilinear
     # interpolation on any grid, also when extrapolating (slew/load transposed fails)
@@ -259,6 +297,20 @@ def test_stress_waveform_counts_closed_form(m):
     assert (r["p_gl"] > 0) == (m > 1)
     e_tot = r["e_int"] + r["e_sw"] + r["e_gl"] + r["e_leak"]
     assert float(r["wave_energy"].sum()) == pytest.approx(e_tot, rel=1e-12)
+
+
+@pytest.mark.parametrize("seed,quantum,k_mode,glitch_mode,esw_mode", [
+    (2, 0.25, 1, 1, 0), (3, 0.125, 2, 0, 1), (7, 0.05, 1, 1, 1),
+])
+def test_oracle_modes_match_brute_force(seed, quantum, k_mode, glitch_mode, esw_mode):
+    w = _tiny_random(seed, quantum, k_mode=k_mode)
+    r = oracle.run(w, debug=True, glitch_mode=glitch_mode, esw_mode=esw_mode)
+    b = brute_force(w, glitch_mode=glitch_mode, esw_mode=esw_mode)
+    for key in ("p_int", "p_sw", "p_gl", "p_leak"):
+        assert r[key] == pytest.approx(b[key], rel=1e-11, abs=1e-22), key
+    np.testing.assert_array_equal(r["glcount"], b["glcount"])
+    np.testing.assert_array_equal(r["is_glitch"].astype(np.int64), b["is_glitch"])
+    assert b["glcount"].sum() > 0
 
 
 def test_brute_force_ties_are_exercised():
