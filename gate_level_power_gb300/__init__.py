@@ -22,7 +22,7 @@ PA_OK = 0
 PA_ERR_ARG, PA_ERR_ORDER, PA_ERR_UNSORTED, PA_ERR_RANGE = -1, -2, -3, -4
 PA_ERR_TOGGLE, PA_ERR_OOM, PA_ERR_CUDA, PA_ERR_INTERNAL = -5, -6, -7, -8
 PA_MEM_HOST, PA_MEM_DEVICE = 0, 1
-PA_RUN_TIMING = 1
+PA_RUN_TIMING, PA_RUN_GLITCH_ALL, PA_RUN_ESW_RISE = 1, 2, 4
 
 ERR_NAMES = {0: "PA_OK", -1: "PA_ERR_ARG", -2: "PA_ERR_ORDER", -3: "PA_ERR_UNSORTED", -4: "PA_ERR_RANGE",
              -5: "PA_ERR_TOGGLE", -6: "PA_ERR_OOM", -7: "PA_ERR_CUDA", -8: "PA_ERR_INTERNAL"}
@@ -254,17 +254,21 @@ class PowerAnalyzer:
         self.load_events(w.pin_off, w.t_ns, w.slew_ps, w.value if with_value else None)
 
     def run(self, vdd, t_clk_ns, n_cycles, t_max_ns=0.0, tile_events=0, heavy_events=0, timing=False,
-            waveform=True, counts=True, debug=False, gate_power=False, out=None):
+            waveform=True, counts=True, debug=False, gate_power=False, glitch_all=False, esw_rise=False,
+            out=None):
         """Run the power computation. Returns a dict with ``p_int, p_sw, p_gl,
         p_leak`` (W), ``t_max`` and, as requested, ``waveform`` (f32 W per
         cycle), ``event_count``/``glitch_count`` (u32 per cycle), per-event
         ``state_pre``/``lut_ij``/``is_glitch`` (u8), per-gate ``gate_power``
         (f64 W, [gates, 4]: internal, switching, glitch, leakage), and ``ms_*``
-        timings.
+        timings. ``glitch_all`` / ``esw_rise`` select the alternative readings
+        (PA_RUN_GLITCH_ALL / PA_RUN_ESW_RISE).
         ``out`` may hold preallocated arrays (numpy or CUDA tensors) under the
         same names; CUDA tensors select device output."""
+        flags = ((PA_RUN_TIMING if timing else 0) | (PA_RUN_GLITCH_ALL if glitch_all else 0)
+                 | (PA_RUN_ESW_RISE if esw_rise else 0))
         p = PaRunParams(float(vdd), float(t_clk_ns), int(n_cycles), float(t_max_ns), int(tile_events),
-                        int(heavy_events), PA_RUN_TIMING if timing else 0)
+                        int(heavy_events), flags)
         r = PaResult()
         res = {}
         out = dict(out or {})

@@ -175,7 +175,7 @@ struct RunPlan {
   float T = 0.f;
   double Td = 0.0, t_max = 0.0;
   uint32_t tile = 0, heavy = 0, N = 0, G = 0, nblk = 0;
-  bool pow2 = false, debug = false, timing = false, gate = false;
+  bool pow2 = false, debug = false, timing = false, gate = false, glitch_all = false, esw_rise = false;
   double vdd = 0.0;
 };
 
@@ -227,6 +227,12 @@ int check_run(pa_ctx* c, const pa_run_params* prm, const pa_result* out, const c
   plan->gate = out->gate_power_w != nullptr;
   plan->debug = out->state_pre || out->lut_ij || out->is_glitch || plan->gate;
   plan->timing = (prm->flags & PA_RUN_TIMING) != 0;
+  plan->glitch_all = (prm->flags & PA_RUN_GLITCH_ALL) != 0;
+  plan->esw_rise = (prm->flags & PA_RUN_ESW_RISE) != 0;
+  // the alternative readings are ablations: they run in the per-event path
+  if (plan->glitch_all || plan->esw_rise) plan->debug = true;
+  if (prm->flags & ~(PA_RUN_TIMING | PA_RUN_GLITCH_ALL | PA_RUN_ESW_RISE))
+    return fail(c, PA_ERR_ARG, "%s: unknown flags 0x%x", who, prm->flags);
   plan->pow2 = is_pow2(plan->T);
   plan->vdd = prm->vdd;
   return PA_OK;
@@ -258,6 +264,8 @@ int run_pass(pa_ctx* c, const RunPlan& plan, const PassBufs& B, pa_result* out, 
   a.inv_t_clk = plan.pow2 ? 1.0f / plan.T : 0.f;
   a.t_max_f = (float)plan.t_max;
   a.half_vdd2 = (float)(0.5 * plan.vdd * plan.vdd);
+  a.glitch_all = plan.glitch_all ? 1u : 0u;
+  a.esw_rise = plan.esw_rise ? 1u : 0u;
   a.n_cycles = N;
   a.tile_target = plan.tile;
   a.heavy_thresh = plan.heavy;

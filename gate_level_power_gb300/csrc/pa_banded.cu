@@ -190,6 +190,7 @@ __global__ void __launch_bounds__(256) k_bw_walk(const BandBuildArgs a) {
       cy[p] = (uint32_t)lane < hi[p] ? bcyc(a, a.t[lo[p] + lane]) : kNoCycle;
     }
     uint32_t state = r.init & ((1u << k) - 1u);  // input state at the window start
+    uint32_t oval = (r.init >> 8) & 1u;          // output value at the window start
     uint32_t band = kNoCycle, units = 0, events = 0, max_unit = 0;
     uint64_t u = 0, dst = 0;  // next unit / banded event of this (band, gate)
     bool big = false, split = false;
@@ -249,7 +250,8 @@ __global__ void __launch_bounds__(256) k_bw_walk(const BandBuildArgs a) {
 #pragma unroll
             for (int p = 0; p < P; ++p) x |= n[p] << (4 * p);
             x |= state << 20;
-            x |= (r.cell & 0xffu) << 24;
+            x |= (r.cell & 63u) << 24;
+            x |= oval << 30;
             a.urec2[u] = make_uint2(x, __float_as_uint(r.load));
             a.L.ugate[u] = (uint32_t)g;
             a.uband[u] = band;
@@ -274,6 +276,7 @@ __global__ void __launch_bounds__(256) k_bw_walk(const BandBuildArgs a) {
 #pragma unroll
       for (int p = 0; p < P; ++p) {
         if (p < k) state ^= (n[p] & 1u) << p;
+        if (p == k) oval ^= n[p] & 1u;
         j[p] += n[p];
         if (j[p] - cb[p] > 16u && j[p] < hi[p]) {  // keep 16 events of lookahead inside the chunk
           cb[p] = j[p];
@@ -410,7 +413,7 @@ __global__ void __launch_bounds__(kFinWarps * 32) k_bw_finalize(const BandBuildA
       uint32_t pk = 0, n_in = 0, x = 0, y = 0;
       if (uu < nu) {
         x = a.urec2[u0 + uu].x;
-        const uint32_t k = a.cells[x >> 24].k;
+        const uint32_t k = a.cells[(x >> 24) & 63u].k;
         uint32_t s = 0;
 #pragma unroll
         for (int p = 0; p < kMaxK; ++p) {
@@ -421,6 +424,7 @@ __global__ void __launch_bounds__(kFinWarps * 32) k_bw_finalize(const BandBuildA
           y |= s << (8 * p);
         }
         y |= (k - 1u) << 30;
+        y |= ((x >> 30) & 1u) << 6;  // output value at the window start
         n_in = s;
         const uint32_t n_out = (x >> (4 * k)) & 15u;
         pk = (n_in + n_out) | (n_in << 10) | (n_out << 20);
@@ -485,7 +489,7 @@ __global__ void __launch_bounds__(kFinWarps * 32) k_bw_finalize(const BandBuildA
       const int uu = lane + 32 * r;
       if (uu < nu) {
         const uint2 w = a.urec2[u0 + uu];
-        const uint32_t cell = w.x >> 24;
+        const uint32_t cell = (w.x >> 24) & 63u;
         const CellDesc& cd = a.cells[cell];
         const float C = __uint_as_float(w.y);
         int j = 0;
@@ -859,14 +863,27 @@ struct EvDbg {
 // Glitch test against the pin's previous event (staged index e - 1 if idx > 0;
 // for idx == 0 the event itself, unused) and scaling of the dynamic energy;
 // no branches, since on dense pins most warps hold a glitch somewhere.
-template <bool kPow2>
+// has_next: the pin's next event is staged at e + 1 (only asked for in the
+// glitch-all reading, where the first event of a multi-event pin-cycle takes
+// the pulse to that next event).
+template <bool kPow2, bool kDebug>
 __device__ __forceinline__ float glitch_scale(const RunArgs& a, const float* ts, const float* gs, int e, int idx,
-                                              float t, float s, uint32_t c, float e_dyn, bool& glitch) {
+                                              float t, float s, uint32_t c, float e_dyn, bool has_next,
+                                              bool& glitch) {
   const int ep = e - (idx > 0 ? 1 : 0);
-  const float tp = ts[ep];
-  const float sp = __ldg(gs + ep);
+  float tp = ts[ep];
+  float sp = __ldg(gs + ep);
   glitch = idx > 0 && cyc<kPow2>(tp, a.t_clk, a.inv_t_clk) == c;
-  const float r = fminf(1.f, __fdividef(2000.f * (t - tp), s + sp));
+  float pw = t - tp;
+  if (kDebug && a.glitch_all && !glitch && has_next) {  // the reading runs in the per-event path
+    const float tn = ts[e + 1];
+    if (cyc<kPow2>(tn, a.t_clk, a.inv_t_clk) == c) {
+      glitch = true;
+      pw = tn - t;
+      sp = __ldg(gs + e + 1);
+    }
+  }
+  const float r = fminf(1.f, __fdividef(2000.f * pw, s + sp));
   return glitch ? r * e_dyn : e_dyn;
 }
 
@@ -928,7 +945,8 @@ __device__ __forceinline__ EvOut ev_input(const RunArgs& a, const CellTab& CT, c
   const float T = a.t_clk;
   const uint32_t c = cyc<kPow2>(t, T, a.inv_t_clk);
   bool glitch;
-  float e_w = glitch_scale<kPow2>(a, ts, gs, i, idx, t, s, c, e_int, glitch);
+  const bool has_next = kDebug && a.glitch_all && idx + 1 < pin_start(y, p + 1) - pin_start(y, p);
+  float e_w = glitch_scale<kPow2, kDebug>(a, ts, gs, i, idx, t, s, c, e_int, has_next, glitch);
   if (valid) {
     acc.e_gl += glitch ? e_w : 0.f;
     acc.e_int += glitch ? 0.f : e_int;
@@ -945,17 +963,20 @@ __device__ __forceinline__ EvOut ev_input(const RunArgs& a, const CellTab& CT, c
 // Output-pin event at staged index i: switching energy, glitch, totals.
 template <bool kPow2, bool kDebug>
 __device__ __forceinline__ EvOut ev_output(const RunArgs& a, const float* ts, const uint8_t* tg, const uint4* rec,
-                                           const float* gs, int i, uint32_t steps, bool valid, BAcc& acc,
+                                           const float* gs, int i, int n, uint32_t steps, bool valid, BAcc& acc,
                                            EvDbg& dbg) {
   const uint32_t tag = tg[i];
   const uint4 R = rec[tag & 63u];
   const float t = ts[i];
   const float s = __ldg(gs + i);  // only a glitch ratio uses it
   const int idx = i - (int)((R.x >> 9) & 511u);
-  const float e_sw = a.half_vdd2 * __uint_as_float(R.w);
+  float e_sw = a.half_vdd2 * __uint_as_float(R.w);
+  if (kDebug && a.esw_rise)  // C V^2 on a rise: the output's value at the window start, flipped per earlier event
+    e_sw = ((((R.y >> 6) & 1u) ^ ((uint32_t)(idx + 1) & 1u)) != 0u) ? 2.f * e_sw : 0.f;
   const uint32_t c = cyc<kPow2>(t, a.t_clk, a.inv_t_clk);
   bool glitch;
-  const float e_w = glitch_scale<kPow2>(a, ts, gs, i, idx, t, s, c, e_sw, glitch);
+  const bool has_next = kDebug && a.glitch_all && i + 1 < n && (tg[i + 1] & 63u) == (tag & 63u);
+  const float e_w = glitch_scale<kPow2, kDebug>(a, ts, gs, i, idx, t, s, c, e_sw, has_next, glitch);
   if (valid) {
     acc.e_gl += glitch ? e_w : 0.f;
     acc.e_sw += glitch ? 0.f : e_sw;
@@ -1053,7 +1074,7 @@ __device__ __forceinline__ void band_item(const BandRunArgs& A, const CellTab& C
   if (kDebug) {
     for (int i = lane; i < n; i += 32) {
       const EvOut o = i < n_in ? ev_input<kPow2, true, true>(a, CT, ts, tg, rec, gs, i, steps, true, acc, d0)
-                               : ev_output<kPow2, true>(a, ts, tg, rec, gs, i, steps, true, acc, d0);
+                               : ev_output<kPow2, true>(a, ts, tg, rec, gs, i, n, steps, true, acc, d0);
       ev_commit<kExact>(A, hist, o, item, c0);
       const uint32_t gate = A.L.ugate[g.u0 + d0.unit];
       if (a.gate_e) {  // this event's share of its gate's energies
@@ -1085,12 +1106,12 @@ __device__ __forceinline__ void band_item(const BandRunArgs& A, const CellTab& C
       const int i0 = base + lane;
       if (base + 32 < n) {
         const int i1 = i0 + 32;
-        const EvOut o0 = ev_output<kPow2, false>(a, ts, tg, rec, gs, i0, steps, true, acc, d0);
-        const EvOut o1 = ev_output<kPow2, false>(a, ts, tg, rec, gs, min(i1, n - 1), steps, i1 < n, acc, d1);
+        const EvOut o0 = ev_output<kPow2, false>(a, ts, tg, rec, gs, i0, n, steps, true, acc, d0);
+        const EvOut o1 = ev_output<kPow2, false>(a, ts, tg, rec, gs, min(i1, n - 1), n, steps, i1 < n, acc, d1);
         ev_commit<kExact>(A, hist, o0, item, c0);
         if (i1 < n) ev_commit<kExact>(A, hist, o1, item, c0);
       } else if (i0 < n) {
-        ev_commit<kExact>(A, hist, ev_output<kPow2, false>(a, ts, tg, rec, gs, i0, steps, true, acc, d0), item, c0);
+        ev_commit<kExact>(A, hist, ev_output<kPow2, false>(a, ts, tg, rec, gs, i0, n, steps, true, acc, d0), item, c0);
       }
     }
   }

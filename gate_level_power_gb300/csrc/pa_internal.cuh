@@ -95,6 +95,8 @@ struct RunArgs {
   float t_clk, inv_t_clk;
   float t_max_f;           // window end as f32 (for per-event leakage spans)
   float half_vdd2;         // 0.5 * V^2
+  uint32_t glitch_all;     // PA_RUN_GLITCH_ALL: every event of a multi-event pin-cycle is a glitch
+  uint32_t esw_rise;       // PA_RUN_ESW_RISE: C V^2 on a rising output edge, 0 on a falling one
   uint32_t n_cycles;
   uint32_t tile_target, heavy_thresh;
   // partition
@@ -172,8 +174,10 @@ constexpr uint32_t kItemStepShift = 29;
 //   y: start of input pins 1, 2, 3 and the end of the inputs, one byte each
 //      (pins beyond k start at the end), | (k - 1) << 30
 //   z: load-axis fraction v (f32), w: load C (f32, fF)
+//   y also holds, in bit 6, the output pin's value at the window start.
 // Unit record of the walk (uint2, a build temporary): x = counts of pins 0..4
-// (4 bits each) | start state << 20 | cell << 24, y = load (f32 bits).
+// (4 bits each) | start state << 20 | cell << 24 (6 bits) | output value at
+// the window start << 30, y = load (f32 bits).
 // Event tag (u8): unit within the item (bits 0..5) | input pin (bits 6..7).
 struct BandItem {
   uint64_t e0;    // first event in the banded arrays

@@ -352,13 +352,30 @@ __device__ __forceinline__ void do_event(const RunArgs& a, const float* __restri
     tp = ts[e - 1];
     sp = ss[e - 1];
   }
-  const bool glitch = has_prev && cycle_of<kPow2>(tp, a.t_clk, a.inv_t_clk) == c;
+  bool glitch = has_prev && cycle_of<kPow2>(tp, a.t_clk, a.inv_t_clk) == c;
+  bool fwd = false;  // glitch-all reading: the first event of a pin-cycle takes the pulse to the next
+  if (kDebug && a.glitch_all && !glitch) {  // the alternative readings run in the per-event path
+    const GateRec gr = a.gates[S.gate];
+    if (gidx + 1 < a.pin_off[(uint64_t)gr.pin_base + p + 1]) {
+      const float tn = a.t[gidx + 1];
+      if (cycle_of<kPow2>(tn, a.t_clk, a.inv_t_clk) == c) {
+        glitch = fwd = true;
+        tp = tn;
+        sp = a.s[gidx + 1];
+      }
+    }
+  }
   const int k = S.k;
   float e_int = 0.f, e_sw = 0.f, dp = 0.f;
   uint32_t s_pre = 0;
   int li = 0;
   if (p == k) {
     e_sw = S.esw;
+    if (kDebug && a.esw_rise) {  // C V^2 on a rise: the output's new value from its initial one and its rank
+      const GateRec gr = a.gates[S.gate];
+      const uint64_t rank = gidx - a.pin_off[(uint64_t)gr.pin_base + k];
+      e_sw = ((((gr.init >> 8) & 1u) ^ (uint32_t)((rank + 1) & 1u)) != 0u) ? 2.f * S.esw : 0.f;
+    }
     if (kDebug) s_pre = state_before(ts, S, t);
   } else {
     const CellDesc& cd = cells[S.cell];
@@ -388,7 +405,7 @@ __device__ __forceinline__ void do_event(const RunArgs& a, const float* __restri
   const float e_dyn = e_int + e_sw;
   float e_w;
   if (glitch) {
-    const float r = fminf(1.f, 2000.f * (t - tp) / (s + sp));
+    const float r = fminf(1.f, 2000.f * (fwd ? tp - t : t - tp) / (s + sp));
     e_w = r * e_dyn;
     acc.e_gl += e_w;
   } else {

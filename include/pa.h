@@ -143,6 +143,16 @@ typedef struct pa_events {
 } pa_events;
 
 #define PA_RUN_TIMING 1u /* record per-kernel CUDA-event times in pa_result */
+/* Alternative readings of the paper's stripped definitions (ablations; the
+ * defaults are the readings listed at the top of this header):
+ *   PA_RUN_GLITCH_ALL  every event of a pin-cycle holding two or more events
+ *                      is a glitch; the first one takes the pulse it opens
+ *                      (width and slew of the pin's next event);
+ *   PA_RUN_ESW_RISE    switching energy C * V^2 on a rising output transition
+ *                      and none on a falling one (Eq. 1 read per charge).
+ * Either flag selects the slower per-event path (as debug outputs do). */
+#define PA_RUN_GLITCH_ALL 2u
+#define PA_RUN_ESW_RISE 4u
 
 /*
  * Run parameters. pa_default_params() fills the defaults.
