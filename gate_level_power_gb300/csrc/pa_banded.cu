@@ -872,8 +872,10 @@ __device__ __forceinline__ float glitch_scale(const RunArgs& a, const float* ts,
                                               bool& glitch) {
   const int ep = e - (idx > 0 ? 1 : 0);
   float tp = ts[ep];
-  float sp = __ldg(gs + ep);
   glitch = idx > 0 && cyc<kPow2>(tp, a.t_clk, a.inv_t_clk) == c;
+  // the previous edge's slew only for glitches (a predicated load: only those lanes touch L1)
+  float sp = s;
+  if (glitch) sp = __ldg(gs + ep);
   float pw = t - tp;
   if (kDebug && a.glitch_all && !glitch && has_next) {  // the reading runs in the per-event path
     const float tn = ts[e + 1];
@@ -968,8 +970,11 @@ __device__ __forceinline__ EvOut ev_output(const RunArgs& a, const float* ts, co
   const uint32_t tag = tg[i];
   const uint4 R = rec[tag & 63u];
   const float t = ts[i];
-  const float s = __ldg(gs + i);  // only a glitch ratio uses it
   const int idx = i - (int)((R.x >> 9) & 511u);
+  // the slew only enters a glitch ratio: loaded for lanes whose previous event
+  // is on the pin (or, in the glitch-all reading, for every lane)
+  float s = 0.f;
+  if (idx > 0 || (kDebug && a.glitch_all)) s = __ldg(gs + i);
   float e_sw = a.half_vdd2 * __uint_as_float(R.w);
   if (kDebug && a.esw_rise)  // C V^2 on a rise: the output's value at the window start, flipped per earlier event
     e_sw = ((((R.y >> 6) & 1u) ^ ((uint32_t)(idx + 1) & 1u)) != 0u) ? 2.f * e_sw : 0.f;
