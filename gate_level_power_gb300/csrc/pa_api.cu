@@ -63,7 +63,7 @@ struct pa_ctx {
   uint32_t band_windowed = 0;  // gates cut into windows narrower than a band
   DevBuf b_bt, b_bs, b_btag, b_urec, b_ugate, b_items, b_big;
   DevBuf b_bigf, b_grank, b_cnt, b_evc, b_ubase, b_ebase, b_uband, b_uoff, b_flags, b_ipos, b_scan, b_counters,
-      b_urec2;
+      b_urec2, b_dense, b_gflag;
   DevBuf b_part;
   DevBuf scratch_small;
 };
@@ -444,7 +444,7 @@ void pa_destroy(pa_ctx* c) {
                    &c->chunk_sums, &c->b_bt, &c->b_bs, &c->b_btag, &c->b_urec, &c->b_ugate, &c->b_items,
                    &c->b_big, &c->b_bigf, &c->b_grank, &c->b_cnt, &c->b_evc, &c->b_ubase, &c->b_ebase,
                    &c->b_uband, &c->b_uoff, &c->b_flags, &c->b_ipos, &c->b_scan, &c->b_counters,
-                   &c->b_urec2, &c->b_part};
+                   &c->b_urec2, &c->b_dense, &c->b_gflag, &c->b_part};
   for (DevBuf* b : all) dfree(*b);
   for (auto& e : c->ev)
     if (e) cudaEventDestroy(e);
@@ -797,7 +797,8 @@ int check_build_err(pa_ctx* c) {
 
 void free_build_temps(pa_ctx* c) {
   DevBuf* tmp[] = {&c->b_bigf, &c->b_grank, &c->b_cnt, &c->b_evc, &c->b_ubase, &c->b_ebase, &c->b_uband,
-                   &c->b_uoff, &c->b_flags, &c->b_ipos, &c->b_scan, &c->b_counters, &c->b_urec2};
+                   &c->b_uoff, &c->b_flags, &c->b_ipos, &c->b_scan, &c->b_counters, &c->b_urec2,
+                   &c->b_dense, &c->b_gflag};
   for (DevBuf* b : tmp) dfree(*b);
 }
 
@@ -836,6 +837,8 @@ int build_bands(pa_ctx* c, float t_clk, uint32_t cb) {
   PA_TRY(dreserve(c, c->b_big, ((size_t)G + 1) * sizeof(uint32_t)));
   PA_TRY(dreserve(c, c->b_counters, 4 * sizeof(uint32_t)));
   PA_TRY(dreserve(c, c->b_bigf, (size_t)G + 1));
+  PA_TRY(dreserve(c, c->b_dense, ((size_t)G + 1) * sizeof(uint32_t)));
+  PA_TRY(dreserve(c, c->b_gflag, (size_t)G + 1));
   PA_TRY(dreserve(c, c->b_grank, ((size_t)G + 1) * sizeof(uint32_t)));
   PA_TRY(dreserve(c, c->b_flags, ((size_t)G + 1) * sizeof(uint32_t)));
   PA_TRY(dreserve(c, c->b_ipos, ((size_t)G + 2) * sizeof(uint64_t)));
@@ -847,6 +850,8 @@ int build_bands(pa_ctx* c, float t_clk, uint32_t cb) {
   L.big = (uint32_t*)c->b_big.p;
   a.counters = (uint32_t*)c->b_counters.p;
   a.bigf = (uint8_t*)c->b_bigf.p;
+  a.dense = (uint32_t*)c->b_dense.p;
+  a.gflag = (uint8_t*)c->b_gflag.p;
   a.grank = (uint32_t*)c->b_grank.p;
   a.flags = (uint32_t*)c->b_flags.p;
   a.ipos = (uint64_t*)c->b_ipos.p;

@@ -154,15 +154,24 @@ __device__ __forceinline__ uint32_t bcyc(const BandBuildArgs& a, float t) {
 }
 
 constexpr uint32_t kNoCycle = 0xFFFFFFFFu;
+// Gates with more events than this are walked by warps, the others by a thread.
+constexpr uint64_t kDenseGate = 256;
+constexpr int kWalkSegs = 64;  // band segments per dense gate walked in parallel
 
-// kWrite false: units / events per (band, gate) and big gates; true: records,
-// unit offsets and the event copy. One warp per gate. Each pin keeps a chunk of
-// 32 consecutive events' cycles in the warp's lanes, refilled (one coalesced
+// Dense gates (more than kDenseGate events) are walked one warp per (gate,
+// segment of consecutive bands), up to kWalkSegs segments per gate: windows
+// never cross a band boundary, and the input state and output value at a
+// segment's start are the parities of each pin's earlier events, so the
+// segments of one gate are independent (a Zipf-hot gate's bands no longer
+// run one after another). kWrite false: units / events per (band, gate), big
+// gates flagged (cleared and listed by k_bw_dense_fix); true:
+// records, unit offsets and the event copy. Each pin keeps a chunk of 32
+// consecutive events' cycles in the warp's lanes, refilled (one coalesced
 // load) before its lookahead of 16 events would leave the chunk. One window
 // per step: it starts at the earliest next cycle of the pins and ends at the
-// band end or at the cycle of some pin's 16th event from its cursor, whichever
-// is first; each pin's count in the window is one ballot. This gives the same
-// windows as walking the gate's cycles one by one.
+// band end or at the cycle of some pin's (kUnitPinSoft + 1)-th event from its
+// cursor, whichever is first; each pin's count in the window is one ballot.
+// This gives the same windows as walking the gate's cycles one by one.
 template <bool kWrite>
 __global__ void __launch_bounds__(256) k_bw_walk(const BandBuildArgs a) {
   constexpr int P = kMaxK + 1;
@@ -170,27 +179,68 @@ __global__ void __launch_bounds__(256) k_bw_walk(const BandBuildArgs a) {
   const uint64_t warp = (blockIdx.x * (uint64_t)blockDim.x + threadIdx.x) >> 5;
   const uint64_t n_warps = ((uint64_t)gridDim.x * blockDim.x) >> 5;
   const uint64_t G = a.n_gates;
-  for (uint64_t g = warp; g < G; g += n_warps) {
+  const uint64_t NB = a.n_bands;
+  const uint64_t NS = NB < (uint64_t)kWalkSegs ? NB : (uint64_t)kWalkSegs;  // segments per gate
+  const uint64_t SB = (NB + NS - 1) / NS;                                       // bands per segment
+  const uint64_t n_work = (uint64_t)a.counters[3] * NS;
+  for (uint64_t w = warp; w < n_work; w += n_warps) {
+    const uint64_t g = a.dense[w / NS];
+    const uint64_t b0 = (w % NS) * SB, b1 = b0 + SB < NB ? b0 + SB : NB;
+    if (b0 >= b1) continue;
     if (kWrite && a.bigf[g]) continue;
-    const uint64_t gr = a.grank[g];  // the gate's place in the layout's gate order
     const GateRec r = a.gates[g];
     const int k = (int)((r.init >> 16) & 0xff);
+    const uint64_t gr = a.grank[g];  // the gate's place in the layout's gate order
+    const uint32_t c_lo = (uint32_t)(b0 << a.mb);
+    const uint64_t se = b1 << a.mb;
+    const uint32_t c_seg_end = se > 0xFFFFFFFFull ? 0xFFFFFFFFu : (uint32_t)se;
+    // lane p <= k: its pin's events of this segment, [first with cycle >= c_lo, first with cycle >= its end)
+    uint64_t my_lo = 0;
+    uint32_t my_j = 0, my_hi = 0;
+    if (lane <= k) {
+      my_lo = a.pin_off[(uint64_t)r.pin_base + lane];
+      const uint32_t n = (uint32_t)(a.pin_off[(uint64_t)r.pin_base + lane + 1] - my_lo);
+      uint32_t l = 0, m = n;
+      while (m > 0) {
+        const uint32_t h = m >> 1;
+        if (bcyc(a, a.t[my_lo + l + h]) < c_lo) {
+          l += h + 1;
+          m -= h + 1;
+        } else {
+          m = h;
+        }
+      }
+      my_j = l;
+      m = n - l;
+      while (m > 0) {
+        const uint32_t h = m >> 1;
+        if (bcyc(a, a.t[my_lo + l + h]) < c_seg_end) {
+          l += h + 1;
+          m -= h + 1;
+        } else {
+          m = h;
+        }
+      }
+      my_hi = l;
+    }
     uint64_t lo[P];
-    uint32_t hi[P], j[P], cb[P], cy[P];  // pin length, cursor, chunk base (relative to lo), lane's chunk cycle
+    uint32_t hi[P], j[P], cb[P], cy[P];  // segment end, cursor, chunk base (relative to lo), lane's chunk cycle
+    bool any = false;
 #pragma unroll
     for (int p = 0; p < P; ++p) {
-      lo[p] = 0;
-      hi[p] = 0;
-      j[p] = 0;
-      cb[p] = 0;
-      if (p <= k) {
-        lo[p] = a.pin_off[(uint64_t)r.pin_base + p];
-        hi[p] = (uint32_t)(a.pin_off[(uint64_t)r.pin_base + p + 1] - lo[p]);
-      }
-      cy[p] = (uint32_t)lane < hi[p] ? bcyc(a, a.t[lo[p] + lane]) : kNoCycle;
+      lo[p] = __shfl_sync(0xffffffffu, my_lo, p);
+      j[p] = __shfl_sync(0xffffffffu, my_j, p);
+      hi[p] = __shfl_sync(0xffffffffu, my_hi, p);
+      cb[p] = j[p];
+      any |= j[p] < hi[p];
+      cy[p] = j[p] + (uint32_t)lane < hi[p] ? bcyc(a, a.t[lo[p] + j[p] + lane]) : kNoCycle;
     }
-    uint32_t state = r.init & ((1u << k) - 1u);  // input state at the window start
-    uint32_t oval = (r.init >> 8) & 1u;          // output value at the window start
+    if (!any) continue;  // no event of this gate in this segment
+    uint32_t state = r.init & ((1u << k) - 1u);  // input state at the segment start
+#pragma unroll
+    for (int p = 0; p < kMaxK; ++p)
+      if (p < k) state ^= (j[p] & 1u) << p;
+    uint32_t oval = ((r.init >> 8) & 1u) ^ (j[k] & 1u);  // output value at the segment start
     uint32_t band = kNoCycle, units = 0, events = 0, max_unit = 0;
     uint64_t u = 0, dst = 0;  // next unit / banded event of this (band, gate)
     bool big = false, split = false;
@@ -216,8 +266,8 @@ __global__ void __launch_bounds__(256) k_bw_walk(const BandBuildArgs a) {
           dst = a.ebase[(uint64_t)b * G + gr];
         }
       }
-      const uint64_t be = ((uint64_t)b + 1) << a.mb;
-      const uint32_t c_band_end = be > 0xFFFFFFFFull ? 0xFFFFFFFFu : (uint32_t)be;
+      const uint64_t bend = ((uint64_t)b + 1) << a.mb;
+      const uint32_t c_band_end = bend > 0xFFFFFFFFull ? 0xFFFFFFFFu : (uint32_t)bend;
       uint32_t c_end = c_band_end, c_hard = c_band_end;
 #pragma unroll
       for (int p = 0; p < P; ++p) {
@@ -286,18 +336,182 @@ __global__ void __launch_bounds__(256) k_bw_walk(const BandBuildArgs a) {
       ++units;
       events += size;
     }
+    if (!kWrite && lane == 0) {
+      if (big) {
+        a.bigf[g] = 1;  // k_bw_dense_fix clears the gate's bands and lists it
+      } else {
+        if (band != kNoCycle) {
+          a.cnt_gb[(uint64_t)band * G + gr] = units;
+          a.evc_gb[(uint64_t)band * G + gr] = events;
+        }
+        if (split) a.gflag[g] = 1;
+        if (max_unit) atomicMax(a.counters + 2, max_unit);
+      }
+    }
+  }
+}
+
+int walk_grid(uint64_t n_gates) {
+  return (int)std::min<uint64_t>((n_gates * 32 + 255) / 256 + 1, 152ull * 64);
+}
+
+// The dense-gate list (counters[3] entries, any order); their flags cleared.
+__global__ void __launch_bounds__(256) k_bw_dense_list(const BandBuildArgs a) {
+  const uint64_t g = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (g >= a.n_gates) return;
+  const GateRec r = a.gates[g];
+  const uint32_t k = (r.init >> 16) & 0xffu;
+  if (a.pin_off[(uint64_t)r.pin_base + k + 1] - a.pin_off[r.pin_base] <= kDenseGate) return;
+  a.bigf[g] = 0;
+  a.gflag[g] = 0;
+  a.dense[atomicAdd(a.counters + 3, 1u)] = (uint32_t)g;
+}
+
+// After the dense counting walk: a dense gate with a too-dense cycle in any
+// band has none of its units kept (its bands cleared) and joins the list of
+// gates the unbanded kernel streams; the others with a window narrower than a
+// band are counted.
+__global__ void __launch_bounds__(256) k_bw_dense_fix(const BandBuildArgs a) {
+  const uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= a.counters[3]) return;
+  const uint32_t g = a.dense[i];
+  if (a.bigf[g]) {
+    const uint64_t gr = a.grank[g], G = a.n_gates;
+    for (uint32_t bb = 0; bb < a.n_bands; ++bb) {
+      a.cnt_gb[(uint64_t)bb * G + gr] = 0;
+      a.evc_gb[(uint64_t)bb * G + gr] = 0;
+    }
+    a.L.big[atomicAdd(a.counters, 1u)] = g;
+  } else if (a.gflag[g]) {
+    atomicAdd(a.counters + 1, 1u);
+  }
+}
+
+// The same walk for one sparse gate (at most kDenseGate events) by one thread:
+// each window's bounds and per-pin counts read the gate's few events directly
+// (they stay in L1 across its windows) instead of a warp's shuffles and
+// ballots, which for a handful of events per window idle most of the warp.
+// Produces exactly the windows, records and copies of k_bw_walk.
+
+template <bool kWrite>
+__global__ void __launch_bounds__(256) k_bw_walk_sparse(const BandBuildArgs a) {
+  constexpr int P = kMaxK + 1;
+  const uint64_t G = a.n_gates;
+  for (uint64_t g = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; g < G; g += (uint64_t)gridDim.x * blockDim.x) {
+    const GateRec r = a.gates[g];
+    const int k = (int)((r.init >> 16) & 0xff);
+    const uint64_t g_lo = a.pin_off[r.pin_base], g_hi = a.pin_off[(uint64_t)r.pin_base + k + 1];
+    if (g_hi - g_lo > kDenseGate) continue;  // dense gates: the warp walk
+    if (kWrite && a.bigf[g]) continue;
+    const uint64_t gr = a.grank[g];
+    uint64_t lo[P];
+    uint32_t hi[P], j[P];
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+      lo[p] = 0;
+      hi[p] = 0;
+      j[p] = 0;
+      if (p <= k) {
+        lo[p] = a.pin_off[(uint64_t)r.pin_base + p];
+        hi[p] = (uint32_t)(a.pin_off[(uint64_t)r.pin_base + p + 1] - lo[p]);
+      }
+    }
+    uint32_t state = r.init & ((1u << k) - 1u);
+    uint32_t oval = (r.init >> 8) & 1u;
+    uint32_t band = kNoCycle, units = 0, events = 0, max_unit = 0;
+    uint64_t u = 0, dst = 0;
+    bool big = false, split = false;
+    for (;;) {
+      uint32_t c_start = kNoCycle;
+#pragma unroll
+      for (int p = 0; p < P; ++p)
+        if (j[p] < hi[p]) c_start = min(c_start, bcyc(a, a.t[lo[p] + j[p]]));
+      if (c_start == kNoCycle) break;
+      const uint32_t b = c_start >> a.mb;
+      if (b != band) {
+        if (!kWrite && band != kNoCycle) {
+          a.cnt_gb[(uint64_t)band * G + gr] = units;
+          a.evc_gb[(uint64_t)band * G + gr] = events;
+        }
+        band = b;
+        units = 0;
+        events = 0;
+        if (kWrite) {
+          u = a.ubase[(uint64_t)b * G + gr];
+          dst = a.ebase[(uint64_t)b * G + gr];
+        }
+      }
+      const uint64_t be = ((uint64_t)b + 1) << a.mb;
+      const uint32_t c_band_end = be > 0xFFFFFFFFull ? 0xFFFFFFFFu : (uint32_t)be;
+      uint32_t c_end = c_band_end, c_hard = c_band_end;
+#pragma unroll
+      for (int p = 0; p < P; ++p) {
+        if (j[p] + kUnitPinSoft < hi[p]) c_end = min(c_end, bcyc(a, a.t[lo[p] + j[p] + kUnitPinSoft]));
+        if (j[p] + kUnitPinMax < hi[p]) c_hard = min(c_hard, bcyc(a, a.t[lo[p] + j[p] + kUnitPinMax]));
+      }
+      if (c_end <= c_start) {
+        if (c_hard <= c_start) {
+          big = true;
+          break;
+        }
+        c_end = c_start + 1;
+      }
+      if (c_end < c_band_end) split = true;
+      uint32_t n[P], size = 0;
+#pragma unroll
+      for (int p = 0; p < P; ++p) {
+        uint32_t m = j[p];
+        while (m < hi[p] && m < j[p] + (uint32_t)kUnitPinMax + 1u && bcyc(a, a.t[lo[p] + m]) < c_end) ++m;
+        n[p] = m - j[p];
+        size += n[p];
+      }
+      if (!kWrite) max_unit = max(max_unit, size);
+      if (kWrite) {
+        if (u < (uint64_t)a.L.n_units && dst + size <= a.L.n_ev) {
+          uint32_t x = 0;
+#pragma unroll
+          for (int p = 0; p < P; ++p) x |= n[p] << (4 * p);
+          x |= state << 20;
+          x |= (r.cell & 63u) << 24;
+          x |= oval << 30;
+          a.urec2[u] = make_uint2(x, __float_as_uint(r.load));
+          a.L.ugate[u] = (uint32_t)g;
+          a.uband[u] = band;
+          a.uoff[u] = dst;
+          uint64_t d = dst;
+#pragma unroll
+          for (int p = 0; p < P; ++p) {
+            for (uint32_t m = 0; m < n[p]; ++m) {
+              const uint64_t src = lo[p] + j[p] + m;
+              a.L.bt[d + m] = a.t[src];
+              a.L.bs[d + m] = a.s[src];
+            }
+            d += n[p];
+          }
+        } else {
+          atomicMin(a.err, (unsigned long long)((g << 8) | kErrTileOverflow));
+        }
+        ++u;
+        dst += size;
+      }
+#pragma unroll
+      for (int p = 0; p < P; ++p) {
+        if (p < k) state ^= (n[p] & 1u) << p;
+        if (p == k) oval ^= n[p] & 1u;
+        j[p] += n[p];
+      }
+      ++units;
+      events += size;
+    }
     if (!kWrite) {
       if (big) {
-        // no unit of a big gate: clear what the walk wrote before it saw the cycle
-        for (uint32_t bb = lane; bb < a.n_bands; bb += 32) {
+        for (uint32_t bb = 0; bb < a.n_bands; ++bb) {
           a.cnt_gb[(uint64_t)bb * G + gr] = 0;
           a.evc_gb[(uint64_t)bb * G + gr] = 0;
         }
-        if (lane == 0) {
-          a.L.big[atomicAdd(a.counters, 1u)] = (uint32_t)g;
-          a.bigf[g] = 1;
-        }
-      } else if (lane == 0) {
+        a.L.big[atomicAdd(a.counters, 1u)] = (uint32_t)g;
+        a.bigf[g] = 1;
+      } else {
         a.bigf[g] = 0;
         if (band != kNoCycle) {
           a.cnt_gb[(uint64_t)band * G + gr] = units;
@@ -310,15 +524,14 @@ __global__ void __launch_bounds__(256) k_bw_walk(const BandBuildArgs a) {
   }
 }
 
-int walk_grid(uint64_t n_gates) {
-  return (int)std::min<uint64_t>((n_gates * 32 + 255) / 256 + 1, 152ull * 64);
+int walk_grid_sparse(uint64_t n_gates) {
+  return (int)std::min<uint64_t>((n_gates + 255) / 256 + 1, 152ull * 16);
 }
 
 // Layout gate order: gates grouped by class (k, and whether the gate has more
 // than kDenseGate events), gate order kept inside a class. Units of a band
 // follow this order, so the lanes of a warp mostly see cells with the same
 // number of inputs and pin segments of similar length.
-constexpr uint64_t kDenseGate = 256;
 constexpr int kGateClasses = 2 * (kMaxK + 1);
 
 __device__ __forceinline__ uint32_t gate_class(const BandBuildArgs& a, uint32_t g) {
@@ -535,7 +748,12 @@ cudaError_t band_build_count(BandBuildArgs& a, cudaStream_t st) {
   if (e == cudaSuccess) e = cudaMemsetAsync(a.cnt_gb, 0, (n + 1) * sizeof(uint32_t), st);
   if (e == cudaSuccess) e = cudaMemsetAsync(a.evc_gb, 0, (n + 1) * sizeof(uint32_t), st);
   if (e != cudaSuccess) return e;
-  if (a.n_gates) k_bw_walk<false><<<walk_grid(a.n_gates), 256, 0, st>>>(a);
+  if (a.n_gates) {
+    k_bw_dense_list<<<(a.n_gates + 255) / 256, 256, 0, st>>>(a);
+    k_bw_walk_sparse<false><<<walk_grid_sparse(a.n_gates), 256, 0, st>>>(a);
+    k_bw_walk<false><<<walk_grid(a.n_gates), 256, 0, st>>>(a);
+    k_bw_dense_fix<<<(a.n_gates + 255) / 256, 256, 0, st>>>(a);
+  }
   e = scan_u32_to_u64(a.cnt_gb, n, a.scan_blk, a.ubase, st);
   if (e == cudaSuccess) e = scan_u32_to_u64(a.evc_gb, n, a.scan_blk, a.ebase, st);
   if (e != cudaSuccess) return e;
@@ -543,7 +761,10 @@ cudaError_t band_build_count(BandBuildArgs& a, cudaStream_t st) {
 }
 
 cudaError_t band_build_write(BandBuildArgs& a, cudaStream_t st) {
-  if (a.n_gates) k_bw_walk<true><<<walk_grid(a.n_gates), 256, 0, st>>>(a);
+  if (a.n_gates) {
+    k_bw_walk_sparse<true><<<walk_grid_sparse(a.n_gates), 256, 0, st>>>(a);
+    k_bw_walk<true><<<walk_grid(a.n_gates), 256, 0, st>>>(a);
+  }
   const uint32_t nu = a.L.n_units;
   cudaError_t e = cudaMemcpyAsync(a.uoff + nu, &a.L.n_ev, sizeof(uint64_t), cudaMemcpyHostToDevice, st);
   if (e != cudaSuccess) return e;

@@ -221,7 +221,10 @@ struct BandBuildArgs {
   uint32_t* flags;       // [max(G, n_units)] class flags, then item heads -- temporary
   uint64_t* ipos;        // [max(G + 2, n_units + 1)] scans -- temporary
   uint64_t* scan_blk;    // scan scratch -- temporary
-  uint32_t* counters;    // [4]: big gates, gates with windows narrower than a band, largest unit -- temporary
+  uint32_t* counters;    // [4]: big gates, gates with windows narrower than a band, largest unit,
+                         //      dense gates -- temporary
+  uint32_t* dense;       // [G] gates walked one warp per (gate, band) -- temporary
+  uint8_t* gflag;        // [G] a dense gate has a window narrower than a band -- temporary
   uint32_t item_bucket;  // events per item bucket (set after the counting pass)
   uint2* urec2;          // [n_units] unit records of the walk -- temporary
   const CellDesc* cells; // library (load axes for the unit records)
