@@ -12,9 +12,10 @@ Printed (rank 0, one JSON line):
   e2e      same metric through the public API with host buffers: per step the
            events are copied from pinned host memory (pa_load_events, with
            device-side validation), the pass runs, and the waveform and counts
-           come back to the host; a one-shot run either runs the unbanded
-           kernel on the loaded layout or builds the banded layout first: both
-           are timed and the faster is the value
+           come back to the host; a one-shot run streams the trace through
+           the device (pa_run_stream), or loads it and runs the unbanded kernel,
+           or loads it and builds the banded layout first: all are timed and the
+           fastest is the value
   roofline the fused kernel's algorithmic bytes per launch / its mean duration
            (CUDA events recorded on its stream inside pa_run) against the
            measured HBM copy bandwidth
@@ -106,6 +107,26 @@ class Dist:
 
 
 # ----------------------------------------------------------------- clocks
+
+def gpu_local_cpus(dev: int):
+    """CPUs of the GPU's own NUMA node (from sysfs, via its PCI address), as
+    allowed for this process; None when they cannot be found. Pinned host
+    buffers first touched from these CPUs live next to the GPU, so host <->
+    device copies do not cross to the other socket."""
+    try:
+        bus = subprocess.run(["nvidia-smi", "-i", str(dev), "--query-gpu=pci.bus_id", "--format=csv,noheader"],
+                             capture_output=True, text=True, timeout=20).stdout.strip().lower()
+        dom, rest = bus.split(":", 1)
+        path = f"/sys/bus/pci/devices/{int(dom, 16):04x}:{rest}/local_cpulist"
+        cpus = set()
+        for part in open(path).read().strip().split(","):
+            a, _, b = part.partition("-")
+            cpus.update(range(int(a), int(b or a) + 1))
+        cpus &= os.sched_getaffinity(0)
+        return cpus or None
+    except Exception:
+        return None
+
 
 class ClockSampler:
     """nvidia-smi samples (200 ms) while timed work runs."""
@@ -335,7 +356,17 @@ def run_ours(args):
     alloc, keep = pinned_alloc()
     t0 = time.perf_counter()
     over = synth_overrides(args.synth)
-    w = synth.generate(args.config, seed=args.seed, alloc=alloc, **over)
+    # the trace's pinned pages are first written by the generator: do that on the GPU's own socket
+    all_cpus = os.sched_getaffinity(0)
+    near = gpu_local_cpus(local)
+    if near:
+        os.sched_setaffinity(0, near)
+    try:
+        w = synth.generate(args.config, seed=args.seed, alloc=alloc, threads=len(near or all_cpus), **over)
+    finally:
+        os.sched_setaffinity(0, all_cpus)
+    host_placement = (f"trace generated on the GPU-local CPUs ({len(near)} of {len(all_cpus)})" if near
+                      else "GPU-local CPUs not found: default placement")
     gen_s = time.perf_counter() - t0
     cfg = synth.make_cfg(args.config, args.seed, **over)
     E, G, N = w.n_events, w.n_gates, w.n_cycles
@@ -391,23 +422,26 @@ def run_ours(args):
         # layout (unbanded kernel) or after building the cycle-banded layout.
         # Both are timed; the faster is the headline (a user running a trace
         # once takes it), the other is reported beside it.
-        def e2e_step(with_bands):
+        def e2e_step(path):
+            if path == "stream_run":  # pa_run_stream: chunk copies overlapping the computation
+                pa.run(w.vdd, w.t_clk_ns, N, out=out, stream=(w.pin_off, w.t_ns, w.slew_ps, w.value))
+                return
             pa.load_events(w.pin_off, w.t_ns, w.slew_ps, w.value)
-            if with_bands:
+            if path == "load_build_bands_run":
                 pa.build_bands(w.t_clk_ns, args.band_cycles)
             step()
-        for with_bands in ((False, True) if banded else (False,)):
+        paths = ["stream_run", "load_run_unbanded"] + (["load_build_bands_run"] if banded else [])
+        for path in paths:
             for _ in range(2):
-                e2e_step(with_bands)
+                e2e_step(path)
             dist.barrier()
             torch.cuda.synchronize()
             t0 = time.perf_counter()
             for _ in range(args.e2e_steps):
-                e2e_step(with_bands)
+                e2e_step(path)
             torch.cuda.synchronize()
             e2e_s = dist.max(time.perf_counter() - t0)
-            e2e_paths["load_build_bands_run" if with_bands else "load_run_unbanded"] = \
-                world * E * args.e2e_steps / e2e_s
+            e2e_paths[path] = world * E * args.e2e_steps / e2e_s
         e2e_value = max(e2e_paths.values())
     clk.active = False
     clk.stop()
@@ -439,12 +473,14 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "e2e": None if e2e_value is None else {"value": e2e_value, "unit": "events/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": args.e2e_steps, "paths": e2e_paths,
-                    "note": "per step: pa_load_events from pinned host memory (device-side validation) + "
-                            "pa_run (+ pa_build_bands before it on the banded path) + waveform/count copy to "
-                            "host; library and netlist loaded once; value = the faster path"},
+                    "note": "per step from pinned host memory: pa_run_stream (chunked copies overlapping "
+                            "validation and the unbanded kernel), or pa_load_events (device-side validation) + "
+                            "pa_run (+ pa_build_bands before it on the banded path); waveform/count copy to host; "
+                            "library and netlist loaded once; value = the fastest path"},
             "clocks": clk.summary(),
             "gpu_launches": launches,
             "gen_seconds": gen_s,
+            "host_placement": host_placement,
             "p_total_w": r["p_int"] + r["p_sw"] + r["p_gl"] + r["p_leak"],
             "n_tiles": r["n_tiles"], "n_heavy": r["n_heavy"],
             "path": "banded" if r["path"] == glp.PA_PATH_BANDED else "unbanded",

@@ -69,7 +69,7 @@ class PaError(RuntimeError):
 
 
 EXPORTS = ("pa_create", "pa_destroy", "pa_load_library", "pa_load_netlist", "pa_load_events", "pa_run",
-           "pa_run_noalloc", "pa_build_bands", "pa_default_params", "pa_last_error", "pa_version")
+           "pa_run_noalloc", "pa_run_stream", "pa_build_bands", "pa_default_params", "pa_last_error", "pa_version")
 PA_PATH_UNBANDED, PA_PATH_BANDED = 0, 1
 PA_NOALLOC_MAX_CYCLES = 65536
 PA_NOALLOC_MAX_GATES = 262144
@@ -96,6 +96,8 @@ def load_library():
         L.pa_load_events.argtypes = [_vp, ctypes.POINTER(PaEvents)]
         L.pa_run.argtypes = [_vp, ctypes.POINTER(PaRunParams), ctypes.POINTER(PaResult)]
         L.pa_run_noalloc.argtypes = [_vp, ctypes.POINTER(PaRunParams), ctypes.POINTER(PaResult)]
+        L.pa_run_stream.argtypes = [_vp, ctypes.POINTER(PaRunParams), ctypes.POINTER(PaEvents), ctypes.c_uint64,
+                                    ctypes.POINTER(PaResult)]
         L.pa_build_bands.argtypes = [_vp, ctypes.c_float, ctypes.c_uint32]
         L.pa_default_params.argtypes = [ctypes.POINTER(PaRunParams)]
         L.pa_default_params.restype = None
@@ -147,6 +149,13 @@ def pa_run_noalloc(ctx: int, params: PaRunParams, result: PaResult) -> None:
     array; device output arrays only; limits PA_NOALLOC_MAX_CYCLES and
     PA_NOALLOC_MAX_GATES). For callers that may not allocate at run time."""
     _check(ctx, load_library().pa_run_noalloc(ctx, ctypes.byref(params), ctypes.byref(result)))
+
+
+def pa_run_stream(ctx: int, params: PaRunParams, events: PaEvents, chunk_events: int, result: PaResult) -> None:
+    """pa_run on a trace kept in host memory, streamed through the device in
+    chunks of whole gates (copies overlapping the computation)."""
+    _check(ctx, load_library().pa_run_stream(ctx, ctypes.byref(params), ctypes.byref(events), int(chunk_events),
+                                             ctypes.byref(result)))
 
 
 def pa_build_bands(ctx: int, t_clk_ns: float, band_cycles: int = 0) -> None:
@@ -255,14 +264,17 @@ class PowerAnalyzer:
 
     def run(self, vdd, t_clk_ns, n_cycles, t_max_ns=0.0, tile_events=0, heavy_events=0, timing=False,
             waveform=True, counts=True, debug=False, gate_power=False, glitch_all=False, esw_rise=False,
-            out=None):
+            out=None, stream=None, chunk_events=0):
         """Run the power computation. Returns a dict with ``p_int, p_sw, p_gl,
         p_leak`` (W), ``t_max`` and, as requested, ``waveform`` (f32 W per
         cycle), ``event_count``/``glitch_count`` (u32 per cycle), per-event
         ``state_pre``/``lut_ij``/``is_glitch`` (u8), per-gate ``gate_power``
         (f64 W, [gates, 4]: internal, switching, glitch, leakage), and ``ms_*``
         timings. ``glitch_all`` / ``esw_rise`` select the alternative readings
-        (PA_RUN_GLITCH_ALL / PA_RUN_ESW_RISE).
+        (PA_RUN_GLITCH_ALL / PA_RUN_ESW_RISE). ``stream = (pin_off, t_ns,
+        slew_ps, value)`` (host arrays; value may be None) runs pa_run_stream on
+        that trace instead of pa_run on the loaded one, in chunks of about
+        ``chunk_events`` events (0 = the library's default).
         ``out`` may hold preallocated arrays (numpy or CUDA tensors) under the
         same names; CUDA tensors select device output."""
         flags = ((PA_RUN_TIMING if timing else 0) | (PA_RUN_GLITCH_ALL if glitch_all else 0)
@@ -291,7 +303,15 @@ class PowerAnalyzer:
         r.lut_ij = arr("lut_ij", self.n_events, np.uint8, debug)
         r.is_glitch = arr("is_glitch", self.n_events, np.uint8, debug)
         r.gate_power_w = arr("gate_power", self.n_gates * 4, np.float64, gate_power)
-        pa_run(self.ctx, p, r)
+        if stream is None:
+            pa_run(self.ctx, p, r)
+        else:
+            po, tt, ss, vv = stream
+            keep = [_host(po, np.uint64), _host(tt, np.float32), _host(ss, np.float32),
+                    None if vv is None else _host(vv, np.uint8)]
+            ev = PaEvents(len(keep[0]) - 1, len(keep[1]), keep[0].ctypes.data, keep[1].ctypes.data,
+                          keep[2].ctypes.data, None if keep[3] is None else keep[3].ctypes.data, PA_MEM_HOST)
+            pa_run_stream(self.ctx, p, ev, chunk_events, r)
         if "gate_power" in res and not (hasattr(res["gate_power"], "is_cuda") and res["gate_power"].is_cuda):
             res["gate_power"] = np.asarray(res["gate_power"]).reshape(-1, 4)
         res.update(p_int=r.p_int_w, p_sw=r.p_sw_w, p_gl=r.p_gl_w, p_leak=r.p_leak_w, t_max=r.t_max_ns,

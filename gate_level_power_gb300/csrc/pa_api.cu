@@ -46,6 +46,7 @@ struct pa_ctx {
   uint32_t n_gates = 0;
   uint64_t n_pins = 0;
   DevBuf gates;
+  std::vector<GateRec> h_gates;  // host copy (pa_run_stream cuts the netlist into chunks with it)
 
   // events
   bool has_ev = false;
@@ -66,6 +67,11 @@ struct pa_ctx {
       b_urec2, b_dense, b_gflag;
   DevBuf b_part;
   DevBuf scratch_small;
+
+  // pa_run_stream: two staging slots per chunk array, a copy stream and its events
+  cudaStream_t copy_stream = nullptr;
+  cudaEvent_t st_copied[2] = {nullptr, nullptr}, st_free[2] = {nullptr, nullptr};
+  DevBuf st_t[2], st_s[2], st_v[2], st_pin[2], st_gates[2], st_goff[2];
 };
 
 namespace {
@@ -196,9 +202,13 @@ struct PassBufs {
   double* gate_e = nullptr;  // per-gate accumulators (fJ), converted to W in place
 };
 
-int check_run(pa_ctx* c, const pa_run_params* prm, const pa_result* out, const char* who, RunPlan* plan) {
+// stream: the events come with the call (pa_run_stream), so none need be
+// loaded and their range is checked chunk by chunk.
+int check_run(pa_ctx* c, const pa_run_params* prm, const pa_result* out, const char* who, RunPlan* plan,
+              bool stream = false) {
   if (!c) return PA_ERR_ARG;
-  if (!c->has_ev) return fail(c, PA_ERR_ORDER, "%s: events not loaded", who);
+  if (stream ? !c->has_net : !c->has_ev)
+    return fail(c, PA_ERR_ORDER, stream ? "%s: no netlist loaded" : "%s: events not loaded", who);
   if (!prm || !out) return fail(c, PA_ERR_ARG, "%s: null params or result", who);
   if (!(prm->t_clk_ns > 0.f) || !is_finite_f(prm->t_clk_ns)) return fail(c, PA_ERR_ARG, "%s: t_clk_ns must be > 0", who);
   if (prm->n_cycles == 0) return fail(c, PA_ERR_ARG, "%s: n_cycles must be > 0", who);
@@ -212,7 +222,7 @@ int check_run(pa_ctx* c, const pa_run_params* prm, const pa_result* out, const c
   plan->Td = (double)plan->T;
   plan->t_max = prm->t_max_ns > 0 ? prm->t_max_ns : (double)prm->n_cycles * plan->Td;
   if (!std::isfinite(plan->t_max)) return fail(c, PA_ERR_ARG, "%s: t_max not finite", who);
-  if (c->n_events) {
+  if (!stream && c->n_events) {
     const float cyc = std::floor(c->t_last / plan->T);  // fp32 division, as the kernels take it
     if (!(cyc < (float)prm->n_cycles))
       return fail(c, PA_ERR_RANGE, "%s: latest event t = %.9g ns lies in cycle %.0f >= n_cycles %u", who,
@@ -243,8 +253,9 @@ int check_run(pa_ctx* c, const pa_run_params* prm, const pa_result* out, const c
 // gates) -> final reduction. Counts are taken in f32 and the pass is repeated
 // with integer counts and fp64 bins if a cycle reached 2^24 events. Copies
 // outputs on success.
-int run_pass(pa_ctx* c, const RunPlan& plan, const PassBufs& B, pa_result* out, const char* who,
-             const BandLayout* band) {
+// Run arguments of a pass over the loaded data (a streamed chunk replaces the
+// netlist and event pointers).
+RunArgs make_run_args(pa_ctx* c, const RunPlan& plan, const PassBufs& B) {
   const uint32_t N = plan.N;
   RunArgs a;
   std::memset(&a, 0, sizeof(a));
@@ -272,7 +283,7 @@ int run_pass(pa_ctx* c, const RunPlan& plan, const PassBufs& B, pa_result* out, 
   a.part_blk = B.part_blk;
   a.part_counts = B.part_counts;
   a.tiles = B.tiles;
-  a.heavy = band ? band->big : B.heavy;
+  a.heavy = B.heavy;
   a.p0 = B.p0_tot;
   a.totals = B.p0_tot + 4;
   a.bins = B.bins;
@@ -284,6 +295,14 @@ int run_pass(pa_ctx* c, const RunPlan& plan, const PassBufs& B, pa_result* out, 
   a.dbg_lut = B.dbg[1];
   a.dbg_glitch = B.dbg[2];
   a.gate_e = B.gate_e;
+  return a;
+}
+
+int run_pass(pa_ctx* c, const RunPlan& plan, const PassBufs& B, pa_result* out, const char* who,
+             const BandLayout* band) {
+  const uint32_t N = plan.N;
+  RunArgs a = make_run_args(c, plan, B);
+  if (band) a.heavy = band->big;  // the unbanded kernel streams the gates the layout left out
   BandRunArgs A;
   if (band) {
     A.r = a;
@@ -375,6 +394,236 @@ int run_pass(pa_ctx* c, const RunPlan& plan, const PassBufs& B, pa_result* out, 
   return PA_OK;
 }
 
+// ----------------------------------------------------------------- streamed run
+//
+// pa_run_stream: the events stay in host memory and pass through the device
+// in chunks of whole gates (about `target` events each). Chunk i + 1 is copied
+// on the copy stream while chunk i is validated and computed on the context's
+// stream, each chunk by partition -> unbanded fused kernel into the same cycle
+// bins and totals; one final reduction at the end. Two staging slots: the copy
+// into a slot waits for the compute of the chunk that used it last.
+
+struct StreamChunk {
+  uint32_t g0, g1;     // gates
+  uint64_t pin0, pin1; // pins
+  uint64_t e0, e1;     // events
+};
+
+int stream_copy(pa_ctx* c, const pa_events* ev, const StreamChunk& k, int slot, bool wait_free) {
+  cudaStream_t cs = c->copy_stream;
+  if (wait_free) CUDA_TRY(c, cudaStreamWaitEvent(cs, c->st_free[slot], 0));
+  const uint64_t ne = k.e1 - k.e0;
+  CUDA_TRY(c, cudaMemcpyAsync(c->st_pin[slot].p, ev->pin_off + k.pin0, (k.pin1 - k.pin0 + 1) * sizeof(uint64_t),
+                              cudaMemcpyHostToDevice, cs));
+  if (ne) {
+    CUDA_TRY(c, cudaMemcpyAsync(c->st_t[slot].p, ev->t_ns + k.e0, ne * sizeof(float), cudaMemcpyHostToDevice, cs));
+    CUDA_TRY(c, cudaMemcpyAsync(c->st_s[slot].p, ev->slew_ps + k.e0, ne * sizeof(float), cudaMemcpyHostToDevice, cs));
+    if (ev->value) CUDA_TRY(c, cudaMemcpyAsync(c->st_v[slot].p, ev->value + k.e0, ne, cudaMemcpyHostToDevice, cs));
+  }
+  CUDA_TRY(c, cudaEventRecord(c->st_copied[slot], cs));
+  return PA_OK;
+}
+
+int run_stream(pa_ctx* c, const RunPlan& plan, const pa_events* ev, uint64_t target, pa_result* out) {
+  const char* who = "pa_run_stream";
+  const uint32_t G = c->n_gates, N = plan.N;
+  const uint64_t P = ev->n_pins, E = ev->n_events;
+  const uint64_t* hpo = ev->pin_off;
+  // the host pin offsets decide the chunks: check them first
+  if (hpo[0] != 0 || hpo[P] != E) return fail(c, PA_ERR_ARG, "%s: pin_off must start at 0 and end at n_events", who);
+  for (uint64_t p = 0; p < P; ++p)
+    if (hpo[p + 1] < hpo[p]) return fail(c, PA_ERR_ARG, "%s: pin_off not monotone (first at pin %llu)", who,
+                                         (unsigned long long)p);
+  // chunks of whole gates
+  std::vector<StreamChunk> ch;
+  {
+    StreamChunk k{0, 0, 0, 0, 0, 0};
+    uint64_t acc = 0;
+    for (uint32_t g = 0; g < G; ++g) {
+      const GateRec& r = c->h_gates[g];
+      const uint64_t p1 = (uint64_t)r.pin_base + ((r.init >> 16) & 0xffu) + 1;
+      const uint64_t ne = hpo[p1] - hpo[r.pin_base];
+      if (acc > 0 && acc + ne > target) {
+        k.g1 = g;
+        ch.push_back(k);
+        k.g0 = g;
+        acc = 0;
+      }
+      acc += ne;
+    }
+    k.g1 = G;
+    ch.push_back(k);
+  }
+  uint64_t max_ev = 0, max_pins = 0;
+  uint32_t max_g = 0;
+  for (StreamChunk& k : ch) {
+    k.pin0 = k.g0 < G ? c->h_gates[k.g0].pin_base : P;
+    k.pin1 = k.g1 < G ? c->h_gates[k.g1].pin_base : P;
+    k.e0 = hpo[k.pin0];
+    k.e1 = hpo[k.pin1];
+    max_ev = std::max(max_ev, k.e1 - k.e0);
+    max_pins = std::max(max_pins, k.pin1 - k.pin0);
+    max_g = std::max(max_g, k.g1 - k.g0);
+  }
+  // staging slots and run scratch
+  if (!c->copy_stream) {
+    CUDA_TRY(c, cudaStreamCreateWithFlags(&c->copy_stream, cudaStreamNonBlocking));
+    for (int i = 0; i < 2; ++i) {
+      CUDA_TRY(c, cudaEventCreateWithFlags(&c->st_copied[i], cudaEventDisableTiming));
+      CUDA_TRY(c, cudaEventCreateWithFlags(&c->st_free[i], cudaEventDisableTiming));
+    }
+  }
+  const size_t ev_bytes = ((max_ev + 64) & ~(size_t)15) * sizeof(float);
+  for (int i = 0; i < 2; ++i) {
+    PA_TRY(dreserve(c, c->st_t[i], ev_bytes));
+    PA_TRY(dreserve(c, c->st_s[i], ev_bytes));
+    if (ev->value) PA_TRY(dreserve(c, c->st_v[i], max_ev + 16));
+    PA_TRY(dreserve(c, c->st_pin[i], (max_pins + 1) * sizeof(uint64_t)));
+    PA_TRY(dreserve(c, c->st_gates[i], ((size_t)max_g + 1) * sizeof(GateRec)));
+    PA_TRY(dreserve(c, c->st_goff[i], ((size_t)max_g + 1) * sizeof(uint64_t)));
+  }
+  const uint32_t nblk = partition_blocks(max_g);
+  PassBufs B;
+  PA_TRY(dreserve(c, c->bins, (size_t)N * sizeof(float4)));
+  PA_TRY(dreserve(c, c->part_blk, (size_t)(nblk + 1) * 2 * sizeof(uint32_t)));
+  PA_TRY(dreserve(c, c->part_counts, 4 * sizeof(uint32_t)));
+  PA_TRY(dreserve(c, c->tiles, ((size_t)max_g + 1) * sizeof(Tile)));
+  PA_TRY(dreserve(c, c->heavy, ((size_t)max_g + 1) * sizeof(uint32_t)));
+  PA_TRY(dreserve(c, c->p0_tot, 8 * sizeof(double)));
+  PA_TRY(dreserve(c, c->p_out, 4 * sizeof(double)));
+  PA_TRY(dreserve(c, c->chunk_sums, (size_t)reduce_chunks(N) * sizeof(double)));
+  PA_TRY(dreserve(c, c->wave_tmp, (size_t)N * sizeof(float)));
+  PA_TRY(dreserve(c, c->cnt_tmp, (size_t)N * 2 * sizeof(uint32_t)));
+  PA_TRY(dreserve(c, c->err_word, sizeof(unsigned long long)));
+  PA_TRY(dreserve(c, c->tmax_bits, sizeof(unsigned int)));
+  if (plan.gate && out->out_mem != PA_MEM_DEVICE) PA_TRY(dreserve(c, c->gate_tmp, ((size_t)G + 1) * 4 * sizeof(double)));
+  B.bins = (float4*)c->bins.p;
+  B.part_blk = (uint32_t*)c->part_blk.p;
+  B.part_counts = (uint32_t*)c->part_counts.p;
+  B.tiles = (Tile*)c->tiles.p;
+  B.heavy = (uint32_t*)c->heavy.p;
+  B.p0_tot = (double*)c->p0_tot.p;
+  B.p_out = (double*)c->p_out.p;
+  B.chunk_sums = (double*)c->chunk_sums.p;
+  B.wave = (float*)c->wave_tmp.p;
+  B.cnt_ev = (uint32_t*)c->cnt_tmp.p;
+  B.cnt_gl = (uint32_t*)c->cnt_tmp.p + N;
+  if (plan.gate) B.gate_e = out->out_mem == PA_MEM_DEVICE ? out->gate_power_w : (double*)c->gate_tmp.p;
+  cudaStream_t st = c->stream;
+  const int nc = (int)ch.size();
+  double p[4];
+  unsigned long long key = kNoErr;
+  uint32_t launches = 0;
+  for (int exact = 0; exact < 2; ++exact) {
+    launches = 0;
+    if (plan.timing) CUDA_TRY(c, cudaEventRecord(c->ev[0], st));
+    CUDA_TRY(c, cudaMemsetAsync(B.bins, 0, (size_t)N * sizeof(float4), st));
+    if (exact) CUDA_TRY(c, cudaMemsetAsync(B.cnt_ev, 0, (size_t)N * 2 * sizeof(uint32_t), st));
+    CUDA_TRY(c, cudaMemsetAsync(B.p0_tot, 0, 8 * sizeof(double), st));
+    CUDA_TRY(c, cudaMemsetAsync(c->err_word.p, 0xff, sizeof(unsigned long long), st));
+    CUDA_TRY(c, cudaMemsetAsync(c->tmax_bits.p, 0, sizeof(unsigned int), st));
+    if (B.gate_e) CUDA_TRY(c, cudaMemsetAsync(B.gate_e, 0, (size_t)G * 4 * sizeof(double), st));
+    CUDA_TRY(c, cudaStreamSynchronize(st));  // the slots are free and the accumulators clear
+    PA_TRY(stream_copy(c, ev, ch[0], 0, false));
+    for (int i = 0; i < nc; ++i) {
+      const StreamChunk& k = ch[i];
+      const int slot = i & 1;
+      if (i + 1 < nc) PA_TRY(stream_copy(c, ev, ch[i + 1], (i + 1) & 1, i + 1 >= 2));
+      CUDA_TRY(c, cudaStreamWaitEvent(st, c->st_copied[slot], 0));
+      const uint32_t gk = k.g1 - k.g0;
+      const uint64_t pk = k.pin1 - k.pin0, ek = k.e1 - k.e0;
+      uint64_t* pin = (uint64_t*)c->st_pin[slot].p;
+      GateRec* gates = (GateRec*)c->st_gates[slot].p;
+      CUDA_TRY(c, launch_rebase_chunk(pin, pk, k.e0, (const GateRec*)c->gates.p + k.g0, gates, gk,
+                                      (uint32_t)k.pin0, st));
+      CUDA_TRY(c, launch_check_pin_off(pin, pk, ek, (unsigned long long*)c->err_word.p, st));
+      ValidateArgs va;
+      va.gates = gates;
+      va.n_gates = gk;
+      va.n_pins = pk;
+      va.n_events = ek;
+      va.pin_off = pin;
+      va.t = (const float*)c->st_t[slot].p;
+      va.s = (const float*)c->st_s[slot].p;
+      va.value = ev->value ? (const uint8_t*)c->st_v[slot].p : nullptr;
+      va.gate_off = (uint64_t*)c->st_goff[slot].p;
+      va.err = (unsigned long long*)c->err_word.p;
+      va.t_max_bits = (unsigned int*)c->tmax_bits.p;
+      CUDA_TRY(c, launch_validate_events(va, st));
+      launches += 4;
+      // the chunk must be valid, and its events inside the window, before it touches the bins
+      unsigned int tbits = 0;
+      CUDA_TRY(c, cudaMemcpyAsync(&key, c->err_word.p, sizeof(key), cudaMemcpyDeviceToHost, st));
+      CUDA_TRY(c, cudaMemcpyAsync(&tbits, c->tmax_bits.p, sizeof(tbits), cudaMemcpyDeviceToHost, st));
+      CUDA_TRY(c, cudaStreamSynchronize(st));
+      if (key != kNoErr) {
+        const uint32_t code = (uint32_t)(key & 0xff);
+        const uint64_t base = code == kErrPinOff ? k.pin0 : (code == kErrTileOverflow ? k.g0 : k.e0);
+        CUDA_TRY(c, cudaStreamSynchronize(c->copy_stream));
+        return map_dev_err(c, (((key >> 8) + base) << 8) | code, who);
+      }
+      float t_last;
+      std::memcpy(&t_last, &tbits, sizeof(float));
+      if (ek) {
+        const float cyc = std::floor(t_last / plan.T);
+        if (!(cyc < (float)N) || (double)t_last > plan.t_max) {
+          CUDA_TRY(c, cudaStreamSynchronize(c->copy_stream));
+          return fail(c, PA_ERR_RANGE, "%s: an event at t = %.9g ns lies outside the window (%u cycles, t_max %.9g)",
+                      who, (double)t_last, N, plan.t_max);
+        }
+      }
+      RunArgs a = make_run_args(c, plan, B);
+      a.gates = gates;
+      a.n_gates = gk;
+      a.pin_off = pin;
+      a.gate_off = (const uint64_t*)c->st_goff[slot].p;
+      a.t = (const float*)c->st_t[slot].p;
+      a.s = (const float*)c->st_s[slot].p;
+      a.gate_e = B.gate_e ? B.gate_e + (size_t)k.g0 * 4 : nullptr;
+      CUDA_TRY(c, cudaMemsetAsync(B.part_counts, 0, 4 * sizeof(uint32_t), st));
+      CUDA_TRY(c, launch_partition(a, partition_blocks(gk), st));
+      const int grid = c->sm_count * fused_blocks_per_sm(plan.pow2, plan.debug, exact != 0);
+      CUDA_TRY(c, launch_fused(a, grid, plan.pow2, plan.debug, exact != 0, st));
+      launches += (gk ? 3 : 0) + 1;
+      CUDA_TRY(c, cudaEventRecord(c->st_free[slot], st));
+    }
+    RunArgs a = make_run_args(c, plan, B);
+    a.n_gates = G;
+    a.gates = (const GateRec*)c->gates.p;
+    CUDA_TRY(c, launch_final_reduce(a, plan.Td, plan.t_max, B.wave, B.p_out, exact != 0, st));
+    launches += 2;
+    if (B.gate_e && G) {
+      CUDA_TRY(c, launch_gate_power(a, plan.t_max, st));
+      launches += 1;
+    }
+    if (plan.timing) CUDA_TRY(c, cudaEventRecord(c->ev[3], st));
+    CUDA_TRY(c, cudaMemcpyAsync(p, B.p_out, sizeof(p), cudaMemcpyDeviceToHost, st));
+    CUDA_TRY(c, cudaMemcpyAsync(&key, c->err_word.p, sizeof(key), cudaMemcpyDeviceToHost, st));
+    CUDA_TRY(c, cudaStreamSynchronize(st));
+    if (key == kNoErr) break;
+    if ((key & 0xff) != kErrCountOverflow || exact) return map_dev_err(c, key, who);
+  }
+  const cudaMemcpyKind dk = out->out_mem == PA_MEM_HOST ? cudaMemcpyDeviceToHost : cudaMemcpyDeviceToDevice;
+  if (out->waveform_w) CUDA_TRY(c, cudaMemcpyAsync(out->waveform_w, B.wave, (size_t)N * sizeof(float), dk, st));
+  if (out->event_count) CUDA_TRY(c, cudaMemcpyAsync(out->event_count, B.cnt_ev, (size_t)N * 4, dk, st));
+  if (out->glitch_count) CUDA_TRY(c, cudaMemcpyAsync(out->glitch_count, B.cnt_gl, (size_t)N * 4, dk, st));
+  if (out->gate_power_w && out->gate_power_w != B.gate_e && G)
+    CUDA_TRY(c, cudaMemcpyAsync(out->gate_power_w, B.gate_e, (size_t)G * 4 * sizeof(double), dk, st));
+  CUDA_TRY(c, cudaStreamSynchronize(st));
+  out->p_int_w = p[0];
+  out->p_sw_w = p[1];
+  out->p_gl_w = p[2];
+  out->p_leak_w = p[3];
+  out->t_max_ns = plan.t_max;
+  out->n_tiles = (uint32_t)nc;  // chunks
+  out->n_heavy = 0;
+  out->kernel_launches = launches;
+  out->path = PA_PATH_UNBANDED;
+  out->ms_partition = out->ms_fused = out->ms_reduce = out->ms_total = 0.f;
+  if (plan.timing) cudaEventElapsedTime(&out->ms_total, c->ev[0], c->ev[3]);
+  return PA_OK;
+}
+
 bool same_bits(float a, float b) { return std::memcmp(&a, &b, sizeof(float)) == 0; }
 
 }  // namespace
@@ -446,6 +695,13 @@ void pa_destroy(pa_ctx* c) {
                    &c->b_uband, &c->b_uoff, &c->b_flags, &c->b_ipos, &c->b_scan, &c->b_counters,
                    &c->b_urec2, &c->b_dense, &c->b_gflag, &c->b_part};
   for (DevBuf* b : all) dfree(*b);
+  for (int i = 0; i < 2; ++i) {
+    DevBuf* st[] = {&c->st_t[i], &c->st_s[i], &c->st_v[i], &c->st_pin[i], &c->st_gates[i], &c->st_goff[i]};
+    for (DevBuf* b : st) dfree(*b);
+    if (c->st_copied[i]) cudaEventDestroy(c->st_copied[i]);
+    if (c->st_free[i]) cudaEventDestroy(c->st_free[i]);
+  }
+  if (c->copy_stream) cudaStreamDestroy(c->copy_stream);
   for (auto& e : c->ev)
     if (e) cudaEventDestroy(e);
   if (c->own_stream && c->stream) cudaStreamDestroy(c->stream);
@@ -569,6 +825,7 @@ int pa_load_netlist(pa_ctx* c, const pa_netlist* N) {
   PA_TRY(dreserve(c, c->gates, (size_t)G * sizeof(GateRec)));
   if (G) CUDA_TRY(c, cudaMemcpyAsync(c->gates.p, recs.data(), (size_t)G * sizeof(GateRec), cudaMemcpyHostToDevice, c->stream));
   CUDA_TRY(c, cudaStreamSynchronize(c->stream));
+  c->h_gates = std::move(recs);
   c->n_gates = G;
   c->n_pins = pb;
   c->has_net = true;
@@ -678,6 +935,22 @@ int pa_run(pa_ctx* c, const pa_run_params* prm, pa_result* out) {
   for (int i = 0; i < 3; ++i) B.dbg[i] = dbg_arrays ? (uint8_t*)c->dbg[i].p : nullptr;
   if (plan.gate) B.gate_e = out->out_mem == PA_MEM_DEVICE ? out->gate_power_w : (double*)c->gate_tmp.p;
   return run_pass(c, plan, B, out, "pa_run", banded ? &c->band : nullptr);
+}
+
+int pa_run_stream(pa_ctx* c, const pa_run_params* prm, const pa_events* ev, uint64_t chunk_events,
+                  pa_result* out) {
+  RunPlan plan;
+  PA_TRY(check_run(c, prm, out, "pa_run_stream", &plan, true));
+  if (!ev || !ev->pin_off || (ev->n_events && (!ev->t_ns || !ev->slew_ps)))
+    return fail(c, PA_ERR_ARG, "pa_run_stream: null event pointer");
+  if (ev->mem != PA_MEM_HOST) return fail(c, PA_ERR_ARG, "pa_run_stream: events must be host memory (PA_MEM_HOST)");
+  if (ev->n_pins != c->n_pins)
+    return fail(c, PA_ERR_ARG, "pa_run_stream: n_pins %llu != netlist pins %llu", (unsigned long long)ev->n_pins,
+                (unsigned long long)c->n_pins);
+  if (out->state_pre || out->lut_ij || out->is_glitch)
+    return fail(c, PA_ERR_ARG, "pa_run_stream: per-event debug arrays are not available on a streamed run");
+  CUDA_TRY(c, cudaSetDevice(c->device));
+  return run_stream(c, plan, ev, chunk_events ? chunk_events : PA_STREAM_DEFAULT_CHUNK, out);
 }
 
 }  // extern "C"

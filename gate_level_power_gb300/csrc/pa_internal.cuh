@@ -275,6 +275,11 @@ cudaError_t launch_final_reduce(const RunArgs& a, double t_clk, double t_max, fl
 // Per-gate power in place: a.gate_e (fJ) -> W, with each gate's initial-state
 // leakage held to t_max added to its leakage.
 cudaError_t launch_gate_power(const RunArgs& a, double t_max, cudaStream_t st);
+// A chunk of pa_run_stream: its pin offsets (n_pins + 1, in place) made relative
+// to its first event ev0, and its gate records copied with pin bases relative
+// to its first pin pin0.
+cudaError_t launch_rebase_chunk(uint64_t* pin_off, uint64_t n_pins, uint64_t ev0, const GateRec* gates_src,
+                                GateRec* gates_dst, uint32_t n_gates, uint32_t pin0, cudaStream_t st);
 inline uint32_t reduce_chunks(uint32_t n_cycles) { return (n_cycles + kReduceChunk - 1) / kReduceChunk; }
 
 }  // namespace pa

@@ -855,3 +855,35 @@ cudaError_t launch_gate_power(const RunArgs& a, double t_max, cudaStream_t st) {
 }
 
 }  // namespace pa
+
+// ------------------------------------------------------------------ chunk rebasing (pa_run_stream)
+
+namespace pa {
+
+namespace {
+
+__global__ void __launch_bounds__(256) k_rebase_pin_off(uint64_t* p, uint64_t n, uint64_t base) {
+  const uint64_t i = (uint64_t)blockIdx.x * 256u + threadIdx.x;
+  if (i < n) p[i] -= base;
+}
+
+__global__ void __launch_bounds__(256) k_rebase_gates(const GateRec* __restrict__ src, GateRec* dst, uint32_t n,
+                                                      uint32_t pin0) {
+  const uint32_t g = blockIdx.x * 256u + threadIdx.x;
+  if (g < n) {
+    GateRec r = src[g];
+    r.pin_base -= pin0;
+    dst[g] = r;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_rebase_chunk(uint64_t* pin_off, uint64_t n_pins, uint64_t ev0, const GateRec* gates_src,
+                                GateRec* gates_dst, uint32_t n_gates, uint32_t pin0, cudaStream_t st) {
+  if (n_pins + 1) k_rebase_pin_off<<<(unsigned)((n_pins + 1 + 255) / 256), 256, 0, st>>>(pin_off, n_pins + 1, ev0);
+  if (n_gates) k_rebase_gates<<<(n_gates + 255) / 256, 256, 0, st>>>(gates_src, gates_dst, n_gates, pin0);
+  return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -319,6 +319,28 @@ int pa_run(pa_ctx *ctx, const pa_run_params *params, pa_result *out);
 #define PA_NOALLOC_SCRATCH_BYTES (5u << 20)
 int pa_run_noalloc(pa_ctx *ctx, const pa_run_params *params, pa_result *out);
 
+/*
+ * pa_run_stream -- the run of pa_run on a trace that stays in host memory,
+ * for traces larger than the device's memory or runs made once per trace.
+ * The paper's flow overlaps the host's event packing with the GPU work; here
+ * the events pass through the device in chunks of whole gates (about
+ * chunk_events events each; 0 = PA_STREAM_DEFAULT_CHUNK), the copy of the next
+ * chunk overlapping the validation and computation of the current one (pinned
+ * host memory gives the overlap). Each chunk is checked as pa_load_events
+ * checks a trace and computed by the unbanded kernel into the same cycle bins
+ * and totals; results equal pa_run's on the loaded trace to floating-point
+ * summation order.
+ *   ev   host arrays (mem = PA_MEM_HOST) in pa_load_events' form; not retained
+ * Requires a netlist; does not use or change the loaded events or bands. Device
+ * memory: two staging slots of about 9 bytes per event of the largest chunk,
+ * plus pa_run's scratch. Outputs as pa_run, without the per-event debug arrays
+ * (PA_ERR_ARG); n_tiles returns the number of chunks. Errors as pa_load_events
+ * and pa_run (indices of the offending pin / event / gate in the whole trace).
+ */
+#define PA_STREAM_DEFAULT_CHUNK (1ull << 27)
+int pa_run_stream(pa_ctx *ctx, const pa_run_params *params, const pa_events *ev, uint64_t chunk_events,
+                  pa_result *out);
+
 /* Defaults: vdd 0.9 V, t_clk 1 ns, n_cycles 1, t_max 0, partition knobs 0. */
 void pa_default_params(pa_run_params *params);
 
