@@ -59,7 +59,7 @@ class PaResult(ctypes.Structure):
                 ("lut_ij", _vp), ("is_glitch", _vp), ("ms_partition", ctypes.c_float),
                 ("ms_fused", ctypes.c_float), ("ms_reduce", ctypes.c_float), ("ms_total", ctypes.c_float),
                 ("n_tiles", ctypes.c_uint32), ("n_heavy", ctypes.c_uint32), ("kernel_launches", ctypes.c_uint32),
-                ("path", ctypes.c_uint32), ("gate_power_w", _vp)]
+                ("path", ctypes.c_uint32), ("gate_power_w", _vp), ("cell_power_w", _vp)]
 
 
 class PaError(RuntimeError):
@@ -201,6 +201,7 @@ class PowerAnalyzer:
         self.n_cycles = None
         self.n_events = 0
         self.n_gates = 0
+        self.n_cells = 0
 
     def close(self):
         if self.ctx:
@@ -226,6 +227,7 @@ class PowerAnalyzer:
         L = PaLibrary(len(keep[0]), *(k.ctypes.data for k in keep[:7]), len(keep[6]),
                       keep[7].ctypes.data, keep[8].ctypes.data, len(keep[8]))
         pa_load_library(self.ctx, L)
+        self.n_cells = len(keep[0])
 
     def load_netlist(self, cell_id, load_ff, init_in, init_out):
         keep = [_host(cell_id, np.uint32), _host(load_ff, np.float32), _host(init_in, np.uint8),
@@ -263,13 +265,14 @@ class PowerAnalyzer:
         self.load_events(w.pin_off, w.t_ns, w.slew_ps, w.value if with_value else None)
 
     def run(self, vdd, t_clk_ns, n_cycles, t_max_ns=0.0, tile_events=0, heavy_events=0, timing=False,
-            waveform=True, counts=True, debug=False, gate_power=False, glitch_all=False, esw_rise=False,
-            out=None, stream=None, chunk_events=0):
+            waveform=True, counts=True, debug=False, gate_power=False, cell_power=False, glitch_all=False,
+            esw_rise=False, out=None, stream=None, chunk_events=0):
         """Run the power computation. Returns a dict with ``p_int, p_sw, p_gl,
         p_leak`` (W), ``t_max`` and, as requested, ``waveform`` (f32 W per
         cycle), ``event_count``/``glitch_count`` (u32 per cycle), per-event
         ``state_pre``/``lut_ij``/``is_glitch`` (u8), per-gate ``gate_power``
-        (f64 W, [gates, 4]: internal, switching, glitch, leakage), and ``ms_*``
+        (f64 W, [gates, 4]: internal, switching, glitch, leakage), per-cell
+        ``cell_power`` (f64 W, [cells, 4]: sums over each cell's gates), and ``ms_*``
         timings. ``glitch_all`` / ``esw_rise`` select the alternative readings
         (PA_RUN_GLITCH_ALL / PA_RUN_ESW_RISE). ``stream = (pin_off, t_ns,
         slew_ps, value)`` (host arrays; value may be None) runs pa_run_stream on
@@ -303,6 +306,7 @@ class PowerAnalyzer:
         r.lut_ij = arr("lut_ij", self.n_events, np.uint8, debug)
         r.is_glitch = arr("is_glitch", self.n_events, np.uint8, debug)
         r.gate_power_w = arr("gate_power", self.n_gates * 4, np.float64, gate_power)
+        r.cell_power_w = arr("cell_power", self.n_cells * 4, np.float64, cell_power)
         if stream is None:
             pa_run(self.ctx, p, r)
         else:
@@ -312,8 +316,9 @@ class PowerAnalyzer:
             ev = PaEvents(len(keep[0]) - 1, len(keep[1]), keep[0].ctypes.data, keep[1].ctypes.data,
                           keep[2].ctypes.data, None if keep[3] is None else keep[3].ctypes.data, PA_MEM_HOST)
             pa_run_stream(self.ctx, p, ev, chunk_events, r)
-        if "gate_power" in res and not (hasattr(res["gate_power"], "is_cuda") and res["gate_power"].is_cuda):
-            res["gate_power"] = np.asarray(res["gate_power"]).reshape(-1, 4)
+        for name in ("gate_power", "cell_power"):
+            if name in res and not (hasattr(res[name], "is_cuda") and res[name].is_cuda):
+                res[name] = np.asarray(res[name]).reshape(-1, 4)
         res.update(p_int=r.p_int_w, p_sw=r.p_sw_w, p_gl=r.p_gl_w, p_leak=r.p_leak_w, t_max=r.t_max_ns,
                    n_tiles=r.n_tiles, n_heavy=r.n_heavy, kernel_launches=r.kernel_launches, path=r.path)
         if timing:

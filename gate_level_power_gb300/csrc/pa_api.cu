@@ -57,7 +57,7 @@ struct pa_ctx {
   // scratch
   DevBuf value_tmp, err_word, tmax_bits;
   DevBuf bins, part_blk, part_counts, tiles, heavy, p0_tot, p_out;
-  DevBuf dbg[3], wave_tmp, cnt_tmp, chunk_sums, gate_tmp;
+  DevBuf dbg[3], wave_tmp, cnt_tmp, chunk_sums, gate_tmp, cell_tmp;
 
   // banded layout (pa_build_bands): persistent parts, build temporaries, run scratch
   BandLayout band;
@@ -200,6 +200,7 @@ struct PassBufs {
   uint32_t* cnt_gl = nullptr;
   uint8_t* dbg[3] = {nullptr, nullptr, nullptr};
   double* gate_e = nullptr;  // per-gate accumulators (fJ), converted to W in place
+  double* cell_p = nullptr;  // per-cell sums (W)
 };
 
 // stream: the events come with the call (pa_run_stream), so none need be
@@ -234,7 +235,7 @@ int check_run(pa_ctx* c, const pa_run_params* prm, const pa_result* out, const c
   plan->N = prm->n_cycles;
   plan->G = c->n_gates;
   plan->nblk = partition_blocks(plan->G);
-  plan->gate = out->gate_power_w != nullptr;
+  plan->gate = out->gate_power_w != nullptr || out->cell_power_w != nullptr;
   plan->debug = out->state_pre || out->lut_ij || out->is_glitch || plan->gate;
   plan->timing = (prm->flags & PA_RUN_TIMING) != 0;
   plan->glitch_all = (prm->flags & PA_RUN_GLITCH_ALL) != 0;
@@ -253,6 +254,28 @@ int check_run(pa_ctx* c, const pa_run_params* prm, const pa_result* out, const c
 // gates) -> final reduction. Counts are taken in f32 and the pass is repeated
 // with integer counts and fp64 bins if a cycle reached 2^24 events. Copies
 // outputs on success.
+// Per-gate and per-cell accumulators of a run that asks for them: the caller's
+// device arrays, else the context's temporaries (copied out at the end).
+int setup_gate_bufs(pa_ctx* c, const RunPlan& plan, const pa_result* out, PassBufs& B) {
+  if (!plan.gate) return PA_OK;
+  const bool dev = out->out_mem == PA_MEM_DEVICE;
+  if (out->gate_power_w && dev) {
+    B.gate_e = out->gate_power_w;
+  } else {
+    PA_TRY(dreserve(c, c->gate_tmp, ((size_t)plan.G + 1) * 4 * sizeof(double)));
+    B.gate_e = (double*)c->gate_tmp.p;
+  }
+  if (out->cell_power_w) {
+    if (dev) {
+      B.cell_p = out->cell_power_w;
+    } else {
+      PA_TRY(dreserve(c, c->cell_tmp, ((size_t)c->n_cells + 1) * 4 * sizeof(double)));
+      B.cell_p = (double*)c->cell_tmp.p;
+    }
+  }
+  return PA_OK;
+}
+
 // Run arguments of a pass over the loaded data (a streamed chunk replaces the
 // netlist and event pointers).
 RunArgs make_run_args(pa_ctx* c, const RunPlan& plan, const PassBufs& B) {
@@ -295,6 +318,7 @@ RunArgs make_run_args(pa_ctx* c, const RunPlan& plan, const PassBufs& B) {
   a.dbg_lut = B.dbg[1];
   a.dbg_glitch = B.dbg[2];
   a.gate_e = B.gate_e;
+  a.cell_p = B.cell_p;
   return a;
 }
 
@@ -323,6 +347,7 @@ int run_pass(pa_ctx* c, const RunPlan& plan, const PassBufs& B, pa_result* out, 
     CUDA_TRY(c, cudaMemsetAsync(B.p0_tot, 0, 8 * sizeof(double), st));
     CUDA_TRY(c, cudaMemsetAsync(c->err_word.p, 0xff, sizeof(unsigned long long), st));
     if (B.gate_e) CUDA_TRY(c, cudaMemsetAsync(B.gate_e, 0, (size_t)plan.G * 4 * sizeof(double), st));
+    if (B.cell_p) CUDA_TRY(c, cudaMemsetAsync(B.cell_p, 0, (size_t)c->n_cells * 4 * sizeof(double), st));
     if (band) {
       // the unbanded kernel's work list: no tiles, the big gates as heavy gates
       const uint32_t part[4] = {0, band->n_big, 0, 0};
@@ -365,6 +390,8 @@ int run_pass(pa_ctx* c, const RunPlan& plan, const PassBufs& B, pa_result* out, 
   if (out->glitch_count) CUDA_TRY(c, cudaMemcpyAsync(out->glitch_count, B.cnt_gl, (size_t)N * 4, dk, st));
   if (out->gate_power_w && out->gate_power_w != B.gate_e && plan.G)
     CUDA_TRY(c, cudaMemcpyAsync(out->gate_power_w, B.gate_e, (size_t)plan.G * 4 * sizeof(double), dk, st));
+  if (out->cell_power_w && out->cell_power_w != B.cell_p)
+    CUDA_TRY(c, cudaMemcpyAsync(out->cell_power_w, B.cell_p, (size_t)c->n_cells * 4 * sizeof(double), dk, st));
   if (plan.debug && c->n_events) {
     uint8_t* dst[3] = {out->state_pre, out->lut_ij, out->is_glitch};
     for (int i = 0; i < 3; ++i)
@@ -496,7 +523,6 @@ int run_stream(pa_ctx* c, const RunPlan& plan, const pa_events* ev, uint64_t tar
   PA_TRY(dreserve(c, c->cnt_tmp, (size_t)N * 2 * sizeof(uint32_t)));
   PA_TRY(dreserve(c, c->err_word, sizeof(unsigned long long)));
   PA_TRY(dreserve(c, c->tmax_bits, sizeof(unsigned int)));
-  if (plan.gate && out->out_mem != PA_MEM_DEVICE) PA_TRY(dreserve(c, c->gate_tmp, ((size_t)G + 1) * 4 * sizeof(double)));
   B.bins = (float4*)c->bins.p;
   B.part_blk = (uint32_t*)c->part_blk.p;
   B.part_counts = (uint32_t*)c->part_counts.p;
@@ -508,7 +534,7 @@ int run_stream(pa_ctx* c, const RunPlan& plan, const pa_events* ev, uint64_t tar
   B.wave = (float*)c->wave_tmp.p;
   B.cnt_ev = (uint32_t*)c->cnt_tmp.p;
   B.cnt_gl = (uint32_t*)c->cnt_tmp.p + N;
-  if (plan.gate) B.gate_e = out->out_mem == PA_MEM_DEVICE ? out->gate_power_w : (double*)c->gate_tmp.p;
+  PA_TRY(setup_gate_bufs(c, plan, out, B));
   cudaStream_t st = c->stream;
   const int nc = (int)ch.size();
   double p[4];
@@ -523,6 +549,7 @@ int run_stream(pa_ctx* c, const RunPlan& plan, const pa_events* ev, uint64_t tar
     CUDA_TRY(c, cudaMemsetAsync(c->err_word.p, 0xff, sizeof(unsigned long long), st));
     CUDA_TRY(c, cudaMemsetAsync(c->tmax_bits.p, 0, sizeof(unsigned int), st));
     if (B.gate_e) CUDA_TRY(c, cudaMemsetAsync(B.gate_e, 0, (size_t)G * 4 * sizeof(double), st));
+    if (B.cell_p) CUDA_TRY(c, cudaMemsetAsync(B.cell_p, 0, (size_t)c->n_cells * 4 * sizeof(double), st));
     CUDA_TRY(c, cudaStreamSynchronize(st));  // the slots are free and the accumulators clear
     PA_TRY(stream_copy(c, ev, ch[0], 0, false));
     for (int i = 0; i < nc; ++i) {
@@ -609,6 +636,8 @@ int run_stream(pa_ctx* c, const RunPlan& plan, const pa_events* ev, uint64_t tar
   if (out->glitch_count) CUDA_TRY(c, cudaMemcpyAsync(out->glitch_count, B.cnt_gl, (size_t)N * 4, dk, st));
   if (out->gate_power_w && out->gate_power_w != B.gate_e && G)
     CUDA_TRY(c, cudaMemcpyAsync(out->gate_power_w, B.gate_e, (size_t)G * 4 * sizeof(double), dk, st));
+  if (out->cell_power_w && out->cell_power_w != B.cell_p)
+    CUDA_TRY(c, cudaMemcpyAsync(out->cell_power_w, B.cell_p, (size_t)c->n_cells * 4 * sizeof(double), dk, st));
   CUDA_TRY(c, cudaStreamSynchronize(st));
   out->p_int_w = p[0];
   out->p_sw_w = p[1];
@@ -689,7 +718,7 @@ void pa_destroy(pa_ctx* c) {
   DevBuf* all[] = {&c->cells, &c->lut, &c->leak, &c->patch, &c->dleak, &c->gates, &c->pin_off, &c->gate_off, &c->t, &c->s,
                    &c->value_tmp, &c->err_word, &c->tmax_bits, &c->bins, &c->part_blk,
                    &c->part_counts, &c->tiles, &c->heavy, &c->p0_tot, &c->p_out, &c->dbg[0],
-                   &c->dbg[1], &c->dbg[2], &c->wave_tmp, &c->cnt_tmp, &c->gate_tmp, &c->scratch_small,
+                   &c->dbg[1], &c->dbg[2], &c->wave_tmp, &c->cnt_tmp, &c->gate_tmp, &c->cell_tmp, &c->scratch_small,
                    &c->chunk_sums, &c->b_bt, &c->b_bs, &c->b_btag, &c->b_urec, &c->b_ugate, &c->b_items,
                    &c->b_big, &c->b_bigf, &c->b_grank, &c->b_cnt, &c->b_evc, &c->b_ubase, &c->b_ebase,
                    &c->b_uband, &c->b_uoff, &c->b_flags, &c->b_ipos, &c->b_scan, &c->b_counters,
@@ -920,7 +949,6 @@ int pa_run(pa_ctx* c, const pa_run_params* prm, pa_result* out) {
   if (dbg_arrays) {
     for (int i = 0; i < 3; ++i) PA_TRY(dreserve(c, c->dbg[i], c->n_events));
   }
-  if (plan.gate && out->out_mem != PA_MEM_DEVICE) PA_TRY(dreserve(c, c->gate_tmp, ((size_t)G + 1) * 4 * sizeof(double)));
   B.bins = (float4*)c->bins.p;
   B.part_blk = (uint32_t*)c->part_blk.p;
   B.part_counts = (uint32_t*)c->part_counts.p;
@@ -933,7 +961,7 @@ int pa_run(pa_ctx* c, const pa_run_params* prm, pa_result* out) {
   B.cnt_ev = (uint32_t*)c->cnt_tmp.p;
   B.cnt_gl = (uint32_t*)c->cnt_tmp.p + N;
   for (int i = 0; i < 3; ++i) B.dbg[i] = dbg_arrays ? (uint8_t*)c->dbg[i].p : nullptr;
-  if (plan.gate) B.gate_e = out->out_mem == PA_MEM_DEVICE ? out->gate_power_w : (double*)c->gate_tmp.p;
+  PA_TRY(setup_gate_bufs(c, plan, out, B));
   return run_pass(c, plan, B, out, "pa_run", banded ? &c->band : nullptr);
 }
 
@@ -1023,7 +1051,7 @@ extern "C" int pa_run_noalloc(pa_ctx* c, const pa_run_params* prm, pa_result* ou
     return fail(c, PA_ERR_ARG, "pa_run_noalloc: %u gates exceed PA_NOALLOC_MAX_GATES (%u)", c->n_gates,
                 PA_NOALLOC_MAX_GATES);
   const bool any_array = out->waveform_w || out->event_count || out->glitch_count || out->state_pre ||
-                         out->lut_ij || out->is_glitch || out->gate_power_w;
+                         out->lut_ij || out->is_glitch || out->gate_power_w || out->cell_power_w;
   if (any_array && out->out_mem != PA_MEM_DEVICE)
     return fail(c, PA_ERR_ARG, "pa_run_noalloc: output arrays must be device memory (out_mem = PA_MEM_DEVICE)");
   CUDA_TRY(c, cudaSetDevice(c->device));
@@ -1045,7 +1073,10 @@ extern "C" int pa_run_noalloc(pa_ctx* c, const pa_run_params* prm, pa_result* ou
   B.dbg[0] = out->state_pre;
   B.dbg[1] = out->lut_ij;
   B.dbg[2] = out->is_glitch;
+  if (out->cell_power_w && !out->gate_power_w)
+    return fail(c, PA_ERR_ARG, "pa_run_noalloc: cell_power_w needs gate_power_w (the per-gate accumulators)");
   B.gate_e = out->gate_power_w;  // accumulated in place
+  B.cell_p = out->cell_power_w;
   return run_pass(c, plan, B, out, "pa_run_noalloc", nullptr);
 }
 

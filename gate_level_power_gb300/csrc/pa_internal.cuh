@@ -124,6 +124,7 @@ struct RunArgs {
   uint8_t* dbg_glitch;
   // per-gate energies {E_int, E_sw, E_gl, sum dP (t_max - t)} (fJ, zeroed), or null
   double* gate_e;
+  double* cell_p;          // [n_cells * 4] per-cell sums of the per-gate power (W, zeroed), or null
 };
 
 // ------------------------------------------------------------------ banded layout
@@ -273,7 +274,8 @@ int band_blocks_per_sm(bool pow2, bool debug, bool exact);
 cudaError_t launch_final_reduce(const RunArgs& a, double t_clk, double t_max, float* wave_out,
                                 double* p_out, bool exact, cudaStream_t st);
 // Per-gate power in place: a.gate_e (fJ) -> W, with each gate's initial-state
-// leakage held to t_max added to its leakage.
+// leakage held to t_max added to its leakage; with a.cell_p, each gate's power
+// is also added to its cell's.
 cudaError_t launch_gate_power(const RunArgs& a, double t_max, cudaStream_t st);
 // A chunk of pa_run_stream: its pin offsets (n_pins + 1, in place) made relative
 // to its first event ev0, and its gate records copied with pin bases relative

@@ -845,6 +845,11 @@ __global__ void __launch_bounds__(256) k_gate_power(const RunArgs a, double t_ma
   ge[1] *= f;
   ge[2] *= f;
   ge[3] = (p0 * t_max + ge[3]) * f;
+  if (a.cell_p) {
+    double* cp = a.cell_p + (size_t)r.cell * 4;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) atomicAdd(cp + m, ge[m]);
+  }
 }
 
 }  // namespace

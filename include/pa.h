@@ -197,7 +197,11 @@ typedef struct pa_run_params {
  *                           out_mem = PA_MEM_DEVICE the array itself accumulates
  *                           the gate energies, so after an error it may hold
  *                           partial values.
- * The per-event debug arrays and gate_power_w take a slower per-event path
+ *   cell_power_w[n_cells * 4]  per library cell c at [4c .. 4c + 3]: the sum of
+ *                           gate_power over the gates that instantiate it (W,
+ *                           double); may be asked for with or without
+ *                           gate_power_w.
+ * The per-event debug arrays, gate_power_w and cell_power_w take a slower per-event path
  * (one event per lane, extra global writes); ask for them only when needed.
  * With PA_RUN_TIMING, ms_* hold CUDA-event times of the partition, fused and
  * reduction kernels and of the whole device pass. n_tiles / n_heavy count the
@@ -218,6 +222,7 @@ typedef struct pa_result {
   uint32_t kernel_launches;
   uint32_t path;  /* out: PA_PATH_UNBANDED or PA_PATH_BANDED */
   double *gate_power_w;
+  double *cell_power_w;
 } pa_result;
 
 #define PA_PATH_UNBANDED 0u

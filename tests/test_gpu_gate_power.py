@@ -130,3 +130,41 @@ def test_gate_power_through_noalloc_matches_pa_run(glp):
             got = gp.cpu().numpy().reshape(-1, 4)
             assert_gate_parity(got, ref["gate_power"])
             assert r.p_int_w == pytest.approx(ref["p_int"], rel=TOL_G)
+
+
+def oracle_cell_power(w, og):
+    cp = np.zeros((len(w.n_inputs), 4))
+    np.add.at(cp, w.cell_id.astype(np.int64), og)
+    return cp
+
+
+@pytest.mark.parametrize("banded,with_gates", [(False, True), (True, True), (True, False)])
+def test_cell_power_sums_gate_power_by_cell(glp, banded, with_gates):
+    w = synth.generate(2)
+    with glp.PowerAnalyzer(0) as pa:
+        pa.load_workload(w)
+        if banded:
+            pa.build_bands(w.t_clk_ns)
+        r = pa.run(w.vdd, w.t_clk_ns, w.n_cycles, gate_power=with_gates, cell_power=True)
+    o = oracle.run(w, gate_power=True, threads=8)
+    oc = oracle_cell_power(w, o["gate_power"])
+    assert_gate_parity(r["cell_power"], oc)
+    if with_gates:
+        np.testing.assert_allclose(r["cell_power"], oracle_cell_power(w, r["gate_power"]), rtol=1e-9, atol=0)
+    for m, key in enumerate(("p_int", "p_sw", "p_gl", "p_leak")):
+        assert float(r["cell_power"][:, m].sum()) == pytest.approx(r[key], rel=TOL_G), key
+
+
+def test_cell_power_streamed_and_device_output(glp):
+    import torch
+    w = synth.generate(1)
+    cp = torch.full((len(w.n_inputs) * 4,), float("nan"), dtype=torch.float64, device="cuda")
+    with glp.PowerAnalyzer(0) as pa:
+        pa.load_library(w.n_inputs, w.n_slew, w.n_load, w.slew_axis, w.load_axis, w.lut_off, w.lut, w.leak_off,
+                        w.leak)
+        pa.load_netlist(w.cell_id, w.load_ff, w.init_in, w.init_out)
+        pa.run(w.vdd, w.t_clk_ns, w.n_cycles, out={"cell_power": cp}, stream=(w.pin_off, w.t_ns, w.slew_ps, w.value),
+               chunk_events=3000)
+    torch.cuda.synchronize()
+    o = oracle.run(w, gate_power=True)
+    assert_gate_parity(cp.cpu().numpy().reshape(-1, 4), oracle_cell_power(w, o["gate_power"]))
