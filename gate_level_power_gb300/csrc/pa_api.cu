@@ -331,7 +331,7 @@ int run_pass(pa_ctx* c, const RunPlan& plan, const PassBufs& B, pa_result* out, 
   if (band) {
     A.r = a;
     A.L = *band;
-    A.item_ctr = B.part_counts + 3;  // part_counts[2] is the unbanded kernel's item counter
+    A.item_ctr = B.part_counts + 4;  // part_counts[2] is the unbanded kernel's item counter
   }
   cudaStream_t st = c->stream;
   uint32_t launches = 0;
@@ -350,7 +350,7 @@ int run_pass(pa_ctx* c, const RunPlan& plan, const PassBufs& B, pa_result* out, 
     if (B.cell_p) CUDA_TRY(c, cudaMemsetAsync(B.cell_p, 0, (size_t)c->n_cells * 4 * sizeof(double), st));
     if (band) {
       // the unbanded kernel's work list: no tiles, the big gates as heavy gates
-      const uint32_t part[4] = {0, band->n_big, 0, 0};
+      const uint32_t part[8] = {0, band->n_big, 0, 0, 0, 0, 0, 0};
       CUDA_TRY(c, cudaMemcpyAsync(B.part_counts, part, sizeof(part), cudaMemcpyHostToDevice, st));
       CUDA_TRY(c, band_p0(a, st));
       launches += plan.G ? 1 : 0;
@@ -513,7 +513,7 @@ int run_stream(pa_ctx* c, const RunPlan& plan, const pa_events* ev, uint64_t tar
   PassBufs B;
   PA_TRY(dreserve(c, c->bins, (size_t)N * sizeof(float4)));
   PA_TRY(dreserve(c, c->part_blk, (size_t)(nblk + 1) * 2 * sizeof(uint32_t)));
-  PA_TRY(dreserve(c, c->part_counts, 4 * sizeof(uint32_t)));
+  PA_TRY(dreserve(c, c->part_counts, 8 * sizeof(uint32_t)));
   PA_TRY(dreserve(c, c->tiles, ((size_t)max_g + 1) * sizeof(Tile)));
   PA_TRY(dreserve(c, c->heavy, ((size_t)max_g + 1) * sizeof(uint32_t)));
   PA_TRY(dreserve(c, c->p0_tot, 8 * sizeof(double)));
@@ -937,7 +937,7 @@ int pa_run(pa_ctx* c, const pa_run_params* prm, pa_result* out) {
   PassBufs B;
   PA_TRY(dreserve(c, c->bins, (size_t)N * sizeof(float4)));
   PA_TRY(dreserve(c, c->part_blk, (size_t)(plan.nblk + 1) * 2 * sizeof(uint32_t)));
-  PA_TRY(dreserve(c, c->part_counts, 4 * sizeof(uint32_t)));
+  PA_TRY(dreserve(c, c->part_counts, 8 * sizeof(uint32_t)));
   PA_TRY(dreserve(c, c->tiles, ((size_t)G + 1) * sizeof(Tile)));
   PA_TRY(dreserve(c, c->heavy, ((size_t)G + 1) * sizeof(uint32_t)));
   PA_TRY(dreserve(c, c->p0_tot, 8 * sizeof(double)));
@@ -1001,7 +1001,7 @@ constexpr size_t kNaMaxC = PA_NOALLOC_MAX_CYCLES, kNaMaxG = PA_NOALLOC_MAX_GATES
 constexpr size_t kNaBins = 0;
 constexpr size_t kNaPartBlk = align256(kNaBins + kNaMaxC * sizeof(float4));
 constexpr size_t kNaPartCounts = align256(kNaPartBlk + (kNaMaxG / 256 + 2) * 2 * sizeof(uint32_t));
-constexpr size_t kNaTiles = align256(kNaPartCounts + 4 * sizeof(uint32_t));
+constexpr size_t kNaTiles = align256(kNaPartCounts + 8 * sizeof(uint32_t));
 constexpr size_t kNaHeavy = align256(kNaTiles + (kNaMaxG + 1) * sizeof(Tile));
 constexpr size_t kNaP0Tot = align256(kNaHeavy + (kNaMaxG + 1) * sizeof(uint32_t));
 constexpr size_t kNaPOut = align256(kNaP0Tot + 8 * sizeof(double));

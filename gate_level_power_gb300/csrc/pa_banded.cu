@@ -959,9 +959,16 @@ __device__ void bflush_band(const BandRunArgs& A, float* hist, float4* rows, uin
 __device__ __forceinline__ uint32_t item_band(const BandItem& it) { return it.bw & kItemBandMask; }
 
 // Thread 0 of a CTA: the next chunk [x, y) of items, y == x when none is left.
+// The last twentieth of the items goes out in quarter-size chunks from a
+// second counter (ctr[1]), so the CTAs finish closer together; big chunks for
+// the rest keep the band flushes few.
 __device__ __forceinline__ uint2 take_chunk(uint32_t* ctr, uint32_t n, uint32_t chunk) {
+  const uint32_t n_main = n - n / 20;
   const uint32_t x = atomicAdd(ctr, chunk);
-  return x >= n ? make_uint2(n, n) : make_uint2(x, x + min(chunk, n - x));
+  if (x < n_main) return make_uint2(x, x + min(chunk, n_main - x));
+  const uint32_t small = max(kChunkMin / 2, chunk / 4);
+  const uint32_t y = n_main + atomicAdd(ctr + 1, small);
+  return y >= n ? make_uint2(n, n) : make_uint2(y, y + min(small, n - y));
 }
 
 // First item in [lo, hi) whose band differs from `band` (items are band-sorted;

@@ -236,7 +236,7 @@ struct BandBuildArgs {
 struct BandRunArgs {
   RunArgs r;             // cells, lut, leak, gates, params, bins, totals, err, debug
   BandLayout L;
-  uint32_t* item_ctr;    // items handed out so far (zero before the launch)
+  uint32_t* item_ctr;    // [2] items handed out so far, of the main part and of the tail (zero before the launch)
   uint32_t chunk;        // items a CTA takes at a time (set by band_fused)
 };
 
