@@ -24,6 +24,15 @@ Printed (rank 0, one JSON line):
 
 ``--impl reference`` times the oracle alone (rank 0), on the same workload and
 metric.
+
+``--partition density|fixed`` times the paper's (gate, window) thread partition
+instead (one thread per gate window, a global atomic per event);
+``--partition-sweep`` compares the event-density-aware partition (n_evt,tgt =
+8) with globally fixed windows of 2 .. 32 cycles on one workload, one JSON line
+per setting with the fused-kernel time and the thread statistics (thread
+count, events per thread at the 50th/90th/99th percentile and the maximum), the
+comparison of the paper's Figs. 19 and 20 (the large skewed workload,
+``--config 3``, keeps the fixed settings' thread counts moderate).
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..6] [--synth KNOB=VALUE ...]
 """
 from __future__ import annotations
@@ -63,6 +72,14 @@ def parse_args():
     ap.add_argument("--unbanded", action="store_true",
                     help="skip the cycle-banded layout (pa_build_bands) and time the unbanded kernel")
     ap.add_argument("--band-cycles", type=int, default=0, help="cycles per band (0 = library default)")
+    ap.add_argument("--partition", choices=["events", "density", "fixed"], default="events",
+                    help="work partition: the library's event-count partition (default) or the paper's "
+                         "(gate, window) threads, event-density-aware or globally fixed")
+    ap.add_argument("--n-evt-tgt", type=int, default=8, help="density partition: target events per thread")
+    ap.add_argument("--n-thr-floor", type=int, default=1, help="density partition: parallelism floor")
+    ap.add_argument("--n-cyc-fix", type=int, default=8, help="fixed partition: cycles per thread")
+    ap.add_argument("--partition-sweep", action="store_true",
+                    help="time the density partition against fixed windows of 2..32 cycles (one line each)")
     ap.add_argument("--synth", nargs="*", default=[], metavar="KNOB=VALUE",
                     help="generator overrides for a scaled-down profiling case, e.g. n_gates=1000000 "
                          "n_events=200000000 (the line then names the workload as modified)")
@@ -374,7 +391,8 @@ def run_ours(args):
     pa = glp.PowerAnalyzer(local, stream.cuda_stream)
     pa.load_workload(w)
     build_ms = None
-    banded = not args.unbanded
+    windows = args.partition != "events" or args.partition_sweep
+    banded = not args.unbanded and not windows
     if banded:
         t0 = time.perf_counter()
         pa.build_bands(w.t_clk_ns, args.band_cycles)
@@ -384,8 +402,14 @@ def run_ours(args):
     glc = np.empty(N, np.uint32)
     out = dict(waveform=wave, event_count=evc, glitch_count=glc)
 
+    part = dict(partition=args.partition, n_evt_tgt=args.n_evt_tgt, n_thr_floor=args.n_thr_floor,
+                n_cyc_fix=args.n_cyc_fix)
+
     def step(timing=False):
-        return pa.run(w.vdd, w.t_clk_ns, N, out=out, timing=timing)
+        return pa.run(w.vdd, w.t_clk_ns, N, out=out, timing=timing, **part)
+
+    if args.partition_sweep:
+        return partition_sweep(args, pa, w, out, dist, rank)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -430,7 +454,8 @@ def run_ours(args):
             if path == "load_build_bands_run":
                 pa.build_bands(w.t_clk_ns, args.band_cycles)
             step()
-        paths = ["stream_run", "load_run_unbanded"] + (["load_build_bands_run"] if banded else [])
+        paths = (["load_run_windows"] if windows
+                 else ["stream_run", "load_run_unbanded"] + (["load_build_bands_run"] if banded else []))
         for path in paths:
             for _ in range(2):
                 e2e_step(path)
@@ -450,7 +475,7 @@ def run_ours(args):
     B = algorithmic_bytes(w)
     peak, peak_kind = hbm_peak()
     achieved = B / (fused_mean * 1e-3) / 1e9
-    kname = "k_band" if r["path"] == glp.PA_PATH_BANDED else "k_fused"
+    kname = {glp.PA_PATH_BANDED: "k_band", glp.PA_PATH_WINDOWS: "k_window"}.get(r["path"], "k_fused")
     traffic = None if args.synth else ncu_traffic(kname, args.config)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -467,6 +492,7 @@ def run_ours(args):
                          "frac": achieved / peak, "traffic": traffic,
                          "kernel": kname + " (fused dynamic + leakage power"
                          + (", with the unbanded kernel streaming big gates)" if r["path"] == glp.PA_PATH_BANDED
+                            else ", the paper's (gate, window) threads)" if r["path"] == glp.PA_PATH_WINDOWS
                             else ")"),
                          "algorithmic_bytes_per_launch": B, "mean_launch_ms": fused_mean,
                          "peak_source": f"{peak_kind} HBM copy bandwidth"},
@@ -483,13 +509,44 @@ def run_ours(args):
             "host_placement": host_placement,
             "p_total_w": r["p_int"] + r["p_sw"] + r["p_gl"] + r["p_leak"],
             "n_tiles": r["n_tiles"], "n_heavy": r["n_heavy"],
-            "path": "banded" if r["path"] == glp.PA_PATH_BANDED else "unbanded",
+            "path": {glp.PA_PATH_BANDED: "banded", glp.PA_PATH_WINDOWS: "windows"}.get(r["path"], "unbanded"),
+            **({"partition": dict(part, part_threads=r["part_threads"])} if windows else {}),
             **({"build_bands_ms": build_ms} if build_ms is not None else {}),
         }
         print(json.dumps(line), flush=True)
     pa.close()
     dist.close()
     del keep
+    return 0
+
+
+def partition_sweep(args, pa, w, out, dist, rank):
+    """The paper's partition comparison (Figs. 19 and 20) on this GPU: the
+    event-density-aware per-gate windows against globally fixed windows, on the
+    same (gate, window) thread kernel. One JSON line per setting."""
+    import torch
+    settings = [dict(partition="density", n_evt_tgt=args.n_evt_tgt, n_thr_floor=args.n_thr_floor)]
+    settings += [dict(partition="fixed", n_cyc_fix=n) for n in (2, 4, 8, 16, 32)]
+    steps = max(1, min(args.steps, 20))
+    for st in settings:
+        s = pa.run(w.vdd, w.t_clk_ns, w.n_cycles, out=out, part_stats=True, **st)  # thread statistics, untimed
+        for _ in range(max(3, args.warmup)):
+            pa.run(w.vdd, w.t_clk_ns, w.n_cycles, out=out, **st)
+        torch.cuda.synchronize()
+        ms = [pa.run(w.vdd, w.t_clk_ns, w.n_cycles, out=out, timing=True, **st) for _ in range(steps)]
+        fused = dist.max(statistics.median(m["ms_fused"] for m in ms))
+        total = dist.max(statistics.median(m["ms_total"] for m in ms))
+        if rank == 0:
+            print(json.dumps({
+                "metric": "fused kernel time, partition comparison", "unit": "ms", "value": fused,
+                "ms_pass": total, "events_per_s": w.n_events / (total * 1e-3), "steps": steps,
+                "config": {"workload": f"config {args.config}", "gates": w.n_gates, "events": w.n_events,
+                           "cycles": w.n_cycles}, **st,
+                "threads": s["part_threads"], "events_per_thread": dict(zip(("p50", "p90", "p99", "max"),
+                                                                           s["part_evt"])),
+            }), flush=True)
+    pa.close()
+    dist.close()
     return 0
 
 

@@ -22,7 +22,9 @@ PA_OK = 0
 PA_ERR_ARG, PA_ERR_ORDER, PA_ERR_UNSORTED, PA_ERR_RANGE = -1, -2, -3, -4
 PA_ERR_TOGGLE, PA_ERR_OOM, PA_ERR_CUDA, PA_ERR_INTERNAL = -5, -6, -7, -8
 PA_MEM_HOST, PA_MEM_DEVICE = 0, 1
-PA_RUN_TIMING, PA_RUN_GLITCH_ALL, PA_RUN_ESW_RISE = 1, 2, 4
+PA_RUN_TIMING, PA_RUN_GLITCH_ALL, PA_RUN_ESW_RISE, PA_RUN_PART_STATS = 1, 2, 4, 8
+PA_PART_EVENTS, PA_PART_DENSITY, PA_PART_FIXED = 0, 1, 2
+PARTITIONS = {"events": PA_PART_EVENTS, "density": PA_PART_DENSITY, "fixed": PA_PART_FIXED}
 
 ERR_NAMES = {0: "PA_OK", -1: "PA_ERR_ARG", -2: "PA_ERR_ORDER", -3: "PA_ERR_UNSORTED", -4: "PA_ERR_RANGE",
              -5: "PA_ERR_TOGGLE", -6: "PA_ERR_OOM", -7: "PA_ERR_CUDA", -8: "PA_ERR_INTERNAL"}
@@ -49,7 +51,8 @@ class PaEvents(ctypes.Structure):
 class PaRunParams(ctypes.Structure):
     _fields_ = [("vdd", ctypes.c_double), ("t_clk_ns", ctypes.c_float), ("n_cycles", ctypes.c_uint32),
                 ("t_max_ns", ctypes.c_double), ("tile_events", ctypes.c_uint32),
-                ("heavy_events", ctypes.c_uint32), ("flags", ctypes.c_uint32)]
+                ("heavy_events", ctypes.c_uint32), ("flags", ctypes.c_uint32), ("part_mode", ctypes.c_uint32),
+                ("n_evt_tgt", ctypes.c_uint32), ("n_thr_floor", ctypes.c_uint32), ("n_cyc_fix", ctypes.c_uint32)]
 
 
 class PaResult(ctypes.Structure):
@@ -59,7 +62,10 @@ class PaResult(ctypes.Structure):
                 ("lut_ij", _vp), ("is_glitch", _vp), ("ms_partition", ctypes.c_float),
                 ("ms_fused", ctypes.c_float), ("ms_reduce", ctypes.c_float), ("ms_total", ctypes.c_float),
                 ("n_tiles", ctypes.c_uint32), ("n_heavy", ctypes.c_uint32), ("kernel_launches", ctypes.c_uint32),
-                ("path", ctypes.c_uint32), ("gate_power_w", _vp), ("cell_power_w", _vp)]
+                ("path", ctypes.c_uint32), ("gate_power_w", _vp), ("cell_power_w", _vp),
+                ("part_threads", ctypes.c_uint64), ("part_evt_p50", ctypes.c_uint32),
+                ("part_evt_p90", ctypes.c_uint32), ("part_evt_p99", ctypes.c_uint32),
+                ("part_evt_max", ctypes.c_uint32)]
 
 
 class PaError(RuntimeError):
@@ -70,7 +76,7 @@ class PaError(RuntimeError):
 
 EXPORTS = ("pa_create", "pa_destroy", "pa_load_library", "pa_load_netlist", "pa_load_events", "pa_run",
            "pa_run_noalloc", "pa_run_stream", "pa_build_bands", "pa_default_params", "pa_last_error", "pa_version")
-PA_PATH_UNBANDED, PA_PATH_BANDED = 0, 1
+PA_PATH_UNBANDED, PA_PATH_BANDED, PA_PATH_WINDOWS = 0, 1, 2
 PA_NOALLOC_MAX_CYCLES = 65536
 PA_NOALLOC_MAX_GATES = 262144
 
@@ -266,7 +272,8 @@ class PowerAnalyzer:
 
     def run(self, vdd, t_clk_ns, n_cycles, t_max_ns=0.0, tile_events=0, heavy_events=0, timing=False,
             waveform=True, counts=True, debug=False, gate_power=False, cell_power=False, glitch_all=False,
-            esw_rise=False, out=None, stream=None, chunk_events=0):
+            esw_rise=False, out=None, stream=None, chunk_events=0, partition="events", n_evt_tgt=0,
+            n_thr_floor=0, n_cyc_fix=0, part_stats=False):
         """Run the power computation. Returns a dict with ``p_int, p_sw, p_gl,
         p_leak`` (W), ``t_max`` and, as requested, ``waveform`` (f32 W per
         cycle), ``event_count``/``glitch_count`` (u32 per cycle), per-event
@@ -278,12 +285,17 @@ class PowerAnalyzer:
         slew_ps, value)`` (host arrays; value may be None) runs pa_run_stream on
         that trace instead of pa_run on the loaded one, in chunks of about
         ``chunk_events`` events (0 = the library's default).
+        ``partition`` = "density" or "fixed" runs the paper's (gate, window)
+        thread partition (knobs ``n_evt_tgt``, ``n_thr_floor``, ``n_cyc_fix``;
+        0 = the library's defaults); the result then holds ``part_threads`` and,
+        with ``part_stats``, ``part_evt`` = (p50, p90, p99, max) events per thread.
         ``out`` may hold preallocated arrays (numpy or CUDA tensors) under the
         same names; CUDA tensors select device output."""
         flags = ((PA_RUN_TIMING if timing else 0) | (PA_RUN_GLITCH_ALL if glitch_all else 0)
-                 | (PA_RUN_ESW_RISE if esw_rise else 0))
+                 | (PA_RUN_ESW_RISE if esw_rise else 0) | (PA_RUN_PART_STATS if part_stats else 0))
         p = PaRunParams(float(vdd), float(t_clk_ns), int(n_cycles), float(t_max_ns), int(tile_events),
-                        int(heavy_events), flags)
+                        int(heavy_events), flags, PARTITIONS[partition], int(n_evt_tgt), int(n_thr_floor),
+                        int(n_cyc_fix))
         r = PaResult()
         res = {}
         out = dict(out or {})
@@ -321,6 +333,10 @@ class PowerAnalyzer:
                 res[name] = np.asarray(res[name]).reshape(-1, 4)
         res.update(p_int=r.p_int_w, p_sw=r.p_sw_w, p_gl=r.p_gl_w, p_leak=r.p_leak_w, t_max=r.t_max_ns,
                    n_tiles=r.n_tiles, n_heavy=r.n_heavy, kernel_launches=r.kernel_launches, path=r.path)
+        if r.path == PA_PATH_WINDOWS:
+            res["part_threads"] = r.part_threads
+            if part_stats:
+                res["part_evt"] = (r.part_evt_p50, r.part_evt_p90, r.part_evt_p99, r.part_evt_max)
         if timing:
             res.update(ms_partition=r.ms_partition, ms_fused=r.ms_fused, ms_reduce=r.ms_reduce,
                        ms_total=r.ms_total)

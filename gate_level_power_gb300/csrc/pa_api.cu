@@ -58,6 +58,9 @@ struct pa_ctx {
   DevBuf value_tmp, err_word, tmax_bits;
   DevBuf bins, part_blk, part_counts, tiles, heavy, p0_tot, p_out;
   DevBuf dbg[3], wave_tmp, cnt_tmp, chunk_sums, gate_tmp, cell_tmp;
+  // the paper's (gate, window) partition: per-gate plan, thread offsets, scan
+  // scratch, total slots (+ the largest events per thread), histogram
+  DevBuf w_ncyc, w_nthr, w_off, w_blk, w_tot, w_hist;
 
   // banded layout (pa_build_bands): persistent parts, build temporaries, run scratch
   BandLayout band;
@@ -183,6 +186,9 @@ struct RunPlan {
   uint32_t tile = 0, heavy = 0, N = 0, G = 0, nblk = 0;
   bool pow2 = false, debug = false, timing = false, gate = false, glitch_all = false, esw_rise = false;
   double vdd = 0.0;
+  // partition: PA_PART_*, with the paper's knobs
+  uint32_t part_mode = PA_PART_EVENTS, n_evt_tgt = 8, n_thr_floor = 1, n_cyc_fix = 1;
+  bool part_stats = false;
 };
 
 // Device buffers of one run (owned by the ctx or by the no-alloc scratch).
@@ -242,8 +248,16 @@ int check_run(pa_ctx* c, const pa_run_params* prm, const pa_result* out, const c
   plan->esw_rise = (prm->flags & PA_RUN_ESW_RISE) != 0;
   // the alternative readings are ablations: they run in the per-event path
   if (plan->glitch_all || plan->esw_rise) plan->debug = true;
-  if (prm->flags & ~(PA_RUN_TIMING | PA_RUN_GLITCH_ALL | PA_RUN_ESW_RISE))
+  if (prm->flags & ~(PA_RUN_TIMING | PA_RUN_GLITCH_ALL | PA_RUN_ESW_RISE | PA_RUN_PART_STATS))
     return fail(c, PA_ERR_ARG, "%s: unknown flags 0x%x", who, prm->flags);
+  if (prm->part_mode > PA_PART_FIXED) return fail(c, PA_ERR_ARG, "%s: unknown part_mode %u", who, prm->part_mode);
+  if (stream && prm->part_mode != PA_PART_EVENTS)
+    return fail(c, PA_ERR_ARG, "%s: part_mode must be PA_PART_EVENTS on a streamed run", who);
+  plan->part_mode = prm->part_mode;
+  plan->n_evt_tgt = prm->n_evt_tgt ? prm->n_evt_tgt : 8u;
+  plan->n_thr_floor = prm->n_thr_floor ? prm->n_thr_floor : 1u;
+  plan->n_cyc_fix = prm->n_cyc_fix ? prm->n_cyc_fix : 1u;
+  plan->part_stats = (prm->flags & PA_RUN_PART_STATS) != 0 && plan->part_mode != PA_PART_EVENTS;
   plan->pow2 = is_pow2(plan->T);
   plan->vdd = prm->vdd;
   return PA_OK;
@@ -322,8 +336,22 @@ RunArgs make_run_args(pa_ctx* c, const RunPlan& plan, const PassBufs& B) {
   return a;
 }
 
+// Nearest-rank percentile q of a histogram of n counts (bins[i]: counts equal
+// to i; the last bin holds the rest): the smallest x with at least
+// ceil(q n / 100) counts <= x.
+uint32_t hist_rank(const std::vector<unsigned long long>& bins, uint64_t n, uint32_t q) {
+  if (n == 0) return 0;
+  const uint64_t r = (q * n + 99) / 100;
+  uint64_t cum = 0;
+  for (size_t i = 0; i < bins.size(); ++i) {
+    cum += bins[i];
+    if (cum >= r) return (uint32_t)i;
+  }
+  return (uint32_t)(bins.size() - 1);
+}
+
 int run_pass(pa_ctx* c, const RunPlan& plan, const PassBufs& B, pa_result* out, const char* who,
-             const BandLayout* band) {
+             const BandLayout* band, const WinArgs* win = nullptr) {
   const uint32_t N = plan.N;
   RunArgs a = make_run_args(c, plan, B);
   if (band) a.heavy = band->big;  // the unbanded kernel streams the gates the layout left out
@@ -348,7 +376,17 @@ int run_pass(pa_ctx* c, const RunPlan& plan, const PassBufs& B, pa_result* out, 
     CUDA_TRY(c, cudaMemsetAsync(c->err_word.p, 0xff, sizeof(unsigned long long), st));
     if (B.gate_e) CUDA_TRY(c, cudaMemsetAsync(B.gate_e, 0, (size_t)plan.G * 4 * sizeof(double), st));
     if (B.cell_p) CUDA_TRY(c, cudaMemsetAsync(B.cell_p, 0, (size_t)c->n_cells * 4 * sizeof(double), st));
-    if (band) {
+    if (win) {
+      // the paper's partition: cycles and threads per gate, then P0
+      CUDA_TRY(c, cudaMemsetAsync(win->tot_slots, 0, (size_t)kWinTotSlots * 4 * sizeof(double), st));
+      if (win->hist) {
+        CUDA_TRY(c, cudaMemsetAsync(win->hist, 0, (size_t)kWinHistBins * sizeof(unsigned long long), st));
+        CUDA_TRY(c, cudaMemsetAsync(win->ev_max, 0, sizeof(unsigned int), st));
+      }
+      CUDA_TRY(c, launch_window_plan(a, *win, st));
+      CUDA_TRY(c, band_p0(a, st));
+      launches += plan.G ? 5 : 0;
+    } else if (band) {
       // the unbanded kernel's work list: no tiles, the big gates as heavy gates
       const uint32_t part[8] = {0, band->n_big, 0, 0, 0, 0, 0, 0};
       CUDA_TRY(c, cudaMemcpyAsync(B.part_counts, part, sizeof(part), cudaMemcpyHostToDevice, st));
@@ -360,11 +398,16 @@ int run_pass(pa_ctx* c, const RunPlan& plan, const PassBufs& B, pa_result* out, 
       launches += plan.nblk ? 3 : 0;
     }
     if (plan.timing) CUDA_TRY(c, cudaEventRecord(c->ev[1], st));
+    if (win) {
+      const int grid = c->sm_count * window_blocks_per_sm(plan.pow2, plan.debug, exact != 0);
+      CUDA_TRY(c, launch_window(a, *win, grid, plan.pow2, plan.debug, exact != 0, st));
+      launches += 2;
+    }
     if (band) {
       CUDA_TRY(c, band_fused(A, c->sm_count, plan.debug, exact != 0, st));
       launches += band->n_items ? 1 : 0;
     }
-    if (!band || band->n_big) {
+    if (!win && (!band || band->n_big)) {
       const int grid = c->sm_count * fused_blocks_per_sm(plan.pow2, plan.debug, exact != 0);
       CUDA_TRY(c, launch_fused(a, grid, plan.pow2, plan.debug, exact != 0, st));
       launches += 1;
@@ -379,7 +422,7 @@ int run_pass(pa_ctx* c, const RunPlan& plan, const PassBufs& B, pa_result* out, 
     if (plan.timing) CUDA_TRY(c, cudaEventRecord(c->ev[3], st));
     CUDA_TRY(c, cudaMemcpyAsync(p, B.p_out, sizeof(p), cudaMemcpyDeviceToHost, st));
     CUDA_TRY(c, cudaMemcpyAsync(&key, c->err_word.p, sizeof(key), cudaMemcpyDeviceToHost, st));
-    CUDA_TRY(c, cudaMemcpyAsync(counts, B.part_counts, sizeof(counts), cudaMemcpyDeviceToHost, st));
+    if (!win) CUDA_TRY(c, cudaMemcpyAsync(counts, B.part_counts, sizeof(counts), cudaMemcpyDeviceToHost, st));
     CUDA_TRY(c, cudaStreamSynchronize(st));
     if (key == kNoErr) break;
     if ((key & 0xff) != kErrCountOverflow || exact) return map_dev_err(c, key, who);
@@ -403,7 +446,25 @@ int run_pass(pa_ctx* c, const RunPlan& plan, const PassBufs& B, pa_result* out, 
   out->p_gl_w = p[2];
   out->p_leak_w = p[3];
   out->t_max_ns = plan.t_max;
-  if (band) {
+  out->part_threads = 0;
+  out->part_evt_p50 = out->part_evt_p90 = out->part_evt_p99 = out->part_evt_max = 0;
+  if (win) {
+    out->n_tiles = 0;
+    out->n_heavy = 0;
+    uint64_t n_thr = 0;
+    CUDA_TRY(c, cudaMemcpy(&n_thr, win->thr_off + plan.G, sizeof(n_thr), cudaMemcpyDeviceToHost));
+    out->part_threads = n_thr;
+    if (win->hist) {
+      std::vector<unsigned long long> h(kWinHistBins);
+      unsigned int mx = 0;
+      CUDA_TRY(c, cudaMemcpy(h.data(), win->hist, h.size() * sizeof(unsigned long long), cudaMemcpyDeviceToHost));
+      CUDA_TRY(c, cudaMemcpy(&mx, win->ev_max, sizeof(mx), cudaMemcpyDeviceToHost));
+      out->part_evt_p50 = hist_rank(h, n_thr, 50);
+      out->part_evt_p90 = hist_rank(h, n_thr, 90);
+      out->part_evt_p99 = hist_rank(h, n_thr, 99);
+      out->part_evt_max = mx;
+    }
+  } else if (band) {
     out->n_tiles = band->n_items;
     out->n_heavy = c->band_windowed + band->n_big;
   } else {
@@ -411,7 +472,7 @@ int run_pass(pa_ctx* c, const RunPlan& plan, const PassBufs& B, pa_result* out, 
     out->n_heavy = counts[1];
   }
   out->kernel_launches = launches;
-  out->path = band ? PA_PATH_BANDED : PA_PATH_UNBANDED;
+  out->path = win ? PA_PATH_WINDOWS : band ? PA_PATH_BANDED : PA_PATH_UNBANDED;
   if (plan.timing) {
     cudaEventElapsedTime(&out->ms_partition, c->ev[0], c->ev[1]);
     cudaEventElapsedTime(&out->ms_fused, c->ev[1], c->ev[2]);
@@ -722,7 +783,8 @@ void pa_destroy(pa_ctx* c) {
                    &c->chunk_sums, &c->b_bt, &c->b_bs, &c->b_btag, &c->b_urec, &c->b_ugate, &c->b_items,
                    &c->b_big, &c->b_bigf, &c->b_grank, &c->b_cnt, &c->b_evc, &c->b_ubase, &c->b_ebase,
                    &c->b_uband, &c->b_uoff, &c->b_flags, &c->b_ipos, &c->b_scan, &c->b_counters,
-                   &c->b_urec2, &c->b_dense, &c->b_gflag, &c->b_part};
+                   &c->b_urec2, &c->b_dense, &c->b_gflag, &c->b_part, &c->w_ncyc, &c->w_nthr, &c->w_off,
+                   &c->w_blk, &c->w_tot, &c->w_hist};
   for (DevBuf* b : all) dfree(*b);
   for (int i = 0; i < 2; ++i) {
     DevBuf* st[] = {&c->st_t[i], &c->st_s[i], &c->st_v[i], &c->st_pin[i], &c->st_gates[i], &c->st_goff[i]};
@@ -962,6 +1024,28 @@ int pa_run(pa_ctx* c, const pa_run_params* prm, pa_result* out) {
   B.cnt_gl = (uint32_t*)c->cnt_tmp.p + N;
   for (int i = 0; i < 3; ++i) B.dbg[i] = dbg_arrays ? (uint8_t*)c->dbg[i].p : nullptr;
   PA_TRY(setup_gate_bufs(c, plan, out, B));
+  if (plan.part_mode != PA_PART_EVENTS) {
+    // the paper's (gate, window) thread partition
+    PA_TRY(dreserve(c, c->w_ncyc, ((size_t)G + 1) * sizeof(uint32_t)));
+    PA_TRY(dreserve(c, c->w_nthr, ((size_t)G + 1) * sizeof(uint32_t)));
+    PA_TRY(dreserve(c, c->w_off, ((size_t)G + 1) * sizeof(uint64_t)));
+    PA_TRY(dreserve(c, c->w_blk, ((size_t)band_scan_blocks(G) + 1) * sizeof(uint64_t)));
+    PA_TRY(dreserve(c, c->w_tot, (size_t)kWinTotSlots * 4 * sizeof(double) + 256));
+    if (plan.part_stats) PA_TRY(dreserve(c, c->w_hist, (size_t)kWinHistBins * sizeof(unsigned long long)));
+    WinArgs w;
+    w.mode = plan.part_mode;
+    w.n_evt_tgt = plan.n_evt_tgt;
+    w.n_thr_floor = plan.n_thr_floor;
+    w.n_cyc_fix = plan.n_cyc_fix;
+    w.ncyc = (uint32_t*)c->w_ncyc.p;
+    w.nthr = (uint32_t*)c->w_nthr.p;
+    w.thr_off = (uint64_t*)c->w_off.p;
+    w.scan_blk = (uint64_t*)c->w_blk.p;
+    w.tot_slots = (double*)c->w_tot.p;
+    w.ev_max = (unsigned int*)((char*)c->w_tot.p + (size_t)kWinTotSlots * 4 * sizeof(double));
+    w.hist = plan.part_stats ? (unsigned long long*)c->w_hist.p : nullptr;
+    return run_pass(c, plan, B, out, "pa_run", nullptr, &w);
+  }
   return run_pass(c, plan, B, out, "pa_run", banded ? &c->band : nullptr);
 }
 
@@ -1044,6 +1128,8 @@ int noalloc_scratch(pa_ctx* c, int dev, unsigned char** out) {
 extern "C" int pa_run_noalloc(pa_ctx* c, const pa_run_params* prm, pa_result* out) {
   RunPlan plan;
   PA_TRY(check_run(c, prm, out, "pa_run_noalloc", &plan));
+  if (plan.part_mode != PA_PART_EVENTS)
+    return fail(c, PA_ERR_ARG, "pa_run_noalloc: part_mode must be PA_PART_EVENTS (the window partition allocates)");
   if (prm->n_cycles > PA_NOALLOC_MAX_CYCLES)
     return fail(c, PA_ERR_ARG, "pa_run_noalloc: n_cycles %u exceeds PA_NOALLOC_MAX_CYCLES (%u)", prm->n_cycles,
                 PA_NOALLOC_MAX_CYCLES);

@@ -271,6 +271,32 @@ cudaError_t band_p0(const RunArgs& r, cudaStream_t st);
 cudaError_t band_fused(const BandRunArgs& A, int sm_count, bool debug, bool exact, cudaStream_t st);
 int band_blocks_per_sm(bool pow2, bool debug, bool exact);
 
+// The paper's (gate, window) thread partition (pa_window.cu): plan, then the
+// window kernel, whose per-thread sums go through kWinTotSlots slots into
+// RunArgs::totals.
+constexpr uint32_t kWinHistBins = 65536;  // events-per-thread histogram (the last bin: 65535 or more)
+constexpr int kWinTotSlots = 256;         // total accumulator slots (spread the CTAs' fp64 atomics)
+
+struct WinArgs {
+  uint32_t mode;          // PA_PART_DENSITY or PA_PART_FIXED
+  uint32_t n_evt_tgt, n_thr_floor, n_cyc_fix;
+  uint32_t* ncyc;         // [G] cycles per thread of each gate
+  uint32_t* nthr;         // [G] threads of each gate
+  uint64_t* thr_off;      // [G + 1] first thread of each gate; [G] = threads in all
+  uint64_t* scan_blk;     // scan scratch (band_scan_blocks(G) entries)
+  double* tot_slots;      // [kWinTotSlots * 4] zeroed before the window kernel
+  unsigned long long* hist;  // [kWinHistBins] events per thread (zeroed), or null: no statistics
+  unsigned int* ev_max;   // largest events per thread (zeroed; with hist)
+};
+
+// Plan: cycles and threads per gate, and their scan (thr_off[G] = threads).
+cudaError_t launch_window_plan(const RunArgs& a, const WinArgs& w, cudaStream_t st);
+// The window kernel over the planned (gate, window) threads (grid-stride over
+// chunks of thread ids, the count read on the device), then the totals fold.
+cudaError_t launch_window(const RunArgs& a, const WinArgs& w, int grid, bool pow2, bool debug, bool exact,
+                          cudaStream_t st);
+int window_blocks_per_sm(bool pow2, bool debug, bool exact);
+
 cudaError_t launch_final_reduce(const RunArgs& a, double t_clk, double t_max, float* wave_out,
                                 double* p_out, bool exact, cudaStream_t st);
 // Per-gate power in place: a.gate_e (fJ) -> W, with each gate's initial-state

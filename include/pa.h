@@ -51,7 +51,7 @@
 extern "C" {
 #endif
 
-#define PA_VERSION 2
+#define PA_VERSION 3
 
 #define PA_OK 0
 #define PA_ERR_ARG (-1)      /* null pointer, bad size, bad axis, bad parameter      */
@@ -153,6 +153,31 @@ typedef struct pa_events {
  * Either flag selects the slower per-event path (as debug outputs do). */
 #define PA_RUN_GLITCH_ALL 2u
 #define PA_RUN_ESW_RISE 4u
+/* With part_mode PA_PART_DENSITY or PA_PART_FIXED: count the events of every
+ * (gate, window) thread and report their quantiles in pa_result (a slower
+ * run; leave it off when timing the partition). */
+#define PA_RUN_PART_STATS 8u
+
+/* Work partitions (pa_run_params.part_mode). The results do not depend on the
+ * partition beyond floating-point summation order; the paper's two partitions
+ * are there to compare them (Figs. 5, 19 and 20: event-density-aware per-gate
+ * cycle windows against one globally fixed window length), on one kernel that
+ * runs one thread per (gate, window) and adds every event to the cycle bins
+ * with a global atomic, as the paper's fused kernel does.
+ *   PA_PART_EVENTS   the library's own event-count partition (default): the
+ *                    banded layout if one is built for this clock, else
+ *                    event-count tiles of the CSR arrays;
+ *   PA_PART_DENSITY  per gate g: rho = N_evt^(g) / n_cycles, n_cyc,floor =
+ *                    ceil(n_cycles / n_thr_floor), rho_floor = n_evt_tgt /
+ *                    n_cyc,floor, n_cyc^(g) = floor(n_evt_tgt / (rho +
+ *                    rho_floor) + 1/2) clamped to [1, n_cycles] (fp64);
+ *   PA_PART_FIXED    n_cyc^(g) = min(n_cyc_fix, n_cycles) for every gate.
+ * Thread tau of gate g takes the events whose cycle floor(fl32(t / t_clk))
+ * lies in [tau n_cyc^(g), (tau + 1) n_cyc^(g)); a gate has
+ * ceil(n_cycles / n_cyc^(g)) threads, gates without events included. */
+#define PA_PART_EVENTS 0u
+#define PA_PART_DENSITY 1u
+#define PA_PART_FIXED 2u
 
 /*
  * Run parameters. pa_default_params() fills the defaults.
@@ -166,6 +191,11 @@ typedef struct pa_events {
  *                  windows by one CTA (0 = default 2048); tile_events +
  *                  heavy_events must not exceed 4096
  *   flags          PA_RUN_* bits
+ *   part_mode      PA_PART_* (pa_run only; the other entry points take
+ *                  PA_PART_EVENTS)
+ *   n_evt_tgt      PA_PART_DENSITY: target events per thread (0 = 8, the paper's)
+ *   n_thr_floor    PA_PART_DENSITY: parallelism floor N_thr,floor (0 = 1)
+ *   n_cyc_fix      PA_PART_FIXED: cycles per thread (0 = 1)
  * The partition knobs change only how work is cut, never the results beyond
  * floating-point summation order.
  */
@@ -177,6 +207,10 @@ typedef struct pa_run_params {
   uint32_t tile_events;
   uint32_t heavy_events;
   uint32_t flags;
+  uint32_t part_mode;
+  uint32_t n_evt_tgt;
+  uint32_t n_thr_floor;
+  uint32_t n_cyc_fix;
 } pa_run_params;
 
 /*
@@ -206,6 +240,11 @@ typedef struct pa_run_params {
  * With PA_RUN_TIMING, ms_* hold CUDA-event times of the partition, fused and
  * reduction kernels and of the whole device pass. n_tiles / n_heavy count the
  * work items (light tiles / heavy items); path says which kernel ran.
+ * With part_mode PA_PART_DENSITY or PA_PART_FIXED, part_threads is the number
+ * of (gate, window) threads, and with PA_RUN_PART_STATS the part_evt_* hold
+ * the nearest-rank 50th, 90th and 99th percentiles and the maximum of the
+ * events per thread (the smallest x with at least ceil(q n / 100) of the n
+ * threads at or below x; percentiles of 65535 or more read 65535).
  */
 typedef struct pa_result {
   double p_int_w, p_sw_w, p_gl_w, p_leak_w;
@@ -223,10 +262,13 @@ typedef struct pa_result {
   uint32_t path;  /* out: PA_PATH_UNBANDED or PA_PATH_BANDED */
   double *gate_power_w;
   double *cell_power_w;
+  uint64_t part_threads;
+  uint32_t part_evt_p50, part_evt_p90, part_evt_p99, part_evt_max;
 } pa_result;
 
 #define PA_PATH_UNBANDED 0u
 #define PA_PATH_BANDED 1u
+#define PA_PATH_WINDOWS 2u /* the paper's (gate, window) thread partition */
 
 /* Create a context on CUDA device `cuda_device`. `cuda_stream` is a
  * cudaStream_t to run on (borrowed, must outlive the ctx) or NULL for a stream

@@ -34,7 +34,7 @@ def test_library_exports_every_declared_symbol():
 def test_version_and_defaults_without_gpu():
     import gate_level_power_gb300 as glp
     glp.build()
-    assert glp.pa_version() == 2
+    assert glp.pa_version() == 3
     p = glp.pa_default_params()
     assert p.n_cycles == 1 and abs(p.vdd - 0.9) < 1e-12 and p.t_clk_ns == 1.0
 
@@ -76,3 +76,25 @@ def test_create_without_gpu_fails_cleanly():
     with pytest.raises(glp.PaError) as ei:
         glp.pa_create(0)
     assert ei.value.code == glp.PA_ERR_CUDA
+
+
+def test_ctypes_structs_match_the_c_layout(tmp_path):
+    # the binding's ctypes mirrors of the header's structs: sizes and offsets
+    import subprocess
+    import gate_level_power_gb300 as glp
+    structs = {"pa_run_params": glp.PaRunParams, "pa_result": glp.PaResult, "pa_events": glp.PaEvents}
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "pa.h"', "int main(void) {"]
+    for cname, cls in structs.items():
+        lines.append(f'  printf("{cname} %zu\\n", sizeof({cname}));')
+        for f in cls._fields_:
+            lines.append(f'  printf("{cname}.{f[0]} %zu\\n", offsetof({cname}, {f[0]}));')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.check_call(["gcc", "-std=c11", f"-I{os.path.join(ROOT, 'include')}", str(src), "-o", str(exe)])
+    got = dict(line.split() for line in subprocess.check_output([str(exe)]).decode().splitlines())
+    for cname, cls in structs.items():
+        assert int(got[cname]) == ctypes.sizeof(cls), cname
+        for f in cls._fields_:
+            assert int(got[f"{cname}.{f[0]}"]) == getattr(cls, f[0]).offset, (cname, f[0])

@@ -64,7 +64,7 @@ def test_unknown_flag_is_rejected(glp):
     w = synth.generate(1)
     with glp.PowerAnalyzer(0) as pa:
         pa.load_workload(w)
-        p = glp.PaRunParams(float(w.vdd), float(w.t_clk_ns), int(w.n_cycles), 0.0, 0, 0, 8)
+        p = glp.PaRunParams(float(w.vdd), float(w.t_clk_ns), int(w.n_cycles), 0.0, 0, 0, 16)
         with pytest.raises(glp.PaError) as ei:
             glp.pa_run(pa.ctx, p, glp.PaResult())
         assert ei.value.code == glp.PA_ERR_ARG
