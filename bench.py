@@ -32,7 +32,9 @@ instead (one thread per gate window, a global atomic per event);
 per setting with the fused-kernel time and the thread statistics (thread
 count, events per thread at the 50th/90th/99th percentile and the maximum), the
 comparison of the paper's Figs. 19 and 20 (the large skewed workload,
-``--config 3``, keeps the fixed settings' thread counts moderate).
+``--config 3``, keeps the fixed settings' thread counts moderate), followed by
+the library's own event-count partition (unbanded, then banded) on the same
+workload.
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..6] [--synth KNOB=VALUE ...]
 """
 from __future__ import annotations
@@ -527,23 +529,34 @@ def partition_sweep(args, pa, w, out, dist, rank):
     import torch
     settings = [dict(partition="density", n_evt_tgt=args.n_evt_tgt, n_thr_floor=args.n_thr_floor)]
     settings += [dict(partition="fixed", n_cyc_fix=n) for n in (2, 4, 8, 16, 32)]
+    # the library's own event-count partition beside them: event-count tiles of
+    # the per-pin arrays (unbanded kernel), then the cycle-banded layout
+    settings += [dict(partition="events"), dict(partition="events", banded=True)]
     steps = max(1, min(args.steps, 20))
     for st in settings:
-        s = pa.run(w.vdd, w.t_clk_ns, w.n_cycles, out=out, part_stats=True, **st)  # thread statistics, untimed
+        st = dict(st)
+        if st.pop("banded", False):
+            pa.build_bands(w.t_clk_ns, args.band_cycles)
+        windows = st["partition"] != "events"
+        s = pa.run(w.vdd, w.t_clk_ns, w.n_cycles, out=out, part_stats=windows, **st)  # statistics, untimed
         for _ in range(max(3, args.warmup)):
             pa.run(w.vdd, w.t_clk_ns, w.n_cycles, out=out, **st)
         torch.cuda.synchronize()
         ms = [pa.run(w.vdd, w.t_clk_ns, w.n_cycles, out=out, timing=True, **st) for _ in range(steps)]
         fused = dist.max(statistics.median(m["ms_fused"] for m in ms))
         total = dist.max(statistics.median(m["ms_total"] for m in ms))
+        if windows:
+            work = {"threads": s["part_threads"],
+                    "events_per_thread": dict(zip(("p50", "p90", "p99", "max"), s["part_evt"]))}
+        else:
+            work = {"path": "banded" if s["path"] == 1 else "unbanded", "work_items": s["n_tiles"],
+                    "heavy_items": s["n_heavy"]}
         if rank == 0:
             print(json.dumps({
                 "metric": "fused kernel time, partition comparison", "unit": "ms", "value": fused,
                 "ms_pass": total, "events_per_s": w.n_events / (total * 1e-3), "steps": steps,
                 "config": {"workload": f"config {args.config}", "gates": w.n_gates, "events": w.n_events,
-                           "cycles": w.n_cycles}, **st,
-                "threads": s["part_threads"], "events_per_thread": dict(zip(("p50", "p90", "p99", "max"),
-                                                                           s["part_evt"])),
+                           "cycles": w.n_cycles}, **st, **work,
             }), flush=True)
     pa.close()
     dist.close()

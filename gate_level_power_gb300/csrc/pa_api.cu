@@ -55,7 +55,7 @@ struct pa_ctx {
   DevBuf pin_off, gate_off, t, s;
 
   // scratch
-  DevBuf value_tmp, err_word, tmax_bits;
+  DevBuf value_tmp, err_word, tmax_bits, val_starts;
   DevBuf bins, part_blk, part_counts, tiles, heavy, p0_tot, p_out;
   DevBuf dbg[3], wave_tmp, cnt_tmp, chunk_sums, gate_tmp, cell_tmp;
   // the paper's (gate, window) partition: per-gate plan, thread offsets, scan
@@ -517,41 +517,43 @@ int run_stream(pa_ctx* c, const RunPlan& plan, const pa_events* ev, uint64_t tar
   const uint32_t G = c->n_gates, N = plan.N;
   const uint64_t P = ev->n_pins, E = ev->n_events;
   const uint64_t* hpo = ev->pin_off;
-  // the host pin offsets decide the chunks: check them first
   if (hpo[0] != 0 || hpo[P] != E) return fail(c, PA_ERR_ARG, "%s: pin_off must start at 0 and end at n_events", who);
-  for (uint64_t p = 0; p < P; ++p)
-    if (hpo[p + 1] < hpo[p]) return fail(c, PA_ERR_ARG, "%s: pin_off not monotone (first at pin %llu)", who,
-                                         (unsigned long long)p);
-  // chunks of whole gates
+  // Chunks of whole gates, each the longest run of gates from its first one
+  // that holds at most `target` events (at least one gate), found by binary
+  // search over the gates' first event offsets: a few reads of the host pin
+  // offsets per chunk, none per pin. The offsets are checked where they cut
+  // the trace (here: chunk boundaries in order, so every copy stays inside
+  // the caller's arrays) and inside each chunk on the device before the chunk
+  // reaches the bins (monotone, ending at the chunk's event count), which
+  // together check the whole array.
+  auto gate_pin = [&](uint32_t g) -> uint64_t { return g < G ? (uint64_t)c->h_gates[g].pin_base : P; };
   std::vector<StreamChunk> ch;
-  {
-    StreamChunk k{0, 0, 0, 0, 0, 0};
-    uint64_t acc = 0;
-    for (uint32_t g = 0; g < G; ++g) {
-      const GateRec& r = c->h_gates[g];
-      const uint64_t p1 = (uint64_t)r.pin_base + ((r.init >> 16) & 0xffu) + 1;
-      const uint64_t ne = hpo[p1] - hpo[r.pin_base];
-      if (acc > 0 && acc + ne > target) {
-        k.g1 = g;
-        ch.push_back(k);
-        k.g0 = g;
-        acc = 0;
-      }
-      acc += ne;
-    }
-    k.g1 = G;
-    ch.push_back(k);
-  }
   uint64_t max_ev = 0, max_pins = 0;
   uint32_t max_g = 0;
-  for (StreamChunk& k : ch) {
-    k.pin0 = k.g0 < G ? c->h_gates[k.g0].pin_base : P;
-    k.pin1 = k.g1 < G ? c->h_gates[k.g1].pin_base : P;
+  for (uint32_t g0 = 0; g0 < G || ch.empty();) {
+    StreamChunk k{g0, 0, 0, 0, 0, 0};
+    k.pin0 = gate_pin(g0);
     k.e0 = hpo[k.pin0];
+    const uint64_t lim = k.e0 + target;
+    uint32_t lo = g0 + 1, hi = G;  // the last g in [g0 + 1, G] whose first event offset is <= lim
+    if (g0 < G && hpo[gate_pin(lo)] <= lim) {
+      while (lo < hi) {
+        const uint32_t mid = lo + (hi - lo + 1) / 2;
+        if (hpo[gate_pin(mid)] <= lim) lo = mid;
+        else hi = mid - 1;
+      }
+    }
+    k.g1 = g0 < G ? lo : G;
+    k.pin1 = gate_pin(k.g1);
     k.e1 = hpo[k.pin1];
+    if (k.e1 < k.e0 || k.e1 > E)
+      return fail(c, PA_ERR_ARG, "%s: pin_off not monotone (at pin %llu)", who, (unsigned long long)k.pin1);
     max_ev = std::max(max_ev, k.e1 - k.e0);
     max_pins = std::max(max_pins, k.pin1 - k.pin0);
     max_g = std::max(max_g, k.g1 - k.g0);
+    ch.push_back(k);
+    if (k.g1 == g0) break;  // no gates
+    g0 = k.g1;
   }
   // staging slots and run scratch
   if (!c->copy_stream) {
@@ -584,6 +586,7 @@ int run_stream(pa_ctx* c, const RunPlan& plan, const pa_events* ev, uint64_t tar
   PA_TRY(dreserve(c, c->cnt_tmp, (size_t)N * 2 * sizeof(uint32_t)));
   PA_TRY(dreserve(c, c->err_word, sizeof(unsigned long long)));
   PA_TRY(dreserve(c, c->tmax_bits, sizeof(unsigned int)));
+  PA_TRY(dreserve(c, c->val_starts, ((max_ev + 31) / 32 + 1) * sizeof(uint32_t)));
   B.bins = (float4*)c->bins.p;
   B.part_blk = (uint32_t*)c->part_blk.p;
   B.part_counts = (uint32_t*)c->part_counts.p;
@@ -637,8 +640,9 @@ int run_stream(pa_ctx* c, const RunPlan& plan, const pa_events* ev, uint64_t tar
       va.gate_off = (uint64_t*)c->st_goff[slot].p;
       va.err = (unsigned long long*)c->err_word.p;
       va.t_max_bits = (unsigned int*)c->tmax_bits.p;
+      va.starts = (uint32_t*)c->val_starts.p;
       CUDA_TRY(c, launch_validate_events(va, st));
-      launches += 4;
+      launches += 1 + (gk ? 1 : 0) + 1 + 1 + (ek ? 1 : 0);  // rebase (pins, gates), check, validate (gates, events)
       // the chunk must be valid, and its events inside the window, before it touches the bins
       unsigned int tbits = 0;
       CUDA_TRY(c, cudaMemcpyAsync(&key, c->err_word.p, sizeof(key), cudaMemcpyDeviceToHost, st));
@@ -777,7 +781,7 @@ void pa_destroy(pa_ctx* c) {
   cudaSetDevice(c->device);
   if (c->stream) cudaStreamSynchronize(c->stream);
   DevBuf* all[] = {&c->cells, &c->lut, &c->leak, &c->patch, &c->dleak, &c->gates, &c->pin_off, &c->gate_off, &c->t, &c->s,
-                   &c->value_tmp, &c->err_word, &c->tmax_bits, &c->bins, &c->part_blk,
+                   &c->value_tmp, &c->err_word, &c->tmax_bits, &c->val_starts, &c->bins, &c->part_blk,
                    &c->part_counts, &c->tiles, &c->heavy, &c->p0_tot, &c->p_out, &c->dbg[0],
                    &c->dbg[1], &c->dbg[2], &c->wave_tmp, &c->cnt_tmp, &c->gate_tmp, &c->cell_tmp, &c->scratch_small,
                    &c->chunk_sums, &c->b_bt, &c->b_bs, &c->b_btag, &c->b_urec, &c->b_ugate, &c->b_items,
@@ -978,6 +982,8 @@ int pa_load_events(pa_ctx* c, const pa_events* ev) {
   va.gate_off = (uint64_t*)c->gate_off.p;
   va.err = (unsigned long long*)c->err_word.p;
   va.t_max_bits = (unsigned int*)c->tmax_bits.p;
+  PA_TRY(dreserve(c, c->val_starts, ((E + 31) / 32 + 1) * sizeof(uint32_t)));
+  va.starts = (uint32_t*)c->val_starts.p;
   CUDA_TRY(c, launch_validate_events(va, c->stream));
   unsigned int tbits = 0;
   CUDA_TRY(c, cudaMemcpyAsync(&key, c->err_word.p, sizeof(key), cudaMemcpyDeviceToHost, c->stream));

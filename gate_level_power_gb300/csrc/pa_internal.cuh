@@ -75,6 +75,7 @@ struct ValidateArgs {
   uint64_t* gate_off;     // out [G + 1]
   unsigned long long* err;
   unsigned int* t_max_bits;  // out: max event time as ordered bits
+  uint32_t* starts;       // scratch [(n_events + 31) / 32 + 1]: bit e set if event e starts a pin
 };
 
 struct RunArgs {

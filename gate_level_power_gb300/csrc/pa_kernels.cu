@@ -114,47 +114,75 @@ cudaError_t launch_check_pin_off(const uint64_t* pin_off, uint64_t n_pins, uint6
   return cudaGetLastError();
 }
 
-// One warp per gate: per-pin time order, ranges, toggles; writes gate_off.
-__global__ void k_validate_events(const ValidateArgs a) {
-  const int lane = threadIdx.x & 31;
-  const uint64_t warp = (blockIdx.x * (uint64_t)blockDim.x + threadIdx.x) >> 5;
-  const uint64_t n_warps = ((uint64_t)gridDim.x * blockDim.x) >> 5;
-  unsigned tmax = 0;
-  for (uint64_t g = warp; g < a.n_gates; g += n_warps) {
+// Event checks in two flat passes, so that no gate's length sets the time:
+// one thread per gate marks the first event of each of its non-empty pins in
+// a bitmap, checks that event's value against the pin's initial value and
+// writes gate_off; then one thread per event checks its time and slew ranges
+// and, unless it starts a pin, its order and toggle against the event before
+// it (the pin's previous event). Pin offsets are clamped to [0, n_events], so
+// offsets that k_check_pin_off rejects cannot take a read out of bounds.
+__global__ void __launch_bounds__(256) k_validate_gates(const ValidateArgs a) {
+  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+  const uint64_t E = a.n_events;
+  for (uint64_t g = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; g < a.n_gates; g += stride) {
     const GateRec r = a.gates[g];
     const int k = (int)((r.init >> 16) & 0xff);
     const uint64_t pb = r.pin_base;
-    if (lane == 0) a.gate_off[g] = a.pin_off[pb];
+    a.gate_off[g] = a.pin_off[pb];
     for (int p = 0; p <= k; ++p) {
-      const uint64_t lo = a.pin_off[pb + p], hi = a.pin_off[pb + p + 1];
-      const uint32_t init = p < k ? (r.init >> p) & 1u : (r.init >> 8) & 1u;
-      for (uint64_t e = lo + lane; e < hi; e += 32) {
-        const float t = a.t[e], s = a.s[e];
-        if (!(t >= 0.f) || !(t <= FLT_MAX)) {
-          dev_err(a.err, e, kErrRangeT);
-        } else {
-          tmax = max(tmax, t == 0.f ? 0u : __float_as_uint(t));
-        }
-        if (!(s > 0.f) || !(s <= FLT_MAX)) dev_err(a.err, e, kErrRangeSlew);
-        if (e > lo && !(t > a.t[e - 1])) dev_err(a.err, e, kErrUnsorted);
-        if (a.value) {
-          const uint32_t v = a.value[e];
-          const uint32_t pv = e > lo ? (uint32_t)a.value[e - 1] : init;
-          if (v > 1u) dev_err(a.err, e, kErrValue);
-          else if (v == pv) dev_err(a.err, e, kErrToggle);
-        }
+      const uint64_t lo = min(a.pin_off[pb + p], E), hi = min(a.pin_off[pb + p + 1], E);
+      if (lo >= hi) continue;
+      atomicOr(a.starts + (lo >> 5), 1u << (lo & 31u));
+      if (a.value) {
+        const uint32_t init = p < k ? (r.init >> p) & 1u : (r.init >> 8) & 1u;
+        const uint32_t v = a.value[lo];
+        if (v > 1u) dev_err(a.err, lo, kErrValue);
+        else if (v == init) dev_err(a.err, lo, kErrToggle);
       }
     }
   }
-  if (warp == 0 && lane == 0) a.gate_off[a.n_gates] = a.n_events;
+  if (blockIdx.x == 0 && threadIdx.x == 0) a.gate_off[a.n_gates] = E;
+}
+
+__global__ void __launch_bounds__(256) k_validate_events(const ValidateArgs a) {
+  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+  unsigned tmax = 0;
+  for (uint64_t e = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; e < a.n_events; e += stride) {
+    const float t = a.t[e], s = a.s[e];
+    if (!(t >= 0.f) || !(t <= FLT_MAX)) {
+      dev_err(a.err, e, kErrRangeT);
+    } else {
+      tmax = max(tmax, t == 0.f ? 0u : __float_as_uint(t));
+    }
+    if (!(s > 0.f) || !(s <= FLT_MAX)) dev_err(a.err, e, kErrRangeSlew);
+    const bool first = ((a.starts[e >> 5] >> (e & 31u)) & 1u) != 0u;
+    if (!first && e > 0 && !(t > a.t[e - 1])) dev_err(a.err, e, kErrUnsorted);
+    if (a.value) {
+      const uint32_t v = a.value[e];
+      if (v > 1u) dev_err(a.err, e, kErrValue);
+      else if (!first && e > 0 && v == (uint32_t)a.value[e - 1]) dev_err(a.err, e, kErrToggle);
+    }
+  }
   tmax = warp_max_u32(tmax);
-  if (lane == 0) atomicMax(a.t_max_bits, tmax);
+  __shared__ unsigned s_max[8];
+  if ((threadIdx.x & 31) == 0) s_max[threadIdx.x >> 5] = tmax;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned m = 0;
+    for (int i = 0; i < 8; ++i) m = max(m, s_max[i]);
+    if (m) atomicMax(a.t_max_bits, m);
+  }
 }
 
 cudaError_t launch_validate_events(const ValidateArgs& a, cudaStream_t st) {
-  const uint64_t warps = a.n_gates ? a.n_gates : 1;
-  const int grid = (int)std::min<uint64_t>((warps * 32 + 255) / 256, 152ull * 64);
-  k_validate_events<<<grid, 256, 0, st>>>(a);
+  cudaError_t e = cudaMemsetAsync(a.starts, 0, ((a.n_events + 31) / 32 + 1) * sizeof(uint32_t), st);
+  if (e != cudaSuccess) return e;
+  const int gg = (int)std::min<uint64_t>(((uint64_t)a.n_gates + 255) / 256, 152ull * 16);
+  k_validate_gates<<<gg > 0 ? gg : 1, 256, 0, st>>>(a);
+  if (a.n_events) {
+    const int ge = (int)std::min<uint64_t>((a.n_events + 255) / 256, 152ull * 32);
+    k_validate_events<<<ge, 256, 0, st>>>(a);
+  }
   return cudaGetLastError();
 }
 

@@ -380,11 +380,13 @@ int pa_run_noalloc(pa_ctx *ctx, const pa_run_params *params, pa_result *out);
  *   ev   host arrays (mem = PA_MEM_HOST) in pa_load_events' form; not retained
  * Requires a netlist; does not use or change the loaded events or bands. Device
  * memory: two staging slots of about 9 bytes per event of the largest chunk,
- * plus pa_run's scratch. Outputs as pa_run, without the per-event debug arrays
+ * plus pa_run's scratch. The host reads pin_off only where chunks are cut
+ * (a binary search per chunk); the offsets inside a chunk are checked on the
+ * device before the chunk is computed. Outputs as pa_run, without the per-event debug arrays
  * (PA_ERR_ARG); n_tiles returns the number of chunks. Errors as pa_load_events
  * and pa_run (indices of the offending pin / event / gate in the whole trace).
  */
-#define PA_STREAM_DEFAULT_CHUNK (1ull << 27)
+#define PA_STREAM_DEFAULT_CHUNK (1ull << 26)
 int pa_run_stream(pa_ctx *ctx, const pa_run_params *params, const pa_events *ev, uint64_t chunk_events,
                   pa_result *out);
 

@@ -96,6 +96,22 @@ def test_stream_errors_are_located_in_the_whole_trace(glp):
             pa.run(w.vdd, w.t_clk_ns, w.n_cycles // 2, stream=(w.pin_off, w.t_ns, w.slew_ps, w.value),
                    chunk_events=1000)
         assert ei.value.code == glp.PA_ERR_RANGE
+        # pin offsets out of order inside a chunk (checked on the device before
+        # the chunk is used) and at a chunk boundary (checked on the host)
+        po = w.pin_off.copy()
+        q = int(np.searchsorted(po, w.n_events // 2))
+        while not (po[q - 1] < po[q] < po[q + 1]):
+            q += 1
+        po[q] = po[q + 1] + 5
+        with pytest.raises(glp.PaError) as ei:
+            pa.run(w.vdd, w.t_clk_ns, w.n_cycles, stream=(po, w.t_ns, w.slew_ps, w.value), chunk_events=1000)
+        assert ei.value.code == glp.PA_ERR_ARG
+        po = w.pin_off.copy()
+        po[len(po) // 2:] = po[len(po) // 2:] // 3
+        po[-1] = w.n_events
+        with pytest.raises(glp.PaError) as ei:
+            pa.run(w.vdd, w.t_clk_ns, w.n_cycles, stream=(po, w.t_ns, w.slew_ps, w.value), chunk_events=1000)
+        assert ei.value.code == glp.PA_ERR_ARG
         # per-event debug arrays are not on this path
         with pytest.raises(glp.PaError) as ei:
             pa.run(w.vdd, w.t_clk_ns, w.n_cycles, debug=True, stream=(w.pin_off, w.t_ns, w.slew_ps, w.value))
