@@ -1277,7 +1277,7 @@ int build_bands(pa_ctx* c, float t_clk, uint32_t cb) {
   const size_t ev_bytes = ((n_ev + 64) & ~(size_t)15) * sizeof(float);
   PA_TRY(dreserve(c, c->b_urec2, (nu + 1) * sizeof(uint2)));
   PA_TRY(dreserve(c, c->b_urec, (nu + 1) * sizeof(uint4)));
-  PA_TRY(dreserve(c, c->b_btag, (size_t)n_ev + 64));
+  PA_TRY(dreserve(c, c->b_btag, ((size_t)n_ev + 64) * sizeof(uint16_t)));
   PA_TRY(dreserve(c, c->b_ugate, (nu + 1) * sizeof(uint32_t)));
   PA_TRY(dreserve(c, c->b_uband, (nu + 1) * sizeof(uint32_t)));
   PA_TRY(dreserve(c, c->b_uoff, (nu + 1) * sizeof(uint64_t)));
@@ -1287,7 +1287,7 @@ int build_bands(pa_ctx* c, float t_clk, uint32_t cb) {
   PA_TRY(dreserve(c, c->b_bs, ev_bytes));
   PA_TRY(dreserve(c, c->b_scan, ((size_t)band_scan_blocks(std::max<uint64_t>(nbg, nu)) + 1) * sizeof(uint64_t)));
   L.urec = (uint4*)c->b_urec.p;
-  L.btag = (uint8_t*)c->b_btag.p;
+  L.btag = (uint16_t*)c->b_btag.p;
   a.urec2 = (uint2*)c->b_urec2.p;
   L.ugate = (uint32_t*)c->b_ugate.p;
   L.bt = (float*)c->b_bt.p;

@@ -591,20 +591,25 @@ __global__ void __launch_bounds__(256) k_bw_item_emit(const BandBuildArgs a, uin
 }
 
 // Finalize pass, one warp per item: the item's events are moved into an
-// input region (every unit's input-pin events, unit by unit) followed by an
-// output region (every unit's output-pin events, unit by unit), each event
-// gets its tag, and each unit its 16-byte record. The load-axis interval and
-// fraction of the unit's gate are fixed here (the library and the netlist do
-// not change while the layout lives); everything that depends on the events'
-// arithmetic is left to the run.
-constexpr int kFinWarps = 8;
+// input region (every unit's input-pin events, unit by unit, each unit's in
+// (time, pin) order: the merge of its pins' time-ordered runs) followed by an
+// output region (every unit's output-pin events, unit by unit, in time
+// order), each event gets its tag word, and each unit its 16-byte record. The
+// merge is the order of the layout, fixed once like the regions; the gate
+// states along it are left to the run, as is everything that depends on the
+// events' arithmetic. The load-axis interval and fraction of the unit's gate
+// are fixed here (the library and the netlist do not change while the layout
+// lives).
+constexpr int kFinWarps = 6;
 
 __global__ void __launch_bounds__(kFinWarps * 32) k_bw_finalize(const BandBuildArgs a) {
   __shared__ float tb[kFinWarps][kItemEvents];
   __shared__ float sb[kFinWarps][kItemEvents];
-  __shared__ uint8_t gb[kFinWarps][kItemEvents];
+  __shared__ uint16_t gb[kFinWarps][kItemEvents];  // tag words, in region order
+  __shared__ uint16_t dd[kFinWarps][kItemEvents];  // region index of each event, in the walk's order
   __shared__ uint32_t ust[kFinWarps][kItemUnits];  // unit starts in the walk's order, item-relative
   __shared__ uint32_t udst[kFinWarps][kItemUnits]; // input offset | output offset (in the region) << 9 | inputs << 18
+  __shared__ uint32_t ups[kFinWarps][kItemUnits];  // ends of input pins 0..3 in the walk's order, one byte each
   __shared__ uint32_t upin[kFinWarps][kItemUnits]; // record word y
   __shared__ uint32_t utie[kFinWarps][kItemUnits / 32];  // units with events at one time on two input pins
   const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
@@ -619,11 +624,11 @@ __global__ void __launch_bounds__(kFinWarps * 32) k_bw_finalize(const BandBuildA
       continue;
     }
     const int n = (int)(e1 - e0), nu = (int)(u1 - u0);
-    // units: sizes, the two regions' offsets, pin starts
+    // units: sizes, the two regions' offsets, pin runs
     uint32_t carry = 0, seg_max = 0;
     for (int r = 0; r < 2; ++r) {
       const int uu = lane + 32 * r;
-      uint32_t pk = 0, n_in = 0, x = 0, y = 0;
+      uint32_t pk = 0, n_in = 0, x = 0, ends = 0;
       if (uu < nu) {
         x = a.urec2[u0 + uu].x;
         const uint32_t k = a.cells[(x >> 24) & 63u].k;
@@ -634,13 +639,14 @@ __global__ void __launch_bounds__(kFinWarps * 32) k_bw_finalize(const BandBuildA
             s += (x >> (4 * p)) & 15u;
             seg_max = max(seg_max, (x >> (4 * p)) & 15u);
           }
-          y |= s << (8 * p);
+          ends |= s << (8 * p);
         }
-        y |= (k - 1u) << 30;
-        y |= ((x >> 30) & 1u) << 6;  // output value at the window start
         n_in = s;
         const uint32_t n_out = (x >> (4 * k)) & 15u;
         pk = (n_in + n_out) | (n_in << 10) | (n_out << 20);
+        // record word y: the unit's input events | output value at the window start << 6 | (k - 1) << 30
+        upin[wl][uu] = n_in | (((x >> 30) & 1u) << 6) | ((k - 1u) << 30);
+        ups[wl][uu] = ends;
       }
       uint32_t inc = pk;
 #pragma unroll
@@ -653,7 +659,6 @@ __global__ void __launch_bounds__(kFinWarps * 32) k_bw_finalize(const BandBuildA
       if (uu < nu) {
         ust[wl][uu] = ex & 1023u;
         udst[wl][uu] = ((ex >> 10) & 1023u) | (((ex >> 20) & 1023u) << 9) | (n_in << 18);
-        upin[wl][uu] = y;
       }
     }
     __syncwarp();
@@ -662,42 +667,73 @@ __global__ void __launch_bounds__(kFinWarps * 32) k_bw_finalize(const BandBuildA
       if (lane == 0) atomicMin(a.err, (unsigned long long)((it << 8) | kErrTileOverflow));
       continue;
     }
-    // events: each to its place in the two regions
+    for (int i = lane; i < n; i += 32) sb[wl][i] = L.bt[e0 + i];  // times in the walk's order
+    __syncwarp();
+    // each event's place: an input event at its rank in its unit's (time,
+    // pin) order -- its index in its pin's run plus, for every other input
+    // pin, the events earlier than it (at an equal time: on a lower pin)
     for (int i = lane; i < n; i += 32) {
       int u = 0;
 #pragma unroll
       for (int h = kItemUnits / 2; h > 0; h >>= 1)
         if (u + h < nu && ust[wl][u + h] <= (uint32_t)i) u += h;
-      const int li = i - (int)ust[wl][u];
-      const uint32_t d = udst[wl][u], y = upin[wl][u];
+      const int ub = (int)ust[wl][u], li = i - ub;
+      const uint32_t d = udst[wl][u], ends = ups[wl][u];
       const int n_in = (int)(d >> 18);
+      const int k = (int)(upin[wl][u] >> 30) + 1;
       int dst;
       uint32_t tag = (uint32_t)u;
       if (li < n_in) {
-        dst = (int)(d & 511u) + li;
-        const uint32_t p = (uint32_t)(li >= (int)(y & 63u)) + (uint32_t)(li >= (int)((y >> 8) & 63u)) +
-                           (uint32_t)(li >= (int)((y >> 16) & 63u));
-        tag |= p << 6;
+        int p = 0;
+        while (p < k - 1 && li >= (int)((ends >> (8 * p)) & 255u)) ++p;
+        const int ps = p == 0 ? 0 : (int)((ends >> (8 * (p - 1))) & 255u);
+        const float t = sb[wl][i];
+        int rank = li - ps;
+        for (int q = 0; q < k; ++q) {
+          if (q == p) continue;
+          const int qa = q == 0 ? 0 : (int)((ends >> (8 * (q - 1))) & 255u);
+          const int qb = (int)((ends >> (8 * q)) & 255u);
+          for (int m = ub + qa; m < ub + qb; ++m) {
+            const float tq = sb[wl][m];
+            rank += (tq < t || (tq == t && q < p)) ? 1 : 0;
+          }
+        }
+        dst = (int)(d & 511u) + rank;
+        tag |= (uint32_t)p << 6;
       } else {
         dst = (int)n_in_all + (int)((d >> 9) & 511u) + (li - n_in);
       }
-      tb[wl][dst] = L.bt[e0 + i];
-      sb[wl][dst] = L.bs[e0 + i];
-      gb[wl][dst] = (uint8_t)tag;
+      dd[wl][i] = (uint16_t)dst;
+      gb[wl][dst] = (uint16_t)tag;
+      tb[wl][dst] = sb[wl][i];
+    }
+    __syncwarp();
+    // distance back to the pin's previous event in the unit (input events; 0
+    // for a unit's first event of a pin): in the walk's order that event is
+    // the one just before, when it lies in the same pin run
+    for (int i = lane; i < n; i += 32) {
+      const int dst = dd[wl][i];
+      if (dst < (int)n_in_all) {
+        int u = 0;
+#pragma unroll
+        for (int h = kItemUnits / 2; h > 0; h >>= 1)
+          if (u + h < nu && ust[wl][u + h] <= (uint32_t)i) u += h;
+        const int li = i - (int)ust[wl][u];
+        const uint32_t ends = ups[wl][u];
+        const int p = (int)((gb[wl][dst] >> 6) & 3u);
+        const int ps = p == 0 ? 0 : (int)((ends >> (8 * (p - 1))) & 255u);
+        if (li > ps) gb[wl][dst] |= (uint16_t)((dst - (int)dd[wl][i - 1]) << 8);
+      }
     }
     if (lane < kItemUnits / 32) utie[wl][lane] = 0u;
     __syncwarp();
-    // ties: an input event whose time another input pin of its unit also has
-    for (int i = lane; i < (int)n_in_all; i += 32) {
-      const uint32_t tag = gb[wl][i], u = tag & 63u;
-      const uint32_t d = udst[wl][u];
-      const int lo = (int)(d & 511u), hi = lo + (int)(d >> 18);
-      const float t = tb[wl][i];
-      bool tie = false;
-      for (int m = lo; m < hi; ++m) tie |= (gb[wl][m] >> 6) != (tag >> 6) && tb[wl][m] == t;
-      if (tie) atomicOr(&utie[wl][u >> 5], 1u << (u & 31u));
+    // ties: in (time, pin) order two input events of a unit at one time are neighbours
+    for (int i = lane + 1; i < (int)n_in_all; i += 32) {
+      const uint32_t u = gb[wl][i] & 63u;
+      if ((gb[wl][i - 1] & 63u) == u && tb[wl][i - 1] == tb[wl][i]) atomicOr(&utie[wl][u >> 5], 1u << (u & 31u));
     }
     __syncwarp();
+    for (int i = lane; i < n; i += 32) sb[wl][dd[wl][i]] = L.bs[e0 + i];  // the walk-order times are no longer read
     for (int r = 0; r < 2; ++r) {
       const int uu = lane + 32 * r;
       if (uu < nu) {
@@ -715,6 +751,7 @@ __global__ void __launch_bounds__(kFinWarps * 32) k_bw_finalize(const BandBuildA
         L.urec[u0 + uu] = make_uint4(x, upin[wl][uu], __float_as_uint(v), w.y);
       }
     }
+    __syncwarp();
     for (int i = lane; i < n; i += 32) {
       L.bt[e0 + i] = tb[wl][i];
       L.bs[e0 + i] = sb[wl][i];
@@ -834,8 +871,8 @@ namespace {
 constexpr int kBW = 32;
 constexpr int kBT = kBW * 32;
 constexpr int kStEv = kItemEvents + 8;                     // staged times (16-byte rounding)
-constexpr size_t kStTagOff = (size_t)kStEv * 4;            // staged event tags
-constexpr size_t kStRecOff = kStTagOff + kItemEvents + 32; // staged unit records
+constexpr size_t kStTagOff = (size_t)kStEv * 4;            // staged event tag words
+constexpr size_t kStRecOff = kStTagOff + (size_t)kStEv * 2; // staged unit records
 constexpr size_t kWarpB = kStRecOff + (size_t)kItemUnits * 16;
 constexpr size_t kHist = (size_t)kBandMaxCycles * 16;
 // Cell table in shared memory: per cell the slew axis as two float4 (points
@@ -848,7 +885,7 @@ constexpr size_t kHist = (size_t)kBandMaxCycles * 16;
 constexpr size_t kCellsB = (size_t)kSmemCells * 32 + (size_t)kSmemCells * 4 + (size_t)kSmemCells * 8 * 8;
 // Item records of the CTA's current and next chunk (the next one's copy in
 // flight while the current one is worked on), one more for the end.
-constexpr uint32_t kChunkMaxItems = 1024;
+constexpr uint32_t kChunkMaxItems = 512;
 constexpr size_t kChunkRecB = (size_t)(kChunkMaxItems + 1) * sizeof(BandItem);
 constexpr size_t kSmemB = kHist + kCellsB + kBW * kWarpB + 2 * kChunkRecB;
 static_assert(kStTagOff % 16 == 0 && kStRecOff % 16 == 0 && kWarpB % 16 == 0 && kHist % 16 == 0 &&
@@ -1004,7 +1041,7 @@ __device__ __forceinline__ ItemGeo item_geo(const BandItem& a, const BandItem& b
   g.u0 = a.u0;
   g.ea = a.e0 & ~3ull;
   g.ev_off = (uint32_t)(a.e0 - g.ea);
-  g.tag_off = (uint32_t)(a.e0 & 15ull);
+  g.tag_off = (uint32_t)(a.e0 & 7ull);  // tag words: 16-byte copies of 8
   g.n_in = (a.bw >> kItemBandBits) & 511u;  // bits 20..28
   g.steps = a.bw >> kItemStepShift;
   g.ok = b.e0 > a.e0 && b.u0 > a.u0 && b.e0 - a.e0 < (uint64_t)kItemEvents && b.u0 - a.u0 <= (uint32_t)kItemUnits &&
@@ -1012,7 +1049,7 @@ __device__ __forceinline__ ItemGeo item_geo(const BandItem& a, const BandItem& b
   g.n = g.ok ? (uint32_t)(b.e0 - a.e0) : 0u;
   g.nu = g.ok ? b.u0 - a.u0 : 0u;
   g.ev_bytes = ((g.ev_off + g.n + 3u) & ~3u) * 4u;
-  g.tag_bytes = (g.tag_off + g.n + 15u) & ~15u;
+  g.tag_bytes = ((g.tag_off + g.n + 7u) & ~7u) * 2u;
   return g;
 }
 
@@ -1041,25 +1078,28 @@ __device__ __forceinline__ void prefetch_item(const BandLayout& L, const ItemGeo
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(L.urec + g.u0), "r"(g.nu * 16u) : "memory");
 }
 
-// Events of a sorted pin segment b[0, qn) earlier than t, by binary lifting
-// in `steps` steps (the same for the whole warp: enough for the item's
-// longest input-pin segment, qn < 2^steps).
-// kLong: the item may hold segments of 8 to 15 events (a fourth step).
-static_assert(kUnitPinMax <= 15, "four lifting steps cover a pin segment");
-template <bool kLong>
-__device__ __forceinline__ int seg_rank(const float* b, int qn, float t, uint32_t steps) {
-  int r = 0;
-  if (kLong && 8 <= qn && b[7] < t) r = 8;
-  if (steps >= 3 && r + 4 <= qn && b[r + 3] < t) r += 4;
-  if (steps >= 2 && r + 2 <= qn && b[r + 1] < t) r += 2;
-  if (steps >= 1 && r + 1 <= qn && b[r] < t) r += 1;
-  return r;
-}
-
-// Start of input pin q (0..4; 4 = end of the inputs) inside the unit's input
-// run, from record word y.
-__device__ __forceinline__ int pin_start(uint32_t y, int q) {
-  return (int)(__byte_perm(y << 8, y, q < 4 ? (uint32_t)q : 7u) & 63u);
+// Gate states of one round of 32 input events (lane l: staged index base +
+// l). A unit's input events are contiguous and in (time, pin) order, so the
+// input values just before an event in that order are the unit's start state
+// flipped by the pin bits x of the unit's earlier events: a prefix XOR over
+// the round, restarted at the unit's first event (lane in_off - base), plus
+// `carry`, the XOR of the round's first unit's bits in earlier rounds
+// (warp-uniform, advanced to the next round here). Lanes past the item's
+// input events pass x = 0 and come after every valid lane.
+__device__ __forceinline__ uint32_t round_state(uint32_t x, int in_off, int base, uint32_t start, uint32_t& carry,
+                                                int lane) {
+  uint32_t v = x;  // inclusive prefix XOR over the round
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, v, d);
+    if (lane >= d) v ^= y;
+  }
+  const uint32_t ex = v ^ x;
+  const int ss = in_off > base ? in_off - base : 0;  // the unit's first lane in this round
+  const uint32_t ex_ss = __shfl_sync(0xffffffffu, ex, ss);
+  const uint32_t before = ex_ss ^ (in_off < base ? carry : 0u);  // bits of the unit's events before lane ss
+  carry = __shfl_sync(0xffffffffu, v ^ before, 31);
+  return start ^ ex ^ before;
 }
 
 struct CellTab {
@@ -1088,72 +1128,52 @@ struct EvDbg {
   float g_int, g_sw, g_gl, g_lk;  // fJ
 };
 
-// Glitch test against the pin's previous event (staged index e - 1 if idx > 0;
-// for idx == 0 the event itself, unused) and scaling of the dynamic energy;
-// no branches, since on dense pins most warps hold a glitch somewhere.
-// has_next: the pin's next event is staged at e + 1 (only asked for in the
-// glitch-all reading, where the first event of a multi-event pin-cycle takes
-// the pulse to that next event).
+// Glitch test against the pin's previous event (staged index ep, if has_prev)
+// and scaling of the dynamic energy; no branches, since on dense pins most
+// warps hold a glitch somewhere. en: the pin's next event in the unit (staged
+// index, -1 if none; only asked for in the glitch-all reading, where the
+// first event of a multi-event pin-cycle takes the pulse to that next event).
 template <bool kPow2, bool kDebug>
-__device__ __forceinline__ float glitch_scale(const RunArgs& a, const float* ts, const float* gs, int e, int idx,
-                                              float t, float s, uint32_t c, float e_dyn, bool has_next,
+__device__ __forceinline__ float glitch_scale(const RunArgs& a, const float* ts, const float* gs, int ep,
+                                              bool has_prev, int en, float t, float s, uint32_t c, float e_dyn,
                                               bool& glitch) {
-  const int ep = e - (idx > 0 ? 1 : 0);
   float tp = ts[ep];
-  glitch = idx > 0 && cyc<kPow2>(tp, a.t_clk, a.inv_t_clk) == c;
+  glitch = has_prev && cyc<kPow2>(tp, a.t_clk, a.inv_t_clk) == c;
   // the previous edge's slew only for glitches (a predicated load: only those lanes touch L1)
   float sp = s;
   if (glitch) sp = __ldg(gs + ep);
   float pw = t - tp;
-  if (kDebug && a.glitch_all && !glitch && has_next) {  // the reading runs in the per-event path
-    const float tn = ts[e + 1];
+  if (kDebug && a.glitch_all && !glitch && en >= 0) {  // the reading runs in the per-event path
+    const float tn = ts[en];
     if (cyc<kPow2>(tn, a.t_clk, a.inv_t_clk) == c) {
       glitch = true;
       pw = tn - t;
-      sp = __ldg(gs + e + 1);
+      sp = __ldg(gs + en);
     }
   }
   const float r = fminf(1.f, __fdividef(2000.f * pw, s + sp));
   return glitch ? r * e_dyn : e_dyn;
 }
 
-// Input-pin event at staged index i: gate state, LUT energy, leakage step,
-// glitch, totals. `valid` false: computed for a padding lane, not counted.
-template <bool kPow2, bool kDebug, bool kLong>
-__device__ __forceinline__ EvOut ev_input(const RunArgs& a, const CellTab& CT, const float* ts, const uint8_t* tg,
-                                          const uint4* rec, const float* gs, int i, uint32_t steps, bool valid,
-                                          BAcc& acc, EvDbg& dbg) {
-  const uint32_t tag = tg[i];
-  const uint4 R = rec[tag & 63u];
+// Input-pin event at staged index i (tag word w, unit record R): its state
+// s_b (input values just before it in (time, pin) order, from round_state),
+// LUT energy, leakage step, glitch, totals. `valid` false: computed for a
+// padding lane, not counted.
+template <bool kPow2, bool kDebug>
+__device__ __forceinline__ EvOut ev_input(const RunArgs& a, const CellTab& CT, const float* ts, const uint16_t* tg,
+                                          const float* gs, int i, uint32_t w, const uint4& R, uint32_t s_b,
+                                          bool valid, BAcc& acc, EvDbg& dbg) {
   const float t = ts[i];
   const float s = __ldg(gs + i);
-  const uint32_t y = R.y;
-  const int k = (int)(y >> 30) + 1;
-  const int p = (int)(tag >> 6);
-  const int in_off = (int)(R.x & 511u);
-  const int idx = i - in_off - (int)(__byte_perm(y << 8, 0u, (uint32_t)p) & 63u);  // p < 4
-  const float* ub = ts + in_off;
-  uint32_t s_pre = ((R.x >> 24) & 15u) ^ (((uint32_t)idx & 1u) << p);
-  uint32_t s_b = s_pre;
-  const bool ties = (R.x >> 31) != 0u;  // the unit has events at one time on two input pins
-  // other input pins: parity of their events before t and, for lower pins, a
-  // tie at t (leakage steps are taken in pin order at a tie)
-  // (exactly k - 1 iterations per lane: with k the same across most of a
-  // warp's units, no lane idles)
-  for (int jj = 0; jj < k - 1; ++jj) {
-    const int q = jj + (jj >= p ? 1 : 0);
-    // byte 0: start of pin q (from y << 8, whose byte 0 is 0), byte 1: start
-    // of pin q + 1 (byte q of y)
-    const uint32_t se = __byte_perm(y << 8, y, (uint32_t)q | ((uint32_t)(q + 4) << 4));
-    const int qa = (int)(se & 63u);
-    const int qn = (int)((se >> 8) & 63u) - qa;
-    const float* b = ub + qa;
-    const int r = seg_rank<kLong>(b, qn, t, steps);
-    bool eq = false;
-    if (ties) eq = q < p && r < qn && b[r] == t;
-    const uint32_t par = (uint32_t)r & 1u;
-    s_pre ^= par << q;
-    s_b ^= (par ^ (uint32_t)eq) << q;
+  const int p = (int)((w >> 6) & 3u);
+  const int d = (int)(w >> 8);  // back to the pin's previous event in the unit (0: none)
+  // the LUT's state is the state before the whole timestamp: at a time two
+  // input pins share (flagged units only), the lower pins' events at t, just
+  // before this one in (time, pin) order, are taken back out
+  uint32_t s_pre = s_b;
+  if ((R.x >> 31) != 0u) {
+    const int in_off = (int)(R.x & 511u);
+    for (int j = i - 1; j >= in_off && ts[j] == t; --j) s_pre ^= 1u << ((tg[j] >> 6) & 3u);
   }
   const uint32_t cell = (R.x >> 18) & 63u;
   const uint32_t info = CT.info[cell];  // ns - 1 | (nl - 1) << 8 | patch offset << 16
@@ -1174,16 +1194,24 @@ __device__ __forceinline__ EvOut ev_input(const RunArgs& a, const CellTab& CT, c
   const float dp = __ldg(a.dleak + cell * kDleakStride + s_b * 4 + p);
   const float T = a.t_clk;
   const uint32_t c = cyc<kPow2>(t, T, a.inv_t_clk);
+  int en = -1;
+  if (kDebug && a.glitch_all) {  // the pin's next event in the unit
+    const int end = (int)(R.x & 511u) + (int)(R.y & 63u);
+    for (int m = i + 1; m < end; ++m)
+      if ((int)((tg[m] >> 6) & 3u) == p) {
+        en = m;
+        break;
+      }
+  }
   bool glitch;
-  const bool has_next = kDebug && a.glitch_all && idx + 1 < pin_start(y, p + 1) - pin_start(y, p);
-  float e_w = glitch_scale<kPow2, kDebug>(a, ts, gs, i, idx, t, s, c, e_int, has_next, glitch);
+  float e_w = glitch_scale<kPow2, kDebug>(a, ts, gs, i - d, d > 0, en, t, s, c, e_int, glitch);
   if (valid) {
     acc.e_gl += glitch ? e_w : 0.f;
     acc.e_int += glitch ? 0.f : e_int;
     acc.e_lk = fmaf(dp, a.t_max_f - t, acc.e_lk);
   }
   if (kDebug)
-    dbg = EvDbg{s_pre, (uint32_t)((lis << 4) | j), tag & 63u, p, t, glitch, glitch ? 0.f : e_int, 0.f,
+    dbg = EvDbg{s_pre, (uint32_t)((lis << 4) | j), w & 63u, p, t, glitch, glitch ? 0.f : e_int, 0.f,
                 glitch ? e_w : 0.f, dp * (a.t_max_f - t)};
   const float rem = fmaf(-(float)c, T, t);  // t - c T: the step's part inside its own cycle
   e_w = fmaf(dp, T - rem, e_w);
@@ -1192,11 +1220,10 @@ __device__ __forceinline__ EvOut ev_input(const RunArgs& a, const CellTab& CT, c
 
 // Output-pin event at staged index i: switching energy, glitch, totals.
 template <bool kPow2, bool kDebug>
-__device__ __forceinline__ EvOut ev_output(const RunArgs& a, const float* ts, const uint8_t* tg, const uint4* rec,
-                                           const float* gs, int i, int n, uint32_t steps, bool valid, BAcc& acc,
-                                           EvDbg& dbg) {
-  const uint32_t tag = tg[i];
-  const uint4 R = rec[tag & 63u];
+__device__ __forceinline__ EvOut ev_output(const RunArgs& a, const float* ts, const uint16_t* tg, const uint4* rec,
+                                           const float* gs, int i, int n, bool valid, BAcc& acc, EvDbg& dbg) {
+  const uint32_t w = tg[i];
+  const uint4 R = rec[w & 63u];
   const float t = ts[i];
   const int idx = i - (int)((R.x >> 9) & 511u);
   // the slew only enters a glitch ratio: loaded for lanes whose previous event
@@ -1207,23 +1234,21 @@ __device__ __forceinline__ EvOut ev_output(const RunArgs& a, const float* ts, co
   if (kDebug && a.esw_rise)  // C V^2 on a rise: the output's value at the window start, flipped per earlier event
     e_sw = ((((R.y >> 6) & 1u) ^ ((uint32_t)(idx + 1) & 1u)) != 0u) ? 2.f * e_sw : 0.f;
   const uint32_t c = cyc<kPow2>(t, a.t_clk, a.inv_t_clk);
+  const int en = (kDebug && a.glitch_all && i + 1 < n && (tg[i + 1] & 63u) == (w & 63u)) ? i + 1 : -1;
   bool glitch;
-  const bool has_next = kDebug && a.glitch_all && i + 1 < n && (tg[i + 1] & 63u) == (tag & 63u);
-  const float e_w = glitch_scale<kPow2, kDebug>(a, ts, gs, i, idx, t, s, c, e_sw, has_next, glitch);
+  const float e_w = glitch_scale<kPow2, kDebug>(a, ts, gs, idx > 0 ? i - 1 : i, idx > 0, en, t, s, c, e_sw, glitch);
   if (valid) {
     acc.e_gl += glitch ? e_w : 0.f;
     acc.e_sw += glitch ? 0.f : e_sw;
   }
   if (kDebug) {
-    const uint32_t y = R.y;
-    const int k = (int)(y >> 30) + 1;
+    // input values before t: the unit's start state flipped by its input
+    // events earlier than t (in time order)
     uint32_t s_pre = (R.x >> 24) & 15u;
-    const float* ub = ts + (int)(R.x & 511u);
-    for (int q = 0; q < k; ++q) {
-      const int qa = pin_start(y, q);
-      s_pre ^= ((uint32_t)seg_rank<true>(ub + qa, pin_start(y, q + 1) - qa, t, steps) & 1u) << q;
-    }
-    dbg = EvDbg{s_pre, 0xFFu, tag & 63u, k, t, glitch, 0.f, glitch ? 0.f : e_sw, glitch ? e_w : 0.f, 0.f};
+    const int in_off = (int)(R.x & 511u), in_end = in_off + (int)(R.y & 63u);
+    for (int m = in_off; m < in_end && ts[m] < t; ++m) s_pre ^= 1u << ((tg[m] >> 6) & 3u);
+    dbg = EvDbg{s_pre, 0xFFu, w & 63u, (int)(R.y >> 30) + 1, t, glitch, 0.f, glitch ? 0.f : e_sw,
+                glitch ? e_w : 0.f, 0.f};
   }
   return EvOut{c, e_w, 0.f, glitch ? 2u : 0u};
 }
@@ -1282,9 +1307,10 @@ __device__ void event_debug(const RunArgs& a, uint32_t gate, int p, float t, uin
 }
 
 // One staged item on one warp: one lane per event, the input region first,
-// then the output region. Where a region has events left for a second round,
-// each lane computes two events before committing either.
-template <bool kPow2, bool kDebug, bool kExact, bool kLong>
+// then the output region. Input events take their states from a scan over
+// each round of 32; where a region has events left for a second round, each
+// lane computes two events before committing either.
+template <bool kPow2, bool kDebug, bool kExact>
 __device__ __forceinline__ void band_item(const BandRunArgs& A, const CellTab& CT, float* hist,
                                           const uint8_t* stage, uint32_t item, const ItemGeo& g, uint32_t c0,
                                           BAcc& acc) {
@@ -1295,19 +1321,33 @@ __device__ __forceinline__ void band_item(const BandRunArgs& A, const CellTab& C
     return;
   }
   const float* ts = reinterpret_cast<const float*>(stage) + g.ev_off;
-  const uint8_t* tg = stage + kStTagOff + g.tag_off;
+  const uint16_t* tg = reinterpret_cast<const uint16_t*>(stage + kStTagOff) + g.tag_off;
   const uint4* rec = reinterpret_cast<const uint4*>(stage + kStRecOff);
   const float* gs = A.L.bs + g.e0;  // slews: read once, from HBM (prefetched into L2 ahead of the item)
   // and into L1: one 128-byte line per lane
   if ((uint32_t)lane * 32u < g.ev_off + g.n)
     asm volatile("prefetch.global.L1 [%0];" ::"l"(A.L.bs + g.ea + 32u * (uint32_t)lane) : "memory");
   const int n = (int)g.n, n_in = (int)g.n_in;
-  const uint32_t steps = g.steps;
   EvDbg d0{}, d1{};
+  uint32_t carry = 0;  // state scan across rounds
   if (kDebug) {
-    for (int i = lane; i < n; i += 32) {
-      const EvOut o = i < n_in ? ev_input<kPow2, true, true>(a, CT, ts, tg, rec, gs, i, steps, true, acc, d0)
-                               : ev_output<kPow2, true>(a, ts, tg, rec, gs, i, n, steps, true, acc, d0);
+    for (int base = 0; base < n; base += 32) {
+      const int i = base + lane;
+      EvOut o;
+      bool valid = i < n;
+      if (base < n_in) {  // an input round (warp-uniform)
+        const bool v = i < n_in;
+        const int jj = v ? i : n_in - 1;
+        const uint32_t w = tg[jj];
+        const uint4 R = rec[w & 63u];
+        const uint32_t sb = round_state(v ? 1u << ((w >> 6) & 3u) : 0u, (int)(R.x & 511u), base,
+                                        (R.x >> 24) & 15u, carry, lane);
+        if (v) o = ev_input<kPow2, true>(a, CT, ts, tg, gs, i, w, R, sb, true, acc, d0);
+        else if (valid) o = ev_output<kPow2, true>(a, ts, tg, rec, gs, i, n, true, acc, d0);
+      } else if (valid) {
+        o = ev_output<kPow2, true>(a, ts, tg, rec, gs, i, n, true, acc, d0);
+      }
+      if (!valid) continue;
       ev_commit<kExact>(A, hist, o, item, c0);
       const uint32_t gate = A.L.ugate[g.u0 + d0.unit];
       if (a.gate_e) {  // this event's share of its gate's energies
@@ -1322,16 +1362,21 @@ __device__ __forceinline__ void band_item(const BandRunArgs& A, const CellTab& C
     }
   } else {
     for (int base = 0; base < n_in; base += 64) {
-      const int i0 = base + lane;
+      const int i0 = base + lane, i1 = i0 + 32;
+      const bool v1 = i1 < n_in;
+      const uint32_t w0 = tg[min(i0, n_in - 1)], w1 = tg[min(i1, n_in - 1)];
+      const uint4 R0 = rec[w0 & 63u], R1 = rec[w1 & 63u];
+      const uint32_t s0 = round_state(i0 < n_in ? 1u << ((w0 >> 6) & 3u) : 0u, (int)(R0.x & 511u), base,
+                                      (R0.x >> 24) & 15u, carry, lane);
       if (base + 32 < n_in) {  // every lane has a first event; some a second
-        const int i1 = i0 + 32;
-        const EvOut o0 = ev_input<kPow2, false, kLong>(a, CT, ts, tg, rec, gs, i0, steps, true, acc, d0);
-        const EvOut o1 = ev_input<kPow2, false, kLong>(a, CT, ts, tg, rec, gs, min(i1, n_in - 1), steps, i1 < n_in,
-                                                acc, d1);
+        const uint32_t s1 = round_state(v1 ? 1u << ((w1 >> 6) & 3u) : 0u, (int)(R1.x & 511u), base + 32,
+                                        (R1.x >> 24) & 15u, carry, lane);
+        const EvOut o0 = ev_input<kPow2, false>(a, CT, ts, tg, gs, i0, w0, R0, s0, true, acc, d0);
+        const EvOut o1 = ev_input<kPow2, false>(a, CT, ts, tg, gs, min(i1, n_in - 1), w1, R1, s1, v1, acc, d1);
         ev_commit<kExact>(A, hist, o0, item, c0);
-        if (i1 < n_in) ev_commit<kExact>(A, hist, o1, item, c0);
+        if (v1) ev_commit<kExact>(A, hist, o1, item, c0);
       } else if (i0 < n_in) {
-        ev_commit<kExact>(A, hist, ev_input<kPow2, false, kLong>(a, CT, ts, tg, rec, gs, i0, steps, true, acc, d0), item,
+        ev_commit<kExact>(A, hist, ev_input<kPow2, false>(a, CT, ts, tg, gs, i0, w0, R0, s0, true, acc, d0), item,
                           c0);
       }
     }
@@ -1339,12 +1384,12 @@ __device__ __forceinline__ void band_item(const BandRunArgs& A, const CellTab& C
       const int i0 = base + lane;
       if (base + 32 < n) {
         const int i1 = i0 + 32;
-        const EvOut o0 = ev_output<kPow2, false>(a, ts, tg, rec, gs, i0, n, steps, true, acc, d0);
-        const EvOut o1 = ev_output<kPow2, false>(a, ts, tg, rec, gs, min(i1, n - 1), n, steps, i1 < n, acc, d1);
+        const EvOut o0 = ev_output<kPow2, false>(a, ts, tg, rec, gs, i0, n, true, acc, d0);
+        const EvOut o1 = ev_output<kPow2, false>(a, ts, tg, rec, gs, min(i1, n - 1), n, i1 < n, acc, d1);
         ev_commit<kExact>(A, hist, o0, item, c0);
         if (i1 < n) ev_commit<kExact>(A, hist, o1, item, c0);
       } else if (i0 < n) {
-        ev_commit<kExact>(A, hist, ev_output<kPow2, false>(a, ts, tg, rec, gs, i0, n, steps, true, acc, d0), item, c0);
+        ev_commit<kExact>(A, hist, ev_output<kPow2, false>(a, ts, tg, rec, gs, i0, n, true, acc, d0), item, c0);
       }
     }
   }
@@ -1500,10 +1545,7 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
           break;
         }
         phase ^= 1u;
-        if (gcur.steps > 3)  // an item with a pin segment of 8 to 15 events (warp-uniform)
-          band_item<kPow2, kDebug, kExact, true>(A, CT, hist, wbuf, my, gcur, c0, acc);
-        else
-          band_item<kPow2, kDebug, kExact, false>(A, CT, hist, wbuf, my, gcur, c0, acc);
+        band_item<kPow2, kDebug, kExact>(A, CT, hist, wbuf, my, gcur, c0, acc);
         if (++since == kTotEvery) {
           bflush_acc(acc, s_tot);
           since = 0;

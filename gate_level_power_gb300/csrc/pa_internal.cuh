@@ -139,11 +139,12 @@ struct RunArgs {
 // unit is one non-empty (gate, window). Units are
 // ordered band by band, gate by gate; work items are runs of whole units of
 // one band. Inside an item the events are stored in two regions: first the
-// input-pin events of all its units (unit by unit, each unit's pins in order,
-// each pin in time order), then the output-pin events (unit by unit, in time
-// order). Each event carries a one-byte tag (unit within the item, and the
-// input pin), each unit a 16-byte record (region offsets, pin starts, window
-// start state, cell, load-axis interval and fraction, load). Windows start on
+// input-pin events of all its units (unit by unit, each unit's events merged
+// in (time, pin) order), then the output-pin events (unit by unit, in time
+// order). Each event carries a two-byte tag word (unit within the item, input
+// pin, distance back to the pin's previous event in the unit), each unit a
+// 16-byte record (region offsets, input count, window start state, cell,
+// load-axis interval and fraction, load). Windows start on
 // cycle boundaries, so the event before a unit's first event on a pin lies in
 // an earlier cycle: glitches never straddle units. Gates with more than
 // kUnitPinMax events of one pin in a single cycle ("big" gates) stay out of
@@ -162,9 +163,9 @@ constexpr int kItemUnits = 64;                   // units per item (cap): 6-bit 
 // every kItemUnits units), so an item holds fewer than kItemEvents events.
 
 // Item word `bw`: band (bits 0..19; items[n_items] is a sentinel with band =
-// n_bands) | input events of the item (bits 20..28) | binary-lifting steps
-// that cover the item's longest input-pin segment (bits 29..31: the smallest
-// s with 2^s > that length, 0..4).
+// n_bands) | input events of the item (bits 20..28) | a size class of the
+// item's longest input-pin run (bits 29..31: the smallest s with 2^s > that
+// length, 0..4; informational).
 constexpr uint32_t kItemBandBits = 20;
 constexpr uint32_t kItemBandMask = (1u << kItemBandBits) - 1u;
 constexpr uint32_t kItemStepShift = 29;
@@ -173,14 +174,18 @@ constexpr uint32_t kItemStepShift = 29;
 //   x: input offset in the item (bits 0..8) | output offset in the item (9..17)
 //      | cell (18..23) | input state at the window start (24..27)
 //      | load-axis interval j (28..30)
-//   y: start of input pins 1, 2, 3 and the end of the inputs, one byte each
-//      (pins beyond k start at the end), | (k - 1) << 30
+//      | the unit has input events at one time on two pins (31)
+//   y: the unit's input events (bits 0..5) | the output pin's value at the
+//      window start (6) | (k - 1) << 30
 //   z: load-axis fraction v (f32), w: load C (f32, fF)
-//   y also holds, in bit 6, the output pin's value at the window start.
+// A unit's input events are stored in (time, pin) order (the merge of its
+// pins' time-ordered runs), its output events in time order.
 // Unit record of the walk (uint2, a build temporary): x = counts of pins 0..4
 // (4 bits each) | start state << 20 | cell << 24 (6 bits) | output value at
 // the window start << 30, y = load (f32 bits).
-// Event tag (u8): unit within the item (bits 0..5) | input pin (bits 6..7).
+// Event tag word (u16): unit within the item (bits 0..5) | input pin (bits
+// 6..7) | for an input event, the distance back (in the unit's (time, pin)
+// order) to the previous event of its pin in the unit, 0 if none (bits 8..15).
 struct BandItem {
   uint64_t e0;    // first event in the banded arrays
   uint32_t u0;    // first unit
@@ -195,7 +200,7 @@ struct BandLayout {
   uint32_t n_units = 0, n_items = 0, n_big = 0;
   float* bt = nullptr;        // [n_ev + pad] banded times
   float* bs = nullptr;        // [n_ev + pad] banded slews
-  uint8_t* btag = nullptr;    // [n_ev + pad] event tags
+  uint16_t* btag = nullptr;   // [n_ev + pad] event tag words
   uint4* urec = nullptr;      // [n_units] unit records
   uint32_t* ugate = nullptr;  // [n_units] gate of each unit
   BandItem* items = nullptr;  // [n_items + 1]

@@ -304,8 +304,8 @@ int pa_load_events(pa_ctx *ctx, const pa_events *ev);
  * 8 to 15 events is a window of its own. Every non-empty (gate, window) is a
  * unit; units are ordered band by band and grouped into work items of at
  * most 511 events, and inside an item the events are copied into an input
- * region (the units' input-pin events, pin by pin in the per-pin CSR order)
- * followed by an output region. Dense gates thus get narrow
+ * region (each unit's input-pin events merged in (time, pin) order) followed
+ * by an output region. Dense gates thus get narrow
  * cycle windows and sparse gates wide ones, as in the event-density-aware
  * per-gate cycle partitioning (Figs. 5, 19 and 20), fixed here at load time by
  * a per-pin event bound instead of a per-thread event target. Every pa_run whose t_clk_ns equals this
@@ -316,8 +316,8 @@ int pa_load_events(pa_ctx *ctx, const pa_events *ev);
  * within the same run. Results agree with the unbanded path to floating-point
  * summation order.
  *   band_cycles  cycles per band: a power of two <= 4096; 0 = 4096
- * Memory: a second copy of the times and slews plus a one-byte tag (9 bytes
- * per event), 20 bytes per unit and 16 bytes per work item; the build also
+ * Memory: a second copy of the times and slews plus a two-byte tag word (10
+ * bytes per event), 20 bytes per unit and 16 bytes per work item; the build also
  * takes temporary space of about 24 bytes per (band, gate) and 32 bytes per
  * unit.
  * Errors: PA_ERR_ORDER (no events loaded), PA_ERR_ARG (t_clk_ns not > 0,
