@@ -875,14 +875,15 @@ constexpr size_t kStTagOff = (size_t)kStEv * 4;            // staged event tag w
 constexpr size_t kStRecOff = kStTagOff + (size_t)kStEv * 2; // staged unit records
 constexpr size_t kWarpB = kStRecOff + (size_t)kItemUnits * 16;
 constexpr size_t kHist = (size_t)kBandMaxCycles * 16;
-// Cell table in shared memory: per cell the slew axis as two float4 (points
-// 0..3 and 4..7, the halves swapped for cells with bit 2 set so that lanes
-// of different cells spread over the banks; points past ns - 2 read +inf),
-// then one info word per cell (ns - 1 | (nl - 1) << 8 | patch offset << 16;
-// a library of at most 64 cells with axes of at most 8 points has fewer than
-// 2^16 corner patches), then per cell and slew interval i the pair
-// {axis point i, 1 / interval width} (one 8-byte load per event).
-constexpr size_t kCellsB = (size_t)kSmemCells * 32 + (size_t)kSmemCells * 4 + (size_t)kSmemCells * 8 * 8;
+// Cell table in shared memory: per cell the slew axis points 0..8 at a
+// stride of 9 words (an odd stride, so that lanes of different cells spread
+// over the banks; points 1..8 past ns - 2 read +inf), then one info word per
+// cell (ns - 1 | (nl - 1) << 8 | patch offset << 16; a library of at most 64
+// cells with axes of at most 8 points has fewer than 2^16 corner patches),
+// then per cell and slew interval i the pair {axis point i, 1 / interval
+// width} (one 8-byte load per event).
+constexpr int kAxStride = 9;
+constexpr size_t kCellsB = (size_t)kSmemCells * kAxStride * 4 + (size_t)kSmemCells * 4 + (size_t)kSmemCells * 8 * 8;
 // Item records of the CTA's current and next chunk (the next one's copy in
 // flight while the current one is worked on), one more for the end.
 constexpr uint32_t kChunkMaxItems = 512;
@@ -1102,8 +1103,31 @@ __device__ __forceinline__ uint32_t round_state(uint32_t x, int in_off, int base
   return start ^ ex ^ before;
 }
 
+// The same for two rounds at once (staged indices base + l and base + 32 +
+// l): their pin bits travel through one scan in one word (the first round's
+// in bits 0..3, the second's in bits 8..11).
+__device__ __forceinline__ void pair_state(uint32_t xa, int offa, uint32_t sta, uint32_t xb, int offb, uint32_t stb,
+                                           int base, uint32_t& carry, int lane, uint32_t& sa, uint32_t& sb) {
+  const uint32_t x = xa | (xb << 8);
+  uint32_t v = x;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, v, d);
+    if (lane >= d) v ^= y;
+  }
+  const uint32_t ex = v ^ x;
+  const int ssa = offa > base ? offa - base : 0;
+  const int ssb = offb > base + 32 ? offb - base - 32 : 0;
+  const uint32_t befa = (__shfl_sync(0xffffffffu, ex, ssa) & 15u) ^ (offa < base ? carry : 0u);
+  sa = sta ^ (ex & 15u) ^ befa;
+  const uint32_t ca = __shfl_sync(0xffffffffu, (v & 15u) ^ befa, 31);  // into the second round
+  const uint32_t befb = ((__shfl_sync(0xffffffffu, ex, ssb) >> 8) & 15u) ^ (offb < base + 32 ? ca : 0u);
+  sb = stb ^ ((ex >> 8) & 15u) ^ befb;
+  carry = __shfl_sync(0xffffffffu, ((v >> 8) & 15u) ^ befb, 31);
+}
+
 struct CellTab {
-  const float4* saxv;     // [kSmemCells * 2] swizzled slew axes, +inf past ns - 2
+  const float* sax;       // [kSmemCells * kAxStride] slew axes, +inf past ns - 2
   const uint32_t* info;   // [kSmemCells] ns - 1 | (nl - 1) << 8 | patch offset << 16
   const float2* sxp;      // [kSmemCells * 8] {slew axis point i, 1 / (ax[i + 1] - ax[i])}
 };
@@ -1177,11 +1201,12 @@ __device__ __forceinline__ EvOut ev_input(const RunArgs& a, const CellTab& CT, c
   }
   const uint32_t cell = (R.x >> 18) & 63u;
   const uint32_t info = CT.info[cell];  // ns - 1 | (nl - 1) << 8 | patch offset << 16
-  // slew interval: axis points 1 .. ns - 2 that are <= s (independent compares)
-  const uint32_t sw = (cell >> 2) & 1u;
-  const float4 A0 = CT.saxv[2 * cell + sw], A1 = CT.saxv[2 * cell + (sw ^ 1u)];
-  const int lis = (int)(s >= A0.y) + (int)(s >= A0.z) + (int)(s >= A0.w) + (int)(s >= A1.x) + (int)(s >= A1.y) +
-                  (int)(s >= A1.z);
+  // slew interval: the number of axis points 1 .. ns - 2 that are <= s, by a
+  // three-step binary search over points 1..7 (sorted, +inf past ns - 2)
+  const float* axs = CT.sax + cell * kAxStride;
+  int lis = s >= axs[4] ? 4 : 0;
+  lis += s >= axs[lis + 2] ? 2 : 0;
+  lis += s >= axs[lis + 1] ? 1 : 0;
   const float2 ax = CT.sxp[cell * 8 + lis];
   const float uu2 = (s - ax.x) * ax.y;
   const int j = (int)((R.x >> 28) & 7u);
@@ -1366,18 +1391,20 @@ __device__ __forceinline__ void band_item(const BandRunArgs& A, const CellTab& C
       const bool v1 = i1 < n_in;
       const uint32_t w0 = tg[min(i0, n_in - 1)], w1 = tg[min(i1, n_in - 1)];
       const uint4 R0 = rec[w0 & 63u], R1 = rec[w1 & 63u];
-      const uint32_t s0 = round_state(i0 < n_in ? 1u << ((w0 >> 6) & 3u) : 0u, (int)(R0.x & 511u), base,
-                                      (R0.x >> 24) & 15u, carry, lane);
       if (base + 32 < n_in) {  // every lane has a first event; some a second
-        const uint32_t s1 = round_state(v1 ? 1u << ((w1 >> 6) & 3u) : 0u, (int)(R1.x & 511u), base + 32,
-                                        (R1.x >> 24) & 15u, carry, lane);
+        uint32_t s0, s1;
+        pair_state(1u << ((w0 >> 6) & 3u), (int)(R0.x & 511u), (R0.x >> 24) & 15u, v1 ? 1u << ((w1 >> 6) & 3u) : 0u,
+                   (int)(R1.x & 511u), (R1.x >> 24) & 15u, base, carry, lane, s0, s1);
         const EvOut o0 = ev_input<kPow2, false>(a, CT, ts, tg, gs, i0, w0, R0, s0, true, acc, d0);
         const EvOut o1 = ev_input<kPow2, false>(a, CT, ts, tg, gs, min(i1, n_in - 1), w1, R1, s1, v1, acc, d1);
         ev_commit<kExact>(A, hist, o0, item, c0);
         if (v1) ev_commit<kExact>(A, hist, o1, item, c0);
-      } else if (i0 < n_in) {
-        ev_commit<kExact>(A, hist, ev_input<kPow2, false>(a, CT, ts, tg, gs, i0, w0, R0, s0, true, acc, d0), item,
-                          c0);
+      } else {
+        const uint32_t s0 = round_state(i0 < n_in ? 1u << ((w0 >> 6) & 3u) : 0u, (int)(R0.x & 511u), base,
+                                        (R0.x >> 24) & 15u, carry, lane);
+        if (i0 < n_in)
+          ev_commit<kExact>(A, hist, ev_input<kPow2, false>(a, CT, ts, tg, gs, i0, w0, R0, s0, true, acc, d0), item,
+                            c0);
       }
     }
     for (int base = n_in; base < n; base += 64) {
@@ -1420,19 +1447,18 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
   for (uint32_t i = tid; i < 4 * kBandMaxCycles; i += kBT) hist[i] = 0.f;
   CellTab CT;
   {  // the layout is only built for libraries of at most kSmemCells cells
-    float* saxv = reinterpret_cast<float*>(cells_s);
-    uint32_t* info = cells_s + kSmemCells * 8;
+    float* sax = reinterpret_cast<float*>(cells_s);
+    uint32_t* info = cells_s + kSmemCells * kAxStride;
     float2* sxp = reinterpret_cast<float2*>(info + kSmemCells);
     const uint32_t nc = min(a.n_cells, (uint32_t)kSmemCells);
-    for (uint32_t i = tid; i < nc * 8u; i += kBT) {
-      const uint32_t ci = i >> 3, m = i & 7u;
+    for (uint32_t i = tid; i < nc * (uint32_t)kAxStride; i += kBT) {
+      const uint32_t ci = i / kAxStride, m = i % kAxStride;
       const CellDesc& cd = a.cells[ci];
       if (m == 0) info[ci] = (uint32_t)(cd.ns - 1) | ((uint32_t)(cd.nl - 1) << 8) | (cd.patch_off << 16);
-      const uint32_t half = (m >> 2) ^ ((ci >> 2) & 1u);
-      saxv[ci * 8 + half * 4 + (m & 3u)] = (int)m <= (int)cd.ns - 2 ? cd.sax[m] : __int_as_float(0x7f800000);
-      sxp[ci * 8 + m] = make_float2(cd.sax[m], cd.isax[m]);
+      sax[i] = m == 0 ? cd.sax[0] : ((int)m <= (int)cd.ns - 2 ? cd.sax[m] : __int_as_float(0x7f800000));
+      if (m < 8) sxp[ci * 8 + m] = make_float2(cd.sax[m], cd.isax[m]);
     }
-    CT.saxv = reinterpret_cast<const float4*>(saxv);
+    CT.sax = sax;
     CT.info = info;
     CT.sxp = sxp;
   }
