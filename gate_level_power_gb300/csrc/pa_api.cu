@@ -39,7 +39,7 @@ struct pa_ctx {
   bool has_lib = false;
   uint32_t n_cells = 0;
   std::vector<CellDesc> h_cells;
-  DevBuf cells, lut, leak, patch, dleak;
+  DevBuf cells, lut, leak, patch;
 
   // netlist
   bool has_net = false;
@@ -301,7 +301,6 @@ RunArgs make_run_args(pa_ctx* c, const RunPlan& plan, const PassBufs& B) {
   a.lut = (const float*)c->lut.p;
   a.leak = (const float*)c->leak.p;
   a.patch = (const float4*)c->patch.p;
-  a.dleak = (const float*)c->dleak.p;
   a.gates = (const GateRec*)c->gates.p;
   a.n_gates = plan.G;
   a.pin_off = (const uint64_t*)c->pin_off.p;
@@ -780,7 +779,7 @@ void pa_destroy(pa_ctx* c) {
   if (!c) return;
   cudaSetDevice(c->device);
   if (c->stream) cudaStreamSynchronize(c->stream);
-  DevBuf* all[] = {&c->cells, &c->lut, &c->leak, &c->patch, &c->dleak, &c->gates, &c->pin_off, &c->gate_off, &c->t, &c->s,
+  DevBuf* all[] = {&c->cells, &c->lut, &c->leak, &c->patch, &c->gates, &c->pin_off, &c->gate_off, &c->t, &c->s,
                    &c->value_tmp, &c->err_word, &c->tmax_bits, &c->val_starts, &c->bins, &c->part_blk,
                    &c->part_counts, &c->tiles, &c->heavy, &c->p0_tot, &c->p_out, &c->dbg[0],
                    &c->dbg[1], &c->dbg[2], &c->wave_tmp, &c->cnt_tmp, &c->gate_tmp, &c->cell_tmp, &c->scratch_small,
@@ -853,9 +852,8 @@ int pa_load_library(pa_ctx* c, const pa_library* L) {
     if (!is_finite_f(L->leak[i])) return fail(c, PA_ERR_ARG, "leakage value %llu not finite", (unsigned long long)i);
     leak_uw[i] = (float)((double)L->leak[i] * 1e-3);  // nW -> uW (= fJ / ns)
   }
-  // derived tables: LUT corner patches and per-(state, pin) leakage steps
+  // derived table: LUT corner patches
   std::vector<float> patch;
-  std::vector<float> dleak((size_t)L->n_cells * kDleakStride, 0.f);
   for (uint32_t ci = 0; ci < L->n_cells; ++ci) {
     CellDesc& d = cells[ci];
     d.patch_off = (uint32_t)(patch.size() / 4);
@@ -869,16 +867,10 @@ int pa_load_library(pa_ctx* c, const pa_library* L) {
           patch.push_back(T[(i + 1) * nl + j]);
           patch.push_back(T[(i + 1) * nl + j + 1]);
         }
-      for (int p = 0; p < k; ++p) {
-        const float a = leak_uw[d.leak_off + (st ^ (1 << p))], b = leak_uw[d.leak_off + st];
-        dleak[(size_t)ci * kDleakStride + st * 4 + p] = a - b;
-      }
     }
   }
   PA_TRY(dreserve(c, c->patch, patch.size() * sizeof(float)));
-  PA_TRY(dreserve(c, c->dleak, dleak.size() * sizeof(float)));
   CUDA_TRY(c, cudaMemcpyAsync(c->patch.p, patch.data(), patch.size() * sizeof(float), cudaMemcpyHostToDevice, c->stream));
-  CUDA_TRY(c, cudaMemcpyAsync(c->dleak.p, dleak.data(), dleak.size() * sizeof(float), cudaMemcpyHostToDevice, c->stream));
   PA_TRY(dreserve(c, c->cells, cells.size() * sizeof(CellDesc)));
   PA_TRY(dreserve(c, c->lut, L->lut_len * sizeof(float)));
   PA_TRY(dreserve(c, c->leak, L->leak_len * sizeof(float)));

@@ -881,9 +881,13 @@ constexpr size_t kHist = (size_t)kBandMaxCycles * 16;
 // cell (ns - 1 | (nl - 1) << 8 | patch offset << 16; a library of at most 64
 // cells with axes of at most 8 points has fewer than 2^16 corner patches),
 // then per cell and slew interval i the pair {axis point i, 1 / interval
-// width} (one 8-byte load per event).
+// width} (one 8-byte load per event), then per cell its leakage per state
+// (uW, at a stride of 17 words: the step of an event is the difference of
+// two of them, the same f32 subtraction as the unbanded kernel's).
 constexpr int kAxStride = 9;
-constexpr size_t kCellsB = (size_t)kSmemCells * kAxStride * 4 + (size_t)kSmemCells * 4 + (size_t)kSmemCells * 8 * 8;
+constexpr int kLeakStride = 17;
+constexpr size_t kCellsB = (size_t)kSmemCells * kAxStride * 4 + (size_t)kSmemCells * 4 + (size_t)kSmemCells * 8 * 8 +
+                           (size_t)kSmemCells * kLeakStride * 4;
 // Item records of the CTA's current and next chunk (the next one's copy in
 // flight while the current one is worked on), one more for the end.
 constexpr uint32_t kChunkMaxItems = 512;
@@ -1130,6 +1134,7 @@ struct CellTab {
   const float* sax;       // [kSmemCells * kAxStride] slew axes, +inf past ns - 2
   const uint32_t* info;   // [kSmemCells] ns - 1 | (nl - 1) << 8 | patch offset << 16
   const float2* sxp;      // [kSmemCells * 8] {slew axis point i, 1 / (ax[i + 1] - ax[i])}
+  const float* leak;      // [kSmemCells * kLeakStride] leakage per state, uW
 };
 
 // One event's result before any shared or global memory is written: its
@@ -1216,7 +1221,8 @@ __device__ __forceinline__ EvOut ev_input(const RunArgs& a, const CellTab& CT, c
   const float vv = __uint_as_float(R.z);
   const float r0 = fmaf(vv, P.y - P.x, P.x), r1 = fmaf(vv, P.w - P.z, P.z);
   const float e_int = fmaf(uu2, r1 - r0, r0);
-  const float dp = __ldg(a.dleak + cell * kDleakStride + s_b * 4 + p);
+  const float* lk = CT.leak + cell * kLeakStride;
+  const float dp = lk[s_b ^ (1u << p)] - lk[s_b];
   const float T = a.t_clk;
   const uint32_t c = cyc<kPow2>(t, T, a.inv_t_clk);
   int en = -1;
@@ -1458,7 +1464,14 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
       sax[i] = m == 0 ? cd.sax[0] : ((int)m <= (int)cd.ns - 2 ? cd.sax[m] : __int_as_float(0x7f800000));
       if (m < 8) sxp[ci * 8 + m] = make_float2(cd.sax[m], cd.isax[m]);
     }
+    float* lk = reinterpret_cast<float*>(sxp + kSmemCells * 8);
+    for (uint32_t i = tid; i < nc * (uint32_t)kLeakStride; i += kBT) {
+      const uint32_t ci = i / kLeakStride, st = i % kLeakStride;
+      const CellDesc& cd = a.cells[ci];
+      lk[i] = st < (1u << cd.k) ? a.leak[cd.leak_off + st] : 0.f;
+    }
     CT.sax = sax;
+    CT.leak = lk;
     CT.info = info;
     CT.sxp = sxp;
   }

@@ -28,12 +28,9 @@ struct __align__(16) CellDesc {
   float isax[8], ilax[8];  // 1 / (ax[i+1] - ax[i])
 };
 
-// Derived tables built with the library (used by the banded kernel): for each
+// Derived table built with the library (used by the banded kernel): for each
 // state and interpolation cell (i, j) of a LUT the four corners {L[i][j],
-// L[i][j+1], L[i+1][j], L[i+1][j+1]} as one float4, and for each cell, state s
-// and input pin p the leakage step leak[s ^ (1 << p)] - leak[s] (f32, uW) at
-// index cell * kDleakStride + s * 4 + p.
-constexpr int kDleakStride = 64;
+// L[i][j+1], L[i+1][j], L[i+1][j+1]} as one float4.
 
 // Per-gate record (16 B): pin base, cell, load, initial values and k.
 struct __align__(16) GateRec {
@@ -85,7 +82,6 @@ struct RunArgs {
   const float* lut;
   const float* leak;       // uW
   const float4* patch;     // LUT corner patches
-  const float* dleak;      // leakage steps per (cell, state, pin)
   const GateRec* gates;
   uint32_t n_gates;
   const uint64_t* pin_off;
