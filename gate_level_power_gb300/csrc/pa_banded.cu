@@ -890,7 +890,7 @@ constexpr size_t kCellsB = (size_t)kSmemCells * kAxStride * 4 + (size_t)kSmemCel
                            (size_t)kSmemCells * kLeakStride * 4;
 // Item records of the CTA's current and next chunk (the next one's copy in
 // flight while the current one is worked on), one more for the end.
-constexpr uint32_t kChunkMaxItems = 512;
+constexpr uint32_t kChunkMaxItems = 680;
 constexpr size_t kChunkRecB = (size_t)(kChunkMaxItems + 1) * sizeof(BandItem);
 constexpr size_t kSmemB = kHist + kCellsB + kBW * kWarpB + 2 * kChunkRecB;
 static_assert(kStTagOff % 16 == 0 && kStRecOff % 16 == 0 && kWarpB % 16 == 0 && kHist % 16 == 0 &&
