@@ -442,6 +442,7 @@ def run_ours(args):
     d2h = 4 * N + 4 * N + 4 * N + 4 * 8
     e2e_value = None
     e2e_paths = {}
+    e2e_step_ms = {}
     if args.e2e_steps > 0:
         # A one-shot run through the public API: load the step's events from
         # pinned host memory and run, either straight on the loaded per-pin
@@ -464,11 +465,15 @@ def run_ours(args):
             dist.barrier()
             torch.cuda.synchronize()
             t0 = time.perf_counter()
+            step_ms = []
             for _ in range(args.e2e_steps):
-                e2e_step(path)
+                ts = time.perf_counter()
+                e2e_step(path)  # synchronous: returns once the results are on the host
+                step_ms.append(round((time.perf_counter() - ts) * 1e3, 2))
             torch.cuda.synchronize()
             e2e_s = dist.max(time.perf_counter() - t0)
             e2e_paths[path] = world * E * args.e2e_steps / e2e_s
+            e2e_step_ms[path] = step_ms
         e2e_value = max(e2e_paths.values())
     clk.active = False
     clk.stop()
@@ -501,6 +506,7 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "e2e": None if e2e_value is None else {"value": e2e_value, "unit": "events/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": args.e2e_steps, "paths": e2e_paths,
+                    "step_ms": e2e_step_ms,
                     "note": "per step from pinned host memory: pa_run_stream (chunked copies overlapping "
                             "validation and the unbanded kernel), or pa_load_events (device-side validation) + "
                             "pa_run (+ pa_build_bands before it on the banded path); waveform/count copy to host; "
