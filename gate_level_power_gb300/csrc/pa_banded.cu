@@ -702,6 +702,7 @@ __global__ void __launch_bounds__(kFinWarps * 32) k_bw_finalize(const BandBuildA
         tag |= (uint32_t)p << 6;
       } else {
         dst = (int)n_in_all + (int)((d >> 9) & 511u) + (li - n_in);
+        if (li > n_in) tag |= 1u << 8;  // the output's previous event is the one just before
       }
       dd[wl][i] = (uint16_t)dst;
       gb[wl][dst] = (uint16_t)tag;
@@ -748,7 +749,7 @@ __global__ void __launch_bounds__(kFinWarps * 32) k_bw_finalize(const BandBuildA
         const uint32_t x = (d & 511u) | ((n_in_all + ((d >> 9) & 511u)) << 9) | (cell << 18) |
                            (((w.x >> 20) & 15u) << 24) | ((uint32_t)j << 28) |
                            (((utie[wl][uu >> 5] >> (uu & 31)) & 1u) << 31);
-        L.urec[u0 + uu] = make_uint4(x, upin[wl][uu], __float_as_uint(v), w.y);
+        L.urec[u0 + uu] = make_uint4(x, __float_as_uint(v), w.y, upin[wl][uu]);
       }
     }
     __syncwarp();
@@ -1190,8 +1191,8 @@ __device__ __forceinline__ float glitch_scale(const RunArgs& a, const float* ts,
 // padding lane, not counted.
 template <bool kPow2, bool kDebug>
 __device__ __forceinline__ EvOut ev_input(const RunArgs& a, const CellTab& CT, const float* ts, const uint16_t* tg,
-                                          const float* gs, int i, uint32_t w, const uint4& R, uint32_t s_b,
-                                          bool valid, BAcc& acc, EvDbg& dbg) {
+                                          const uint4* rec, const float* gs, int i, uint32_t w, const uint2& R,
+                                          uint32_t s_b, bool valid, BAcc& acc, EvDbg& dbg) {
   const float t = ts[i];
   const float s = __ldg(gs + i);
   const int p = (int)((w >> 6) & 3u);
@@ -1218,7 +1219,7 @@ __device__ __forceinline__ EvOut ev_input(const RunArgs& a, const CellTab& CT, c
   // corners {L[i][j], L[i][j+1], L[i+1][j], L[i+1][j+1]} of the state's table
   const float4 P =
       __ldg(a.patch + (info >> 16) + ((int)s_pre * (int)(info & 0xFFu) + lis) * (int)((info >> 8) & 0xFFu) + j);
-  const float vv = __uint_as_float(R.z);
+  const float vv = __uint_as_float(R.y);
   const float r0 = fmaf(vv, P.y - P.x, P.x), r1 = fmaf(vv, P.w - P.z, P.z);
   const float e_int = fmaf(uu2, r1 - r0, r0);
   const float* lk = CT.leak + cell * kLeakStride;
@@ -1227,7 +1228,7 @@ __device__ __forceinline__ EvOut ev_input(const RunArgs& a, const CellTab& CT, c
   const uint32_t c = cyc<kPow2>(t, T, a.inv_t_clk);
   int en = -1;
   if (kDebug && a.glitch_all) {  // the pin's next event in the unit
-    const int end = (int)(R.x & 511u) + (int)(R.y & 63u);
+    const int end = (int)(R.x & 511u) + (int)(rec[w & 63u].w & 63u);
     for (int m = i + 1; m < end; ++m)
       if ((int)((tg[m] >> 6) & 3u) == p) {
         en = m;
@@ -1254,20 +1255,23 @@ template <bool kPow2, bool kDebug>
 __device__ __forceinline__ EvOut ev_output(const RunArgs& a, const float* ts, const uint16_t* tg, const uint4* rec,
                                            const float* gs, int i, int n, bool valid, BAcc& acc, EvDbg& dbg) {
   const uint32_t w = tg[i];
-  const uint4 R = rec[w & 63u];
   const float t = ts[i];
-  const int idx = i - (int)((R.x >> 9) & 511u);
+  const bool has_prev = (w >> 8) != 0u;  // the unit's previous output event is the one just before
   // the slew only enters a glitch ratio: loaded for lanes whose previous event
   // is on the pin (or, in the glitch-all reading, for every lane)
   float s = 0.f;
-  if (idx > 0 || (kDebug && a.glitch_all)) s = __ldg(gs + i);
-  float e_sw = a.half_vdd2 * __uint_as_float(R.w);
-  if (kDebug && a.esw_rise)  // C V^2 on a rise: the output's value at the window start, flipped per earlier event
-    e_sw = ((((R.y >> 6) & 1u) ^ ((uint32_t)(idx + 1) & 1u)) != 0u) ? 2.f * e_sw : 0.f;
+  if (has_prev || (kDebug && a.glitch_all)) s = __ldg(gs + i);
+  float e_sw = a.half_vdd2 * __uint_as_float(reinterpret_cast<const uint32_t*>(rec)[(w & 63u) * 4u + 2u]);
+  uint4 R = make_uint4(0u, 0u, 0u, 0u);
+  if (kDebug) R = rec[w & 63u];
+  if (kDebug && a.esw_rise) {  // C V^2 on a rise: the output's value at the window start, flipped per earlier event
+    const int idx = i - (int)((R.x >> 9) & 511u);
+    e_sw = ((((R.w >> 6) & 1u) ^ ((uint32_t)(idx + 1) & 1u)) != 0u) ? 2.f * e_sw : 0.f;
+  }
   const uint32_t c = cyc<kPow2>(t, a.t_clk, a.inv_t_clk);
   const int en = (kDebug && a.glitch_all && i + 1 < n && (tg[i + 1] & 63u) == (w & 63u)) ? i + 1 : -1;
   bool glitch;
-  const float e_w = glitch_scale<kPow2, kDebug>(a, ts, gs, idx > 0 ? i - 1 : i, idx > 0, en, t, s, c, e_sw, glitch);
+  const float e_w = glitch_scale<kPow2, kDebug>(a, ts, gs, has_prev ? i - 1 : i, has_prev, en, t, s, c, e_sw, glitch);
   if (valid) {
     acc.e_gl += glitch ? e_w : 0.f;
     acc.e_sw += glitch ? 0.f : e_sw;
@@ -1276,9 +1280,9 @@ __device__ __forceinline__ EvOut ev_output(const RunArgs& a, const float* ts, co
     // input values before t: the unit's start state flipped by its input
     // events earlier than t (in time order)
     uint32_t s_pre = (R.x >> 24) & 15u;
-    const int in_off = (int)(R.x & 511u), in_end = in_off + (int)(R.y & 63u);
+    const int in_off = (int)(R.x & 511u), in_end = in_off + (int)(R.w & 63u);
     for (int m = in_off; m < in_end && ts[m] < t; ++m) s_pre ^= 1u << ((tg[m] >> 6) & 3u);
-    dbg = EvDbg{s_pre, 0xFFu, w & 63u, (int)(R.y >> 30) + 1, t, glitch, 0.f, glitch ? 0.f : e_sw,
+    dbg = EvDbg{s_pre, 0xFFu, w & 63u, (int)(R.w >> 30) + 1, t, glitch, 0.f, glitch ? 0.f : e_sw,
                 glitch ? e_w : 0.f, 0.f};
   }
   return EvOut{c, e_w, 0.f, glitch ? 2u : 0u};
@@ -1354,6 +1358,7 @@ __device__ __forceinline__ void band_item(const BandRunArgs& A, const CellTab& C
   const float* ts = reinterpret_cast<const float*>(stage) + g.ev_off;
   const uint16_t* tg = reinterpret_cast<const uint16_t*>(stage + kStTagOff) + g.tag_off;
   const uint4* rec = reinterpret_cast<const uint4*>(stage + kStRecOff);
+  const uint2* rec2 = reinterpret_cast<const uint2*>(stage + kStRecOff);  // {x, v} of unit u at 2 u
   const float* gs = A.L.bs + g.e0;  // slews: read once, from HBM (prefetched into L2 ahead of the item)
   // and into L1: one 128-byte line per lane
   if ((uint32_t)lane * 32u < g.ev_off + g.n)
@@ -1370,10 +1375,10 @@ __device__ __forceinline__ void band_item(const BandRunArgs& A, const CellTab& C
         const bool v = i < n_in;
         const int jj = v ? i : n_in - 1;
         const uint32_t w = tg[jj];
-        const uint4 R = rec[w & 63u];
+        const uint2 R = rec2[(w & 63u) * 2u];
         const uint32_t sb = round_state(v ? 1u << ((w >> 6) & 3u) : 0u, (int)(R.x & 511u), base,
                                         (R.x >> 24) & 15u, carry, lane);
-        if (v) o = ev_input<kPow2, true>(a, CT, ts, tg, gs, i, w, R, sb, true, acc, d0);
+        if (v) o = ev_input<kPow2, true>(a, CT, ts, tg, rec, gs, i, w, R, sb, true, acc, d0);
         else if (valid) o = ev_output<kPow2, true>(a, ts, tg, rec, gs, i, n, true, acc, d0);
       } else if (valid) {
         o = ev_output<kPow2, true>(a, ts, tg, rec, gs, i, n, true, acc, d0);
@@ -1396,21 +1401,21 @@ __device__ __forceinline__ void band_item(const BandRunArgs& A, const CellTab& C
       const int i0 = base + lane, i1 = i0 + 32;
       const bool v1 = i1 < n_in;
       const uint32_t w0 = tg[min(i0, n_in - 1)], w1 = tg[min(i1, n_in - 1)];
-      const uint4 R0 = rec[w0 & 63u], R1 = rec[w1 & 63u];
+      const uint2 R0 = rec2[(w0 & 63u) * 2u], R1 = rec2[(w1 & 63u) * 2u];
       if (base + 32 < n_in) {  // every lane has a first event; some a second
         uint32_t s0, s1;
         pair_state(1u << ((w0 >> 6) & 3u), (int)(R0.x & 511u), (R0.x >> 24) & 15u, v1 ? 1u << ((w1 >> 6) & 3u) : 0u,
                    (int)(R1.x & 511u), (R1.x >> 24) & 15u, base, carry, lane, s0, s1);
-        const EvOut o0 = ev_input<kPow2, false>(a, CT, ts, tg, gs, i0, w0, R0, s0, true, acc, d0);
-        const EvOut o1 = ev_input<kPow2, false>(a, CT, ts, tg, gs, min(i1, n_in - 1), w1, R1, s1, v1, acc, d1);
+        const EvOut o0 = ev_input<kPow2, false>(a, CT, ts, tg, rec, gs, i0, w0, R0, s0, true, acc, d0);
+        const EvOut o1 = ev_input<kPow2, false>(a, CT, ts, tg, rec, gs, min(i1, n_in - 1), w1, R1, s1, v1, acc, d1);
         ev_commit<kExact>(A, hist, o0, item, c0);
         if (v1) ev_commit<kExact>(A, hist, o1, item, c0);
       } else {
         const uint32_t s0 = round_state(i0 < n_in ? 1u << ((w0 >> 6) & 3u) : 0u, (int)(R0.x & 511u), base,
                                         (R0.x >> 24) & 15u, carry, lane);
         if (i0 < n_in)
-          ev_commit<kExact>(A, hist, ev_input<kPow2, false>(a, CT, ts, tg, gs, i0, w0, R0, s0, true, acc, d0), item,
-                            c0);
+          ev_commit<kExact>(A, hist, ev_input<kPow2, false>(a, CT, ts, tg, rec, gs, i0, w0, R0, s0, true, acc, d0),
+                            item, c0);
       }
     }
     for (int base = n_in; base < n; base += 64) {

@@ -171,9 +171,10 @@ constexpr uint32_t kItemStepShift = 29;
 //      | cell (18..23) | input state at the window start (24..27)
 //      | load-axis interval j (28..30)
 //      | the unit has input events at one time on two pins (31)
-//   y: the unit's input events (bits 0..5) | the output pin's value at the
+//   y: load-axis fraction v (f32), z: load C (f32, fF)
+//   w: the unit's input events (bits 0..5) | the output pin's value at the
 //      window start (6) | (k - 1) << 30
-//   z: load-axis fraction v (f32), w: load C (f32, fF)
+// (an input event reads {x, y}, an output event z)
 // A unit's input events are stored in (time, pin) order (the merge of its
 // pins' time-ordered runs), its output events in time order.
 // Unit record of the walk (uint2, a build temporary): x = counts of pins 0..4
@@ -181,7 +182,8 @@ constexpr uint32_t kItemStepShift = 29;
 // the window start << 30, y = load (f32 bits).
 // Event tag word (u16): unit within the item (bits 0..5) | input pin (bits
 // 6..7) | for an input event, the distance back (in the unit's (time, pin)
-// order) to the previous event of its pin in the unit, 0 if none (bits 8..15).
+// order) to the previous event of its pin in the unit, 0 if none; for an
+// output event 1 if the unit has an earlier output event (bits 8..15).
 struct BandItem {
   uint64_t e0;    // first event in the banded arrays
   uint32_t u0;    // first unit
