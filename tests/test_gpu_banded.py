@@ -151,9 +151,37 @@ def test_more_than_2_pow_24_events_in_one_cycle_banded(glp):
 def test_stress_waveform_banded(glp, m):
     # every pin toggling m times per cycle: single-cycle windows for m >= 4,
     # and at m = 8 (more than 7 events of a pin in a cycle) single-cycle
-    # windows whose pin segments need a fourth search step
+    # windows of up to 32 input events
     w = synth.generate(6, n_gates=40, n_cycles=300, toggles=m)
     r = banded_run(glp, w)
     o = oracle.run(w, debug=True, threads=4)
     assert_parity(r, o)
     assert r["n_tiles"] > 0 and r["n_heavy"] > 0
+
+
+@pytest.mark.parametrize("m", [15, 16])
+def test_longest_units_banded(glp, m):
+    # every pin toggling m times per cycle: at m = 15 the layout's longest
+    # units (a 4-input gate's window of one cycle holds 60 input events, so
+    # its states carry across rounds of 32 lanes); at m = 16 no gate fits a
+    # unit and all are streamed by the unbanded kernel in the same run
+    w = synth.generate(6, n_gates=40, n_cycles=60, toggles=m)
+    r = banded_run(glp, w)
+    o = oracle.run(w, debug=True, threads=4)
+    assert_parity(r, o)
+    assert r["n_heavy"] > 0
+    assert (r["n_tiles"] > 0) == (m == 15)
+    assert_parity(banded_run(glp, w, debug=False), o, debug=False)  # the two-rounds-per-lane path
+
+
+def test_tie_heavy_long_units_banded(glp):
+    # 4-input gates with about 9 events per pin per cycle on a 1/16 ns grid:
+    # long single-cycle units full of cross-pin ties (the pre-timestamp
+    # fix-up), a few pins past 15 events in a cycle (streamed gates)
+    w = synth.custom(seed=77, n_gates=30, n_cells=8, k_mode=2, n_slew=5, n_load=4, n_cycles=12, t_clk_ns=1.0,
+                     n_events=9000, pair_frac=0.0, quantum_ns=1 / 16, threads=2)
+    r = banded_run(glp, w, band_cycles=4)
+    o = oracle.run(w, debug=True)
+    assert_parity(r, o)
+    assert r["n_tiles"] > 0 and r["n_heavy"] > 0
+    assert_parity(banded_run(glp, w, band_cycles=4, debug=False), o, debug=False)
