@@ -6,15 +6,15 @@
 // its clock cycle (Fig. 7's atomicAdd into w). With one global atomic per event
 // a billion events are bound by the L2 atomic units. Here the events are first
 // regrouped (a load-time layout for one clock period) into units: one gate's
-// events inside one aligned window of 2^m cycles, the window chosen per gate so
-// that no pin has more than 15 events in it (the role of the paper's
-// event-density-aware cycle partitioning, Figs. 5, 19 and 20: dense gates get
-// narrow windows, sparse gates one window per band). Units are stored band by
-// band, so a CTA keeps the band's cycle bins in shared memory and adds them to
-// global memory once per band with a TMA bulk reduction. Inside a unit the
-// per-pin CSR order is kept, each pin segment holds at most 15 events, and the
-// gate state before an event is the unit's start state flipped by the parities
-// of the earlier events on each pin (short searches in the staged segments).
+// events inside one window of whole cycles of a band, cut greedily so that no
+// pin has more than 7 events in a window (15 in a window of one cycle) -- the
+// role of the paper's event-density-aware cycle partitioning, Figs. 5, 19 and
+// 20: dense gates get narrow windows, sparse gates one window per band. Units
+// are stored band by band, so a CTA keeps the band's cycle bins in shared
+// memory and adds them to global memory once per band with a TMA bulk
+// reduction. Inside a unit the input events are stored merged in (time, pin)
+// order, so the gate state before an event is the unit's start state flipped
+// by the pin bits of the unit's earlier events: a warp prefix XOR at run time.
 #include <cfloat>
 #include <cstdint>
 
@@ -1568,7 +1568,6 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
         gcur.n = __shfl_sync(0xffffffffu, gl.n, 0);
         gcur.nu = __shfl_sync(0xffffffffu, gl.nu, 0);
         gcur.n_in = __shfl_sync(0xffffffffu, gl.n_in, 0);
-        gcur.steps = __shfl_sync(0xffffffffu, gl.steps, 0);
         gcur.ev_off = __shfl_sync(0xffffffffu, gl.ev_off, 0);
         gcur.tag_off = __shfl_sync(0xffffffffu, gl.tag_off, 0);
         gcur.ev_bytes = gcur.tag_bytes = 0;
