@@ -437,6 +437,11 @@ def run_ours(args):
     el_ms = e0.elapsed_time(e1)
     el_ms = dist.max(el_ms)
     value = world * E * args.steps / (el_ms * 1e-3)
+    # the clocks are sampled over the device-resident timed region only: a
+    # running nvidia-smi poller measurably slows host-to-device copies (some
+    # 8 GB copies took 55-67 ms instead of 38 ms while it ran)
+    clk.active = False
+    clk.stop()
     # ---- end to end through the public API, host buffers
     h2d = 8 * (w.n_pins + 1) + 4 * E + 4 * E + E
     d2h = 4 * N + 4 * N + 4 * N + 4 * 8
@@ -475,8 +480,6 @@ def run_ours(args):
             e2e_paths[path] = world * E * args.e2e_steps / e2e_s
             e2e_step_ms[path] = step_ms
         e2e_value = max(e2e_paths.values())
-    clk.active = False
-    clk.stop()
     # ---- roofline of the fused kernel
     fused_mean = statistics.mean(fused_ms)
     B = algorithmic_bytes(w)
@@ -507,6 +510,8 @@ def run_ours(args):
             "e2e": None if e2e_value is None else {"value": e2e_value, "unit": "events/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": args.e2e_steps, "paths": e2e_paths,
                     "step_ms": e2e_step_ms,
+                    "paths_at_median_step": {k: world * E / (statistics.median(v) * 1e-3)
+                                             for k, v in e2e_step_ms.items() if v},
                     "note": "per step from pinned host memory: pa_run_stream (chunked copies overlapping "
                             "validation and the unbanded kernel), or pa_load_events (device-side validation) + "
                             "pa_run (+ pa_build_bands before it on the banded path); waveform/count copy to host; "
