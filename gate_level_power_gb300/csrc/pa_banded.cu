@@ -625,7 +625,7 @@ __global__ void __launch_bounds__(kFinWarps * 32) k_bw_finalize(const BandBuildA
     }
     const int n = (int)(e1 - e0), nu = (int)(u1 - u0);
     // units: sizes, the two regions' offsets, pin runs
-    uint32_t carry = 0, seg_max = 0;
+    uint32_t carry = 0;
     for (int r = 0; r < 2; ++r) {
       const int uu = lane + 32 * r;
       uint32_t pk = 0, n_in = 0, x = 0, ends = 0;
@@ -635,10 +635,7 @@ __global__ void __launch_bounds__(kFinWarps * 32) k_bw_finalize(const BandBuildA
         uint32_t s = 0;
 #pragma unroll
         for (int p = 0; p < kMaxK; ++p) {
-          if ((uint32_t)p < k) {
-            s += (x >> (4 * p)) & 15u;
-            seg_max = max(seg_max, (x >> (4 * p)) & 15u);
-          }
+          if ((uint32_t)p < k) s += (x >> (4 * p)) & 15u;
           ends |= s << (8 * p);
         }
         n_in = s;
@@ -758,11 +755,15 @@ __global__ void __launch_bounds__(kFinWarps * 32) k_bw_finalize(const BandBuildA
       L.bs[e0 + i] = sb[wl][i];
       L.btag[e0 + i] = gb[wl][i];
     }
+    // events sharing the cycle of the event stored before them (same region)
+    uint32_t cont = 0;
+    for (int i = lane + 1; i < n; i += 32)
+      cont += (i != (int)n_in_all && bcyc(a, tb[wl][i]) == bcyc(a, tb[wl][i - 1])) ? 1u : 0u;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) seg_max = max(seg_max, __shfl_xor_sync(0xffffffffu, seg_max, o));
-    const uint32_t steps = seg_max == 0 ? 0u : seg_max == 1 ? 1u : seg_max <= 3 ? 2u : seg_max <= 7 ? 3u : 4u;
+    for (int o = 16; o > 0; o >>= 1) cont += __shfl_xor_sync(0xffffffffu, cont, o);
     if (lane == 0)
-      L.items[it].bw = (L.items[it].bw & kItemBandMask) | (n_in_all << kItemBandBits) | (steps << kItemStepShift);
+      L.items[it].bw = (L.items[it].bw & kItemBandMask) | (n_in_all << kItemBandBits) |
+                       (3u * cont >= 2u * (uint32_t)n ? kItemRunsBit : 0u);
     __syncwarp();
   }
 }
@@ -1037,7 +1038,8 @@ __device__ uint32_t band_end(const BandItem* it, uint32_t lo, uint32_t hi, uint3
 // layout).
 struct ItemGeo {
   uint64_t e0, ea;
-  uint32_t u0, n, nu, n_in, steps, ev_off, tag_off, ev_bytes, tag_bytes;
+  uint32_t u0, n, nu, n_in, ev_off, tag_off, ev_bytes, tag_bytes;
+  bool runs;  // the item's events come in runs of one cycle (merge their bin updates)
   bool ok;
 };
 
@@ -1049,7 +1051,7 @@ __device__ __forceinline__ ItemGeo item_geo(const BandItem& a, const BandItem& b
   g.ev_off = (uint32_t)(a.e0 - g.ea);
   g.tag_off = (uint32_t)(a.e0 & 7ull);  // tag words: 16-byte copies of 8
   g.n_in = (a.bw >> kItemBandBits) & 511u;  // bits 20..28
-  g.steps = a.bw >> kItemStepShift;
+  g.runs = (a.bw & kItemRunsBit) != 0u;
   g.ok = b.e0 > a.e0 && b.u0 > a.u0 && b.e0 - a.e0 < (uint64_t)kItemEvents && b.u0 - a.u0 <= (uint32_t)kItemUnits &&
          (uint64_t)g.n_in <= b.e0 - a.e0;
   g.n = g.ok ? (uint32_t)(b.e0 - a.e0) : 0u;
@@ -1315,6 +1317,48 @@ __device__ __forceinline__ void ev_commit(const BandRunArgs& A, float* hist, con
   }
 }
 
+// The bins of one round of 32 events whose equal cycles come in runs of
+// neighbouring lanes (items flagged by the layout): a segmented sum over each
+// run of equal cycles, then one set of shared-memory atomics per run, by its
+// last lane, instead of one per event -- lanes of a run would otherwise hit
+// the same words and serialise. Called by all 32 lanes; `valid` false for
+// lanes without an event.
+__device__ __forceinline__ void ev_commit_runs(const BandRunArgs& A, float* hist, const EvOut& o, bool valid,
+                                               uint32_t item, uint32_t c0, int lane) {
+  uint32_t lc = o.c - c0;
+  if (valid && lc >= A.L.band_cycles) {  // an event outside its band: layout inconsistency
+    berr(A.r.err, item, kErrTileOverflow);
+    valid = false;
+  }
+  if (!valid) lc = 0xFFFFFFFFu;  // lanes without an event come last and form runs of their own
+  const uint32_t lc_up = __shfl_up_sync(0xffffffffu, lc, 1);
+  bool f = lane == 0 || lc_up != lc;  // the lane starts a run
+  float w = o.e_w, d = (o.flags & 1u) ? o.dp : 0.f;
+  uint32_t nc = valid ? (1u | ((o.flags & 2u) ? 1u << 16 : 0u)) : 0u;  // events | glitches << 16
+#pragma unroll
+  for (int sh = 1; sh < 32; sh <<= 1) {
+    const float w2 = __shfl_up_sync(0xffffffffu, w, sh), d2 = __shfl_up_sync(0xffffffffu, d, sh);
+    const uint32_t n2 = __shfl_up_sync(0xffffffffu, nc, sh);
+    const bool f2 = __shfl_up_sync(0xffffffffu, (int)f, sh) != 0;
+    if (lane >= sh) {
+      if (!f) {
+        w += w2;
+        d += d2;
+        nc += n2;
+      }
+      f = f || f2;
+    }
+  }
+  const uint32_t lc_dn = __shfl_down_sync(0xffffffffu, lc, 1);
+  if (valid && (lane == 31 || lc_dn != lc)) {  // the run's last lane holds its sums
+    float* h = hist + lc;
+    atomicAdd(h + kHW, w);
+    if (d != 0.f) atomicAdd(h + kHD, d);
+    atomicAdd(reinterpret_cast<uint32_t*>(h + kHE), nc & 0xFFFFu);
+    if (nc >> 16) atomicAdd(reinterpret_cast<uint32_t*>(h + kHG), nc >> 16);
+  }
+}
+
 // Debug outputs of one event: its CSR index is found by its time among its
 // pin's events.
 __device__ void event_debug(const RunArgs& a, uint32_t gate, int p, float t, uint32_t s_pre, int lut_ij,
@@ -1345,7 +1389,7 @@ __device__ void event_debug(const RunArgs& a, uint32_t gate, int p, float t, uin
 // then the output region. Input events take their states from a scan over
 // each round of 32; where a region has events left for a second round, each
 // lane computes two events before committing either.
-template <bool kPow2, bool kDebug, bool kExact>
+template <bool kPow2, bool kDebug, bool kExact, bool kRuns>
 __device__ __forceinline__ void band_item(const BandRunArgs& A, const CellTab& CT, float* hist,
                                           const uint8_t* stage, uint32_t item, const ItemGeo& g, uint32_t c0,
                                           BAcc& acc) {
@@ -1395,6 +1439,35 @@ __device__ __forceinline__ void band_item(const BandRunArgs& A, const CellTab& C
       }
       if (a.dbg_state || a.dbg_lut || a.dbg_glitch)
         event_debug(a, gate, d0.p, d0.t, d0.s_pre, (int)d0.lut_ij, d0.glitch, item);
+    }
+  } else if (kRuns) {
+    // the same rounds, every lane computing (padding lanes on a clamped
+    // index, not counted) so that the merged commit has all 32 lanes
+    for (int base = 0; base < n_in; base += 64) {
+      const int i0 = base + lane, i1 = i0 + 32;
+      const bool v0 = i0 < n_in, v1 = i1 < n_in;
+      const int j0 = min(i0, n_in - 1), j1 = min(i1, n_in - 1);
+      const uint32_t w0 = tg[j0], w1 = tg[j1];
+      const uint2 R0 = rec2[(w0 & 63u) * 2u], R1 = rec2[(w1 & 63u) * 2u];
+      if (base + 32 < n_in) {
+        uint32_t s0, s1;
+        pair_state(1u << ((w0 >> 6) & 3u), (int)(R0.x & 511u), (R0.x >> 24) & 15u, v1 ? 1u << ((w1 >> 6) & 3u) : 0u,
+                   (int)(R1.x & 511u), (R1.x >> 24) & 15u, base, carry, lane, s0, s1);
+        const EvOut o0 = ev_input<kPow2, false>(a, CT, ts, tg, rec, gs, j0, w0, R0, s0, true, acc, d0);
+        const EvOut o1 = ev_input<kPow2, false>(a, CT, ts, tg, rec, gs, j1, w1, R1, s1, v1, acc, d1);
+        ev_commit_runs(A, hist, o0, true, item, c0, lane);
+        ev_commit_runs(A, hist, o1, v1, item, c0, lane);
+      } else {
+        const uint32_t s0 = round_state(v0 ? 1u << ((w0 >> 6) & 3u) : 0u, (int)(R0.x & 511u), base,
+                                        (R0.x >> 24) & 15u, carry, lane);
+        const EvOut o0 = ev_input<kPow2, false>(a, CT, ts, tg, rec, gs, j0, w0, R0, s0, v0, acc, d0);
+        ev_commit_runs(A, hist, o0, v0, item, c0, lane);
+      }
+    }
+    for (int base = n_in; base < n; base += 32) {
+      const int i0 = base + lane;
+      const EvOut o0 = ev_output<kPow2, false>(a, ts, tg, rec, gs, min(i0, n - 1), n, i0 < n, acc, d0);
+      ev_commit_runs(A, hist, o0, i0 < n, item, c0, lane);
     }
   } else {
     for (int base = 0; base < n_in; base += 64) {
@@ -1572,6 +1645,7 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
         gcur.tag_off = __shfl_sync(0xffffffffu, gl.tag_off, 0);
         gcur.ev_bytes = gcur.tag_bytes = 0;
         gcur.ok = __shfl_sync(0xffffffffu, (int)gl.ok, 0) != 0;
+        gcur.runs = __shfl_sync(0xffffffffu, (int)gl.runs, 0) != 0;
         bool ok = false;
         for (uint32_t w = 0; w < kWaitLimit && !ok; ++w) ok = mbar_try_wait(bar, phase);
         ok = __all_sync(0xffffffffu, ok);
@@ -1588,7 +1662,10 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
           break;
         }
         phase ^= 1u;
-        band_item<kPow2, kDebug, kExact>(A, CT, hist, wbuf, my, gcur, c0, acc);
+        if (!kDebug && !kExact && gcur.runs)  // warp-uniform
+          band_item<kPow2, kDebug, kExact, true>(A, CT, hist, wbuf, my, gcur, c0, acc);
+        else
+          band_item<kPow2, kDebug, kExact, false>(A, CT, hist, wbuf, my, gcur, c0, acc);
         if (++since == kTotEvery) {
           bflush_acc(acc, s_tot);
           since = 0;

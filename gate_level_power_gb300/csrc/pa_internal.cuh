@@ -159,12 +159,14 @@ constexpr int kItemUnits = 64;                   // units per item (cap): 6-bit 
 // every kItemUnits units), so an item holds fewer than kItemEvents events.
 
 // Item word `bw`: band (bits 0..19; items[n_items] is a sentinel with band =
-// n_bands) | input events of the item (bits 20..28) | a size class of the
-// item's longest input-pin run (bits 29..31: the smallest s with 2^s > that
-// length, 0..4; informational).
+// n_bands) | input events of the item (bits 20..28) | bit 29: the item's
+// events come in runs of one cycle (at least two thirds of them share the
+// cycle of the event stored before them: runs of three or more on average),
+// so the run merges the bin updates of each run of equal cycles in a warp
+// before its shared-memory atomics.
 constexpr uint32_t kItemBandBits = 20;
 constexpr uint32_t kItemBandMask = (1u << kItemBandBits) - 1u;
-constexpr uint32_t kItemStepShift = 29;
+constexpr uint32_t kItemRunsBit = 1u << 29;
 
 // Unit record (uint4), written by the finalize pass:
 //   x: input offset in the item (bits 0..8) | output offset in the item (9..17)
