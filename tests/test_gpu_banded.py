@@ -157,6 +157,9 @@ def test_stress_waveform_banded(glp, m):
     o = oracle.run(w, debug=True, threads=4)
     assert_parity(r, o)
     assert r["n_tiles"] > 0 and r["n_heavy"] > 0
+    # the timed kernel: for m >= 2 the items come in runs of one cycle and merge
+    # their bin updates per run
+    assert_parity(banded_run(glp, w, debug=False), o, debug=False)
 
 
 @pytest.mark.parametrize("m", [15, 16])
