@@ -126,6 +126,23 @@ def test_build_bands_errors(glp):
             assert ei.value.code == glp.PA_ERR_ARG
 
 
+def test_band_count_limit(glp):
+    # events up to cycle ~1.1M: one-cycle bands would be more than the layout's
+    # 2^20 - 1 (rejected before any allocation); 4096-cycle bands are fine
+    w = synth.custom(seed=5, n_gates=5, n_cells=2, n_cycles=(1 << 20) + 50000, n_events=2000, threads=1)
+    assert int(np.floor(w.t_ns.astype(np.float32) / np.float32(w.t_clk_ns)).max()) >= (1 << 20)
+    o = oracle.run(w, debug=True)
+    with glp.PowerAnalyzer(0) as pa:
+        pa.load_workload(w)
+        with pytest.raises(glp.PaError) as ei:
+            pa.build_bands(w.t_clk_ns, 1)
+        assert ei.value.code == glp.PA_ERR_ARG
+        pa.build_bands(w.t_clk_ns)
+        r = pa.run(w.vdd, w.t_clk_ns, w.n_cycles, debug=True)
+    assert r["path"] == glp.PA_PATH_BANDED
+    assert_parity(r, o)
+
+
 def test_big_gates_banded(glp):
     # more than 15 events of a pin in one cycle: those gates stay out of the
     # banded layout and are streamed by the unbanded kernel in the same run
