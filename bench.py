@@ -28,7 +28,8 @@ metric.
 ``--partition density|fixed`` times the paper's (gate, window) thread partition
 instead (one thread per gate window, a global atomic per event);
 ``--partition-sweep`` compares the event-density-aware partition (n_evt,tgt =
-8) with globally fixed windows of 2 .. 32 cycles on one workload, one JSON line
+8; parallelism floors 1, 16 and 256) with globally fixed windows of 2 .. 32
+cycles on one workload, one JSON line
 per setting with the fused-kernel time and the thread statistics (thread
 count, events per thread at the 50th/90th/99th percentile and the maximum), the
 comparison of the paper's Figs. 19 and 20 (the large skewed workload,
@@ -538,7 +539,8 @@ def partition_sweep(args, pa, w, out, dist, rank):
     event-density-aware per-gate windows against globally fixed windows, on the
     same (gate, window) thread kernel. One JSON line per setting."""
     import torch
-    settings = [dict(partition="density", n_evt_tgt=args.n_evt_tgt, n_thr_floor=args.n_thr_floor)]
+    settings = [dict(partition="density", n_evt_tgt=args.n_evt_tgt, n_thr_floor=f)
+                for f in sorted({args.n_thr_floor, 16, 256})]
     settings += [dict(partition="fixed", n_cyc_fix=n) for n in (2, 4, 8, 16, 32)]
     # the library's own event-count partition beside them: event-count tiles of
     # the per-pin arrays (unbanded kernel), then the cycle-banded layout
