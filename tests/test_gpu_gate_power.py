@@ -70,6 +70,9 @@ def test_gate_power_standard_configs(glp, cfg, banded, bc):
     assert_gate_parity(r["gate_power"], o["gate_power"])
     assert_sums(r)
     assert_parity(r, o, debug=False)
+    # the paper's spatial accuracy measures, against the oracle's gate power
+    assert glp.hotspot_overlap(r["gate_power"], o["gate_power"], 0.01) >= 0.99
+    assert glp.rank_correlation(r["gate_power"], o["gate_power"]) >= 0.999
 
 
 @pytest.mark.parametrize("banded", [False, True])
