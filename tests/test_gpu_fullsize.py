@@ -1,6 +1,7 @@
 """Full-size parity on the large configurations (200M, 1B and 2B events), in
 the launch configuration the benchmark times (the banded layout, and the
-unbanded kernel alongside).
+unbanded kernel alongside), for the per-event-output variant of the kernels and
+for the timed variant the benchmark runs.
 
 At these sizes the oracle cannot afford its full per-cycle leakage split over
 every gate, so it checks what it can compute one by one:
@@ -56,21 +57,24 @@ def test_full_size_config(glp, cfg, banded):
         if banded:
             pa.build_bands(w.t_clk_ns)
         r = pa.run(w.vdd, w.t_clk_ns, N, debug=True, timing=True)
-    assert r["path"] == (glp.PA_PATH_BANDED if banded else glp.PA_PATH_UNBANDED)
+        fast = pa.run(w.vdd, w.t_clk_ns, N, timing=True)  # the timed kernel variant (no per-event outputs)
+    assert r["path"] == fast["path"] == (glp.PA_PATH_BANDED if banded else glp.PA_PATH_UNBANDED)
     assert r["n_heavy"] > 0 and r["n_tiles"] > 0
-    # totals, counts and sampled cycles over all gates
+    # totals, counts and sampled cycles over all gates, for both variants
     rng = np.random.default_rng(cfg)
     peak_c = int(np.argmax(r["waveform"]))
-    cyc = np.unique(np.concatenate([[0, N - 1, peak_c], rng.choice(N, 61, replace=False)])).astype(np.uint32)
+    cyc = np.unique(np.concatenate([[0, N - 1, peak_c, int(np.argmax(fast["waveform"]))],
+                                    rng.choice(N, 61, replace=False)])).astype(np.uint32)
     o = oracle.run(w, wave="sample", sample_cycles=cyc, threads=threads)
-    for key in ("p_int", "p_sw", "p_gl", "p_leak"):
-        assert abs(r[key] - o[key]) <= TOL_P * abs(o[key]), (key, r[key], o[key])
-    np.testing.assert_array_equal(r["event_count"].astype(np.uint64), o["evcount"])
-    np.testing.assert_array_equal(r["glitch_count"].astype(np.uint64), o["glcount"])
     assert int(o["evcount"].sum()) == E
     peak = float(np.abs(o["waveform"]).max())
-    err = np.abs(r["waveform"][cyc].astype(np.float64) - o["waveform"])
-    assert float(err.max()) <= TOL_W * peak, (float(err.max()), peak)
+    for res in (r, fast):
+        for key in ("p_int", "p_sw", "p_gl", "p_leak"):
+            assert abs(res[key] - o[key]) <= TOL_P * abs(o[key]), (key, res[key], o[key])
+        np.testing.assert_array_equal(res["event_count"].astype(np.uint64), o["evcount"])
+        np.testing.assert_array_equal(res["glitch_count"].astype(np.uint64), o["glcount"])
+        err = np.abs(res["waveform"][cyc].astype(np.float64) - o["waveform"])
+        assert float(err.max()) <= TOL_W * peak, (float(err.max()), peak)
     # per-event outputs on sampled gate blocks, heaviest gates included
     pb = w.pin_base().astype(np.int64)
     n_g = np.diff(w.pin_off.astype(np.int64)[pb])
