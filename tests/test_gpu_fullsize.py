@@ -47,7 +47,7 @@ def sub_workload(w, pb, g0, g1):
     return s, e0, e1
 
 
-@pytest.mark.parametrize("cfg,banded", [(3, False), (3, True), (4, False), (4, True), (5, True)])
+@pytest.mark.parametrize("cfg,banded", [(3, False), (3, True), (4, False), (4, True), (5, True), (6, True)])
 def test_full_size_config(glp, cfg, banded):
     threads = os.cpu_count() or 8
     w = synth.generate(cfg)
@@ -80,8 +80,9 @@ def test_full_size_config(glp, cfg, banded):
     n_g = np.diff(w.pin_off.astype(np.int64)[pb])
     heavy = np.argsort(n_g)[-12:]
     blocks = [(int(g), int(g) + 1) for g in heavy]
-    for b in rng.choice(G - 3000, 6, replace=False):
-        blocks.append((int(b), int(b) + 3000))
+    bs = max(1, min(3000, G // 8, int(2e6 * G / max(1, E))))  # blocks of about 2M events at most
+    for b in rng.choice(G - bs, 6, replace=False):
+        blocks.append((int(b), int(b) + bs))
     for g0, g1 in blocks:
         s, e0, e1 = sub_workload(w, pb, g0, g1)
         so = oracle.run(s, wave="none", debug=True)
