@@ -88,3 +88,26 @@ def test_full_size_config(glp, cfg, banded):
         so = oracle.run(s, wave="none", debug=True)
         for key in ("state_pre", "lut_ij", "is_glitch"):
             np.testing.assert_array_equal(r[key][e0:e1], so[key], err_msg=f"{key} gates [{g0}, {g1})")
+
+
+@pytest.mark.parametrize("partition,knobs", [("density", {}), ("fixed", {"n_cyc_fix": 32})])
+def test_full_size_paper_partition(glp, partition, knobs):
+    # the paper's (gate, window) thread partition on the large skewed workload
+    # (config 3: 26M threads at density, 313M at 32 cycles per thread)
+    threads = os.cpu_count() or 8
+    w = synth.generate(3)
+    N = w.n_cycles
+    with glp.PowerAnalyzer(0) as pa:
+        pa.load_workload(w)
+        r = pa.run(w.vdd, w.t_clk_ns, N, partition=partition, **knobs)
+    assert r["path"] == glp.PA_PATH_WINDOWS
+    rng = np.random.default_rng(7)
+    cyc = np.unique(np.concatenate([[0, N - 1, int(np.argmax(r["waveform"]))],
+                                    rng.choice(N, 61, replace=False)])).astype(np.uint32)
+    o = oracle.run(w, wave="sample", sample_cycles=cyc, threads=threads)
+    for key in ("p_int", "p_sw", "p_gl", "p_leak"):
+        assert abs(r[key] - o[key]) <= TOL_P * abs(o[key]), (key, r[key], o[key])
+    np.testing.assert_array_equal(r["event_count"].astype(np.uint64), o["evcount"])
+    np.testing.assert_array_equal(r["glitch_count"].astype(np.uint64), o["glcount"])
+    peak = float(np.abs(o["waveform"]).max())
+    assert float(np.abs(r["waveform"][cyc].astype(np.float64) - o["waveform"]).max()) <= TOL_W * peak
