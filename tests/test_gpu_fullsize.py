@@ -111,3 +111,27 @@ def test_full_size_paper_partition(glp, partition, knobs):
     np.testing.assert_array_equal(r["glitch_count"].astype(np.uint64), o["glcount"])
     peak = float(np.abs(o["waveform"]).max())
     assert float(np.abs(r["waveform"][cyc].astype(np.float64) - o["waveform"]).max()) <= TOL_W * peak
+
+
+def test_full_size_streamed_run(glp):
+    # the one-shot path of the benchmark's e2e figure: the 1B-event trace kept
+    # in host memory, streamed through the device in chunks
+    threads = os.cpu_count() or 8
+    w = synth.generate(4)
+    N = w.n_cycles
+    with glp.PowerAnalyzer(0) as pa:
+        pa.load_library(w.n_inputs, w.n_slew, w.n_load, w.slew_axis, w.load_axis, w.lut_off, w.lut, w.leak_off,
+                        w.leak)
+        pa.load_netlist(w.cell_id, w.load_ff, w.init_in, w.init_out)
+        r = pa.run(w.vdd, w.t_clk_ns, N, stream=(w.pin_off, w.t_ns, w.slew_ps, w.value))
+    assert r["n_tiles"] > 1  # chunks
+    rng = np.random.default_rng(11)
+    cyc = np.unique(np.concatenate([[0, N - 1, int(np.argmax(r["waveform"]))],
+                                    rng.choice(N, 61, replace=False)])).astype(np.uint32)
+    o = oracle.run(w, wave="sample", sample_cycles=cyc, threads=threads)
+    for key in ("p_int", "p_sw", "p_gl", "p_leak"):
+        assert abs(r[key] - o[key]) <= TOL_P * abs(o[key]), (key, r[key], o[key])
+    np.testing.assert_array_equal(r["event_count"].astype(np.uint64), o["evcount"])
+    np.testing.assert_array_equal(r["glitch_count"].astype(np.uint64), o["glcount"])
+    peak = float(np.abs(o["waveform"]).max())
+    assert float(np.abs(r["waveform"][cyc].astype(np.float64) - o["waveform"]).max()) <= TOL_W * peak
