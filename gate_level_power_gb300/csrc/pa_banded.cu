@@ -953,12 +953,24 @@ __device__ __forceinline__ void bulk_red_add_f32(void* dst, const void* src, uin
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// A lane's running sums of its events' totals. The leakage term dP (t_max -
+// t) of an event is large (t_max - t up to the whole window) and of either
+// sign, and the terms of a gate's rising and falling steps almost cancel, so
+// its f32 sum is compensated (Kahan: c_lk holds the low-order part lost so
+// far) and the warp sums are taken in fp64.
 struct BAcc {
-  float e_int, e_sw, e_gl, e_lk;
+  float e_int, e_sw, e_gl, e_lk, c_lk;
 };
 
+__device__ __forceinline__ void kahan_add(float& sum, float& comp, float x) {
+  const float y = x - comp;
+  const float t = sum + y;
+  comp = (t - sum) - y;
+  sum = t;
+}
+
 __device__ __forceinline__ void bflush_acc(BAcc& acc, double* s_tot) {
-  float v[4] = {acc.e_int, acc.e_sw, acc.e_gl, acc.e_lk};
+  double v[4] = {acc.e_int, acc.e_sw, acc.e_gl, (double)acc.e_lk - (double)acc.c_lk};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
 #pragma unroll
@@ -966,9 +978,9 @@ __device__ __forceinline__ void bflush_acc(BAcc& acc, double* s_tot) {
   }
   if ((threadIdx.x & 31) == 0) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) atomicAdd(s_tot + i, (double)v[i]);
+    for (int i = 0; i < 4; ++i) atomicAdd(s_tot + i, v[i]);
   }
-  acc = BAcc{0.f, 0.f, 0.f, 0.f};
+  acc = BAcc{0.f, 0.f, 0.f, 0.f, 0.f};
 }
 
 // The band's bins in shared memory: four arrays of kBandMaxCycles words,
@@ -1242,7 +1254,7 @@ __device__ __forceinline__ EvOut ev_input(const RunArgs& a, const CellTab& CT, c
   if (valid) {
     acc.e_gl += glitch ? e_w : 0.f;
     acc.e_int += glitch ? 0.f : e_int;
-    acc.e_lk = fmaf(dp, a.t_max_f - t, acc.e_lk);
+    kahan_add(acc.e_lk, acc.c_lk, dp * (a.t_max_f - t));
   }
   if (kDebug)
     dbg = EvDbg{s_pre, (uint32_t)((lis << 4) | j), w & 63u, p, t, glitch, glitch ? 0.f : e_int, 0.f,
@@ -1562,7 +1574,7 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  BAcc acc{0.f, 0.f, 0.f, 0.f};
+  BAcc acc{0.f, 0.f, 0.f, 0.f, 0.f};
   int since = 0;
   uint32_t phase = 0;  // parity of the stage barrier's next completion
   bool bad = false;    // a stage copy never landed: this warp stops working

@@ -360,9 +360,19 @@ __device__ __forceinline__ uint32_t state_before(const float* ts, const Slot& S,
   return st;
 }
 
+// A thread's running sums of its events' totals; the leakage term dP (t_max -
+// t) is large and of either sign (a gate's steps almost cancel), so its sum is
+// compensated (Kahan, c_lk) and the warp sums are taken in fp64.
 struct Acc {
-  float e_int, e_sw, e_gl, e_lk;
+  float e_int, e_sw, e_gl, e_lk, c_lk;
 };
+
+__device__ __forceinline__ void kahan_add(float& sum, float& comp, float x) {
+  const float y = x - comp;
+  const float t = sum + y;
+  comp = (t - sum) - y;
+  sum = t;
+}
 
 template <bool kPow2, bool kDebug, bool kExact>
 __device__ __forceinline__ void do_event(const RunArgs& a, const float* __restrict__ ts,
@@ -445,7 +455,7 @@ __device__ __forceinline__ void do_event(const RunArgs& a, const float* __restri
   if (p < k) {
     const float rem = fmaf(-(float)c, a.t_clk, t);  // t - c T
     e_w = fmaf(dp, a.t_clk - rem, e_w);
-    acc.e_lk = fmaf(dp, a.t_max_f - t, acc.e_lk);
+    kahan_add(acc.e_lk, acc.c_lk, dp * (a.t_max_f - t));
   }
   if (kExact) {
     // dense cycles: fp64 energy and step sums, integer counts
@@ -500,15 +510,15 @@ __device__ __forceinline__ void fill_slot(const RunArgs& a, const CellDesc* cell
 }
 
 __device__ __forceinline__ void flush_acc(Acc& acc, double* s_tot) {
-  const float v0 = warp_sum_f32(acc.e_int), v1 = warp_sum_f32(acc.e_sw);
-  const float v2 = warp_sum_f32(acc.e_gl), v3 = warp_sum_f32(acc.e_lk);
+  const double v0 = warp_sum_f64(acc.e_int), v1 = warp_sum_f64(acc.e_sw);
+  const double v2 = warp_sum_f64(acc.e_gl), v3 = warp_sum_f64((double)acc.e_lk - (double)acc.c_lk);
   if ((threadIdx.x & 31) == 0) {
-    atomicAdd(s_tot + 0, (double)v0);
-    atomicAdd(s_tot + 1, (double)v1);
-    atomicAdd(s_tot + 2, (double)v2);
-    atomicAdd(s_tot + 3, (double)v3);
+    atomicAdd(s_tot + 0, v0);
+    atomicAdd(s_tot + 1, v1);
+    atomicAdd(s_tot + 2, v2);
+    atomicAdd(s_tot + 3, v3);
   }
-  acc = Acc{0.f, 0.f, 0.f, 0.f};
+  acc = Acc{0.f, 0.f, 0.f, 0.f, 0.f};
 }
 
 template <bool kPow2, bool kDebug, bool kExact>
@@ -536,7 +546,7 @@ __global__ void __launch_bounds__(kThreads) k_fused(const RunArgs a) {
   const CellDesc* cells = cells_in_smem ? cells_s : a.cells;
   const uint32_t n_tiles = a.part_counts[0], n_heavy = a.part_counts[1];
   const uint32_t n_items = n_tiles + n_heavy;
-  Acc acc{0.f, 0.f, 0.f, 0.f};
+  Acc acc{0.f, 0.f, 0.f, 0.f, 0.f};
   __syncthreads();
 
   for (;;) {

@@ -102,13 +102,21 @@ __global__ void __launch_bounds__(256) k_win_plan(const RunArgs a, const WinArgs
 
 struct WAcc {
   float f[4];   // E_int, E_sw, E_gl, sum dP (t_max - t): the current run of events
+  float c3;     // Kahan compensation of f[3] (large terms of either sign that nearly cancel)
   double d[4];  // folded sums
+  __device__ __forceinline__ void add_lk(float x) {
+    const float y = x - c3;
+    const float t = f[3] + y;
+    c3 = (t - f[3]) - y;
+    f[3] = t;
+  }
   __device__ __forceinline__ void fold() {
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      d[m] += (double)f[m];
-      f[m] = 0.f;
-    }
+    for (int m = 0; m < 4; ++m) d[m] += (double)f[m];
+    d[3] -= (double)c3;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) f[m] = 0.f;
+    c3 = 0.f;
   }
 };
 
@@ -240,7 +248,7 @@ __device__ __forceinline__ uint32_t win_thread(const RunArgs& a, const WinArgs& 
     if (p < k) {
       const float rem = fmaf(-(float)c, T, t);  // t - c T: the step's part inside its own cycle
       e_w = fmaf(dp, T - rem, e_w);
-      acc.f[3] = fmaf(dp, a.t_max_f - t, acc.f[3]);
+      acc.add_lk(dp * (a.t_max_f - t));
       if (kDebug) ge[3] += (double)(dp * (a.t_max_f - t));
     }
     if (kExact) {
@@ -297,6 +305,7 @@ __global__ void __launch_bounds__(kWT, 3) k_window(const RunArgs a, const WinArg
   const uint64_t total = w.thr_off[G];
   const uint64_t n_chunks = (total + kWT - 1) / kWT;  // CTAs take chunks of kWT thread ids, grid-strided
   WAcc acc;
+  acc.c3 = 0.f;
 #pragma unroll
   for (int m = 0; m < 4; ++m) {
     acc.f[m] = 0.f;

@@ -47,7 +47,7 @@ def sub_workload(w, pb, g0, g1):
     return s, e0, e1
 
 
-@pytest.mark.parametrize("cfg,banded", [(3, False), (3, True), (4, False), (4, True), (5, True), (6, True)])
+@pytest.mark.parametrize("cfg,banded", [(3, False), (3, True), (4, False), (4, True), (5, True), (6, False), (6, True)])
 def test_full_size_config(glp, cfg, banded):
     threads = os.cpu_count() or 8
     w = synth.generate(cfg)
@@ -59,7 +59,8 @@ def test_full_size_config(glp, cfg, banded):
         r = pa.run(w.vdd, w.t_clk_ns, N, debug=True, timing=True)
         fast = pa.run(w.vdd, w.t_clk_ns, N, timing=True)  # the timed kernel variant (no per-event outputs)
     assert r["path"] == fast["path"] == (glp.PA_PATH_BANDED if banded else glp.PA_PATH_UNBANDED)
-    assert r["n_heavy"] > 0 and r["n_tiles"] > 0
+    assert r["n_heavy"] > 0
+    assert r["n_tiles"] > 0 or (cfg == 6 and not banded)  # config 6's gates are all heavy for the unbanded kernel
     # totals, counts and sampled cycles over all gates, for both variants
     rng = np.random.default_rng(cfg)
     peak_c = int(np.argmax(r["waveform"]))
