@@ -2,13 +2,23 @@
 
 One step = one pass of the whole hot path over the loaded workload: event-count
 partition -> fused dynamic + leakage power kernel -> final reduction (one
-``pa_run``). Default workload: the very large skewed configuration (5M gates,
-64 cells with 1-4 inputs and 8x8 LUTs, 100k cycles at 1 ns, 1B events with
+``pa_run`` on the loaded per-pin layout; nothing is prepared for it outside the
+step). Default workload: the very large skewed configuration (5M gates, 64
+cells with 1-4 inputs and 8x8 LUTs, 100k cycles at 1 ns, 1B events with
 Zipf(1.1) gate activity), seeded synthetic inputs.
 
 Printed (rank 0, one JSON line):
   value    events/s over all ranks, inputs resident in HBM, timed with CUDA
-           events on the library's stream, max over ranks
+           events on the library's stream over the timed steps (after a
+           warm-up of at least --warmup steps and --warmup-seconds), max over
+           ranks; the median step beside it
+  roofline the fused kernel's algorithmic bytes per launch / its mean duration
+           (CUDA events recorded on its stream inside pa_run) against the
+           measured HBM copy bandwidth; the median and the whole pass beside it
+  banded_layout  the cycle-banded layout beside the timed pass: its build time
+           (pa_build_bands, once per trace and clock) and runs on it (the
+           re-run figure of a trace analysed at several voltages or window
+           ends), reported, not the value
   e2e      same metric through the public API with host buffers: per step the
            events are copied from pinned host memory (pa_load_events, with
            device-side validation), the pass runs, and the waveform and counts
@@ -16,14 +26,15 @@ Printed (rank 0, one JSON line):
            the device (pa_run_stream), or loads it and runs the unbanded kernel,
            or loads it and builds the banded layout first: all are timed and the
            fastest is the value
-  roofline the fused kernel's algorithmic bytes per launch / its mean duration
-           (CUDA events recorded on its stream inside pa_run) against the
-           measured HBM copy bandwidth
+  clocks   nvidia-smi samples from the start of the warm-up to the end of the
+           timed region
   cpu_baseline  the fp64 oracle timed on this host's cores on a bounded gate
            sample of the same workload
 
-``--impl reference`` times the oracle alone (rank 0), on the same workload and
-metric.
+``--path banded-rerun`` times pa_run on a layout built before the timed region
+instead (labelled as a re-run figure). ``--impl reference`` times the oracle
+alone (rank 0), on the same workload and metric. ``--oracle-single`` times the
+oracle on one host thread on configs 1..3.
 
 ``--partition density|fixed`` times the paper's (gate, window) thread partition
 instead (one thread per gate window, a global atomic per event);
@@ -72,8 +83,15 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle sample time")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--unbanded", action="store_true",
-                    help="skip the cycle-banded layout (pa_build_bands) and time the unbanded kernel")
+    ap.add_argument("--path", choices=["pass", "banded-rerun"], default="pass",
+                    help="pass (default): every timed step is a whole pa_run on the loaded per-pin layout "
+                         "(partition + fused kernel + final reduction); banded-rerun: pa_run on a cycle-banded "
+                         "layout built before the timed region (a re-run figure)")
+    ap.add_argument("--no-banded", action="store_true",
+                    help="skip the banded layout's build / re-run figures and its e2e path")
+    ap.add_argument("--warmup-seconds", type=float, default=1.0, help="minimum warm-up time")
+    ap.add_argument("--oracle-single", action="store_true",
+                    help="time the oracle on one host thread on configs 1..3 (bounded samples) and exit")
     ap.add_argument("--band-cycles", type=int, default=0, help="cycles per band (0 = library default)")
     ap.add_argument("--partition", choices=["events", "density", "fixed"], default="events",
                     help="work partition: the library's event-count partition (default) or the paper's "
@@ -393,10 +411,10 @@ def run_ours(args):
     stream = torch.cuda.Stream(device=local)
     pa = glp.PowerAnalyzer(local, stream.cuda_stream)
     pa.load_workload(w)
-    build_ms = None
     windows = args.partition != "events" or args.partition_sweep
-    banded = not args.unbanded and not windows
-    if banded:
+    rerun = args.path == "banded-rerun" and not windows
+    build_ms = None
+    if rerun:  # a re-run figure: the layout is built before the timed region (reported as such)
         t0 = time.perf_counter()
         pa.build_bands(w.t_clk_ns, args.band_cycles)
         build_ms = (time.perf_counter() - t0) * 1e3
@@ -414,23 +432,31 @@ def run_ours(args):
     if args.partition_sweep:
         return partition_sweep(args, pa, w, out, dist, rank)
 
-    for _ in range(max(3, args.warmup)):
-        step()
+    # clocks are sampled from the start of the warm-up to the end of the
+    # device-resident timed region
     clk = ClockSampler(local)
     clk.start()
     time.sleep(0.3)
+    clk.active = True
+    # warm-up: at least --warmup steps (3 at least) and at least --warmup-seconds
+    t0 = time.perf_counter()
+    n_warm = 0
+    while n_warm < max(3, args.warmup) or time.perf_counter() - t0 < args.warmup_seconds:
+        step()
+        n_warm += 1
+    warm_s = time.perf_counter() - t0
     # ---- device-resident timed region
     dist.barrier()
     torch.cuda.synchronize()
-    clk.active = True
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    fused_ms = []
+    fused_ms, pass_ms = [], []
     launches = 0
     for _ in range(args.steps):
         r = step(timing=True)
         fused_ms.append(r["ms_fused"])
+        pass_ms.append(r["ms_total"])
         launches += r["kernel_launches"]
     e1.record(stream)
     torch.cuda.synchronize()
@@ -438,11 +464,36 @@ def run_ours(args):
     el_ms = e0.elapsed_time(e1)
     el_ms = dist.max(el_ms)
     value = world * E * args.steps / (el_ms * 1e-3)
-    # the clocks are sampled over the device-resident timed region only: a
-    # running nvidia-smi poller measurably slows host-to-device copies (some
-    # 8 GB copies took 55-67 ms instead of 38 ms while it ran)
+    med_pass = dist.max(statistics.median(pass_ms))
+    # a running nvidia-smi poller measurably slows host-to-device copies (some
+    # 8 GB copies took 55-67 ms instead of 38 ms while it ran): stop it before
+    # the end-to-end runs
     clk.active = False
     clk.stop()
+    B = algorithmic_bytes(w)
+    peak, peak_kind = hbm_peak()
+    # ---- the cycle-banded layout beside the timed pass: its build, then runs
+    # on it (the re-run figure of a trace analysed at several voltages or
+    # window ends); reported, not the value
+    banded = None
+    if not windows and not rerun and not args.no_banded:
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        pa.build_bands(w.t_clk_ns, args.band_cycles)
+        torch.cuda.synchronize()
+        b_ms = (time.perf_counter() - t0) * 1e3
+        for _ in range(3):
+            step()
+        rr = [step(timing=True) for _ in range(max(10, min(args.steps, 50)))]
+        k_ms = statistics.median(x["ms_fused"] for x in rr)
+        run_ms = statistics.median(x["ms_total"] for x in rr)
+        banded = {"path": "banded" if rr[-1]["path"] == glp.PA_PATH_BANDED else "unbanded",
+                  "build_ms": b_ms, "rerun_ms_median": run_ms, "k_band_ms_median": k_ms,
+                  "rerun_events_per_s": E / (run_ms * 1e-3),
+                  "build_plus_run_events_per_s": E / ((b_ms + run_ms) * 1e-3),
+                  "rerun_roofline_frac": B / (k_ms * 1e-3) / 1e9 / peak,
+                  "note": "pa_build_bands (layout build, once per trace and clock) then pa_run on the layout; "
+                          "steps = " + str(len(rr))}
     # ---- end to end through the public API, host buffers
     h2d = 8 * (w.n_pins + 1) + 4 * E + 4 * E + E
     d2h = 4 * N + 4 * N + 4 * N + 4 * 8
@@ -452,9 +503,10 @@ def run_ours(args):
     if args.e2e_steps > 0:
         # A one-shot run through the public API: load the step's events from
         # pinned host memory and run, either straight on the loaded per-pin
-        # layout (unbanded kernel) or after building the cycle-banded layout.
-        # Both are timed; the faster is the headline (a user running a trace
-        # once takes it), the other is reported beside it.
+        # layout (unbanded kernel) or after building the cycle-banded layout,
+        # or stream the trace through the device. All are timed; the fastest
+        # is the headline (a user running a trace once takes it), the others
+        # are reported beside it.
         def e2e_step(path):
             if path == "stream_run":  # pa_run_stream: chunk copies overlapping the computation
                 pa.run(w.vdd, w.t_clk_ns, N, out=out, stream=(w.pin_off, w.t_ns, w.slew_ps, w.value))
@@ -464,7 +516,7 @@ def run_ours(args):
                 pa.build_bands(w.t_clk_ns, args.band_cycles)
             step()
         paths = (["load_run_windows"] if windows
-                 else ["stream_run", "load_run_unbanded"] + (["load_build_bands_run"] if banded else []))
+                 else ["stream_run", "load_run_unbanded"] + ([] if args.no_banded else ["load_build_bands_run"]))
         for path in paths:
             for _ in range(2):
                 e2e_step(path)
@@ -481,10 +533,9 @@ def run_ours(args):
             e2e_paths[path] = world * E * args.e2e_steps / e2e_s
             e2e_step_ms[path] = step_ms
         e2e_value = max(e2e_paths.values())
-    # ---- roofline of the fused kernel
+    # ---- roofline of the fused kernel of the timed pass
     fused_mean = statistics.mean(fused_ms)
-    B = algorithmic_bytes(w)
-    peak, peak_kind = hbm_peak()
+    fused_med = statistics.median(fused_ms)
     achieved = B / (fused_mean * 1e-3) / 1e9
     kname = {glp.PA_PATH_BANDED: "k_band", glp.PA_PATH_WINDOWS: "k_window"}.get(r["path"], "k_fused")
     traffic = None if args.synth else ncu_traffic(kname, args.config)
@@ -492,12 +543,22 @@ def run_ours(args):
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args.config, args.seed, args.cpu_seconds, E, G, **over)
     if rank == 0:
+        step_what = ("pa_run on a cycle-banded layout built before the timed region (re-run figure; the "
+                     "layout build is not timed)" if rerun else
+                     "pa_run on the loaded per-pin layout: the paper's partition (k_win_plan) + k_window + final "
+                     "reduction" if windows else
+                     "pa_run on the loaded per-pin layout: event-count partition (k_part_*) + fused kernel "
+                     "(k_fused) + final reduction, every step")
         line = {
             "metric": METRIC, "value": value, "unit": "events/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": el_ms / args.steps, "higher_is_better": True,
+            "warmup": n_warm, "ms_per_step": el_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": dict(workload_config(args.config, G, E, cfg),
                            **({"modified": " ".join(args.synth)} if args.synth else {})),
+            "step": step_what,
+            "ms_per_step_median": med_pass,
+            "value_at_median_step": world * E / (med_pass * 1e-3),
+            "warmup_seconds": warm_s,
             "gate_cycles_per_s": world * G * N * args.steps / (el_ms * 1e-3),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
@@ -506,8 +567,12 @@ def run_ours(args):
                             else ", the paper's (gate, window) threads)" if r["path"] == glp.PA_PATH_WINDOWS
                             else ")"),
                          "algorithmic_bytes_per_launch": B, "mean_launch_ms": fused_mean,
+                         "median_launch_ms": fused_med,
+                         "frac_at_median_launch": B / (fused_med * 1e-3) / 1e9 / peak,
+                         "pass_frac": B / (statistics.mean(pass_ms) * 1e-3) / 1e9 / peak,
                          "peak_source": f"{peak_kind} HBM copy bandwidth"},
             "cpu_baseline": cpu,
+            "banded_layout": banded,
             "e2e": None if e2e_value is None else {"value": e2e_value, "unit": "events/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": args.e2e_steps, "paths": e2e_paths,
                     "step_ms": e2e_step_ms,
@@ -531,6 +596,33 @@ def run_ours(args):
     pa.close()
     dist.close()
     del keep
+    return 0
+
+
+def oracle_single(args):
+    """The oracle on one host thread, on a bounded gate sample of each of
+    configs 1..3 (grown until one run takes about --cpu-seconds): one JSON
+    line per configuration, events/s and gate-cycles/s of the sample."""
+    import oracle
+    import synth
+    for config in (1, 2, 3):
+        G, _, E = synth.sizes(config, args.seed)
+        cfg = synth.make_cfg(config, args.seed)
+        g0 = 0 if G <= 2000 else G // 3
+        n = min(G, 2000)
+        while True:
+            w = synth.generate_range(config, g0, min(G, g0 + n), seed=args.seed)
+            t0 = time.perf_counter()
+            oracle.run(w, threads=1)
+            el = time.perf_counter() - t0
+            if el >= 0.5 * args.cpu_seconds or g0 + n >= G:
+                break
+            n = int(min(G - g0, max(2 * n, n * min(args.cpu_seconds / max(el, 1e-3), 50))))
+        print(json.dumps({"metric": "oracle events/s, one host thread", "config": config,
+                          "value": w.n_events / el, "unit": "events/s",
+                          "gate_cycles_per_s": w.n_gates * int(cfg.n_cycles) / el, "threads": 1,
+                          "sample": f"fp64 oracle, full waveform, gates [{g0}, {g0 + w.n_gates}) of {G} "
+                                    f"({w.n_events} of {E} events), {el:.2f} s"}), flush=True)
     return 0
 
 
@@ -578,6 +670,8 @@ def partition_sweep(args, pa, w, out, dist, rank):
 
 def main():
     args = parse_args()
+    if args.oracle_single:
+        return oracle_single(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -8,7 +8,6 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
-#include <mutex>
 #include <string>
 #include <vector>
 
@@ -32,6 +31,9 @@ struct pa_ctx {
   int sm_count = 0;
   std::string err;
   long alloc_fail_at = -1;  // test hook: the n-th device allocation fails (PA_TEST_FAIL_ALLOC)
+  // test hook (PA_TEST_STAGE_TIMEOUT=i): the banded kernel never starts the
+  // stage copy of item i and its bounded waits give up after a few ms
+  uint32_t test_skip_item = kNoItem;
   long alloc_count = 0;
   cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
 
@@ -70,6 +72,12 @@ struct pa_ctx {
       b_urec2, b_dense, b_gflag;
   DevBuf b_part;
   DevBuf scratch_small;
+
+  // pa_run_noalloc's scratch: the device address of the library's file-scope
+  // array on this ctx's device, looked up by pa_create (null if that failed,
+  // with the reason kept for pa_run_noalloc to report)
+  unsigned char* noalloc_base = nullptr;
+  std::string noalloc_err;
 
   // pa_run_stream: two staging slots per chunk array, a copy stream and its events
   cudaStream_t copy_stream = nullptr;
@@ -152,6 +160,8 @@ const char* err_code_name(uint32_t code) {
     case kErrToggle: return "event value equals the pin's previous value";
     case kErrValue: return "event value not 0/1";
     case kErrTileOverflow: return "work item exceeds its shared-memory tile";
+    case kErrLayout: return "banded layout inconsistent";
+    case kErrStageTimeout: return "stage wait timed out (a bounded wait for a shared-memory stage copy gave up)";
     default: return "unknown";
   }
 }
@@ -169,7 +179,10 @@ int map_dev_err(pa_ctx* c, unsigned long long key, const char* what) {
     case kErrValue: rc = PA_ERR_TOGGLE; break;
     default: rc = PA_ERR_INTERNAL; break;
   }
-  const char* unit = code == kErrPinOff ? "pin" : (code == kErrTileOverflow ? "gate" : "event");
+  const char* unit = code == kErrPinOff            ? "pin"
+                     : code == kErrTileOverflow     ? "gate"
+                     : code == kErrLayout || code == kErrStageTimeout ? "item"
+                                                    : "event";
   return fail(c, rc, "%s: %s (first at %s %llu)", what, err_code_name(code), unit, idx);
 }
 
@@ -359,6 +372,8 @@ int run_pass(pa_ctx* c, const RunPlan& plan, const PassBufs& B, pa_result* out, 
     A.r = a;
     A.L = *band;
     A.item_ctr = B.part_counts + 4;  // part_counts[2] is the unbanded kernel's item counter
+    A.skip_item = c->test_skip_item;
+    A.wait_limit = c->test_skip_item == kNoItem ? kBandWaitLimit : kBandTestWaitLimit;
   }
   cudaStream_t st = c->stream;
   uint32_t launches = 0;
@@ -719,6 +734,10 @@ int run_stream(pa_ctx* c, const RunPlan& plan, const pa_events* ev, uint64_t tar
 
 bool same_bits(float a, float b) { return std::memcmp(&a, &b, sizeof(float)) == 0; }
 
+// Looks up the device address of pa_run_noalloc's scratch array on the
+// current device (defined with the array, below).
+void noalloc_lookup(pa_ctx* c);
+
 }  // namespace
 
 extern "C" {
@@ -748,6 +767,7 @@ int pa_create(pa_ctx** out, int cuda_device, void* cuda_stream) {
   if (!c) return PA_ERR_OOM;
   c->device = cuda_device;
   if (const char* f = std::getenv("PA_TEST_FAIL_ALLOC")) c->alloc_fail_at = std::atol(f);
+  if (const char* f = std::getenv("PA_TEST_STAGE_TIMEOUT")) c->test_skip_item = (uint32_t)std::strtoul(f, nullptr, 10);
   if (cudaSetDevice(cuda_device) != cudaSuccess ||
       cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, cuda_device) != cudaSuccess) {
     cudaGetLastError();
@@ -771,6 +791,7 @@ int pa_create(pa_ctx** out, int cuda_device, void* cuda_stream) {
       return PA_ERR_CUDA;
     }
   }
+  noalloc_lookup(c);
   *out = c;
   return PA_OK;
 }
@@ -1075,6 +1096,8 @@ int pa_run_stream(pa_ctx* c, const pa_run_params* prm, const pa_events* ev, uint
 // counters, tiles and heavy-gate lists for PA_NOALLOC_MAX_GATES gates, P0 and
 // totals (8 doubles), the four result powers, the final reduction's chunk
 // sums, and staging for the waveform and the two count arrays.
+// pa_create resolves the array's address (noalloc_lookup) and keeps it in the
+// context; pa_run_noalloc only reads it.
 
 namespace {
 
@@ -1099,26 +1122,22 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[PA_NOALLOC_SCRA
 
 namespace {
 
-constexpr int kNaMaxDevices = 64;
-std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[kNaMaxDevices] = {};
-
-// Device address of g_noalloc_scratch on the current device `dev` (looked up
-// once per device).
-int noalloc_scratch(pa_ctx* c, int dev, unsigned char** out) {
-  if (dev < 0 || dev >= kNaMaxDevices) return fail(c, PA_ERR_ARG, "pa_run_noalloc: device ordinal %d too large", dev);
-  std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess || !p) {
-      cudaGetLastError();
-      return fail(c, PA_ERR_CUDA, "pa_run_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
-    }
-    g_noalloc_ptr[dev] = p;
+// The array's device address on the current device. Under lazy module loading
+// this lookup is what loads the module holding the array, so the 5 MiB are
+// committed here, once per context at pa_create, and never inside
+// pa_run_noalloc. A failure is kept and reported by pa_run_noalloc: the
+// other entry points do not need the array.
+void noalloc_lookup(pa_ctx* c) {
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess || !p) {
+    cudaGetLastError();
+    c->noalloc_base = nullptr;
+    c->noalloc_err = std::string("cudaGetSymbolAddress of the scratch array at pa_create: ") +
+                     (e != cudaSuccess ? cudaGetErrorString(e) : "null address");
+    return;
   }
-  *out = (unsigned char*)g_noalloc_ptr[dev];
-  return PA_OK;
+  c->noalloc_base = (unsigned char*)p;
 }
 
 }  // namespace
@@ -1138,9 +1157,11 @@ extern "C" int pa_run_noalloc(pa_ctx* c, const pa_run_params* prm, pa_result* ou
                          out->lut_ij || out->is_glitch || out->gate_power_w || out->cell_power_w;
   if (any_array && out->out_mem != PA_MEM_DEVICE)
     return fail(c, PA_ERR_ARG, "pa_run_noalloc: output arrays must be device memory (out_mem = PA_MEM_DEVICE)");
+  if (out->cell_power_w && !out->gate_power_w)
+    return fail(c, PA_ERR_ARG, "pa_run_noalloc: cell_power_w needs gate_power_w (the per-gate accumulators)");
+  unsigned char* base = c->noalloc_base;
+  if (!base) return fail(c, PA_ERR_CUDA, "pa_run_noalloc: %s", c->noalloc_err.c_str());
   CUDA_TRY(c, cudaSetDevice(c->device));
-  unsigned char* base = nullptr;
-  PA_TRY(noalloc_scratch(c, c->device, &base));
   PassBufs B;
   B.bins = (float4*)(base + kNaBins);
   B.part_blk = (uint32_t*)(base + kNaPartBlk);
@@ -1157,8 +1178,6 @@ extern "C" int pa_run_noalloc(pa_ctx* c, const pa_run_params* prm, pa_result* ou
   B.dbg[0] = out->state_pre;
   B.dbg[1] = out->lut_ij;
   B.dbg[2] = out->is_glitch;
-  if (out->cell_power_w && !out->gate_power_w)
-    return fail(c, PA_ERR_ARG, "pa_run_noalloc: cell_power_w needs gate_power_w (the per-gate accumulators)");
   B.gate_e = out->gate_power_w;  // accumulated in place
   B.cell_p = out->cell_power_w;
   return run_pass(c, plan, B, out, "pa_run_noalloc", nullptr);
@@ -1314,10 +1333,12 @@ extern "C" int pa_build_bands(pa_ctx* c, float t_clk, uint32_t band_cycles) {
   const uint32_t cb = band_cycles ? band_cycles : kBandDefaultCycles;
   if (cb > kBandMaxCycles || (cb & (cb - 1)) != 0)
     return fail(c, PA_ERR_ARG, "pa_build_bands: band_cycles %u is not a power of two <= %u", cb, kBandMaxCycles);
-  if (c->n_cells > (uint32_t)kSmemCells)
-    return fail(c, PA_ERR_ARG, "pa_build_bands: %u cells; the banded kernel holds at most %d", c->n_cells, kSmemCells);
   CUDA_TRY(c, cudaSetDevice(c->device));
   c->band.built = false;
+  // The banded kernel stages the cell tables of at most kSmemCells cells in
+  // shared memory; with a larger library no layout is built and runs at this
+  // clock take the unbanded path (pa_result.path says which ran).
+  if (c->n_cells > (uint32_t)kSmemCells) return PA_OK;
   const int rc = build_bands(c, t_clk, cb);
   free_build_temps(c);
   return rc;

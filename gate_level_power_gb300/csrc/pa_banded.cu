@@ -620,7 +620,7 @@ __global__ void __launch_bounds__(kFinWarps * 32) k_bw_finalize(const BandBuildA
     const uint64_t e0 = L.items[it].e0, e1 = L.items[it + 1].e0;
     const uint32_t u0 = L.items[it].u0, u1 = L.items[it + 1].u0;
     if (e1 <= e0 || e1 - e0 >= (uint64_t)kItemEvents || u1 <= u0 || u1 - u0 > (uint32_t)kItemUnits) {
-      if (lane == 0) atomicMin(a.err, (unsigned long long)((it << 8) | kErrTileOverflow));
+      if (lane == 0) atomicMin(a.err, (unsigned long long)((it << 8) | kErrLayout));
       continue;
     }
     const int n = (int)(e1 - e0), nu = (int)(u1 - u0);
@@ -661,7 +661,7 @@ __global__ void __launch_bounds__(kFinWarps * 32) k_bw_finalize(const BandBuildA
     __syncwarp();
     const uint32_t n_in_all = (carry >> 10) & 1023u;
     if ((carry & 1023u) != (uint32_t)n || n_in_all + ((carry >> 20) & 1023u) != (uint32_t)n) {
-      if (lane == 0) atomicMin(a.err, (unsigned long long)((it << 8) | kErrTileOverflow));
+      if (lane == 0) atomicMin(a.err, (unsigned long long)((it << 8) | kErrLayout));
       continue;
     }
     for (int i = lane; i < n; i += 32) sb[wl][i] = L.bt[e0 + i];  // times in the walk's order
@@ -906,7 +906,6 @@ constexpr int kTotEvery = 16;              // items between flushes of a warp's 
 // small ones a shorter tail; item costs vary with the gate class, so chunks
 // that shrink over the run would leave the early, big ones unbalanced).
 constexpr uint32_t kChunkMin = 64, kChunkMax = kChunkMaxItems;
-constexpr uint32_t kWaitLimit = 1u << 16;  // bounded mbarrier waits before giving up (seconds in all)
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -1195,7 +1194,8 @@ __device__ __forceinline__ float glitch_scale(const RunArgs& a, const float* ts,
       sp = __ldg(gs + en);
     }
   }
-  const float r = fminf(1.f, __fdividef(2000.f * pw, s + sp));
+  // IEEE division, as in the unbanded kernel: both kernels give one event the same r_gl
+  const float r = fminf(1.f, __fdiv_rn(2000.f * pw, s + sp));
   return glitch ? r * e_dyn : e_dyn;
 }
 
@@ -1310,7 +1310,7 @@ __device__ __forceinline__ void ev_commit(const BandRunArgs& A, float* hist, con
   const RunArgs& a = A.r;
   const uint32_t lc = o.c - c0;
   if (lc >= A.L.band_cycles) {  // an event outside its band: layout inconsistency
-    berr(a.err, item, kErrTileOverflow);
+    berr(a.err, item, kErrLayout);
     return;
   }
   const bool input = (o.flags & 1u) != 0u, glitch = (o.flags & 2u) != 0u;
@@ -1339,7 +1339,7 @@ __device__ __forceinline__ void ev_commit_runs(const BandRunArgs& A, float* hist
                                                uint32_t item, uint32_t c0, int lane) {
   uint32_t lc = o.c - c0;
   if (valid && lc >= A.L.band_cycles) {  // an event outside its band: layout inconsistency
-    berr(A.r.err, item, kErrTileOverflow);
+    berr(A.r.err, item, kErrLayout);
     valid = false;
   }
   if (!valid) lc = 0xFFFFFFFFu;  // lanes without an event come last and form runs of their own
@@ -1393,7 +1393,7 @@ __device__ void event_debug(const RunArgs& a, uint32_t gate, int p, float t, uin
     if (a.dbg_lut) a.dbg_lut[l] = (uint8_t)lut_ij;
     if (a.dbg_glitch) a.dbg_glitch[l] = (uint8_t)glitch;
   } else {
-    berr(a.err, item, kErrTileOverflow);
+    berr(a.err, item, kErrLayout);
   }
 }
 
@@ -1408,7 +1408,7 @@ __device__ __forceinline__ void band_item(const BandRunArgs& A, const CellTab& C
   const RunArgs& a = A.r;
   const int lane = threadIdx.x & 31;
   if (!g.ok) {
-    if (lane == 0) berr(a.err, item, kErrTileOverflow);
+    if (lane == 0) berr(a.err, item, kErrLayout);
     return;
   }
   const float* ts = reinterpret_cast<const float*>(stage) + g.ev_off;
@@ -1607,11 +1607,11 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
     const BandItem* it = s_items + ibuf * (kChunkMaxItems + 1);  // records of items c_lo .. c_hi
     if (tid == 0) {
       bool ok = false;
-      for (uint32_t w = 0; w < kWaitLimit && !ok; ++w) ok = mbar_try_wait(&s_ibar[ibuf], (iphase >> ibuf) & 1u);
+      for (uint32_t w = 0; w < A.wait_limit && !ok; ++w) ok = mbar_try_wait(&s_ibar[ibuf], (iphase >> ibuf) & 1u);
       if (ok) {
         iphase ^= 1u << ibuf;
       } else {
-        berr(a.err, c_lo, kErrTileOverflow);
+        berr(a.err, c_lo, kErrStageTimeout);
         s_abort = 1;
       }
     }
@@ -1641,7 +1641,9 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
         ItemGeo gl{};
         if (lane == 0) {
           gl = item_geo(it[my - c_lo], it[my + 1 - c_lo]);
-          stage_item(L, gl, wbuf, bar);
+          // (test hook: the skipped item gets neither an arrival nor a copy,
+          // so its bounded wait below runs out)
+          if (my != A.skip_item) stage_item(L, gl, wbuf, bar);
           // take the next item now and start bringing its data into L2
           nx = cur + atomicAdd(&s_next, 1u);
           if (nx < seg_end) prefetch_item(L, item_geo(it[nx - c_lo], it[nx + 1 - c_lo]));
@@ -1659,15 +1661,15 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
         gcur.ok = __shfl_sync(0xffffffffu, (int)gl.ok, 0) != 0;
         gcur.runs = __shfl_sync(0xffffffffu, (int)gl.runs, 0) != 0;
         bool ok = false;
-        for (uint32_t w = 0; w < kWaitLimit && !ok; ++w) ok = mbar_try_wait(bar, phase);
+        for (uint32_t w = 0; w < A.wait_limit && !ok; ++w) ok = mbar_try_wait(bar, phase);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) {
           if (lane == 0) {
-            berr(a.err, my, kErrTileOverflow);
+            berr(a.err, my, kErrStageTimeout);
             // keep waiting (bounded) for the copy in flight: the warp buffers
             // are reused as flush rows once the band's items are done
             bool done = false;
-            for (uint32_t w = 0; w < kWaitLimit && !done; ++w) done = mbar_try_wait(bar, phase);
+            for (uint32_t w = 0; w < A.wait_limit && !done; ++w) done = mbar_try_wait(bar, phase);
           }
           __syncwarp();
           bad = true;
@@ -1710,7 +1712,7 @@ __global__ void __launch_bounds__(kBT, 1) k_band(const BandRunArgs A) {
     // still be in flight before the CTA's shared memory is released
     for (int bsel = 0; bsel < 2; ++bsel) {
       bool done = false;
-      for (uint32_t w = 0; w < kWaitLimit && !done; ++w) done = mbar_try_wait(&s_ibar[bsel], (iphase >> bsel) & 1u);
+      for (uint32_t w = 0; w < A.wait_limit && !done; ++w) done = mbar_try_wait(&s_ibar[bsel], (iphase >> bsel) & 1u);
     }
   }
 }

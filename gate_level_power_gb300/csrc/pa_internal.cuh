@@ -58,6 +58,8 @@ enum DevErrCode : uint32_t {
   kErrToggle = 6,
   kErrTileOverflow = 7,
   kErrCountOverflow = 8,  // a cycle reached 2^24 events: counts must be accumulated exactly
+  kErrLayout = 9,         // a work item of the banded layout is inconsistent (index: item)
+  kErrStageTimeout = 10,  // a bounded wait for a shared-memory stage copy gave up (index: item)
 };
 constexpr unsigned long long kNoErr = ~0ull;
 
@@ -239,11 +241,22 @@ struct BandBuildArgs {
   unsigned long long* err;
 };
 
+// Bounded waits of the banded kernel on its TMA stage copies: tries of
+// mbarrier.try_wait (each suspends the thread for at most about 0.1 ms)
+// before the wait gives up, records kErrStageTimeout and the warp stops.
+constexpr uint32_t kBandWaitLimit = 1u << 16;
+// The same limit under the test hook that leaves one item's stage unstarted
+// (PA_TEST_STAGE_TIMEOUT): a few milliseconds.
+constexpr uint32_t kBandTestWaitLimit = 64;
+constexpr uint32_t kNoItem = 0xFFFFFFFFu;
+
 struct BandRunArgs {
   RunArgs r;             // cells, lut, leak, gates, params, bins, totals, err, debug
   BandLayout L;
   uint32_t* item_ctr;    // [2] items handed out so far, of the main part and of the tail (zero before the launch)
   uint32_t chunk;        // items a CTA takes at a time (set by band_fused)
+  uint32_t wait_limit;   // tries per bounded stage wait (kBandWaitLimit)
+  uint32_t skip_item;    // test hook: the item whose stage copy is never started (kNoItem: none)
 };
 
 // kernels (pa_kernels.cu)

@@ -62,7 +62,8 @@ extern "C" {
 #define PA_ERR_TOGGLE (-5)   /* an event's value equals the pin's previous value      */
 #define PA_ERR_OOM (-6)      /* device or host allocation failed                     */
 #define PA_ERR_CUDA (-7)     /* a CUDA runtime call failed                           */
-#define PA_ERR_INTERNAL (-8) /* a device-side consistency check failed               */
+#define PA_ERR_INTERNAL (-8) /* a device-side consistency check failed, or a bounded
+                                device-side wait gave up (pa_last_error says which)  */
 
 #define PA_MEM_HOST 0   /* pointers are host memory (pageable or pinned)   */
 #define PA_MEM_DEVICE 1 /* pointers are device memory on the ctx's device  */
@@ -320,10 +321,13 @@ int pa_load_events(pa_ctx *ctx, const pa_events *ev);
  * bytes per event), 20 bytes per unit and 16 bytes per work item; the build also
  * takes temporary space of about 24 bytes per (band, gate) and 32 bytes per
  * unit.
+ * A library of more than 64 cells gets no layout (the banded kernel stages
+ * at most 64 cells' tables in shared memory): the call succeeds and runs take
+ * the unbanded path (pa_result.path = PA_PATH_UNBANDED).
  * Errors: PA_ERR_ORDER (no events loaded), PA_ERR_ARG (t_clk_ns not > 0,
- * band_cycles not a power of two <= 4096, more than 64 cells, events spanning
- * more than 2^20 bands), PA_ERR_OOM, PA_ERR_CUDA. Loading a new library,
- * netlist or events drops the bands.
+ * band_cycles not a power of two <= 4096, events spanning more than 2^20
+ * bands), PA_ERR_OOM, PA_ERR_CUDA. Loading a new library, netlist or events
+ * drops the bands.
  */
 int pa_build_bands(pa_ctx *ctx, float t_clk_ns, uint32_t band_cycles);
 
@@ -344,21 +348,29 @@ int pa_run(pa_ctx *ctx, const pa_run_params *params, pa_result *out);
  * that forbid allocation after start-up. pa_run may grow its scratch buffers
  * on the first call or when n_cycles or the gate count grows; this entry point
  * never does: its per-run scratch (cycle bins, work lists, totals) lives in
- * one file-scope device array of PA_NOALLOC_SCRATCH_BYTES (5 MiB) that
- * every GPU loading libpa.so holds until the process exits.
+ * one file-scope device array of PA_NOALLOC_SCRATCH_BYTES (5 MiB).
+ *
+ * When the array is committed: pa_create looks up the array's device address
+ * on the context's device (with that device current) and keeps it in the
+ * context; under CUDA's lazy module loading that lookup is what loads the
+ * library's module holding the array, so the 5 MiB are taken at the first
+ * pa_create on a device and held until the process exits. pa_run_noalloc
+ * itself only reads the kept address. If the lookup failed at pa_create
+ * (e.g. the device had no memory left), pa_create still succeeds and
+ * pa_run_noalloc returns PA_ERR_CUDA with that reason.
  *
  * Same arguments, computation and results as pa_run on the data loaded into
  * ctx (loading itself still allocates; do it beforehand), with these limits:
  *   n_cycles <= PA_NOALLOC_MAX_CYCLES, netlist gates <= PA_NOALLOC_MAX_GATES,
- *   out->out_mem == PA_MEM_DEVICE for every non-NULL array in out.
+ *   out->out_mem == PA_MEM_DEVICE for every non-NULL array in out,
+ *   part_mode == PA_PART_EVENTS, and cell_power_w only together with
+ *   gate_power_w (the per-gate sums are accumulated in gate_power_w).
  * Beyond them it returns PA_ERR_ARG and says which limit was hit.
- * The first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any stream
- * capture. All calls share the one array and it keeps the last call's
- * contents (each call clears what it needs zeroed): calls whose device work
- * overlaps -- from several threads, contexts or streams at once -- race and
- * must be serialised by the caller. Per-event debug arrays and gate_power_w
- * are written in place and may hold partial data after an error; the other
+ * All calls share the one array and it keeps the last call's contents (each
+ * call clears what it needs zeroed): calls whose device work overlaps -- from
+ * several threads, contexts or streams at once -- race and must be
+ * serialised by the caller. Per-event debug arrays and gate_power_w are
+ * written in place and may hold partial data after an error; the other
  * outputs are written only on PA_OK.
  */
 #define PA_NOALLOC_MAX_CYCLES 65536u

@@ -205,3 +205,21 @@ def test_tie_heavy_long_units_banded(glp):
     assert_parity(r, o)
     assert r["n_tiles"] > 0 and r["n_heavy"] > 0
     assert_parity(banded_run(glp, w, band_cycles=4, debug=False), o, debug=False)
+
+
+def test_large_library_falls_back_to_unbanded(glp):
+    # 200 cells: more than the banded kernel stages in shared memory. The
+    # layout call succeeds, builds nothing, and the run takes the unbanded
+    # path, at the same bar against the oracle.
+    w = synth.custom(seed=29, n_gates=3000, n_cells=200, k_mode=1, n_slew=7, n_load=7, n_cycles=120,
+                     n_events=60000, pair_frac=0.1, threads=4)
+    assert len(w.n_inputs) == 200
+    with glp.PowerAnalyzer(0) as pa:
+        pa.load_workload(w)
+        pa.build_bands(w.t_clk_ns)
+        r = pa.run(w.vdd, w.t_clk_ns, w.n_cycles, debug=True)
+        fast = pa.run(w.vdd, w.t_clk_ns, w.n_cycles)
+    assert r["path"] == fast["path"] == glp.PA_PATH_UNBANDED
+    o = oracle.run(w, debug=True, threads=8)
+    assert_parity(r, o)
+    assert_parity(fast, o, debug=False)

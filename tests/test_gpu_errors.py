@@ -145,3 +145,32 @@ def test_injected_allocation_failure(glp, w):
         # later allocations succeed again
         pa.load_library(w.n_inputs, w.n_slew, w.n_load, w.slew_axis, w.load_axis, w.lut_off, w.lut,
                         w.leak_off, w.leak)
+
+
+def test_stage_wait_timeout_is_reported(glp):
+    # Test hook PA_TEST_STAGE_TIMEOUT=i: the banded kernel never starts the
+    # TMA stage copy of work item i, so the warp's bounded mbarrier wait runs
+    # out (after a few ms under the hook). The kernel records a distinct
+    # error, stops that warp and returns; nothing faults and nothing spins.
+    w = synth.generate(1)
+    os.environ["PA_TEST_STAGE_TIMEOUT"] = "3"
+    try:
+        pa = glp.PowerAnalyzer(0)
+    finally:
+        del os.environ["PA_TEST_STAGE_TIMEOUT"]
+    with pa:
+        pa.load_workload(w)
+        pa.build_bands(w.t_clk_ns)
+        msg = expect(glp, glp.PA_ERR_INTERNAL, pa.run, w.vdd, w.t_clk_ns, w.n_cycles)
+        assert "stage wait timed out" in msg and "item 3" in msg, msg
+    # the device context is still usable: a context without the hook runs the
+    # same layout to the unbanded run's results
+    with glp.PowerAnalyzer(0) as pa:
+        pa.load_workload(w)
+        ref = pa.run(w.vdd, w.t_clk_ns, w.n_cycles)
+        pa.build_bands(w.t_clk_ns)
+        r = pa.run(w.vdd, w.t_clk_ns, w.n_cycles)
+    assert r["path"] == glp.PA_PATH_BANDED
+    np.testing.assert_array_equal(r["event_count"], ref["event_count"])
+    for key in ("p_int", "p_sw", "p_gl", "p_leak"):
+        assert abs(r[key] - ref[key]) <= 1e-5 * abs(ref[key]), key

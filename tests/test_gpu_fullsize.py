@@ -1,16 +1,19 @@
 """Full-size parity on the large configurations (200M, 1B and 2B events), in
-the launch configuration the benchmark times (the banded layout, and the
-unbanded kernel alongside), for the per-event-output variant of the kernels and
-for the timed variant the benchmark runs.
+the launch configurations the benchmark times (the unbanded pass, the banded
+layout), for the per-event-output variant of the kernels and for the timed
+variant the benchmark runs.
 
-At these sizes the oracle cannot afford its full per-cycle leakage split over
-every gate, so it checks what it can compute one by one:
-  * all four power totals and the per-cycle event and glitch counts over every
-    gate (totals within 1e-5 relative, counts bit-exact);
-  * the waveform on sampled cycles, including the GPU's peak cycle (each
-    within 1e-4 of the peak bin), all gates contributing;
+The oracle runs over the whole workload with its full per-cycle leakage split
+(every gate's intervals over every cycle; about a minute per configuration on
+the host's cores) and checks:
+  * all four power totals and the per-cycle event and glitch counts (totals
+    within 1e-5 relative, counts bit-exact);
+  * every waveform bin, within 1e-4 of the peak bin;
   * per-event gate state, LUT interval and glitch flag bit-exact on sampled gate
-    blocks, which include the heaviest gates (streamed in windows).
+    blocks, which include the heaviest gates (streamed in windows); the
+    oracle's per-event outputs of every event would need the whole trace's
+    arrays a second time in host memory.
+The oracle's results are kept per configuration, so each runs once per module.
 """
 import os
 
@@ -33,6 +36,31 @@ def glp():
     return glp
 
 
+_ORACLE = {}
+
+
+def oracle_full(cfg, w):
+    """The oracle over all of workload ``w`` (config ``cfg``), full waveform;
+    computed once per configuration."""
+    if cfg not in _ORACLE:
+        _ORACLE[cfg] = oracle.run(w, wave="full", threads=os.cpu_count() or 8)
+    return _ORACLE[cfg]
+
+
+def assert_every_bin(res, o, E=None):
+    for key in ("p_int", "p_sw", "p_gl", "p_leak"):
+        assert abs(res[key] - o[key]) <= TOL_P * abs(o[key]), (key, res[key], o[key])
+    if E is not None:
+        assert int(o["evcount"].sum()) == E
+    np.testing.assert_array_equal(res["event_count"].astype(np.uint64), o["evcount"])
+    np.testing.assert_array_equal(res["glitch_count"].astype(np.uint64), o["glcount"])
+    peak = float(np.abs(o["waveform"]).max())
+    err = np.abs(res["waveform"].astype(np.float64) - o["waveform"])
+    worst = int(np.argmax(err))
+    assert len(err) == len(o["waveform"])
+    assert float(err[worst]) <= TOL_W * peak, (worst, float(err[worst]), peak)
+
+
 def sub_workload(w, pb, g0, g1):
     """Gates [g0, g1) of w as a workload of their own (offsets rebased)."""
     import copy
@@ -47,9 +75,9 @@ def sub_workload(w, pb, g0, g1):
     return s, e0, e1
 
 
-@pytest.mark.parametrize("cfg,banded", [(3, False), (3, True), (4, False), (4, True), (5, True), (6, False), (6, True)])
+@pytest.mark.parametrize("cfg,banded", [(3, False), (3, True), (4, False), (4, True), (5, False), (5, True), (6, False),
+                                        (6, True)])
 def test_full_size_config(glp, cfg, banded):
-    threads = os.cpu_count() or 8
     w = synth.generate(cfg)
     E, G, N = w.n_events, w.n_gates, w.n_cycles
     with glp.PowerAnalyzer(0) as pa:
@@ -61,22 +89,12 @@ def test_full_size_config(glp, cfg, banded):
     assert r["path"] == fast["path"] == (glp.PA_PATH_BANDED if banded else glp.PA_PATH_UNBANDED)
     assert r["n_heavy"] > 0
     assert r["n_tiles"] > 0 or (cfg == 6 and not banded)  # config 6's gates are all heavy for the unbanded kernel
-    # totals, counts and sampled cycles over all gates, for both variants
-    rng = np.random.default_rng(cfg)
-    peak_c = int(np.argmax(r["waveform"]))
-    cyc = np.unique(np.concatenate([[0, N - 1, peak_c, int(np.argmax(fast["waveform"]))],
-                                    rng.choice(N, 61, replace=False)])).astype(np.uint32)
-    o = oracle.run(w, wave="sample", sample_cycles=cyc, threads=threads)
-    assert int(o["evcount"].sum()) == E
-    peak = float(np.abs(o["waveform"]).max())
+    # totals, counts and every waveform bin over all gates, for both variants
+    o = oracle_full(cfg, w)
     for res in (r, fast):
-        for key in ("p_int", "p_sw", "p_gl", "p_leak"):
-            assert abs(res[key] - o[key]) <= TOL_P * abs(o[key]), (key, res[key], o[key])
-        np.testing.assert_array_equal(res["event_count"].astype(np.uint64), o["evcount"])
-        np.testing.assert_array_equal(res["glitch_count"].astype(np.uint64), o["glcount"])
-        err = np.abs(res["waveform"][cyc].astype(np.float64) - o["waveform"])
-        assert float(err.max()) <= TOL_W * peak, (float(err.max()), peak)
+        assert_every_bin(res, o, E)
     # per-event outputs on sampled gate blocks, heaviest gates included
+    rng = np.random.default_rng(cfg)
     pb = w.pin_base().astype(np.int64)
     n_g = np.diff(w.pin_off.astype(np.int64)[pb])
     heavy = np.argsort(n_g)[-12:]
@@ -95,29 +113,18 @@ def test_full_size_config(glp, cfg, banded):
 def test_full_size_paper_partition(glp, partition, knobs):
     # the paper's (gate, window) thread partition on the large skewed workload
     # (config 3: 26M threads at density, 313M at 32 cycles per thread)
-    threads = os.cpu_count() or 8
     w = synth.generate(3)
     N = w.n_cycles
     with glp.PowerAnalyzer(0) as pa:
         pa.load_workload(w)
         r = pa.run(w.vdd, w.t_clk_ns, N, partition=partition, **knobs)
     assert r["path"] == glp.PA_PATH_WINDOWS
-    rng = np.random.default_rng(7)
-    cyc = np.unique(np.concatenate([[0, N - 1, int(np.argmax(r["waveform"]))],
-                                    rng.choice(N, 61, replace=False)])).astype(np.uint32)
-    o = oracle.run(w, wave="sample", sample_cycles=cyc, threads=threads)
-    for key in ("p_int", "p_sw", "p_gl", "p_leak"):
-        assert abs(r[key] - o[key]) <= TOL_P * abs(o[key]), (key, r[key], o[key])
-    np.testing.assert_array_equal(r["event_count"].astype(np.uint64), o["evcount"])
-    np.testing.assert_array_equal(r["glitch_count"].astype(np.uint64), o["glcount"])
-    peak = float(np.abs(o["waveform"]).max())
-    assert float(np.abs(r["waveform"][cyc].astype(np.float64) - o["waveform"]).max()) <= TOL_W * peak
+    assert_every_bin(r, oracle_full(3, w), w.n_events)
 
 
 def test_full_size_streamed_run(glp):
     # the one-shot path of the benchmark's e2e figure: the 1B-event trace kept
     # in host memory, streamed through the device in chunks
-    threads = os.cpu_count() or 8
     w = synth.generate(4)
     N = w.n_cycles
     with glp.PowerAnalyzer(0) as pa:
@@ -126,13 +133,4 @@ def test_full_size_streamed_run(glp):
         pa.load_netlist(w.cell_id, w.load_ff, w.init_in, w.init_out)
         r = pa.run(w.vdd, w.t_clk_ns, N, stream=(w.pin_off, w.t_ns, w.slew_ps, w.value))
     assert r["n_tiles"] > 1  # chunks
-    rng = np.random.default_rng(11)
-    cyc = np.unique(np.concatenate([[0, N - 1, int(np.argmax(r["waveform"]))],
-                                    rng.choice(N, 61, replace=False)])).astype(np.uint32)
-    o = oracle.run(w, wave="sample", sample_cycles=cyc, threads=threads)
-    for key in ("p_int", "p_sw", "p_gl", "p_leak"):
-        assert abs(r[key] - o[key]) <= TOL_P * abs(o[key]), (key, r[key], o[key])
-    np.testing.assert_array_equal(r["event_count"].astype(np.uint64), o["evcount"])
-    np.testing.assert_array_equal(r["glitch_count"].astype(np.uint64), o["glcount"])
-    peak = float(np.abs(o["waveform"]).max())
-    assert float(np.abs(r["waveform"][cyc].astype(np.float64) - o["waveform"]).max()) <= TOL_W * peak
+    assert_every_bin(r, oracle_full(4, w), w.n_events)

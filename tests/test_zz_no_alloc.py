@@ -5,8 +5,9 @@ scratch is one fixed device array inside libpa.so.
 
 Checked through the C ABI against pa_run on the same loaded data, twice in a
 row (the shared array keeps the previous call's contents, so the second call
-shows the clearing is complete). This file is collected last; it passes alone
-in a fresh process and after the other tests.
+shows the clearing is complete), with the device's free memory read before and
+after the two calls: it must not move. This file is collected last; it passes
+alone in a fresh process and after the other tests.
 """
 import numpy as np
 import pytest
@@ -27,21 +28,53 @@ def glp():
     return glp
 
 
-def _noalloc(glp, pa, w, torch, **kw):
+def _outputs(w, torch, per_gate=False, debug=False):
+    """Caller-owned device output arrays, filled with junk."""
     dev = torch.device("cuda", 0)
-    wave = torch.full((w.n_cycles,), float("nan"), dtype=torch.float32, device=dev)
-    evc = torch.full((w.n_cycles,), -1, dtype=torch.int32, device=dev)
-    glc = torch.full((w.n_cycles,), -1, dtype=torch.int32, device=dev)
+    o = dict(waveform=torch.full((w.n_cycles,), float("nan"), dtype=torch.float32, device=dev),
+             event_count=torch.full((w.n_cycles,), -1, dtype=torch.int32, device=dev),
+             glitch_count=torch.full((w.n_cycles,), -1, dtype=torch.int32, device=dev))
+    if per_gate:
+        o["gate_power"] = torch.full((len(w.cell_id) * 4,), float("nan"), dtype=torch.float64, device=dev)
+        o["cell_power"] = torch.full((len(w.n_inputs) * 4,), float("nan"), dtype=torch.float64, device=dev)
+    if debug:
+        for k in ("state_pre", "lut_ij", "is_glitch"):
+            o[k] = torch.full((len(w.t_ns),), 0xAB, dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
+    return o
+
+
+def _call(glp, pa, w, o, **kw):
+    """One pa_run_noalloc through the C ABI into the arrays of ``o``."""
     p = glp.PaRunParams(float(w.vdd), float(w.t_clk_ns), int(w.n_cycles), 0.0, int(kw.get("tile", 0)),
                         int(kw.get("heavy", 0)), 0)
     r = glp.PaResult()
     r.out_mem = glp.PA_MEM_DEVICE
-    r.waveform_w, r.event_count, r.glitch_count = wave.data_ptr(), evc.data_ptr(), glc.data_ptr()
+    r.waveform_w, r.event_count, r.glitch_count = (o["waveform"].data_ptr(), o["event_count"].data_ptr(),
+                                                   o["glitch_count"].data_ptr())
+    if "gate_power" in o:
+        r.gate_power_w, r.cell_power_w = o["gate_power"].data_ptr(), o["cell_power"].data_ptr()
+    if "state_pre" in o:
+        r.state_pre, r.lut_ij, r.is_glitch = (o["state_pre"].data_ptr(), o["lut_ij"].data_ptr(),
+                                              o["is_glitch"].data_ptr())
     glp.pa_run_noalloc(pa.ctx, p, r)
-    return dict(p_int=r.p_int_w, p_sw=r.p_sw_w, p_gl=r.p_gl_w, p_leak=r.p_leak_w,
-                waveform=wave.cpu().numpy(), event_count=evc.cpu().numpy().view(np.uint32),
-                glitch_count=glc.cpu().numpy().view(np.uint32))
+    return r
+
+
+def _host(r, o):
+    res = dict(p_int=r.p_int_w, p_sw=r.p_sw_w, p_gl=r.p_gl_w, p_leak=r.p_leak_w)
+    for k, v in o.items():
+        a = v.cpu().numpy()
+        res[k] = a.view(np.uint32) if k in ("event_count", "glitch_count") else a
+    for k in ("gate_power", "cell_power"):
+        if k in res:
+            res[k] = res[k].reshape(-1, 4)
+    return res
+
+
+def _noalloc(glp, pa, w, torch, **kw):
+    o = _outputs(w, torch)
+    return _host(_call(glp, pa, w, o, **kw), o)
 
 
 def _same(a, b):
@@ -66,10 +99,37 @@ def test_noalloc_matches_pa_run_two_calls(glp, case):
         pa.load_workload(w)
         ref = pa.run(w.vdd, w.t_clk_ns, w.n_cycles, tile_events=kw.get("tile", 0),
                      heavy_events=kw.get("heavy", 0))
-        first = _noalloc(glp, pa, w, torch, **kw)
-        second = _noalloc(glp, pa, w, torch, **kw)
+        o1, o2 = _outputs(w, torch), _outputs(w, torch)
+        _call(glp, pa, w, o1, **kw)  # warm-up: kernel modules load on first use
+        torch.cuda.synchronize()
+        free0 = torch.cuda.mem_get_info(0)[0]
+        r1 = _call(glp, pa, w, o1, **kw)
+        r2 = _call(glp, pa, w, o2, **kw)
+        torch.cuda.synchronize()
+        free1 = torch.cuda.mem_get_info(0)[0]
+        first, second = _host(r1, o1), _host(r2, o2)
+    assert free1 == free0, (free0, free1)
     _same(first, ref)
     _same(second, ref)
+
+
+def test_noalloc_per_gate_and_debug_outputs(glp):
+    # gate and cell power accumulated in the caller's arrays, the per-event
+    # arrays written straight to the caller: compared with pa_run, states, LUT
+    # intervals, glitch flags and counts bit for bit, two calls in a row
+    import torch
+    w = synth.custom(seed=23, n_gates=400, n_cells=12, n_cycles=300, n_events=40000, pair_frac=0.1, threads=4)
+    with glp.PowerAnalyzer(0) as pa:
+        pa.load_workload(w)
+        ref = pa.run(w.vdd, w.t_clk_ns, w.n_cycles, debug=True, gate_power=True, cell_power=True)
+        for _ in range(2):
+            o = _outputs(w, torch, per_gate=True, debug=True)
+            got = _host(_call(glp, pa, w, o), o)
+            _same(got, ref)
+            for k in ("state_pre", "lut_ij", "is_glitch"):
+                np.testing.assert_array_equal(got[k], ref[k], err_msg=k)
+            for k in ("gate_power", "cell_power"):
+                np.testing.assert_allclose(got[k], ref[k], rtol=1e-9, atol=1e-30, err_msg=k)
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(glp):
@@ -91,3 +151,11 @@ def test_noalloc_rejects_sizes_beyond_its_scratch(glp):
         with pytest.raises(glp.PaError) as ei:
             glp.pa_run_noalloc(pa.ctx, p, r)
         assert ei.value.code == glp.PA_ERR_ARG
+        # per-cell sums need the per-gate accumulators in the caller's array
+        cell = torch.zeros(len(w.n_inputs) * 4, dtype=torch.float64, device="cuda")
+        r = glp.PaResult()
+        r.out_mem = glp.PA_MEM_DEVICE
+        r.cell_power_w = cell.data_ptr()
+        with pytest.raises(glp.PaError) as ei:
+            glp.pa_run_noalloc(pa.ctx, p, r)
+        assert ei.value.code == glp.PA_ERR_ARG and "gate_power_w" in str(ei.value)
