@@ -537,7 +537,8 @@ def run_ours(args):
     fused_mean = statistics.mean(fused_ms)
     fused_med = statistics.median(fused_ms)
     achieved = B / (fused_mean * 1e-3) / 1e9
-    kname = {glp.PA_PATH_BANDED: "k_band", glp.PA_PATH_WINDOWS: "k_window"}.get(r["path"], "k_fused")
+    kname = {glp.PA_PATH_BANDED: "k_band", glp.PA_PATH_WINDOWS: "k_window", glp.PA_PATH_WARP: "k_csr"}.get(
+        r["path"], "k_fused")
     traffic = None if args.synth else ncu_traffic(kname, args.config)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -547,6 +548,9 @@ def run_ours(args):
                      "layout build is not timed)" if rerun else
                      "pa_run on the loaded per-pin layout: the paper's partition (k_win_plan) + k_window + final "
                      "reduction" if windows else
+                     "pa_run on the loaded per-pin layout: event-count partition (k_cp_*: light tiles and "
+                     "heavy-gate pieces) + fused kernel (k_csr, one warp per item) + final reduction, every step"
+                     if r["path"] == glp.PA_PATH_WARP else
                      "pa_run on the loaded per-pin layout: event-count partition (k_part_*) + fused kernel "
                      "(k_fused) + final reduction, every step")
         line = {
@@ -588,7 +592,8 @@ def run_ours(args):
             "host_placement": host_placement,
             "p_total_w": r["p_int"] + r["p_sw"] + r["p_gl"] + r["p_leak"],
             "n_tiles": r["n_tiles"], "n_heavy": r["n_heavy"],
-            "path": {glp.PA_PATH_BANDED: "banded", glp.PA_PATH_WINDOWS: "windows"}.get(r["path"], "unbanded"),
+            "path": {glp.PA_PATH_BANDED: "banded", glp.PA_PATH_WINDOWS: "windows",
+                     glp.PA_PATH_WARP: "unbanded, warp kernel"}.get(r["path"], "unbanded"),
             **({"partition": dict(part, part_threads=r["part_threads"])} if windows else {}),
             **({"build_bands_ms": build_ms} if build_ms is not None else {}),
         }

@@ -76,7 +76,7 @@ class PaError(RuntimeError):
 
 EXPORTS = ("pa_create", "pa_destroy", "pa_load_library", "pa_load_netlist", "pa_load_events", "pa_run",
            "pa_run_noalloc", "pa_run_stream", "pa_build_bands", "pa_default_params", "pa_last_error", "pa_version")
-PA_PATH_UNBANDED, PA_PATH_BANDED, PA_PATH_WINDOWS = 0, 1, 2
+PA_PATH_UNBANDED, PA_PATH_BANDED, PA_PATH_WINDOWS, PA_PATH_WARP = 0, 1, 2, 3
 PA_NOALLOC_MAX_CYCLES = 65536
 PA_NOALLOC_MAX_GATES = 262144
 

@@ -10,7 +10,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libpa.so")
-SOURCES = ["pa_api.cu", "pa_kernels.cu", "pa_banded.cu", "pa_window.cu"]
+SOURCES = ["pa_api.cu", "pa_kernels.cu", "pa_banded.cu", "pa_window.cu", "pa_csr.cu"]
 HEADERS = [os.path.join(CSRC, "pa_internal.cuh"), os.path.join(INCLUDE, "pa.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", f"-I{INCLUDE}"]

@@ -58,7 +58,7 @@ struct pa_ctx {
 
   // scratch
   DevBuf value_tmp, err_word, tmax_bits, val_starts;
-  DevBuf bins, part_blk, part_counts, tiles, heavy, p0_tot, p_out;
+  DevBuf bins, part_blk, part_counts, tiles, heavy, pieces, p0_tot, p_out;
   DevBuf dbg[3], wave_tmp, cnt_tmp, chunk_sums, gate_tmp, cell_tmp;
   // the paper's (gate, window) partition: per-gate plan, thread offsets, scan
   // scratch, total slots (+ the largest events per thread), histogram
@@ -197,6 +197,10 @@ struct RunPlan {
   float T = 0.f;
   double Td = 0.0, t_max = 0.0;
   uint32_t tile = 0, heavy = 0, N = 0, G = 0, nblk = 0;
+  // the warp kernel's tile knobs (the user's, else its defaults) and whether
+  // it runs the fast pass (no per-event outputs; cells and knobs within its limits)
+  uint32_t csr_tile = 0, csr_heavy = 0;
+  bool csr = false;
   bool pow2 = false, debug = false, timing = false, gate = false, glitch_all = false, esw_rise = false;
   double vdd = 0.0;
   // partition: PA_PART_*, with the paper's knobs
@@ -211,6 +215,8 @@ struct PassBufs {
   uint32_t* part_counts = nullptr;
   Tile* tiles = nullptr;
   uint32_t* heavy = nullptr;
+  Piece* pieces = nullptr;   // the warp kernel's heavy-gate pieces (null: the CTA kernel runs)
+  uint64_t max_pieces = 0;
   double* p0_tot = nullptr;
   double* p_out = nullptr;
   double* chunk_sums = nullptr;
@@ -273,6 +279,9 @@ int check_run(pa_ctx* c, const pa_run_params* prm, const pa_result* out, const c
   plan->part_stats = (prm->flags & PA_RUN_PART_STATS) != 0 && plan->part_mode != PA_PART_EVENTS;
   plan->pow2 = is_pow2(plan->T);
   plan->vdd = prm->vdd;
+  plan->csr_tile = prm->tile_events ? prm->tile_events : kCsrDefaultTile;
+  plan->csr_heavy = prm->heavy_events ? prm->heavy_events : kCsrDefaultHeavy;
+  plan->csr = !plan->debug && plan->part_mode == PA_PART_EVENTS && csr_eligible(c->n_cells, plan->csr_tile, plan->csr_heavy);
   return PA_OK;
 }
 
@@ -367,6 +376,14 @@ int run_pass(pa_ctx* c, const RunPlan& plan, const PassBufs& B, pa_result* out, 
   const uint32_t N = plan.N;
   RunArgs a = make_run_args(c, plan, B);
   if (band) a.heavy = band->big;  // the unbanded kernel streams the gates the layout left out
+  // the warp kernel runs the fast pass when the run has room for its pieces
+  // (the exact-count retry and the per-event outputs take the CTA kernel)
+  const bool csr = plan.csr && B.pieces != nullptr && !band && !win;
+  if (csr) {
+    a.tile_target = plan.csr_tile;
+    a.heavy_thresh = plan.csr_heavy;
+    a.pieces = B.pieces;
+  }
   BandRunArgs A;
   if (band) {
     A.r = a;
@@ -380,8 +397,10 @@ int run_pass(pa_ctx* c, const RunPlan& plan, const PassBufs& B, pa_result* out, 
   double p[4];
   unsigned long long key = kNoErr;
   uint32_t counts[4] = {0, 0, 0, 0};
+  bool ran_csr = false;
   for (int exact = 0; exact < 2; ++exact) {
     launches = 0;
+    ran_csr = csr && !exact;
     if (plan.timing) CUDA_TRY(c, cudaEventRecord(c->ev[0], st));
     CUDA_TRY(c, cudaMemsetAsync(B.bins, 0, (size_t)N * sizeof(float4), st));
     if (exact) CUDA_TRY(c, cudaMemsetAsync(B.cnt_ev, 0, (size_t)N * sizeof(uint32_t), st));
@@ -406,7 +425,14 @@ int run_pass(pa_ctx* c, const RunPlan& plan, const PassBufs& B, pa_result* out, 
       CUDA_TRY(c, cudaMemcpyAsync(B.part_counts, part, sizeof(part), cudaMemcpyHostToDevice, st));
       CUDA_TRY(c, band_p0(a, st));
       launches += plan.G ? 1 : 0;
+    } else if (csr && !exact) {
+      // the warp kernel's partition: light tiles and heavy-gate pieces
+      CUDA_TRY(c, cudaMemsetAsync(B.part_counts, 0, 4 * sizeof(uint32_t), st));
+      CUDA_TRY(c, launch_csr_partition(a, plan.nblk, B.max_pieces, st));
+      launches += plan.nblk ? 4 : 0;
     } else {
+      a.tile_target = plan.tile;
+      a.heavy_thresh = plan.heavy;
       CUDA_TRY(c, cudaMemsetAsync(B.part_counts, 0, 4 * sizeof(uint32_t), st));
       CUDA_TRY(c, launch_partition(a, plan.nblk, st));
       launches += plan.nblk ? 3 : 0;
@@ -422,8 +448,12 @@ int run_pass(pa_ctx* c, const RunPlan& plan, const PassBufs& B, pa_result* out, 
       launches += band->n_items ? 1 : 0;
     }
     if (!win && (!band || band->n_big)) {
-      const int grid = c->sm_count * fused_blocks_per_sm(plan.pow2, plan.debug, exact != 0);
-      CUDA_TRY(c, launch_fused(a, grid, plan.pow2, plan.debug, exact != 0, st));
+      if (csr && !exact && !band) {
+        CUDA_TRY(c, launch_csr(a, c->sm_count, plan.pow2, st));
+      } else {
+        const int grid = c->sm_count * fused_blocks_per_sm(plan.pow2, plan.debug, exact != 0);
+        CUDA_TRY(c, launch_fused(a, grid, plan.pow2, plan.debug, exact != 0, st));
+      }
       launches += 1;
     }
     if (plan.timing) CUDA_TRY(c, cudaEventRecord(c->ev[2], st));
@@ -486,7 +516,7 @@ int run_pass(pa_ctx* c, const RunPlan& plan, const PassBufs& B, pa_result* out, 
     out->n_heavy = counts[1];
   }
   out->kernel_launches = launches;
-  out->path = win ? PA_PATH_WINDOWS : band ? PA_PATH_BANDED : PA_PATH_UNBANDED;
+  out->path = win ? PA_PATH_WINDOWS : band ? PA_PATH_BANDED : ran_csr ? PA_PATH_WARP : PA_PATH_UNBANDED;
   if (plan.timing) {
     cudaEventElapsedTime(&out->ms_partition, c->ev[0], c->ev[1]);
     cudaEventElapsedTime(&out->ms_fused, c->ev[1], c->ev[2]);
@@ -612,14 +642,21 @@ int run_stream(pa_ctx* c, const RunPlan& plan, const pa_events* ev, uint64_t tar
   B.wave = (float*)c->wave_tmp.p;
   B.cnt_ev = (uint32_t*)c->cnt_tmp.p;
   B.cnt_gl = (uint32_t*)c->cnt_tmp.p + N;
+  if (plan.csr) {
+    B.max_pieces = csr_max_pieces(max_ev, max_g, plan.csr_heavy);
+    PA_TRY(dreserve(c, c->pieces, (size_t)B.max_pieces * sizeof(Piece)));
+    B.pieces = (Piece*)c->pieces.p;
+  }
   PA_TRY(setup_gate_bufs(c, plan, out, B));
   cudaStream_t st = c->stream;
   const int nc = (int)ch.size();
   double p[4];
   unsigned long long key = kNoErr;
   uint32_t launches = 0;
+  bool stream_csr = false;
   for (int exact = 0; exact < 2; ++exact) {
     launches = 0;
+    stream_csr = B.pieces && !exact;
     if (plan.timing) CUDA_TRY(c, cudaEventRecord(c->ev[0], st));
     CUDA_TRY(c, cudaMemsetAsync(B.bins, 0, (size_t)N * sizeof(float4), st));
     if (exact) CUDA_TRY(c, cudaMemsetAsync(B.cnt_ev, 0, (size_t)N * 2 * sizeof(uint32_t), st));
@@ -687,10 +724,19 @@ int run_stream(pa_ctx* c, const RunPlan& plan, const pa_events* ev, uint64_t tar
       a.s = (const float*)c->st_s[slot].p;
       a.gate_e = B.gate_e ? B.gate_e + (size_t)k.g0 * 4 : nullptr;
       CUDA_TRY(c, cudaMemsetAsync(B.part_counts, 0, 4 * sizeof(uint32_t), st));
-      CUDA_TRY(c, launch_partition(a, partition_blocks(gk), st));
-      const int grid = c->sm_count * fused_blocks_per_sm(plan.pow2, plan.debug, exact != 0);
-      CUDA_TRY(c, launch_fused(a, grid, plan.pow2, plan.debug, exact != 0, st));
-      launches += (gk ? 3 : 0) + 1;
+      if (B.pieces && !exact) {  // the warp kernel (fast pass)
+        a.tile_target = plan.csr_tile;
+        a.heavy_thresh = plan.csr_heavy;
+        a.pieces = B.pieces;
+        CUDA_TRY(c, launch_csr_partition(a, partition_blocks(gk), B.max_pieces, st));
+        CUDA_TRY(c, launch_csr(a, c->sm_count, plan.pow2, st));
+        launches += (gk ? 4 : 0) + 1;
+      } else {
+        CUDA_TRY(c, launch_partition(a, partition_blocks(gk), st));
+        const int grid = c->sm_count * fused_blocks_per_sm(plan.pow2, plan.debug, exact != 0);
+        CUDA_TRY(c, launch_fused(a, grid, plan.pow2, plan.debug, exact != 0, st));
+        launches += (gk ? 3 : 0) + 1;
+      }
       CUDA_TRY(c, cudaEventRecord(c->st_free[slot], st));
     }
     RunArgs a = make_run_args(c, plan, B);
@@ -726,7 +772,7 @@ int run_stream(pa_ctx* c, const RunPlan& plan, const pa_events* ev, uint64_t tar
   out->n_tiles = (uint32_t)nc;  // chunks
   out->n_heavy = 0;
   out->kernel_launches = launches;
-  out->path = PA_PATH_UNBANDED;
+  out->path = stream_csr ? PA_PATH_WARP : PA_PATH_UNBANDED;
   out->ms_partition = out->ms_fused = out->ms_reduce = out->ms_total = 0.f;
   if (plan.timing) cudaEventElapsedTime(&out->ms_total, c->ev[0], c->ev[3]);
   return PA_OK;
@@ -802,7 +848,7 @@ void pa_destroy(pa_ctx* c) {
   if (c->stream) cudaStreamSynchronize(c->stream);
   DevBuf* all[] = {&c->cells, &c->lut, &c->leak, &c->patch, &c->gates, &c->pin_off, &c->gate_off, &c->t, &c->s,
                    &c->value_tmp, &c->err_word, &c->tmax_bits, &c->val_starts, &c->bins, &c->part_blk,
-                   &c->part_counts, &c->tiles, &c->heavy, &c->p0_tot, &c->p_out, &c->dbg[0],
+                   &c->part_counts, &c->tiles, &c->heavy, &c->pieces, &c->p0_tot, &c->p_out, &c->dbg[0],
                    &c->dbg[1], &c->dbg[2], &c->wave_tmp, &c->cnt_tmp, &c->gate_tmp, &c->cell_tmp, &c->scratch_small,
                    &c->chunk_sums, &c->b_bt, &c->b_bs, &c->b_btag, &c->b_urec, &c->b_ugate, &c->b_items,
                    &c->b_big, &c->b_bigf, &c->b_grank, &c->b_cnt, &c->b_evc, &c->b_ubase, &c->b_ebase,
@@ -1042,6 +1088,11 @@ int pa_run(pa_ctx* c, const pa_run_params* prm, pa_result* out) {
   B.cnt_ev = (uint32_t*)c->cnt_tmp.p;
   B.cnt_gl = (uint32_t*)c->cnt_tmp.p + N;
   for (int i = 0; i < 3; ++i) B.dbg[i] = dbg_arrays ? (uint8_t*)c->dbg[i].p : nullptr;
+  if (plan.csr && !banded) {
+    B.max_pieces = csr_max_pieces(c->n_events, G, plan.csr_heavy);
+    PA_TRY(dreserve(c, c->pieces, (size_t)B.max_pieces * sizeof(Piece)));
+    B.pieces = (Piece*)c->pieces.p;
+  }
   PA_TRY(setup_gate_bufs(c, plan, out, B));
   if (plan.part_mode != PA_PART_EVENTS) {
     // the paper's (gate, window) thread partition

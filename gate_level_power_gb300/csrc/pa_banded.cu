@@ -1172,8 +1172,8 @@ struct EvDbg {
 };
 
 // Glitch test against the pin's previous event (staged index ep, if has_prev)
-// and scaling of the dynamic energy; no branches, since on dense pins most
-// warps hold a glitch somewhere. en: the pin's next event in the unit (staged
+// and scaling of the dynamic energy; the one branch is the division of a
+// narrow glitch pulse (predicated lanes). en: the pin's next event in the unit (staged
 // index, -1 if none; only asked for in the glitch-all reading, where the
 // first event of a multi-event pin-cycle takes the pulse to that next event).
 template <bool kPow2, bool kDebug>
@@ -1194,8 +1194,12 @@ __device__ __forceinline__ float glitch_scale(const RunArgs& a, const float* ts,
       sp = __ldg(gs + en);
     }
   }
-  // IEEE division, as in the unbanded kernel: both kernels give one event the same r_gl
-  const float r = fminf(1.f, __fdiv_rn(2000.f * pw, s + sp));
+  // r_gl = min(1, x / y) with IEEE division, as in the unbanded kernel, so
+  // both kernels give one event the same value; x >= y gives 1 (the rounded
+  // quotient of x >= y is >= 1), so only glitch lanes with a narrow pulse divide
+  const float x = 2000.f * pw, y = s + sp;
+  float r = 1.f;
+  if (glitch && x < y) r = __fdiv_rn(x, y);
   return glitch ? r * e_dyn : e_dyn;
 }
 

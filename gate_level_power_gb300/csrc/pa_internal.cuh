@@ -77,6 +77,8 @@ struct ValidateArgs {
   uint32_t* starts;       // scratch [(n_events + 31) / 32 + 1]: bit e set if event e starts a pin
 };
 
+struct Piece;  // a piece of a heavy gate (warp kernel, below)
+
 struct RunArgs {
   // inputs
   const CellDesc* cells;
@@ -100,9 +102,10 @@ struct RunArgs {
   uint32_t tile_target, heavy_thresh;
   // partition
   uint32_t* part_blk;      // [2 * n_blocks] heads / heavies per block, then scanned
-  uint32_t* part_counts;   // [4]: n_tiles, n_heavy, item counter, pad
+  uint32_t* part_counts;   // [4]: n_tiles, n_heavy (n_pieces for the warp kernel), item counter, pad
   Tile* tiles;
   uint32_t* heavy;
+  Piece* pieces;           // heavy-gate pieces of the warp kernel (pa_csr.cu)
   double* p0;              // sum of leakage of initial states, uW
   // accumulators: per cycle {W, D, ev, gl}
   //   W  energy in the cycle: dynamic + in-cycle leakage parts (fJ)
@@ -259,7 +262,47 @@ struct BandRunArgs {
   uint32_t skip_item;    // test hook: the item whose stage copy is never started (kNoItem: none)
 };
 
+// ------------------------------------------------------------------ warp kernel on the per-pin layout
+//
+// The fused kernel of the run on the loaded (CSR) layout (pa_csr.cu), one
+// warp per work item. Work items: light tiles, runs of consecutive whole
+// gates of at most kCsrGates gates whose events fit one warp's stage (the
+// event-count rule of the CTA kernel's tiles, with a target of tile_target
+// events and gates of at most heavy_thresh events), and pieces of the heavy
+// gates: gate g with n_g events is cut into ceil(n_g / kCsrPiece) pieces at
+// times taken from its densest pin (that pin's events split evenly), each pin
+// split at the first event at or after that time, so a piece holds every
+// event of the gate in a time interval. A warp works through a piece in
+// windows of at most kCsrWin events.
+constexpr uint32_t kCsrDefaultTile = 256;
+constexpr uint32_t kCsrDefaultHeavy = 256;
+constexpr uint32_t kCsrMaxTileHeavy = 512;  // tile_target + heavy_thresh a warp's stage holds
+constexpr uint32_t kCsrGates = 32;          // gates per light tile (one lane per gate)
+constexpr uint32_t kCsrPiece = 2048;        // target events per piece of a heavy gate
+constexpr uint32_t kCsrWin = 512;           // events per window of a piece
+
+struct Piece {
+  uint32_t gate, idx;          // the gate; the piece's index among the gate's pieces
+  uint32_t lo[kMaxK + 1];      // per pin, the piece's first event as an index into the pin's events
+  uint32_t pad;
+};
+static_assert(sizeof(Piece) == 32, "piece record size");
+
+// Upper bound of the pieces of a run over n_events events of n_gates gates
+// (gates with more than heavy_thresh events).
+uint64_t csr_max_pieces(uint64_t n_events, uint32_t n_gates, uint32_t heavy_thresh);
+// The warp kernel runs a pass (no per-event outputs, f32 bins) when the
+// library fits its shared-memory cell tables and the tile knobs fit its stage.
+bool csr_eligible(uint32_t n_cells, uint32_t tile_target, uint32_t heavy_thresh);
+// Partition (tiles, pieces and their cut points; P0) into a.tiles / a.pieces /
+// a.part_counts, then the kernel.
+cudaError_t launch_csr_partition(const RunArgs& a, uint32_t n_blocks, uint64_t max_pieces, cudaStream_t st);
+cudaError_t launch_csr(const RunArgs& a, int sm_count, bool pow2, cudaStream_t st);
+
 // kernels (pa_kernels.cu)
+// Exclusive scan of the per-block (heads, heavies) pairs of a partition
+// (single block), totals into part_counts[0..1], part_counts[2] = 0.
+cudaError_t launch_part_scan(const RunArgs& a, uint32_t n_blocks, cudaStream_t st);
 cudaError_t launch_check_pin_off(const uint64_t* pin_off, uint64_t n_pins, uint64_t n_events,
                                  unsigned long long* err, cudaStream_t st);
 cudaError_t launch_validate_events(const ValidateArgs& a, cudaStream_t st);

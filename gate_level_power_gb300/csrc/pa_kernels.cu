@@ -288,6 +288,11 @@ __global__ void __launch_bounds__(256) k_part_emit(const RunArgs a) {
 
 uint32_t partition_blocks(uint32_t n_gates) { return (n_gates + 255) / 256; }
 
+cudaError_t launch_part_scan(const RunArgs& a, uint32_t n_blocks, cudaStream_t st) {
+  k_part_scan<<<1, 1024, 0, st>>>(a, n_blocks);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_partition(const RunArgs& a, uint32_t n_blocks, cudaStream_t st) {
   if (n_blocks == 0) return cudaSuccess;
   k_part_count<<<n_blocks, 256, 0, st>>>(a);

@@ -187,10 +187,19 @@ typedef struct pa_events {
  *   n_cycles       cycle bins (> 0); every event needs floor(fl32(t/t_clk)) < n_cycles
  *   t_max_ns       analysis window end for Eq. 3 and leakage; 0 -> n_cycles * t_clk;
  *                  otherwise it must be >= the latest event time
- *   tile_events    work partition: target events per light tile (0 = default 2048)
- *   heavy_events   gates with more events than this are streamed in event-count
- *                  windows by one CTA (0 = default 2048); tile_events +
- *                  heavy_events must not exceed 4096
+ *   tile_events    work partition: target events per light tile (0 = default:
+ *                  256 for the warp kernel, 2048 for the CTA kernel)
+ *   heavy_events   gates with more events than this are heavy (0 = default: 256
+ *                  / 2048): cut into time pieces of about 2048 events, each
+ *                  worked through by one warp in windows (warp kernel), or
+ *                  streamed in event-count windows by one CTA (CTA kernel);
+ *                  tile_events + heavy_events must not exceed 4096. The run on
+ *                  the per-pin layout takes the warp kernel when it asks for
+ *                  no per-event output (state_pre, lut_ij, is_glitch,
+ *                  gate_power_w, cell_power_w, the alternative readings),
+ *                  the library has at most 64 cells and tile_events +
+ *                  heavy_events (defaults resolved) is at most 512; else the
+ *                  CTA kernel. pa_run_noalloc always takes the CTA kernel.
  *   flags          PA_RUN_* bits
  *   part_mode      PA_PART_* (pa_run only; the other entry points take
  *                  PA_PART_EVENTS)
@@ -240,7 +249,8 @@ typedef struct pa_run_params {
  * (one event per lane, extra global writes); ask for them only when needed.
  * With PA_RUN_TIMING, ms_* hold CUDA-event times of the partition, fused and
  * reduction kernels and of the whole device pass. n_tiles / n_heavy count the
- * work items (light tiles / heavy items); path says which kernel ran.
+ * work items (light tiles / heavy items: heavy gates for the CTA kernel, heavy
+ * gates' pieces for the warp kernel); path says which kernel ran.
  * With part_mode PA_PART_DENSITY or PA_PART_FIXED, part_threads is the number
  * of (gate, window) threads, and with PA_RUN_PART_STATS the part_evt_* hold
  * the nearest-rank 50th, 90th and 99th percentiles and the maximum of the
@@ -260,16 +270,17 @@ typedef struct pa_result {
   float ms_partition, ms_fused, ms_reduce, ms_total;
   uint32_t n_tiles, n_heavy;
   uint32_t kernel_launches;
-  uint32_t path;  /* out: PA_PATH_UNBANDED or PA_PATH_BANDED */
+  uint32_t path;  /* out: PA_PATH_* of the kernel that ran */
   double *gate_power_w;
   double *cell_power_w;
   uint64_t part_threads;
   uint32_t part_evt_p50, part_evt_p90, part_evt_p99, part_evt_max;
 } pa_result;
 
-#define PA_PATH_UNBANDED 0u
+#define PA_PATH_UNBANDED 0u /* the per-pin layout, the CTA kernel (per-event outputs, exact counts) */
 #define PA_PATH_BANDED 1u
 #define PA_PATH_WINDOWS 2u /* the paper's (gate, window) thread partition */
+#define PA_PATH_WARP 3u    /* the per-pin layout, the warp kernel (the pass without per-event outputs) */
 
 /* Create a context on CUDA device `cuda_device`. `cuda_stream` is a
  * cudaStream_t to run on (borrowed, must outlive the ctx) or NULL for a stream

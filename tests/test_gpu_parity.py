@@ -26,12 +26,20 @@ def glp():
 
 
 def gpu_run(glp, w, *, with_value=True, t_max=0.0, debug=True, **kw):
+    """One run; with debug, the per-event-output run (CTA kernel), with the
+    same run without per-event outputs (the warp kernel, where it applies)
+    under ``"fast"``, which assert_parity checks too."""
     with glp.PowerAnalyzer(0) as pa:
         pa.load_workload(w, with_value=with_value)
-        return pa.run(w.vdd, w.t_clk_ns, w.n_cycles, t_max_ns=t_max, debug=debug, **kw)
+        r = pa.run(w.vdd, w.t_clk_ns, w.n_cycles, t_max_ns=t_max, debug=debug, **kw)
+        if debug:
+            r["fast"] = pa.run(w.vdd, w.t_clk_ns, w.n_cycles, t_max_ns=t_max, **kw)
+    return r
 
 
 def assert_parity(r, o, debug=True):
+    if "fast" in r:
+        assert_parity(r["fast"], o, debug=False)
     for key in ("p_int", "p_sw", "p_gl", "p_leak"):
         assert abs(r[key] - o[key]) <= TOL_P * abs(o[key]) + 1e-30, (key, r[key], o[key])
     peak = float(np.abs(o["waveform"]).max())
@@ -180,7 +188,9 @@ def test_timing_and_work_counts_reported(glp):
     w = synth.generate(2)
     r = gpu_run(glp, w, debug=False, timing=True)
     assert r["ms_fused"] > 0 and r["ms_total"] >= r["ms_fused"]
-    assert r["n_tiles"] > 0 and r["kernel_launches"] == 6
+    assert r["path"] == glp.PA_PATH_WARP
+    # partition (count, scan, emit, piece cut points), fused kernel, final reduction (2)
+    assert r["n_tiles"] > 0 and r["kernel_launches"] == 7
 
 
 def test_more_than_2_pow_24_events_in_one_cycle_counts_exactly(glp):

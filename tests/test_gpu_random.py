@@ -48,6 +48,9 @@ def test_random_workload_on_every_path(glp, seed):
     with glp.PowerAnalyzer(0) as pa:
         pa.load_workload(w)
         runs = {"unbanded": pa.run(w.vdd, w.t_clk_ns, w.n_cycles, debug=True),
+                "unbanded timed": pa.run(w.vdd, w.t_clk_ns, w.n_cycles),
+                "unbanded timed, small tiles": pa.run(w.vdd, w.t_clk_ns, w.n_cycles, tile_events=16,
+                                                      heavy_events=8),
                 "window density": pa.run(w.vdd, w.t_clk_ns, w.n_cycles, debug=True, partition="density"),
                 "window fixed": pa.run(w.vdd, w.t_clk_ns, w.n_cycles, partition="fixed", n_cyc_fix=3)}
         pa.build_bands(w.t_clk_ns, band)
