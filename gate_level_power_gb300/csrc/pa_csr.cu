@@ -44,12 +44,13 @@ namespace pa {
 
 namespace {
 
-constexpr int kCW = 32;               // warps per CTA
+constexpr int kCW = 32;               // warps per CTA (their stages fill the shared memory)
 constexpr int kCT = kCW * 32;
-constexpr int kStCap = 528;           // staged events per warp: 512 + 16-byte alignment slack
+constexpr int kStCap = 400;           // staged events per warp: 384 + alignment slack and window bounds
 constexpr int kAx = 9;                // slew axis stride of the cell table (odd: lanes of different cells spread)
 constexpr int kLk = 17;               // leakage stride of the cell table
 constexpr int kTotEvery = 16;         // items between flushes of a warp's per-lane totals
+constexpr uint32_t kChunk = 8;        // items a warp takes from the global counter at a time
 
 // Cell tables in shared memory (libraries of at most kSmemCells cells): per
 // cell the slew axis points 0..8 (+inf past ns - 2), an info word (ns - 1 |
@@ -58,7 +59,7 @@ constexpr int kTotEvery = 16;         // items between flushes of a warp's per-l
 constexpr size_t kCellsB =
     (size_t)kSmemCells * kAx * 4 + (size_t)kSmemCells * 4 + (size_t)kSmemCells * 8 * 8 + (size_t)kSmemCells * kLk * 4;
 
-// Per gate of the warp's current item.
+// Per gate of the warp's current item (read by an event as two 16-byte words).
 struct __align__(16) CSlot {
   uint16_t st[kMaxK + 2];    // staged start of pins 0..k; st[k + 1] = end
   uint8_t k, init, j, pre;   // inputs, initial input bits, load-axis interval, parity of earlier events per pin
@@ -67,18 +68,36 @@ struct __align__(16) CSlot {
 };
 static_assert(sizeof(CSlot) == 32, "slot size");
 
-// Per pin of a piece's current window.
+// Per pin of a piece's current window: the events taken in this window (a
+// prefix of the pin's staged run) and the pin's event before the window.
 struct HWin {
-  uint16_t np[kMaxK + 1];    // events of the pin taken in this window
+  uint16_t take[kMaxK + 1];
   uint8_t hp[kMaxK + 1];     // the pin has an event before the window
   float pt[kMaxK + 1], ps[kMaxK + 1];  // that event's time and slew
-  uint64_t src[kMaxK + 1];   // global index of the window's first staged event of the pin
 };
 
-constexpr size_t kWarpB = (size_t)kStCap * 4 * 2 + kStCap + sizeof(CSlot) * kCsrGates + 128;
-static_assert(sizeof(HWin) <= 128, "window record");
-static_assert(kWarpB % 16 == 0 && kCellsB % 16 == 0, "alignment");
-constexpr size_t kSmemB = kCellsB + (size_t)kCW * kWarpB;
+// A light tile's map from staged event to (slot, pin): a bit per event that
+// starts a pin's run, and per run (the tile's non-empty pins in order) its
+// slot << 3 | pin.
+constexpr int kSegWords = (kStCap + 31) / 32;
+constexpr int kSegMax = kCsrGates * (kMaxK + 1);
+struct TSeg {
+  uint32_t bits[kSegWords];
+  uint8_t run[kSegMax];
+};
+
+// One warp's shared memory.
+struct __align__(16) WarpBuf {
+  float ts[kStCap], ss[kStCap];   // staged times (ns) and slews (ps)
+  uint8_t tg[kStCap];             // staged event -> slot << 3 | pin
+  uint16_t mg[2][kStCap];         // a window's merges: staged indices in (time, pin) order
+  CSlot slot[kCsrGates];
+  HWin hw;
+  TSeg seg;
+};
+static_assert(kCellsB % 16 == 0 && sizeof(WarpBuf) % 16 == 0, "alignment");
+static_assert(kCsrWin + 2 * (kMaxK + 1) <= (uint32_t)kStCap && kCsrMaxTileHeavy + 4 <= (uint32_t)kStCap, "stage");
+constexpr size_t kSmemB = kCellsB + (size_t)kCW * sizeof(WarpBuf);
 static_assert(kSmemB + 1024 <= 227 * 1024, "shared memory budget");
 
 struct CTab {
@@ -140,6 +159,13 @@ __device__ __forceinline__ int lower_bound_f(const float* a, int n, float x) {
   return lo;
 }
 
+// Staged start of pin q (0..k + 1) from the slot's first 16 bytes.
+__device__ __forceinline__ int st_of(const uint4& A, int q) {
+  const uint32_t w = q < 2 ? A.x : (q < 4 ? A.y : A.z);
+  return (int)((w >> ((q & 1) * 16)) & 0xFFFFu);
+}
+
+
 // Gate g's slot: cell, inputs, initial bits, load-axis interval and
 // fraction, switching energy; pin starts relative to `base` (light tiles).
 __device__ __forceinline__ void fill_slot(const RunArgs& a, CSlot& S, uint32_t g, uint64_t base, bool starts) {
@@ -160,79 +186,248 @@ __device__ __forceinline__ void fill_slot(const RunArgs& a, CSlot& S, uint32_t g
   S.esw = a.half_vdd2 * C;
 }
 
-// One event: staged index i of pin p of slot S; (has_prev, tp, *spp) the
-// pin's previous event (time; slew, read only for a glitch).
-template <bool kPow2>
-__device__ __forceinline__ void csr_event(const RunArgs& a, const CTab& CT, const float* ts, const float* ss,
-                                          const CSlot& S, int p, int i, bool has_prev, float tp, const float* spp,
-                                          Acc& acc) {
-  const float t = ts[i], s = ss[i];
-  const float T = a.t_clk;
-  const uint32_t c = cyc<kPow2>(t, T, a.inv_t_clk);
-  const bool glitch = has_prev && cyc<kPow2>(tp, T, a.inv_t_clk) == c;
-  const int k = S.k;
-  float e_int = 0.f, e_sw = 0.f, dp = 0.f;
-  if (p == k) {
-    e_sw = S.esw;
-  } else {
-    // own pin: value before this event = initial value flipped per earlier event
-    const int idx = i - (int)S.st[p];
-    uint32_t s_pre = (uint32_t)S.init ^ (((((uint32_t)S.pre >> p) ^ (uint32_t)idx) & 1u) << p);
-    uint32_t s_b = s_pre;  // state just before this event in (time, pin) order
-    for (int q = 0; q < k; ++q) {
-      if (q == p) continue;
-      const int qa = S.st[q], qn = (int)S.st[q + 1] - qa;
-      const int r = lower_bound_f(ts + qa, qn, t);
-      const bool eq = r < qn && ts[qa + r] == t;
-      const uint32_t par = (((uint32_t)S.pre >> q) ^ (uint32_t)r) & 1u;
-      s_pre ^= par << q;
-      s_b ^= ((par ^ (uint32_t)(q < p && eq)) & 1u) << q;
-    }
-    const uint32_t cell = S.cell;
-    const uint32_t info = CT.info[cell];  // ns - 1 | (nl - 1) << 8 | patch offset << 16
-    // slew interval: the number of axis points 1 .. ns - 2 that are <= s
-    const float* axs = CT.sax + cell * kAx;
-    int lis = s >= axs[4] ? 4 : 0;
-    lis += s >= axs[lis + 2] ? 2 : 0;
-    lis += s >= axs[lis + 1] ? 1 : 0;
-    const float2 ax = CT.sxp[cell * 8 + lis];
-    const float u = (s - ax.x) * ax.y;
-    // corners {L[i][j], L[i][j+1], L[i+1][j], L[i+1][j+1]} of the state's table
-    const float4 P = __ldg(a.patch + (info >> 16) +
-                           ((int)s_pre * (int)(info & 0xFFu) + lis) * (int)((info >> 8) & 0xFFu) + S.j);
-    const float r0 = fmaf(S.v, P.y - P.x, P.x), r1 = fmaf(S.v, P.w - P.z, P.z);
-    e_int = fmaf(u, r1 - r0, r0);
-    const float* lk = CT.leak + cell * kLk;
-    dp = lk[s_b ^ (1u << p)] - lk[s_b];
-  }
-  const float e_dyn = e_int + e_sw;
-  float e_w;
-  if (glitch) {
-    // r_gl = min(1, x / y), IEEE division; x >= y gives 1 without dividing
-    const float x = 2000.f * (t - tp), y = s + *spp;
-    const float r = x < y ? __fdiv_rn(x, y) : 1.f;
-    e_w = r * e_dyn;
-    acc.e_gl += e_w;
-  } else {
-    acc.e_int += e_int;
-    acc.e_sw += e_sw;
-    e_w = e_dyn;
-  }
-  if (p < k) {
-    const float rem = fmaf(-(float)c, T, t);  // t - c T: the step's part inside its own cycle
-    e_w = fmaf(dp, T - rem, e_w);
-    kahan_add(acc.e_lk, acc.c_lk, dp * (a.t_max_f - t));
-  }
+__device__ __forceinline__ void commit(const RunArgs& a, uint32_t c, float e_w, float dp, bool glitch) {
   float* bin = reinterpret_cast<float*>(a.bins + c);
+  // one 16-byte reduction per event: energy, leakage step, event and glitch counts
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(bin), "f"(e_w), "f"(dp), "f"(1.0f),
                "f"(glitch ? 1.0f : 0.0f)
                : "memory");
 }
 
+// The glitch ratio of an event at t (slew s) whose previous event on the pin
+// is at tp (slew sp): r_gl = min(1, x / y), IEEE division; x >= y gives 1
+// without dividing.
+__device__ __forceinline__ float glitch_ratio(float t, float s, float tp, float sp) {
+  const float x = 2000.f * (t - tp), y = s + sp;
+  return x < y ? __fdiv_rn(x, y) : 1.f;
+}
+
+// An output-pin event at staged index i (has_prev: the pin's previous event
+// is at tp, slew *spp).
+template <bool kPow2>
+__device__ __forceinline__ void out_event(const RunArgs& a, const float* ts, const float* ss, const uint4& B, int i,
+                                          bool has_prev, float tp, const float* spp, Acc& acc) {
+  const float t = ts[i];
+  const float T = a.t_clk;
+  const uint32_t c = cyc<kPow2>(t, T, a.inv_t_clk);
+  const bool glitch = has_prev && cyc<kPow2>(tp, T, a.inv_t_clk) == c;
+  const float e_sw = __uint_as_float(B.z);
+  float e_w = e_sw;
+  if (glitch) {
+    e_w = glitch_ratio(t, ss[i], tp, *spp) * e_sw;
+    acc.e_gl += e_w;
+  } else {
+    acc.e_sw += e_sw;
+  }
+  commit(a, c, e_w, 0.f, glitch);
+}
+
+// An input-pin event at staged index i of pin p, with its states: s_pre
+// before its timestamp (selects the table), s_b just before it in (time, pin)
+// order (the leakage step's base).
+template <bool kPow2>
+__device__ __forceinline__ void in_event(const RunArgs& a, const CTab& CT, const float* ts, const float* ss,
+                                         const uint4& A, const uint4& B, int i, int p, uint32_t s_pre, uint32_t s_b,
+                                         bool has_prev, float tp, const float* spp, Acc& acc) {
+  const float t = ts[i], s = ss[i];
+  const float T = a.t_clk;
+  const uint32_t c = cyc<kPow2>(t, T, a.inv_t_clk);
+  const bool glitch = has_prev && cyc<kPow2>(tp, T, a.inv_t_clk) == c;
+  const uint32_t cell = B.x & 0xFFFFu;
+  const uint32_t info = CT.info[cell];  // ns - 1 | (nl - 1) << 8 | patch offset << 16
+  // slew interval: the number of axis points 1 .. ns - 2 that are <= s
+  const float* axs = CT.sax + cell * kAx;
+  int lis = s >= axs[4] ? 4 : 0;
+  lis += s >= axs[lis + 2] ? 2 : 0;
+  lis += s >= axs[lis + 1] ? 1 : 0;
+  const float2 ax = CT.sxp[cell * 8 + lis];
+  const float u = (s - ax.x) * ax.y;
+  // corners {L[i][j], L[i][j+1], L[i+1][j], L[i+1][j+1]} of the state's table
+  const float4 P = __ldg(a.patch + (info >> 16) +
+                         ((int)s_pre * (int)(info & 0xFFu) + lis) * (int)((info >> 8) & 0xFFu) +
+                         (int)((A.w >> 16) & 0xFFu));
+  const float v = __uint_as_float(B.y);
+  const float r0 = fmaf(v, P.y - P.x, P.x), r1 = fmaf(v, P.w - P.z, P.z);
+  const float e_int = fmaf(u, r1 - r0, r0);
+  const float* lk = CT.leak + cell * kLk;
+  const float dp = lk[s_b ^ (1u << p)] - lk[s_b];
+  float e_w = e_int;
+  if (glitch) {
+    e_w = glitch_ratio(t, s, tp, *spp) * e_int;
+    acc.e_gl += e_w;
+  } else {
+    acc.e_int += e_int;
+  }
+  const float rem = fmaf(-(float)c, T, t);  // t - c T: the step's part inside its own cycle
+  e_w = fmaf(dp, T - rem, e_w);
+  kahan_add(acc.e_lk, acc.c_lk, dp * (a.t_max_f - t));
+  commit(a, c, e_w, dp, glitch);
+}
+
+// The pin's previous event for staged event i (index idx in the pin's
+// staged run): the staged one before it, or, for the first of a window, the
+// one before the window (pieces; light gates are staged whole).
+__device__ __forceinline__ void prev_event(const WarpBuf& W, const float* ts, const float* ss, int i, int idx, int p,
+                                           bool window, bool& has_prev, float& tp, const float*& spp) {
+  if (idx > 0) {
+    has_prev = true;
+    tp = ts[i - 1];
+    spp = ss + i - 1;
+  } else {
+    has_prev = window && W.hw.hp[p] != 0;
+    tp = W.hw.pt[p];
+    spp = &W.hw.ps[p];
+  }
+}
+
+// One merge of two runs of staged events, each in (time, pin) order, all
+// pins of run a below all pins of run b (so a tie in time takes a first):
+// run x is the staged indices xb[0, nx) or, with xb null, x0 .. x0 + nx - 1.
+// Merge path: lane l writes the outputs [d0, d1) of an even split, starting
+// from the cut found by a binary search along its first diagonal, then
+// merging sequentially (no divergence: every lane does the same steps).
+__device__ __forceinline__ void merge_runs(const float* ts, const uint16_t* ab, int a0, int na, const uint16_t* bb,
+                                           int b0, int nb, uint16_t* out) {
+  const int lane = threadIdx.x & 31;
+  const int n = na + nb;
+  const int per = (n + 31) >> 5;
+  const int d0 = min(n, lane * per), d1 = min(n, d0 + per);
+  int lo = max(0, d0 - nb), hi = min(d0, na);
+  while (lo < hi) {  // the number of a's among the first d0 outputs
+    const int mid = (lo + hi) >> 1;
+    const int ia = ab ? ab[mid] : a0 + mid, ib = bb ? bb[d0 - mid - 1] : b0 + d0 - mid - 1;
+    if (ts[ia] <= ts[ib]) lo = mid + 1;
+    else hi = mid;
+  }
+  int i = lo, j = d0 - lo;
+  for (int d = d0; d < d1; ++d) {
+    const int ia = i < na ? (ab ? ab[i] : a0 + i) : -1;
+    const int ib = j < nb ? (bb ? bb[j] : b0 + j) : -1;
+    const bool take_a = ib < 0 || (ia >= 0 && ts[ia] <= ts[ib]);
+    out[d] = (uint16_t)(take_a ? ia : ib);
+    i += take_a ? 1 : 0;
+    j += take_a ? 0 : 1;
+  }
+}
+
+// A piece's window step (gate slot 0, the taken events of each pin a prefix
+// of its staged run): output events one lane each; input events merged in
+// (time, pin) order (pairwise merges of the pins' runs), then computed in
+// that order with their states from a prefix XOR of pin bits (from the gate's
+// state at the window start), the pre-timestamp state taking back out the
+// lower pins' events at the same time.
+template <bool kPow2>
+__device__ __forceinline__ void window_step(const RunArgs& a, const CTab& CT, WarpBuf& W, Acc& acc) {
+  const int lane = threadIdx.x & 31;
+  const float* ts = W.ts;
+  const float* ss = W.ss;
+  const uint4 A = reinterpret_cast<const uint4*>(&W.slot[0])[0];
+  const uint4 B = reinterpret_cast<const uint4*>(&W.slot[0])[1];
+  const int k = (int)(A.w & 0xFFu);
+  // output events
+  {
+    const int o0 = st_of(A, k), on = W.hw.take[k];
+    for (int x = lane; x < on; x += 32) {
+      const int i = o0 + x;
+      bool hp;
+      float tp;
+      const float* spp;
+      prev_event(W, ts, ss, i, x, k, true, hp, tp, spp);
+      out_event<kPow2>(a, ts, ss, B, i, hp, tp, spp, acc);
+    }
+  }
+  // the merge of the input pins' runs
+  const int n0 = W.hw.take[0], n1 = k > 1 ? W.hw.take[1] : 0, n2 = k > 2 ? W.hw.take[2] : 0,
+            n3 = k > 3 ? W.hw.take[3] : 0;
+  const int s0 = st_of(A, 0), s1 = st_of(A, 1), s2 = st_of(A, 2), s3 = st_of(A, 3);
+  const int nin = n0 + n1 + n2 + n3;
+  const uint16_t* mrg = nullptr;  // null: pin 0's run is the merge (k = 1)
+  if (k >= 2) {
+    merge_runs(ts, nullptr, s0, n0, nullptr, s1, n1, W.mg[0]);
+    mrg = W.mg[0];
+    if (k == 3) {
+      __syncwarp();
+      merge_runs(ts, W.mg[0], 0, n0 + n1, nullptr, s2, n2, W.mg[1]);
+      mrg = W.mg[1];
+    } else if (k == 4) {
+      merge_runs(ts, nullptr, s2, n2, nullptr, s3, n3, W.mg[0] + n0 + n1);
+      __syncwarp();
+      merge_runs(ts, W.mg[0], 0, n0 + n1, W.mg[0] + n0 + n1, 0, n2 + n3, W.mg[1]);
+      mrg = W.mg[1];
+    }
+  }
+  __syncwarp();
+  const uint32_t kmask = (1u << k) - 1u;
+  const uint32_t start = (((A.w >> 8) & 0xFFu) ^ (A.w >> 24)) & kmask;  // initial bits ^ parities before the window
+  uint32_t carry = 0;
+  for (int m0 = 0; m0 < nin; m0 += 32) {
+    const int m = m0 + lane;
+    const bool valid = m < nin;
+    const int i = valid ? (mrg ? (int)mrg[m] : s0 + m) : 0;
+    const int p = (int)(W.tg[i] & 7u);
+    const uint32_t x = valid ? 1u << p : 0u;
+    uint32_t v = x;  // inclusive XOR over the merged order
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, v, d);
+      if (lane >= d) v ^= y;
+    }
+    v ^= carry;
+    carry = __shfl_sync(0xffffffffu, v, 31);
+    if (!valid) continue;
+    const uint32_t s_b = start ^ v ^ x;
+    uint32_t s_pre = s_b;
+    const float t = ts[i];
+    for (int j = m - 1; j >= 0; --j) {  // lower pins' events at the same time
+      const int e = mrg ? (int)mrg[j] : s0 + j;
+      if (ts[e] != t) break;
+      s_pre ^= 1u << (W.tg[e] & 7u);
+    }
+    bool hp;
+    float tp;
+    const float* spp;
+    prev_event(W, ts, ss, i, i - st_of(A, p), p, true, hp, tp, spp);
+    in_event<kPow2>(a, CT, ts, ss, A, B, i, p, s_pre, s_b, hp, tp, spp, acc);
+  }
+  __syncwarp();  // the stage is read before it is refilled
+}
+
+// A light tile's event at staged index e (slot S, pin p): the input state
+// before the event's timestamp from the parities of each input pin's earlier
+// events (the count on another pin a binary search of t in its staged run;
+// simultaneous events on lower pins are taken back out for the leakage base).
+template <bool kPow2>
+__device__ __forceinline__ void tile_event(const RunArgs& a, const CTab& CT, const float* ts, const float* ss,
+                                           const CSlot& S, int p, int e, Acc& acc) {
+  const uint4 A = reinterpret_cast<const uint4*>(&S)[0];
+  const uint4 B = reinterpret_cast<const uint4*>(&S)[1];
+  const int k = (int)(A.w & 0xFFu);
+  const int idx = e - st_of(A, p);
+  const bool hp = idx > 0;  // light gates are staged whole: the pin's previous event is staged
+  const float tp = hp ? ts[e - 1] : 0.f;
+  if (p == k) {
+    out_event<kPow2>(a, ts, ss, B, e, hp, tp, ss + e - 1, acc);
+    return;
+  }
+  const uint32_t init = (A.w >> 8) & 0xFFu;
+  uint32_t s_pre = init ^ (((uint32_t)idx & 1u) << p);
+  uint32_t s_b = s_pre;  // state just before this event in (time, pin) order
+  const float t = ts[e];
+  for (int q = 0; q < k; ++q) {
+    if (q == p) continue;
+    const int qa = st_of(A, q), qn = st_of(A, q + 1) - qa;
+    const int r = lower_bound_f(ts + qa, qn, t);
+    const bool eq = r < qn && ts[qa + r] == t;
+    const uint32_t par = (uint32_t)r & 1u;
+    s_pre ^= par << q;
+    s_b ^= ((par ^ (uint32_t)(q < p && eq)) & 1u) << q;
+  }
+  in_event<kPow2>(a, CT, ts, ss, A, B, e, p, s_pre, s_b, hp, tp, ss + e - 1, acc);
+}
+
 // A light tile: consecutive whole gates, staged whole.
 template <bool kPow2>
-__device__ __forceinline__ void csr_tile(const RunArgs& a, const CTab& CT, uint32_t ti, float* ts0, float* ss0,
-                                         uint8_t* tg, CSlot* slots, Acc& acc) {
+__device__ __forceinline__ void csr_tile(const RunArgs& a, const CTab& CT, uint32_t ti, WarpBuf& W, Acc& acc) {
   const int lane = threadIdx.x & 31;
   const Tile tl = a.tiles[ti];
   const uint32_t ng = tl.ge - tl.gb;
@@ -240,7 +435,7 @@ __device__ __forceinline__ void csr_tile(const RunArgs& a, const CTab& CT, uint3
     if (lane == 0) dev_err(a.err, tl.gb, kErrTileOverflow);
     return;
   }
-  const uint64_t ea = a.gate_off[tl.gb], eb = a.gate_off[tl.ge];
+  const uint64_t ea = a.tile_ev[2 * ti], eb = a.tile_ev[2 * ti + 1];  // its events, from the partition
   if (eb < ea || eb - ea > (uint64_t)(kStCap - 4)) {
     if (lane == 0) dev_err(a.err, tl.gb, kErrTileOverflow);
     return;
@@ -248,44 +443,66 @@ __device__ __forceinline__ void csr_tile(const RunArgs& a, const CTab& CT, uint3
   const int n = (int)(eb - ea);
   if (n == 0) return;
   // times and slews [ea, eb) with 16-byte loads from ea rounded down (the
-  // event arrays are padded past their end)
+  // event arrays are padded past their end): staged event i is at W.ts[off + i]
   const uint64_t e4 = ea & ~3ull;
   const int off = (int)(ea - e4), nv = (off + n + 3) >> 2;
   const float4* t4 = reinterpret_cast<const float4*>(a.t + e4);
   const float4* s4 = reinterpret_cast<const float4*>(a.s + e4);
   for (int v = lane; v < nv; v += 32) {
-    reinterpret_cast<float4*>(ts0)[v] = __ldg(t4 + v);
-    reinterpret_cast<float4*>(ss0)[v] = __ldg(s4 + v);
+    reinterpret_cast<float4*>(W.ts)[v] = __ldg(t4 + v);
+    reinterpret_cast<float4*>(W.ss)[v] = __ldg(s4 + v);
   }
-  if (lane < (int)ng) fill_slot(a, slots[lane], tl.gb + (uint32_t)lane, ea, true);
+  if (lane < kSegWords) W.seg.bits[lane] = 0u;
+  // a lane per gate: its slot, then its non-empty pins' runs
+  uint32_t runs = 0, nonempty = 0;
+  if (lane < (int)ng) {
+    CSlot& S = W.slot[lane];
+    fill_slot(a, S, tl.gb + (uint32_t)lane, ea, true);
+    for (int p = 0; p <= S.k; ++p)
+      if (S.st[p + 1] > S.st[p]) {
+        nonempty |= 1u << p;
+        ++runs;
+      }
+  }
+  uint32_t rbase = runs;  // exclusive scan of the gates' run counts
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, rbase, d);
+    if (lane >= d) rbase += y;
+  }
+  rbase -= runs;
+  __syncwarp();  // bits cleared
+  if (lane < (int)ng) {
+    const CSlot& S = W.slot[lane];
+    for (int p = 0; p <= S.k; ++p)
+      if ((nonempty >> p) & 1u) {
+        const int e = S.st[p];
+        atomicOr(&W.seg.bits[e >> 5], 1u << (e & 31));
+        W.seg.run[rbase++] = (uint8_t)((lane << 3) | p);
+      }
+  }
   __syncwarp();
-  const float* ts = ts0 + off;
-  const float* ss = ss0 + off;
-  // tags: slot << 3 | pin
-  for (uint32_t gi = 0; gi < ng; ++gi) {
-    const CSlot& S = slots[gi];
-    const int k = S.k;
-    for (int e = (int)S.st[0] + lane; e < (int)S.st[k + 1]; e += 32) {
-      int p = 0;
-      for (int q = 1; q <= k; ++q) p += (e >= (int)S.st[q]) ? 1 : 0;
-      tg[e] = (uint8_t)((gi << 3) | (uint32_t)p);
+  // one lane per event; the event's run is the number of run starts at or
+  // before it, minus one
+  const float* ts = W.ts + off;  // staged event i: time ts[i], slew ss[i]
+  const float* ss = W.ss + off;
+  int carry = 0;
+  const uint32_t le = 0xFFFFFFFFu >> (31 - lane);  // lanes <= this one
+  for (int e0 = 0; e0 < n; e0 += 32) {
+    const uint32_t word = W.seg.bits[e0 >> 5];
+    const int e = e0 + lane;
+    if (e < n) {
+      const uint32_t w = W.seg.run[carry + __popc(word & le) - 1];
+      tile_event<kPow2>(a, CT, ts, ss, W.slot[w >> 3], (int)(w & 7u), e, acc);
     }
-  }
-  __syncwarp();
-  for (int e = lane; e < n; e += 32) {
-    const uint32_t w = tg[e];
-    const CSlot& S = slots[w >> 3];
-    const int p = (int)(w & 7u);
-    const bool hp = e > (int)S.st[p];  // light gates are whole: the pin's previous event is staged
-    csr_event<kPow2>(a, CT, ts, ss, S, p, e, hp, hp ? ts[e - 1] : 0.f, ss + e - 1, acc);
+    carry += __popc(word);
   }
   __syncwarp();  // the stage is read before the next item overwrites it
 }
 
 // A piece of a heavy gate, in windows of at most kCsrWin events.
 template <bool kPow2>
-__device__ __forceinline__ void csr_piece(const RunArgs& a, const CTab& CT, uint32_t pi, float* ts, float* ss,
-                                          uint8_t* tg, CSlot& S, HWin& hw, Acc& acc) {
+__device__ __forceinline__ void csr_piece(const RunArgs& a, const CTab& CT, uint32_t pi, WarpBuf& W, Acc& acc) {
   const int lane = threadIdx.x & 31;
   const Piece& P = a.pieces[pi];
   const uint32_t g = P.gate, pidx = P.idx;
@@ -311,6 +528,7 @@ __device__ __forceinline__ void csr_piece(const RunArgs& a, const CTab& CT, uint
       psv = a.s[pst + cur - 1];
     }
   }
+  CSlot& S = W.slot[0];
   if (lane == 0) fill_slot(a, S, g, 0, false);
   for (int guard = 0;; ++guard) {
     const uint32_t rem = mine ? hi - cur : 0u;
@@ -321,58 +539,62 @@ __device__ __forceinline__ void csr_piece(const RunArgs& a, const CTab& CT, uint
       const uint64_t sh = (uint64_t)kCsrWin * rem / R;
       share = sh < 1 ? 1u : (sh > rem ? rem : (uint32_t)sh);
     }
-    uint32_t incl = share;  // prefix over lanes 0..k
+    // a pin's share is staged with the pin's next event after it, whose time
+    // bounds the window (the pins' runs are st .. st + share, then that event)
+    const bool more = mine && cur + share < hi;
+    const uint32_t ns_ = share + (more ? 1u : 0u);
+    uint32_t incl = ns_;  // prefix over lanes 0..k
 #pragma unroll
     for (int d = 1; d <= 4; d <<= 1) {
       const uint32_t y = __shfl_up_sync(0xffffffffu, incl, d);
       if (lane >= d) incl += y;
     }
-    const uint32_t st = incl - share;
+    const uint32_t st = incl - ns_;
     const int nw = (int)__shfl_sync(0xffffffffu, incl, k);
-    // the first unstaged event of each pin bounds the window (+inf: none left)
-    float bound = FLT_MAX;
-    if (mine && cur + share < hi) bound = a.t[pst + cur + share];
-    const bool bounded = __any_sync(0xffffffffu, mine && cur + share < hi);
-    const float hz = __uint_as_float(__reduce_min_sync(0xffffffffu, __float_as_uint(bound)));  // t >= 0
+    const bool bounded = __any_sync(0xffffffffu, more);
     if (mine) {
       S.st[lane] = (uint16_t)st;
-      hw.src[lane] = pst + cur;
-      hw.hp[lane] = (uint8_t)hp;
-      hw.pt[lane] = ptv;
-      hw.ps[lane] = psv;
+      W.hw.hp[lane] = (uint8_t)hp;
+      W.hw.pt[lane] = ptv;
+      W.hw.ps[lane] = psv;
     }
     if (lane == 0) S.st[k + 1] = (uint16_t)nw;
     const uint32_t pre = __ballot_sync(0xffffffffu, mine && (cur & 1u)) & 31u;
     if (lane == 0) S.pre = (uint8_t)pre;
-    __syncwarp();
-    for (int i = lane; i < nw; i += 32) {
-      int p = 0;
-      for (int q = 1; q <= k; ++q) p += (i >= (int)S.st[q]) ? 1 : 0;
-      const uint64_t src = hw.src[p] + (uint64_t)(i - (int)S.st[p]);
-      ts[i] = a.t[src];
-      ss[i] = a.s[src];
-      tg[i] = (uint8_t)p;
+    // bring the pin's next window into L2 while this one is worked on (about
+    // the same share: the bytes from the pin's first unstaged event on)
+    if (mine && cur + share < hi) {
+      const uint64_t e = pst + cur + share;
+      const uint32_t nb = min(hi - (cur + share), share);
+      const uint64_t a0 = e & ~3ull;
+      const uint32_t bytes = (uint32_t)(((e + nb + 3) & ~3ull) - a0) * 4u;
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.t + a0), "r"(bytes) : "memory");
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.s + a0), "r"(bytes) : "memory");
+    }
+    // stage pin by pin (each pin's run is contiguous in the per-pin arrays)
+    for (int q = 0; q <= k; ++q) {
+      const uint32_t sq = __shfl_sync(0xffffffffu, st, q), nq = __shfl_sync(0xffffffffu, ns_, q);
+      const uint64_t src = __shfl_sync(0xffffffffu, pst + cur, q);
+      for (uint32_t i = (uint32_t)lane; i < nq; i += 32) {
+        W.ts[sq + i] = a.t[src + i];
+        W.ss[sq + i] = a.s[src + i];
+        W.tg[sq + i] = (uint8_t)q;
+      }
     }
     __syncwarp();
+    // the first unstaged event of each pin bounds the window
+    const float bound = more ? W.ts[st + share] : FLT_MAX;
+    const float hz = __uint_as_float(__reduce_min_sync(0xffffffffu, __float_as_uint(bound)));  // t >= 0
     // the events before the horizon are taken (a timestamp group is never split)
     uint32_t take = share;
-    if (mine && share > 0 && bounded) take = (uint32_t)lower_bound_f(ts + st, (int)share, hz);
-    if (mine) hw.np[lane] = (uint16_t)take;
+    if (mine && share > 0 && bounded) take = (uint32_t)lower_bound_f(W.ts + st, (int)share, hz);
+    if (mine) W.hw.take[lane] = (uint16_t)take;
     __syncwarp();
-    for (int i = lane; i < nw; i += 32) {
-      const int p = tg[i];
-      const int idx = i - (int)S.st[p];
-      if (idx >= (int)hw.np[p]) continue;
-      const bool has_prev = idx > 0 || hw.hp[p] != 0;
-      const float tp = idx > 0 ? ts[i - 1] : hw.pt[p];
-      const float* spp = idx > 0 ? ss + i - 1 : &hw.ps[p];
-      csr_event<kPow2>(a, CT, ts, ss, S, p, i, has_prev, tp, spp, acc);
-    }
-    __syncwarp();
+    window_step<kPow2>(a, CT, W, acc);
     if (mine && take > 0) {
       hp = true;
-      ptv = ts[st + take - 1];
-      psv = ss[st + take - 1];
+      ptv = W.ts[st + take - 1];
+      psv = W.ss[st + take - 1];
       cur += take;
     }
     const uint32_t moved = __reduce_add_sync(0xffffffffu, mine ? take : 0u);
@@ -393,12 +615,7 @@ __global__ void __launch_bounds__(kCT, 1) k_csr(const RunArgs a) {
   uint32_t* info = reinterpret_cast<uint32_t*>(sax + kSmemCells * kAx);
   float2* sxp = reinterpret_cast<float2*>(info + kSmemCells);
   float* lk = reinterpret_cast<float*>(sxp + kSmemCells * 8);
-  uint8_t* wb = smem + kCellsB + (size_t)warp * kWarpB;
-  float* ts = reinterpret_cast<float*>(wb);
-  float* ss = ts + kStCap;
-  uint8_t* tg = reinterpret_cast<uint8_t*>(ss + kStCap);
-  CSlot* slots = reinterpret_cast<CSlot*>(tg + kStCap);
-  HWin* hw = reinterpret_cast<HWin*>(slots + kCsrGates);
+  WarpBuf& W = reinterpret_cast<WarpBuf*>(smem + kCellsB)[warp];
   if (tid < 4) s_tot[tid] = 0.0;
   {  // cell tables (the kernel runs for libraries of at most kSmemCells cells)
     const uint32_t nc = min(a.n_cells, (uint32_t)kSmemCells);
@@ -421,19 +638,36 @@ __global__ void __launch_bounds__(kCT, 1) k_csr(const RunArgs a) {
   const uint32_t n_items = n_tiles + n_pieces;
   Acc acc{0.f, 0.f, 0.f, 0.f, 0.f};
   int since = 0;
-  for (;;) {
-    uint32_t item = 0;
-    if (lane == 0) item = atomicAdd(a.part_counts + 2, 1u);
-    item = __shfl_sync(0xffffffffu, item, 0);
-    if (item >= n_items) break;
-    if (item < n_pieces)  // the heavy gates' pieces first: the longest items
-      csr_piece<kPow2>(a, CT, item, ts, ss, tg, slots[0], *hw, acc);
-    else
-      csr_tile<kPow2>(a, CT, item - n_pieces, ts, ss, tg, slots, acc);
-    if (++since == kTotEvery) {
-      flush_acc(acc, s_tot);
-      since = 0;
+  // a warp takes kChunk items at a time (the heavy gates' pieces come first:
+  // the longest items); the next chunk is asked for as soon as one begins
+  uint32_t base = 0;
+  if (lane == 0) base = atomicAdd(a.part_counts + 2, kChunk);
+  base = __shfl_sync(0xffffffffu, base, 0);
+  while (base < n_items) {
+    uint32_t nbase = 0;
+    if (lane == 0) nbase = atomicAdd(a.part_counts + 2, kChunk);
+    // bring the chunk's later tiles' events into L2 while the first ones are worked on
+    if (lane >= 1 && lane < (int)kChunk && base + lane < n_items && base + lane >= n_pieces) {
+      const uint32_t ti = base + lane - n_pieces;
+      const uint64_t ea = a.tile_ev[2 * ti] & ~3ull, eb = (a.tile_ev[2 * ti + 1] + 3) & ~3ull;
+      if (eb > ea && eb - ea <= (uint64_t)kStCap) {
+        const uint32_t bytes = (uint32_t)(eb - ea) * 4u;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.t + ea), "r"(bytes) : "memory");
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.s + ea), "r"(bytes) : "memory");
+      }
     }
+    for (uint32_t j = 0; j < kChunk && base + j < n_items; ++j) {
+      const uint32_t item = base + j;
+      if (item < n_pieces)
+        csr_piece<kPow2>(a, CT, item, W, acc);
+      else
+        csr_tile<kPow2>(a, CT, item - n_pieces, W, acc);
+      if (++since == kTotEvery) {
+        flush_acc(acc, s_tot);
+        since = 0;
+      }
+    }
+    base = __shfl_sync(0xffffffffu, nbase, 0);
   }
   flush_acc(acc, s_tot);
   __syncthreads();
@@ -541,8 +775,14 @@ __global__ void __launch_bounds__(256) k_cp_emit(const RunArgs a) {
   const uint32_t th = a.part_blk[2 * blockIdx.x] + ea;
   const uint32_t tv = a.part_blk[2 * blockIdx.x + 1] + eb;
   if (g < a.n_gates) {
-    if (h) a.tiles[th].gb = g;
-    if (tail) a.tiles[th + h - 1].ge = g + 1;
+    if (h) {
+      a.tiles[th].gb = g;
+      a.tile_ev[2 * th] = a.gate_off[g];
+    }
+    if (tail) {
+      a.tiles[th + h - 1].ge = g + 1;
+      a.tile_ev[2 * (th + h - 1) + 1] = a.gate_off[g + 1];
+    }
     for (uint32_t i = 0; i < pc; ++i) {
       a.pieces[tv + i].gate = g;
       a.pieces[tv + i].idx = i;

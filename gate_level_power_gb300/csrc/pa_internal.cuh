@@ -106,6 +106,7 @@ struct RunArgs {
   Tile* tiles;
   uint32_t* heavy;
   Piece* pieces;           // heavy-gate pieces of the warp kernel (pa_csr.cu)
+  uint64_t* tile_ev;       // per light tile of the warp kernel: its first event and its end
   double* p0;              // sum of leakage of initial states, uW
   // accumulators: per cycle {W, D, ev, gl}
   //   W  energy in the cycle: dynamic + in-cycle leakage parts (fJ)
@@ -275,11 +276,11 @@ struct BandRunArgs {
 // event of the gate in a time interval. A warp works through a piece in
 // windows of at most kCsrWin events.
 constexpr uint32_t kCsrDefaultTile = 256;
-constexpr uint32_t kCsrDefaultHeavy = 256;
-constexpr uint32_t kCsrMaxTileHeavy = 512;  // tile_target + heavy_thresh a warp's stage holds
+constexpr uint32_t kCsrDefaultHeavy = 128;
+constexpr uint32_t kCsrMaxTileHeavy = 384;  // tile_target + heavy_thresh a warp's stage holds
 constexpr uint32_t kCsrGates = 32;          // gates per light tile (one lane per gate)
 constexpr uint32_t kCsrPiece = 2048;        // target events per piece of a heavy gate
-constexpr uint32_t kCsrWin = 512;           // events per window of a piece
+constexpr uint32_t kCsrWin = 384;           // events per window of a piece
 
 struct Piece {
   uint32_t gate, idx;          // the gate; the piece's index among the gate's pieces
