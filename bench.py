@@ -93,6 +93,11 @@ def parse_args():
     ap.add_argument("--oracle-single", action="store_true",
                     help="time the oracle on one host thread on configs 1..3 (bounded samples) and exit")
     ap.add_argument("--band-cycles", type=int, default=0, help="cycles per band (0 = library default)")
+    ap.add_argument("--tile-events", type=int, default=0,
+                    help="work partition knob: target events per light tile (0 = the library's default)")
+    ap.add_argument("--heavy-events", type=int, default=0,
+                    help="work partition knob: gates with more events are heavy (0 = the library's default); "
+                         "tile + heavy above 384 selects the CTA kernel (k_fused) instead of the warp kernel")
     ap.add_argument("--partition", choices=["events", "density", "fixed"], default="events",
                     help="work partition: the library's event-count partition (default) or the paper's "
                          "(gate, window) threads, event-density-aware or globally fixed")
@@ -424,7 +429,7 @@ def run_ours(args):
     out = dict(waveform=wave, event_count=evc, glitch_count=glc)
 
     part = dict(partition=args.partition, n_evt_tgt=args.n_evt_tgt, n_thr_floor=args.n_thr_floor,
-                n_cyc_fix=args.n_cyc_fix)
+                n_cyc_fix=args.n_cyc_fix, tile_events=args.tile_events, heavy_events=args.heavy_events)
 
     def step(timing=False):
         return pa.run(w.vdd, w.t_clk_ns, N, out=out, timing=timing, **part)
