@@ -664,7 +664,7 @@ def partition_sweep(args, pa, w, out, dist, rank):
             work = {"threads": s["part_threads"],
                     "events_per_thread": dict(zip(("p50", "p90", "p99", "max"), s["part_evt"]))}
         else:
-            work = {"path": "banded" if s["path"] == 1 else "unbanded", "work_items": s["n_tiles"],
+            work = {"path": {1: "banded", 3: "unbanded, warp kernel"}.get(s["path"], "unbanded"), "work_items": s["n_tiles"],
                     "heavy_items": s["n_heavy"]}
         if rank == 0:
             print(json.dumps({
