@@ -538,6 +538,26 @@ def run_ours(args):
             e2e_paths[path] = world * E * args.e2e_steps / e2e_s
             e2e_step_ms[path] = step_ms
         e2e_value = max(e2e_paths.values())
+        # the same bytes copied host -> device by a plain pinned-memory copy
+        # (torch, no library code), the same number of times: the copies'
+        # own step times, so that slow steps of the one-shot paths can be
+        # told apart from slow steps of the host link
+        dt = torch.empty(E, dtype=torch.float32, device=local)
+        ds = torch.empty(E, dtype=torch.float32, device=local)
+        dv = torch.empty(E, dtype=torch.uint8, device=local)
+        ht, hs, hv = torch.from_numpy(w.t_ns), torch.from_numpy(w.slew_ps), torch.from_numpy(w.value)
+        copy_ms = []
+        for _ in range(args.e2e_steps + 2):
+            torch.cuda.synchronize()
+            ts = time.perf_counter()
+            with torch.cuda.stream(stream):
+                dt.copy_(ht, non_blocking=True)
+                ds.copy_(hs, non_blocking=True)
+                dv.copy_(hv, non_blocking=True)
+            stream.synchronize()
+            copy_ms.append(round((time.perf_counter() - ts) * 1e3, 2))
+        copy_ms = copy_ms[2:]
+        del dt, ds, dv
     # ---- roofline of the fused kernel of the timed pass
     fused_mean = statistics.mean(fused_ms)
     fused_med = statistics.median(fused_ms)
@@ -585,6 +605,9 @@ def run_ours(args):
             "e2e": None if e2e_value is None else {"value": e2e_value, "unit": "events/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": args.e2e_steps, "paths": e2e_paths,
                     "step_ms": e2e_step_ms,
+                    "plain_copy_step_ms": copy_ms,
+                    "plain_copy_note": "the steps' event bytes (times, slews, values) copied host -> device by a "
+                                       "plain pinned-memory copy after the paths, for comparison",
                     "paths_at_median_step": {k: world * E / (statistics.median(v) * 1e-3)
                                              for k, v in e2e_step_ms.items() if v},
                     "note": "per step from pinned host memory: pa_run_stream (chunked copies overlapping "
