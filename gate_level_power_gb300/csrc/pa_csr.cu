@@ -159,6 +159,23 @@ __device__ __forceinline__ int lower_bound_f(const float* a, int n, float x) {
   return lo;
 }
 
+// Asynchronous global -> shared copies (cp.async: no register round trip, so
+// a lane's copies are all in flight at once); each lane waits for its own
+// before the warp syncs.
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void copy4_async(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void copy16_async(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void copies_wait() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 // Staged start of pin q (0..k + 1) from the slot's first 16 bytes.
 __device__ __forceinline__ int st_of(const uint4& A, int q) {
   const uint32_t w = q < 2 ? A.x : (q < 4 ? A.y : A.z);
@@ -172,15 +189,23 @@ __device__ __forceinline__ void fill_slot(const RunArgs& a, CSlot& S, uint32_t g
   const GateRec r = a.gates[g];
   const int k = (int)((r.init >> 16) & 0xff);
   const CellDesc& cd = a.cells[r.cell];
-  if (starts)
-    for (int p = 0; p <= k + 1; ++p) S.st[p] = (uint16_t)(a.pin_off[r.pin_base + p] - base);
+  if (starts) {  // the gate's pin offsets, all loads issued before any use
+    uint64_t po[kMaxK + 2];
+#pragma unroll
+    for (int p = 0; p < kMaxK + 2; ++p) po[p] = p <= k + 1 ? a.pin_off[r.pin_base + p] : 0ull;
+#pragma unroll
+    for (int p = 0; p < kMaxK + 2; ++p)
+      if (p <= k + 1) S.st[p] = (uint16_t)(po[p] - base);
+  }
   S.k = (uint8_t)k;
   S.init = (uint8_t)(r.init & 0xffu);
   S.pre = 0;
   S.cell = (uint16_t)r.cell;
   const float C = r.load;
+  const int nl = cd.nl;
   int j = 0;
-  for (int m = 1; m <= cd.nl - 2; ++m) j += (C >= cd.lax[m]) ? 1 : 0;
+#pragma unroll
+  for (int m = 1; m <= PA_MAX_AXIS - 2; ++m) j += (m <= nl - 2 && C >= cd.lax[m]) ? 1 : 0;
   S.j = (uint8_t)j;
   S.v = (C - cd.lax[j]) * cd.ilax[j];
   S.esw = a.half_vdd2 * C;
@@ -448,9 +473,9 @@ __device__ __forceinline__ void csr_tile(const RunArgs& a, const CTab& CT, uint3
   const int off = (int)(ea - e4), nv = (off + n + 3) >> 2;
   const float4* t4 = reinterpret_cast<const float4*>(a.t + e4);
   const float4* s4 = reinterpret_cast<const float4*>(a.s + e4);
-  for (int v = lane; v < nv; v += 32) {
-    reinterpret_cast<float4*>(W.ts)[v] = __ldg(t4 + v);
-    reinterpret_cast<float4*>(W.ss)[v] = __ldg(s4 + v);
+  for (int v = lane; v < nv; v += 32) {  // in flight while the gates' slots are filled
+    copy16_async(reinterpret_cast<float4*>(W.ts) + v, t4 + v);
+    copy16_async(reinterpret_cast<float4*>(W.ss) + v, s4 + v);
   }
   if (lane < kSegWords) W.seg.bits[lane] = 0u;
   // a lane per gate: its slot, then its non-empty pins' runs
@@ -481,6 +506,8 @@ __device__ __forceinline__ void csr_tile(const RunArgs& a, const CTab& CT, uint3
         W.seg.run[rbase++] = (uint8_t)((lane << 3) | p);
       }
   }
+  __syncwarp();
+  copies_wait();
   __syncwarp();
   // one lane per event; the event's run is the number of run starts at or
   // before it, minus one
@@ -576,11 +603,12 @@ __device__ __forceinline__ void csr_piece(const RunArgs& a, const CTab& CT, uint
       const uint32_t sq = __shfl_sync(0xffffffffu, st, q), nq = __shfl_sync(0xffffffffu, ns_, q);
       const uint64_t src = __shfl_sync(0xffffffffu, pst + cur, q);
       for (uint32_t i = (uint32_t)lane; i < nq; i += 32) {
-        W.ts[sq + i] = a.t[src + i];
-        W.ss[sq + i] = a.s[src + i];
+        copy4_async(W.ts + sq + i, a.t + src + i);
+        copy4_async(W.ss + sq + i, a.s + src + i);
         W.tg[sq + i] = (uint8_t)q;
       }
     }
+    copies_wait();
     __syncwarp();
     // the first unstaged event of each pin bounds the window
     const float bound = more ? W.ts[st + share] : FLT_MAX;
