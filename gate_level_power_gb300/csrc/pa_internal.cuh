@@ -275,8 +275,8 @@ struct BandRunArgs {
 // split at the first event at or after that time, so a piece holds every
 // event of the gate in a time interval. A warp works through a piece in
 // windows of at most kCsrWin events.
-constexpr uint32_t kCsrDefaultTile = 256;
-constexpr uint32_t kCsrDefaultHeavy = 128;
+constexpr uint32_t kCsrDefaultTile = 320;
+constexpr uint32_t kCsrDefaultHeavy = 64;
 constexpr uint32_t kCsrMaxTileHeavy = 384;  // tile_target + heavy_thresh a warp's stage holds
 constexpr uint32_t kCsrGates = 32;          // gates per light tile (one lane per gate)
 constexpr uint32_t kCsrPiece = 2048;        // target events per piece of a heavy gate

@@ -188,8 +188,8 @@ typedef struct pa_events {
  *   t_max_ns       analysis window end for Eq. 3 and leakage; 0 -> n_cycles * t_clk;
  *                  otherwise it must be >= the latest event time
  *   tile_events    work partition: target events per light tile (0 = default:
- *                  256 for the warp kernel, 2048 for the CTA kernel)
- *   heavy_events   gates with more events than this are heavy (0 = default: 256
+ *                  320 for the warp kernel, 2048 for the CTA kernel)
+ *   heavy_events   gates with more events than this are heavy (0 = default: 64
  *                  / 2048): cut into time pieces of about 2048 events, each
  *                  worked through by one warp in windows (warp kernel), or
  *                  streamed in event-count windows by one CTA (CTA kernel);
@@ -198,7 +198,7 @@ typedef struct pa_events {
  *                  no per-event output (state_pre, lut_ij, is_glitch,
  *                  gate_power_w, cell_power_w, the alternative readings),
  *                  the library has at most 64 cells and tile_events +
- *                  heavy_events (defaults resolved) is at most 512; else the
+ *                  heavy_events (defaults resolved) is at most 384; else the
  *                  CTA kernel. pa_run_noalloc always takes the CTA kernel.
  *   flags          PA_RUN_* bits
  *   part_mode      PA_PART_* (pa_run only; the other entry points take
