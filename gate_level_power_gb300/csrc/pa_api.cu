@@ -211,6 +211,7 @@ struct RunPlan {
 // Device buffers of one run (owned by the ctx or by the no-alloc scratch).
 struct PassBufs {
   float4* bins = nullptr;
+  uint32_t n_rep = 1;        // copies of the f32 bins the buffer holds (the warp kernel's pass)
   uint32_t* part_blk = nullptr;
   uint32_t* part_counts = nullptr;
   Tile* tiles = nullptr;
@@ -346,6 +347,7 @@ RunArgs make_run_args(pa_ctx* c, const RunPlan& plan, const PassBufs& B) {
   a.p0 = B.p0_tot;
   a.totals = B.p0_tot + 4;
   a.bins = B.bins;
+  a.n_rep = 1;
   a.cnt_ev = B.cnt_ev;
   a.cnt_gl = B.cnt_gl;
   a.chunk_sums = B.chunk_sums;
@@ -403,8 +405,9 @@ int run_pass(pa_ctx* c, const RunPlan& plan, const PassBufs& B, pa_result* out, 
   for (int exact = 0; exact < 2; ++exact) {
     launches = 0;
     ran_csr = csr && !exact;
+    a.n_rep = ran_csr ? B.n_rep : 1u;
     if (plan.timing) CUDA_TRY(c, cudaEventRecord(c->ev[0], st));
-    CUDA_TRY(c, cudaMemsetAsync(B.bins, 0, (size_t)N * sizeof(float4), st));
+    CUDA_TRY(c, cudaMemsetAsync(B.bins, 0, (size_t)N * a.n_rep * sizeof(float4), st));
     if (exact) CUDA_TRY(c, cudaMemsetAsync(B.cnt_ev, 0, (size_t)N * sizeof(uint32_t), st));
     if (exact) CUDA_TRY(c, cudaMemsetAsync(B.cnt_gl, 0, (size_t)N * sizeof(uint32_t), st));
     CUDA_TRY(c, cudaMemsetAsync(B.p0_tot, 0, 8 * sizeof(double), st));
@@ -620,7 +623,8 @@ int run_stream(pa_ctx* c, const RunPlan& plan, const pa_events* ev, uint64_t tar
   }
   const uint32_t nblk = partition_blocks(max_g);
   PassBufs B;
-  PA_TRY(dreserve(c, c->bins, (size_t)N * sizeof(float4)));
+  B.n_rep = plan.csr ? bin_copies(N) : 1u;
+  PA_TRY(dreserve(c, c->bins, (size_t)N * B.n_rep * sizeof(float4)));
   PA_TRY(dreserve(c, c->part_blk, (size_t)(nblk + 1) * 2 * sizeof(uint32_t)));
   PA_TRY(dreserve(c, c->part_counts, 8 * sizeof(uint32_t)));
   PA_TRY(dreserve(c, c->tiles, ((size_t)max_g + 1) * sizeof(Tile)));
@@ -661,8 +665,9 @@ int run_stream(pa_ctx* c, const RunPlan& plan, const pa_events* ev, uint64_t tar
   for (int exact = 0; exact < 2; ++exact) {
     launches = 0;
     stream_csr = B.pieces && !exact;
+    const uint32_t n_rep = stream_csr ? B.n_rep : 1u;
     if (plan.timing) CUDA_TRY(c, cudaEventRecord(c->ev[0], st));
-    CUDA_TRY(c, cudaMemsetAsync(B.bins, 0, (size_t)N * sizeof(float4), st));
+    CUDA_TRY(c, cudaMemsetAsync(B.bins, 0, (size_t)N * n_rep * sizeof(float4), st));
     if (exact) CUDA_TRY(c, cudaMemsetAsync(B.cnt_ev, 0, (size_t)N * 2 * sizeof(uint32_t), st));
     CUDA_TRY(c, cudaMemsetAsync(B.p0_tot, 0, 8 * sizeof(double), st));
     CUDA_TRY(c, cudaMemsetAsync(c->err_word.p, 0xff, sizeof(unsigned long long), st));
@@ -720,6 +725,7 @@ int run_stream(pa_ctx* c, const RunPlan& plan, const pa_events* ev, uint64_t tar
         }
       }
       RunArgs a = make_run_args(c, plan, B);
+      a.n_rep = n_rep;
       a.gates = gates;
       a.n_gates = gk;
       a.pin_off = pin;
@@ -745,6 +751,7 @@ int run_stream(pa_ctx* c, const RunPlan& plan, const pa_events* ev, uint64_t tar
       CUDA_TRY(c, cudaEventRecord(c->st_free[slot], st));
     }
     RunArgs a = make_run_args(c, plan, B);
+    a.n_rep = n_rep;
     a.n_gates = G;
     a.gates = (const GateRec*)c->gates.p;
     CUDA_TRY(c, launch_final_reduce(a, plan.Td, plan.t_max, B.wave, B.p_out, exact != 0, st));
@@ -1067,7 +1074,8 @@ int pa_run(pa_ctx* c, const pa_run_params* prm, pa_result* out) {
   const bool banded = c->band.built && same_bits(c->band.t_clk, plan.T);
   const uint32_t N = plan.N, G = plan.G;
   PassBufs B;
-  PA_TRY(dreserve(c, c->bins, (size_t)N * sizeof(float4)));
+  B.n_rep = plan.csr && !banded ? bin_copies(N) : 1u;
+  PA_TRY(dreserve(c, c->bins, (size_t)N * B.n_rep * sizeof(float4)));
   PA_TRY(dreserve(c, c->part_blk, (size_t)(plan.nblk + 1) * 2 * sizeof(uint32_t)));
   PA_TRY(dreserve(c, c->part_counts, 8 * sizeof(uint32_t)));
   PA_TRY(dreserve(c, c->tiles, ((size_t)G + 1) * sizeof(Tile)));

@@ -17,18 +17,22 @@
 //    the sparse ones whole timelines, the role of the event-density-aware
 //    per-gate partitioning of Figs. 5, 19 and 20, cut by event count.
 //  * One warp per item, no CTA-wide barrier in the item loop. A light tile's
-//    times and slews are one contiguous range, staged with 16-byte loads; a
+//    times and slews are one contiguous range, staged with 16-byte copies; a
 //    lane per gate fills the gate's slot (pin starts, cell, load-axis
 //    interval and fraction, switching energy). A piece is staged in windows of
 //    at most kCsrWin events shared among its pins in proportion to their
-//    remaining events; the events before the earliest first unstaged event of
-//    any pin are taken, so every pin's events earlier than a taken event are
-//    either staged or counted in the pin's parity.
-//  * One lane per event. The gate state before the event's timestamp: each
-//    input pin's initial value flipped once per earlier event, the count on
-//    another pin being a binary search of t in that pin's staged events (ties
-//    see the pre-timestamp state; the leakage step is taken in (time, pin)
-//    order, so simultaneous steps telescope). The slew interval by a
+//    remaining events (16-byte copies per pin run); the events before the
+//    earliest first unstaged event of any pin are taken, so every pin's
+//    events earlier than a taken event are either staged or counted in the
+//    pin's parity.
+//  * The gate state before an event's timestamp (ties see the pre-timestamp
+//    state; the leakage step is taken in (time, pin) order, so simultaneous
+//    steps telescope): in a light tile, one lane per event, each input pin's
+//    initial value flipped once per earlier event, the count on another pin
+//    being a binary search of t in that pin's staged events. In a piece's
+//    window, the input events are walked in (time, pin) order, each lane an
+//    even share of the merge of the pins' runs, the state following from the
+//    parities of the events taken so far on each pin. The slew interval by a
 //    three-step search over the cell's axis in shared memory, the state's four
 //    LUT corners in one 16-byte load, the leakage per state in shared memory.
 //    Glitch: the previous event of the same pin in the same cycle (the CSR
@@ -36,6 +40,7 @@
 //    cycle's bin with one red.global.add.v4.f32; per-lane totals (the
 //    leakage term compensated) are reduced in fp64.
 #include <cfloat>
+#include <cstddef>
 #include <cstdint>
 
 #include "pa_internal.cuh"
@@ -46,7 +51,7 @@ namespace {
 
 constexpr int kCW = 32;               // warps per CTA (their stages fill the shared memory)
 constexpr int kCT = kCW * 32;
-constexpr int kStCap = 400;           // staged events per warp: 384 + alignment slack and window bounds
+constexpr int kStCap = 424;           // staged events per warp: a window, its bounds and 16-byte alignment slack
 constexpr int kAx = 9;                // slew axis stride of the cell table (odd: lanes of different cells spread)
 constexpr int kLk = 17;               // leakage stride of the cell table
 constexpr int kTotEvery = 16;         // items between flushes of a warp's per-lane totals
@@ -86,17 +91,41 @@ struct TSeg {
   uint8_t run[kSegMax];
 };
 
-// One warp's shared memory.
-struct __align__(16) WarpBuf {
-  float ts[kStCap], ss[kStCap];   // staged times (ns) and slews (ps)
-  uint8_t tg[kStCap];             // staged event -> slot << 3 | pin
-  uint16_t mg[2][kStCap];         // a window's merges: staged indices in (time, pin) order
+// A window's pairwise merges of two input pins' runs: per entry the staged
+// index, whether the event is on the upper pin of the pair, and the parities
+// of both pins' events up to and including it.
+constexpr uint32_t kIdxMask = 0x3FFu;
+constexpr int kSelShift = 10, kParShift = 11;
+
+// A piece's gate: its LUT corner patches for its load-axis interval, per
+// state and slew interval ([2^k][ns - 1] of the cell's [2^k][ns - 1][nl - 1]).
+constexpr int kSliceMax = (1 << kMaxK) * (PA_MAX_AXIS - 1);
+
+// One warp's shared memory. A light tile uses all the slots and the run map;
+// a piece uses slot 0 and its gate's patch slice in their place.
+struct TileMem {
   CSlot slot[kCsrGates];
-  HWin hw;
   TSeg seg;
 };
-static_assert(kCellsB % 16 == 0 && sizeof(WarpBuf) % 16 == 0, "alignment");
-static_assert(kCsrWin + 2 * (kMaxK + 1) <= (uint32_t)kStCap && kCsrMaxTileHeavy + 4 <= (uint32_t)kStCap, "stage");
+struct PieceMem {
+  CSlot slot0;
+  float4 slice[kSliceMax];
+};
+struct __align__(16) WarpBuf {
+  float ts[kStCap], ss[kStCap];   // staged times (ns) and slews (ps)
+  uint16_t mg[kStCap];            // a window's pairwise merges
+  HWin hw;
+  union {
+    TileMem t;
+    PieceMem p;
+  } u;
+};
+static_assert(kCellsB % 16 == 0 && sizeof(WarpBuf) % 16 == 0 && kStCap % 4 == 0 && offsetof(WarpBuf, u) % 16 == 0,
+              "alignment");
+// a window: shares of at most kCsrWin + one per pin, a bound event per pin,
+// up to 6 slots of 16-byte alignment per pin
+static_assert(kCsrWin + 8 * (kMaxK + 1) <= (uint32_t)kStCap && kCsrMaxTileHeavy + 4 <= (uint32_t)kStCap, "stage");
+static_assert(kStCap <= (int)kIdxMask + 1, "merge entry index");
 constexpr size_t kSmemB = kCellsB + (size_t)kCW * sizeof(WarpBuf);
 static_assert(kSmemB + 1024 <= 227 * 1024, "shared memory budget");
 
@@ -107,8 +136,10 @@ struct CTab {
   const float* leak;
 };
 
+// A lane's totals, and the first bin of its warp's copy of the bins.
 struct Acc {
   float e_int, e_sw, e_gl, e_lk, c_lk;
+  uint32_t bin0;
 };
 
 __device__ __forceinline__ void kahan_add(float& sum, float& comp, float x) {
@@ -129,7 +160,7 @@ __device__ __forceinline__ void flush_acc(Acc& acc, double* s_tot) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) atomicAdd(s_tot + i, v[i]);
   }
-  acc = Acc{0.f, 0.f, 0.f, 0.f, 0.f};
+  acc = Acc{0.f, 0.f, 0.f, 0.f, 0.f, acc.bin0};
 }
 
 __device__ __forceinline__ void dev_err(unsigned long long* err, uint64_t idx, uint32_t code) {
@@ -163,10 +194,6 @@ __device__ __forceinline__ int lower_bound_f(const float* a, int n, float x) {
 // a lane's copies are all in flight at once); each lane waits for its own
 // before the warp syncs.
 __device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void copy4_async(void* dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
-}
 
 __device__ __forceinline__ void copy16_async(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
@@ -211,9 +238,11 @@ __device__ __forceinline__ void fill_slot(const RunArgs& a, CSlot& S, uint32_t g
   S.esw = a.half_vdd2 * C;
 }
 
-__device__ __forceinline__ void commit(const RunArgs& a, uint32_t c, float e_w, float dp, bool glitch) {
-  float* bin = reinterpret_cast<float*>(a.bins + c);
-  // one 16-byte reduction per event: energy, leakage step, event and glitch counts
+// One 16-byte reduction per event into its cycle's bin, in the warp's copy
+// of the bins: energy, leakage step, event and glitch counts.
+__device__ __forceinline__ void commit(const RunArgs& a, const Acc& acc, uint32_t c, float e_w, float dp,
+                                       bool glitch) {
+  float* bin = reinterpret_cast<float*>(a.bins + acc.bin0 + c);
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(bin), "f"(e_w), "f"(dp), "f"(1.0f),
                "f"(glitch ? 1.0f : 0.0f)
                : "memory");
@@ -244,16 +273,18 @@ __device__ __forceinline__ void out_event(const RunArgs& a, const float* ts, con
   } else {
     acc.e_sw += e_sw;
   }
-  commit(a, c, e_w, 0.f, glitch);
+  commit(a, acc, c, e_w, 0.f, glitch);
 }
 
 // An input-pin event at staged index i of pin p, with its states: s_pre
 // before its timestamp (selects the table), s_b just before it in (time, pin)
 // order (the leakage step's base).
-template <bool kPow2>
-__device__ __forceinline__ void in_event(const RunArgs& a, const CTab& CT, const float* ts, const float* ss,
-                                         const uint4& A, const uint4& B, int i, int p, uint32_t s_pre, uint32_t s_b,
-                                         bool has_prev, float tp, const float* spp, Acc& acc) {
+// The corners come from the gate's patch slice in shared memory in a piece,
+// from the global patch table in a light tile.
+template <bool kPow2, bool kPiece>
+__device__ __forceinline__ void in_event(const RunArgs& a, const CTab& CT, const float4* slice, const float* ts,
+                                         const float* ss, const uint4& A, const uint4& B, int i, int p, uint32_t s_pre,
+                                         uint32_t s_b, bool has_prev, float tp, const float* spp, Acc& acc) {
   const float t = ts[i], s = ss[i];
   const float T = a.t_clk;
   const uint32_t c = cyc<kPow2>(t, T, a.inv_t_clk);
@@ -268,9 +299,9 @@ __device__ __forceinline__ void in_event(const RunArgs& a, const CTab& CT, const
   const float2 ax = CT.sxp[cell * 8 + lis];
   const float u = (s - ax.x) * ax.y;
   // corners {L[i][j], L[i][j+1], L[i+1][j], L[i+1][j+1]} of the state's table
-  const float4 P = __ldg(a.patch + (info >> 16) +
-                         ((int)s_pre * (int)(info & 0xFFu) + lis) * (int)((info >> 8) & 0xFFu) +
-                         (int)((A.w >> 16) & 0xFFu));
+  const int x = (int)s_pre * (int)(info & 0xFFu) + lis;
+  const float4 P = kPiece ? slice[x]
+                          : __ldg(a.patch + (info >> 16) + x * (int)((info >> 8) & 0xFFu) + (int)((A.w >> 16) & 0xFFu));
   const float v = __uint_as_float(B.y);
   const float r0 = fmaf(v, P.y - P.x, P.x), r1 = fmaf(v, P.w - P.z, P.z);
   const float e_int = fmaf(u, r1 - r0, r0);
@@ -286,7 +317,7 @@ __device__ __forceinline__ void in_event(const RunArgs& a, const CTab& CT, const
   const float rem = fmaf(-(float)c, T, t);  // t - c T: the step's part inside its own cycle
   e_w = fmaf(dp, T - rem, e_w);
   kahan_add(acc.e_lk, acc.c_lk, dp * (a.t_max_f - t));
-  commit(a, c, e_w, dp, glitch);
+  commit(a, acc, c, e_w, dp, glitch);
 }
 
 // The pin's previous event for staged event i (index idx in the pin's
@@ -305,49 +336,173 @@ __device__ __forceinline__ void prev_event(const WarpBuf& W, const float* ts, co
   }
 }
 
-// One merge of two runs of staged events, each in (time, pin) order, all
-// pins of run a below all pins of run b (so a tie in time takes a first):
-// run x is the staged indices xb[0, nx) or, with xb null, x0 .. x0 + nx - 1.
-// Merge path: lane l writes the outputs [d0, d1) of an even split, starting
-// from the cut found by a binary search along its first diagonal, then
-// merging sequentially (no divergence: every lane does the same steps).
-__device__ __forceinline__ void merge_runs(const float* ts, const uint16_t* ab, int a0, int na, const uint16_t* bb,
-                                           int b0, int nb, uint16_t* out) {
+__device__ __forceinline__ float f_inf() { return __int_as_float(0x7f800000); }
+
+// The pairwise merge of two input pins' runs (staged a0 .. a0 + na - 1 of the
+// lower pin, b0 .. b0 + nb - 1 of the upper; a tie in time takes the lower
+// pin first) by the 2^lg lanes of a group, this lane being number `sub`:
+// merge path, each lane writing an even share of the outputs from the cut a
+// binary search along its first diagonal finds.
+__device__ __forceinline__ void merge_pair(const float* ts, int a0, int na, int b0, int nb, uint16_t* out, int sub,
+                                           int lg) {
+  const int n = na + nb;
+  const int per = (n + (1 << lg) - 1) >> lg;
+  const int d0 = min(n, sub * per), d1 = min(n, d0 + per);
+  int lo = max(0, d0 - nb), hi = min(d0, na);
+  while (lo < hi) {  // the number of lower-pin events among the first d0 outputs
+    const int mid = (lo + hi) >> 1;
+    if (ts[a0 + mid] <= ts[b0 + d0 - mid - 1]) lo = mid + 1;
+    else hi = mid;
+  }
+  int i = lo, j = d0 - lo;
+  float ta = i < na ? ts[a0 + i] : f_inf(), tb = j < nb ? ts[b0 + j] : f_inf();
+  for (int d = d0; d < d1; ++d) {
+    const bool take_a = ta <= tb;
+    int idx;
+    if (take_a) {
+      idx = a0 + i++;
+      ta = i < na ? ts[a0 + i] : f_inf();
+    } else {
+      idx = b0 + j++;
+      tb = j < nb ? ts[b0 + j] : f_inf();
+    }
+    out[d] = (uint16_t)((uint32_t)idx | (take_a ? 0u : 1u << kSelShift) |
+                        (((uint32_t)i & 1u) | ((uint32_t)j & 1u) << 1) << kParShift);
+  }
+}
+
+// A merged run of n elements: with e, the entries mg[x0 ..] of a pairwise
+// merge of pins q and q + 1; without, pin q's staged run from x0.
+struct MRun {
+  int x0, n, q;
+  bool e;
+};
+
+// Element m of a run: staged index and pin.
+__device__ __forceinline__ void run_at(const uint16_t* mg, const MRun& r, int m, int& idx, int& p) {
+  const uint32_t w = r.e ? (uint32_t)mg[r.x0 + m] : (uint32_t)(r.x0 + m);
+  idx = (int)(w & kIdxMask);
+  p = r.q + (int)((w >> kSelShift) & 1u);
+}
+
+// The run's pins' parity bits (at the pins' positions) over its first m elements.
+__device__ __forceinline__ uint32_t run_par(const uint16_t* mg, const MRun& r, int m) {
+  if (r.e) return m > 0 ? (((uint32_t)mg[r.x0 + m - 1] >> kParShift) & 3u) << r.q : 0u;
+  return ((uint32_t)m & 1u) << r.q;
+}
+
+// A window's input events in (time, pin) order, computed while merging the
+// two runs A (pins below those of B) that hold them: lane l takes an even
+// share of the merged order from the cut a binary search finds and walks it.
+// The state just before an event in that order is the window's start state
+// flipped by the parities of the events taken so far on each pin (known at
+// the cut from the runs' counts or the entries' parities); the state before
+// its timestamp is the one before the first event of its timestamp group.
+template <bool kPow2>
+__device__ __forceinline__ void walk_inputs(const RunArgs& a, const CTab& CT, const WarpBuf& W, const uint4& SA,
+                                            const uint4& SB, const MRun& RA, const MRun& RB, uint32_t start, Acc& acc) {
   const int lane = threadIdx.x & 31;
+  const float* ts = W.ts;
+  const float* ss = W.ss;
+  const uint16_t* mg = W.mg;
+  const int na = RA.n, nb = RB.n;
   const int n = na + nb;
   const int per = (n + 31) >> 5;
   const int d0 = min(n, lane * per), d1 = min(n, d0 + per);
+  if (d0 >= d1) return;
   int lo = max(0, d0 - nb), hi = min(d0, na);
-  while (lo < hi) {  // the number of a's among the first d0 outputs
+  while (lo < hi) {
     const int mid = (lo + hi) >> 1;
-    const int ia = ab ? ab[mid] : a0 + mid, ib = bb ? bb[d0 - mid - 1] : b0 + d0 - mid - 1;
+    int ia, ib, px;
+    run_at(mg, RA, mid, ia, px);
+    run_at(mg, RB, d0 - mid - 1, ib, px);
     if (ts[ia] <= ts[ib]) lo = mid + 1;
     else hi = mid;
   }
   int i = lo, j = d0 - lo;
+  uint32_t s = start ^ run_par(mg, RA, i) ^ run_par(mg, RB, j);
+  int ia = 0, pa = RA.q, ib = 0, pb = RB.q;
+  float ta = f_inf(), tb = f_inf();
+  if (i < na) {
+    run_at(mg, RA, i, ia, pa);
+    ta = ts[ia];
+  }
+  if (j < nb) {
+    run_at(mg, RB, j, ib, pb);
+    tb = ts[ib];
+  }
+  // a timestamp group that began before this lane's share: its state is the
+  // cut's with the group's earlier events (the ends of both prefixes) taken out
+  float t_prev = -1.f;  // times are >= 0
+  uint32_t g = 0;
+  if (d0 > 0) {
+    int x, px;
+    float tla = -1.f, tlb = -1.f;
+    if (i > 0) {
+      run_at(mg, RA, i - 1, x, px);
+      tla = ts[x];
+    }
+    if (j > 0) {
+      run_at(mg, RB, j - 1, x, px);
+      tlb = ts[x];
+    }
+    t_prev = fmaxf(tla, tlb);
+    const float t0 = fminf(ta, tb);
+    if (t0 == t_prev) {
+      g = s;
+      for (int m = i - 1; m >= 0; --m) {
+        run_at(mg, RA, m, x, px);
+        if (ts[x] != t0) break;
+        g ^= 1u << px;
+      }
+      for (int m = j - 1; m >= 0; --m) {
+        run_at(mg, RB, m, x, px);
+        if (ts[x] != t0) break;
+        g ^= 1u << px;
+      }
+    }
+  }
   for (int d = d0; d < d1; ++d) {
-    const int ia = i < na ? (ab ? ab[i] : a0 + i) : -1;
-    const int ib = j < nb ? (bb ? bb[j] : b0 + j) : -1;
-    const bool take_a = ib < 0 || (ia >= 0 && ts[ia] <= ts[ib]);
-    out[d] = (uint16_t)(take_a ? ia : ib);
-    i += take_a ? 1 : 0;
-    j += take_a ? 0 : 1;
+    const bool take_a = ta <= tb;
+    const int idx = take_a ? ia : ib, p = take_a ? pa : pb;
+    const float t = take_a ? ta : tb;
+    if (take_a) {
+      ta = f_inf();
+      if (++i < na) {
+        run_at(mg, RA, i, ia, pa);
+        ta = ts[ia];
+      }
+    } else {
+      tb = f_inf();
+      if (++j < nb) {
+        run_at(mg, RB, j, ib, pb);
+        tb = ts[ib];
+      }
+    }
+    const uint32_t s_b = s;
+    s ^= 1u << p;
+    if (t != t_prev) g = s_b;
+    t_prev = t;
+    bool hp;
+    float tp;
+    const float* spp;
+    prev_event(W, ts, ss, idx, idx - st_of(SA, p), p, true, hp, tp, spp);
+    in_event<kPow2, true>(a, CT, W.u.p.slice, ts, ss, SA, SB, idx, p, g, s_b, hp, tp, spp, acc);
   }
 }
 
 // A piece's window step (gate slot 0, the taken events of each pin a prefix
-// of its staged run): output events one lane each; input events merged in
-// (time, pin) order (pairwise merges of the pins' runs), then computed in
-// that order with their states from a prefix XOR of pin bits (from the gate's
-// state at the window start), the pre-timestamp state taking back out the
-// lower pins' events at the same time.
+// of its staged run): output events one lane each; input events in (time,
+// pin) order: one pin's run as it is, two pins' runs merged as they are
+// walked, three or four pins by pairwise merges first (pins 0 + 1, and 2 + 3
+// on the other half-warp) whose results are merged as they are walked.
 template <bool kPow2>
 __device__ __forceinline__ void window_step(const RunArgs& a, const CTab& CT, WarpBuf& W, Acc& acc) {
   const int lane = threadIdx.x & 31;
   const float* ts = W.ts;
   const float* ss = W.ss;
-  const uint4 A = reinterpret_cast<const uint4*>(&W.slot[0])[0];
-  const uint4 B = reinterpret_cast<const uint4*>(&W.slot[0])[1];
+  const uint4 A = reinterpret_cast<const uint4*>(&W.u.p.slot0)[0];
+  const uint4 B = reinterpret_cast<const uint4*>(&W.u.p.slot0)[1];
   const int k = (int)(A.w & 0xFFu);
   // output events
   {
@@ -361,59 +516,20 @@ __device__ __forceinline__ void window_step(const RunArgs& a, const CTab& CT, Wa
       out_event<kPow2>(a, ts, ss, B, i, hp, tp, spp, acc);
     }
   }
-  // the merge of the input pins' runs
   const int n0 = W.hw.take[0], n1 = k > 1 ? W.hw.take[1] : 0, n2 = k > 2 ? W.hw.take[2] : 0,
             n3 = k > 3 ? W.hw.take[3] : 0;
   const int s0 = st_of(A, 0), s1 = st_of(A, 1), s2 = st_of(A, 2), s3 = st_of(A, 3);
-  const int nin = n0 + n1 + n2 + n3;
-  const uint16_t* mrg = nullptr;  // null: pin 0's run is the merge (k = 1)
-  if (k >= 2) {
-    merge_runs(ts, nullptr, s0, n0, nullptr, s1, n1, W.mg[0]);
-    mrg = W.mg[0];
-    if (k == 3) {
-      __syncwarp();
-      merge_runs(ts, W.mg[0], 0, n0 + n1, nullptr, s2, n2, W.mg[1]);
-      mrg = W.mg[1];
-    } else if (k == 4) {
-      merge_runs(ts, nullptr, s2, n2, nullptr, s3, n3, W.mg[0] + n0 + n1);
-      __syncwarp();
-      merge_runs(ts, W.mg[0], 0, n0 + n1, W.mg[0] + n0 + n1, 0, n2 + n3, W.mg[1]);
-      mrg = W.mg[1];
-    }
-  }
-  __syncwarp();
   const uint32_t kmask = (1u << k) - 1u;
   const uint32_t start = (((A.w >> 8) & 0xFFu) ^ (A.w >> 24)) & kmask;  // initial bits ^ parities before the window
-  uint32_t carry = 0;
-  for (int m0 = 0; m0 < nin; m0 += 32) {
-    const int m = m0 + lane;
-    const bool valid = m < nin;
-    const int i = valid ? (mrg ? (int)mrg[m] : s0 + m) : 0;
-    const int p = (int)(W.tg[i] & 7u);
-    const uint32_t x = valid ? 1u << p : 0u;
-    uint32_t v = x;  // inclusive XOR over the merged order
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, v, d);
-      if (lane >= d) v ^= y;
-    }
-    v ^= carry;
-    carry = __shfl_sync(0xffffffffu, v, 31);
-    if (!valid) continue;
-    const uint32_t s_b = start ^ v ^ x;
-    uint32_t s_pre = s_b;
-    const float t = ts[i];
-    for (int j = m - 1; j >= 0; --j) {  // lower pins' events at the same time
-      const int e = mrg ? (int)mrg[j] : s0 + j;
-      if (ts[e] != t) break;
-      s_pre ^= 1u << (W.tg[e] & 7u);
-    }
-    bool hp;
-    float tp;
-    const float* spp;
-    prev_event(W, ts, ss, i, i - st_of(A, p), p, true, hp, tp, spp);
-    in_event<kPow2>(a, CT, ts, ss, A, B, i, p, s_pre, s_b, hp, tp, spp, acc);
+  if (k >= 3) {  // pins 0 + 1 (the whole warp, or its lower half while the upper merges 2 + 3)
+    const bool up = k == 4 && lane >= 16;
+    merge_pair(ts, up ? s2 : s0, up ? n2 : n0, up ? s3 : s1, up ? n3 : n1, W.mg + (up ? n0 + n1 : 0),
+               lane & (k == 4 ? 15 : 31), k == 4 ? 4 : 5);
+    __syncwarp();
   }
+  const MRun RA = k >= 3 ? MRun{0, n0 + n1, 0, true} : MRun{s0, n0, 0, false};
+  const MRun RB = k == 4 ? MRun{n0 + n1, n2 + n3, 2, true} : (k == 3 ? MRun{s2, n2, 2, false} : MRun{s1, n1, 1, false});
+  walk_inputs<kPow2>(a, CT, W, A, B, RA, RB, start, acc);
   __syncwarp();  // the stage is read before it is refilled
 }
 
@@ -447,7 +563,7 @@ __device__ __forceinline__ void tile_event(const RunArgs& a, const CTab& CT, con
     s_pre ^= par << q;
     s_b ^= ((par ^ (uint32_t)(q < p && eq)) & 1u) << q;
   }
-  in_event<kPow2>(a, CT, ts, ss, A, B, e, p, s_pre, s_b, hp, tp, ss + e - 1, acc);
+  in_event<kPow2, false>(a, CT, nullptr, ts, ss, A, B, e, p, s_pre, s_b, hp, tp, ss + e - 1, acc);
 }
 
 // A light tile: consecutive whole gates, staged whole.
@@ -477,11 +593,11 @@ __device__ __forceinline__ void csr_tile(const RunArgs& a, const CTab& CT, uint3
     copy16_async(reinterpret_cast<float4*>(W.ts) + v, t4 + v);
     copy16_async(reinterpret_cast<float4*>(W.ss) + v, s4 + v);
   }
-  if (lane < kSegWords) W.seg.bits[lane] = 0u;
+  if (lane < kSegWords) W.u.t.seg.bits[lane] = 0u;
   // a lane per gate: its slot, then its non-empty pins' runs
   uint32_t runs = 0, nonempty = 0;
   if (lane < (int)ng) {
-    CSlot& S = W.slot[lane];
+    CSlot& S = W.u.t.slot[lane];
     fill_slot(a, S, tl.gb + (uint32_t)lane, ea, true);
     for (int p = 0; p <= S.k; ++p)
       if (S.st[p + 1] > S.st[p]) {
@@ -498,12 +614,12 @@ __device__ __forceinline__ void csr_tile(const RunArgs& a, const CTab& CT, uint3
   rbase -= runs;
   __syncwarp();  // bits cleared
   if (lane < (int)ng) {
-    const CSlot& S = W.slot[lane];
+    const CSlot& S = W.u.t.slot[lane];
     for (int p = 0; p <= S.k; ++p)
       if ((nonempty >> p) & 1u) {
         const int e = S.st[p];
-        atomicOr(&W.seg.bits[e >> 5], 1u << (e & 31));
-        W.seg.run[rbase++] = (uint8_t)((lane << 3) | p);
+        atomicOr(&W.u.t.seg.bits[e >> 5], 1u << (e & 31));
+        W.u.t.seg.run[rbase++] = (uint8_t)((lane << 3) | p);
       }
   }
   __syncwarp();
@@ -516,11 +632,11 @@ __device__ __forceinline__ void csr_tile(const RunArgs& a, const CTab& CT, uint3
   int carry = 0;
   const uint32_t le = 0xFFFFFFFFu >> (31 - lane);  // lanes <= this one
   for (int e0 = 0; e0 < n; e0 += 32) {
-    const uint32_t word = W.seg.bits[e0 >> 5];
+    const uint32_t word = W.u.t.seg.bits[e0 >> 5];
     const int e = e0 + lane;
     if (e < n) {
-      const uint32_t w = W.seg.run[carry + __popc(word & le) - 1];
-      tile_event<kPow2>(a, CT, ts, ss, W.slot[w >> 3], (int)(w & 7u), e, acc);
+      const uint32_t w = W.u.t.seg.run[carry + __popc(word & le) - 1];
+      tile_event<kPow2>(a, CT, ts, ss, W.u.t.slot[w >> 3], (int)(w & 7u), e, acc);
     }
     carry += __popc(word);
   }
@@ -555,29 +671,42 @@ __device__ __forceinline__ void csr_piece(const RunArgs& a, const CTab& CT, uint
       psv = a.s[pst + cur - 1];
     }
   }
-  CSlot& S = W.slot[0];
+  CSlot& S = W.u.p.slot0;
   if (lane == 0) fill_slot(a, S, g, 0, false);
+  __syncwarp();
+  {  // the gate's patch slice (in flight with the first window's copies)
+    const uint32_t info = CT.info[r.cell];
+    const int ns1 = (int)(info & 0xFFu), nl1 = (int)((info >> 8) & 0xFFu);
+    const float4* src = a.patch + (info >> 16) + S.j;
+    for (int x = lane; x < (ns1 << k); x += 32) copy16_async(&W.u.p.slice[x], src + x * nl1);
+  }
   for (int guard = 0;; ++guard) {
     const uint32_t rem = mine ? hi - cur : 0u;
     const uint32_t R = __reduce_add_sync(0xffffffffu, rem);
     if (R == 0) break;
     uint32_t share = 0;
     if (rem) {
-      const uint64_t sh = (uint64_t)kCsrWin * rem / R;
-      share = sh < 1 ? 1u : (sh > rem ? rem : (uint32_t)sh);
+      const uint32_t sh = rem <= 0xFFFFFFFFu / kCsrWin ? kCsrWin * rem / R : (uint32_t)((uint64_t)kCsrWin * rem / R);
+      share = sh < 1 ? 1u : (sh > rem ? rem : sh);
     }
     // a pin's share is staged with the pin's next event after it, whose time
-    // bounds the window (the pins' runs are st .. st + share, then that event)
+    // bounds the window; each pin's run is copied in 16-byte vectors from its
+    // first event rounded down to a multiple of 4, into 16-byte aligned slots
+    // (the pin's events at st .. st + share, then that event)
     const bool more = mine && cur + share < hi;
     const uint32_t ns_ = share + (more ? 1u : 0u);
-    uint32_t incl = ns_;  // prefix over lanes 0..k
+    const uint64_t src = pst + cur;
+    const uint32_t h = ns_ ? (uint32_t)(src & 3u) : 0u;
+    const uint32_t nv = (h + ns_ + 3u) >> 2;
+    uint32_t vin = nv;  // inclusive prefix of the vectors over lanes 0..k
 #pragma unroll
     for (int d = 1; d <= 4; d <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, d);
-      if (lane >= d) incl += y;
+      const uint32_t y = __shfl_up_sync(0xffffffffu, vin, d);
+      if (lane >= d) vin += y;
     }
-    const uint32_t st = incl - ns_;
-    const int nw = (int)__shfl_sync(0xffffffffu, incl, k);
+    const uint32_t vex = vin - nv;
+    const uint32_t st = 4u * vex + h;
+    const uint32_t NV = __shfl_sync(0xffffffffu, vin, k);
     const bool bounded = __any_sync(0xffffffffu, more);
     if (mine) {
       S.st[lane] = (uint16_t)st;
@@ -585,7 +714,7 @@ __device__ __forceinline__ void csr_piece(const RunArgs& a, const CTab& CT, uint
       W.hw.pt[lane] = ptv;
       W.hw.ps[lane] = psv;
     }
-    if (lane == 0) S.st[k + 1] = (uint16_t)nw;
+    if (lane == 0) S.st[k + 1] = (uint16_t)(4u * NV);
     const uint32_t pre = __ballot_sync(0xffffffffu, mine && (cur & 1u)) & 31u;
     if (lane == 0) S.pre = (uint8_t)pre;
     // bring the pin's next window into L2 while this one is worked on (about
@@ -598,14 +727,24 @@ __device__ __forceinline__ void csr_piece(const RunArgs& a, const CTab& CT, uint
       asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.t + a0), "r"(bytes) : "memory");
       asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.s + a0), "r"(bytes) : "memory");
     }
-    // stage pin by pin (each pin's run is contiguous in the per-pin arrays)
-    for (int q = 0; q <= k; ++q) {
-      const uint32_t sq = __shfl_sync(0xffffffffu, st, q), nq = __shfl_sync(0xffffffffu, ns_, q);
-      const uint64_t src = __shfl_sync(0xffffffffu, pst + cur, q);
-      for (uint32_t i = (uint32_t)lane; i < nq; i += 32) {
-        copy4_async(W.ts + sq + i, a.t + src + i);
-        copy4_async(W.ss + sq + i, a.s + src + i);
-        W.tg[sq + i] = (uint8_t)q;
+    // the vectors of all pins, a lane each (vector v belongs to the pin
+    // whose prefix range holds it; the event arrays are padded past their end)
+    {
+      uint32_t vend[kMaxK];
+#pragma unroll
+      for (int x = 0; x < kMaxK; ++x) vend[x] = __shfl_sync(0xffffffffu, vin, x);
+      const uint64_t src4 = src >> 2;
+      for (uint32_t v0 = 0; v0 < NV; v0 += 32) {
+        const uint32_t v = v0 + (uint32_t)lane;
+        int q = 0;
+#pragma unroll
+        for (int x = 0; x < kMaxK; ++x) q += (x < k && v >= vend[x]) ? 1 : 0;
+        const uint64_t g4 = __shfl_sync(0xffffffffu, src4, q);
+        const uint32_t vq = __shfl_sync(0xffffffffu, vex, q);
+        if (v < NV) {
+          copy16_async(reinterpret_cast<float4*>(W.ts) + v, reinterpret_cast<const float4*>(a.t) + g4 + (v - vq));
+          copy16_async(reinterpret_cast<float4*>(W.ss) + v, reinterpret_cast<const float4*>(a.s) + g4 + (v - vq));
+        }
       }
     }
     copies_wait();
@@ -632,6 +771,8 @@ __device__ __forceinline__ void csr_piece(const RunArgs& a, const CTab& CT, uint
       break;
     }
   }
+  copies_wait();  // (the slice's copies, for a piece without events)
+  __syncwarp();
 }
 
 template <bool kPow2>
@@ -664,7 +805,8 @@ __global__ void __launch_bounds__(kCT, 1) k_csr(const RunArgs a) {
   const CTab CT{sax, info, sxp, lk};
   const uint32_t n_tiles = a.part_counts[0], n_pieces = a.part_counts[1];
   const uint32_t n_items = n_tiles + n_pieces;
-  Acc acc{0.f, 0.f, 0.f, 0.f, 0.f};
+  // the warps spread their reductions over n_rep (a power of two) copies of the bins
+  Acc acc{0.f, 0.f, 0.f, 0.f, 0.f, ((blockIdx.x * (uint32_t)kCW + (uint32_t)warp) & (a.n_rep - 1u)) * a.n_cycles};
   int since = 0;
   // a warp takes kChunk items at a time (the heavy gates' pieces come first:
   // the longest items); the next chunk is asked for as soon as one begins

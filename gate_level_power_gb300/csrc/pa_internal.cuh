@@ -115,7 +115,9 @@ struct RunArgs {
   //   exact mode (a cycle reached 2^24 events) the same 16 bytes hold {W, D} as
   //   fp64 -- f32 sums of that many terms are too coarse -- and the counts go
   //   to cnt_ev / cnt_gl as integers.
-  float4* bins;            // [n_cycles]
+  float4* bins;            // [n_rep][n_cycles]
+  uint32_t n_rep;          // copies of the f32 bins (a power of two; the warp kernel's pass spreads its
+                           // reductions over them, the final reduction adds them up), else 1
   uint32_t* cnt_ev;        // [n_cycles] exact counts (exact mode) / count output (fast mode), may be null
   uint32_t* cnt_gl;
   double* chunk_sums;      // [ceil(n_cycles / kReduceChunk)] final-reduction partial sums
@@ -372,5 +374,17 @@ cudaError_t launch_gate_power(const RunArgs& a, double t_max, cudaStream_t st);
 cudaError_t launch_rebase_chunk(uint64_t* pin_off, uint64_t n_pins, uint64_t ev0, const GateRec* gates_src,
                                 GateRec* gates_dst, uint32_t n_gates, uint32_t pin0, cudaStream_t st);
 inline uint32_t reduce_chunks(uint32_t n_cycles) { return (n_cycles + kReduceChunk - 1) / kReduceChunk; }
+
+// Copies of the f32 bins for the warp kernel's pass: up to kBinCopies, within
+// kBinCopyBytes in all. Reductions of many events into one cycle's bin
+// serialise at its L2 slice; spread over copies, bursts of activity in a few
+// cycles cost less.
+constexpr uint32_t kBinCopies = 8;
+constexpr size_t kBinCopyBytes = (size_t)64 << 20;
+inline uint32_t bin_copies(uint32_t n_cycles) {
+  uint32_t r = kBinCopies;
+  while (r > 1 && (size_t)r * n_cycles * 16 > kBinCopyBytes) r >>= 1;
+  return r;
+}
 
 }  // namespace pa

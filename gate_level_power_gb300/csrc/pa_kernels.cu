@@ -767,13 +767,18 @@ cudaError_t launch_fused(const RunArgs& a, int grid, bool pow2, bool debug, bool
 constexpr int kRedThreads = 256;
 constexpr int kRedPer = (int)kReduceChunk / kRedThreads;  // cycles per thread
 
-// Energy W and step D of cycle c: f32 {W, D, ev, gl} bins, or fp64 {W, D}
-// bins (same 16 bytes) when counts are taken exactly.
+// Energy W and step D of cycle c: f32 {W, D, ev, gl} bins (the sum of their
+// copies), or fp64 {W, D} bins (same 16 bytes) when counts are taken exactly.
 template <bool kExact>
 __device__ __forceinline__ double2 bin_wd(const RunArgs& a, uint32_t c) {
   if (kExact) return reinterpret_cast<const double2*>(a.bins)[c];
-  const float4 v = a.bins[c];
-  return make_double2((double)v.x, (double)v.y);
+  double2 r = make_double2(0.0, 0.0);
+  for (uint32_t k = 0; k < max(a.n_rep, 1u); ++k) {
+    const float4 v = a.bins[(size_t)k * a.n_cycles + c];
+    r.x += (double)v.x;
+    r.y += (double)v.y;
+  }
+  return r;
 }
 
 template <bool kExact>
@@ -837,11 +842,18 @@ __global__ void __launch_bounds__(kRedThreads) k_reduce_apply(const RunArgs a, d
     if (t_max > lo && t_max < hi) e -= d * (hi - t_max);
     if (wave) wave[c] = (float)(e / T * 1e-6);
     if (!kExact) {
-      // f32 counts are exact integers while below 2^24
-      const float4 f = a.bins[c];
-      if (f.z >= 16777216.0f) overflow = true;
-      if (a.cnt_ev) a.cnt_ev[c] = (uint32_t)f.z;
-      if (a.cnt_gl) a.cnt_gl[c] = (uint32_t)f.w;
+      // f32 counts are exact integers while below 2^24: a cycle with 2^24
+      // events or more in all repeats the pass with integer counts
+      uint32_t ne = 0, ng = 0;
+      for (uint32_t k = 0; k < max(a.n_rep, 1u); ++k) {
+        const float4 f = a.bins[(size_t)k * a.n_cycles + c];
+        if (f.z >= 16777216.0f) overflow = true;
+        ne += (uint32_t)f.z;
+        ng += (uint32_t)f.w;
+      }
+      if (ne >= (1u << 24)) overflow = true;
+      if (a.cnt_ev) a.cnt_ev[c] = ne;
+      if (a.cnt_gl) a.cnt_gl[c] = ng;
     }
     pre += d;
   }
