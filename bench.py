@@ -97,7 +97,7 @@ def parse_args():
                     help="work partition knob: target events per light tile (0 = the library's default)")
     ap.add_argument("--heavy-events", type=int, default=0,
                     help="work partition knob: gates with more events are heavy (0 = the library's default); "
-                         "tile + heavy above 384 selects the CTA kernel (k_fused) instead of the warp kernel")
+                         "tile + heavy above 448 selects the CTA kernel (k_fused) instead of the warp kernel")
     ap.add_argument("--partition", choices=["events", "density", "fixed"], default="events",
                     help="work partition: the library's event-count partition (default) or the paper's "
                          "(gate, window) threads, event-density-aware or globally fixed")

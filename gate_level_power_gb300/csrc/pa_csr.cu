@@ -51,7 +51,7 @@ namespace {
 
 constexpr int kCW = 32;               // warps per CTA (their stages fill the shared memory)
 constexpr int kCT = kCW * 32;
-constexpr int kStCap = 424;           // staged events per warp: a window, its bounds and 16-byte alignment slack
+constexpr int kStCap = 496;           // staged events per warp: a window, its bounds, the pins' previous events and 16-byte alignment slack
 constexpr int kAx = 9;                // slew axis stride of the cell table (odd: lanes of different cells spread)
 constexpr int kLk = 17;               // leakage stride of the cell table
 constexpr int kTotEvery = 16;         // items between flushes of a warp's per-lane totals
@@ -68,17 +68,16 @@ constexpr size_t kCellsB =
 struct __align__(16) CSlot {
   uint16_t st[kMaxK + 2];    // staged start of pins 0..k; st[k + 1] = end
   uint8_t k, init, j, pre;   // inputs, initial input bits, load-axis interval, parity of earlier events per pin
-  uint16_t cell, pad;
+  uint16_t cell;
+  uint16_t hp;               // a piece's window: pins whose previous event is staged just before their run
   float v, esw;              // load-axis fraction; switching energy C V^2 / 2 (fJ)
 };
 static_assert(sizeof(CSlot) == 32, "slot size");
 
 // Per pin of a piece's current window: the events taken in this window (a
-// prefix of the pin's staged run) and the pin's event before the window.
+// prefix of the pin's staged run).
 struct HWin {
   uint16_t take[kMaxK + 1];
-  uint8_t hp[kMaxK + 1];     // the pin has an event before the window
-  float pt[kMaxK + 1], ps[kMaxK + 1];  // that event's time and slew
 };
 
 // A light tile's map from staged event to (slot, pin): a bit per event that
@@ -122,9 +121,9 @@ struct __align__(16) WarpBuf {
 };
 static_assert(kCellsB % 16 == 0 && sizeof(WarpBuf) % 16 == 0 && kStCap % 4 == 0 && offsetof(WarpBuf, u) % 16 == 0,
               "alignment");
-// a window: shares of at most kCsrWin + one per pin, a bound event per pin,
-// up to 6 slots of 16-byte alignment per pin
-static_assert(kCsrWin + 8 * (kMaxK + 1) <= (uint32_t)kStCap && kCsrMaxTileHeavy + 4 <= (uint32_t)kStCap, "stage");
+// a window: shares of at most kCsrWin + one per pin, per pin a bound event, a
+// previous event and up to 6 slots of 16-byte alignment
+static_assert(kCsrWin + 9 * (kMaxK + 1) <= (uint32_t)kStCap && kCsrMaxTileHeavy + 4 <= (uint32_t)kStCap, "stage");
 static_assert(kStCap <= (int)kIdxMask + 1, "merge entry index");
 constexpr size_t kSmemB = kCellsB + (size_t)kCW * sizeof(WarpBuf);
 static_assert(kSmemB + 1024 <= 227 * 1024, "shared memory budget");
@@ -227,6 +226,7 @@ __device__ __forceinline__ void fill_slot(const RunArgs& a, CSlot& S, uint32_t g
   S.k = (uint8_t)k;
   S.init = (uint8_t)(r.init & 0xffu);
   S.pre = 0;
+  S.hp = 0;
   S.cell = (uint16_t)r.cell;
   const float C = r.load;
   const int nl = cd.nl;
@@ -320,20 +320,15 @@ __device__ __forceinline__ void in_event(const RunArgs& a, const CTab& CT, const
   commit(a, acc, c, e_w, dp, glitch);
 }
 
-// The pin's previous event for staged event i (index idx in the pin's
-// staged run): the staged one before it, or, for the first of a window, the
-// one before the window (pieces; light gates are staged whole).
-__device__ __forceinline__ void prev_event(const WarpBuf& W, const float* ts, const float* ss, int i, int idx, int p,
-                                           bool window, bool& has_prev, float& tp, const float*& spp) {
-  if (idx > 0) {
-    has_prev = true;
-    tp = ts[i - 1];
-    spp = ss + i - 1;
-  } else {
-    has_prev = window && W.hw.hp[p] != 0;
-    tp = W.hw.pt[p];
-    spp = &W.hw.ps[p];
-  }
+// The pin's previous event for staged event i, the first of its pin's run
+// in the stage or not: staged just before it (a piece's window stages each
+// pin's run with the pin's previous event, where there is one).
+__device__ __forceinline__ void prev_event(const float* ts, const float* ss, int i, bool first, bool hp_first,
+                                           bool& has_prev, float& tp, const float*& spp) {
+  has_prev = !first || hp_first;
+  const int x = max(i - 1, 0);
+  tp = ts[x];
+  spp = ss + x;
 }
 
 __device__ __forceinline__ float f_inf() { return __int_as_float(0x7f800000); }
@@ -466,17 +461,25 @@ __device__ __forceinline__ void walk_inputs(const RunArgs& a, const CTab& CT, co
     const bool take_a = ta <= tb;
     const int idx = take_a ? ia : ib, p = take_a ? pa : pb;
     const float t = take_a ? ta : tb;
-    if (take_a) {
-      ta = f_inf();
-      if (++i < na) {
-        run_at(mg, RA, i, ia, pa);
-        ta = ts[ia];
+    {  // the next head of the run the event came from
+      const int m = (take_a ? i : j) + 1;
+      const MRun R{take_a ? RA.x0 : RB.x0, take_a ? na : nb, take_a ? RA.q : RB.q, take_a ? RA.e : RB.e};
+      int nidx = 0, np = 0;
+      float nt = f_inf();
+      if (m < R.n) {
+        run_at(mg, R, m, nidx, np);
+        nt = ts[nidx];
       }
-    } else {
-      tb = f_inf();
-      if (++j < nb) {
-        run_at(mg, RB, j, ib, pb);
-        tb = ts[ib];
+      if (take_a) {
+        i = m;
+        ia = nidx;
+        pa = np;
+        ta = nt;
+      } else {
+        j = m;
+        ib = nidx;
+        pb = np;
+        tb = nt;
       }
     }
     const uint32_t s_b = s;
@@ -486,7 +489,7 @@ __device__ __forceinline__ void walk_inputs(const RunArgs& a, const CTab& CT, co
     bool hp;
     float tp;
     const float* spp;
-    prev_event(W, ts, ss, idx, idx - st_of(SA, p), p, true, hp, tp, spp);
+    prev_event(ts, ss, idx, idx == st_of(SA, p), (SB.x >> (16 + p)) & 1u, hp, tp, spp);
     in_event<kPow2, true>(a, CT, W.u.p.slice, ts, ss, SA, SB, idx, p, g, s_b, hp, tp, spp, acc);
   }
 }
@@ -512,7 +515,7 @@ __device__ __forceinline__ void window_step(const RunArgs& a, const CTab& CT, Wa
       bool hp;
       float tp;
       const float* spp;
-      prev_event(W, ts, ss, i, x, k, true, hp, tp, spp);
+      prev_event(ts, ss, i, x == 0, (B.x >> (16 + k)) & 1u, hp, tp, spp);
       out_event<kPow2>(a, ts, ss, B, i, hp, tp, spp, acc);
     }
   }
@@ -657,19 +660,12 @@ __device__ __forceinline__ void csr_piece(const RunArgs& a, const CTab& CT, uint
   const bool mine = lane <= k;  // lane p holds pin p
   uint64_t pst = 0;
   uint32_t cur = 0, hi = 0;
-  bool hp = false;
-  float ptv = 0.f, psv = 0.f;
   if (mine) {
     pst = a.pin_off[(uint64_t)r.pin_base + lane];
     const uint64_t pe = a.pin_off[(uint64_t)r.pin_base + lane + 1];
     cur = P.lo[lane];
     hi = last ? (uint32_t)(pe - pst) : a.pieces[pi + 1].lo[lane];
     if (hi < cur) hi = cur;  // (never for a consistent partition)
-    if (cur > 0) {  // the pin's event before the piece
-      hp = true;
-      ptv = a.t[pst + cur - 1];
-      psv = a.s[pst + cur - 1];
-    }
   }
   CSlot& S = W.u.p.slot0;
   if (lane == 0) fill_slot(a, S, g, 0, false);
@@ -684,18 +680,23 @@ __device__ __forceinline__ void csr_piece(const RunArgs& a, const CTab& CT, uint
     const uint32_t rem = mine ? hi - cur : 0u;
     const uint32_t R = __reduce_add_sync(0xffffffffu, rem);
     if (R == 0) break;
+    // the pins' shares of the window, in proportion to their remaining
+    // events (rounded down throughout, so they add up to at most kCsrWin,
+    // plus one for each pin whose share rounds to nothing)
     uint32_t share = 0;
     if (rem) {
-      const uint32_t sh = rem <= 0xFFFFFFFFu / kCsrWin ? kCsrWin * rem / R : (uint32_t)((uint64_t)kCsrWin * rem / R);
-      share = sh < 1 ? 1u : (sh > rem ? rem : sh);
+      const float f = __fmul_rd(__uint2float_rd(rem), __fmul_rd((float)kCsrWin, __frcp_rd(__uint2float_ru(R))));
+      share = min(rem, max(1u, __float2uint_rd(f)));
     }
-    // a pin's share is staged with the pin's next event after it, whose time
-    // bounds the window; each pin's run is copied in 16-byte vectors from its
-    // first event rounded down to a multiple of 4, into 16-byte aligned slots
-    // (the pin's events at st .. st + share, then that event)
+    // a pin's share is staged after the pin's previous event (if any) and
+    // before its next one after the share, whose time bounds the window; each
+    // pin's run is copied in 16-byte vectors from its first event rounded
+    // down to a multiple of 4, into 16-byte aligned slots (the pin's events
+    // at st .. st + share, then that event)
     const bool more = mine && cur + share < hi;
-    const uint32_t ns_ = share + (more ? 1u : 0u);
-    const uint64_t src = pst + cur;
+    const uint32_t before = mine && cur > 0 ? 1u : 0u;
+    const uint32_t ns_ = before + share + (more ? 1u : 0u);
+    const uint64_t src = pst + cur - before;
     const uint32_t h = ns_ ? (uint32_t)(src & 3u) : 0u;
     const uint32_t nv = (h + ns_ + 3u) >> 2;
     uint32_t vin = nv;  // inclusive prefix of the vectors over lanes 0..k
@@ -705,15 +706,12 @@ __device__ __forceinline__ void csr_piece(const RunArgs& a, const CTab& CT, uint
       if (lane >= d) vin += y;
     }
     const uint32_t vex = vin - nv;
-    const uint32_t st = 4u * vex + h;
+    const uint32_t st = 4u * vex + h + before;
     const uint32_t NV = __shfl_sync(0xffffffffu, vin, k);
     const bool bounded = __any_sync(0xffffffffu, more);
-    if (mine) {
-      S.st[lane] = (uint16_t)st;
-      W.hw.hp[lane] = (uint8_t)hp;
-      W.hw.pt[lane] = ptv;
-      W.hw.ps[lane] = psv;
-    }
+    if (mine) S.st[lane] = (uint16_t)st;
+    const uint32_t hpm = __ballot_sync(0xffffffffu, before != 0u) & 31u;
+    if (lane == 0) S.hp = (uint16_t)hpm;
     if (lane == 0) S.st[k + 1] = (uint16_t)(4u * NV);
     const uint32_t pre = __ballot_sync(0xffffffffu, mine && (cur & 1u)) & 31u;
     if (lane == 0) S.pre = (uint8_t)pre;
@@ -758,12 +756,7 @@ __device__ __forceinline__ void csr_piece(const RunArgs& a, const CTab& CT, uint
     if (mine) W.hw.take[lane] = (uint16_t)take;
     __syncwarp();
     window_step<kPow2>(a, CT, W, acc);
-    if (mine && take > 0) {
-      hp = true;
-      ptv = W.ts[st + take - 1];
-      psv = W.ss[st + take - 1];
-      cur += take;
-    }
+    cur += take;
     const uint32_t moved = __reduce_add_sync(0xffffffffu, mine ? take : 0u);
     __syncwarp();
     if (moved == 0 || guard > (1 << 24)) {  // cannot happen for valid input; never spin

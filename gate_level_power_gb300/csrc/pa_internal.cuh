@@ -279,10 +279,10 @@ struct BandRunArgs {
 // windows of at most kCsrWin events.
 constexpr uint32_t kCsrDefaultTile = 320;
 constexpr uint32_t kCsrDefaultHeavy = 64;
-constexpr uint32_t kCsrMaxTileHeavy = 384;  // tile_target + heavy_thresh a warp's stage holds
+constexpr uint32_t kCsrMaxTileHeavy = 448;  // tile_target + heavy_thresh a warp's stage holds
 constexpr uint32_t kCsrGates = 32;          // gates per light tile (one lane per gate)
 constexpr uint32_t kCsrPiece = 2048;        // target events per piece of a heavy gate
-constexpr uint32_t kCsrWin = 384;           // events per window of a piece
+constexpr uint32_t kCsrWin = 448;           // events per window of a piece
 
 struct Piece {
   uint32_t gate, idx;          // the gate; the piece's index among the gate's pieces

@@ -198,7 +198,7 @@ typedef struct pa_events {
  *                  no per-event output (state_pre, lut_ij, is_glitch,
  *                  gate_power_w, cell_power_w, the alternative readings),
  *                  the library has at most 64 cells and tile_events +
- *                  heavy_events (defaults resolved) is at most 384; else the
+ *                  heavy_events (defaults resolved) is at most 448; else the
  *                  CTA kernel. pa_run_noalloc always takes the CTA kernel.
  *   flags          PA_RUN_* bits
  *   part_mode      PA_PART_* (pa_run only; the other entry points take

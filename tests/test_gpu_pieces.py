@@ -15,7 +15,7 @@ from tests.test_gpu_parity import assert_parity
 
 pytestmark = pytest.mark.gpu
 
-KNOBS = [(0, 0), (8, 8), (64, 16), (1, 1)]
+KNOBS = [(0, 0), (8, 8), (64, 16), (1, 1), (400, 48)]  # 400 + 48: the largest tiles of the warp kernel
 
 
 @pytest.fixture(scope="module")
@@ -117,3 +117,17 @@ def test_non_power_of_two_clock_bursts(glp):
         return np.concatenate([rng.uniform(7.0, 9.1, nb), rng.uniform(0.0, 69.9, n - nb)])
     w = hand_made(54, [(2000, 2000, 900), (100, 3000, 30, 1200)], 100, 0.7, burst)
     check_all(glp, w)
+
+
+def test_tile_limit_selects_the_kernel(glp):
+    # tile_events + heavy_events up to 448 run on the warp kernel, above it on
+    # the CTA kernel; both at the same bar against the oracle
+    w = synth.custom(seed=57, n_gates=3000, n_cells=16, k_mode=1, n_cycles=200, t_clk_ns=1.0,
+                     n_events=400000, activity=1, zipf_s=1.1, pair_frac=0.1, threads=4)
+    o = oracle.run(w, threads=4)
+    with glp.PowerAnalyzer(0) as pa:
+        pa.load_workload(w)
+        for tile, heavy, path in ((400, 48, glp.PA_PATH_WARP), (400, 49, glp.PA_PATH_UNBANDED)):
+            r = pa.run(w.vdd, w.t_clk_ns, w.n_cycles, tile_events=tile, heavy_events=heavy)
+            assert r["path"] == path, (tile, heavy)
+            assert_parity(r, o, debug=False)
