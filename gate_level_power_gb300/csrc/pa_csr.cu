@@ -243,9 +243,10 @@ __device__ __forceinline__ void fill_slot(const RunArgs& a, CSlot& S, uint32_t g
 __device__ __forceinline__ void commit(const RunArgs& a, const Acc& acc, uint32_t c, float e_w, float dp,
                                        bool glitch) {
   float* bin = reinterpret_cast<float*>(a.bins + acc.bin0 + c);
+  // (nothing in the kernel reads the bins: no memory clobber, so shared
+  // memory values need not be reloaded after it)
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(bin), "f"(e_w), "f"(dp), "f"(1.0f),
-               "f"(glitch ? 1.0f : 0.0f)
-               : "memory");
+               "f"(glitch ? 1.0f : 0.0f));
 }
 
 // The glitch ratio of an event at t (slew s) whose previous event on the pin
@@ -353,15 +354,14 @@ __device__ __forceinline__ void merge_pair(const float* ts, int a0, int na, int 
   float ta = i < na ? ts[a0 + i] : f_inf(), tb = j < nb ? ts[b0 + j] : f_inf();
   for (int d = d0; d < d1; ++d) {
     const bool take_a = ta <= tb;
-    int idx;
-    if (take_a) {
-      idx = a0 + i++;
-      ta = i < na ? ts[a0 + i] : f_inf();
-    } else {
-      idx = b0 + j++;
-      tb = j < nb ? ts[b0 + j] : f_inf();
-    }
-    out[d] = (uint16_t)((uint32_t)idx | (take_a ? 0u : 1u << kSelShift) |
+    const int m = (take_a ? i : j) + 1;  // the taken run's next element
+    const int x = (take_a ? a0 : b0) + m;
+    const float nt = m < (take_a ? na : nb) ? ts[x] : f_inf();
+    i = take_a ? m : i;
+    j = take_a ? j : m;
+    ta = take_a ? nt : ta;
+    tb = take_a ? tb : nt;
+    out[d] = (uint16_t)((uint32_t)(x - 1) | (take_a ? 0u : 1u << kSelShift) |
                         (((uint32_t)i & 1u) | ((uint32_t)j & 1u) << 1) << kParShift);
   }
 }
@@ -722,8 +722,8 @@ __device__ __forceinline__ void csr_piece(const RunArgs& a, const CTab& CT, uint
       const uint32_t nb = min(hi - (cur + share), share);
       const uint64_t a0 = e & ~3ull;
       const uint32_t bytes = (uint32_t)(((e + nb + 3) & ~3ull) - a0) * 4u;
-      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.t + a0), "r"(bytes) : "memory");
-      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.s + a0), "r"(bytes) : "memory");
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.t + a0), "r"(bytes));
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.s + a0), "r"(bytes));
     }
     // the vectors of all pins, a lane each (vector v belongs to the pin
     // whose prefix range holds it; the event arrays are padded past their end)
@@ -815,8 +815,8 @@ __global__ void __launch_bounds__(kCT, 1) k_csr(const RunArgs a) {
       const uint64_t ea = a.tile_ev[2 * ti] & ~3ull, eb = (a.tile_ev[2 * ti + 1] + 3) & ~3ull;
       if (eb > ea && eb - ea <= (uint64_t)kStCap) {
         const uint32_t bytes = (uint32_t)(eb - ea) * 4u;
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.t + ea), "r"(bytes) : "memory");
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.s + ea), "r"(bytes) : "memory");
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.t + ea), "r"(bytes));
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.s + ea), "r"(bytes));
       }
     }
     for (uint32_t j = 0; j < kChunk && base + j < n_items; ++j) {
