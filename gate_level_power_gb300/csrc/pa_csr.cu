@@ -68,8 +68,7 @@ constexpr size_t kCellsB =
 struct __align__(16) CSlot {
   uint16_t st[kMaxK + 2];    // staged start of pins 0..k; st[k + 1] = end
   uint8_t k, init, j, pre;   // inputs, initial input bits, load-axis interval, parity of earlier events per pin
-  uint16_t cell;
-  uint16_t hp;               // a piece's window: pins whose previous event is staged just before their run
+  uint16_t cell, pad;
   float v, esw;              // load-axis fraction; switching energy C V^2 / 2 (fJ)
 };
 static_assert(sizeof(CSlot) == 32, "slot size");
@@ -121,8 +120,9 @@ struct __align__(16) WarpBuf {
 };
 static_assert(kCellsB % 16 == 0 && sizeof(WarpBuf) % 16 == 0 && kStCap % 4 == 0 && offsetof(WarpBuf, u) % 16 == 0,
               "alignment");
-// a window: shares of at most kCsrWin + one per pin, per pin a bound event, a
-// previous event and up to 6 slots of 16-byte alignment
+// a window: shares of at most kCsrWin + one per pin; per pin a bound event
+// and at most 7 slots for its previous event (or the late time) and 16-byte
+// alignment
 static_assert(kCsrWin + 9 * (kMaxK + 1) <= (uint32_t)kStCap && kCsrMaxTileHeavy + 4 <= (uint32_t)kStCap, "stage");
 static_assert(kStCap <= (int)kIdxMask + 1, "merge entry index");
 constexpr size_t kSmemB = kCellsB + (size_t)kCW * sizeof(WarpBuf);
@@ -226,7 +226,6 @@ __device__ __forceinline__ void fill_slot(const RunArgs& a, CSlot& S, uint32_t g
   S.k = (uint8_t)k;
   S.init = (uint8_t)(r.init & 0xffu);
   S.pre = 0;
-  S.hp = 0;
   S.cell = (uint16_t)r.cell;
   const float C = r.load;
   const int nl = cd.nl;
@@ -321,16 +320,11 @@ __device__ __forceinline__ void in_event(const RunArgs& a, const CTab& CT, const
   commit(a, acc, c, e_w, dp, glitch);
 }
 
-// The pin's previous event for staged event i, the first of its pin's run
-// in the stage or not: staged just before it (a piece's window stages each
-// pin's run with the pin's previous event, where there is one).
-__device__ __forceinline__ void prev_event(const float* ts, const float* ss, int i, bool first, bool hp_first,
-                                           bool& has_prev, float& tp, const float*& spp) {
-  has_prev = !first || hp_first;
-  const int x = max(i - 1, 0);
-  tp = ts[x];
-  spp = ss + x;
-}
+// A piece's window stages each pin's run after the pin's previous event, or,
+// where the pin has none, after a time so late that its cycle (the largest
+// 32-bit index, as the conversion saturates) never equals an event's: the
+// glitch test needs no flag.
+constexpr float kNoPrev = 3.0e38f;
 
 __device__ __forceinline__ float f_inf() { return __int_as_float(0x7f800000); }
 
@@ -486,11 +480,7 @@ __device__ __forceinline__ void walk_inputs(const RunArgs& a, const CTab& CT, co
     s ^= 1u << p;
     if (t != t_prev) g = s_b;
     t_prev = t;
-    bool hp;
-    float tp;
-    const float* spp;
-    prev_event(ts, ss, idx, idx == st_of(SA, p), (SB.x >> (16 + p)) & 1u, hp, tp, spp);
-    in_event<kPow2, true>(a, CT, W.u.p.slice, ts, ss, SA, SB, idx, p, g, s_b, hp, tp, spp, acc);
+    in_event<kPow2, true>(a, CT, W.u.p.slice, ts, ss, SA, SB, idx, p, g, s_b, true, ts[idx - 1], ss + idx - 1, acc);
   }
 }
 
@@ -512,11 +502,7 @@ __device__ __forceinline__ void window_step(const RunArgs& a, const CTab& CT, Wa
     const int o0 = st_of(A, k), on = W.hw.take[k];
     for (int x = lane; x < on; x += 32) {
       const int i = o0 + x;
-      bool hp;
-      float tp;
-      const float* spp;
-      prev_event(ts, ss, i, x == 0, (B.x >> (16 + k)) & 1u, hp, tp, spp);
-      out_event<kPow2>(a, ts, ss, B, i, hp, tp, spp, acc);
+      out_event<kPow2>(a, ts, ss, B, i, true, ts[i - 1], ss + i - 1, acc);
     }
   }
   const int n0 = W.hw.take[0], n1 = k > 1 ? W.hw.take[1] : 0, n2 = k > 2 ? W.hw.take[2] : 0,
@@ -698,7 +684,10 @@ __device__ __forceinline__ void csr_piece(const RunArgs& a, const CTab& CT, uint
     const uint32_t ns_ = before + share + (more ? 1u : 0u);
     const uint64_t src = pst + cur - before;
     const uint32_t h = ns_ ? (uint32_t)(src & 3u) : 0u;
-    const uint32_t nv = (h + ns_ + 3u) >> 2;
+    // a pin without a previous event whose run would start a vector gets an
+    // empty leading vector, which holds the late time in its place
+    const uint32_t lead = mine && !before && h == 0u ? 1u : 0u;
+    const uint32_t nv = ((h + ns_ + 3u) >> 2) + lead;
     uint32_t vin = nv;  // inclusive prefix of the vectors over lanes 0..k
 #pragma unroll
     for (int d = 1; d <= 4; d <<= 1) {
@@ -706,12 +695,11 @@ __device__ __forceinline__ void csr_piece(const RunArgs& a, const CTab& CT, uint
       if (lane >= d) vin += y;
     }
     const uint32_t vex = vin - nv;
-    const uint32_t st = 4u * vex + h + before;
+    const uint32_t v0q = vex + lead;  // the pin's first copied vector
+    const uint32_t st = 4u * v0q + h + before;
     const uint32_t NV = __shfl_sync(0xffffffffu, vin, k);
     const bool bounded = __any_sync(0xffffffffu, more);
     if (mine) S.st[lane] = (uint16_t)st;
-    const uint32_t hpm = __ballot_sync(0xffffffffu, before != 0u) & 31u;
-    if (lane == 0) S.hp = (uint16_t)hpm;
     if (lane == 0) S.st[k + 1] = (uint16_t)(4u * NV);
     const uint32_t pre = __ballot_sync(0xffffffffu, mine && (cur & 1u)) & 31u;
     if (lane == 0) S.pre = (uint8_t)pre;
@@ -738,14 +726,16 @@ __device__ __forceinline__ void csr_piece(const RunArgs& a, const CTab& CT, uint
 #pragma unroll
         for (int x = 0; x < kMaxK; ++x) q += (x < k && v >= vend[x]) ? 1 : 0;
         const uint64_t g4 = __shfl_sync(0xffffffffu, src4, q);
-        const uint32_t vq = __shfl_sync(0xffffffffu, vex, q);
-        if (v < NV) {
+        const uint32_t vq = __shfl_sync(0xffffffffu, v0q, q);
+        if (v < NV && v >= vq) {
           copy16_async(reinterpret_cast<float4*>(W.ts) + v, reinterpret_cast<const float4*>(a.t) + g4 + (v - vq));
           copy16_async(reinterpret_cast<float4*>(W.ss) + v, reinterpret_cast<const float4*>(a.s) + g4 + (v - vq));
         }
       }
     }
     copies_wait();
+    __syncwarp();
+    if (mine && !before) W.ts[st - 1] = kNoPrev;  // (in the pin's own vectors, after all copies landed)
     __syncwarp();
     // the first unstaged event of each pin bounds the window
     const float bound = more ? W.ts[st + share] : FLT_MAX;
