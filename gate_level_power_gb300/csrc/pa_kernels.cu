@@ -773,10 +773,13 @@ template <bool kExact>
 __device__ __forceinline__ double2 bin_wd(const RunArgs& a, uint32_t c) {
   if (kExact) return reinterpret_cast<const double2*>(a.bins)[c];
   double2 r = make_double2(0.0, 0.0);
-  for (uint32_t k = 0; k < max(a.n_rep, 1u); ++k) {
-    const float4 v = a.bins[(size_t)k * a.n_cycles + c];
-    r.x += (double)v.x;
-    r.y += (double)v.y;
+#pragma unroll
+  for (uint32_t k = 0; k < kBinCopies; ++k) {  // (all copies' loads in flight at once)
+    if (k == 0 || k < a.n_rep) {
+      const float4 v = a.bins[(size_t)k * a.n_cycles + c];
+      r.x += (double)v.x;
+      r.y += (double)v.y;
+    }
   }
   return r;
 }
@@ -806,10 +809,11 @@ __global__ void __launch_bounds__(kRedThreads) k_reduce_apply(const RunArgs a, d
   __shared__ double wsum[kRedThreads / 32];
   __shared__ double s_base;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  if (tid == 0) {
-    double b = *a.p0;
-    for (uint32_t j = 0; j < blockIdx.x; ++j) b += a.chunk_sums[j];
-    s_base = b;
+  if (w == 0) {  // P0 + the step sums of the chunks before this one (the first warp's lanes in parallel)
+    double b = 0.0;
+    for (uint32_t j = (uint32_t)lane; j < blockIdx.x; j += 32) b += a.chunk_sums[j];
+    b = warp_sum_f64(b);
+    if (lane == 0) s_base = *a.p0 + b;
   }
   const uint32_t c0 = blockIdx.x * kReduceChunk + (uint32_t)tid * kRedPer;
   double2 v[kRedPer];
@@ -845,7 +849,9 @@ __global__ void __launch_bounds__(kRedThreads) k_reduce_apply(const RunArgs a, d
       // f32 counts are exact integers while below 2^24: a cycle with 2^24
       // events or more in all repeats the pass with integer counts
       uint32_t ne = 0, ng = 0;
-      for (uint32_t k = 0; k < max(a.n_rep, 1u); ++k) {
+#pragma unroll
+      for (uint32_t k = 0; k < kBinCopies; ++k) {
+        if (k > 0 && k >= a.n_rep) continue;
         const float4 f = a.bins[(size_t)k * a.n_cycles + c];
         if (f.z >= 16777216.0f) overflow = true;
         ne += (uint32_t)f.z;
