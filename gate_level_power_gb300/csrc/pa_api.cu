@@ -58,7 +58,7 @@ struct pa_ctx {
 
   // scratch
   DevBuf value_tmp, err_word, tmax_bits, val_starts;
-  DevBuf bins, part_blk, part_counts, tiles, heavy, pieces, tile_ev, p0_tot, p_out;
+  DevBuf bins, part_blk, part_counts, tiles, heavy, pieces, tile_ev, gslot, p0_tot, p_out;
   DevBuf dbg[3], wave_tmp, cnt_tmp, chunk_sums, gate_tmp, cell_tmp;
   // the paper's (gate, window) partition: per-gate plan, thread offsets, scan
   // scratch, total slots (+ the largest events per thread), histogram
@@ -219,6 +219,7 @@ struct PassBufs {
   Piece* pieces = nullptr;   // the warp kernel's heavy-gate pieces (null: the CTA kernel runs)
   uint64_t max_pieces = 0;
   uint64_t* tile_ev = nullptr;  // the warp kernel's per-tile event ranges
+  uint4* gslot = nullptr;       // the warp kernel's light-gate slots
   double* p0_tot = nullptr;
   double* p_out = nullptr;
   double* chunk_sums = nullptr;
@@ -387,6 +388,7 @@ int run_pass(pa_ctx* c, const RunPlan& plan, const PassBufs& B, pa_result* out, 
     a.heavy_thresh = plan.csr_heavy;
     a.pieces = B.pieces;
     a.tile_ev = B.tile_ev;
+    a.gslot = B.gslot;
   }
   BandRunArgs A;
   if (band) {
@@ -652,6 +654,8 @@ int run_stream(pa_ctx* c, const RunPlan& plan, const pa_events* ev, uint64_t tar
     B.max_pieces = csr_max_pieces(max_ev, max_g, plan.csr_heavy);
     PA_TRY(dreserve(c, c->pieces, (size_t)B.max_pieces * sizeof(Piece)));
     PA_TRY(dreserve(c, c->tile_ev, ((size_t)max_g + 1) * 2 * sizeof(uint64_t)));
+    PA_TRY(dreserve(c, c->gslot, ((size_t)max_g + 1) * 2 * sizeof(uint4)));
+    B.gslot = (uint4*)c->gslot.p;
     B.pieces = (Piece*)c->pieces.p;
     B.tile_ev = (uint64_t*)c->tile_ev.p;
   }
@@ -739,6 +743,7 @@ int run_stream(pa_ctx* c, const RunPlan& plan, const pa_events* ev, uint64_t tar
         a.heavy_thresh = plan.csr_heavy;
         a.pieces = B.pieces;
         a.tile_ev = B.tile_ev;
+        a.gslot = B.gslot;
         CUDA_TRY(c, launch_csr_partition(a, partition_blocks(gk), B.max_pieces, st));
         CUDA_TRY(c, launch_csr(a, c->sm_count, plan.pow2, st));
         launches += (gk ? 4 : 0) + 1;
@@ -860,7 +865,7 @@ void pa_destroy(pa_ctx* c) {
   if (c->stream) cudaStreamSynchronize(c->stream);
   DevBuf* all[] = {&c->cells, &c->lut, &c->leak, &c->patch, &c->gates, &c->pin_off, &c->gate_off, &c->t, &c->s,
                    &c->value_tmp, &c->err_word, &c->tmax_bits, &c->val_starts, &c->bins, &c->part_blk,
-                   &c->part_counts, &c->tiles, &c->heavy, &c->pieces, &c->tile_ev, &c->p0_tot, &c->p_out, &c->dbg[0],
+                   &c->part_counts, &c->tiles, &c->heavy, &c->pieces, &c->tile_ev, &c->gslot, &c->p0_tot, &c->p_out, &c->dbg[0],
                    &c->dbg[1], &c->dbg[2], &c->wave_tmp, &c->cnt_tmp, &c->gate_tmp, &c->cell_tmp, &c->scratch_small,
                    &c->chunk_sums, &c->b_bt, &c->b_bs, &c->b_btag, &c->b_urec, &c->b_ugate, &c->b_items,
                    &c->b_big, &c->b_bigf, &c->b_grank, &c->b_cnt, &c->b_evc, &c->b_ubase, &c->b_ebase,
@@ -1105,6 +1110,8 @@ int pa_run(pa_ctx* c, const pa_run_params* prm, pa_result* out) {
     B.max_pieces = csr_max_pieces(c->n_events, G, plan.csr_heavy);
     PA_TRY(dreserve(c, c->pieces, (size_t)B.max_pieces * sizeof(Piece)));
     PA_TRY(dreserve(c, c->tile_ev, ((size_t)G + 1) * 2 * sizeof(uint64_t)));
+    PA_TRY(dreserve(c, c->gslot, ((size_t)G + 1) * 2 * sizeof(uint4)));
+    B.gslot = (uint4*)c->gslot.p;
     B.pieces = (Piece*)c->pieces.p;
     B.tile_ev = (uint64_t*)c->tile_ev.p;
   }

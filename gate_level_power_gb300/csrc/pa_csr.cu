@@ -209,34 +209,6 @@ __device__ __forceinline__ int st_of(const uint4& A, int q) {
 }
 
 
-// Gate g's slot: cell, inputs, initial bits, load-axis interval and
-// fraction, switching energy; pin starts relative to `base` (light tiles).
-__device__ __forceinline__ void fill_slot(const RunArgs& a, CSlot& S, uint32_t g, uint64_t base, bool starts) {
-  const GateRec r = a.gates[g];
-  const int k = (int)((r.init >> 16) & 0xff);
-  const CellDesc& cd = a.cells[r.cell];
-  if (starts) {  // the gate's pin offsets, all loads issued before any use
-    uint64_t po[kMaxK + 2];
-#pragma unroll
-    for (int p = 0; p < kMaxK + 2; ++p) po[p] = p <= k + 1 ? a.pin_off[r.pin_base + p] : 0ull;
-#pragma unroll
-    for (int p = 0; p < kMaxK + 2; ++p)
-      if (p <= k + 1) S.st[p] = (uint16_t)(po[p] - base);
-  }
-  S.k = (uint8_t)k;
-  S.init = (uint8_t)(r.init & 0xffu);
-  S.pre = 0;
-  S.cell = (uint16_t)r.cell;
-  const float C = r.load;
-  const int nl = cd.nl;
-  int j = 0;
-#pragma unroll
-  for (int m = 1; m <= PA_MAX_AXIS - 2; ++m) j += (m <= nl - 2 && C >= cd.lax[m]) ? 1 : 0;
-  S.j = (uint8_t)j;
-  S.v = (C - cd.lax[j]) * cd.ilax[j];
-  S.esw = a.half_vdd2 * C;
-}
-
 // One 16-byte reduction per event into its cycle's bin, in the warp's copy
 // of the bins: energy, leakage step, event and glitch counts.
 __device__ __forceinline__ void commit(const RunArgs& a, const Acc& acc, uint32_t c, float e_w, float dp,
@@ -583,13 +555,33 @@ __device__ __forceinline__ void csr_tile(const RunArgs& a, const CTab& CT, uint3
     copy16_async(reinterpret_cast<float4*>(W.ss) + v, s4 + v);
   }
   if (lane < kSegWords) W.u.t.seg.bits[lane] = 0u;
-  // a lane per gate: its slot, then its non-empty pins' runs
+  // a lane per gate: its slot (from the partition's record, pin starts moved
+  // by the gate's first event in the tile: the events of the lanes below),
+  // then its non-empty pins' runs
+  uint4 SA = make_uint4(0u, 0u, 0u, 0u), SB = SA;
+  if (lane < (int)ng) {
+    SA = a.gslot[2 * (size_t)(tl.gb + (uint32_t)lane)];
+    SB = a.gslot[2 * (size_t)(tl.gb + (uint32_t)lane) + 1];
+  }
+  const int gk = (int)(SA.w & 0xFFu);
+  const uint32_t gn = lane < (int)ng ? (uint32_t)st_of(SA, gk + 1) : 0u;
+  uint32_t gbase = gn;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, gbase, d);
+    if (lane >= d) gbase += y;
+  }
+  gbase -= gn;
   uint32_t runs = 0, nonempty = 0;
   if (lane < (int)ng) {
-    CSlot& S = W.u.t.slot[lane];
-    fill_slot(a, S, tl.gb + (uint32_t)lane, ea, true);
-    for (int p = 0; p <= S.k; ++p)
-      if (S.st[p + 1] > S.st[p]) {
+    const uint32_t add = gbase | gbase << 16;  // each field stays below 2^16
+    SA.x += add;
+    SA.y += add;
+    SA.z += add;
+    reinterpret_cast<uint4*>(&W.u.t.slot[lane])[0] = SA;
+    reinterpret_cast<uint4*>(&W.u.t.slot[lane])[1] = SB;
+    for (int p = 0; p <= gk; ++p)
+      if (st_of(SA, p + 1) > st_of(SA, p)) {
         nonempty |= 1u << p;
         ++runs;
       }
@@ -603,10 +595,9 @@ __device__ __forceinline__ void csr_tile(const RunArgs& a, const CTab& CT, uint3
   rbase -= runs;
   __syncwarp();  // bits cleared
   if (lane < (int)ng) {
-    const CSlot& S = W.u.t.slot[lane];
-    for (int p = 0; p <= S.k; ++p)
+    for (int p = 0; p <= gk; ++p)
       if ((nonempty >> p) & 1u) {
-        const int e = S.st[p];
+        const int e = st_of(SA, p);
         atomicOr(&W.u.t.seg.bits[e >> 5], 1u << (e & 31));
         W.u.t.seg.run[rbase++] = (uint8_t)((lane << 3) | p);
       }
@@ -637,29 +628,34 @@ template <bool kPow2>
 __device__ __forceinline__ void csr_piece(const RunArgs& a, const CTab& CT, uint32_t pi, WarpBuf& W, Acc& acc) {
   const int lane = threadIdx.x & 31;
   const Piece& P = a.pieces[pi];
-  const uint32_t g = P.gate, pidx = P.idx;
-  const GateRec r = a.gates[g];
-  const int k = (int)((r.init >> 16) & 0xff);
-  const uint64_t n_g = a.gate_off[g + 1] - a.gate_off[g];
-  const uint32_t m = (uint32_t)((n_g + kCsrPiece - 1) / kCsrPiece);
-  const bool last = pidx + 1 >= m;
+  const uint32_t g = P.gate, pinfo = P.info;
+  const int k = (int)(pinfo & 7u);
+  const uint32_t cell = (pinfo >> 12) & 0xFFFu, j = (pinfo >> 8) & 0xFu;
+  const bool last = (pinfo >> 31) != 0u;
   const bool mine = lane <= k;  // lane p holds pin p
   uint64_t pst = 0;
   uint32_t cur = 0, hi = 0;
   if (mine) {
-    pst = a.pin_off[(uint64_t)r.pin_base + lane];
-    const uint64_t pe = a.pin_off[(uint64_t)r.pin_base + lane + 1];
+    const uint32_t p0 = P.pin[lane], p1 = lane < k ? P.pin[lane + 1] : P.gend;
+    pst = P.pin0 + p0;
     cur = P.lo[lane];
-    hi = last ? (uint32_t)(pe - pst) : a.pieces[pi + 1].lo[lane];
+    hi = last ? p1 - p0 : a.pieces[pi + 1].lo[lane];
     if (hi < cur) hi = cur;  // (never for a consistent partition)
   }
   CSlot& S = W.u.p.slot0;
-  if (lane == 0) fill_slot(a, S, g, 0, false);
-  __syncwarp();
+  if (lane == 0) {
+    S.k = (uint8_t)k;
+    S.init = (uint8_t)((pinfo >> 4) & 0xFu);
+    S.j = (uint8_t)j;
+    S.pre = 0;
+    S.cell = (uint16_t)cell;
+    S.v = P.v;
+    S.esw = P.esw;
+  }
   {  // the gate's patch slice (in flight with the first window's copies)
-    const uint32_t info = CT.info[r.cell];
+    const uint32_t info = CT.info[cell];
     const int ns1 = (int)(info & 0xFFu), nl1 = (int)((info >> 8) & 0xFFu);
-    const float4* src = a.patch + (info >> 16) + S.j;
+    const float4* src = a.patch + (info >> 16) + j;
     for (int x = lane; x < (ns1 << k); x += 32) copy16_async(&W.u.p.slice[x], src + x * nl1);
   }
   for (int guard = 0;; ++guard) {
@@ -936,54 +932,96 @@ __global__ void __launch_bounds__(256) k_cp_emit(const RunArgs a) {
       a.tiles[th + h - 1].ge = g + 1;
       a.tile_ev[2 * (th + h - 1) + 1] = a.gate_off[g + 1];
     }
-    for (uint32_t i = 0; i < pc; ++i) {
-      a.pieces[tv + i].gate = g;
-      a.pieces[tv + i].idx = i;
+    if (pc) {  // the gate's part of its pieces' records (the cut points follow in k_cp_bounds)
+      const GateRec r = a.gates[g];
+      const int k = (int)((r.init >> 16) & 0xff);
+      const uint64_t* po = a.pin_off + r.pin_base;
+      const uint64_t b0 = po[0];
+      const CellDesc& cd = a.cells[r.cell];
+      const float C = r.load;
+      const int nl = cd.nl;
+      int j = 0;
+#pragma unroll
+      for (int q = 1; q <= PA_MAX_AXIS - 2; ++q) j += (q <= nl - 2 && C >= cd.lax[q]) ? 1 : 0;
+      const uint32_t info = (uint32_t)k | ((r.init & 0xFu) << 4) | ((uint32_t)j << 8) | (r.cell << 12);
+      const float v = (C - cd.lax[j]) * cd.ilax[j], esw = a.half_vdd2 * C;
+      const uint32_t gend = (uint32_t)(po[k + 1] - b0);
+      for (uint32_t i = 0; i < pc; ++i) {
+        Piece& P = a.pieces[tv + i];
+        P.gate = g;
+        P.idx = i;
+        P.info = info | (i + 1 == pc ? 1u << 31 : 0u);
+        P.v = v;
+        P.esw = esw;
+        P.gend = gend;
+        P.pin0 = b0;
+        for (int p = 0; p <= kMaxK; ++p) {
+          P.lo[p] = 0;
+          P.pin[p] = p <= k ? (uint32_t)(po[p] - b0) : 0u;
+        }
+      }
+    } else {  // a light gate: its slot, pin starts from its first event
+      const GateRec r = a.gates[g];
+      const int k = (int)((r.init >> 16) & 0xff);
+      const uint64_t* po = a.pin_off + r.pin_base;
+      uint32_t st[kMaxK + 2];
+#pragma unroll
+      for (int p = 0; p <= kMaxK + 1; ++p) st[p] = p <= k + 1 ? (uint32_t)(po[p] - po[0]) : 0u;
+      const CellDesc& cd = a.cells[r.cell];
+      const float C = r.load;
+      const int nl = cd.nl;
+      int j = 0;
+#pragma unroll
+      for (int q = 1; q <= PA_MAX_AXIS - 2; ++q) j += (q <= nl - 2 && C >= cd.lax[q]) ? 1 : 0;
+      const float v = (C - cd.lax[j]) * cd.ilax[j], esw = a.half_vdd2 * C;
+      a.gslot[2 * (size_t)g] = make_uint4(st[0] | st[1] << 16, st[2] | st[3] << 16, st[4] | st[5] << 16,
+                                         (uint32_t)k | (r.init & 0xFFu) << 8 | (uint32_t)j << 16);
+      a.gslot[2 * (size_t)g + 1] = make_uint4(r.cell, __float_as_uint(v), __float_as_uint(esw), 0u);
     }
   }
 }
 
-// Cut points of every piece: piece i > 0 of gate g starts, on each pin, at
-// the first event at or after time tau_i, the time of event floor(i c / m)
-// of the gate's densest pin (c events, m pieces).
+// The cut points of the pieces after a gate's first: piece i > 0 of gate g
+// starts, on each pin, at the first event at or after time tau_i, the time of
+// event floor(i c / m) of the gate's densest pin (c events, m pieces). The
+// pins' starts come from the record k_cp_emit wrote.
 __global__ void __launch_bounds__(256) k_cp_bounds(const RunArgs a) {
   const uint32_t n = a.part_counts[1];
   for (uint32_t pi = blockIdx.x * 256u + threadIdx.x; pi < n; pi += gridDim.x * 256u) {
     Piece& P = a.pieces[pi];
-    const uint32_t g = P.gate, i = P.idx;
-    const GateRec r = a.gates[g];
-    const int k = (int)((r.init >> 16) & 0xff);
-    uint32_t lo[kMaxK + 1] = {0, 0, 0, 0, 0};
-    if (i > 0) {
-      const uint64_t pb = r.pin_base;
-      uint64_t cmax = 0;
-      int pmax = 0;
-      for (int p = 0; p <= k; ++p) {
-        const uint64_t c = a.pin_off[pb + p + 1] - a.pin_off[pb + p];
-        if (c > cmax) {
-          cmax = c;
-          pmax = p;
-        }
-      }
-      const uint64_t m = (gate_events(a, g) + kCsrPiece - 1) / kCsrPiece;
-      const float tau = a.t[a.pin_off[pb + pmax] + (uint64_t)i * cmax / m];
-      for (int p = 0; p <= k; ++p) {
-        const uint64_t b = a.pin_off[pb + p];
-        uint64_t l = 0, len = a.pin_off[pb + p + 1] - b;
-        while (len > 0) {  // first event at or after tau
-          const uint64_t half = len >> 1;
-          if (a.t[b + l + half] < tau) {
-            l += half + 1;
-            len -= half + 1;
-          } else {
-            len = half;
-          }
-        }
-        lo[p] = (uint32_t)l;
+    const uint32_t i = P.idx;
+    if (i == 0) continue;
+    const uint32_t info = P.info, gend = P.gend;
+    const int k = (int)(info & 7u);
+    const uint64_t b0 = P.pin0;
+    uint32_t ps[kMaxK + 2];
+#pragma unroll
+    for (int p = 0; p <= kMaxK + 1; ++p) ps[p] = p <= k ? P.pin[p] : gend;
+    uint32_t cmax = 0, smax = 0;
+#pragma unroll
+    for (int p = 0; p <= kMaxK; ++p) {
+      const uint32_t c = p <= k ? ps[p + 1] - ps[p] : 0u;
+      if (c > cmax) {
+        cmax = c;
+        smax = ps[p];
       }
     }
-#pragma unroll
-    for (int p = 0; p <= kMaxK; ++p) P.lo[p] = lo[p];
+    const uint64_t m = ((uint64_t)gend + kCsrPiece - 1) / kCsrPiece;
+    const float tau = a.t[b0 + smax + (uint64_t)i * cmax / m];
+    for (int p = 0; p <= k; ++p) {
+      const uint64_t b = b0 + ps[p];
+      uint32_t l = 0, len = ps[p + 1] - ps[p];
+      while (len > 0) {  // first event at or after tau
+        const uint32_t half = len >> 1;
+        if (a.t[b + l + half] < tau) {
+          l += half + 1;
+          len -= half + 1;
+        } else {
+          len = half;
+        }
+      }
+      P.lo[p] = l;
+    }
   }
 }
 

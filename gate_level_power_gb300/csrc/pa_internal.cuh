@@ -107,6 +107,7 @@ struct RunArgs {
   uint32_t* heavy;
   Piece* pieces;           // heavy-gate pieces of the warp kernel (pa_csr.cu)
   uint64_t* tile_ev;       // per light tile of the warp kernel: its first event and its end
+  uint4* gslot;            // per light gate of the warp kernel: its slot (two uint4), pin starts from its first event
   double* p0;              // sum of leakage of initial states, uW
   // accumulators: per cycle {W, D, ev, gl}
   //   W  energy in the cycle: dynamic + in-cycle leakage parts (fJ)
@@ -284,12 +285,19 @@ constexpr uint32_t kCsrGates = 32;          // gates per light tile (one lane pe
 constexpr uint32_t kCsrPiece = 2048;        // target events per piece of a heavy gate
 constexpr uint32_t kCsrWin = 448;           // events per window of a piece
 
-struct Piece {
+// A piece of a heavy gate, with what the warp kernel needs to start it
+// without further dependent loads (filled by the partition).
+struct __align__(16) Piece {
   uint32_t gate, idx;          // the gate; the piece's index among the gate's pieces
+  uint32_t info;               // k | initial input bits << 4 | load-axis interval j << 8 | cell << 12 | last piece << 31
+  float v, esw;                // load-axis fraction; switching energy C V^2 / 2 (fJ)
+  uint32_t gend;               // the gate's events, from its first one
+  uint64_t pin0;               // the gate's first event (its first pin's start)
   uint32_t lo[kMaxK + 1];      // per pin, the piece's first event as an index into the pin's events
-  uint32_t pad;
+  uint32_t pin[kMaxK + 1];     // per pin, its first event from the gate's first event
+  uint32_t pad[2];
 };
-static_assert(sizeof(Piece) == 32, "piece record size");
+static_assert(sizeof(Piece) == 80, "piece record size");
 
 // Upper bound of the pieces of a run over n_events events of n_gates gates
 // (gates with more than heavy_thresh events).
