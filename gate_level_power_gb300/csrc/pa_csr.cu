@@ -55,7 +55,7 @@ constexpr int kStCap = 496;           // staged events per warp: a window, its b
 constexpr int kAx = 9;                // slew axis stride of the cell table (odd: lanes of different cells spread)
 constexpr int kLk = 17;               // leakage stride of the cell table
 constexpr int kTotEvery = 16;         // items between flushes of a warp's per-lane totals
-constexpr uint32_t kChunk = 8;        // items a warp takes from the global counter at a time
+constexpr uint32_t kChunk = 4;        // items a warp takes from the global counter at a time
 
 // Cell tables in shared memory (libraries of at most kSmemCells cells): per
 // cell the slew axis points 0..8 (+inf past ns - 2), an info word (ns - 1 |
@@ -795,16 +795,6 @@ __global__ void __launch_bounds__(kCT, 1) k_csr(const RunArgs a) {
   while (base < n_items) {
     uint32_t nbase = 0;
     if (lane == 0) nbase = atomicAdd(a.part_counts + 2, kChunk);
-    // bring the chunk's later tiles' events into L2 while the first ones are worked on
-    if (lane >= 1 && lane < (int)kChunk && base + lane < n_items && base + lane >= n_pieces) {
-      const uint32_t ti = base + lane - n_pieces;
-      const uint64_t ea = a.tile_ev[2 * ti] & ~3ull, eb = (a.tile_ev[2 * ti + 1] + 3) & ~3ull;
-      if (eb > ea && eb - ea <= (uint64_t)kStCap) {
-        const uint32_t bytes = (uint32_t)(eb - ea) * 4u;
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.t + ea), "r"(bytes));
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.s + ea), "r"(bytes));
-      }
-    }
     for (uint32_t j = 0; j < kChunk && base + j < n_items; ++j) {
       const uint32_t item = base + j;
       if (item < n_pieces)
