@@ -922,7 +922,7 @@ __global__ void __launch_bounds__(256) k_cp_emit(const RunArgs a) {
       a.tiles[th + h - 1].ge = g + 1;
       a.tile_ev[2 * (th + h - 1) + 1] = a.gate_off[g + 1];
     }
-    if (pc) {  // the gate's part of its pieces' records (the cut points follow in k_cp_bounds)
+    if (pc) {  // a heavy gate: what its pieces share, in its slot entry (k_cp_bounds builds their records)
       const GateRec r = a.gates[g];
       const int k = (int)((r.init >> 16) & 0xff);
       const uint64_t* po = a.pin_off + r.pin_base;
@@ -935,20 +935,11 @@ __global__ void __launch_bounds__(256) k_cp_emit(const RunArgs a) {
       for (int q = 1; q <= PA_MAX_AXIS - 2; ++q) j += (q <= nl - 2 && C >= cd.lax[q]) ? 1 : 0;
       const uint32_t info = (uint32_t)k | ((r.init & 0xFu) << 4) | ((uint32_t)j << 8) | (r.cell << 12);
       const float v = (C - cd.lax[j]) * cd.ilax[j], esw = a.half_vdd2 * C;
-      const uint32_t gend = (uint32_t)(po[k + 1] - b0);
+      a.gslot[2 * (size_t)g] = make_uint4(info, __float_as_uint(v), __float_as_uint(esw), (uint32_t)(po[k + 1] - b0));
+      a.gslot[2 * (size_t)g + 1] = make_uint4((uint32_t)b0, (uint32_t)(b0 >> 32), r.pin_base, 0u);
       for (uint32_t i = 0; i < pc; ++i) {
-        Piece& P = a.pieces[tv + i];
-        P.gate = g;
-        P.idx = i;
-        P.info = info | (i + 1 == pc ? 1u << 31 : 0u);
-        P.v = v;
-        P.esw = esw;
-        P.gend = gend;
-        P.pin0 = b0;
-        for (int p = 0; p <= kMaxK; ++p) {
-          P.lo[p] = 0;
-          P.pin[p] = p <= k ? (uint32_t)(po[p] - b0) : 0u;
-        }
+        a.pieces[tv + i].gate = g;
+        a.pieces[tv + i].idx = i;
       }
     } else {  // a light gate: its slot, pin starts from its first event
       const GateRec r = a.gates[g];
@@ -971,36 +962,43 @@ __global__ void __launch_bounds__(256) k_cp_emit(const RunArgs a) {
   }
 }
 
-// The cut points of the pieces after a gate's first: piece i > 0 of gate g
-// starts, on each pin, at the first event at or after time tau_i, the time of
-// event floor(i c / m) of the gate's densest pin (c events, m pieces). The
-// pins' starts come from the record k_cp_emit wrote.
+// Every piece's record, from its gate's slot entry (k_cp_emit) and pin
+// offsets, with its cut points: piece i > 0 of gate g starts, on each pin, at
+// the first event at or after time tau_i, the time of event floor(i c / m) of
+// the gate's densest pin (c events, m pieces).
 __global__ void __launch_bounds__(256) k_cp_bounds(const RunArgs a) {
   const uint32_t n = a.part_counts[1];
   for (uint32_t pi = blockIdx.x * 256u + threadIdx.x; pi < n; pi += gridDim.x * 256u) {
     Piece& P = a.pieces[pi];
-    const uint32_t i = P.idx;
-    if (i == 0) continue;
-    const uint32_t info = P.info, gend = P.gend;
-    const int k = (int)(info & 7u);
-    const uint64_t b0 = P.pin0;
-    uint32_t ps[kMaxK + 2];
-#pragma unroll
-    for (int p = 0; p <= kMaxK + 1; ++p) ps[p] = p <= k ? P.pin[p] : gend;
+    const uint32_t g = P.gate, i = P.idx;
+    const uint4 G0 = a.gslot[2 * (size_t)g], G1 = a.gslot[2 * (size_t)g + 1];
+    const int k = (int)(G0.x & 7u);
+    const uint32_t gend = G0.w;
+    const uint64_t b0 = (uint64_t)G1.x | (uint64_t)G1.y << 32;
+    const uint64_t* po = a.pin_off + G1.z;
+    const uint64_t m = ((uint64_t)gend + kCsrPiece - 1) / kCsrPiece;
     uint32_t cmax = 0, smax = 0;
-#pragma unroll
-    for (int p = 0; p <= kMaxK; ++p) {
-      const uint32_t c = p <= k ? ps[p + 1] - ps[p] : 0u;
-      if (c > cmax) {
-        cmax = c;
-        smax = ps[p];
+    for (int p = 0; p <= k; ++p) {
+      const uint32_t s0 = (uint32_t)(po[p] - b0), s1 = p < k ? (uint32_t)(po[p + 1] - b0) : gend;
+      P.pin[p] = s0;
+      if (s1 - s0 > cmax) {
+        cmax = s1 - s0;
+        smax = s0;
       }
     }
-    const uint64_t m = ((uint64_t)gend + kCsrPiece - 1) / kCsrPiece;
+    P.info = G0.x | (i + 1 >= m ? 1u << 31 : 0u);
+    P.v = __uint_as_float(G0.y);
+    P.esw = __uint_as_float(G0.z);
+    P.gend = gend;
+    P.pin0 = b0;
+    if (i == 0) {
+      for (int p = 0; p <= k; ++p) P.lo[p] = 0;
+      continue;
+    }
     const float tau = a.t[b0 + smax + (uint64_t)i * cmax / m];
     for (int p = 0; p <= k; ++p) {
-      const uint64_t b = b0 + ps[p];
-      uint32_t l = 0, len = ps[p + 1] - ps[p];
+      const uint64_t b = po[p];
+      uint32_t l = 0, len = (uint32_t)((p < k ? po[p + 1] : b0 + gend) - b);
       while (len > 0) {  // first event at or after tau
         const uint32_t half = len >> 1;
         if (a.t[b + l + half] < tau) {
