@@ -15,11 +15,14 @@
 //    event at or after each such time. A piece thus holds all of the gate's
 //    events in a time interval: the dense gates get short time windows and
 //    the sparse ones whole timelines, the role of the event-density-aware
-//    per-gate partitioning of Figs. 5, 19 and 20, cut by event count.
+//    per-gate partitioning of Figs. 5, 19 and 20, cut by event count. The
+//    partition also writes what a warp needs to start an item: per light gate
+//    its slot (pin starts, cell, load-axis interval and fraction, switching
+//    energy), per piece its record (the same gate fields, the pins' starts,
+//    the cut points), so an item starts from one coalesced read.
 //  * One warp per item, no CTA-wide barrier in the item loop. A light tile's
-//    times and slews are one contiguous range, staged with 16-byte copies; a
-//    lane per gate fills the gate's slot (pin starts, cell, load-axis
-//    interval and fraction, switching energy). A piece is staged in windows of
+//    times and slews are one contiguous range, staged with 16-byte copies
+//    while a lane per gate loads the gate's slot. A piece is staged in windows of
 //    at most kCsrWin events shared among its pins in proportion to their
 //    remaining events (16-byte copies per pin run); the events before the
 //    earliest first unstaged event of any pin are taken, so every pin's
@@ -34,11 +37,14 @@
 //    even share of the merge of the pins' runs, the state following from the
 //    parities of the events taken so far on each pin. The slew interval by a
 //    three-step search over the cell's axis in shared memory, the state's four
-//    LUT corners in one 16-byte load, the leakage per state in shared memory.
+//    LUT corners in one 16-byte load (a piece: from its gate's slice of the
+//    table, copied into shared memory once), the leakage per state in shared
+//    memory.
 //    Glitch: the previous event of the same pin in the same cycle (the CSR
 //    neighbour). Each event adds {energy, leakage step, 1, glitch} to its
-//    cycle's bin with one red.global.add.v4.f32; per-lane totals (the
-//    leakage term compensated) are reduced in fp64.
+//    cycle's bin with one red.global.add.v4.f32, in its warp's copy of the
+//    bins (the final reduction adds the copies); per-lane totals (the leakage
+//    term compensated) are reduced in fp64.
 #include <cfloat>
 #include <cstddef>
 #include <cstdint>
