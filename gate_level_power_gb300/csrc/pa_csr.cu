@@ -254,16 +254,16 @@ __device__ __forceinline__ void out_event(const RunArgs& a, const float* ts, con
   commit(a, acc, c, e_w, 0.f, glitch);
 }
 
-// An input-pin event at staged index i of pin p, with its states: s_pre
+// An input-pin event at staged index i (time t, held by the caller) of pin p, with its states: s_pre
 // before its timestamp (selects the table), s_b just before it in (time, pin)
 // order (the leakage step's base).
 // The corners come from the gate's patch slice in shared memory in a piece,
 // from the global patch table in a light tile.
 template <bool kPow2, bool kPiece>
-__device__ __forceinline__ void in_event(const RunArgs& a, const CTab& CT, const float4* slice, const float* ts,
-                                         const float* ss, const uint4& A, const uint4& B, int i, int p, uint32_t s_pre,
+__device__ __forceinline__ void in_event(const RunArgs& a, const CTab& CT, const float4* slice, const float* ss,
+                                         const uint4& A, const uint4& B, int i, float t, int p, uint32_t s_pre,
                                          uint32_t s_b, bool has_prev, float tp, const float* spp, Acc& acc) {
-  const float t = ts[i], s = ss[i];
+  const float s = ss[i];
   const float T = a.t_clk;
   const uint32_t c = cyc<kPow2>(t, T, a.inv_t_clk);
   const bool glitch = has_prev && cyc<kPow2>(tp, T, a.inv_t_clk) == c;
@@ -458,7 +458,7 @@ __device__ __forceinline__ void walk_inputs(const RunArgs& a, const CTab& CT, co
     s ^= 1u << p;
     if (t != t_prev) g = s_b;
     t_prev = t;
-    in_event<kPow2, true>(a, CT, W.u.p.slice, ts, ss, SA, SB, idx, p, g, s_b, true, ts[idx - 1], ss + idx - 1, acc);
+    in_event<kPow2, true>(a, CT, W.u.p.slice, ss, SA, SB, idx, t, p, g, s_b, true, ts[idx - 1], ss + idx - 1, acc);
   }
 }
 
@@ -530,7 +530,7 @@ __device__ __forceinline__ void tile_event(const RunArgs& a, const CTab& CT, con
     s_pre ^= par << q;
     s_b ^= ((par ^ (uint32_t)(q < p && eq)) & 1u) << q;
   }
-  in_event<kPow2, false>(a, CT, nullptr, ts, ss, A, B, e, p, s_pre, s_b, hp, tp, ss + e - 1, acc);
+  in_event<kPow2, false>(a, CT, nullptr, ss, A, B, e, t, p, s_pre, s_b, hp, tp, ss + e - 1, acc);
 }
 
 // A light tile: consecutive whole gates, staged whole.
